@@ -1,0 +1,363 @@
+#!/usr/bin/env python3
+"""Decode-step benchmark of the persistent MoE megakernel.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl mk|reference]
+
+One step = one call of ``mk_decode_step``: the whole hot path (embedding,
+RMSNorm, QKV, RoPE + KV append, paged GQA attention, O-proj, router, experts,
+combine, final norm, LM head) for one batch, as one persistent kernel launch.
+Default workload: the 30B-total / ~3.3B-active MoE at batch 1 with 8192 cached
+tokens (page size 16), random-init bf16 weights (synthetic, seeded).  Each step
+reads ~6.9 GB, far more than the 129 MB L2, so no L2 flush is needed between
+timed steps.
+
+Prints ONE JSON line (rank 0).  ``value`` is decode tokens/s over all ranks,
+timed with CUDA events on the launching stream with inputs resident in HBM;
+``e2e`` repeats the measurement through the C ABI with host buffers (token ids
+and block tables copied in, logits copied out, every step).  ``roofline``
+relates the algorithmic bytes of a step to the measured HBM copy bandwidth.
+``cpu_baseline`` times the CPU oracle on a bounded sample of the same step.
+Under torchrun each rank runs an independent replica (the step does not shard).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+from persistent_moe_decode_megakernel_gb300 import roofline as R  # noqa: E402
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="moe30b_bs1_ctx8k", choices=W.NAMES)
+    ap.add_argument("--impl", default="mk", choices=("mk", "reference"))
+    ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling captures only)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-s", type=float, default=12.0, help="target seconds of oracle work for the baseline")
+    return ap.parse_args()
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([c.strip() for c in line.split(",")])
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if len(r) > 5 + i and r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+def setup_workload(wl, layers_override, device):
+    import torch
+    m = dict(wl.model)
+    if layers_override:
+        m["layers"] = layers_override
+    bias = W.zipf_router_bias(m, wl.zipf) if wl.zipf else None
+    w = W.make_weights(m, device, router_bias=bias)
+    ps = wl.page_size
+    lens = list(wl.lengths)
+    B = len(lens)
+    max_pages = max((L + ps - 1) // ps for L in lens)
+    num_pages = W.pages_needed(lens, ps) + 8
+    bt, _ = W.make_block_tables(lens, ps, num_pages, max_pages)
+    used = [int(p) for p in bt.flatten() if p >= 0]
+    kv = W.make_kv_random(m, num_pages, ps, device, used_pages=used)
+    tokens = W.make_tokens(B, m["vocab"])
+    torch.cuda.synchronize()
+    return dict(model=m, w=w, lens=lens, B=B, ps=ps, num_pages=num_pages, max_pages=max_pages, bt=bt, kv=kv,
+                tokens=tokens, bias=bias)
+
+
+def cpu_baseline(st, budget_s: float):
+    """Time the CPU oracle (as it stands) on a bounded sample of the same step: whole
+    layers of the model (attention, routing and the routed experts) plus the final
+    norm and LM head; the per-step time is scaled from the sampled layers."""
+    import torch
+    from oracle import Oracle, make_dims
+    m, B = st["model"], st["B"]
+    orc = Oracle("f32")
+    dims = make_dims(m, st["ps"], st["num_pages"], st["max_pages"])
+    bt = st["bt"].numpy()
+    sl = np.array(st["lens"], dtype=np.int32)
+    x = W.bf16_bits(st["w"]["embed"][st["tokens"].long().cuda()]).astype(np.uint32) << 16
+    x = x.view(np.float32).reshape(B, m["hidden"]).copy()
+    fn, head = W.bf16_bits(st["w"]["final_norm"]), W.bf16_bits(st["w"]["lm_head"])
+    t0 = time.perf_counter()
+    logits = np.empty((B, m["vocab"]), dtype=np.float32)
+    import ctypes
+    orc._fn("final")(ctypes.byref(dims), fn.ctypes.data, head.ctypes.data, B, x.ctypes.data, logits.ctypes.data)
+    t_head = time.perf_counter() - t0
+    del head
+    layer_times = []
+    spent = t_head
+    l = 0
+    while l < m["layers"] and (spent < budget_s or not layer_times):
+        lw = st["w"]["layers"][l]
+        host = {k: W.bf16_bits(lw[k]) for k in ("attn_norm", "w_qkv", "w_o", "ffn_norm", "w_router", "w_gate_up",
+                                               "w_down")}
+        host["router_bias"] = None if lw.get("router_bias") is None else lw["router_bias"].cpu().numpy()
+        kvl = W.bf16_bits(st["kv"][l]).copy()
+        t0 = time.perf_counter()
+        tr = orc.layer_trace(dims, host, x, sl, bt, kvl)
+        dt = time.perf_counter() - t0
+        x = tr["x_out"].astype(np.float32)
+        layer_times.append(dt)
+        spent += dt
+        l += 1
+        del host, kvl
+    step_s = t_head + statistics.mean(layer_times) * m["layers"]
+    cores = os.cpu_count()
+    return {"value": B / step_s, "unit": "tok/s", "cores": int(os.environ.get("OMP_NUM_THREADS", cores)),
+            "kind": "oracle", "seconds_per_step": step_s,
+            "sample": f"{len(layer_times)} of {m['layers']} layers + final norm/LM head of one step "
+                      f"(batch {B}), timed on the host, scaled to the whole step"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import torch
+    wl = W.get(args.workload)
+    torch.cuda.set_device(0)
+    st = setup_workload(wl, args.layers, "cuda")
+    for _ in range(args.warmup):
+        pass   # the oracle has no warm state; one sample per step below
+    vals = []
+    budget = max(2.0, 60.0 / max(1, args.steps))
+    cb = None
+    for _ in range(args.steps):
+        cb = cpu_baseline(st, budget)
+        vals.append(cb["seconds_per_step"])
+    sps = statistics.median(vals)
+    value = st["B"] / sps
+    cb["value"] = value
+    line = {"metric": "decode tok/s at bs=1 and bs=64; % of HBM SoL (active weights+KV bytes/step)",
+            "impl": "reference", "value": value, "unit": "tok/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": sps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded random-init weights, random bf16 KV)",
+            "config": {"workload": wl.name, "batch": st["B"], "seq_lens": "8193" if st["B"] == 1 else "ragged",
+                       "page_size": st["ps"], "layers": st["model"]["layers"]},
+            "cpu_baseline": cb, "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0,
+                                        "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    import torch
+    import persistent_moe_decode_megakernel_gb300 as mk
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    mk.build()
+    wl = W.get(args.workload)
+    st = setup_workload(wl, args.layers, "cuda")
+    m, B = st["model"], st["B"]
+    eng = mk.Engine(m, st["w"], st["ps"], st["num_pages"], max(B, 1), st["max_pages"])
+    stream = torch.cuda.Stream()
+    tok_d = st["tokens"].cuda()
+    bt_d = st["bt"].cuda()
+    sl = np.array(st["lens"], dtype=np.int32)
+    logits = torch.empty(B, m["vocab"], dtype=torch.float32, device="cuda")
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            eng.step(tok_d, sl, bt_d, st["kv"], logits, stream=stream)
+    stream.synchronize()
+    eng.check()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    # ---- device-resident timing: events around each step on the launching stream
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(local) as clocks:
+        barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            eng.step(tok_d, sl, bt_d, st["kv"], logits, stream=stream)
+            ev[i][1].record(stream)
+        stream.synchronize()
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        barrier()
+    eng.check()
+    per = [a.elapsed_time(b) for a, b in ev]
+    ms_mean = sum(per) / len(per)
+    ms_med = statistics.median(per)
+    if world > 1:
+        t = torch.tensor([ms_mean], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_mean = float(t.item())
+    value = world * B / (ms_mean / 1e3)
+
+    # ---- end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        tok_h = st["tokens"].clone().pin_memory()
+        bt_h = st["bt"].clone().pin_memory()
+        out_h = torch.empty(B, m["vocab"], dtype=torch.float32).pin_memory()
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                tok_d.copy_(tok_h, non_blocking=True)
+                bt_d.copy_(bt_h, non_blocking=True)
+                eng.step(tok_d, sl, bt_d, st["kv"], logits, stream=stream)
+                out_h.copy_(logits, non_blocking=True)
+        stream.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(args.steps):
+                tok_d.copy_(tok_h, non_blocking=True)
+                bt_d.copy_(bt_h, non_blocking=True)
+                eng.step(tok_d, sl, bt_d, st["kv"], logits, stream=stream)
+                out_h.copy_(logits, non_blocking=True)
+            e1.record(stream)
+        stream.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / args.steps
+        if world > 1:
+            t = torch.tensor([e2e_ms], device="cuda")
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * B / (e2e_ms / 1e3), "unit": "tok/s",
+               "h2d_bytes_per_step": int(tok_h.numel() * 4 + bt_h.numel() * 4),
+               "d2h_bytes_per_step": int(out_h.numel() * 4), "ms_per_step": e2e_ms,
+               "note": "token ids and block tables copied from pinned host memory, logits copied back, every step"}
+        eng.check()
+
+    # ---- roofline of the (single) step kernel
+    union = None
+    if B > 1:
+        union = [len(set(eng.debug_read("route_ids", l).ravel().tolist())) for l in range(m["layers"])]
+    by = R.step_bytes(m, st["lens"], expert_union=union, router_bias=st["bias"] is not None)
+    peak, peak_kind = measured_peaks()
+    achieved = by["total"] / (ms_mean / 1e3) / 1e9
+    sol = R.sol_tokens_per_s(by["total"], peak * 1e9, B)
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
+            "traffic": None, "algorithmic_bytes_per_step": by["total"], "bytes_breakdown": by,
+            "sol_tok_s": sol, "frac_of_nominal_8tbs": achieved / 8000.0,
+            "kernel": "mk::step_kernel (one launch per step; events also cover the 1 small per-step H2D copy)"}
+    traffic_file = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(traffic_file):
+        try:
+            tr = json.load(open(traffic_file)).get(wl.name)
+            if tr and tr.get("kernel_source_hash") == _kernel_hash():
+                roof["traffic"] = tr["bytes_per_step"]
+        except Exception:
+            pass
+
+    cb = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = cpu_baseline(st, args.cpu_sample_s)
+
+    if rank == 0:
+        cs = clocks.summary()
+        line = {"metric": "decode tok/s at bs=1 and bs=64; % of HBM SoL (active weights+KV bytes/step)",
+                "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": ms_mean, "ms_per_step_median": ms_med, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16 weights/KV, fp32 accumulate",
+                "data": "synthetic (seeded random-init bf16 weights ~N(0,0.02), KV ~N(0,1))",
+                "config": {"workload": wl.name, "batch": B, "context": int(max(st["lens"]) - 1),
+                           "page_size": st["ps"], "layers": m["layers"], "hidden": m["hidden"],
+                           "experts": f"{m['n_exp']} top-{m['top_k']}", "parallelism": f"replicas x{world}",
+                           "l2": "inputs larger than L2 (%.1f GB read per step), no flush" % (by["total"] / 1e9)},
+                "roofline": roof, "clocks": {"sm_mhz": cs["sm_mhz"], "sm_max_mhz": cs["sm_max_mhz"],
+                                             "reasons": cs["reasons"], "samples": cs["samples"]},
+                "gpu_launches": args.steps, "wall_s_timed": wall}
+        if e2e:
+            line["e2e"] = e2e
+        if cb:
+            line["cpu_baseline"] = cb
+        print(json.dumps(line))
+    eng.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def _kernel_hash():
+    import hashlib
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "persistent_moe_decode_megakernel_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        h.update(open(os.path.join(d, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,167 @@
+/*
+ * mk.h -- C ABI of the persistent MoE decode megakernel for GB300 (sm_103a).
+ *
+ * One call of mk_decode_step runs one decode step of a mixture-of-experts
+ * transformer for a batch of sequences as a single persistent kernel: one
+ * thread block per SM stays resident for the whole step, walks a task list
+ * prepared on the host, and waits on dependency counters in global memory
+ * ("Inside the megakernel serving engine for North Mini Code", section "What
+ * is a Megakernel?" and the "Image 2" paragraph).  The step covers RMSNorm,
+ * fused QKV, RoPE, paged GQA decode attention over ragged lengths with block
+ * tables, O-proj + residual, router softmax/top-k, SwiGLU experts, the
+ * weighted combine, the final norm and the LM head.
+ *
+ * The calls follow the page's statement of the problem (serving paragraph:
+ * "continuous batching, paged attention, and ragged sequence lengths"):
+ * every call may use a different batch and different lengths; the caller owns
+ * the paged KV cache and its block tables.
+ *
+ * Conventions
+ *   - All weights are bf16, row-major [out, in]; accumulation is fp32.
+ *   - Pointers marked "device" are CUDA device pointers of the current device;
+ *     "host" pointers are ordinary host memory read during the call.
+ *   - Every pointer passed to the library must be 16-byte aligned.
+ *   - The library never takes ownership of caller memory.  Weights must stay
+ *     valid until mk_destroy; step arguments until the step has completed on
+ *     its stream.
+ *   - Functions return MK_OK (0) or a negative MK_ERR_* code; mk_last_error()
+ *     then gives a text for the calling thread.  Arguments are checked before
+ *     anything is launched: out-of-range calls are rejected, never clamped.
+ *   - Errors found on the device (a wait that ran out, a page id or token out
+ *     of range) cannot be returned by the asynchronous step call; they are
+ *     recorded and read with mk_get_status.
+ */
+#ifndef MK_H
+#define MK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MK_OK 0
+#define MK_ERR_INVALID_ARG (-1)   /* bad argument; nothing was launched */
+#define MK_ERR_CUDA (-2)          /* a CUDA runtime call failed */
+#define MK_ERR_OOM (-3)           /* device or pinned allocation failed */
+#define MK_ERR_UNSUPPORTED (-4)   /* not an sm_103 device, no cooperative launch, shape outside the compiled limits */
+#define MK_ERR_TIMEOUT (-5)       /* device: a dependency wait exceeded the watchdog budget (mk_get_status) */
+#define MK_ERR_DEVICE_BOUNDS (-6) /* device: a token id or block-table page id was out of range (mk_get_status) */
+
+/* CUDA stream handle; ABI-identical to cudaStream_t (NULL = legacy default stream). */
+typedef struct CUstream_st* mk_stream_t;
+
+/*
+ * Model and cache shape.  All sizes must be > 0.  Limits of this build
+ * (mk_create returns MK_ERR_UNSUPPORTED outside them):
+ *   head_dim in {64, 128}; num_q_heads % num_kv_heads == 0 with at most 8 query
+ *   heads per KV head; hidden, num_q_heads*head_dim and expert_ffn multiples of 8
+ *   and <= 4096; num_experts <= 256; top_k <= min(8, num_experts);
+ *   page_size*head_dim*2 <= 16384 bytes; max_batch <= 64.
+ */
+typedef struct mk_config {
+  int32_t num_layers;
+  int32_t hidden;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t num_experts;
+  int32_t top_k;
+  int32_t expert_ffn;
+  int32_t vocab;
+  float rope_theta;          /* RoPE base; angles pos*theta^(-2i/D) are evaluated in fp64 on the host */
+  float rms_eps;             /* RMSNorm epsilon */
+  int32_t page_size;         /* tokens per KV page */
+  int32_t num_pages;         /* pages per layer in the caller's KV pool */
+  int32_t max_batch;         /* largest batch a step may use */
+  int32_t max_pages_per_seq; /* row length of the block table */
+  int32_t norm_topk;         /* 1: router weights renormalised over the k chosen experts; 0: raw softmax probs */
+  int32_t flags;             /* reserved, must be 0 */
+  uint32_t watchdog_ms;      /* per-wait device budget in ms; 0 selects the default (1000 ms) */
+} mk_config;
+
+/* One layer's weights (device pointers, bf16 unless noted).  Borrowed. */
+typedef struct mk_layer_weights {
+  const void* attn_norm;    /* [hidden] RMSNorm gain before attention */
+  const void* w_qkv;        /* [(Hq + 2*Hkv)*D, hidden]: rows are q heads, then k heads, then v heads */
+  const void* w_o;          /* [hidden, Hq*D] */
+  const void* ffn_norm;     /* [hidden] RMSNorm gain before the MoE block */
+  const void* w_router;     /* [num_experts, hidden] */
+  const float* router_bias; /* [num_experts] fp32 added to the router logits, or NULL */
+  const void* w_gate_up;    /* [num_experts, 2*expert_ffn, hidden]: gate rows, then up rows */
+  const void* w_down;       /* [num_experts, hidden, expert_ffn] */
+} mk_layer_weights;
+
+typedef struct mk_weights {
+  const void* embed;              /* [vocab, hidden] */
+  const void* final_norm;         /* [hidden] */
+  const void* lm_head;            /* [vocab, hidden] (untied from embed) */
+  const mk_layer_weights* layers; /* host array [num_layers]; copied by mk_create */
+} mk_weights;
+
+/* Device-side error record of the last failing step (see mk_get_status). */
+typedef struct mk_status {
+  int32_t code;      /* MK_OK, MK_ERR_TIMEOUT or MK_ERR_DEVICE_BOUNDS */
+  int32_t op;        /* task kind that failed (1 embed, 2 qkv, 3 attention, 4 o-proj, 5 router, 6 moe, 7 head) */
+  int32_t layer;
+  int32_t cta;       /* thread block that recorded the error */
+  uint32_t counter;  /* counter index waited on (timeout) */
+  uint32_t observed; /* its value when the wait gave up (timeout) / the bad value (bounds) */
+  uint32_t target;   /* the value the wait needed (timeout) */
+  int32_t detail;    /* row / page slot involved, or -1 */
+} mk_status;
+
+typedef struct mk_ctx mk_ctx;
+
+/*
+ * Create a context on the current CUDA device.
+ *   cfg, weights: host structs, read during the call; weight tensors are device
+ *                 pointers that must outlive the context.
+ *   out:          receives the new context.
+ * Allocates the library's workspace (per-layer activations, counters, task
+ * lists, pinned staging).  Errors: MK_ERR_INVALID_ARG (null or non-positive or
+ * misaligned argument), MK_ERR_UNSUPPORTED (device or shape outside the
+ * build's limits), MK_ERR_OOM, MK_ERR_CUDA.
+ */
+int mk_create(const mk_config* cfg, const mk_weights* weights, mk_ctx** out);
+
+/*
+ * Enqueue one decode step on `stream` and return without waiting.
+ *   batch:        number of rows, 1..max_batch.
+ *   token_ids:    device int32 [batch], the token decoded by each row.
+ *   seq_lens:     HOST int32 [batch], each row's length including this token
+ *                 (its position is seq_len-1), 1..max_pages_per_seq*page_size.
+ *                 The host splits attention work from these lengths.
+ *   block_tables: device int32 [batch, max_pages_per_seq]; entry p of row b is
+ *                 the pool page holding positions p*page_size..; entries past
+ *                 ceil(seq_len/page_size) are not read.
+ *   kv_pages:     device bf16 [num_layers][num_pages][2 (K,V)][num_kv_heads]
+ *                 [page_size][head_dim].  K is stored after RoPE.  The step
+ *                 writes this token's K and V at position seq_len-1 of every
+ *                 layer and reads positions 0..seq_len-2.
+ *   logits_out:   device fp32 [batch, vocab].
+ * Re-running a step with the same arguments is idempotent.  Steps on one
+ * context must not run concurrently (the workspace is shared).
+ */
+int mk_decode_step(mk_ctx* ctx, int32_t batch, const int32_t* token_ids, const int32_t* seq_lens,
+                   const int32_t* block_tables, void* kv_pages, float* logits_out, mk_stream_t stream);
+
+/*
+ * Wait for the last enqueued step and report device-side errors.  Fills `out`
+ * and returns out->code (MK_OK when the step ran clean).  Reading clears the
+ * record.  After an error the context stays usable.
+ */
+int mk_get_status(mk_ctx* ctx, mk_status* out);
+
+/* Text of the last error of the calling thread ("" if none).  Valid until the thread's next call. */
+const char* mk_last_error(void);
+
+/* Free everything the library allocated.  NULL is ignored.  Does not touch caller memory. */
+void mk_destroy(mk_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MK_H */

@@ -1,0 +1,749 @@
+// mk_host.cpp -- host side of the megakernel library: argument checks, the
+// static task lists, the per-step attention split plan, the workspace, the
+// cooperative launch, status readback, debug reads and a CPU simulator of the
+// task graph.
+//
+// Scheduling follows "Inside the megakernel serving engine for North Mini
+// Code" ("Image 2" paragraph): the step is split into tasks of one tile of one
+// operation, dealt over the SMs, one list per SM in global memory; attention
+// and MoE work depend on live lengths and routing.  Here the static lists (all
+// GEMV tiles, one "drain attention" and one "drain MoE" task per layer) are
+// built once per context; the attention split plan is rebuilt on the host each
+// step from the host-side lengths; the MoE tiles are queued on the device by
+// the router.
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <random>
+#include <string>
+#include <vector>
+
+#include "mk.h"
+#include "mk_debug.h"
+#include "mk_layout.h"
+
+namespace mk {
+cudaError_t launch_step(const Params& p, cudaStream_t s);
+cudaError_t configure_kernels(int D);
+cudaError_t occupancy(int D, int* blocks);
+size_t smem_bytes();
+}  // namespace mk
+
+using mk::CounterMap;
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(e == cudaErrorMemoryAllocation ? MK_ERR_OOM : MK_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------- config checks
+int check_config(const mk_config* c) {
+  if (!c) return fail(MK_ERR_INVALID_ARG, "config is NULL");
+  const struct { const char* n; int32_t v; } pos[] = {
+      {"num_layers", c->num_layers}, {"hidden", c->hidden}, {"num_q_heads", c->num_q_heads},
+      {"num_kv_heads", c->num_kv_heads}, {"head_dim", c->head_dim}, {"num_experts", c->num_experts},
+      {"top_k", c->top_k}, {"expert_ffn", c->expert_ffn}, {"vocab", c->vocab}, {"page_size", c->page_size},
+      {"num_pages", c->num_pages}, {"max_batch", c->max_batch}, {"max_pages_per_seq", c->max_pages_per_seq}};
+  for (const auto& f : pos)
+    if (f.v <= 0) return fail(MK_ERR_INVALID_ARG, "config.%s must be > 0 (got %d)", f.n, f.v);
+  if (!(c->rope_theta > 0.f) || !(c->rms_eps >= 0.f)) return fail(MK_ERR_INVALID_ARG, "rope_theta must be > 0, rms_eps >= 0");
+  if (c->norm_topk != 0 && c->norm_topk != 1) return fail(MK_ERR_INVALID_ARG, "norm_topk must be 0 or 1");
+  if (c->flags != 0) return fail(MK_ERR_INVALID_ARG, "flags must be 0");
+  if (c->num_q_heads % c->num_kv_heads) return fail(MK_ERR_INVALID_ARG, "num_q_heads must be a multiple of num_kv_heads");
+  if (c->top_k > c->num_experts) return fail(MK_ERR_INVALID_ARG, "top_k > num_experts");
+  // limits of this build
+  if (c->head_dim != 64 && c->head_dim != 128) return fail(MK_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if (c->num_q_heads / c->num_kv_heads > mk::kMaxG) return fail(MK_ERR_UNSUPPORTED, "more than 8 query heads per KV head");
+  const int32_t ks[3] = {c->hidden, c->num_q_heads * c->head_dim, c->expert_ffn};
+  for (int32_t k : ks)
+    if (k % 8 || k > mk::kMaxK) return fail(MK_ERR_UNSUPPORTED, "GEMV input lengths must be multiples of 8 and <= 4096");
+  if (c->num_experts > mk::kMaxExperts) return fail(MK_ERR_UNSUPPORTED, "num_experts > 256");
+  if (c->top_k > mk::kMaxTopK) return fail(MK_ERR_UNSUPPORTED, "top_k > 8");
+  if (c->page_size * c->head_dim * 2 > mk::kSlotBytes / 2) return fail(MK_ERR_UNSUPPORTED, "page_size*head_dim*2 > 16384");
+  if (c->max_batch > mk::kMaxBatch) return fail(MK_ERR_UNSUPPORTED, "max_batch > 64");
+  if ((int64_t)c->max_pages_per_seq * c->page_size > (int64_t)1 << 30) return fail(MK_ERR_UNSUPPORTED, "sequence too long");
+  return MK_OK;
+}
+
+// ---------------------------------------------------------------- static plan
+struct Plan {
+  std::vector<mk_task> tasks;
+  std::vector<int32_t> off;
+  mk_plan_info info;
+  CounterMap cm;
+};
+
+void split_range(uint32_t n, int parts, int i, uint32_t* lo, uint32_t* hi) {
+  *lo = (uint32_t)((uint64_t)n * i / parts);
+  *hi = (uint32_t)((uint64_t)n * (i + 1) / parts);
+}
+
+void build_static_plan(const mk_config& c, int n_ctas, Plan& plan) {
+  mk_plan_info& in = plan.info;
+  std::memset(&in, 0, sizeof in);
+  const int L = c.num_layers, H = c.hidden, E = c.num_experts, V = c.vocab;
+  const int nqkv = (c.num_q_heads + 2 * c.num_kv_heads) * c.head_dim;
+  in.n_ctas = n_ctas;
+  in.f_tile = mk::kFTile;
+  in.n_ftiles = (c.expert_ffn + mk::kFTile - 1) / mk::kFTile;
+  in.r_tile = mk::kRTile;
+  in.n_rtiles = (H + mk::kRTile - 1) / mk::kRTile;
+  plan.cm = mk::counter_map(L, c.max_batch, c.num_kv_heads, E, in.n_rtiles);
+  in.n_counters = (int32_t)plan.cm.total;
+  in.max_items = n_ctas + c.max_batch * c.num_kv_heads;
+  auto count = [&](uint32_t rows) {
+    int n = 0;
+    for (int i = 0; i < n_ctas; ++i) {
+      uint32_t lo, hi;
+      split_range(rows, n_ctas, i, &lo, &hi);
+      n += hi > lo;
+    }
+    return n;
+  };
+  in.n_embed_tiles = count((uint32_t)H);
+  in.n_qkv_tiles = count((uint32_t)nqkv);
+  in.n_o_tiles = count((uint32_t)H);
+  in.n_router_tiles = count((uint32_t)E);
+  in.n_head_tiles = count((uint32_t)V);
+  const CounterMap& cm = plan.cm;
+  plan.tasks.clear();
+  plan.off.assign(n_ctas + 1, 0);
+  auto push = [&](uint16_t op, int layer, uint32_t lo, uint32_t hi, uint32_t wc, uint32_t wb, uint32_t wpb, uint32_t sc) {
+    mk_task t;
+    t.op = op; t.layer = (uint16_t)layer; t.lo = lo; t.hi = hi;
+    t.wait_ctr = wc; t.wait_base = wb; t.wait_per_b = wpb; t.signal_ctr = sc; t.reserved = 0;
+    plan.tasks.push_back(t);
+  };
+  for (int i = 0; i < n_ctas; ++i) {
+    plan.off[i] = (int32_t)plan.tasks.size();
+    uint32_t lo, hi;
+    split_range((uint32_t)H, n_ctas, i, &lo, &hi);
+    if (hi > lo) push(MK_OP_EMBED, 0, lo, hi, MK_NO_COUNTER, 0, 0, mk::C_EMBED);
+    for (int l = 0; l < L; ++l) {
+      const uint32_t base = cm.layer_base(l);
+      split_range((uint32_t)nqkv, n_ctas, i, &lo, &hi);
+      if (hi > lo) {
+        if (l == 0) push(MK_OP_QKV, l, lo, hi, mk::C_EMBED, (uint32_t)in.n_embed_tiles, 0, base + mk::L_QKV);
+        else push(MK_OP_QKV, l, lo, hi, cm.layer_base(l - 1) + mk::L_MOE, (uint32_t)in.n_rtiles, 0, base + mk::L_QKV);
+      }
+      push(MK_OP_ATTN, l, 0, 0, base + mk::L_QKV, (uint32_t)in.n_qkv_tiles, 0, MK_NO_COUNTER);
+      split_range((uint32_t)H, n_ctas, i, &lo, &hi);
+      if (hi > lo) push(MK_OP_OPROJ, l, lo, hi, base + mk::L_ATTN, 0, (uint32_t)c.num_kv_heads, base + mk::L_O);
+      split_range((uint32_t)E, n_ctas, i, &lo, &hi);
+      if (hi > lo) push(MK_OP_ROUTER, l, lo, hi, base + mk::L_O, (uint32_t)in.n_o_tiles, 0, MK_NO_COUNTER);
+      push(MK_OP_MOE, l, 0, 0, base + mk::L_RREADY, 1, 0, MK_NO_COUNTER);
+    }
+    split_range((uint32_t)V, n_ctas, i, &lo, &hi);
+    if (hi > lo)
+      push(MK_OP_HEAD, L, lo, hi, cm.layer_base(L - 1) + mk::L_MOE, (uint32_t)in.n_rtiles, 0, MK_NO_COUNTER);
+    push(MK_OP_END, 0, 0, 0, MK_NO_COUNTER, 0, 0, MK_NO_COUNTER);
+  }
+  plan.off[n_ctas] = (int32_t)plan.tasks.size();
+  in.n_tasks = (int32_t)plan.tasks.size();
+}
+
+// ---------------------------------------------------------------- per-step attention plan
+// Pages of every (row, KV head) pair are dealt over the SMs in order, each SM
+// taking an equal share of pages; a pair cut at an SM boundary becomes several
+// splits whose partial softmax states the last one merges.
+int build_attention_plan(const mk_config& c, int n_ctas, int B, const int32_t* seq_lens, std::vector<mk_attn_item>& items,
+                         std::vector<int32_t>& off, std::vector<int32_t>& pair_first) {
+  const int Hkv = c.num_kv_heads, ps = c.page_size;
+  int64_t total = 0;
+  for (int b = 0; b < B; ++b) total += (int64_t)Hkv * ((seq_lens[b] + ps - 1) / ps);
+  const int64_t quota = std::max<int64_t>(1, (total + n_ctas - 1) / n_ctas);
+  items.clear();
+  std::vector<int32_t> cta_of;
+  pair_first.assign((size_t)B * Hkv, 0);
+  int cta = 0;
+  int64_t room = quota;
+  for (int b = 0; b < B; ++b) {
+    const uint32_t np = (uint32_t)((seq_lens[b] + ps - 1) / ps);
+    for (int kvh = 0; kvh < Hkv; ++kvh) {
+      const size_t first = items.size();
+      pair_first[(size_t)b * Hkv + kvh] = (int32_t)first;
+      uint32_t lo = 0;
+      uint16_t split = 0;
+      while (lo < np) {
+        const uint32_t take = (uint32_t)std::min<int64_t>(room, np - lo);
+        mk_attn_item it;
+        it.b = (uint16_t)b; it.kvh = (uint16_t)kvh; it.split = split++; it.nsplit = 0;
+        it.page_lo = lo; it.page_hi = lo + take;
+        items.push_back(it);
+        cta_of.push_back(cta);
+        lo += take;
+        room -= take;
+        if (room == 0) { ++cta; room = quota; }
+      }
+      for (size_t i = first; i < items.size(); ++i) items[i].nsplit = split;
+    }
+  }
+  off.assign(n_ctas + 1, 0);
+  for (size_t i = 0; i < items.size(); ++i) off[cta_of[i] + 1]++;
+  for (int i = 0; i < n_ctas; ++i) off[i + 1] += off[i];
+  return MK_OK;
+}
+
+}  // namespace
+
+// ==================================================================== context
+struct mk_ctx {
+  mk_config cfg;
+  int device = 0;
+  int n_ctas = 0;
+  Plan plan;
+  mk::LayerW* d_layers = nullptr;
+  mk_task* d_tasks = nullptr;
+  int32_t* d_task_off = nullptr;
+  const uint16_t* embed = nullptr;
+  const uint16_t* final_norm = nullptr;
+  const uint16_t* lm_head = nullptr;
+  // workspace
+  uint8_t* ws = nullptr;
+  float *X = nullptr, *QKV = nullptr, *ATT = nullptr, *PO = nullptr, *PML = nullptr, *RLOG = nullptr, *RW = nullptr,
+        *HB = nullptr, *PART = nullptr;
+  int32_t *RIDS = nullptr, *ACT = nullptr, *NACT = nullptr, *TOK = nullptr, *CNT = nullptr;
+  uint32_t* ctr = nullptr;
+  mk_status* d_status = nullptr;
+  // per-step staging (double-buffered)
+  size_t step_bytes = 0;
+  size_t off_lens = 0, off_cos = 0, off_sin = 0, off_items = 0, off_item_off = 0, off_pair = 0;
+  uint8_t* h_step[2] = {nullptr, nullptr};
+  uint8_t* d_step[2] = {nullptr, nullptr};
+  cudaEvent_t ev_step[2] = {nullptr, nullptr};
+  cudaEvent_t ev_done = nullptr;
+  int cur = 0;
+  bool stepped = false;
+  int last_B = 0;
+  std::vector<double> inv_freq;
+  // test hook
+  int stall_layer = -1;
+  uint32_t stall_ms = 0;
+};
+
+namespace {
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+void free_ctx(mk_ctx* c) {
+  if (!c) return;
+  cudaFree(c->d_layers);
+  cudaFree(c->d_tasks);
+  cudaFree(c->d_task_off);
+  cudaFree(c->ws);
+  for (int i = 0; i < 2; ++i) {
+    if (c->h_step[i]) cudaFreeHost(c->h_step[i]);
+    cudaFree(c->d_step[i]);
+    if (c->ev_step[i]) cudaEventDestroy(c->ev_step[i]);
+  }
+  if (c->ev_done) cudaEventDestroy(c->ev_done);
+  delete c;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mk_last_error(void) { return g_err.c_str(); }
+
+int mk_create(const mk_config* cfg, const mk_weights* w, mk_ctx** out) {
+  g_err.clear();
+  if (!out) return fail(MK_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  if (!w || !w->layers || !w->embed || !w->final_norm || !w->lm_head)
+    return fail(MK_ERR_INVALID_ARG, "weights: a required pointer is NULL");
+  if (!aligned16(w->embed) || !aligned16(w->final_norm) || !aligned16(w->lm_head))
+    return fail(MK_ERR_INVALID_ARG, "weights: pointers must be 16-byte aligned");
+  for (int l = 0; l < cfg->num_layers; ++l) {
+    const mk_layer_weights& lw = w->layers[l];
+    const void* req[7] = {lw.attn_norm, lw.w_qkv, lw.w_o, lw.ffn_norm, lw.w_router, lw.w_gate_up, lw.w_down};
+    for (const void* p : req) {
+      if (!p) return fail(MK_ERR_INVALID_ARG, "weights: layer %d has a NULL tensor", l);
+      if (!aligned16(p)) return fail(MK_ERR_INVALID_ARG, "weights: layer %d tensor not 16-byte aligned", l);
+    }
+    if (lw.router_bias && (reinterpret_cast<uintptr_t>(lw.router_bias) & 3u))
+      return fail(MK_ERR_INVALID_ARG, "weights: layer %d router_bias misaligned", l);
+  }
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  cudaDeviceProp prop;
+  if ((e = cudaGetDeviceProperties(&prop, dev)) != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+  if (prop.major * 10 + prop.minor != 103)
+    return fail(MK_ERR_UNSUPPORTED, "device %s is sm_%d%d; this build is for sm_103", prop.name, prop.major, prop.minor);
+  if (!prop.cooperativeLaunch) return fail(MK_ERR_UNSUPPORTED, "device has no cooperative launch");
+  const size_t smem = mk::smem_bytes();
+  if (prop.sharedMemPerBlockOptin < smem)
+    return fail(MK_ERR_UNSUPPORTED, "needs %zu bytes of shared memory per block, device offers %zu", smem,
+                (size_t)prop.sharedMemPerBlockOptin);
+  if ((e = mk::configure_kernels(cfg->head_dim)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+  int blocks = 0;
+  if ((e = mk::occupancy(cfg->head_dim, &blocks)) != cudaSuccess) return cuda_fail(e, "occupancy");
+  if (blocks < 1) return fail(MK_ERR_UNSUPPORTED, "the step kernel does not fit on an SM");
+
+  mk_ctx* c = new mk_ctx();
+  c->cfg = *cfg;
+  if (c->cfg.watchdog_ms == 0) c->cfg.watchdog_ms = 1000;
+  c->device = dev;
+  c->n_ctas = prop.multiProcessorCount;
+  build_static_plan(c->cfg, c->n_ctas, c->plan);
+  const mk_plan_info& in = c->plan.info;
+  const int L = cfg->num_layers, H = cfg->hidden, D = cfg->head_dim, Hq = cfg->num_q_heads, Hkv = cfg->num_kv_heads;
+  const int G = Hq / Hkv, E = cfg->num_experts, K = cfg->top_k, F = cfg->expert_ffn, MB = cfg->max_batch;
+  const int nqkv = (Hq + 2 * Hkv) * D;
+  c->embed = static_cast<const uint16_t*>(w->embed);
+  c->final_norm = static_cast<const uint16_t*>(w->final_norm);
+  c->lm_head = static_cast<const uint16_t*>(w->lm_head);
+  c->inv_freq.resize(D / 2);
+  for (int i = 0; i < D / 2; ++i) c->inv_freq[i] = std::pow((double)cfg->rope_theta, -2.0 * i / D);
+
+  std::vector<mk::LayerW> lws(L);
+  for (int l = 0; l < L; ++l) {
+    const mk_layer_weights& s = w->layers[l];
+    lws[l] = {static_cast<const uint16_t*>(s.attn_norm), static_cast<const uint16_t*>(s.w_qkv),
+              static_cast<const uint16_t*>(s.w_o), static_cast<const uint16_t*>(s.ffn_norm),
+              static_cast<const uint16_t*>(s.w_router), s.router_bias, static_cast<const uint16_t*>(s.w_gate_up),
+              static_cast<const uint16_t*>(s.w_down)};
+  }
+  // workspace
+  struct Part { void** ptr; size_t bytes; };
+  const size_t f4 = sizeof(float), i4 = sizeof(int32_t);
+  const Part parts[] = {
+      {(void**)&c->X, (size_t)(2 * L + 1) * MB * H * f4},
+      {(void**)&c->QKV, (size_t)L * MB * nqkv * f4},
+      {(void**)&c->ATT, (size_t)L * MB * Hq * D * f4},
+      {(void**)&c->PO, (size_t)in.max_items * G * D * f4},
+      {(void**)&c->PML, (size_t)in.max_items * G * 2 * f4},
+      {(void**)&c->RLOG, (size_t)L * MB * E * f4},
+      {(void**)&c->RIDS, (size_t)L * MB * K * i4},
+      {(void**)&c->RW, (size_t)L * MB * K * f4},
+      {(void**)&c->ACT, (size_t)L * E * i4},
+      {(void**)&c->NACT, (size_t)L * i4},
+      {(void**)&c->TOK, (size_t)L * E * MB * i4},
+      {(void**)&c->CNT, (size_t)L * E * i4},
+      {(void**)&c->HB, (size_t)L * MB * K * F * f4},
+      {(void**)&c->PART, (size_t)L * MB * K * H * f4},
+      {(void**)&c->ctr, (size_t)c->plan.cm.total * 4},
+      {(void**)&c->d_status, sizeof(mk_status)},
+  };
+  size_t total = 0;
+  for (const Part& p : parts) total += align256(p.bytes);
+  if ((e = cudaMalloc(&c->ws, total)) != cudaSuccess) { free_ctx(c); return cuda_fail(e, "workspace"); }
+  size_t o = 0;
+  for (const Part& p : parts) { *p.ptr = c->ws + o; o += align256(p.bytes); }
+  if ((e = cudaMemset(c->ws, 0, total)) != cudaSuccess) { free_ctx(c); return cuda_fail(e, "workspace memset"); }
+  // static plan + layer table
+  if ((e = cudaMalloc(&c->d_layers, sizeof(mk::LayerW) * L)) != cudaSuccess ||
+      (e = cudaMalloc(&c->d_tasks, sizeof(mk_task) * c->plan.tasks.size())) != cudaSuccess ||
+      (e = cudaMalloc(&c->d_task_off, sizeof(int32_t) * c->plan.off.size())) != cudaSuccess) {
+    free_ctx(c);
+    return cuda_fail(e, "plan buffers");
+  }
+  if ((e = cudaMemcpy(c->d_layers, lws.data(), sizeof(mk::LayerW) * L, cudaMemcpyHostToDevice)) != cudaSuccess ||
+      (e = cudaMemcpy(c->d_tasks, c->plan.tasks.data(), sizeof(mk_task) * c->plan.tasks.size(),
+                      cudaMemcpyHostToDevice)) != cudaSuccess ||
+      (e = cudaMemcpy(c->d_task_off, c->plan.off.data(), sizeof(int32_t) * c->plan.off.size(),
+                      cudaMemcpyHostToDevice)) != cudaSuccess) {
+    free_ctx(c);
+    return cuda_fail(e, "plan upload");
+  }
+  // per-step buffer layout
+  size_t so = 0;
+  auto take = [&](size_t bytes) { size_t r = so; so += (bytes + 15) & ~(size_t)15; return r; };
+  c->off_lens = take((size_t)MB * i4);
+  c->off_cos = take((size_t)MB * (D / 2) * f4);
+  c->off_sin = take((size_t)MB * (D / 2) * f4);
+  c->off_items = take((size_t)in.max_items * sizeof(mk_attn_item));
+  c->off_item_off = take((size_t)(c->n_ctas + 1) * i4);
+  c->off_pair = take((size_t)MB * Hkv * i4);
+  c->step_bytes = so;
+  for (int i = 0; i < 2; ++i) {
+    if ((e = cudaHostAlloc((void**)&c->h_step[i], so, cudaHostAllocDefault)) != cudaSuccess ||
+        (e = cudaMalloc(&c->d_step[i], so)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&c->ev_step[i], cudaEventDisableTiming)) != cudaSuccess) {
+      free_ctx(c);
+      return cuda_fail(e, "step staging");
+    }
+  }
+  if ((e = cudaEventCreateWithFlags(&c->ev_done, cudaEventDisableTiming)) != cudaSuccess) {
+    free_ctx(c);
+    return cuda_fail(e, "event");
+  }
+  *out = c;
+  return MK_OK;
+}
+
+int mk_decode_step(mk_ctx* c, int32_t batch, const int32_t* token_ids, const int32_t* seq_lens,
+                   const int32_t* block_tables, void* kv_pages, float* logits_out, mk_stream_t stream) {
+  g_err.clear();
+  if (!c) return fail(MK_ERR_INVALID_ARG, "ctx is NULL");
+  const mk_config& cf = c->cfg;
+  if (batch < 1 || batch > cf.max_batch) return fail(MK_ERR_INVALID_ARG, "batch %d outside 1..%d", batch, cf.max_batch);
+  if (!token_ids || !seq_lens || !block_tables || !kv_pages || !logits_out)
+    return fail(MK_ERR_INVALID_ARG, "a step pointer is NULL");
+  if (!aligned16(kv_pages)) return fail(MK_ERR_INVALID_ARG, "kv_pages must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(token_ids) | reinterpret_cast<uintptr_t>(block_tables) |
+       reinterpret_cast<uintptr_t>(logits_out)) & 3u)
+    return fail(MK_ERR_INVALID_ARG, "token_ids, block_tables and logits_out must be 4-byte aligned");
+  const int64_t max_len = (int64_t)cf.max_pages_per_seq * cf.page_size;
+  for (int b = 0; b < batch; ++b)
+    if (seq_lens[b] < 1 || seq_lens[b] > max_len)
+      return fail(MK_ERR_INVALID_ARG, "seq_lens[%d]=%d outside 1..%lld", b, seq_lens[b], (long long)max_len);
+  cudaError_t e;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // host-built per-step data into the staging buffer not used by the previous step
+  const int cur = c->cur;
+  if ((e = cudaEventSynchronize(c->ev_step[cur])) != cudaSuccess) return cuda_fail(e, "staging event");
+  uint8_t* h = c->h_step[cur];
+  std::vector<mk_attn_item> items;
+  std::vector<int32_t> item_off, pair_first;
+  build_attention_plan(cf, c->n_ctas, batch, seq_lens, items, item_off, pair_first);
+  if ((int)items.size() > c->plan.info.max_items) return fail(MK_ERR_INVALID_ARG, "attention plan overflow");
+  const int D = cf.head_dim;
+  std::memcpy(h + c->off_lens, seq_lens, sizeof(int32_t) * batch);
+  float* cs = reinterpret_cast<float*>(h + c->off_cos);
+  float* sn = reinterpret_cast<float*>(h + c->off_sin);
+  for (int b = 0; b < batch; ++b) {
+    const double pos = (double)(seq_lens[b] - 1);
+    for (int i = 0; i < D / 2; ++i) {
+      const double ang = pos * c->inv_freq[i];
+      cs[b * (D / 2) + i] = (float)std::cos(ang);
+      sn[b * (D / 2) + i] = (float)std::sin(ang);
+    }
+  }
+  std::memcpy(h + c->off_items, items.data(), sizeof(mk_attn_item) * items.size());
+  std::memcpy(h + c->off_item_off, item_off.data(), sizeof(int32_t) * item_off.size());
+  std::memcpy(h + c->off_pair, pair_first.data(), sizeof(int32_t) * pair_first.size());
+  uint8_t* d = c->d_step[cur];
+  if ((e = cudaMemcpyAsync(d, h, c->step_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    return cuda_fail(e, "step upload");
+  if ((e = cudaEventRecord(c->ev_step[cur], s)) != cudaSuccess) return cuda_fail(e, "event record");
+  c->cur ^= 1;
+
+  mk::Params p;
+  std::memset(&p, 0, sizeof p);
+  p.L = cf.num_layers; p.H = cf.hidden; p.Hq = cf.num_q_heads; p.Hkv = cf.num_kv_heads; p.D = D;
+  p.G = cf.num_q_heads / cf.num_kv_heads; p.E = cf.num_experts; p.K = cf.top_k; p.F = cf.expert_ffn;
+  p.V = cf.vocab; p.ps = cf.page_size; p.P = cf.num_pages; p.maxpg = cf.max_pages_per_seq;
+  p.nqkv = (cf.num_q_heads + 2 * cf.num_kv_heads) * D;
+  p.norm_topk = cf.norm_topk;
+  p.eps = cf.rms_eps;
+  p.scale = (float)(1.0 / std::sqrt((double)D));
+  p.B = batch; p.max_batch = cf.max_batch; p.n_ctas = c->n_ctas;
+  const mk_plan_info& in = c->plan.info;
+  p.n_qkv_tiles = in.n_qkv_tiles; p.n_o_tiles = in.n_o_tiles; p.n_router_tiles = in.n_router_tiles;
+  p.n_ftiles = in.n_ftiles; p.n_rtiles = in.n_rtiles;
+  p.cm = c->plan.cm;
+  uint32_t wd_ms = cf.watchdog_ms;
+  p.tasks = c->d_tasks; p.task_off = c->d_task_off;
+  p.layers = c->d_layers; p.embed = c->embed; p.final_norm = c->final_norm; p.lm_head = c->lm_head;
+  p.tokens = token_ids; p.block_tables = block_tables; p.kv = static_cast<uint16_t*>(kv_pages); p.logits = logits_out;
+  p.seq_lens = reinterpret_cast<const int32_t*>(d + c->off_lens);
+  p.rope_cos = reinterpret_cast<const float*>(d + c->off_cos);
+  p.rope_sin = reinterpret_cast<const float*>(d + c->off_sin);
+  p.items = reinterpret_cast<const mk_attn_item*>(d + c->off_items);
+  p.item_off = reinterpret_cast<const int32_t*>(d + c->off_item_off);
+  p.pair_first = reinterpret_cast<const int32_t*>(d + c->off_pair);
+  p.X = c->X; p.QKV = c->QKV; p.ATT = c->ATT; p.PO = c->PO; p.PML = c->PML; p.RLOG = c->RLOG; p.RIDS = c->RIDS;
+  p.RW = c->RW; p.ACT = c->ACT; p.NACT = c->NACT; p.TOK = c->TOK; p.CNT = c->CNT; p.HB = c->HB; p.PART = c->PART;
+  p.ctr = c->ctr; p.status = c->d_status;
+
+  // test hook: one O-proj task waits on a counter nothing increments
+  int stall_idx = -1;
+  mk_task saved;
+  if (c->stall_layer >= 0) {
+    for (int i = c->plan.off[0]; i < c->plan.off[1]; ++i) {
+      const mk_task& t = c->plan.tasks[i];
+      if (t.op == MK_OP_OPROJ && t.layer == c->stall_layer) { stall_idx = i; break; }
+    }
+    if (stall_idx >= 0) {
+      saved = c->plan.tasks[stall_idx];
+      mk_task t = saved;
+      t.wait_ctr = mk::C_NEVER; t.wait_base = 1; t.wait_per_b = 0;
+      if ((e = cudaMemcpyAsync(c->d_tasks + stall_idx, &t, sizeof t, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+        return cuda_fail(e, "stall arm");
+      if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "stall arm sync");
+      if (c->stall_ms) wd_ms = c->stall_ms;
+    }
+    c->stall_layer = -1;
+  }
+  p.watchdog_ns = (uint64_t)wd_ms * 1000000ull;
+  if ((e = mk::launch_step(p, s)) != cudaSuccess) return cuda_fail(e, "cooperative launch");
+  if (stall_idx >= 0) {
+    if ((e = cudaMemcpyAsync(c->d_tasks + stall_idx, &saved, sizeof saved, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+      return cuda_fail(e, "stall disarm");
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "stall disarm sync");
+  }
+  if ((e = cudaEventRecord(c->ev_done, s)) != cudaSuccess) return cuda_fail(e, "event record");
+  c->stepped = true;
+  c->last_B = batch;
+  return MK_OK;
+}
+
+int mk_get_status(mk_ctx* c, mk_status* out) {
+  g_err.clear();
+  if (!c || !out) return fail(MK_ERR_INVALID_ARG, "ctx or out is NULL");
+  std::memset(out, 0, sizeof *out);
+  cudaError_t e;
+  if (c->stepped && (e = cudaEventSynchronize(c->ev_done)) != cudaSuccess) return cuda_fail(e, "step");
+  if ((e = cudaMemcpy(out, c->d_status, sizeof *out, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "status read");
+  if (out->code != MK_OK) {
+    if ((e = cudaMemset(c->d_status, 0, sizeof(mk_status))) != cudaSuccess) return cuda_fail(e, "status clear");
+    g_err = out->code == MK_ERR_TIMEOUT ? "device: a dependency wait ran out" : "device: index out of range";
+  }
+  return out->code;
+}
+
+void mk_destroy(mk_ctx* c) {
+  if (!c) return;
+  if (c->stepped) cudaEventSynchronize(c->ev_done);
+  free_ctx(c);
+}
+
+// ==================================================================== debug / planning
+int mk_num_ctas(mk_ctx* c) { return c ? c->n_ctas : 0; }
+
+int mk_debug_inject_stall(mk_ctx* c, int32_t layer, uint32_t watchdog_ms) {
+  g_err.clear();
+  if (!c) return fail(MK_ERR_INVALID_ARG, "ctx is NULL");
+  if (layer >= c->cfg.num_layers) return fail(MK_ERR_INVALID_ARG, "layer out of range");
+  c->stall_layer = layer;
+  c->stall_ms = watchdog_ms;
+  return MK_OK;
+}
+
+int mk_debug_read(mk_ctx* c, int32_t what, int32_t layer, void* dst, size_t bytes) {
+  g_err.clear();
+  if (!c || !dst) return fail(MK_ERR_INVALID_ARG, "ctx or dst is NULL");
+  if (!c->stepped) return fail(MK_ERR_INVALID_ARG, "no step has run");
+  const mk_config& cf = c->cfg;
+  const int B = c->last_B, MB = cf.max_batch, L = cf.num_layers;
+  if (what != MK_DBG_X && (layer < 0 || layer >= L)) return fail(MK_ERR_INVALID_ARG, "layer out of range");
+  const void* src = nullptr;
+  size_t row = 0, rows = 0, stride = 0;   // copy `rows` rows of `row` bytes, source stride `stride`
+  const size_t nqkv = (size_t)(cf.num_q_heads + 2 * cf.num_kv_heads) * cf.head_dim;
+  const size_t K = cf.top_k, E = cf.num_experts, H = cf.hidden, F = cf.expert_ffn;
+  const size_t QD = (size_t)cf.num_q_heads * cf.head_dim;
+  switch (what) {
+    case MK_DBG_X: src = c->X; row = (size_t)B * H * 4; rows = 2 * L + 1; stride = (size_t)MB * H * 4; break;
+    case MK_DBG_QKV: src = c->QKV + (size_t)layer * MB * nqkv; row = (size_t)B * nqkv * 4; rows = 1; break;
+    case MK_DBG_ATTN: src = c->ATT + (size_t)layer * MB * QD; row = (size_t)B * QD * 4; rows = 1; break;
+    case MK_DBG_ROUTER: src = c->RLOG + (size_t)layer * MB * E; row = (size_t)B * E * 4; rows = 1; break;
+    case MK_DBG_ROUTE_IDS: src = c->RIDS + (size_t)layer * MB * K; row = (size_t)B * K * 4; rows = 1; break;
+    case MK_DBG_ROUTE_W: src = c->RW + (size_t)layer * MB * K; row = (size_t)B * K * 4; rows = 1; break;
+    case MK_DBG_H: src = c->HB + (size_t)layer * MB * K * F; row = (size_t)B * K * F * 4; rows = 1; break;
+    default: return fail(MK_ERR_INVALID_ARG, "unknown buffer %d", what);
+  }
+  if (bytes != row * rows) return fail(MK_ERR_INVALID_ARG, "bytes must be %zu", row * rows);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "sync");
+  if (rows == 1) e = cudaMemcpy(dst, src, row, cudaMemcpyDeviceToHost);
+  else e = cudaMemcpy2D(dst, row, src, stride, row, rows, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "debug read");
+  return MK_OK;
+}
+
+int mk_plan_static(const mk_config* cfg, int32_t n_ctas, mk_plan_info* info, mk_task* tasks, int32_t* cta_offsets) {
+  g_err.clear();
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  if (n_ctas < 1 || !info) return fail(MK_ERR_INVALID_ARG, "n_ctas < 1 or info NULL");
+  Plan plan;
+  build_static_plan(*cfg, n_ctas, plan);
+  *info = plan.info;
+  if (tasks) std::memcpy(tasks, plan.tasks.data(), sizeof(mk_task) * plan.tasks.size());
+  if (cta_offsets) std::memcpy(cta_offsets, plan.off.data(), sizeof(int32_t) * plan.off.size());
+  return MK_OK;
+}
+
+int mk_plan_attention(const mk_config* cfg, int32_t n_ctas, int32_t batch, const int32_t* seq_lens,
+                      mk_attn_item* items, int32_t max_items, int32_t* cta_offsets, int32_t* n_items) {
+  g_err.clear();
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  if (n_ctas < 1 || batch < 1 || batch > cfg->max_batch || !seq_lens || !n_items)
+    return fail(MK_ERR_INVALID_ARG, "bad arguments");
+  const int64_t max_len = (int64_t)cfg->max_pages_per_seq * cfg->page_size;
+  for (int b = 0; b < batch; ++b)
+    if (seq_lens[b] < 1 || seq_lens[b] > max_len) return fail(MK_ERR_INVALID_ARG, "seq_lens[%d] out of range", b);
+  std::vector<mk_attn_item> it;
+  std::vector<int32_t> off, pf;
+  build_attention_plan(*cfg, n_ctas, batch, seq_lens, it, off, pf);
+  *n_items = (int32_t)it.size();
+  if ((int32_t)it.size() > max_items) return fail(MK_ERR_INVALID_ARG, "max_items too small (%zu needed)", it.size());
+  if (items) std::memcpy(items, it.data(), sizeof(mk_attn_item) * it.size());
+  if (cta_offsets) std::memcpy(cta_offsets, off.data(), sizeof(int32_t) * off.size());
+  return MK_OK;
+}
+
+// -------------------------------------------------------------------- CPU simulator
+// A model of the device runtime at tile granularity: per virtual SM, a producer
+// that turns tasks into tile records (claiming MoE queue items as it goes, at
+// most `lead` records ahead) and a consumer that runs records in order, honours
+// each record's counter wait and applies its counter effects (including the
+// "last arrival merges" rules of attention splits, routing and MoE row tiles).
+int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t B, const int32_t* seq_lens, const int32_t* routing_ids,
+                uint64_t seed, int32_t lead, mk_sim_result* out) {
+  g_err.clear();
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  if (!out || !seq_lens || !routing_ids || n_ctas < 1 || B < 1 || B > cfg->max_batch || lead < 1)
+    return fail(MK_ERR_INVALID_ARG, "bad arguments");
+  std::memset(out, 0, sizeof *out);
+  Plan plan;
+  build_static_plan(*cfg, n_ctas, plan);
+  std::vector<mk_attn_item> items;
+  std::vector<int32_t> ioff, pf;
+  build_attention_plan(*cfg, n_ctas, B, seq_lens, items, ioff, pf);
+  const mk_plan_info& in = plan.info;
+  const CounterMap& cm = plan.cm;
+  const int L = cfg->num_layers, E = cfg->num_experts, K = cfg->top_k, Hkv = cfg->num_kv_heads;
+  std::vector<uint32_t> ctr(cm.total, 0);
+  std::vector<int> nact(L, 0);
+  for (int l = 0; l < L; ++l) {
+    std::vector<char> on(E, 0);
+    for (int b = 0; b < B; ++b)
+      for (int j = 0; j < K; ++j) {
+        const int e = routing_ids[((size_t)l * B + b) * K + j];
+        if (e < 0 || e >= E) return fail(MK_ERR_INVALID_ARG, "routing id out of range");
+        on[e] = 1;
+      }
+    for (int e = 0; e < E; ++e) nact[l] += on[e];
+  }
+  std::vector<std::vector<int>> claims(L);
+  for (int l = 0; l < L; ++l) claims[l].assign((size_t)nact[l] * (in.n_ftiles + in.n_rtiles), 0);
+
+  struct Rec { int kind; int task; int layer; uint32_t a; uint32_t x; };   // kind: op, or 100 = gate/up, 101 = down
+  struct Sm { std::vector<Rec> q; size_t qhead = 0; int ti; bool prod_done = false; bool moe_active = false; bool done = false; };
+  std::vector<Sm> sm(n_ctas);
+  for (int i = 0; i < n_ctas; ++i) sm[i].ti = plan.off[i];
+  std::mt19937_64 rng(seed);
+
+  auto target = [&](const mk_task& t) { return t.wait_base + t.wait_per_b * (uint32_t)B; };
+  auto produce = [&](int i) -> bool {   // one record; false if blocked or finished
+    Sm& s = sm[i];
+    if (s.prod_done || (int)(s.q.size() - s.qhead) >= lead) return false;
+    const mk_task& t = plan.tasks[s.ti];
+    switch (t.op) {
+      case MK_OP_ATTN:
+        for (int it = ioff[i]; it < ioff[i + 1]; ++it) s.q.push_back({MK_OP_ATTN, s.ti, t.layer, (uint32_t)it, 0});
+        break;
+      case MK_OP_MOE: {
+        const int l = t.layer;
+        if (ctr[cm.layer_base(l) + mk::L_RREADY] < 1) return false;
+        const uint32_t n_gu = (uint32_t)nact[l] * in.n_ftiles;
+        const uint32_t n_tot = n_gu + (uint32_t)nact[l] * in.n_rtiles;
+        const uint32_t qi = ctr[cm.layer_base(l) + mk::L_MOEQ]++;
+        if (qi < n_tot) {
+          claims[l][qi]++;
+          if (qi < n_gu) s.q.push_back({100, s.ti, l, qi / in.n_ftiles, qi % in.n_ftiles});
+          else s.q.push_back({101, s.ti, l, (qi - n_gu) / in.n_rtiles, (qi - n_gu) % in.n_rtiles});
+          return true;   // stay on this task
+        }
+        break;
+      }
+      default: s.q.push_back({t.op, s.ti, t.layer, 0, 0}); break;
+    }
+    if (t.op == MK_OP_END) s.prod_done = true;
+    else s.ti++;
+    return true;
+  };
+  auto consume = [&](int i) -> bool {
+    Sm& s = sm[i];
+    if (s.done || s.qhead >= s.q.size()) return false;
+    const Rec& r = s.q[s.qhead];
+    const mk_task& t = plan.tasks[r.task];
+    const uint32_t base = cm.layer_base(r.layer);
+    switch (r.kind) {
+      case MK_OP_ATTN: {
+        if (ctr[t.wait_ctr] < target(t)) return false;
+        const mk_attn_item& it = items[r.a];
+        const uint32_t pc = base + mk::L_PAIR + it.b * Hkv + it.kvh;
+        if (++ctr[pc] == it.nsplit) ctr[base + mk::L_ATTN]++;
+        break;
+      }
+      case 100:
+        ctr[base + cm.gu_off + r.a]++;
+        break;
+      case 101:
+        if (ctr[base + cm.gu_off + r.a] < (uint32_t)in.n_ftiles) return false;
+        if (++ctr[base + cm.down_off + r.x] == (uint32_t)nact[r.layer]) ctr[base + mk::L_MOE]++;
+        break;
+      case MK_OP_ROUTER:
+        if (ctr[t.wait_ctr] < target(t)) return false;
+        if (++ctr[base + mk::L_RARR] == (uint32_t)in.n_router_tiles) ctr[base + mk::L_RREADY] = 1;
+        break;
+      case MK_OP_END:
+        ctr[mk::C_FINISH]++;
+        s.done = true;
+        break;
+      default:
+        if (t.wait_ctr != MK_NO_COUNTER && ctr[t.wait_ctr] < target(t)) return false;
+        if (t.signal_ctr != MK_NO_COUNTER) ctr[t.signal_ctr]++;
+        break;
+    }
+    int op = r.kind >= 100 ? MK_OP_MOE : r.kind;
+    out->tiles_run[op]++;
+    s.qhead++;
+    return true;
+  };
+  std::vector<int> order(2 * n_ctas);
+  for (int i = 0; i < 2 * n_ctas; ++i) order[i] = i;
+  int finished = 0;
+  while (finished < n_ctas) {
+    std::shuffle(order.begin(), order.end(), rng);
+    bool progress = false;
+    for (int k : order) {
+      const int i = k >> 1;
+      const bool ok = (k & 1) ? consume(i) : produce(i);
+      if (ok) {
+        progress = true;
+        out->events++;
+        if ((k & 1) && sm[i].done) finished++;
+        break;
+      }
+    }
+    if (!progress) { out->deadlocked = 1; break; }
+  }
+  out->finished = finished == n_ctas;
+  bool ok = ctr[mk::C_EMBED] == (uint32_t)in.n_embed_tiles && ctr[mk::C_FINISH] == (uint32_t)n_ctas;
+  for (int l = 0; l < L && ok; ++l) {
+    const uint32_t base = cm.layer_base(l);
+    ok = ctr[base + mk::L_QKV] == (uint32_t)in.n_qkv_tiles && ctr[base + mk::L_ATTN] == (uint32_t)(B * Hkv) &&
+         ctr[base + mk::L_O] == (uint32_t)in.n_o_tiles && ctr[base + mk::L_RARR] == (uint32_t)in.n_router_tiles &&
+         ctr[base + mk::L_RREADY] == 1u && ctr[base + mk::L_MOE] == (uint32_t)in.n_rtiles;
+    for (int a = 0; a < nact[l] && ok; ++a) ok = ctr[base + cm.gu_off + a] == (uint32_t)in.n_ftiles;
+    for (int rt = 0; rt < in.n_rtiles && ok; ++rt) ok = ctr[base + cm.down_off + rt] == (uint32_t)nact[l];
+  }
+  out->counters_ok = ok;
+  bool qok = true;
+  for (int l = 0; l < L; ++l)
+    for (int v : claims[l]) qok = qok && v == 1;
+  out->queue_items_ok = qok;
+  return MK_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,176 @@
+"""Host-side tests of the CUDA library (no GPU needed): it loads and exports every
+symbol the headers declare, rejects bad arguments before any launch, builds
+plans that cover every tile exactly once in a dependency-respecting order, and
+its task graph runs to completion without deadlock in the CPU simulator."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import workloads as W
+import persistent_moe_decode_megakernel_gb300 as mk
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+N_CTAS = 152
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    mk.build()
+
+
+def _declared():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            names |= set(re.findall(r"^[A-Za-z_][\w \*]*?\b(mk_\w+)\s*\(", src, flags=re.M))
+    return names
+
+
+def test_library_exports_every_declared_symbol():
+    names = _declared()
+    assert {"mk_create", "mk_decode_step", "mk_destroy", "mk_get_status", "mk_last_error"} <= names
+    lib = ctypes.CDLL(mk.LIB_PATH)
+    missing = [n for n in sorted(names) if not hasattr(lib, n)]
+    assert missing == []
+    assert set(mk.EXPORTS) == names
+
+
+def _cfg(model=W.TINY, ps=16, pages=64, mb=8, mpp=32, **over):
+    c = mk.make_config(model, ps, pages, mb, mpp)
+    for k, v in over.items():
+        setattr(c, k, v)
+    return c
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("hidden", 0, mk.MK_ERR_INVALID_ARG), ("num_layers", -1, mk.MK_ERR_INVALID_ARG),
+    ("num_q_heads", 3, mk.MK_ERR_INVALID_ARG), ("top_k", 9, mk.MK_ERR_INVALID_ARG),
+    ("head_dim", 96, mk.MK_ERR_UNSUPPORTED), ("max_batch", 65, mk.MK_ERR_UNSUPPORTED),
+    ("hidden", 4100, mk.MK_ERR_UNSUPPORTED), ("page_size", 256, mk.MK_ERR_UNSUPPORTED),
+    ("norm_topk", 2, mk.MK_ERR_INVALID_ARG), ("flags", 1, mk.MK_ERR_INVALID_ARG),
+    ("num_experts", 300, mk.MK_ERR_UNSUPPORTED),
+])
+def test_create_rejects_bad_config(field, value, code):
+    c = _cfg(**{field: value})
+    ctx = ctypes.c_void_p()
+    w = mk.Weights()
+    rc = mk.lib().mk_create(ctypes.byref(c), ctypes.byref(w), ctypes.byref(ctx))
+    assert rc == code
+    assert not ctx.value
+    assert mk.lib().mk_last_error().decode() != ""
+
+
+def test_create_rejects_null_and_misaligned_weights():
+    c = _cfg()
+    ctx = ctypes.c_void_p()
+    w = mk.Weights()
+    assert mk.lib().mk_create(ctypes.byref(c), ctypes.byref(w), ctypes.byref(ctx)) == mk.MK_ERR_INVALID_ARG
+    lws = (mk.LayerWeights * c.num_layers)()
+    for l in range(c.num_layers):
+        for n in ("attn_norm", "w_qkv", "w_o", "ffn_norm", "w_router", "w_gate_up", "w_down"):
+            setattr(lws[l], n, 4096)
+    w.embed, w.final_norm, w.lm_head, w.layers = 4096, 4096, 4096, lws
+    lws[1].w_o = 4098   # not 16-byte aligned
+    assert mk.lib().mk_create(ctypes.byref(c), ctypes.byref(w), ctypes.byref(ctx)) == mk.MK_ERR_INVALID_ARG
+    assert "aligned" in mk.lib().mk_last_error().decode()
+
+
+def test_step_rejects_null_context():
+    sl = np.array([5], dtype=np.int32)
+    rc = mk.lib().mk_decode_step(None, 1, None, sl.ctypes.data, None, None, None, None)
+    assert rc == mk.MK_ERR_INVALID_ARG
+    st = mk.Status()
+    assert mk.lib().mk_get_status(None, ctypes.byref(st)) == mk.MK_ERR_INVALID_ARG
+    mk.lib().mk_destroy(None)   # NULL is ignored
+
+
+def _check_static_plan(cfg, n_ctas):
+    info, tasks, off = mk.plan_static(cfg, n_ctas)
+    m_rows = {2: (cfg.num_q_heads + 2 * cfg.num_kv_heads) * cfg.head_dim, 4: cfg.hidden, 5: cfg.num_experts,
+              7: cfg.vocab, 1: cfg.hidden}
+    cover = {}
+    for i in range(n_ctas):
+        lst = tasks[off[i]:off[i + 1]]
+        assert lst[-1].op == 8                       # END closes every list
+        L = cfg.num_layers
+        order = [(-1, 0) if t.op == 1 else (L, 0) if t.op == 7 else (L + 1, 0) if t.op == 8 else (t.layer, t.op)
+                 for t in lst]
+        assert order == sorted(order)                # topological: layer by layer, phase by phase
+        for t in lst:
+            if t.op in m_rows:
+                cover.setdefault((t.op, t.layer), []).append((t.lo, t.hi))
+    for (op, layer), ranges in cover.items():
+        ranges.sort()
+        assert ranges[0][0] == 0 and ranges[-1][1] == m_rows[op]
+        assert all(a[1] == b[0] for a, b in zip(ranges, ranges[1:]))   # each row exactly once
+    assert info.n_qkv_tiles == len(cover[(2, 0)]) and info.n_head_tiles == len(cover[(7, cfg.num_layers)])
+    return info
+
+
+def test_static_plan_covers_every_row_once():
+    _check_static_plan(_cfg(), N_CTAS)
+    _check_static_plan(_cfg(), 7)
+    info = _check_static_plan(mk.make_config(W.MOE30B, 16, 1000, 64, 600), N_CTAS)
+    assert info.n_qkv_tiles == N_CTAS and info.n_router_tiles == 128
+    assert info.n_ftiles == 48 and info.n_rtiles == 32
+
+
+@pytest.mark.parametrize("lens", [[65], [1], [16], [17], [512, 1, 33, 200, 16, 15, 100, 7], [8193]])
+def test_attention_plan_covers_pages_once(lens):
+    cfg = _cfg(mpp=1024, pages=4096) if max(lens) > 512 else _cfg()
+    items, off = mk.plan_attention(cfg, N_CTAS, lens)
+    ps, Hkv = cfg.page_size, cfg.num_kv_heads
+    seen = {}
+    for i, it in enumerate(items):
+        seen.setdefault((it.b, it.kvh), []).append((it.split, it.nsplit, it.page_lo, it.page_hi, i))
+    for b, L in enumerate(lens):
+        for h in range(Hkv):
+            s = seen[(b, h)]
+            npg = (L + ps - 1) // ps
+            assert [x[0] for x in s] == list(range(len(s))) and all(x[1] == len(s) for x in s)
+            assert s[0][2] == 0 and s[-1][3] == npg and all(a[3] == b_[2] for a, b_ in zip(s, s[1:]))
+            assert [x[4] for x in s] == list(range(s[0][4], s[0][4] + len(s)))   # consecutive items
+    # CSR over SMs, in order; page load balanced within one page of the quota
+    assert off[0] == 0 and off[-1] == len(items) and (np.diff(off) >= 0).all()
+    loads = [sum(items[j].page_hi - items[j].page_lo for j in range(off[i], off[i + 1])) for i in range(N_CTAS)]
+    total = sum(Hkv * ((L + ps - 1) // ps) for L in lens)
+    quota = -(-total // N_CTAS)
+    assert max(loads) <= quota and sum(loads) == total
+
+
+def _random_routing(cfg, B, seed):
+    rng = np.random.default_rng(seed)
+    return np.stack([np.stack([rng.choice(cfg.num_experts, cfg.top_k, replace=False) for _ in range(B)])
+                     for _ in range(cfg.num_layers)]).astype(np.int32)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_simulated_step_completes_tiny(seed):
+    cfg = _cfg()
+    lens = [65, 1, 300, 17, 16, 512, 2, 90][: 1 + seed % 8]
+    r = mk.simulate(cfg, N_CTAS if seed % 2 else 5, lens, _random_routing(cfg, len(lens), seed), seed=seed,
+                    lead=1 + seed % 6)
+    assert r.finished and not r.deadlocked and r.counters_ok and r.queue_items_ok
+
+
+def test_simulated_step_completes_30b_shapes():
+    cfg = mk.make_config(W.MOE30B, 16, 40000, 64, 2100)
+    for B, seed in ((1, 1), (64, 2)):
+        lens = W.lengths_loguniform(B, 512, 32768) if B > 1 else [8193]
+        r = mk.simulate(cfg, N_CTAS, lens, _random_routing(cfg, B, seed), seed=seed, lead=6)
+        assert r.finished and not r.deadlocked and r.counters_ok and r.queue_items_ok
+        # every MoE item and every attention item ran
+        assert r.tiles_run[3] == len(mk.plan_attention(cfg, N_CTAS, lens)[0]) * cfg.num_layers
+
+
+def test_simulator_detects_a_missing_producer():
+    # a routing table that names an out-of-range expert is rejected up front
+    cfg = _cfg()
+    bad = _random_routing(cfg, 1, 0)
+    bad[0, 0, 0] = 99
+    with pytest.raises(mk.MkError):
+        mk.simulate(cfg, 8, [5], bad)
