@@ -58,7 +58,7 @@ typedef struct CUstream_st* mk_stream_t;
  *   head_dim in {64, 128}; num_q_heads % num_kv_heads == 0 with at most 8 query
  *   heads per KV head; hidden, num_q_heads*head_dim and expert_ffn multiples of 8
  *   and <= 4096; num_experts <= 256; top_k <= min(8, num_experts);
- *   page_size*head_dim*2 <= 16384 bytes; max_batch <= 64.
+ *   page_size*head_dim*2 <= 32768 bytes; max_batch <= 64.
  */
 typedef struct mk_config {
   int32_t num_layers;

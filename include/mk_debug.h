@@ -116,6 +116,18 @@ int mk_debug_read(mk_ctx* ctx, int32_t what, int32_t layer, void* host_dst, size
  * after `watchdog_ms` (0 keeps the context's budget).  layer < 0 disarms. */
 int mk_debug_inject_stall(mk_ctx* ctx, int32_t layer, uint32_t watchdog_ms);
 
+/* Timeline of later steps.  enable != 0 allocates a device buffer of
+ * n_ctas * events_per_cta events (4 x uint64 each: time the tile's first
+ * operand landed, time its dependency was met, time it finished, tag =
+ * op | layer<<8 | kind<<24 | index<<32; globaltimer ns) and records every
+ * later step into it (each step overwrites the previous one); enable == 0
+ * frees it.  Event 0 of each block is a header (consumer events, kernel start,
+ * producer events); producer events fill the block's area from its end. */
+int mk_debug_trace(mk_ctx* ctx, int32_t enable, int32_t events_per_cta);
+
+/* Copy the timeline of the last step to host memory (synchronises). */
+int mk_debug_trace_read(mk_ctx* ctx, void* host_dst, size_t bytes);
+
 /* Number of SMs (persistent thread blocks) a step of this context launches. */
 int mk_num_ctas(mk_ctx* ctx);
 

@@ -130,7 +130,8 @@ class SimResult(ctypes.Structure):
 
 
 EXPORTS = ("mk_create", "mk_decode_step", "mk_get_status", "mk_last_error", "mk_destroy", "mk_plan_static",
-           "mk_plan_attention", "mk_simulate", "mk_debug_read", "mk_debug_inject_stall", "mk_num_ctas")
+           "mk_plan_attention", "mk_simulate", "mk_debug_read", "mk_debug_inject_stall", "mk_num_ctas",
+           "mk_debug_trace", "mk_debug_trace_read")
 
 _lib = None
 _lock = threading.Lock()
@@ -158,6 +159,8 @@ def lib():
             L.mk_debug_read.argtypes = [vp, i32, i32, vp, ctypes.c_size_t]
             L.mk_debug_inject_stall.argtypes = [vp, i32, u32]
             L.mk_num_ctas.argtypes = [vp]
+            L.mk_debug_trace.argtypes = [vp, i32, i32]
+            L.mk_debug_trace_read.argtypes = [vp, vp, ctypes.c_size_t]
             _lib = L
     return _lib
 
@@ -307,6 +310,16 @@ class Engine:
         shape, dt = shapes[what]
         out = np.empty(shape, dtype=dt)
         _check(lib().mk_debug_read(self.ctx, DBG[what], layer, out.ctypes.data, out.nbytes))
+        return out
+
+    def trace(self, enable: bool = True, events_per_cta: int = 2048):
+        """Record the timeline of the following steps (see ``trace.summarize``)."""
+        self._trace_cap = events_per_cta if enable else 0
+        _check(lib().mk_debug_trace(self.ctx, 1 if enable else 0, events_per_cta))
+
+    def read_trace(self):
+        out = np.zeros((self.n_ctas, self._trace_cap, 4), dtype=np.uint64)
+        _check(lib().mk_debug_trace_read(self.ctx, out.ctypes.data, out.nbytes))
         return out
 
     def inject_stall(self, layer: int, watchdog_ms: int = 0):

@@ -79,7 +79,7 @@ int check_config(const mk_config* c) {
     if (k % 8 || k > mk::kMaxK) return fail(MK_ERR_UNSUPPORTED, "GEMV input lengths must be multiples of 8 and <= 4096");
   if (c->num_experts > mk::kMaxExperts) return fail(MK_ERR_UNSUPPORTED, "num_experts > 256");
   if (c->top_k > mk::kMaxTopK) return fail(MK_ERR_UNSUPPORTED, "top_k > 8");
-  if (c->page_size * c->head_dim * 2 > mk::kSlotBytes / 2) return fail(MK_ERR_UNSUPPORTED, "page_size*head_dim*2 > 16384");
+  if (c->page_size * c->head_dim * 2 > mk::kSlotBytes / 2) return fail(MK_ERR_UNSUPPORTED, "page_size*head_dim*2 > 32768");
   if (c->max_batch > mk::kMaxBatch) return fail(MK_ERR_UNSUPPORTED, "max_batch > 64");
   if ((int64_t)c->max_pages_per_seq * c->page_size > (int64_t)1 << 30) return fail(MK_ERR_UNSUPPORTED, "sequence too long");
   return MK_OK;
@@ -221,7 +221,8 @@ struct mk_ctx {
   // workspace
   uint8_t* ws = nullptr;
   float *X = nullptr, *QKV = nullptr, *ATT = nullptr, *PO = nullptr, *PML = nullptr, *RLOG = nullptr, *RW = nullptr,
-        *HB = nullptr, *PART = nullptr;
+        *HB = nullptr, *PART = nullptr, *SS = nullptr;
+  int n_ss_slots = 0;
   int32_t *RIDS = nullptr, *ACT = nullptr, *NACT = nullptr, *TOK = nullptr, *CNT = nullptr;
   uint32_t* ctr = nullptr;
   mk_status* d_status = nullptr;
@@ -236,6 +237,9 @@ struct mk_ctx {
   bool stepped = false;
   int last_B = 0;
   std::vector<double> inv_freq;
+  // timeline
+  uint64_t* trace = nullptr;
+  int32_t trace_cap = 0;
   // test hook
   int stall_layer = -1;
   uint32_t stall_ms = 0;
@@ -251,6 +255,7 @@ void free_ctx(mk_ctx* c) {
   cudaFree(c->d_tasks);
   cudaFree(c->d_task_off);
   cudaFree(c->ws);
+  cudaFree(c->trace);
   for (int i = 0; i < 2; ++i) {
     if (c->h_step[i]) cudaFreeHost(c->h_step[i]);
     cudaFree(c->d_step[i]);
@@ -345,6 +350,7 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_ctx** out) {
       {(void**)&c->CNT, (size_t)L * E * i4},
       {(void**)&c->HB, (size_t)L * MB * K * F * f4},
       {(void**)&c->PART, (size_t)L * MB * K * H * f4},
+      {(void**)&c->SS, (size_t)(2 * L + 1) * std::max(c->n_ctas, in.n_rtiles) * MB * f4},
       {(void**)&c->ctr, (size_t)c->plan.cm.total * 4},
       {(void**)&c->d_status, sizeof(mk_status)},
   };
@@ -468,7 +474,9 @@ int mk_decode_step(mk_ctx* c, int32_t batch, const int32_t* token_ids, const int
   p.pair_first = reinterpret_cast<const int32_t*>(d + c->off_pair);
   p.X = c->X; p.QKV = c->QKV; p.ATT = c->ATT; p.PO = c->PO; p.PML = c->PML; p.RLOG = c->RLOG; p.RIDS = c->RIDS;
   p.RW = c->RW; p.ACT = c->ACT; p.NACT = c->NACT; p.TOK = c->TOK; p.CNT = c->CNT; p.HB = c->HB; p.PART = c->PART;
+  p.SS = c->SS; p.n_ss_slots = std::max(c->n_ctas, in.n_rtiles);
   p.ctr = c->ctr; p.status = c->d_status;
+  p.trace = c->trace; p.trace_cap = c->trace_cap;
 
   // test hook: one O-proj task waits on a counter nothing increments
   int stall_idx = -1;
@@ -563,6 +571,35 @@ int mk_debug_read(mk_ctx* c, int32_t what, int32_t layer, void* dst, size_t byte
   if (rows == 1) e = cudaMemcpy(dst, src, row, cudaMemcpyDeviceToHost);
   else e = cudaMemcpy2D(dst, row, src, stride, row, rows, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e, "debug read");
+  return MK_OK;
+}
+
+int mk_debug_trace(mk_ctx* c, int32_t enable, int32_t events_per_cta) {
+  g_err.clear();
+  if (!c) return fail(MK_ERR_INVALID_ARG, "ctx is NULL");
+  cudaError_t e;
+  if (c->stepped && (e = cudaEventSynchronize(c->ev_done)) != cudaSuccess) return cuda_fail(e, "step");
+  cudaFree(c->trace);
+  c->trace = nullptr;
+  c->trace_cap = 0;
+  if (!enable) return MK_OK;
+  if (events_per_cta < 16 || events_per_cta > (1 << 20)) return fail(MK_ERR_INVALID_ARG, "events_per_cta out of range");
+  const size_t bytes = (size_t)c->n_ctas * events_per_cta * 32;
+  if ((e = cudaMalloc(&c->trace, bytes)) != cudaSuccess) return cuda_fail(e, "trace buffer");
+  if ((e = cudaMemset(c->trace, 0, bytes)) != cudaSuccess) return cuda_fail(e, "trace clear");
+  c->trace_cap = events_per_cta;
+  return MK_OK;
+}
+
+int mk_debug_trace_read(mk_ctx* c, void* dst, size_t bytes) {
+  g_err.clear();
+  if (!c || !dst) return fail(MK_ERR_INVALID_ARG, "ctx or dst is NULL");
+  if (!c->trace) return fail(MK_ERR_INVALID_ARG, "tracing is not enabled");
+  const size_t want = (size_t)c->n_ctas * c->trace_cap * 32;
+  if (bytes != want) return fail(MK_ERR_INVALID_ARG, "bytes must be %zu", want);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "sync");
+  if ((e = cudaMemcpy(dst, c->trace, want, cudaMemcpyDeviceToHost)) != cudaSuccess) return cuda_fail(e, "trace read");
   return MK_OK;
 }
 

@@ -158,6 +158,8 @@ __device__ __forceinline__ float warp_max(float v) {
 
 // --------------------------------------------------------------------------- shared memory
 enum : uint8_t { R_EMBED = 1, R_GEMV = 2, R_ATTN = 3, R_GU = 4, R_DOWN = 5, R_END = 6 };
+// GEMV stream kinds beyond the task ops (MK_OP_QKV / OPROJ / ROUTER / HEAD)
+enum : int { R_OP_GU = 100, R_OP_DOWN = 101 };
 
 struct Meta {
   uint8_t kind, op, first, last;
@@ -180,7 +182,7 @@ struct __align__(128) Smem {
   uint64_t empty[kSlots];
   Meta meta[kSlots];
   union {
-    float red[kConsumerWarps][kMaxRowsPerChunk][4];
+    float seg[2][kMaxRowsPerChunk][kConsumerWarps][4];   // GEMV segment sums [record parity][row][segment][batch row]
     float attn[kAttnScratch];
   } scr;
   float rstd[kMaxBatch];
@@ -234,8 +236,9 @@ __device__ bool wait_counter(const Params& p, uint32_t idx, uint32_t target, int
   }
 }
 
-// all consumer threads: wait until record c has landed in its slot
-__device__ bool wait_record(const Params& p, Smem& S, uint32_t c) {
+// one warp: wait until record c has landed in its slot.  Warps consume records
+// independently; false (warp-uniform) if the step was aborted meanwhile.
+__device__ bool warp_wait_record(const Params& p, Smem& S, uint32_t c) {
   const int s = static_cast<int>(c % kSlots);
   const uint32_t ph = (c / kSlots) & 1u;
   bool ok = mbar_try_wait(&S.full[s], ph);
@@ -246,18 +249,38 @@ __device__ bool wait_record(const Params& p, Smem& S, uint32_t c) {
       if ((it & 63u) == 0u) {
         if (aborted(p)) break;
         if (globaltimer() - t0 > p.watchdog_ns) {
-          record_error(p, MK_ERR_TIMEOUT, 0, -1, MK_NO_COUNTER, c, 0, -1, true);
+          if ((threadIdx.x & 31) == 0) record_error(p, MK_ERR_TIMEOUT, 0, -1, MK_NO_COUNTER, c, 0, -1, true);
           break;
         }
       }
     }
   }
-  return cbar_and(ok);
+  return __all_sync(0xffffffffu, ok);
 }
 
-__device__ __forceinline__ void release_record(Smem& S, uint32_t c) {
+// one warp: done reading record c's slot
+__device__ __forceinline__ void warp_release_record(Smem& S, uint32_t c) {
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(&S.empty[c % kSlots]);
+}
+
+// barrier over the group of `nw` consecutive warps containing this warp (nw in {1, 2, 4, 8}) that ANDs a flag
+__device__ __forceinline__ bool group_bar_and(bool v, int nw) {
+  if (nw == 1) return __all_sync(0xffffffffu, v);
+  if (nw == kConsumerWarps) return cbar_and(v);
+  uint32_t r;
+  const uint32_t id = 2u + static_cast<uint32_t>((threadIdx.x >> 5) / nw);
+  const uint32_t cnt = 32u * static_cast<uint32_t>(nw);
+  __syncwarp();
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(cnt)
+      : "memory");
+  return r != 0;
 }
 
 // consumer-side dependency wait: thread 0 spins, everyone learns the outcome
@@ -271,7 +294,6 @@ __device__ bool consumer_wait(const Params& p, uint32_t idx, uint32_t target, in
 __device__ void consumer_signal(const Params& p, uint32_t idx) {
   cbar();
   if (threadIdx.x == 0 && idx != MK_NO_COUNTER) {
-    __threadfence();
     red_release_add(p.ctr + idx, 1u);
   }
 }
@@ -280,7 +302,6 @@ __device__ void consumer_signal(const Params& p, uint32_t idx) {
 __device__ bool consumer_arrive_last(const Params& p, Smem& S, uint32_t idx, uint32_t total) {
   cbar();
   if (threadIdx.x == 0) {
-    __threadfence();
     const uint32_t old = atom_add_acq_rel(p.ctr + idx, 1u);
     S.flag = (old + 1u == total) ? 1 : 0;
   }
@@ -294,6 +315,7 @@ struct Producer {
   const Params& p;
   Smem& S;
   uint32_t c = 0;
+  uint32_t pev = 0;   // producer trace events (written from the end of the block's trace area)
   uint64_t pol;
   __device__ Producer(const Params& p_, Smem& S_) : p(p_), S(S_) { pol = policy_evict_first(); }
 
@@ -314,7 +336,15 @@ struct Producer {
       }
     }
   }
-  __device__ Meta& meta() { return S.meta[c % kSlots]; }
+  __device__ Meta& meta() {
+    Meta& m = S.meta[c % kSlots];
+    if (p.trace) {
+      const uint64_t t = globaltimer();
+      m.pad[0] = static_cast<uint32_t>(t);
+      m.pad[1] = static_cast<uint32_t>(t >> 32);
+    }
+    return m;
+  }
   __device__ uint8_t* slot() { return S.ring[c % kSlots]; }
   __device__ uint64_t* full() { return &S.full[c % kSlots]; }
 
@@ -397,7 +427,17 @@ struct Producer {
   __device__ bool moe_queue(const mk_task& t) {
     const int l = t.layer;
     const uint32_t base = p.cm.layer_base(l);
+    const uint64_t t0 = p.trace ? globaltimer() : 0;
     if (!wait_counter(p, base + L_RREADY, 1u, MK_OP_MOE, l)) return false;
+    if (p.trace && pev < static_cast<uint32_t>(p.trace_cap) / 2) {
+      uint64_t* e = p.trace + (static_cast<size_t>(blockIdx.x) * p.trace_cap + p.trace_cap - 1 - pev) * 4;
+      e[0] = t0;
+      e[1] = globaltimer();
+      e[2] = e[1];
+      e[3] = static_cast<uint64_t>(MK_OP_MOE) | (static_cast<uint64_t>(l) << 8) |
+             (static_cast<uint64_t>(TR_PRODUCER_ROUTE_WAIT) << 24);
+      ++pev;
+    }
     const uint32_t nact = static_cast<uint32_t>(__ldcg(p.NACT + l));
     const uint32_t n_gu = nact * static_cast<uint32_t>(p.n_ftiles);
     const uint32_t n_tot = n_gu + nact * static_cast<uint32_t>(p.n_rtiles);
@@ -470,219 +510,264 @@ struct Producer {
       if (!ok) break;
     }
     S.prod_count = c;
+    if (p.trace) p.trace[static_cast<size_t>(blockIdx.x) * p.trace_cap * 4 + 2] = pev;
   }
 };
 
 // --------------------------------------------------------------------------- GEMV pieces
-// A chunk holds `n` rows of length K (bf16).  Thread t covers the 16-byte units
-// u = ut + NTG*i of every row its group handles; groups split the rows when a
-// row has fewer than 256 units.
-struct Geom {
-  int K, U, NTG, P, UPT, g, ut;
-  __device__ Geom(int K_) : K(K_) {
-    U = K >> 3;
-    NTG = U >= kConsumerThreads ? kConsumerThreads : ((U + 31) & ~31);
-    P = kConsumerThreads / NTG;
-    UPT = (U + NTG - 1) / NTG;
-    const int t = threadIdx.x;
-    g = t / NTG;
-    ut = t - g * NTG;
+// A chunk holds rows of length K (bf16, row-major).  A row is cut into S
+// segments (S a power of two) so that one segment of the input vector -- at
+// most 2048/TB values per row of the batch -- fits in registers: 8/TB
+// 16-byte units per lane.  Warp w owns segment w % S of rows w/S, w/S + 8/S,
+// ...: each lane dots its units of the row from shared memory against its
+// register slice, and one warp reduction finishes the segment.  With S == 1 a
+// warp finishes whole rows on its own; with S > 1 the segment sums meet in
+// shared memory behind one barrier.
+template <int TB>
+struct Seg {
+  static constexpr int kUnits = 8 / TB;   // 16-byte units per lane held in registers (64 floats in all)
+  int K, S, KS, U;                         // segments per row, segment length, units per segment
+  int s, rg, RPG;                          // this warp's segment, its first row, row stride
+  __device__ explicit Seg(int K_, int min_s = 1) : K(K_) {
+    S = min_s;
+    while (S < kConsumerWarps && S * (256 * kUnits / 8) * 8 < K) S <<= 1;
+    KS = ((K + S - 1) / S + 7) & ~7;
+    U = KS >> 3;
+    const int w = threadIdx.x >> 5;
+    s = w & (S - 1);
+    rg = w / S;
+    RPG = kConsumerWarps / S;
+    full = (U == 32 * kUnits) && (S * KS == K);
   }
-  __device__ bool unit_ok(int i) const { return g < P && i < UPT && (ut + NTG * i) < U; }
-  __device__ int unit(int i) const { return ut + NTG * i; }
+  bool full;   // every lane owns all kUnits units of its segment (no bounds checks needed)
+  // element offset in the row of this lane's j-th unit, or -1
+  __device__ __forceinline__ int unit(int j) const {
+    const int u = (threadIdx.x & 31) + 32 * j;
+    const int e = s * KS + u * 8;
+    return (u < U && e < K) ? e : -1;
+  }
 };
 
-// Load this thread's slice of the GEMV input for `nt` rows.  src(b) points at row
-// b's fp32 vector (length K).  If g is non-null the slice is RMS-normalised with
-// S.rstd[b] and the bf16 gain g.
+__device__ __forceinline__ void unpack8(const uint4 w, float (&f)[8]) {
+  f[0] = bf_lo(w.x); f[1] = bf_hi(w.x); f[2] = bf_lo(w.y); f[3] = bf_hi(w.y);
+  f[4] = bf_lo(w.z); f[5] = bf_hi(w.z); f[6] = bf_lo(w.w); f[7] = bf_hi(w.w);
+}
+
+// this lane's partial dot products of one row (row points at the row in shared memory);
+// independent partial sums per unit pair break the FMA dependency chain
 template <int TB>
-__device__ __forceinline__ void load_slice(const Geom& G, const float* const* src, int nt, const float* rstd,
-                                           const uint16_t* g, float (&y)[2][8][TB]) {
+__device__ __forceinline__ void row_dot(const uint8_t* row, const Seg<TB>& sg, const float (&y)[8 / TB][8][TB],
+                                        float (&acc)[TB]) {
+  constexpr int NU = Seg<TB>::kUnits;
+  float part[TB][2];
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const bool ok = G.unit_ok(i);
-    const int u = ok ? G.unit(i) : 0;
+  for (int tb = 0; tb < TB; ++tb) { part[tb][0] = 0.f; part[tb][1] = 0.f; }
+  if (sg.full) {
+    const uint8_t* base = row + (sg.s * sg.KS + (threadIdx.x & 31) * 8) * 2;
+#pragma unroll
+    for (int j = 0; j < NU; ++j) {
+      float wf[8];
+      unpack8(*reinterpret_cast<const uint4*>(base + j * 512), wf);
+#pragma unroll
+      for (int tb = 0; tb < TB; ++tb)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) part[tb][q & 1] = fmaf(wf[q], y[j][q][tb], part[tb][q & 1]);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < NU; ++j) {
+      const int e = sg.unit(j);
+      if (e >= 0) {
+        float wf[8];
+        unpack8(*reinterpret_cast<const uint4*>(row + e * 2), wf);
+#pragma unroll
+        for (int tb = 0; tb < TB; ++tb)
+#pragma unroll
+          for (int q = 0; q < 8; ++q) part[tb][q & 1] = fmaf(wf[q], y[j][q][tb], part[tb][q & 1]);
+      }
+    }
+  }
+#pragma unroll
+  for (int tb = 0; tb < TB; ++tb) acc[tb] += part[tb][0] + part[tb][1];
+}
+
+// rsqrt(mean(x^2) + eps) of residual-stream vector `xidx`, row b, from the
+// per-tile sums of squares its producers published (fixed order: every warp
+// gets the same value)
+__device__ __forceinline__ float rstd_of(const Params& p, int xidx, int b) {
+  const float* ss = p.SS + static_cast<size_t>(xidx) * p.n_ss_slots * p.max_batch + b;
+  float v = 0.f;
+  for (int i = threadIdx.x & 31; i < p.n_ss_slots; i += 32) v += __ldcg(ss + static_cast<size_t>(i) * p.max_batch);
+  v = warp_sum(v);
+  return 1.0f / sqrtf(v / static_cast<float>(p.H) + p.eps);
+}
+
+// Load this warp's segment of nt input vectors into registers.  src[tb] points
+// at vector tb (fp32); with g non-null each vector is RMS-normalised with rstd[tb]
+// and the bf16 gain g.  Vectors tb >= nt (or with src null) read as zero.
+template <int TB>
+__device__ __forceinline__ void load_y(const Seg<TB>& sg, const float* const (&src)[TB], const float (&rstd)[TB],
+                                       const uint16_t* g, int nt, float (&y)[8 / TB][8][TB]) {
+#pragma unroll
+  for (int j = 0; j < Seg<TB>::kUnits; ++j) {
+    const int e = sg.unit(j);
     float gv[8];
-    if (g != nullptr && ok) {
-      const uint4 gw = __ldg(reinterpret_cast<const uint4*>(g + u * 8));
-      gv[0] = bf_lo(gw.x); gv[1] = bf_hi(gw.x); gv[2] = bf_lo(gw.y); gv[3] = bf_hi(gw.y);
-      gv[4] = bf_lo(gw.z); gv[5] = bf_hi(gw.z); gv[6] = bf_lo(gw.w); gv[7] = bf_hi(gw.w);
+    if (g != nullptr && e >= 0) {
+      unpack8(__ldg(reinterpret_cast<const uint4*>(g + e)), gv);
     }
 #pragma unroll
     for (int tb = 0; tb < TB; ++tb) {
       float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      if (ok && tb < nt) {
-        const float4 a = __ldcg(reinterpret_cast<const float4*>(src[tb] + u * 8));
-        const float4 b = __ldcg(reinterpret_cast<const float4*>(src[tb] + u * 8 + 4));
+      if (e >= 0 && tb < nt && src[tb] != nullptr) {
+        const float4 a = __ldcg(reinterpret_cast<const float4*>(src[tb] + e));
+        const float4 b = __ldcg(reinterpret_cast<const float4*>(src[tb] + e + 4));
         v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
         if (g != nullptr) {
-          const float r = rstd[tb];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) v[j] = (v[j] * r) * gv[j];
+          for (int q = 0; q < 8; ++q) v[q] = (v[q] * rstd[tb]) * gv[q];
         }
       }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) y[i][j][tb] = v[j];
+      for (int q = 0; q < 8; ++q) y[j][q][tb] = v[q];
     }
   }
 }
 
-// Sum of squares of rows src(0..nt-1) (length K, all threads of the consumer
-// group cooperate) -> rstd[tb] in shared memory.
 template <int TB>
-__device__ __forceinline__ void block_rstd(const Params& p, Smem& S, const Geom& G, const float* const* src, int nt, int K,
-                           float* rstd_out) {
-  float ss[TB];
+__device__ __forceinline__ int pick_i(const int (&a)[TB], int i) {
+  int v = a[0];
 #pragma unroll
-  for (int tb = 0; tb < TB; ++tb) ss[tb] = 0.f;
-  if (G.g == 0) {
+  for (int k = 1; k < TB; ++k)
+    if (i == k) v = a[k];
+  return v;
+}
+
+template <int TB>
+__device__ __forceinline__ float pick(const float (&a)[TB], int i) {
+  float v = a[0];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      if (!G.unit_ok(i)) continue;
-      const int u = G.unit(i);
-#pragma unroll
-      for (int tb = 0; tb < TB; ++tb) {
-        if (tb >= nt) continue;
-        const float4 a = __ldcg(reinterpret_cast<const float4*>(src[tb] + u * 8));
-        const float4 b = __ldcg(reinterpret_cast<const float4*>(src[tb] + u * 8 + 4));
-        ss[tb] += a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + b.x * b.x + b.y * b.y + b.z * b.z + b.w * b.w;
-      }
-    }
-  }
+  for (int k = 1; k < TB; ++k)
+    if (i == k) v = a[k];
+  return v;
+}
+
+// per-row-of-the-batch sums of one value per thread (thread's row tb, or tb < 0
+// for none) over all consumer threads, in fixed order -> out[0..nt)
+template <int TB>
+__device__ void block_token_sums(Smem& S, int my_tb, float v, int nt, float* out, size_t out_stride) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
   for (int tb = 0; tb < TB; ++tb) {
-    const float v = warp_sum(ss[tb]);
-    if (lane == 0) S.ssred[warp][tb] = v;
+    const float w = warp_sum(my_tb == tb ? v : 0.f);
+    if (lane == 0) S.ssred[warp][tb] = w;
   }
   cbar();
   if (threadIdx.x < nt) {
     float tot = 0.f;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) tot += S.ssred[w][threadIdx.x];
-    rstd_out[threadIdx.x] = 1.0f / sqrtf(tot / static_cast<float>(K) + p.eps);
+    out[threadIdx.x * out_stride] = tot;
   }
   cbar();
-}
-
-// Dot products of the chunk's rows with the input slices; warp-reduced partials
-// land in S.scr.red; returns after the barrier that makes them visible.
-template <int TB>
-__device__ __forceinline__ void gemv_chunk(Smem& S, const Geom& G, const uint8_t* wsm, int n,
-                                           const float (&y)[2][8][TB]) {
-  float acc[kMaxRowsPerChunk][TB];
-#pragma unroll
-  for (int r = 0; r < kMaxRowsPerChunk; ++r)
-#pragma unroll
-    for (int tb = 0; tb < TB; ++tb) acc[r][tb] = 0.f;
-  if (G.g < G.P) {
-#pragma unroll
-    for (int ri = 0; ri < kMaxRowsPerChunk; ++ri) {
-      const int r = G.g + G.P * ri;
-      if (r < n) {
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          if (G.unit_ok(i)) {
-            const uint4 w = *reinterpret_cast<const uint4*>(wsm + (static_cast<size_t>(r) * G.K + G.unit(i) * 8) * 2);
-            const float wf[8] = {bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y),
-                                 bf_lo(w.z), bf_hi(w.z), bf_lo(w.w), bf_hi(w.w)};
-#pragma unroll
-            for (int tb = 0; tb < TB; ++tb)
-#pragma unroll
-              for (int j = 0; j < 8; ++j) acc[ri][tb] = fmaf(wf[j], y[i][j][tb], acc[ri][tb]);
-          }
-        }
-      }
-    }
-  }
-  const int RG = (n + G.P - 1) / G.P;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-#pragma unroll
-  for (int ri = 0; ri < kMaxRowsPerChunk; ++ri) {
-    if (ri < RG) {
-#pragma unroll
-      for (int tb = 0; tb < TB; ++tb) acc[ri][tb] = warp_sum(acc[ri][tb]);
-    }
-  }
-  cbar();  // previous chunk's readers of S.scr are done
-  if (lane == 0) {
-#pragma unroll
-    for (int ri = 0; ri < kMaxRowsPerChunk; ++ri)
-      if (ri < RG)
-#pragma unroll
-        for (int tb = 0; tb < TB; ++tb) S.scr.red[warp][ri][tb] = acc[ri][tb];
-  }
-  cbar();
-}
-
-// Final value of row r (chunk-local) for input tb: the group's warps in order.
-template <int TB>
-__device__ __forceinline__ float gemv_result(const Smem& S, const Geom& G, int r, int tb) {
-  const int grp = r % G.P, ri = r / G.P;
-  const int w0 = grp * (G.NTG >> 5), nw = G.NTG >> 5;
-  float s = 0.f;
-  for (int w = 0; w < nw; ++w) s += S.scr.red[w0 + w][ri][tb];
-  return s;
 }
 
 // --------------------------------------------------------------------------- consumer
+// Warps consume ring records independently (each waits for and releases every
+// record of a tile); block-wide barriers are taken only at tile boundaries --
+// the dependency wait at a tile's start and the signal at its end -- and, where
+// S warps split a row, over those S warps only.
 template <int TB, int D>
 struct Consumer {
   const Params& p;
   Smem& S;
-  uint32_t c = 0;
-  float y[2][8][TB];
-  int ykey = -1;   // which input the y slices hold (layer*4 + input kind), when B <= TB
+  uint32_t c = 0;       // this warp's current record
+  bool wok = true;      // this warp has not seen the step abort
+  uint32_t nev = 1;     // trace events written (event 0 is the header)
+  uint64_t twait = 0;   // when the current tile's dependency was met
 
   __device__ Consumer(const Params& p_, Smem& S_) : p(p_), S(S_) {}
+
+  __device__ void trace_event(uint32_t kind, const Meta& m, uint64_t t0) {
+    if (p.trace == nullptr || threadIdx.x != 0) return;
+    if (nev < static_cast<uint32_t>(p.trace_cap) / 2) {
+      uint64_t* e = p.trace + (static_cast<size_t>(blockIdx.x) * p.trace_cap + nev) * 4;
+      e[0] = t0;
+      e[1] = twait ? twait : t0;
+      e[2] = globaltimer();
+      e[3] = static_cast<uint64_t>(m.op) | (static_cast<uint64_t>(m.layer) << 8) | (static_cast<uint64_t>(kind) << 24) |
+             (static_cast<uint64_t>(m.kind == R_GU || m.kind == R_DOWN ? m.aux | (m.kind == R_DOWN ? 0x80000000u : 0u)
+                                                                       : m.idx) << 32);
+      ++nev;
+    }
+  }
 
   __device__ const Meta& meta() const { return S.meta[c % kSlots]; }
   __device__ const uint8_t* slot() const { return S.ring[c % kSlots]; }
 
-  // advance to the next record of a multi-chunk tile
-  __device__ bool next() {
-    release_record(S, c);
+  // chunk timeline (tracing only): issue time, when warp 0 saw the data, when it released the slot
+  uint64_t tchunk = 0;
+  __device__ void trace_chunk_seen() {
+    if (p.trace && threadIdx.x == 0) tchunk = globaltimer();
+  }
+  __device__ void trace_chunk_done() {
+    if (p.trace == nullptr || threadIdx.x != 0) return;
+    if (nev < static_cast<uint32_t>(p.trace_cap) / 2) {
+      const Meta& m = meta();
+      uint64_t* ev = p.trace + (static_cast<size_t>(blockIdx.x) * p.trace_cap + nev) * 4;
+      ev[0] = static_cast<uint64_t>(m.pad[0]) | (static_cast<uint64_t>(m.pad[1]) << 32);
+      ev[1] = tchunk;
+      ev[2] = globaltimer();
+      ev[3] = static_cast<uint64_t>(m.op) | (static_cast<uint64_t>(m.layer) << 8) |
+              (static_cast<uint64_t>(TR_CHUNK) << 24) | (static_cast<uint64_t>(c) << 32);
+      ++nev;
+    }
+  }
+
+  // this warp moves to the next record of the current tile; false if the step aborted
+  __device__ bool next_rec() {
+    trace_chunk_done();
+    warp_release_record(S, c);
     ++c;
-    return wait_record(p, S, c);
+    if (!warp_wait_record(p, S, c)) {
+      wok = false;
+      return false;
+    }
+    trace_chunk_seen();
+    return true;
   }
 
   // ------------------------------------------------------------------ inputs
-  // input kinds: 0 attention input (x_in, attn_norm), 1 O-proj input (attention output),
-  //              2 MoE input (x_mid, ffn_norm), 3 head input (x_final, final_norm)
-  __device__ __forceinline__ void input_rows(int kind, int l, int b0, int nt, const float** src, const uint16_t** g, int* K) {
-    const size_t xs = static_cast<size_t>(p.max_batch) * p.H;
-    for (int tb = 0; tb < TB; ++tb) {
-      const int b = b0 + (tb < nt ? tb : 0);
-      switch (kind) {
-        case 0: src[tb] = p.X + (2 * static_cast<size_t>(l)) * xs + static_cast<size_t>(b) * p.H; break;
-        case 1: src[tb] = p.ATT + (static_cast<size_t>(l) * p.max_batch + b) * (p.Hq * p.D); break;
-        case 2: src[tb] = p.X + (2 * static_cast<size_t>(l) + 1) * xs + static_cast<size_t>(b) * p.H; break;
-        default: src[tb] = p.X + (2 * static_cast<size_t>(p.L)) * xs + static_cast<size_t>(b) * p.H; break;
-      }
-    }
-    switch (kind) {
-      case 0: *g = p.layers[l].attn_norm; *K = p.H; break;
-      case 1: *g = nullptr; *K = p.Hq * p.D; break;
-      case 2: *g = p.layers[l].ffn_norm; *K = p.H; break;
-      default: *g = p.final_norm; *K = p.H; break;
-    }
+  // residual-stream vector xidx (layer input 2l, after attention 2l+1), row b
+  __device__ __forceinline__ const float* xrow(int xidx, int b) const {
+    return p.X + (static_cast<size_t>(xidx) * p.max_batch + b) * p.H;
   }
 
-  // load (and normalise) input rows b0..b0+nt-1 into y
-  __device__ __forceinline__ void load_input(int kind, int l, int b0, int nt) {
+  // Load the GEMV input of `kind` for rows rb[0..nt) into y (this warp's segment).
+  // kinds: 0 attention input (x_in, attn_norm), 1 O-proj input (attention output),
+  //        2 MoE input (x_mid, ffn_norm), 3 head input (x_final, final_norm)
+  __device__ __forceinline__ void load_input(const Seg<TB>& sg, int kind, int l, const int (&rb)[TB], int nt,
+                                             float (&y)[8 / TB][8][TB]) {
     const float* src[TB];
-    const uint16_t* g;
-    int K;
-    input_rows(kind, l, b0, nt, src, &g, &K);
-    Geom G(K);
-    if (g != nullptr) block_rstd<TB>(p, S, G, src, nt, K, S.rstd);
-    load_slice<TB>(G, src, nt, S.rstd, g, y);
+    float rs[TB];
+    const uint16_t* g = nullptr;
+    int xidx = 0;
+    if (kind == 0) { g = p.layers[l].attn_norm; xidx = 2 * l; }
+    else if (kind == 2) { g = p.layers[l].ffn_norm; xidx = 2 * l + 1; }
+    else if (kind == 3) { g = p.final_norm; xidx = 2 * p.L; }
+#pragma unroll
+    for (int tb = 0; tb < TB; ++tb) {
+      const int b = tb < nt ? rb[tb] : rb[0];
+      src[tb] = kind == 1 ? p.ATT + (static_cast<size_t>(l) * p.max_batch + b) * (p.Hq * p.D) : xrow(xidx, b);
+      rs[tb] = (g != nullptr && tb < nt) ? rstd_of(p, xidx, b) : 1.f;
+    }
+    load_y<TB>(sg, src, rs, g, nt, y);
   }
 
   // ------------------------------------------------------------------ EMBED
   __device__ bool embed() {
     const Meta m = meta();
     const int H = p.H;
+    float* ssout = p.SS + static_cast<size_t>(blockIdx.x) * p.max_batch;   // vector 0, slot = this block
     for (int b = 0; b < p.B; ++b) {
       int tok = __ldg(p.tokens + b);
       if (tok < 0 || tok >= p.V) {
@@ -693,78 +778,238 @@ struct Consumer {
       }
       const uint16_t* row = p.embed + static_cast<size_t>(tok) * H;
       float* x = p.X + static_cast<size_t>(b) * H;
-      for (uint32_t col = m.lo + threadIdx.x; col < m.hi; col += kConsumerThreads) x[col] = bf1(row[col]);
+      float ss = 0.f;
+      for (uint32_t col = m.lo + threadIdx.x; col < m.hi; col += kConsumerThreads) {
+        const float v = bf1(row[col]);
+        x[col] = v;
+        ss += v * v;
+      }
+      ss = warp_sum(ss);
+      if ((threadIdx.x & 31) == 0) S.ssred[threadIdx.x >> 5][0] = ss;
+      cbar();
+      if (threadIdx.x == 0) {
+        float tot = 0.f;
+        for (int w = 0; w < kConsumerWarps; ++w) tot += S.ssred[w][0];
+        ssout[b] = tot;
+      }
+      cbar();
     }
     consumer_signal(p, m.signal_ctr);
     return true;
   }
 
-  // ------------------------------------------------------------------ GEMV tiles (QKV / O / router / head)
-  __device__ bool gemv_tile() {
-    const Meta m0 = meta();
-    const int op = m0.op, l = m0.layer;
-    const int kind = op == MK_OP_QKV ? 0 : op == MK_OP_OPROJ ? 1 : op == MK_OP_ROUTER ? 2 : 3;
-    if (m0.wait_ctr != MK_NO_COUNTER && !consumer_wait(p, m0.wait_ctr, m0.wait_target, op, l)) return false;
-    const int B = p.B;
-    const float* src[TB];
-    const uint16_t* g;
-    int K;
-    input_rows(kind, op == MK_OP_HEAD ? p.L : l, 0, 1, src, &g, &K);
-    Geom G(K);
-    const int key = (op == MK_OP_HEAD ? p.L : l) * 4 + kind;
-    if (B <= TB && ykey != key) {
-      load_input(kind, l, 0, B);
-      ykey = key;
+  // ------------------------------------------------------------------ GEMV streams
+  // One loop serves every weight-streaming record: QKV / O-proj / router / head
+  // tiles and the expert gate/up and down items.  Only the input, the
+  // dependency and where the results go differ.  Gate/up chunks hold nf gate
+  // rows then the nf matching up rows; the row groups are sized so that gate
+  // row f and up row f land in the same group (one SwiGLU per pair).
+  struct OutMap {
+    float* base;          // output of (row 0 of the batch, slot 0, matrix row 0)
+    size_t sb, sj;        // strides per batch row and per routing slot
+    const float* resid;   // O-proj: residual input (same layout as base), else null
+    const float* bias;    // router bias by matrix row, or null
+  };
+
+  __device__ __forceinline__ OutMap out_map(int op, int l) const {
+    const size_t MB = p.max_batch, xs = MB * p.H;
+    OutMap o{nullptr, 0, 0, nullptr, nullptr};
+    switch (op) {
+      case MK_OP_QKV: o.base = p.QKV + l * MB * p.nqkv; o.sb = p.nqkv; break;
+      case MK_OP_OPROJ: o.base = p.X + (2 * l + 1) * xs; o.sb = p.H; o.resid = p.X + 2 * l * xs; break;
+      case MK_OP_ROUTER: o.base = p.RLOG + l * MB * p.E; o.sb = p.E; o.bias = p.layers[l].router_bias; break;
+      case MK_OP_HEAD: o.base = p.logits; o.sb = p.V; break;
+      case R_OP_GU: o.base = p.HB + l * MB * p.K * p.F; o.sb = static_cast<size_t>(p.K) * p.F; o.sj = p.F; break;
+      default: o.base = p.PART + l * MB * p.K * p.H; o.sb = static_cast<size_t>(p.K) * p.H; o.sj = p.H; break;
     }
-    const size_t xs = static_cast<size_t>(p.max_batch) * p.H;
+    return o;
+  }
+
+  // result v (v2: the matching up row for gate/up) of matrix row `row` for batch row b, slot j
+  __device__ __forceinline__ void put(const OutMap& o, bool gu, uint32_t row, int b, int j, float v, float v2,
+                                      float& my_ss) {
+    if (j < 0) return;
+    const size_t off = static_cast<size_t>(b) * o.sb + static_cast<size_t>(j) * o.sj + row;
+    if (gu) v = (v / (1.0f + expf(-v))) * v2;
+    if (o.resid != nullptr) {
+      v += __ldcg(o.resid + off);
+      my_ss += v * v;
+    }
+    if (o.bias != nullptr) v += __ldg(o.bias + row);
+    o.base[off] = v;
+  }
+
+  __device__ __forceinline__ void stream_load(const Seg<TB>& sg, bool moe, int kind, int l, int e, int b0, int nt,
+                                              int (&rb)[TB], int (&rj)[TB], float (&y)[8 / TB][8][TB]) {
+    if (moe) {
+      expert_rows(l, e, b0, nt, rb, rj);
+    } else {
+#pragma unroll
+      for (int tb = 0; tb < TB; ++tb) { rb[tb] = b0 + tb; rj[tb] = 0; }
+    }
+    if (kind == 4) load_h(sg, l, rb, rj, nt, y);
+    else load_input(sg, kind, l, rb, nt, y);
+  }
+
+  __device__ bool stream_gemv(int op) {
+    constexpr bool kGroups = TB == 4;   // only the widest instantiation sees batches wider than its registers
+    const int l = meta().layer;
+    const uint32_t sig = meta().signal_ctr, lo = meta().lo, hi = meta().hi;
+    const int e = static_cast<int>(meta().e), a = static_cast<int>(meta().idx);
+    const uint32_t rt = meta().aux;
+    const int nf0 = meta().n;
+    const uint32_t base = p.cm.layer_base(l < p.L ? l : 0);
+    const bool moe = op == R_OP_GU || op == R_OP_DOWN;
+    const bool gu = op == R_OP_GU;
+    bool ok;
+    if (gu) ok = consumer_wait(p, base + L_RREADY, 1u, MK_OP_MOE, l);
+    else if (op == R_OP_DOWN) ok = consumer_wait(p, base + p.cm.gu_off + a, static_cast<uint32_t>(p.n_ftiles), MK_OP_MOE, l);
+    else ok = meta().wait_ctr == MK_NO_COUNTER || consumer_wait(p, meta().wait_ctr, meta().wait_target, op, l);
+    if (!ok) return false;
+    twait = globaltimer();
+    const int B = p.B;
+    const int lane = threadIdx.x & 31;
+    const int K = op == MK_OP_OPROJ ? p.Hq * p.D : op == R_OP_DOWN ? p.F : p.H;
+    const Seg<TB> sg(K, gu ? (nf0 >= kConsumerWarps ? 1 : kConsumerWarps / nf0) : 1);
+    // GEMV input: 0 x_in/attn_norm, 1 attention output, 2 x_mid/ffn_norm, 3 x_final/final_norm, 4 SwiGLU h
+    const int kind = op == MK_OP_QKV ? 0 : op == MK_OP_OPROJ ? 1 : (op == MK_OP_ROUTER || gu) ? 2
+                   : op == MK_OP_HEAD ? 3 : 4;
+    if (moe) slots_for_expert(l, e);
+    const int cnt = (!moe || B <= TB) ? B : __ldcg(p.CNT + static_cast<size_t>(l) * p.E + e);
+    const int ngroups = kGroups ? (cnt + TB - 1) / TB : 1;
+    const OutMap om = out_map(op, l);
+    float my_ss = 0.f;    // O-proj: sum of squares of the residual values this lane wrote
+    int rb[TB], rj[TB];
+    float y[8 / TB][8][TB];
+    stream_load(sg, moe, kind, l, e, 0, min(cnt, TB), rb, rj, y);
     for (;;) {
-      const Meta m = meta();
+      const int n = meta().n;
+      const uint32_t row0 = meta().row0;
+      const bool last = meta().last;
       const uint8_t* wsm = slot();
-      for (int b0 = 0; b0 < B; b0 += TB) {
-        const int nt = min(TB, B - b0);
-        if (B > TB) {
-          load_input(kind, l, b0, nt);
-          ykey = -1;
-        }
-        gemv_chunk<TB>(S, G, wsm, m.n, y);
-        const int t = threadIdx.x;
-        if (t < m.n * TB) {
-          const int r = t / TB, tb = t % TB;
-          if (tb < nt) {
-            const float v = gemv_result<TB>(S, G, r, tb);
-            const int b = b0 + tb;
-            const uint32_t row = m.row0 + r;
-            switch (op) {
-              case MK_OP_QKV:
-                p.QKV[(static_cast<size_t>(l) * p.max_batch + b) * p.nqkv + row] = v;
-                break;
-              case MK_OP_OPROJ: {
-                const size_t off = static_cast<size_t>(b) * p.H + row;
-                p.X[(2 * static_cast<size_t>(l) + 1) * xs + off] = __ldcg(p.X + 2 * static_cast<size_t>(l) * xs + off) + v;
-                break;
-              }
-              case MK_OP_ROUTER: {
-                const float* bias = p.layers[l].router_bias;
-                p.RLOG[(static_cast<size_t>(l) * p.max_batch + b) * p.E + row] = bias ? v + __ldg(bias + row) : v;
-                break;
-              }
-              default:
-                p.logits[static_cast<size_t>(b) * p.V + row] = v;
-                break;
-            }
+      const int par = c & 1;
+      ok = true;
+      for (int g = 0; g < ngroups && ok; ++g) {
+        const int b0 = g * TB;
+        const int nt = min(TB, cnt - b0);
+        if (kGroups && ngroups > 1) stream_load(sg, moe, kind, l, e, b0, nt, rb, rj, y);
+        for (int r = sg.rg; r < n; r += sg.RPG) {
+          float acc[TB], acc2[TB];
+#pragma unroll
+          for (int tb = 0; tb < TB; ++tb) { acc[tb] = 0.f; acc2[tb] = 0.f; }
+          row_dot<TB>(wsm + static_cast<size_t>(r) * K * 2, sg, y, acc);
+          if (gu) row_dot<TB>(wsm + static_cast<size_t>(n + r) * K * 2, sg, y, acc2);
+#pragma unroll
+          for (int tb = 0; tb < TB; ++tb) {
+            acc[tb] = warp_sum(acc[tb]);
+            if (gu) acc2[tb] = warp_sum(acc2[tb]);
+          }
+          if (sg.S == 1) {
+            if (lane < nt)
+              put(om, gu, row0 + r, pick_i<TB>(rb, lane), pick_i<TB>(rj, lane), pick<TB>(acc, lane),
+                  pick<TB>(acc2, lane), my_ss);
+          } else if (lane < nt) {
+            S.scr.seg[par][r][sg.s][lane] = pick<TB>(acc, lane);
+            if (gu) S.scr.seg[par][kMaxRowsPerChunk / 2 + r][sg.s][lane] = pick<TB>(acc2, lane);
           }
         }
+        if (sg.S > 1) {
+          // the S warps of this row group meet; segment 0's warp finishes the rows
+          ok = group_bar_and(true, sg.S);
+          if (ok && sg.s == 0 && lane < nt) {
+            for (int r = sg.rg; r < n; r += sg.RPG) {
+              float v = 0.f, v2 = 0.f;
+              for (int q = 0; q < sg.S; ++q) {
+                v += S.scr.seg[par][r][q][lane];
+                if (gu) v2 += S.scr.seg[par][kMaxRowsPerChunk / 2 + r][q][lane];
+              }
+              put(om, gu, row0 + r, pick_i<TB>(rb, lane), pick_i<TB>(rj, lane), v, v2, my_ss);
+            }
+          }
+          if (kGroups && ngroups > 1) ok = group_bar_and(ok, sg.S);   // seg is reused by the next group
+        }
       }
-      if (m.last) break;
-      if (!next()) return false;
+      if (!ok) { wok = false; break; }
+      if (last) break;
+      if (!next_rec()) break;
     }
-    if (op == MK_OP_ROUTER) {
-      const uint32_t base = p.cm.layer_base(l);
-      if (consumer_arrive_last(p, S, base + L_RARR, static_cast<uint32_t>(p.n_router_tiles))) route(l);
-      return true;
+    if (!cbar_and(wok)) return false;
+    switch (op) {
+      case MK_OP_OPROJ: {
+        // publish this tile's share of sum(x_mid^2) for the RMSNorm of the MoE input
+        float* out = p.SS + (static_cast<size_t>(2 * l + 1) * p.n_ss_slots + blockIdx.x) * p.max_batch;
+        if (B <= TB) block_token_sums<TB>(S, lane < B ? lane : -1, my_ss, B, out, 1);
+        else oproj_ss_wide(l, lo, hi, out);
+        consumer_signal(p, sig);
+        break;
+      }
+      case MK_OP_ROUTER:
+        if (consumer_arrive_last(p, S, base + L_RARR, static_cast<uint32_t>(p.n_router_tiles))) route(l);
+        break;
+      case R_OP_GU: consumer_signal(p, base + p.cm.gu_off + a); break;
+      case R_OP_DOWN: {
+        // the last item of this row tile adds every slot into the residual, in rank order
+        const uint32_t nact = static_cast<uint32_t>(__ldcg(p.NACT + l));
+        if (consumer_arrive_last(p, S, base + p.cm.down_off + rt, nact)) down_combine(l, rt);
+        break;
+      }
+      default: consumer_signal(p, sig); break;
     }
-    consumer_signal(p, m0.signal_ctr);
     return true;
+  }
+
+  // x_out = x_mid + sum_j w_j * down_j over rows of row tile rt, rank order; publishes sum(x_out^2)
+  __device__ void down_combine(int l, uint32_t rt) {
+    const int B = p.B, H = p.H, K = p.K;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const size_t xs = static_cast<size_t>(p.max_batch) * H;
+    const int r0 = static_cast<int>(rt) * kRTile, r1 = min(H, r0 + kRTile);
+    float* ssout = p.SS + (static_cast<size_t>(2 * l + 2) * p.n_ss_slots + rt) * p.max_batch;
+    for (int b = warp; b < B; b += kConsumerWarps) {
+      const size_t lb = static_cast<size_t>(l) * p.max_batch + b;
+      float ss = 0.f;
+      for (int r = r0 + lane; r < r1; r += 32) {
+        float acc = 0.f;
+        for (int j = 0; j < K; ++j) acc += __ldcg(p.RW + lb * K + j) * __ldcg(p.PART + (lb * K + j) * H + r);
+        const size_t off = static_cast<size_t>(b) * H + r;
+        const float xv = __ldcg(p.X + (2 * static_cast<size_t>(l) + 1) * xs + off) + acc;
+        p.X[(2 * static_cast<size_t>(l) + 2) * xs + off] = xv;
+        ss += xv * xv;
+      }
+      ss = warp_sum(ss);
+      if (lane == 0) ssout[b] = ss;
+    }
+    consumer_signal(p, p.cm.layer_base(l) + L_MOE);
+  }
+
+  // sums of squares of this O-proj tile's rows for every batch row (batches wider than TB)
+  __device__ void oproj_ss_wide(int l, uint32_t lo, uint32_t hi, float* out) {
+    const size_t xs = static_cast<size_t>(p.max_batch) * p.H;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int b = warp; b < p.B; b += kConsumerWarps) {
+      float ss = 0.f;
+      for (uint32_t r = lo + lane; r < hi; r += 32) {
+        const float v = __ldcg(p.X + (2 * static_cast<size_t>(l) + 1) * xs + static_cast<size_t>(b) * p.H + r);
+        ss += v * v;
+      }
+      ss = warp_sum(ss);
+      if (lane == 0) out[b] = ss;
+    }
+    cbar();
+  }
+
+  // SwiGLU activations of (row, slot) pairs as the down projection's input
+  __device__ __forceinline__ void load_h(const Seg<TB>& sg, int l, const int (&rb)[TB], const int (&rj)[TB], int nt,
+                                         float (&y)[8 / TB][8][TB]) {
+    const float* src[TB];
+    float one[TB];
+#pragma unroll
+    for (int tb = 0; tb < TB; ++tb) {
+      one[tb] = 1.f;
+      src[tb] = (tb < nt && rj[tb] >= 0) ? p.HB + ((static_cast<size_t>(l) * p.max_batch + rb[tb]) * p.K + rj[tb]) * p.F
+                                         : nullptr;
+    }
+    load_y<TB>(sg, src, one, nullptr, nt, y);
   }
 
   // ------------------------------------------------------------------ routing (last router tile)
@@ -868,180 +1113,79 @@ struct Consumer {
     cbar();
   }
 
-  // ------------------------------------------------------------------ MoE gate/up item
-  __device__ bool gate_up_item() {
-    const Meta m0 = meta();
-    const int l = m0.layer, e = static_cast<int>(m0.e), a = static_cast<int>(m0.idx);
-    const uint32_t base = p.cm.layer_base(l);
-    if (!consumer_wait(p, base + L_RREADY, 1u, MK_OP_MOE, l)) return false;
-    const int B = p.B, H = p.H, F = p.F, K = p.K;
-    Geom G(H);
-    slots_for_expert(l, e);
-    const int key = l * 4 + 2;
-    if (B <= TB && ykey != key) {
-      load_input(2, l, 0, B);
-      ykey = key;
-    }
-    const int cnt = B <= TB ? B : __ldcg(p.CNT + static_cast<size_t>(l) * p.E + e);
+  // rows of the batch routed to expert e, in groups of TB: (row, slot); slot -1 = not routed
+  __device__ __forceinline__ void expert_rows(int l, int e, int b0, int nt, int (&rb)[TB], int (&rj)[TB]) {
     const int32_t* tok = p.TOK + (static_cast<size_t>(l) * p.E + e) * p.max_batch;
-    for (;;) {
-      const Meta m = meta();
-      const int nf = m.n;
-      for (int b0 = 0; b0 < cnt; b0 += TB) {
-        const int nt = min(TB, cnt - b0);
-        int rowb[TB], rowj[TB];
-        for (int tb = 0; tb < TB; ++tb) {
-          if (B <= TB) { rowb[tb] = b0 + tb; rowj[tb] = tb < nt ? S.slot_of[b0 + tb] : -1; }
-          else {
-            const int ent = tb < nt ? __ldcg(tok + b0 + tb) : 0;
-            rowb[tb] = ent >> 8; rowj[tb] = tb < nt ? (ent & 0xff) : -1;
-          }
-        }
-        if (B > TB) {
-          const float* src[TB];
-          const size_t xs = static_cast<size_t>(p.max_batch) * p.H;
-          for (int tb = 0; tb < TB; ++tb)
-            src[tb] = p.X + (2 * static_cast<size_t>(l) + 1) * xs + static_cast<size_t>(rowb[tb]) * H;
-          block_rstd<TB>(p, S, G, src, nt, H, S.rstd);
-          load_slice<TB>(G, src, nt, S.rstd, p.layers[l].ffn_norm, y);
-          ykey = -1;
-        }
-        gemv_chunk<TB>(S, G, slot(), 2 * nf, y);
-        const int t = threadIdx.x;
-        if (t < nf * TB) {
-          const int f = t / TB, tb = t % TB;
-          if (tb < nt && rowj[tb] >= 0) {
-            const float gate = gemv_result<TB>(S, G, f, tb);
-            const float up = gemv_result<TB>(S, G, nf + f, tb);
-            const float h = (gate / (1.0f + expf(-gate))) * up;
-            p.HB[((static_cast<size_t>(l) * p.max_batch + rowb[tb]) * K + rowj[tb]) * F + m.row0 + f] = h;
-          }
-        }
-      }
-      if (m.last) break;
-      if (!next()) return false;
-    }
-    consumer_signal(p, base + p.cm.gu_off + a);
-    return true;
-  }
-
-  // ------------------------------------------------------------------ MoE down item
-  __device__ bool down_item() {
-    const Meta m0 = meta();
-    const int l = m0.layer, e = static_cast<int>(m0.e), a = static_cast<int>(m0.idx);
-    const uint32_t base = p.cm.layer_base(l);
-    if (!consumer_wait(p, base + p.cm.gu_off + a, static_cast<uint32_t>(p.n_ftiles), MK_OP_MOE, l)) return false;
-    const int B = p.B, H = p.H, F = p.F, K = p.K;
-    Geom G(F);
-    slots_for_expert(l, e);
-    const int cnt = B <= TB ? B : __ldcg(p.CNT + static_cast<size_t>(l) * p.E + e);
-    const int32_t* tok = p.TOK + (static_cast<size_t>(l) * p.E + e) * p.max_batch;
-    bool loaded = false;
-    for (;;) {
-      const Meta m = meta();
-      for (int b0 = 0; b0 < cnt; b0 += TB) {
-        const int nt = min(TB, cnt - b0);
-        int rowb[TB], rowj[TB];
-        for (int tb = 0; tb < TB; ++tb) {
-          if (B <= TB) { rowb[tb] = b0 + tb; rowj[tb] = tb < nt ? S.slot_of[b0 + tb] : -1; }
-          else {
-            const int ent = tb < nt ? __ldcg(tok + b0 + tb) : 0;
-            rowb[tb] = ent >> 8; rowj[tb] = tb < nt ? (ent & 0xff) : -1;
-          }
-        }
-        if (B > TB || !loaded) {
-          const float* src[TB];
-          for (int tb = 0; tb < TB; ++tb) {
-            const int j = rowj[tb] >= 0 ? rowj[tb] : 0;
-            src[tb] = p.HB + ((static_cast<size_t>(l) * p.max_batch + rowb[tb]) * K + j) * F;
-          }
-          int ntl = nt;
-          load_slice<TB>(G, src, ntl, nullptr, nullptr, y);
-          // rows of other experts contribute nothing
 #pragma unroll
-          for (int tb = 0; tb < TB; ++tb)
-            if (rowj[tb] < 0)
-#pragma unroll
-              for (int i = 0; i < 2; ++i)
-#pragma unroll
-                for (int j = 0; j < 8; ++j) y[i][j][tb] = 0.f;
-          loaded = true;
-          ykey = -1;
-        }
-        gemv_chunk<TB>(S, G, slot(), m.n, y);
-        const int t = threadIdx.x;
-        if (t < m.n * TB) {
-          const int r = t / TB, tb = t % TB;
-          if (tb < nt && rowj[tb] >= 0) {
-            const float v = gemv_result<TB>(S, G, r, tb);
-            p.PART[((static_cast<size_t>(l) * p.max_batch + rowb[tb]) * K + rowj[tb]) * H + m.row0 + r] = v;
-          }
-        }
+    for (int tb = 0; tb < TB; ++tb) {
+      if (p.B <= TB) {
+        rb[tb] = tb;
+        rj[tb] = tb < nt ? S.slot_of[tb] : -1;
+      } else {
+        const int ent = tb < nt ? __ldcg(tok + b0 + tb) : 0;
+        rb[tb] = ent >> 8;
+        rj[tb] = tb < nt ? (ent & 0xff) : -1;
       }
-      if (m.last) break;
-      if (!next()) return false;
     }
-    // the last item of this row tile adds every slot into the residual, in rank order
-    const uint32_t rt = m0.aux;
-    const uint32_t nact = static_cast<uint32_t>(__ldcg(p.NACT + l));
-    if (consumer_arrive_last(p, S, base + p.cm.down_off + rt, nact)) {
-      const size_t xs = static_cast<size_t>(p.max_batch) * H;
-      const int r0 = static_cast<int>(rt) * kRTile, r1 = min(H, r0 + kRTile);
-      const int nr = r1 - r0;
-      for (int idx = threadIdx.x; idx < B * nr; idx += kConsumerThreads) {
-        const int b = idx / nr, r = r0 + idx % nr;
-        const size_t lb = static_cast<size_t>(l) * p.max_batch + b;
-        float acc = 0.f;
-        for (int j = 0; j < K; ++j) acc += __ldcg(p.RW + lb * K + j) * __ldcg(p.PART + (lb * K + j) * H + r);
-        const size_t off = static_cast<size_t>(b) * H + r;
-        p.X[(2 * static_cast<size_t>(l) + 2) * xs + off] = __ldcg(p.X + (2 * static_cast<size_t>(l) + 1) * xs + off) + acc;
-      }
-      consumer_signal(p, base + L_MOE);
-    }
-    return true;
   }
 
   // ------------------------------------------------------------------ attention split item
+  // Warps split the query heads of the KV head into groups of 4 (one group when
+  // G <= 4, two when G = 8) and the chunk's positions among the warps of a group.
+  // A lane owns D/32 consecutive dims: scores are reduced with a reduce-scatter
+  // over the 4 heads (a lane ends holding one head's score), the online softmax
+  // runs per head on the lanes that hold it, and the probabilities are broadcast
+  // back for P*V.  At the end the group's warps merge their (max, sum, output)
+  // states in shared memory; the split's partial goes to global memory and the
+  // last split of (row, KV head) merges all splits in split order.
   __device__ bool attn_item() {
     constexpr int DL = D / 32;   // dims per lane
+    constexpr int HPW = 4;       // heads per warp
     const Meta m0 = meta();
     const int l = m0.layer;
     if (!consumer_wait(p, m0.wait_ctr, m0.wait_target, MK_OP_ATTN, l)) return false;
+    twait = globaltimer();
     const mk_attn_item item = p.items[m0.idx];
     const int b = item.b, kvh = item.kvh, Gq = p.G;
+    const int ngrp = (Gq + HPW - 1) / HPW;           // 1 or 2
+    const int wpg = kConsumerWarps / ngrp;           // warps per head group
     const int Lc = p.seq_lens[b];
     const int pos = Lc - 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gi = warp / wpg, widx = warp - gi * wpg;
+    const int h0 = gi * HPW;
     const float* qkv = p.QKV + (static_cast<size_t>(l) * p.max_batch + b) * p.nqkv;
     const float* cs = p.rope_cos + static_cast<size_t>(b) * (D / 2);
     const float* sn = p.rope_sin + static_cast<size_t>(b) * (D / 2);
-    // q (rotated, scaled) for the group's heads; k and v of this token, bf16-rounded
-    float q[kMaxG][DL], kc[DL], vc[DL];
     const int d0 = lane * DL;
-    float cv[DL], sv[DL];
-#pragma unroll
-    for (int d = 0; d < DL; ++d) {
-      const int i = (d0 + d) % (D / 2);
-      cv[d] = __ldg(cs + i);
-      sv[d] = __ldg(sn + i);
-    }
     const bool lowhalf = lane < 16;
-#pragma unroll
-    for (int h = 0; h < kMaxG; ++h) {
+    float q[HPW][DL], kc[DL], vc[DL];
+    {
+      float cv[DL], sv[DL];
 #pragma unroll
       for (int d = 0; d < DL; ++d) {
-        const float raw = h < Gq ? __ldcg(qkv + (kvh * Gq + h) * D + d0 + d) : 0.f;
-        const float other = __shfl_xor_sync(0xffffffffu, raw, 16);
-        const float rot = lowhalf ? raw * cv[d] - other * sv[d] : raw * cv[d] + other * sv[d];
-        q[h][d] = rot * p.scale;
+        const int i = (d0 + d) % (D / 2);
+        cv[d] = __ldg(cs + i);
+        sv[d] = __ldg(sn + i);
       }
-    }
 #pragma unroll
-    for (int d = 0; d < DL; ++d) {
-      const float raw = __ldcg(qkv + (p.Hq + kvh) * D + d0 + d);
-      const float other = __shfl_xor_sync(0xffffffffu, raw, 16);
-      kc[d] = round_bf16(lowhalf ? raw * cv[d] - other * sv[d] : raw * cv[d] + other * sv[d]);
-      vc[d] = round_bf16(__ldcg(qkv + (p.Hq + p.Hkv + kvh) * D + d0 + d));
+      for (int hh = 0; hh < HPW; ++hh) {
+        const int h = h0 + hh;
+#pragma unroll
+        for (int d = 0; d < DL; ++d) {
+          const float raw = h < Gq ? __ldcg(qkv + (kvh * Gq + h) * D + d0 + d) : 0.f;
+          const float other = __shfl_xor_sync(0xffffffffu, raw, 16);
+          const float rot = lowhalf ? raw * cv[d] - other * sv[d] : raw * cv[d] + other * sv[d];
+          q[hh][d] = rot * p.scale;
+        }
+      }
+#pragma unroll
+      for (int d = 0; d < DL; ++d) {
+        const float raw = __ldcg(qkv + (p.Hq + kvh) * D + d0 + d);
+        const float other = __shfl_xor_sync(0xffffffffu, raw, 16);
+        kc[d] = round_bf16(lowhalf ? raw * cv[d] - other * sv[d] : raw * cv[d] + other * sv[d]);
+        vc[d] = round_bf16(__ldcg(qkv + (p.Hq + p.Hkv + kvh) * D + d0 + d));
+      }
     }
     if (item.split == 0 && warp == 0) {
       // append this token's k and v to the cache
@@ -1060,12 +1204,12 @@ struct Consumer {
                      false);
       }
     }
-    float mrun = -INFINITY, lrun = 0.f;   // for head hl
-    float o[kMaxG][DL];
+    float mrun = -INFINITY, lrun = 0.f;   // for head h0 + ((lane >> 3) & 3)
+    float o[HPW][DL];
 #pragma unroll
-    for (int h = 0; h < kMaxG; ++h)
+    for (int hh = 0; hh < HPW; ++hh)
 #pragma unroll
-      for (int d = 0; d < DL; ++d) o[h][d] = 0.f;
+      for (int d = 0; d < DL; ++d) o[hh][d] = 0.f;
 
     for (;;) {
       const Meta m = meta();
@@ -1073,12 +1217,12 @@ struct Consumer {
       const int npos = min(static_cast<int>(m.n) * p.ps, Lc - p0);
       const uint16_t* Ks = reinterpret_cast<const uint16_t*>(slot());
       const uint16_t* Vs = reinterpret_cast<const uint16_t*>(slot() + kSlotBytes / 2);
-      const int nmine = npos > warp ? (npos - warp + kConsumerWarps - 1) / kConsumerWarps : 0;
+      const int nmine = npos > widx ? (npos - widx + wpg - 1) / wpg : 0;
       for (int i0 = 0; i0 < nmine; i0 += 8) {
         float sc[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const int pl = warp + kConsumerWarps * (i0 + i);
+          const int pl = widx + wpg * (i0 + i);
           const bool valid = (i0 + i) < nmine;
           float kf[DL];
           if (valid && p0 + pl == pos) {
@@ -1090,40 +1234,34 @@ struct Consumer {
 #pragma unroll
             for (int d = 0; d < DL; ++d) kf[d] = 0.f;
           }
-          float v[kMaxG];
+          float v[HPW];
 #pragma unroll
-          for (int h = 0; h < kMaxG; ++h) {
-            float s = 0.f;
+          for (int hh = 0; hh < HPW; ++hh) {
+            float acc = 0.f;
 #pragma unroll
-            for (int d = 0; d < DL; ++d) s = fmaf(q[h][d], kf[d], s);
-            v[h] = s;
+            for (int d = 0; d < DL; ++d) acc = fmaf(q[hh][d], kf[d], acc);
+            v[hh] = acc;
           }
-          // reduce-scatter over the 8 head values: lane ends with head (lane>>2)&7
+          // reduce-scatter over the 4 head values: lane ends with head (lane >> 3) & 3
           {
             const bool b4 = lane & 16;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const float send = b4 ? v[k] : v[k + 4];
-              const float keep = b4 ? v[k + 4] : v[k];
+            for (int k = 0; k < 2; ++k) {
+              const float send = b4 ? v[k] : v[k + 2];
+              const float keep = b4 ? v[k + 2] : v[k];
               v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
             }
             const bool b3 = lane & 8;
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-              const float send = b3 ? v[k] : v[k + 2];
-              const float keep = b3 ? v[k + 2] : v[k];
-              v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-            }
-            const bool b2 = lane & 4;
-            const float send = b2 ? v[0] : v[1];
-            const float keep = b2 ? v[1] : v[0];
-            v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+            const float send = b3 ? v[0] : v[1];
+            const float keep = b3 ? v[1] : v[0];
+            v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], 4);
             v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
             v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
           }
           sc[i] = valid ? v[0] : -INFINITY;
         }
-        // online softmax for head hl over these (up to 8) positions
+        // online softmax for this lane's head over these (up to 8) positions
         float mx = mrun;
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx = fmaxf(mx, sc[i]);
@@ -1137,17 +1275,16 @@ struct Consumer {
         }
         lrun = lrun * corr + ls;
         mrun = mx;
-        // o[h] = o[h]*corr_h + sum_i p_h[i] v_i
 #pragma unroll
-        for (int h = 0; h < kMaxG; ++h) {
-          const float ch = __shfl_sync(0xffffffffu, corr, h * 4);
+        for (int hh = 0; hh < HPW; ++hh) {
+          const float ch = __shfl_sync(0xffffffffu, corr, hh * 8);
 #pragma unroll
-          for (int d = 0; d < DL; ++d) o[h][d] *= ch;
+          for (int d = 0; d < DL; ++d) o[hh][d] *= ch;
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           if ((i0 + i) >= nmine) break;
-          const int pl = warp + kConsumerWarps * (i0 + i);
+          const int pl = widx + wpg * (i0 + i);
           float vf[DL];
           if (p0 + pl == pos) {
 #pragma unroll
@@ -1156,68 +1293,68 @@ struct Consumer {
             unpack_row<DL>(Vs + static_cast<size_t>(pl) * D + d0, vf);
           }
 #pragma unroll
-          for (int h = 0; h < kMaxG; ++h) {
-            const float ph = __shfl_sync(0xffffffffu, pr[i], h * 4);
+          for (int hh = 0; hh < HPW; ++hh) {
+            const float ph = __shfl_sync(0xffffffffu, pr[i], hh * 8);
 #pragma unroll
-            for (int d = 0; d < DL; ++d) o[h][d] = fmaf(ph, vf[d], o[h][d]);
+            for (int d = 0; d < DL; ++d) o[hh][d] = fmaf(ph, vf[d], o[hh][d]);
           }
         }
       }
       if (m.last) break;
-      if (!next()) return false;
+      if (!next_rec()) break;
     }
+    if (!cbar_and(wok)) return false;
 
-    // gather each head's (m, l) on every lane, then merge the 8 warps' states
-    float mh[kMaxG], lh[kMaxG];
+    // merge the group's warps: gather (m, l) per head on every lane, then a tree in shared memory
+    float mh[HPW], lh[HPW];
 #pragma unroll
-    for (int h = 0; h < kMaxG; ++h) {
-      mh[h] = __shfl_sync(0xffffffffu, mrun, h * 4);
-      lh[h] = __shfl_sync(0xffffffffu, lrun, h * 4);
+    for (int hh = 0; hh < HPW; ++hh) {
+      mh[hh] = __shfl_sync(0xffffffffu, mrun, hh * 8);
+      lh[hh] = __shfl_sync(0xffffffffu, lrun, hh * 8);
     }
-    constexpr int kStride = kMaxG * (128 + 2);
-    for (int half = kConsumerWarps / 2; half >= 1; half >>= 1) {
+    constexpr int kStride = HPW * 128 + 2 * HPW;
+    for (int half = wpg / 2; half >= 1; half >>= 1) {
       cbar();
-      if (warp >= half && warp < 2 * half) {
-        float* dst = S.scr.attn + (warp - half) * kStride;
+      if (widx >= half && widx < 2 * half) {
+        float* dst = S.scr.attn + (gi * (kConsumerWarps / 2) + (widx - half)) * kStride;
 #pragma unroll
-        for (int h = 0; h < kMaxG; ++h) {
+        for (int hh = 0; hh < HPW; ++hh)
 #pragma unroll
-          for (int d = 0; d < DL; ++d) dst[h * D + d0 + d] = o[h][d];
-        }
-        if (lane < kMaxG) {
-          dst[kMaxG * D + 2 * lane] = mh[lane];
-          dst[kMaxG * D + 2 * lane + 1] = lh[lane];
+          for (int d = 0; d < DL; ++d) dst[hh * D + d0 + d] = o[hh][d];
+        if (lane < HPW) {
+          dst[HPW * D + 2 * lane] = mh[lane];
+          dst[HPW * D + 2 * lane + 1] = lh[lane];
         }
       }
       cbar();
-      if (warp < half) {
-        const float* src = S.scr.attn + warp * kStride;
+      if (widx < half) {
+        const float* src = S.scr.attn + (gi * (kConsumerWarps / 2) + widx) * kStride;
 #pragma unroll
-        for (int h = 0; h < kMaxG; ++h) {
-          const float mo = src[kMaxG * D + 2 * h], lo = src[kMaxG * D + 2 * h + 1];
-          const float M = fmaxf(mh[h], mo);
-          const float fa = mh[h] == -INFINITY ? 0.f : __expf(mh[h] - M);
+        for (int hh = 0; hh < HPW; ++hh) {
+          const float mo = src[HPW * D + 2 * hh], lo = src[HPW * D + 2 * hh + 1];
+          const float M = fmaxf(mh[hh], mo);
+          const float fa = mh[hh] == -INFINITY ? 0.f : __expf(mh[hh] - M);
           const float fb = mo == -INFINITY ? 0.f : __expf(mo - M);
 #pragma unroll
-          for (int d = 0; d < DL; ++d) o[h][d] = o[h][d] * fa + src[h * D + d0 + d] * fb;
-          lh[h] = lh[h] * fa + lo * fb;
-          mh[h] = M;
+          for (int d = 0; d < DL; ++d) o[hh][d] = o[hh][d] * fa + src[hh * D + d0 + d] * fb;
+          lh[hh] = lh[hh] * fa + lo * fb;
+          mh[hh] = M;
         }
       }
     }
-    if (warp == 0) {
+    if (widx == 0) {
       float* po = p.PO + static_cast<size_t>(m0.idx) * Gq * D;
       float* pml = p.PML + static_cast<size_t>(m0.idx) * Gq * 2;
 #pragma unroll
-      for (int h = 0; h < kMaxG; ++h) {
-        if (h < Gq) {
+      for (int hh = 0; hh < HPW; ++hh) {
+        if (h0 + hh < Gq) {
 #pragma unroll
-          for (int d = 0; d < DL; ++d) po[h * D + d0 + d] = o[h][d];
+          for (int d = 0; d < DL; ++d) po[(h0 + hh) * D + d0 + d] = o[hh][d];
         }
       }
-      if (lane < Gq) {
-        pml[2 * lane] = mh[lane];
-        pml[2 * lane + 1] = lh[lane];
+      if (lane < HPW && h0 + lane < Gq) {
+        pml[2 * (h0 + lane)] = pick<HPW>(mh, lane);
+        pml[2 * (h0 + lane) + 1] = pick<HPW>(lh, lane);
       }
     }
     // the last split of (b, kvh) merges every split in split order
@@ -1231,6 +1368,7 @@ struct Consumer {
         float mloc = -INFINITY;
         for (int s = lane; s < ns; s += 32) mloc = fmaxf(mloc, __ldcg(p.PML + (static_cast<size_t>(first + s) * Gq + h) * 2));
         const float M = warp_max(mloc);
+        // each lane's splits: weight exp(m_s - M); the output is the weighted sum / sum of weighted l
         float lloc = 0.f;
         for (int s = lane; s < ns; s += 32) {
           const float ms = __ldcg(p.PML + (static_cast<size_t>(first + s) * Gq + h) * 2);
@@ -1241,12 +1379,22 @@ struct Consumer {
         float acc[DL];
 #pragma unroll
         for (int d = 0; d < DL; ++d) acc[d] = 0.f;
-        for (int s = 0; s < ns; ++s) {
-          const float ms = __ldcg(p.PML + (static_cast<size_t>(first + s) * Gq + h) * 2);
-          const float f = ms == -INFINITY ? 0.f : __expf(ms - M);
-          const float* src = p.PO + (static_cast<size_t>(first + s) * Gq + h) * D + d0;
+        for (int s0 = 0; s0 < ns; s0 += 8) {
+          float ms[8], ov[8][DL];
 #pragma unroll
-          for (int d = 0; d < DL; ++d) acc[d] = fmaf(f, __ldcg(src + d), acc[d]);
+          for (int j = 0; j < 8; ++j) {
+            const int s = s0 + j;
+            ms[j] = s < ns ? __ldcg(p.PML + (static_cast<size_t>(first + s) * Gq + h) * 2) : -INFINITY;
+#pragma unroll
+            for (int d = 0; d < DL; ++d)
+              ov[j][d] = s < ns ? __ldcg(p.PO + (static_cast<size_t>(first + s) * Gq + h) * D + d0 + d) : 0.f;
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float f = ms[j] == -INFINITY ? 0.f : __expf(ms[j] - M);
+#pragma unroll
+            for (int d = 0; d < DL; ++d) acc[d] = fmaf(f, ov[j][d], acc[d]);
+          }
         }
         float* dst = p.ATT + (static_cast<size_t>(l) * p.max_batch + b) * (p.Hq * D) + (kvh * Gq + h) * D + d0;
 #pragma unroll
@@ -1260,22 +1408,34 @@ struct Consumer {
   // ------------------------------------------------------------------ main loop
   __device__ void run() {
     for (;;) {
-      if (!wait_record(p, S, c)) break;
-      const uint8_t kind = meta().kind;
-      bool ok = true;
-      switch (kind) {
+      bool ok = warp_wait_record(p, S, c);
+      trace_chunk_seen();
+      if (!cbar_and(ok)) break;   // every warp starts a tile together
+      const Meta m0 = meta();
+      const uint64_t t0 = p.trace ? globaltimer() : 0;
+      twait = 0;
+      wok = true;
+      switch (m0.kind) {
         case R_EMBED: ok = embed(); break;
-        case R_GEMV: ok = gemv_tile(); break;
+        case R_GEMV: ok = stream_gemv(m0.op); break;
         case R_ATTN: ok = attn_item(); break;
-        case R_GU: ok = gate_up_item(); break;
-        case R_DOWN: ok = down_item(); break;
+        case R_GU: ok = stream_gemv(R_OP_GU); break;
+        case R_DOWN: ok = stream_gemv(R_OP_DOWN); break;
         default: break;
       }
-      release_record(S, c);
+      if (!ok) break;
+      if (m0.kind != R_END) trace_event(m0.kind == R_ATTN || m0.kind == R_GU || m0.kind == R_DOWN ? TR_ITEM : TR_TILE,
+                                        m0, t0);
+      trace_chunk_done();
+      warp_release_record(S, c);
       ++c;
-      if (kind == R_END || !ok) break;
+      if (m0.kind == R_END) break;
     }
-    if (threadIdx.x == 0) S.cons_count = c;
+    if ((threadIdx.x & 31) == 0) atomicMin(&S.cons_count, c);
+    if (threadIdx.x == 0 && p.trace) {
+      uint64_t* h = p.trace + static_cast<size_t>(blockIdx.x) * p.trace_cap * 4;
+      h[0] = nev;
+    }
   }
 };
 
@@ -1291,7 +1451,8 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
       mbar_init(&S.empty[s], kConsumerWarps);
     }
     S.prod_count = 0;
-    S.cons_count = 0;
+    S.cons_count = 0xffffffffu;
+    if (p.trace) p.trace[static_cast<size_t>(blockIdx.x) * p.trace_cap * 4 + 1] = globaltimer();
     fence_mbar_init();
   }
   __syncthreads();

@@ -23,8 +23,8 @@ constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;
 
 // ---- shared-memory ring of weight / KV tiles --------------------------------
-constexpr int kSlots = 6;
-constexpr int kSlotBytes = 32768;
+constexpr int kSlots = 3;
+constexpr int kSlotBytes = 65536;
 
 // ---- build limits --------------------------------------------------------------
 constexpr int kMaxBatch = 64;
@@ -32,7 +32,7 @@ constexpr int kMaxTopK = 8;
 constexpr int kMaxG = 8;          // query heads per KV head
 constexpr int kMaxExperts = 256;
 constexpr int kMaxK = 4096;       // GEMV input length (two 16-byte units per thread)
-constexpr int kMaxRowsPerChunk = 16;
+constexpr int kMaxRowsPerChunk = 32;
 
 // ---- MoE work-queue tiles --------------------------------------------------------
 constexpr int kFTile = 16;        // expert FFN rows (gate+up pairs) per gate/up item
@@ -134,8 +134,17 @@ struct Params {
   int32_t* CNT;    // [L][E]
   float* HB;       // [L][max_batch][K][F] SwiGLU activations per (row, slot)
   float* PART;     // [L][max_batch][K][H] down-projection output per (row, slot)
+  float* SS;       // [2L+1][n_ss_slots][max_batch] per-tile sums of squares of the residual stream
+  int32_t n_ss_slots;
   uint32_t* ctr;   // [cm.total]
   mk_status* status;
+  // optional timeline: per block `trace_cap` events of 4 x u64 (start, dependency met, end, tag);
+  // event 0 of each block holds (consumer events, kernel start, producer events, 0)
+  uint64_t* trace;
+  int32_t trace_cap;
 };
+
+// trace tags: op | layer << 8 | kind << 24 | (uint64)idx << 32
+enum : uint32_t { TR_TILE = 1, TR_ITEM = 2, TR_PRODUCER_ROUTE_WAIT = 3, TR_CHUNK = 4 };
 
 }  // namespace mk

@@ -60,13 +60,16 @@ def _parity_one_step(setup, max_batch=8, check_layers=True):
                 assert np.allclose(eng.debug_read("route_w", l), tr["w"], rtol=1e-5, atol=1e-7)
                 assert rel_l2(eng.debug_read("h", l), tr["h"]) < 1e-4
                 assert rel_l2(x_all[2 * l + 2], tr["x_out"]) < 1e-5
-    # the appended KV: both sides wrote position seq_len-1 of every row; codes agree to 1 bf16 ulp
+    # the appended KV: both sides wrote position seq_len-1 of every row.  The bf16 values agree to one
+    # bf16 ulp of their own magnitude plus fp32 summation noise at the vector's scale (a value that
+    # cancels to near zero keeps only the latter).
     kv_got = W.bf16_bits(kv_dev)
-    diff = np.nonzero(kv_got != setup["kv"])
-    ref_codes = kv_ref[diff].astype(np.int32)
-    assert np.all(np.abs(kv_got[diff].astype(np.int32) - ref_codes) <= 1)
-    changed_ref = np.count_nonzero(kv_ref != setup["kv"])
-    assert changed_ref > 0 and abs(len(diff[0]) - changed_ref) <= max(2, changed_ref // 50)
+    changed = (kv_got != setup["kv"]) | (kv_ref != setup["kv"])
+    g = (kv_got[changed].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    r = (kv_ref[changed].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    assert changed.any()
+    rms = np.sqrt(np.mean(r * r))
+    assert np.all(np.abs(g - r) <= 2.0 ** -7 * np.maximum(np.abs(r), np.abs(g)) + 1e-4 * rms)
     eng.close()
     return got, ref
 
@@ -148,6 +151,10 @@ def test_tiny_bs8_ragged_continuous_batching():
             kv_dev[:, pages.cuda()] = kv_to_device(kv_ref)[:, pages.cuda()]
             seq[0] = newlen
             tokens[0] = prefix[-1]
+        for b in range(len(seq)):   # a row that crosses a page boundary gets the next free page
+            need = (int(seq[b]) + ps - 1) // ps
+            if bt[b, need - 1] < 0:
+                bt[b, need - 1] = free.pop(0)
         got = gpu_step(eng, tokens, seq, bt, kv_dev)
         ref = orc.decode_step(s["dims"], s["wn"], tokens, seq, bt, kv_ref)
         assert rel_l2(got, ref) <= TOL_LOGITS, (step, rel_l2(got, ref))
@@ -172,7 +179,8 @@ def test_watchdog_times_out_and_context_recovers():
     bt = torch.from_numpy(s["bt"]).cuda()
     eng.step(tok, s["seq_lens"], bt, kv_dev)
     st = eng.status()
-    assert st["code"] == mk.MK_ERR_TIMEOUT and st["layer"] == 1 and st["op"] == "oproj"
+    # the first wait to run out is the stalled O-proj or one that depends on it (router, MoE queue)
+    assert st["code"] == mk.MK_ERR_TIMEOUT and st["layer"] == 1 and st["op"] in ("oproj", "router", "moe"), st
     again = gpu_step(eng, s["tokens"], s["seq_lens"], s["bt"], kv_dev)   # next step runs clean
     assert np.array_equal(again.view(np.uint32), ok.view(np.uint32))
     eng.close()
