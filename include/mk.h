@@ -160,6 +160,38 @@ const char* mk_last_error(void);
 /* Free everything the library allocated.  NULL is ignored.  Does not touch caller memory. */
 void mk_destroy(mk_ctx* ctx);
 
+/*
+ * Paged GQA decode attention with no device allocation (the paper has no
+ * counterpart; it serves callers that cannot call cudaMalloc -- code running
+ * under another framework's allocator or memory-pool hooks, or a plug-in that
+ * is only handed pre-allocated buffers -- and therefore cannot create a
+ * context).  It computes, for every row b and query head h, the softmax
+ * attention of q[b][h] (already rotated; it is scaled by 1/sqrt(head_dim)
+ * here) over positions 0..seq_len[b]-1 of the row's pages, exactly the
+ * attention of one layer of mk_decode_step, and writes out[b][h*head_dim + d].
+ *   q:            device fp32 [batch][num_q_heads][head_dim]
+ *   seq_lens:     HOST int32 [batch], 1..max_pages_per_seq*page_size
+ *   block_tables: device int32 [batch][max_pages_per_seq]
+ *   kv_layer:     device bf16 pages of ONE layer: [num_pages][2 (K,V)][num_kv_heads][page_size][head_dim]
+ *   out:          device fp32 [batch][num_q_heads*head_dim]
+ *   status_out:   device int32 [1] or NULL; receives MK_OK, or MK_ERR_DEVICE_BOUNDS if a
+ *                 block-table entry was outside 0..num_pages-1 (such pages are skipped)
+ * Limits: batch <= 64, head_dim 64 or 128, at most 8 query heads per KV head.
+ * Its only scratch is one fixed 4 MiB __device__ array inside the library,
+ * which every GPU that loads the library keeps until the process exits:
+ * batch * num_kv_heads * (num_q_heads/num_kv_heads) * (head_dim+2) * 4 bytes
+ * must fit in it (about 4 MiB), otherwise the call returns MK_ERR_UNSUPPORTED.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Asynchronous on `stream`; allocates nothing.  Every call uses the
+ * same array, so calls whose work overlaps on the GPU (other streams, other
+ * threads) race and must be serialised by the caller.
+ */
+int mk_paged_attention_noalloc(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                               int32_t page_size, int32_t num_pages, int32_t max_pages_per_seq, const float* q,
+                               const int32_t* seq_lens, const int32_t* block_tables, const void* kv_layer,
+                               float* out, int32_t* status_out, mk_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -131,7 +131,7 @@ class SimResult(ctypes.Structure):
 
 EXPORTS = ("mk_create", "mk_decode_step", "mk_get_status", "mk_last_error", "mk_destroy", "mk_plan_static",
            "mk_plan_attention", "mk_simulate", "mk_debug_read", "mk_debug_inject_stall", "mk_num_ctas",
-           "mk_debug_trace", "mk_debug_trace_read")
+           "mk_debug_trace", "mk_debug_trace_read", "mk_paged_attention_noalloc")
 
 _lib = None
 _lock = threading.Lock()

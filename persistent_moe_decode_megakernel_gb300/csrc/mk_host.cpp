@@ -56,6 +56,15 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+}  // namespace
+
+namespace mk {
+// lets other translation units of the library set the text mk_last_error() returns
+void set_last_error(int, const char* text) { g_err = text; }
+}  // namespace mk
+
+namespace {
+
 // ---------------------------------------------------------------- config checks
 int check_config(const mk_config* c) {
   if (!c) return fail(MK_ERR_INVALID_ARG, "config is NULL");
