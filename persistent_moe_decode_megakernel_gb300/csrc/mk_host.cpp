@@ -12,15 +12,19 @@
 // step from the host-side lengths; the MoE tiles are queued on the device by
 // the router.
 
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <queue>
 #include <random>
 #include <string>
+#include <queue>
 #include <vector>
 
 #include "mk.h"
@@ -89,6 +93,9 @@ int check_config(const mk_config* c) {
   if (c->num_experts > mk::kMaxExperts) return fail(MK_ERR_UNSUPPORTED, "num_experts > 256");
   if (c->top_k > mk::kMaxTopK) return fail(MK_ERR_UNSUPPORTED, "top_k > 8");
   if (c->page_size * c->head_dim * 2 > mk::kSlotBytes / 2) return fail(MK_ERR_UNSUPPORTED, "page_size*head_dim*2 > 32768");
+  if (c->page_size % 8) return fail(MK_ERR_UNSUPPORTED, "page_size must be a multiple of 8");
+  if ((int64_t)c->num_layers * c->num_pages * 2 * c->num_kv_heads * c->page_size >= ((int64_t)1 << 31))
+    return fail(MK_ERR_UNSUPPORTED, "KV pool has 2^31 or more rows");
   if (c->max_batch > mk::kMaxBatch) return fail(MK_ERR_UNSUPPORTED, "max_batch > 64");
   if ((int64_t)c->max_pages_per_seq * c->page_size > (int64_t)1 << 30) return fail(MK_ERR_UNSUPPORTED, "sequence too long");
   return MK_OK;
@@ -132,7 +139,7 @@ void build_static_plan(const mk_config& c, int n_ctas, Plan& plan) {
   in.n_embed_tiles = count((uint32_t)H);
   in.n_qkv_tiles = count((uint32_t)nqkv);
   in.n_o_tiles = count((uint32_t)H);
-  in.n_router_tiles = count((uint32_t)E);
+  in.n_router_tiles = (E + mk::kRouterRows - 1) / mk::kRouterRows;
   in.n_head_tiles = count((uint32_t)V);
   const CounterMap& cm = plan.cm;
   plan.tasks.clear();
@@ -158,8 +165,9 @@ void build_static_plan(const mk_config& c, int n_ctas, Plan& plan) {
       push(MK_OP_ATTN, l, 0, 0, base + mk::L_QKV, (uint32_t)in.n_qkv_tiles, 0, MK_NO_COUNTER);
       split_range((uint32_t)H, n_ctas, i, &lo, &hi);
       if (hi > lo) push(MK_OP_OPROJ, l, lo, hi, base + mk::L_ATTN, 0, (uint32_t)c.num_kv_heads, base + mk::L_O);
-      split_range((uint32_t)E, n_ctas, i, &lo, &hi);
-      if (hi > lo) push(MK_OP_ROUTER, l, lo, hi, base + mk::L_O, (uint32_t)in.n_o_tiles, 0, MK_NO_COUNTER);
+      for (int t = i; t < in.n_router_tiles; t += n_ctas)
+        push(MK_OP_ROUTER, l, (uint32_t)(t * mk::kRouterRows), (uint32_t)std::min(E, (t + 1) * mk::kRouterRows),
+             base + mk::L_O, (uint32_t)in.n_o_tiles, 0, MK_NO_COUNTER);
       push(MK_OP_MOE, l, 0, 0, base + mk::L_RREADY, 1, 0, MK_NO_COUNTER);
     }
     split_range((uint32_t)V, n_ctas, i, &lo, &hi);
@@ -180,10 +188,46 @@ int build_attention_plan(const mk_config& c, int n_ctas, int B, const int32_t* s
   const int Hkv = c.num_kv_heads, ps = c.page_size;
   int64_t total = 0;
   for (int b = 0; b < B; ++b) total += (int64_t)Hkv * ((seq_lens[b] + ps - 1) / ps);
-  const int64_t quota = std::max<int64_t>(1, (total + n_ctas - 1) / n_ctas);
   items.clear();
   std::vector<int32_t> cta_of;
   pair_first.assign((size_t)B * Hkv, 0);
+  const int npairs = B * Hkv;
+  if (npairs <= n_ctas) {
+    // one item per block: every (row, KV head) pair gets splits in proportion to its pages
+    // (at least one, at most one per page), handed out greedily to the pair whose splits are
+    // currently the longest; each pair's pages are then cut into near-equal contiguous ranges
+    std::vector<int32_t> ns((size_t)npairs, 1);
+    std::vector<int64_t> np((size_t)npairs);
+    for (int b = 0; b < B; ++b)
+      for (int kvh = 0; kvh < Hkv; ++kvh) np[(size_t)b * Hkv + kvh] = (seq_lens[b] + ps - 1) / ps;
+    using E = std::pair<double, int>;
+    std::priority_queue<E> pq;
+    for (int i = 0; i < npairs; ++i) pq.push(E((double)np[i], i));
+    for (int left = n_ctas - npairs; left > 0 && !pq.empty(); --left) {
+      const int i = pq.top().second;
+      pq.pop();
+      if (ns[i] >= np[i]) { ++left; continue; }
+      ++ns[i];
+      if (ns[i] < np[i]) pq.push(E((double)np[i] / ns[i], i));
+    }
+    int cta = 0;
+    for (int i = 0; i < npairs; ++i) {
+      pair_first[i] = (int32_t)items.size();
+      for (int k = 0; k < ns[i]; ++k) {
+        mk_attn_item it;
+        it.b = (uint16_t)(i / Hkv); it.kvh = (uint16_t)(i % Hkv); it.split = (uint16_t)k; it.nsplit = (uint16_t)ns[i];
+        it.page_lo = (uint32_t)(np[i] * k / ns[i]);
+        it.page_hi = (uint32_t)(np[i] * (k + 1) / ns[i]);
+        items.push_back(it);
+        cta_of.push_back(cta++);
+      }
+    }
+    off.assign(n_ctas + 1, 0);
+    for (size_t i = 0; i < items.size(); ++i) off[cta_of[i] + 1]++;
+    for (int i = 0; i < n_ctas; ++i) off[i + 1] += off[i];
+    return MK_OK;
+  }
+  const int64_t quota = std::max<int64_t>(1, (total + n_ctas - 1) / n_ctas);
   int cta = 0;
   int64_t room = quota;
   for (int b = 0; b < B; ++b) {
@@ -246,6 +290,9 @@ struct mk_ctx {
   bool stepped = false;
   int last_B = 0;
   std::vector<double> inv_freq;
+  // TMA descriptor of the caller's KV pool (re-encoded when the pool pointer changes)
+  alignas(64) CUtensorMap kv_map;
+  const void* kv_map_ptr = nullptr;
   // timeline
   uint64_t* trace = nullptr;
   int32_t trace_cap = 0;
@@ -257,6 +304,29 @@ struct mk_ctx {
 namespace {
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+// Describe the KV pool [L][P][2][Hkv][ps][D] to TMA as 2-D rows of D elements.
+int encode_kv_map(const mk_config& cf, void* kv, CUtensorMap* out) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+      return fail(MK_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const cuuint64_t rows = (cuuint64_t)cf.num_layers * cf.num_pages * 2 * cf.num_kv_heads * cf.page_size;
+  const cuuint64_t dims[2] = {(cuuint64_t)cf.head_dim, rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cf.head_dim * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)cf.page_size};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv, dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MK_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return MK_OK;
+}
 
 void free_ctx(mk_ctx* c) {
   if (!c) return;
@@ -317,6 +387,7 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_ctx** out) {
   if ((e = mk::occupancy(cfg->head_dim, &blocks)) != cudaSuccess) return cuda_fail(e, "occupancy");
   if (blocks < 1) return fail(MK_ERR_UNSUPPORTED, "the step kernel does not fit on an SM");
 
+  if (prop.multiProcessorCount > 256) return fail(MK_ERR_UNSUPPORTED, "more than 256 SMs");
   mk_ctx* c = new mk_ctx();
   c->cfg = *cfg;
   if (c->cfg.watchdog_ms == 0) c->cfg.watchdog_ms = 1000;
@@ -486,6 +557,13 @@ int mk_decode_step(mk_ctx* c, int32_t batch, const int32_t* token_ids, const int
   p.SS = c->SS; p.n_ss_slots = std::max(c->n_ctas, in.n_rtiles);
   p.ctr = c->ctr; p.status = c->d_status;
   p.trace = c->trace; p.trace_cap = c->trace_cap;
+  if (kv_pages != c->kv_map_ptr) {
+    int rc2 = encode_kv_map(cf, kv_pages, &c->kv_map);
+    if (rc2) return rc2;
+    c->kv_map_ptr = kv_pages;
+  }
+  static_assert(sizeof(CUtensorMap) == sizeof(p.kv_map), "tensor map size");
+  std::memcpy(p.kv_map, &c->kv_map, sizeof(p.kv_map));
 
   // test hook: one O-proj task waits on a counter nothing increments
   int stall_idx = -1;

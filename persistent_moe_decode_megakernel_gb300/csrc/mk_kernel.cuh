@@ -79,6 +79,48 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
       : "memory");
 }
+// 2-D tiled TMA load of box (x, y) of the tensor map into shared memory (completion on an mbarrier)
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y, uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3}], "
+      "[%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+// d += a(16x16 bf16, row) * b(16x8 bf16, col), fp32 accumulate
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+// two floats -> bf16x2 (first in the low half), and the bf16x2 of what rounding left over
+__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  const __nv_bfloat162 r = __floats2bfloat162_rn(a - __low2float(h), b - __high2float(h));
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&r);
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -189,7 +231,12 @@ struct __align__(128) Smem {
   float ssred[kConsumerWarps][4];
   int32_t slot_of[kMaxBatch];
   int32_t rids[kMaxBatch * kMaxTopK];
+  float rval[kMaxBatch * kMaxTopK];
+  float rmax[kMaxBatch], rz[kMaxBatch], rsum[kMaxBatch];
   int32_t ecnt[kMaxExperts];
+  int32_t rcache[kMaxBatch * kMaxTopK];   // this layer's routing ids, cached by the first MoE item of the block
+  int32_t moe_layer;                      // layer whose routing rcache holds, or -1
+  int32_t ykey;                           // layer whose normalised MoE input scr.attn holds, or -1
   uint32_t prod_count, cons_count;
   int32_t flag;
   int32_t is_last;
@@ -387,10 +434,15 @@ struct Producer {
     return true;
   }
 
+  // KV pages of this block's attention items: per page, K then V, each as D/64 boxes of
+  // [page_size rows][64 dims] (128-byte swizzle).  Within a slot, K occupies the first half
+  // and V the second; each holds [dim half][rows][64 dims], page i at rows i*page_size.
   __device__ bool attn_items(const mk_task& t) {
     const int cta = blockIdx.x;
     const int ppc = pages_per_chunk(p.ps, p.D);
-    const uint32_t pb = static_cast<uint32_t>(p.ps * p.D * 2);
+    const int rows_cap = (kSlotBytes / 2) / (p.D * 2);
+    const int halves = p.D / 64;
+    const uint32_t box = static_cast<uint32_t>(p.ps) * 128u;
     for (int it = p.item_off[cta]; it < p.item_off[cta + 1]; ++it) {
       const mk_attn_item item = p.items[it];
       const int32_t* btrow = p.block_tables + static_cast<size_t>(item.b) * p.maxpg;
@@ -403,7 +455,7 @@ struct Producer {
         m.e = 0; m.aux = 0; m.wait_ctr = t.wait_ctr;
         m.wait_target = t.wait_base + t.wait_per_b * static_cast<uint32_t>(p.B);
         m.signal_ctr = t.signal_ctr; m.lo = item.page_lo; m.hi = item.page_hi;
-        mbar_arrive_expect_tx(full(), 2u * n * pb);
+        mbar_arrive_expect_tx(full(), 2u * halves * n * box);
         uint8_t* dst = slot();
         for (uint32_t i = 0; i < n; ++i) {
           int32_t page = btrow[pg + i];
@@ -412,11 +464,13 @@ struct Producer {
                          static_cast<int>(pg + i), false);
             page = 0;  // keep the byte count of the slot; the result is flagged invalid
           }
-          const size_t kbase = ((static_cast<size_t>(t.layer) * p.P + page) * 2 * p.Hkv + item.kvh) *
-                               static_cast<size_t>(p.ps) * p.D;
-          const size_t vbase = kbase + static_cast<size_t>(p.Hkv) * p.ps * p.D;
-          bulk_g2s(dst + i * pb, p.kv + kbase, pb, full(), pol);
-          bulk_g2s(dst + kSlotBytes / 2 + i * pb, p.kv + vbase, pb, full(), pol);
+          const int rowk = (((t.layer * p.P + page) * 2) * p.Hkv + item.kvh) * p.ps;
+          const int rowv = rowk + p.Hkv * p.ps;
+          for (int h = 0; h < halves; ++h) {
+            uint8_t* kd = dst + h * rows_cap * 128 + i * box;
+            tma_load_2d(kd, p.kv_map, 64 * h, rowk, full(), pol);
+            tma_load_2d(kd + kSlotBytes / 2, p.kv_map, 64 * h, rowv, full(), pol);
+          }
         }
         ++c;
       }
@@ -591,15 +645,24 @@ __device__ __forceinline__ void row_dot(const uint8_t* row, const Seg<TB>& sg, c
   for (int tb = 0; tb < TB; ++tb) acc[tb] += part[tb][0] + part[tb][1];
 }
 
-// rsqrt(mean(x^2) + eps) of residual-stream vector `xidx`, row b, from the
-// per-tile sums of squares its producers published (fixed order: every warp
-// gets the same value)
-__device__ __forceinline__ float rstd_of(const Params& p, int xidx, int b) {
+// Sums of squares of residual-stream vector `xidx`, row b, as published per
+// tile by its producers: issue every load at once (slots <= 256), then reduce in
+// fixed order so every warp gets the same value.
+__device__ __forceinline__ void ss_issue(const Params& p, int xidx, int b, float (&v)[8]) {
   const float* ss = p.SS + static_cast<size_t>(xidx) * p.n_ss_slots * p.max_batch + b;
-  float v = 0.f;
-  for (int i = threadIdx.x & 31; i < p.n_ss_slots; i += 32) v += __ldcg(ss + static_cast<size_t>(i) * p.max_batch);
-  v = warp_sum(v);
-  return 1.0f / sqrtf(v / static_cast<float>(p.H) + p.eps);
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int i = lane + 32 * k;
+    v[k] = i < p.n_ss_slots ? __ldcg(ss + static_cast<size_t>(i) * p.max_batch) : 0.f;
+  }
+}
+__device__ __forceinline__ float ss_rstd(const Params& p, const float (&v)[8]) {
+  float t = 0.f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) t += v[k];
+  t = warp_sum(t);
+  return 1.0f / sqrtf(t / static_cast<float>(p.H) + p.eps);
 }
 
 // Load this warp's segment of nt input vectors into registers.  src[tb] points
@@ -701,6 +764,18 @@ struct Consumer {
     }
   }
 
+  // a timestamped point inside a tile (tracing only)
+  __device__ void trace_mark(uint32_t id, int layer) {
+    if (p.trace == nullptr || threadIdx.x != 0) return;
+    if (nev < static_cast<uint32_t>(p.trace_cap) / 2) {
+      const uint64_t t = globaltimer();
+      uint64_t* ev = p.trace + (static_cast<size_t>(blockIdx.x) * p.trace_cap + nev) * 4;
+      ev[0] = t; ev[1] = t; ev[2] = t;
+      ev[3] = static_cast<uint64_t>(id) | (static_cast<uint64_t>(layer) << 8) | (static_cast<uint64_t>(TR_MARK) << 24);
+      ++nev;
+    }
+  }
+
   __device__ const Meta& meta() const { return S.meta[c % kSlots]; }
   __device__ const uint8_t* slot() const { return S.ring[c % kSlots]; }
 
@@ -748,7 +823,6 @@ struct Consumer {
   __device__ __forceinline__ void load_input(const Seg<TB>& sg, int kind, int l, const int (&rb)[TB], int nt,
                                              float (&y)[8 / TB][8][TB]) {
     const float* src[TB];
-    float rs[TB];
     const uint16_t* g = nullptr;
     int xidx = 0;
     if (kind == 0) { g = p.layers[l].attn_norm; xidx = 2 * l; }
@@ -758,9 +832,33 @@ struct Consumer {
     for (int tb = 0; tb < TB; ++tb) {
       const int b = tb < nt ? rb[tb] : rb[0];
       src[tb] = kind == 1 ? p.ATT + (static_cast<size_t>(l) * p.max_batch + b) * (p.Hq * p.D) : xrow(xidx, b);
-      rs[tb] = (g != nullptr && tb < nt) ? rstd_of(p, xidx, b) : 1.f;
     }
-    load_y<TB>(sg, src, rs, g, nt, y);
+    float one[TB];
+#pragma unroll
+    for (int tb = 0; tb < TB; ++tb) one[tb] = 1.f;
+    load_y<TB>(sg, src, one, nullptr, nt, y);   // raw values; the loads below overlap with these
+    if (g == nullptr) return;
+    uint4 gw[Seg<TB>::kUnits];
+#pragma unroll
+    for (int j = 0; j < Seg<TB>::kUnits; ++j) {
+      const int e = sg.unit(j);
+      gw[j] = e >= 0 ? __ldg(reinterpret_cast<const uint4*>(g + e)) : make_uint4(0, 0, 0, 0);
+    }
+    float ssv[TB][8];
+#pragma unroll
+    for (int tb = 0; tb < TB; ++tb) ss_issue(p, xidx, tb < nt ? rb[tb] : rb[0], ssv[tb]);
+    float rs[TB];
+#pragma unroll
+    for (int tb = 0; tb < TB; ++tb) rs[tb] = ss_rstd(p, ssv[tb]);
+#pragma unroll
+    for (int j = 0; j < Seg<TB>::kUnits; ++j) {
+      float gv[8];
+      unpack8(gw[j], gv);
+#pragma unroll
+      for (int tb = 0; tb < TB; ++tb)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) y[j][q][tb] = (y[j][q][tb] * rs[tb]) * gv[q];
+    }
   }
 
   // ------------------------------------------------------------------ EMBED
@@ -825,14 +923,15 @@ struct Consumer {
     return o;
   }
 
-  // result v (v2: the matching up row for gate/up) of matrix row `row` for batch row b, slot j
+  // result v (v2: the matching up row for gate/up) of matrix row `row` for batch row b, slot j;
+  // rv: the residual input of that element when the caller already loaded it (O-proj), else NAN
   __device__ __forceinline__ void put(const OutMap& o, bool gu, uint32_t row, int b, int j, float v, float v2,
-                                      float& my_ss) {
+                                      float& my_ss, float rv = NAN) {
     if (j < 0) return;
     const size_t off = static_cast<size_t>(b) * o.sb + static_cast<size_t>(j) * o.sj + row;
     if (gu) v = (v / (1.0f + expf(-v))) * v2;
     if (o.resid != nullptr) {
-      v += __ldcg(o.resid + off);
+      v += isnan(rv) ? __ldcg(o.resid + off) : rv;
       my_ss += v * v;
     }
     if (o.bias != nullptr) v += __ldg(o.bias + row);
@@ -874,6 +973,7 @@ struct Consumer {
     // GEMV input: 0 x_in/attn_norm, 1 attention output, 2 x_mid/ffn_norm, 3 x_final/final_norm, 4 SwiGLU h
     const int kind = op == MK_OP_QKV ? 0 : op == MK_OP_OPROJ ? 1 : (op == MK_OP_ROUTER || gu) ? 2
                    : op == MK_OP_HEAD ? 3 : 4;
+    trace_mark(10 + (op == MK_OP_ROUTER ? 0 : moe ? 20 : 40), l);
     if (moe) slots_for_expert(l, e);
     const int cnt = (!moe || B <= TB) ? B : __ldcg(p.CNT + static_cast<size_t>(l) * p.E + e);
     const int ngroups = kGroups ? (cnt + TB - 1) / TB : 1;
@@ -881,7 +981,15 @@ struct Consumer {
     float my_ss = 0.f;    // O-proj: sum of squares of the residual values this lane wrote
     int rb[TB], rj[TB];
     float y[8 / TB][8][TB];
-    stream_load(sg, moe, kind, l, e, 0, min(cnt, TB), rb, rj, y);
+    const bool cached = gu && B <= TB && B * p.H <= kAttnScratch;
+    if (cached) {
+      ensure_ffn_input(l);
+      expert_rows(l, e, 0, B, rb, rj);
+      load_y_smem(sg, B, y);
+    } else {
+      stream_load(sg, moe, kind, l, e, 0, min(cnt, TB), rb, rj, y);
+    }
+    trace_mark(11 + (op == MK_OP_ROUTER ? 0 : moe ? 20 : 40), l);
     for (;;) {
       const int n = meta().n;
       const uint32_t row0 = meta().row0;
@@ -914,16 +1022,28 @@ struct Consumer {
           }
         }
         if (sg.S > 1) {
-          // the S warps of this row group meet; segment 0's warp finishes the rows
+          if (threadIdx.x == 0) S.ykey = -1;   // seg shares storage with the MoE input cache
+          // the S warps of this row group meet; segment 0's warp finishes the rows.  Its residual
+          // inputs (O-proj) are loaded before the barrier so that their latency overlaps the wait.
+          float rv[4] = {NAN, NAN, NAN, NAN};
+          if (om.resid != nullptr && sg.s == 0 && lane < nt) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int r = sg.rg + sg.RPG * i;
+              if (r < n) rv[i] = __ldcg(om.resid + static_cast<size_t>(pick_i<TB>(rb, lane)) * om.sb + row0 + r);
+            }
+          }
           ok = group_bar_and(true, sg.S);
           if (ok && sg.s == 0 && lane < nt) {
-            for (int r = sg.rg; r < n; r += sg.RPG) {
+            int i = 0;
+            for (int r = sg.rg; r < n; r += sg.RPG, ++i) {
               float v = 0.f, v2 = 0.f;
               for (int q = 0; q < sg.S; ++q) {
                 v += S.scr.seg[par][r][q][lane];
                 if (gu) v2 += S.scr.seg[par][kMaxRowsPerChunk / 2 + r][q][lane];
               }
-              put(om, gu, row0 + r, pick_i<TB>(rb, lane), pick_i<TB>(rj, lane), v, v2, my_ss);
+              put(om, gu, row0 + r, pick_i<TB>(rb, lane), pick_i<TB>(rj, lane), v, v2, my_ss,
+                  i == 0 ? rv[0] : i == 1 ? rv[1] : i == 2 ? rv[2] : i == 3 ? rv[3] : NAN);
             }
           }
           if (kGroups && ngroups > 1) ok = group_bar_and(ok, sg.S);   // seg is reused by the next group
@@ -944,7 +1064,12 @@ struct Consumer {
         break;
       }
       case MK_OP_ROUTER:
-        if (consumer_arrive_last(p, S, base + L_RARR, static_cast<uint32_t>(p.n_router_tiles))) route(l);
+        trace_mark(12, l);
+        if (consumer_arrive_last(p, S, base + L_RARR, static_cast<uint32_t>(p.n_router_tiles))) {
+          trace_mark(13, l);
+          route(l);
+          trace_mark(14, l);
+        }
         break;
       case R_OP_GU: consumer_signal(p, base + p.cm.gu_off + a); break;
       case R_OP_DOWN: {
@@ -1013,68 +1138,75 @@ struct Consumer {
   }
 
   // ------------------------------------------------------------------ routing (last router tile)
+  // Top-k by logit, ties to the lower expert index: an expert's rank is the number
+  // of experts with a larger logit plus those with an equal logit and a lower
+  // index; every (row, expert) pair counts its own rank against the row's logits
+  // staged in shared memory, so no serial selection rounds are needed.  Weights:
+  // exp(r - max) over the chosen experts, renormalised over them (or over all
+  // experts when norm_topk == 0).  Then the per-expert row lists and the list of
+  // active experts, and the MoE queue is published.
   __device__ void route(int l) {
     const int B = p.B, E = p.E, K = p.K;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const size_t lb = static_cast<size_t>(l) * p.max_batch;
-    for (int b = warp; b < B; b += kConsumerWarps) {
-      const float* r = p.RLOG + (lb + b) * E;
-      float v[kMaxExperts / 32];
-      uint32_t taken = 0;
-      float mx = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < kMaxExperts / 32; ++i) {
-        const int e = lane + 32 * i;
-        v[i] = e < E ? __ldcg(r + e) : -INFINITY;
-        mx = fmaxf(mx, v[i]);
+    float* lg = S.scr.attn;
+    if (threadIdx.x == 0) S.ykey = -1;
+    const int rpp = kAttnScratch / E;   // rows of logits staged per pass
+    for (int b0 = 0; b0 < B; b0 += rpp) {
+      const int nb = min(rpp, B - b0);
+      for (int i = threadIdx.x; i < nb * E; i += kConsumerThreads) lg[i] = __ldcg(p.RLOG + (lb + b0) * E + i);
+      cbar();
+      trace_mark(15, l);
+      for (int b = warp; b < nb; b += kConsumerWarps) {
+        float mx = -INFINITY;
+        for (int e = lane; e < E; e += 32) mx = fmaxf(mx, lg[b * E + e]);
+        mx = warp_max(mx);
+        float z = 0.f;
+        for (int e = lane; e < E; e += 32) z += expf(lg[b * E + e] - mx);
+        z = warp_sum(z);
+        if (lane == 0) { S.rmax[b0 + b] = mx; S.rz[b0 + b] = z; }
       }
-      mx = warp_max(mx);
-      float z = 0.f;
-#pragma unroll
-      for (int i = 0; i < kMaxExperts / 32; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E) z += expf(v[i] - mx);
-      }
-      z = warp_sum(z);
-      float psel[kMaxTopK];
-      int isel[kMaxTopK];
-      float psum = 0.f;
-#pragma unroll
-      for (int j = 0; j < kMaxTopK; ++j) {
-        psel[j] = 0.f;
-        isel[j] = 0;
-        if (j >= K) continue;
-        // local best among untaken: larger value, then lower index
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int i = 0; i < kMaxExperts / 32; ++i) {
-          const int e = lane + 32 * i;
-          if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) { bv = v[i]; bi = e; }
+      for (int i = threadIdx.x; i < nb * E; i += kConsumerThreads) {
+        const int b = i / E, e = i - b * E;
+        const float* row = lg + b * E;
+        const float v = row[e];
+        int rank = 0;
+        int e2 = 0;
+        if ((E & 3) == 0) {
+#pragma unroll 4
+          for (; e2 < E; e2 += 4) {
+            const float4 w = *reinterpret_cast<const float4*>(row + e2);
+            rank += (w.x > v) || (w.x == v && e2 < e);
+            rank += (w.y > v) || (w.y == v && e2 + 1 < e);
+            rank += (w.z > v) || (w.z == v && e2 + 2 < e);
+            rank += (w.w > v) || (w.w == v && e2 + 3 < e);
+          }
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-          if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+        for (; e2 < E; ++e2) {
+          const float v2 = row[e2];
+          rank += (v2 > v) || (v2 == v && e2 < e);
         }
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-        isel[j] = bi;
-        psel[j] = expf(bv - mx) / z;
-        psum += psel[j];
-      }
-      if (lane == 0) {
-#pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j) {
-          if (j >= K) continue;
-          const float w = p.norm_topk ? psel[j] / psum : psel[j];
-          p.RIDS[(lb + b) * K + j] = isel[j];
-          p.RW[(lb + b) * K + j] = w;
-          S.rids[b * K + j] = isel[j];
+        if (rank < K) {
+          S.rids[(b0 + b) * K + rank] = e;
+          S.rval[(b0 + b) * K + rank] = v;
         }
       }
+      cbar();
+      trace_mark(16, l);
+    }
+    for (int b = threadIdx.x; b < B; b += kConsumerThreads) {
+      float sum = 0.f;
+      for (int j = 0; j < K; ++j) sum += expf(S.rval[b * K + j] - S.rmax[b]);
+      S.rsum[b] = sum;
     }
     cbar();
+    for (int i = threadIdx.x; i < B * K; i += kConsumerThreads) {
+      const int b = i / K;
+      const float ex = expf(S.rval[i] - S.rmax[b]);
+      p.RIDS[lb * K + i] = S.rids[i];
+      p.RW[lb * K + i] = p.norm_topk ? ex / S.rsum[b] : ex / S.rz[b];
+    }
+    trace_mark(17, l);
     // rows routed to each expert, ascending row
     const size_t le = static_cast<size_t>(l) * E;
     for (int e = threadIdx.x; e < E; e += kConsumerThreads) {
@@ -1097,20 +1229,73 @@ struct Consumer {
       }
       if (lane == 0) p.NACT[l] = nact;
     }
+    trace_mark(18, l);
     consumer_signal(p, p.cm.layer_base(l) + L_RREADY);
   }
 
   // which slot (rank) expert e has in row b's choice, or -1
   __device__ void slots_for_expert(int l, int e) {
     const int K = p.K;
+    if (S.moe_layer != l) {   // first MoE item of this layer in this block: cache the routing
+      for (int i = threadIdx.x; i < p.B * K; i += kConsumerThreads)
+        S.rcache[i] = __ldcg(p.RIDS + static_cast<size_t>(l) * p.max_batch * K + i);
+      cbar();
+      if (threadIdx.x == 0) S.moe_layer = l;
+    }
     if (threadIdx.x < p.B) {
-      const int32_t* ids = p.RIDS + (static_cast<size_t>(l) * p.max_batch + threadIdx.x) * K;
       int s = -1;
       for (int j = 0; j < K; ++j)
-        if (__ldcg(ids + j) == e) s = j;
+        if (S.rcache[threadIdx.x * K + j] == e) s = j;
       S.slot_of[threadIdx.x] = s;
     }
     cbar();
+  }
+
+  // the normalised MoE input of every row (B <= TB), staged once per layer in shared memory
+  __device__ void ensure_ffn_input(int l) {
+    if (S.ykey == l) return;
+    const int B = p.B, H = p.H;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int xidx = 2 * l + 1;
+    if (warp < B) {
+      float v[8];
+      ss_issue(p, xidx, warp, v);
+      const float r = ss_rstd(p, v);
+      if (lane == 0) S.rstd[warp] = r;
+    }
+    cbar();
+    const uint16_t* g = p.layers[l].ffn_norm;
+    float* yc = S.scr.attn;
+    for (int i = threadIdx.x * 4; i < B * H; i += kConsumerThreads * 4) {
+      const int b = i / H, k = i - b * H;
+      const float4 x = __ldcg(reinterpret_cast<const float4*>(xrow(xidx, b) + k));
+      const uint2 gw = __ldg(reinterpret_cast<const uint2*>(g + k));
+      const float r = S.rstd[b];
+      yc[i] = (x.x * r) * bf_lo(gw.x);
+      yc[i + 1] = (x.y * r) * bf_hi(gw.x);
+      yc[i + 2] = (x.z * r) * bf_lo(gw.y);
+      yc[i + 3] = (x.w * r) * bf_hi(gw.y);
+    }
+    cbar();
+    if (threadIdx.x == 0) S.ykey = l;
+  }
+
+  __device__ __forceinline__ void load_y_smem(const Seg<TB>& sg, int nt, float (&y)[8 / TB][8][TB]) {
+    const float* yc = S.scr.attn;
+#pragma unroll
+    for (int j = 0; j < Seg<TB>::kUnits; ++j) {
+      const int e = sg.unit(j);
+#pragma unroll
+      for (int tb = 0; tb < TB; ++tb) {
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+        if (e >= 0 && tb < nt) {
+          a = *reinterpret_cast<const float4*>(yc + tb * p.H + e);
+          b = *reinterpret_cast<const float4*>(yc + tb * p.H + e + 4);
+        }
+        y[j][0][tb] = a.x; y[j][1][tb] = a.y; y[j][2][tb] = a.z; y[j][3][tb] = a.w;
+        y[j][4][tb] = b.x; y[j][5][tb] = b.y; y[j][6][tb] = b.z; y[j][7][tb] = b.w;
+      }
+    }
   }
 
   // rows of the batch routed to expert e, in groups of TB: (row, slot); slot -1 = not routed
@@ -1130,277 +1315,296 @@ struct Consumer {
   }
 
   // ------------------------------------------------------------------ attention split item
-  // Warps split the query heads of the KV head into groups of 4 (one group when
-  // G <= 4, two when G = 8) and the chunk's positions among the warps of a group.
-  // A lane owns D/32 consecutive dims: scores are reduced with a reduce-scatter
-  // over the 4 heads (a lane ends holding one head's score), the online softmax
-  // runs per head on the lanes that hold it, and the probabilities are broadcast
-  // back for P*V.  At the end the group's warps merge their (max, sum, output)
-  // states in shared memory; the split's partial goes to global memory and the
-  // last split of (row, KV head) merges all splits in split order.
-  __device__ bool attn_item() {
-    constexpr int DL = D / 32;   // dims per lane
-    constexpr int HPW = 4;       // heads per warp
+  // Tensor cores: per 16 positions, S^T (positions x 8 grouped query heads) = K . Q^T with K
+  // loaded by ldmatrix from the swizzled tiles and Q^T held in registers, then an online
+  // softmax per head and O^T (dims x heads) += V^T . P^T, V^T by ldmatrix.trans and P^T by a
+  // register transpose of the score fragment.  Q and P are split into bf16 hi + lo parts
+  // (two MMAs each) so that the products keep ~16 bits: K and V are exact in bf16.
+  // Warp w takes the 16-position tiles w, w+8, ... of each chunk; at the end of the item
+  // the warps merge their (max, sum, output) states and the split's partial goes to
+  // global memory; the last split of (row, KV head) merges all splits in split order.
+  __device__ __forceinline__ uint32_t swz(int r, int d, int rows_cap) const {
+    return static_cast<uint32_t>((d >> 6) * rows_cap * 128 + r * 128 + ((((d & 63) >> 3) ^ (r & 7)) << 4) + (d & 7) * 2);
+  }
+
+  __device__ __noinline__ bool attn_item() {
+    constexpr int KS = D / 16;                              // k-steps over head dims (Q K^T)
+    constexpr int MT = D / 16;                              // 16-dim tiles of the output (P V)
+    constexpr int ROWS = (kSlotBytes / 2) / (D * 2);        // positions a chunk's K (or V) region holds
     const Meta m0 = meta();
     const int l = m0.layer;
     if (!consumer_wait(p, m0.wait_ctr, m0.wait_target, MK_OP_ATTN, l)) return false;
     twait = globaltimer();
     const mk_attn_item item = p.items[m0.idx];
     const int b = item.b, kvh = item.kvh, Gq = p.G;
-    const int ngrp = (Gq + HPW - 1) / HPW;           // 1 or 2
-    const int wpg = kConsumerWarps / ngrp;           // warps per head group
     const int Lc = p.seq_lens[b];
     const int pos = Lc - 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int gi = warp / wpg, widx = warp - gi * wpg;
-    const int h0 = gi * HPW;
+    const int g = lane >> 2, t = lane & 3;
+    // Q^T as the B operand of S^T = K Q^T, one 16-byte fragment per (k-step, lane):
+    // lane (g, t) holds head g at dims 16s + 2t (+1) and 16s + 2t + 8 (+1), hi then lo parts
+    // of the rotated, scaled q (zero for heads at or above G); then this token's bf16 k and v
+    uint4* qf = reinterpret_cast<uint4*>(S.scr.attn);                     // [KS][32]
+    uint16_t* kvcur = reinterpret_cast<uint16_t*>(S.scr.attn + KS * 32 * 4);  // [2][D]
+    if (threadIdx.x == 0) S.ykey = -1;                                // the MoE input cache shares this storage
     const float* qkv = p.QKV + (static_cast<size_t>(l) * p.max_batch + b) * p.nqkv;
     const float* cs = p.rope_cos + static_cast<size_t>(b) * (D / 2);
     const float* sn = p.rope_sin + static_cast<size_t>(b) * (D / 2);
-    const int d0 = lane * DL;
-    const bool lowhalf = lane < 16;
-    float q[HPW][DL], kc[DL], vc[DL];
-    {
-      float cv[DL], sv[DL];
+    for (int i = threadIdx.x; i < KS * 32; i += kConsumerThreads) {
+      const int s2 = i >> 5, gg = (i >> 2) & 7, tt = i & 3;
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      if (gg < Gq) {
+        const float* qh = qkv + (kvh * Gq + gg) * D;
 #pragma unroll
-      for (int d = 0; d < DL; ++d) {
-        const int i = (d0 + d) % (D / 2);
-        cv[d] = __ldg(cs + i);
-        sv[d] = __ldg(sn + i);
-      }
-#pragma unroll
-      for (int hh = 0; hh < HPW; ++hh) {
-        const int h = h0 + hh;
-#pragma unroll
-        for (int d = 0; d < DL; ++d) {
-          const float raw = h < Gq ? __ldcg(qkv + (kvh * Gq + h) * D + d0 + d) : 0.f;
-          const float other = __shfl_xor_sync(0xffffffffu, raw, 16);
-          const float rot = lowhalf ? raw * cv[d] - other * sv[d] : raw * cv[d] + other * sv[d];
-          q[hh][d] = rot * p.scale;
+        for (int j = 0; j < 4; ++j) {
+          const int d = 16 * s2 + 2 * tt + 8 * (j >> 1) + (j & 1);
+          const int dh = d % (D / 2);
+          const float raw = __ldcg(qh + d), other = __ldcg(qh + (d < D / 2 ? d + D / 2 : d - D / 2));
+          const float c = __ldg(cs + dh), sv = __ldg(sn + dh);
+          v[j] = (d < D / 2 ? raw * c - other * sv : raw * c + other * sv) * p.scale;
         }
       }
-#pragma unroll
-      for (int d = 0; d < DL; ++d) {
-        const float raw = __ldcg(qkv + (p.Hq + kvh) * D + d0 + d);
-        const float other = __shfl_xor_sync(0xffffffffu, raw, 16);
-        kc[d] = round_bf16(lowhalf ? raw * cv[d] - other * sv[d] : raw * cv[d] + other * sv[d]);
-        vc[d] = round_bf16(__ldcg(qkv + (p.Hq + p.Hkv + kvh) * D + d0 + d));
-      }
+      uint4 f;
+      split_bf16x2(v[0], v[1], f.x, f.z);
+      split_bf16x2(v[2], v[3], f.y, f.w);
+      qf[i] = f;
     }
-    if (item.split == 0 && warp == 0) {
+    for (int d = threadIdx.x; d < D; d += kConsumerThreads) {
+      const float* kh = qkv + (p.Hq + kvh) * D;
+      const float raw = __ldcg(kh + d), other = __ldcg(kh + (d < D / 2 ? d + D / 2 : d - D / 2));
+      const float c = __ldg(cs + (d % (D / 2))), sv = __ldg(sn + (d % (D / 2)));
+      kvcur[d] = to_bf16_bits(d < D / 2 ? raw * c - other * sv : raw * c + other * sv);
+      kvcur[D + d] = to_bf16_bits(__ldcg(qkv + (p.Hq + p.Hkv + kvh) * D + d));
+    }
+    cbar();
+    if (item.split == 0) {
       // append this token's k and v to the cache
       const int pg = pos / p.ps, sl = pos % p.ps;
       const int32_t page = __ldg(p.block_tables + static_cast<size_t>(b) * p.maxpg + pg);
       if (page >= 0 && page < p.P) {
-        const size_t kb = (((static_cast<size_t>(l) * p.P + page) * 2 * p.Hkv + kvh) * p.ps + sl) * D + d0;
+        const size_t kb = (((static_cast<size_t>(l) * p.P + page) * 2 * p.Hkv + kvh) * p.ps + sl) * D;
         const size_t vb = kb + static_cast<size_t>(p.Hkv) * p.ps * D;
-#pragma unroll
-        for (int d = 0; d < DL; ++d) {
-          p.kv[kb + d] = to_bf16_bits(kc[d]);
-          p.kv[vb + d] = to_bf16_bits(vc[d]);
+        for (int d = threadIdx.x; d < D; d += kConsumerThreads) {
+          p.kv[kb + d] = kvcur[d];
+          p.kv[vb + d] = kvcur[D + d];
         }
-      } else if (lane == 0) {
+      } else if (threadIdx.x == 0) {
         record_error(p, MK_ERR_DEVICE_BOUNDS, MK_OP_ATTN, l, MK_NO_COUNTER, static_cast<uint32_t>(page), 0, pg,
                      false);
       }
     }
-    float mrun = -INFINITY, lrun = 0.f;   // for head h0 + ((lane >> 3) & 3)
-    float o[HPW][DL];
+    trace_mark(61, l);
+    float o[MT][4];
 #pragma unroll
-    for (int hh = 0; hh < HPW; ++hh)
-#pragma unroll
-      for (int d = 0; d < DL; ++d) o[hh][d] = 0.f;
+    for (int mm = 0; mm < MT; ++mm) o[mm][0] = o[mm][1] = o[mm][2] = o[mm][3] = 0.f;
+    float mx[2] = {-INFINITY, -INFINITY}, ls[2] = {0.f, 0.f};   // heads 2t, 2t+1 (ls: this lane's share)
 
     for (;;) {
-      const Meta m = meta();
-      const int p0 = static_cast<int>(m.row0) * p.ps;            // first position of the chunk
-      const int npos = min(static_cast<int>(m.n) * p.ps, Lc - p0);
-      const uint16_t* Ks = reinterpret_cast<const uint16_t*>(slot());
-      const uint16_t* Vs = reinterpret_cast<const uint16_t*>(slot() + kSlotBytes / 2);
-      const int nmine = npos > widx ? (npos - widx + wpg - 1) / wpg : 0;
-      for (int i0 = 0; i0 < nmine; i0 += 8) {
-        float sc[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int pl = widx + wpg * (i0 + i);
-          const bool valid = (i0 + i) < nmine;
-          float kf[DL];
-          if (valid && p0 + pl == pos) {
-#pragma unroll
-            for (int d = 0; d < DL; ++d) kf[d] = kc[d];
-          } else if (valid) {
-            unpack_row<DL>(Ks + static_cast<size_t>(pl) * D + d0, kf);
-          } else {
-#pragma unroll
-            for (int d = 0; d < DL; ++d) kf[d] = 0.f;
+      const int p0 = static_cast<int>(meta().row0) * p.ps;            // first position of the chunk
+      const int npos = min(static_cast<int>(meta().n) * p.ps, Lc - p0);
+      const bool last = meta().last;
+      const uint32_t Kb = smem_u32(slot());
+      const uint32_t Vb = Kb + kSlotBytes / 2;
+      for (int tile = warp; tile * 16 < npos; tile += kConsumerWarps) {
+        const int r0 = tile * 16;
+        bool patched = false;
+        if (pos >= p0 + r0 && pos < p0 + r0 + 16) {
+          // this token's k and v are not in the copied page yet: put them in its rows
+          const int rr = pos - p0;
+          for (int cidx = lane; cidx < 2 * (D / 8); cidx += 32) {
+            const int which = cidx / (D / 8), d = (cidx - which * (D / 8)) * 8;
+            const uint4 v = *reinterpret_cast<const uint4*>(kvcur + which * D + d);
+            const uint32_t a = (which ? Vb : Kb) + swz(rr, d, ROWS);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                         : "memory");
           }
-          float v[HPW];
-#pragma unroll
-          for (int hh = 0; hh < HPW; ++hh) {
-            float acc = 0.f;
-#pragma unroll
-            for (int d = 0; d < DL; ++d) acc = fmaf(q[hh][d], kf[d], acc);
-            v[hh] = acc;
-          }
-          // reduce-scatter over the 4 head values: lane ends with head (lane >> 3) & 3
-          {
-            const bool b4 = lane & 16;
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-              const float send = b4 ? v[k] : v[k + 2];
-              const float keep = b4 ? v[k + 2] : v[k];
-              v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+          patched = true;
+        }
+        if (r0 + 16 > npos) {
+          // rows past the sequence: zero them so that 0-probability rows cannot carry NaN into P V
+          for (int cidx = lane; cidx < 16 * 2 * (D / 8); cidx += 32) {
+            const int rr = r0 + cidx / (2 * (D / 8));
+            const int rem = cidx % (2 * (D / 8));
+            const int which = rem / (D / 8), d = (rem - which * (D / 8)) * 8;
+            if (rr >= npos) {
+              const uint32_t a = (which ? Vb : Kb) + swz(rr, d, ROWS);
+              asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
             }
-            const bool b3 = lane & 8;
-            const float send = b3 ? v[0] : v[1];
-            const float keep = b3 ? v[1] : v[0];
-            v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-            v[0] += __shfl_xor_sync(0xffffffffu, v[0], 4);
-            v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
-            v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
           }
-          sc[i] = valid ? v[0] : -INFINITY;
+          patched = true;
         }
-        // online softmax for this lane's head over these (up to 8) positions
-        float mx = mrun;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx = fmaxf(mx, sc[i]);
-        const float corr = (mrun == -INFINITY) ? 0.f : __expf(mrun - mx);
-        float pr[8];
-        float ls = 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          pr[i] = sc[i] == -INFINITY ? 0.f : __expf(sc[i] - mx);
-          ls += pr[i];
+        if (patched) {
+          fence_proxy_async_smem();   // these generic writes precede the slot's next TMA fill
+          __syncwarp();
         }
-        lrun = lrun * corr + ls;
-        mrun = mx;
+        // S^T = K Q^T for this tile
+        float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int hh = 0; hh < HPW; ++hh) {
-          const float ch = __shfl_sync(0xffffffffu, corr, hh * 8);
+        for (int s2 = 0; s2 < KS; ++s2) {
+          uint32_t a[4];
+          ldsm_x4(Kb + swz(r0 + (lane & 7) + ((lane >> 3) & 1) * 8, 16 * s2 + (lane >> 4) * 8, ROWS), a);
+          const uint4 q = qf[s2 * 32 + lane];
+          mma_bf16(sc, a, q.x, q.y);
+          mma_bf16(sc, a, q.z, q.w);
+        }
+        if (r0 + g >= npos) { sc[0] = -INFINITY; sc[1] = -INFINITY; }
+        if (r0 + g + 8 >= npos) { sc[2] = -INFINITY; sc[3] = -INFINITY; }
+        // online softmax per head column (heads 2t, 2t+1 on this lane)
+        float pa[2], pb[2], cr[2];
 #pragma unroll
-          for (int d = 0; d < DL; ++d) o[hh][d] *= ch;
+        for (int j = 0; j < 2; ++j) {
+          float tm = fmaxf(sc[j], sc[j + 2]);
+          tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 4));
+          tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 8));
+          tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
+          const float mn = fmaxf(mx[j], tm);
+          cr[j] = mx[j] == -INFINITY ? 0.f : __expf(mx[j] - mn);
+          pa[j] = sc[j] == -INFINITY ? 0.f : __expf(sc[j] - mn);
+          pb[j] = sc[j + 2] == -INFINITY ? 0.f : __expf(sc[j + 2] - mn);
+          ls[j] = ls[j] * cr[j] + pa[j] + pb[j];
+          mx[j] = mn;
         }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if ((i0 + i) >= nmine) break;
-          const int pl = widx + wpg * (i0 + i);
-          float vf[DL];
-          if (p0 + pl == pos) {
+        for (int mm = 0; mm < MT; ++mm) {
+          o[mm][0] *= cr[0]; o[mm][1] *= cr[1]; o[mm][2] *= cr[0]; o[mm][3] *= cr[1];
+        }
+        // P^T as the B operand (positions x heads), hi and lo parts
+        uint32_t xa_h, xa_l, xb_h, xb_l;
+        split_bf16x2(pa[0], pa[1], xa_h, xa_l);
+        split_bf16x2(pb[0], pb[1], xb_h, xb_l);
+        const uint32_t b0h = movmatrix_t(xa_h), b0l = movmatrix_t(xa_l);
+        const uint32_t b1h = movmatrix_t(xb_h), b1l = movmatrix_t(xb_l);
+        // O^T += V^T P^T
 #pragma unroll
-            for (int d = 0; d < DL; ++d) vf[d] = vc[d];
-          } else {
-            unpack_row<DL>(Vs + static_cast<size_t>(pl) * D + d0, vf);
-          }
-#pragma unroll
-          for (int hh = 0; hh < HPW; ++hh) {
-            const float ph = __shfl_sync(0xffffffffu, pr[i], hh * 8);
-#pragma unroll
-            for (int d = 0; d < DL; ++d) o[hh][d] = fmaf(ph, vf[d], o[hh][d]);
-          }
+        for (int mm = 0; mm < MT; ++mm) {
+          uint32_t a[4];
+          ldsm_x4_t(Vb + swz(r0 + (lane & 7) + (lane >> 4) * 8, 16 * mm + ((lane >> 3) & 1) * 8, ROWS), a);
+          mma_bf16(o[mm], a, b0h, b1h);
+          mma_bf16(o[mm], a, b0l, b1l);
         }
       }
-      if (m.last) break;
+      if (last) break;
       if (!next_rec()) break;
     }
     if (!cbar_and(wok)) return false;
+    trace_mark(62, l);
 
-    // merge the group's warps: gather (m, l) per head on every lane, then a tree in shared memory
-    float mh[HPW], lh[HPW];
+    // sums over the 8 lanes that share each head pair
 #pragma unroll
-    for (int hh = 0; hh < HPW; ++hh) {
-      mh[hh] = __shfl_sync(0xffffffffu, mrun, hh * 8);
-      lh[hh] = __shfl_sync(0xffffffffu, lrun, hh * 8);
+    for (int j = 0; j < 2; ++j) {
+      ls[j] += __shfl_xor_sync(0xffffffffu, ls[j], 4);
+      ls[j] += __shfl_xor_sync(0xffffffffu, ls[j], 8);
+      ls[j] += __shfl_xor_sync(0xffffffffu, ls[j], 16);
     }
-    constexpr int kStride = HPW * 128 + 2 * HPW;
-    for (int half = wpg / 2; half >= 1; half >>= 1) {
+    // merge the warps' states: a tree through shared memory, layout [head][dim] + max[8] + sum[8]
+    constexpr int kStride = kMaxG * D + 2 * kMaxG;
+    for (int half = kConsumerWarps / 2; half >= 1; half >>= 1) {
       cbar();
-      if (widx >= half && widx < 2 * half) {
-        float* dst = S.scr.attn + (gi * (kConsumerWarps / 2) + (widx - half)) * kStride;
+      if (warp >= half && warp < 2 * half) {
+        float* dst = S.scr.attn + (warp - half) * kStride;
 #pragma unroll
-        for (int hh = 0; hh < HPW; ++hh)
-#pragma unroll
-          for (int d = 0; d < DL; ++d) dst[hh * D + d0 + d] = o[hh][d];
-        if (lane < HPW) {
-          dst[HPW * D + 2 * lane] = mh[lane];
-          dst[HPW * D + 2 * lane + 1] = lh[lane];
+        for (int mm = 0; mm < MT; ++mm) {
+          dst[(2 * t) * D + 16 * mm + g] = o[mm][0];
+          dst[(2 * t + 1) * D + 16 * mm + g] = o[mm][1];
+          dst[(2 * t) * D + 16 * mm + g + 8] = o[mm][2];
+          dst[(2 * t + 1) * D + 16 * mm + g + 8] = o[mm][3];
+        }
+        if (g == 0) {
+          dst[kMaxG * D + 2 * t] = mx[0];
+          dst[kMaxG * D + 2 * t + 1] = mx[1];
+          dst[kMaxG * D + kMaxG + 2 * t] = ls[0];
+          dst[kMaxG * D + kMaxG + 2 * t + 1] = ls[1];
         }
       }
       cbar();
-      if (widx < half) {
-        const float* src = S.scr.attn + (gi * (kConsumerWarps / 2) + widx) * kStride;
+      if (warp < half) {
+        const float* src = S.scr.attn + warp * kStride;
+        float fa[2], fb[2];
 #pragma unroll
-        for (int hh = 0; hh < HPW; ++hh) {
-          const float mo = src[HPW * D + 2 * hh], lo = src[HPW * D + 2 * hh + 1];
-          const float M = fmaxf(mh[hh], mo);
-          const float fa = mh[hh] == -INFINITY ? 0.f : __expf(mh[hh] - M);
-          const float fb = mo == -INFINITY ? 0.f : __expf(mo - M);
+        for (int j = 0; j < 2; ++j) {
+          const float mo = src[kMaxG * D + 2 * t + j], lo = src[kMaxG * D + kMaxG + 2 * t + j];
+          const float M = fmaxf(mx[j], mo);
+          fa[j] = mx[j] == -INFINITY ? 0.f : __expf(mx[j] - M);
+          fb[j] = mo == -INFINITY ? 0.f : __expf(mo - M);
+          ls[j] = ls[j] * fa[j] + lo * fb[j];
+          mx[j] = M;
+        }
 #pragma unroll
-          for (int d = 0; d < DL; ++d) o[hh][d] = o[hh][d] * fa + src[hh * D + d0 + d] * fb;
-          lh[hh] = lh[hh] * fa + lo * fb;
-          mh[hh] = M;
+        for (int mm = 0; mm < MT; ++mm) {
+          o[mm][0] = o[mm][0] * fa[0] + src[(2 * t) * D + 16 * mm + g] * fb[0];
+          o[mm][1] = o[mm][1] * fa[1] + src[(2 * t + 1) * D + 16 * mm + g] * fb[1];
+          o[mm][2] = o[mm][2] * fa[0] + src[(2 * t) * D + 16 * mm + g + 8] * fb[0];
+          o[mm][3] = o[mm][3] * fa[1] + src[(2 * t + 1) * D + 16 * mm + g + 8] * fb[1];
         }
       }
     }
-    if (widx == 0) {
+    if (warp == 0) {
       float* po = p.PO + static_cast<size_t>(m0.idx) * Gq * D;
       float* pml = p.PML + static_cast<size_t>(m0.idx) * Gq * 2;
 #pragma unroll
-      for (int hh = 0; hh < HPW; ++hh) {
-        if (h0 + hh < Gq) {
+      for (int j = 0; j < 2; ++j) {
+        const int h = 2 * t + j;
+        if (h < Gq) {
 #pragma unroll
-          for (int d = 0; d < DL; ++d) po[(h0 + hh) * D + d0 + d] = o[hh][d];
+          for (int mm = 0; mm < MT; ++mm) {
+            po[h * D + 16 * mm + g] = o[mm][j];
+            po[h * D + 16 * mm + g + 8] = o[mm][j + 2];
+          }
+          if (g == 0) {
+            pml[2 * h] = mx[j];
+            pml[2 * h + 1] = ls[j];
+          }
         }
       }
-      if (lane < HPW && h0 + lane < Gq) {
-        pml[2 * (h0 + lane)] = pick<HPW>(mh, lane);
-        pml[2 * (h0 + lane) + 1] = pick<HPW>(lh, lane);
-      }
     }
-    // the last split of (b, kvh) merges every split in split order
+    trace_mark(63, l);
+    // the last split of (b, kvh) merges every split in split order.  Thread i owns 4 output
+    // dims of one head and folds the splits in with a running (max, sum, output); the loads of
+    // 16 splits are issued together so that the merge costs a few round trips, not one per split.
     const uint32_t base = p.cm.layer_base(l);
     const int pair = b * p.Hkv + kvh;
     if (consumer_arrive_last(p, S, base + L_PAIR + pair, item.nsplit)) {
+      trace_mark(64, l);
       const int first = p.pair_first[pair];
       const int ns = item.nsplit;
-      if (warp < Gq) {
-        const int h = warp;
-        float mloc = -INFINITY;
-        for (int s = lane; s < ns; s += 32) mloc = fmaxf(mloc, __ldcg(p.PML + (static_cast<size_t>(first + s) * Gq + h) * 2));
-        const float M = warp_max(mloc);
-        // each lane's splits: weight exp(m_s - M); the output is the weighted sum / sum of weighted l
-        float lloc = 0.f;
-        for (int s = lane; s < ns; s += 32) {
-          const float ms = __ldcg(p.PML + (static_cast<size_t>(first + s) * Gq + h) * 2);
-          const float ls = __ldcg(p.PML + (static_cast<size_t>(first + s) * Gq + h) * 2 + 1);
-          if (ms != -INFINITY) lloc += __expf(ms - M) * ls;
-        }
-        const float Lsum = warp_sum(lloc);
-        float acc[DL];
+      const int q4 = threadIdx.x;                 // float4 index into [Gq][D]
+      if (q4 * 4 < Gq * D) {
+        const int h = (q4 * 4) / D;
+        const float4* po = reinterpret_cast<const float4*>(p.PO) + static_cast<size_t>(first) * (Gq * D / 4) + q4;
+        const float2* pml = reinterpret_cast<const float2*>(p.PML) + static_cast<size_t>(first) * Gq + h;
+        float M = -INFINITY, Ls = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        constexpr int kBatch = 16;
+        for (int s0 = 0; s0 < ns; s0 += kBatch) {
+          float2 ml[kBatch];
+          float4 ov[kBatch];
 #pragma unroll
-        for (int d = 0; d < DL; ++d) acc[d] = 0.f;
-        for (int s0 = 0; s0 < ns; s0 += 8) {
-          float ms[8], ov[8][DL];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int s = s0 + j;
-            ms[j] = s < ns ? __ldcg(p.PML + (static_cast<size_t>(first + s) * Gq + h) * 2) : -INFINITY;
-#pragma unroll
-            for (int d = 0; d < DL; ++d)
-              ov[j][d] = s < ns ? __ldcg(p.PO + (static_cast<size_t>(first + s) * Gq + h) * D + d0 + d) : 0.f;
+          for (int j = 0; j < kBatch; ++j) {
+            const int s2 = s0 + j;
+            ml[j] = s2 < ns ? __ldcg(pml + static_cast<size_t>(s2) * Gq) : make_float2(-INFINITY, 0.f);
+            ov[j] = s2 < ns ? __ldcg(po + static_cast<size_t>(s2) * (Gq * D / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
           }
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float f = ms[j] == -INFINITY ? 0.f : __expf(ms[j] - M);
-#pragma unroll
-            for (int d = 0; d < DL; ++d) acc[d] = fmaf(f, ov[j][d], acc[d]);
+          for (int j = 0; j < kBatch; ++j) {
+            if (ml[j].x == -INFINITY) continue;
+            const float Mn = fmaxf(M, ml[j].x);
+            const float fa = M == -INFINITY ? 0.f : __expf(M - Mn);
+            const float fb = __expf(ml[j].x - Mn);
+            Ls = Ls * fa + ml[j].y * fb;
+            acc.x = acc.x * fa + ov[j].x * fb;
+            acc.y = acc.y * fa + ov[j].y * fb;
+            acc.z = acc.z * fa + ov[j].z * fb;
+            acc.w = acc.w * fa + ov[j].w * fb;
+            M = Mn;
           }
         }
-        float* dst = p.ATT + (static_cast<size_t>(l) * p.max_batch + b) * (p.Hq * D) + (kvh * Gq + h) * D + d0;
-#pragma unroll
-        for (int d = 0; d < DL; ++d) dst[d] = acc[d] / Lsum;
+        const float inv = 1.f / Ls;
+        float4* dst = reinterpret_cast<float4*>(p.ATT + (static_cast<size_t>(l) * p.max_batch + b) * (p.Hq * D) +
+                                                static_cast<size_t>(kvh) * Gq * D) + q4;
+        *dst = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
       }
       consumer_signal(p, base + L_ATTN);
+      trace_mark(65, l);
     }
     return true;
   }
@@ -1443,7 +1647,9 @@ struct Consumer {
 template <int TB, int D>
 __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  Smem& S = *reinterpret_cast<Smem*>(smem_raw);
+  // the ring holds 128-byte-swizzled TMA tiles, whose pattern repeats every 1024 bytes
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  Smem& S = *reinterpret_cast<Smem*>(smem_raw + pad);
   const int tid = threadIdx.x;
   if (tid == 0) {
     for (int s = 0; s < kSlots; ++s) {
@@ -1452,6 +1658,8 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     }
     S.prod_count = 0;
     S.cons_count = 0xffffffffu;
+    S.moe_layer = -1;
+    S.ykey = -1;
     if (p.trace) p.trace[static_cast<size_t>(blockIdx.x) * p.trace_cap * 4 + 1] = globaltimer();
     fence_mbar_init();
   }

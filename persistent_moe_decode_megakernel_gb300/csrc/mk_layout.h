@@ -37,6 +37,7 @@ constexpr int kMaxRowsPerChunk = 32;
 // ---- MoE work-queue tiles --------------------------------------------------------
 constexpr int kFTile = 16;        // expert FFN rows (gate+up pairs) per gate/up item
 constexpr int kRTile = 64;        // hidden rows per down item
+constexpr int kRouterRows = 8;    // router (expert) rows per router tile
 
 MK_HD int gemv_rows_per_chunk(int K) {
   int r = kSlotBytes / (2 * K);
@@ -89,7 +90,10 @@ struct LayerW {
   const uint16_t* w_down;
 };
 
-struct Params {
+struct alignas(64) Params {
+  // TMA descriptor (CUtensorMap, 128 bytes) of the KV pool as a 2-D bf16 tensor
+  // [L*num_pages*2*Hkv*page_size rows][head_dim], boxes of 64 elements x page_size rows, 128-byte swizzle
+  alignas(64) uint64_t kv_map[16];
   // shape
   int32_t L, H, Hq, Hkv, D, G, E, K, F, V, ps, P, maxpg;
   int32_t nqkv;          // (Hq + 2Hkv) * D
@@ -145,6 +149,6 @@ struct Params {
 };
 
 // trace tags: op | layer << 8 | kind << 24 | (uint64)idx << 32
-enum : uint32_t { TR_TILE = 1, TR_ITEM = 2, TR_PRODUCER_ROUTE_WAIT = 3, TR_CHUNK = 4 };
+enum : uint32_t { TR_TILE = 1, TR_ITEM = 2, TR_PRODUCER_ROUTE_WAIT = 3, TR_CHUNK = 4, TR_MARK = 5 };
 
 }  // namespace mk

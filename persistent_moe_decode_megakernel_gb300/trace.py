@@ -39,7 +39,8 @@ def summarize(tr: np.ndarray, n_layers: int) -> dict:
     out = {"phases": [], "wait_share": None, "step_us": None}
     kind = ((ev["tag"] >> 24) & 0xff).astype(int)
     chunks = ev[(ev["prod"] == 0) & (kind == 4)]
-    ev = ev[~((ev["prod"] == 0) & (kind == 4))]
+    out["marks"] = ev[(ev["prod"] == 0) & (kind == 5)]
+    ev = ev[~((ev["prod"] == 0) & ((kind == 4) | (kind == 5)))]
     op = (ev["tag"] & 0xff).astype(int)
     layer = ((ev["tag"] >> 8) & 0xffff).astype(int)
     if len(chunks):
