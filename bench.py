@@ -42,7 +42,7 @@ from persistent_moe_decode_megakernel_gb300 import roofline as R  # noqa: E402
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="moe30b_bs1_ctx8k", choices=W.NAMES)
     ap.add_argument("--impl", default="mk", choices=("mk", "reference"))
@@ -204,6 +204,19 @@ def run_reference(args):
     return 0
 
 
+def replica_value(ms_per_step: float, batch: int, device: str):
+    """Whole-job tokens/s of independent replicas: every rank decodes ``batch`` tokens per
+    step; the job's step time is the slowest rank's.  Returns (max ms over ranks, tok/s)."""
+    import torch
+    world = 1
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        world = torch.distributed.get_world_size()
+        t = torch.tensor([ms_per_step], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+    return ms_per_step, world * batch / (ms_per_step / 1e3)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -258,11 +271,7 @@ def main():
     per = [a.elapsed_time(b) for a, b in ev]
     ms_mean = sum(per) / len(per)
     ms_med = statistics.median(per)
-    if world > 1:
-        t = torch.tensor([ms_mean], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_mean = float(t.item())
-    value = world * B / (ms_mean / 1e3)
+    ms_mean, value = replica_value(ms_mean, B, "cuda")
 
     # ---- end to end through the C ABI with host buffers
     e2e = None
@@ -288,12 +297,8 @@ def main():
                 out_h.copy_(logits, non_blocking=True)
             e1.record(stream)
         stream.synchronize()
-        e2e_ms = e0.elapsed_time(e1) / args.steps
-        if world > 1:
-            t = torch.tensor([e2e_ms], device="cuda")
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": world * B / (e2e_ms / 1e3), "unit": "tok/s",
+        e2e_ms, e2e_value = replica_value(e0.elapsed_time(e1) / args.steps, B, "cuda")
+        e2e = {"value": e2e_value, "unit": "tok/s",
                "h2d_bytes_per_step": int(tok_h.numel() * 4 + bt_h.numel() * 4),
                "d2h_bytes_per_step": int(out_h.numel() * 4), "ms_per_step": e2e_ms,
                "note": "token ids and block tables copied from pinned host memory, logits copied back, every step"}
@@ -330,7 +335,7 @@ def main():
         line = {"metric": "decode tok/s at bs=1 and bs=64; % of HBM SoL (active weights+KV bytes/step)",
                 "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": ms_mean, "ms_per_step_median": ms_med, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "bf16 weights/KV, fp32 accumulate",
+                "vs_baseline": None, "dtype": "bf16", "accumulate": "f32",
                 "data": "synthetic (seeded random-init bf16 weights ~N(0,0.02), KV ~N(0,1))",
                 "config": {"workload": wl.name, "batch": B, "context": int(max(st["lens"]) - 1),
                            "page_size": st["ps"], "layers": m["layers"], "hidden": m["hidden"],
