@@ -57,8 +57,9 @@ typedef struct CUstream_st* mk_stream_t;
  * (mk_create returns MK_ERR_UNSUPPORTED outside them):
  *   head_dim in {64, 128}; num_q_heads % num_kv_heads == 0 with at most 8 query
  *   heads per KV head; hidden, num_q_heads*head_dim and expert_ffn multiples of 8
- *   and <= 4096; num_experts <= 256; top_k <= min(8, num_experts);
- *   page_size*head_dim*2 <= 32768 bytes; max_batch <= 64.
+ *   and <= 4096, expert_ffn <= 1024; num_experts <= 256; top_k <= min(8, num_experts);
+ *   page_size*head_dim*2 <= 32768 bytes, page_size a multiple of 8; max_batch <= 64;
+ *   max_batch*(top_k+1)*ceil(hidden/SMs) <= 14336; max_batch*num_experts <= 14336.
  */
 typedef struct mk_config {
   int32_t num_layers;

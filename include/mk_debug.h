@@ -62,8 +62,8 @@ typedef struct mk_plan_info {
   int32_t n_ctas;
   int32_t n_tasks;        /* total tasks over all lists */
   int32_t n_qkv_tiles, n_o_tiles, n_router_tiles, n_head_tiles, n_embed_tiles;
-  int32_t f_tile, n_ftiles; /* expert FFN rows per gate/up queue item, items per expert */
-  int32_t r_tile, n_rtiles; /* hidden rows per down queue item, items per expert */
+  int32_t n_down_ranges;    /* blocks that own hidden rows of the down projection */
+  int32_t reserved[3];
   int32_t n_counters;       /* counters the step uses */
   int32_t max_items;        /* attention items a step can produce for max_batch */
 } mk_plan_info;
@@ -86,14 +86,16 @@ typedef struct mk_sim_result {
   int64_t events;          /* scheduling events simulated */
   int32_t tiles_run[9];    /* tiles / items executed, indexed by op */
   int32_t counters_ok;     /* 1 if every counter ended at its expected value */
-  int32_t queue_items_ok;  /* 1 if every MoE queue item ran exactly once */
+  int32_t moe_units_ok;    /* 1 if every gate/up unit and every (expert, hidden row) of the down
+                              projection was assigned to exactly one block */
 } mk_sim_result;
 
 /* Run the step's task graph on the CPU with `n_ctas` virtual SMs under a seeded
  * random interleaving.  Each virtual SM has a producer that runs at most
- * `producer_lead` tiles ahead of its consumer (claiming MoE queue items as the
- * device does) and a consumer that honours every counter wait.  routing_ids:
- * host [num_layers][batch][top_k] expert ids the router is taken to choose. */
+ * `producer_lead` records ahead of its consumer (splitting the MoE work with the
+ * same rule as the device) and a consumer that honours every counter wait.
+ * routing_ids: host [num_layers][batch][top_k] expert ids the router is taken to
+ * choose. */
 int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t batch, const int32_t* seq_lens,
                 const int32_t* routing_ids, uint64_t seed, int32_t producer_lead, mk_sim_result* out);
 

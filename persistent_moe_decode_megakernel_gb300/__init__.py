@@ -119,14 +119,14 @@ class AttnItem(ctypes.Structure):
 
 class PlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("n_ctas", "n_tasks", "n_qkv_tiles", "n_o_tiles", "n_router_tiles",
-                                               "n_head_tiles", "n_embed_tiles", "f_tile", "n_ftiles", "r_tile",
-                                               "n_rtiles", "n_counters", "max_items")]
+                                               "n_head_tiles", "n_embed_tiles", "n_down_ranges", "reserved0",
+                                               "reserved1", "reserved2", "n_counters", "max_items")]
 
 
 class SimResult(ctypes.Structure):
     _fields_ = [("finished", ctypes.c_int32), ("deadlocked", ctypes.c_int32), ("events", ctypes.c_int64),
                 ("tiles_run", ctypes.c_int32 * 9), ("counters_ok", ctypes.c_int32),
-                ("queue_items_ok", ctypes.c_int32)]
+                ("moe_units_ok", ctypes.c_int32)]
 
 
 EXPORTS = ("mk_create", "mk_decode_step", "mk_get_status", "mk_last_error", "mk_destroy", "mk_plan_static",

@@ -91,6 +91,7 @@ int check_config(const mk_config* c) {
   for (int32_t k : ks)
     if (k % 8 || k > mk::kMaxK) return fail(MK_ERR_UNSUPPORTED, "GEMV input lengths must be multiples of 8 and <= 4096");
   if (c->num_experts > mk::kMaxExperts) return fail(MK_ERR_UNSUPPORTED, "num_experts > 256");
+  if (c->expert_ffn > 1024) return fail(MK_ERR_UNSUPPORTED, "expert_ffn > 1024");
   if (c->top_k > mk::kMaxTopK) return fail(MK_ERR_UNSUPPORTED, "top_k > 8");
   if (c->page_size * c->head_dim * 2 > mk::kSlotBytes / 2) return fail(MK_ERR_UNSUPPORTED, "page_size*head_dim*2 > 32768");
   if (c->page_size % 8) return fail(MK_ERR_UNSUPPORTED, "page_size must be a multiple of 8");
@@ -120,11 +121,7 @@ void build_static_plan(const mk_config& c, int n_ctas, Plan& plan) {
   const int L = c.num_layers, H = c.hidden, E = c.num_experts, V = c.vocab;
   const int nqkv = (c.num_q_heads + 2 * c.num_kv_heads) * c.head_dim;
   in.n_ctas = n_ctas;
-  in.f_tile = mk::kFTile;
-  in.n_ftiles = (c.expert_ffn + mk::kFTile - 1) / mk::kFTile;
-  in.r_tile = mk::kRTile;
-  in.n_rtiles = (H + mk::kRTile - 1) / mk::kRTile;
-  plan.cm = mk::counter_map(L, c.max_batch, c.num_kv_heads, E, in.n_rtiles);
+  plan.cm = mk::counter_map(L, c.max_batch, c.num_kv_heads);
   in.n_counters = (int32_t)plan.cm.total;
   in.max_items = n_ctas + c.max_batch * c.num_kv_heads;
   auto count = [&](uint32_t rows) {
@@ -141,6 +138,7 @@ void build_static_plan(const mk_config& c, int n_ctas, Plan& plan) {
   in.n_o_tiles = count((uint32_t)H);
   in.n_router_tiles = (E + mk::kRouterRows - 1) / mk::kRouterRows;
   in.n_head_tiles = count((uint32_t)V);
+  in.n_down_ranges = count((uint32_t)H);
   const CounterMap& cm = plan.cm;
   plan.tasks.clear();
   plan.off.assign(n_ctas + 1, 0);
@@ -160,7 +158,7 @@ void build_static_plan(const mk_config& c, int n_ctas, Plan& plan) {
       split_range((uint32_t)nqkv, n_ctas, i, &lo, &hi);
       if (hi > lo) {
         if (l == 0) push(MK_OP_QKV, l, lo, hi, mk::C_EMBED, (uint32_t)in.n_embed_tiles, 0, base + mk::L_QKV);
-        else push(MK_OP_QKV, l, lo, hi, cm.layer_base(l - 1) + mk::L_MOE, (uint32_t)in.n_rtiles, 0, base + mk::L_QKV);
+        else push(MK_OP_QKV, l, lo, hi, cm.layer_base(l - 1) + mk::L_MOE, (uint32_t)n_ctas, 0, base + mk::L_QKV);
       }
       push(MK_OP_ATTN, l, 0, 0, base + mk::L_QKV, (uint32_t)in.n_qkv_tiles, 0, MK_NO_COUNTER);
       split_range((uint32_t)H, n_ctas, i, &lo, &hi);
@@ -172,7 +170,7 @@ void build_static_plan(const mk_config& c, int n_ctas, Plan& plan) {
     }
     split_range((uint32_t)V, n_ctas, i, &lo, &hi);
     if (hi > lo)
-      push(MK_OP_HEAD, L, lo, hi, cm.layer_base(L - 1) + mk::L_MOE, (uint32_t)in.n_rtiles, 0, MK_NO_COUNTER);
+      push(MK_OP_HEAD, L, lo, hi, cm.layer_base(L - 1) + mk::L_MOE, (uint32_t)n_ctas, 0, MK_NO_COUNTER);
     push(MK_OP_END, 0, 0, 0, MK_NO_COUNTER, 0, 0, MK_NO_COUNTER);
   }
   plan.off[n_ctas] = (int32_t)plan.tasks.size();
@@ -273,10 +271,14 @@ struct mk_ctx {
   const uint16_t* lm_head = nullptr;
   // workspace
   uint8_t* ws = nullptr;
-  float *X = nullptr, *QKV = nullptr, *ATT = nullptr, *PO = nullptr, *PML = nullptr, *RLOG = nullptr, *RW = nullptr,
-        *HB = nullptr, *PART = nullptr, *SS = nullptr;
+  // tagged 8-byte words (value | step tag << 32)
+  uint64_t *X = nullptr, *QKV = nullptr, *ATT = nullptr, *PO = nullptr, *PML = nullptr, *RLOG = nullptr,
+           *HB = nullptr, *SS = nullptr;
+  float* RW = nullptr;
   int n_ss_slots = 0;
-  int32_t *RIDS = nullptr, *ACT = nullptr, *NACT = nullptr, *TOK = nullptr, *CNT = nullptr;
+  int32_t* RIDS = nullptr;
+  uint32_t tag = 0;        // tag of the last step (0: none yet)
+  size_t tagged_bytes = 0; // bytes of the tagged buffers (cleared when the tag wraps)
   uint32_t* ctr = nullptr;
   mk_status* d_status = nullptr;
   // per-step staging (double-buffered)
@@ -387,7 +389,15 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_ctx** out) {
   if ((e = mk::occupancy(cfg->head_dim, &blocks)) != cudaSuccess) return cuda_fail(e, "occupancy");
   if (blocks < 1) return fail(MK_ERR_UNSUPPORTED, "the step kernel does not fit on an SM");
 
-  if (prop.multiProcessorCount > 256) return fail(MK_ERR_UNSUPPORTED, "more than 256 SMs");
+  if (prop.multiProcessorCount > mk::kMaxCtas) return fail(MK_ERR_UNSUPPORTED, "more than 256 SMs");
+  {
+    // per block: the down projection keeps (row, slot) products and x_mid of its hidden rows on chip
+    const int64_t nr = (cfg->hidden + prop.multiProcessorCount - 1) / prop.multiProcessorCount;
+    if ((int64_t)cfg->max_batch * (cfg->top_k + 1) * nr > mk::kMoeScratch)
+      return fail(MK_ERR_UNSUPPORTED, "max_batch*(top_k+1)*ceil(hidden/SMs) exceeds the down-projection scratch");
+    if ((int64_t)cfg->max_batch * cfg->num_experts > mk::kMoeScratch)
+      return fail(MK_ERR_UNSUPPORTED, "max_batch*num_experts exceeds the routing scratch");
+  }
   mk_ctx* c = new mk_ctx();
   c->cfg = *cfg;
   if (c->cfg.watchdog_ms == 0) c->cfg.watchdog_ms = 1000;
@@ -414,23 +424,18 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_ctx** out) {
   }
   // workspace
   struct Part { void** ptr; size_t bytes; };
-  const size_t f4 = sizeof(float), i4 = sizeof(int32_t);
+  const size_t f4 = sizeof(float), i4 = sizeof(int32_t), w8 = sizeof(uint64_t);
   const Part parts[] = {
-      {(void**)&c->X, (size_t)(2 * L + 1) * MB * H * f4},
-      {(void**)&c->QKV, (size_t)L * MB * nqkv * f4},
-      {(void**)&c->ATT, (size_t)L * MB * Hq * D * f4},
-      {(void**)&c->PO, (size_t)in.max_items * G * D * f4},
-      {(void**)&c->PML, (size_t)in.max_items * G * 2 * f4},
-      {(void**)&c->RLOG, (size_t)L * MB * E * f4},
+      {(void**)&c->X, (size_t)(2 * L + 1) * MB * H * w8},
+      {(void**)&c->QKV, (size_t)L * MB * nqkv * w8},
+      {(void**)&c->ATT, (size_t)L * MB * Hq * D * w8},
+      {(void**)&c->PO, (size_t)L * in.max_items * mk::kMaxG * D * w8},
+      {(void**)&c->PML, (size_t)L * in.max_items * mk::kMaxG * 2 * w8},
+      {(void**)&c->RLOG, (size_t)L * MB * E * w8},
+      {(void**)&c->HB, (size_t)L * MB * K * F * w8},
+      {(void**)&c->SS, (size_t)(2 * L + 1) * c->n_ctas * MB * w8},
       {(void**)&c->RIDS, (size_t)L * MB * K * i4},
       {(void**)&c->RW, (size_t)L * MB * K * f4},
-      {(void**)&c->ACT, (size_t)L * E * i4},
-      {(void**)&c->NACT, (size_t)L * i4},
-      {(void**)&c->TOK, (size_t)L * E * MB * i4},
-      {(void**)&c->CNT, (size_t)L * E * i4},
-      {(void**)&c->HB, (size_t)L * MB * K * F * f4},
-      {(void**)&c->PART, (size_t)L * MB * K * H * f4},
-      {(void**)&c->SS, (size_t)(2 * L + 1) * std::max(c->n_ctas, in.n_rtiles) * MB * f4},
       {(void**)&c->ctr, (size_t)c->plan.cm.total * 4},
       {(void**)&c->d_status, sizeof(mk_status)},
   };
@@ -440,6 +445,7 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_ctx** out) {
   size_t o = 0;
   for (const Part& p : parts) { *p.ptr = c->ws + o; o += align256(p.bytes); }
   if ((e = cudaMemset(c->ws, 0, total)) != cudaSuccess) { free_ctx(c); return cuda_fail(e, "workspace memset"); }
+  c->tagged_bytes = (size_t)(reinterpret_cast<uint8_t*>(c->RIDS) - reinterpret_cast<uint8_t*>(c->X));
   // static plan + layer table
   if ((e = cudaMalloc(&c->d_layers, sizeof(mk::LayerW) * L)) != cudaSuccess ||
       (e = cudaMalloc(&c->d_tasks, sizeof(mk_task) * c->plan.tasks.size())) != cudaSuccess ||
@@ -540,7 +546,6 @@ int mk_decode_step(mk_ctx* c, int32_t batch, const int32_t* token_ids, const int
   p.B = batch; p.max_batch = cf.max_batch; p.n_ctas = c->n_ctas;
   const mk_plan_info& in = c->plan.info;
   p.n_qkv_tiles = in.n_qkv_tiles; p.n_o_tiles = in.n_o_tiles; p.n_router_tiles = in.n_router_tiles;
-  p.n_ftiles = in.n_ftiles; p.n_rtiles = in.n_rtiles;
   p.cm = c->plan.cm;
   uint32_t wd_ms = cf.watchdog_ms;
   p.tasks = c->d_tasks; p.task_off = c->d_task_off;
@@ -553,8 +558,15 @@ int mk_decode_step(mk_ctx* c, int32_t batch, const int32_t* token_ids, const int
   p.item_off = reinterpret_cast<const int32_t*>(d + c->off_item_off);
   p.pair_first = reinterpret_cast<const int32_t*>(d + c->off_pair);
   p.X = c->X; p.QKV = c->QKV; p.ATT = c->ATT; p.PO = c->PO; p.PML = c->PML; p.RLOG = c->RLOG; p.RIDS = c->RIDS;
-  p.RW = c->RW; p.ACT = c->ACT; p.NACT = c->NACT; p.TOK = c->TOK; p.CNT = c->CNT; p.HB = c->HB; p.PART = c->PART;
-  p.SS = c->SS; p.n_ss_slots = std::max(c->n_ctas, in.n_rtiles);
+  p.RW = c->RW; p.HB = c->HB; p.SS = c->SS; p.n_ss_slots = c->n_ctas;
+  p.max_items = c->plan.info.max_items;
+  // a fresh tag per step; tagged words of an earlier step never match it.  When the tag
+  // wraps, the tagged buffers are cleared so that no word from 2^32 steps ago can match.
+  if (++c->tag == 0) {
+    if ((e = cudaMemsetAsync(c->X, 0, c->tagged_bytes, s)) != cudaSuccess) return cuda_fail(e, "tag wrap clear");
+    c->tag = 1;
+  }
+  p.tag = c->tag;
   p.ctr = c->ctr; p.status = c->d_status;
   p.trace = c->trace; p.trace_cap = c->trace_cap;
   if (kv_pages != c->kv_map_ptr) {
@@ -565,32 +577,15 @@ int mk_decode_step(mk_ctx* c, int32_t batch, const int32_t* token_ids, const int
   static_assert(sizeof(CUtensorMap) == sizeof(p.kv_map), "tensor map size");
   std::memcpy(p.kv_map, &c->kv_map, sizeof(p.kv_map));
 
-  // test hook: one O-proj task waits on a counter nothing increments
-  int stall_idx = -1;
-  mk_task saved;
+  // test hook: the O-proj tiles of one layer wait for a tag that is never written
+  p.stall_layer = -1;
   if (c->stall_layer >= 0) {
-    for (int i = c->plan.off[0]; i < c->plan.off[1]; ++i) {
-      const mk_task& t = c->plan.tasks[i];
-      if (t.op == MK_OP_OPROJ && t.layer == c->stall_layer) { stall_idx = i; break; }
-    }
-    if (stall_idx >= 0) {
-      saved = c->plan.tasks[stall_idx];
-      mk_task t = saved;
-      t.wait_ctr = mk::C_NEVER; t.wait_base = 1; t.wait_per_b = 0;
-      if ((e = cudaMemcpyAsync(c->d_tasks + stall_idx, &t, sizeof t, cudaMemcpyHostToDevice, s)) != cudaSuccess)
-        return cuda_fail(e, "stall arm");
-      if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "stall arm sync");
-      if (c->stall_ms) wd_ms = c->stall_ms;
-    }
+    p.stall_layer = c->stall_layer;
+    if (c->stall_ms) wd_ms = c->stall_ms;
     c->stall_layer = -1;
   }
   p.watchdog_ns = (uint64_t)wd_ms * 1000000ull;
   if ((e = mk::launch_step(p, s)) != cudaSuccess) return cuda_fail(e, "cooperative launch");
-  if (stall_idx >= 0) {
-    if ((e = cudaMemcpyAsync(c->d_tasks + stall_idx, &saved, sizeof saved, cudaMemcpyHostToDevice, s)) != cudaSuccess)
-      return cuda_fail(e, "stall disarm");
-    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "stall disarm sync");
-  }
   if ((e = cudaEventRecord(c->ev_done, s)) != cudaSuccess) return cuda_fail(e, "event record");
   c->stepped = true;
   c->last_B = batch;
@@ -642,22 +637,32 @@ int mk_debug_read(mk_ctx* c, int32_t what, int32_t layer, void* dst, size_t byte
   const size_t nqkv = (size_t)(cf.num_q_heads + 2 * cf.num_kv_heads) * cf.head_dim;
   const size_t K = cf.top_k, E = cf.num_experts, H = cf.hidden, F = cf.expert_ffn;
   const size_t QD = (size_t)cf.num_q_heads * cf.head_dim;
+  bool tagged = true;   // buffer of tagged 8-byte words: the value is the low half
   switch (what) {
-    case MK_DBG_X: src = c->X; row = (size_t)B * H * 4; rows = 2 * L + 1; stride = (size_t)MB * H * 4; break;
-    case MK_DBG_QKV: src = c->QKV + (size_t)layer * MB * nqkv; row = (size_t)B * nqkv * 4; rows = 1; break;
-    case MK_DBG_ATTN: src = c->ATT + (size_t)layer * MB * QD; row = (size_t)B * QD * 4; rows = 1; break;
-    case MK_DBG_ROUTER: src = c->RLOG + (size_t)layer * MB * E; row = (size_t)B * E * 4; rows = 1; break;
-    case MK_DBG_ROUTE_IDS: src = c->RIDS + (size_t)layer * MB * K; row = (size_t)B * K * 4; rows = 1; break;
-    case MK_DBG_ROUTE_W: src = c->RW + (size_t)layer * MB * K; row = (size_t)B * K * 4; rows = 1; break;
-    case MK_DBG_H: src = c->HB + (size_t)layer * MB * K * F; row = (size_t)B * K * F * 4; rows = 1; break;
+    case MK_DBG_X: src = c->X; row = (size_t)B * H; rows = 2 * L + 1; stride = (size_t)MB * H; break;
+    case MK_DBG_QKV: src = c->QKV + (size_t)layer * MB * nqkv; row = (size_t)B * nqkv; rows = 1; break;
+    case MK_DBG_ATTN: src = c->ATT + (size_t)layer * MB * QD; row = (size_t)B * QD; rows = 1; break;
+    case MK_DBG_ROUTER: src = c->RLOG + (size_t)layer * MB * E; row = (size_t)B * E; rows = 1; break;
+    case MK_DBG_ROUTE_IDS: src = c->RIDS + (size_t)layer * MB * K; row = (size_t)B * K; rows = 1; tagged = false; break;
+    case MK_DBG_ROUTE_W: src = c->RW + (size_t)layer * MB * K; row = (size_t)B * K; rows = 1; tagged = false; break;
+    case MK_DBG_H: src = c->HB + (size_t)layer * MB * K * F; row = (size_t)B * K * F; rows = 1; break;
     default: return fail(MK_ERR_INVALID_ARG, "unknown buffer %d", what);
   }
-  if (bytes != row * rows) return fail(MK_ERR_INVALID_ARG, "bytes must be %zu", row * rows);
+  if (bytes != row * rows * 4) return fail(MK_ERR_INVALID_ARG, "bytes must be %zu", row * rows * 4);
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "sync");
-  if (rows == 1) e = cudaMemcpy(dst, src, row, cudaMemcpyDeviceToHost);
-  else e = cudaMemcpy2D(dst, row, src, stride, row, rows, cudaMemcpyDeviceToHost);
-  if (e != cudaSuccess) return cuda_fail(e, "debug read");
+  if (!tagged) {
+    e = cudaMemcpy(dst, src, row * 4, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "debug read");
+    return MK_OK;
+  }
+  std::vector<uint64_t> tmp(row);
+  uint32_t* out = static_cast<uint32_t*>(dst);
+  for (size_t r = 0; r < rows; ++r) {
+    e = cudaMemcpy(tmp.data(), static_cast<const uint64_t*>(src) + r * stride, row * 8, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "debug read");
+    for (size_t i = 0; i < row; ++i) out[r * row + i] = (uint32_t)tmp[i];
+  }
   return MK_OK;
 }
 
@@ -724,17 +729,19 @@ int mk_plan_attention(const mk_config* cfg, int32_t n_ctas, int32_t batch, const
 }
 
 // -------------------------------------------------------------------- CPU simulator
-// A model of the device runtime at tile granularity: per virtual SM, a producer
-// that turns tasks into tile records (claiming MoE queue items as it goes, at
-// most `lead` records ahead) and a consumer that runs records in order, honours
-// each record's counter wait and applies its counter effects (including the
-// "last arrival merges" rules of attention splits, routing and MoE row tiles).
+// A model of the device runtime at record granularity: per virtual SM, a producer
+// that turns tasks into records (at most `lead` ahead of its consumer; the MoE
+// records of a layer only once routing is published, split with the device's
+// rule) and a consumer that runs records in order, honours each record's counter
+// wait and applies its counter effects (including the "last arrival merges" rules
+// of attention splits and routing).
 int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t B, const int32_t* seq_lens, const int32_t* routing_ids,
                 uint64_t seed, int32_t lead, mk_sim_result* out) {
   g_err.clear();
   int rc = check_config(cfg);
   if (rc) return rc;
-  if (!out || !seq_lens || !routing_ids || n_ctas < 1 || B < 1 || B > cfg->max_batch || lead < 1)
+  if (!out || !seq_lens || !routing_ids || n_ctas < 1 || n_ctas > mk::kMaxCtas || B < 1 || B > cfg->max_batch ||
+      lead < 1)
     return fail(MK_ERR_INVALID_ARG, "bad arguments");
   std::memset(out, 0, sizeof *out);
   Plan plan;
@@ -745,26 +752,89 @@ int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t B, const int32_t* 
   const mk_plan_info& in = plan.info;
   const CounterMap& cm = plan.cm;
   const int L = cfg->num_layers, E = cfg->num_experts, K = cfg->top_k, Hkv = cfg->num_kv_heads;
+  const int F = cfg->expert_ffn, H = cfg->hidden;
   std::vector<uint32_t> ctr(cm.total, 0);
-  std::vector<int> nact(L, 0);
+  // per layer: active experts (ascending) and the gate/up unit range of every block
+  std::vector<std::vector<int>> act(L);
+  std::vector<std::vector<int32_t>> gu_start(L);
   for (int l = 0; l < L; ++l) {
-    std::vector<char> on(E, 0);
+    std::vector<int> cnt(E, 0);
     for (int b = 0; b < B; ++b)
       for (int j = 0; j < K; ++j) {
         const int e = routing_ids[((size_t)l * B + b) * K + j];
         if (e < 0 || e >= E) return fail(MK_ERR_INVALID_ARG, "routing id out of range");
-        on[e] = 1;
+        cnt[e]++;
       }
-    for (int e = 0; e < E; ++e) nact[l] += on[e];
+    std::vector<int64_t> cost, cum(1, 0);
+    for (int e = 0; e < E; ++e)
+      if (cnt[e]) {
+        act[l].push_back(e);
+        cost.push_back(mk::moe_unit_cost(cnt[e]));
+        cum.push_back(cum.back() + (int64_t)F * cost.back());
+      }
+    const int nact = (int)act[l].size();
+    for (int j = 0; j <= n_ctas; ++j) gu_start[l].push_back(mk::moe_gu_start(j, n_ctas, cum.data(), cost.data(), nact, F));
   }
-  std::vector<std::vector<int>> claims(L);
-  for (int l = 0; l < L; ++l) claims[l].assign((size_t)nact[l] * (in.n_ftiles + in.n_rtiles), 0);
+  // coverage of the MoE work: gate/up units and (active expert, hidden row) pairs of the down projection
+  std::vector<std::vector<int>> gu_seen(L), dn_seen(L);
+  for (int l = 0; l < L; ++l) {
+    gu_seen[l].assign(act[l].size() * F, 0);
+    dn_seen[l].assign(act[l].size() * H, 0);
+  }
 
-  struct Rec { int kind; int task; int layer; uint32_t a; uint32_t x; };   // kind: op, or 100 = gate/up, 101 = down
-  struct Sm { std::vector<Rec> q; size_t qhead = 0; int ti; bool prod_done = false; bool moe_active = false; bool done = false; };
+  // record kinds: a task op, or 100 = gate/up chunk, 101 = down chunk
+  struct Rec { int kind; int task; int layer; uint32_t a; uint32_t x; int flags; };
+  enum { F_FIRST = 1, F_LAST = 2, F_LAST_GU = 4 };
+  struct Sm {
+    std::vector<Rec> q; size_t qhead = 0; int ti;
+    std::vector<Rec> moe; size_t moe_next = 0; bool moe_open = false;
+    bool prod_done = false; bool done = false;
+  };
   std::vector<Sm> sm(n_ctas);
   for (int i = 0; i < n_ctas; ++i) sm[i].ti = plan.off[i];
   std::mt19937_64 rng(seed);
+  const int fpc = std::max(1, mk::gemv_rows_per_chunk(H) / 2);
+  const int rows_fit = std::max(1, mk::kSlotBytes / (F * 2));
+
+  // the MoE records block i produces for layer l (the device producer's loops)
+  auto moe_records = [&](int i, int l, int task) {
+    std::vector<Rec> r;
+    const int nact = (int)act[l].size();
+    const int u0 = gu_start[l][i], u1 = gu_start[l][i + 1];
+    if (u0 >= u1) r.push_back({100, task, l, 0, 0, F_FIRST | F_LAST | F_LAST_GU});
+    for (int u = u0; u < u1;) {
+      const int a = u / F, f0 = u % F, fend = std::min(F, u1 - a * F);
+      for (int f = f0; f < fend; f += fpc) {
+        const int n = std::min(fpc, fend - f);
+        for (int k = 0; k < n; ++k) gu_seen[l][(size_t)a * F + f + k]++;
+        r.push_back({100, task, l, (uint32_t)a, (uint32_t)f,
+                     (f == f0 ? F_FIRST : 0) | (f + n >= fend ? F_LAST : 0) | (a * F + fend >= u1 ? F_LAST_GU : 0)});
+      }
+      u = a * F + fend;
+    }
+    uint32_t r0, r1;
+    split_range((uint32_t)H, n_ctas, i, &r0, &r1);
+    if (r1 <= r0) {
+      r.push_back({101, task, l, 0, r0, F_FIRST | F_LAST});
+      return r;
+    }
+    const int rpc = std::min((int)(r1 - r0), rows_fit);
+    bool first = true;
+    for (int rb = (int)r0; rb < (int)r1; rb += rpc) {
+      const int nrc = std::min(rpc, (int)r1 - rb);
+      const int epc = std::max(1, mk::kSlotBytes / (nrc * F * 2));
+      for (int a = 0; a < nact; a += epc) {
+        const int ne = std::min(epc, nact - a);
+        for (int k = 0; k < ne; ++k)
+          for (int x = 0; x < nrc; ++x) dn_seen[l][(size_t)(a + k) * H + rb + x]++;
+        const bool last = rb + nrc >= (int)r1 && a + ne >= nact;
+        r.push_back({101, task, l, (uint32_t)a, (uint32_t)rb, (first ? F_FIRST : 0) | (last ? F_LAST : 0)});
+        first = false;
+      }
+    }
+    if (nact == 0) r.push_back({101, task, l, 0, r0, F_FIRST | F_LAST});
+    return r;
+  };
 
   auto target = [&](const mk_task& t) { return t.wait_base + t.wait_per_b * (uint32_t)B; };
   auto produce = [&](int i) -> bool {   // one record; false if blocked or finished
@@ -773,23 +843,22 @@ int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t B, const int32_t* 
     const mk_task& t = plan.tasks[s.ti];
     switch (t.op) {
       case MK_OP_ATTN:
-        for (int it = ioff[i]; it < ioff[i + 1]; ++it) s.q.push_back({MK_OP_ATTN, s.ti, t.layer, (uint32_t)it, 0});
+        for (int it = ioff[i]; it < ioff[i + 1]; ++it) s.q.push_back({MK_OP_ATTN, s.ti, t.layer, (uint32_t)it, 0, 0});
         break;
       case MK_OP_MOE: {
         const int l = t.layer;
-        if (ctr[cm.layer_base(l) + mk::L_RREADY] < 1) return false;
-        const uint32_t n_gu = (uint32_t)nact[l] * in.n_ftiles;
-        const uint32_t n_tot = n_gu + (uint32_t)nact[l] * in.n_rtiles;
-        const uint32_t qi = ctr[cm.layer_base(l) + mk::L_MOEQ]++;
-        if (qi < n_tot) {
-          claims[l][qi]++;
-          if (qi < n_gu) s.q.push_back({100, s.ti, l, qi / in.n_ftiles, qi % in.n_ftiles});
-          else s.q.push_back({101, s.ti, l, (qi - n_gu) / in.n_rtiles, (qi - n_gu) % in.n_rtiles});
-          return true;   // stay on this task
+        if (!s.moe_open) {
+          if (ctr[cm.layer_base(l) + mk::L_RREADY] < 1) return false;
+          s.moe = moe_records(i, l, s.ti);
+          s.moe_next = 0;
+          s.moe_open = true;
         }
+        s.q.push_back(s.moe[s.moe_next++]);
+        if (s.moe_next < s.moe.size()) return true;   // stay on this task
+        s.moe_open = false;
         break;
       }
-      default: s.q.push_back({t.op, s.ti, t.layer, 0, 0}); break;
+      default: s.q.push_back({t.op, s.ti, t.layer, 0, 0, 0}); break;
     }
     if (t.op == MK_OP_END) s.prod_done = true;
     else s.ti++;
@@ -809,12 +878,12 @@ int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t B, const int32_t* 
         if (++ctr[pc] == it.nsplit) ctr[base + mk::L_ATTN]++;
         break;
       }
-      case 100:
-        ctr[base + cm.gu_off + r.a]++;
+      case 100:   // the device signals once, at the end of the block's last gate/up run
+        if ((r.flags & F_LAST_GU) && (r.flags & F_LAST)) ctr[base + mk::L_GU]++;
         break;
       case 101:
-        if (ctr[base + cm.gu_off + r.a] < (uint32_t)in.n_ftiles) return false;
-        if (++ctr[base + cm.down_off + r.x] == (uint32_t)nact[r.layer]) ctr[base + mk::L_MOE]++;
+        if ((r.flags & F_FIRST) && ctr[base + mk::L_GU] < (uint32_t)n_ctas) return false;
+        if (r.flags & F_LAST) ctr[base + mk::L_MOE]++;
         break;
       case MK_OP_ROUTER:
         if (ctr[t.wait_ctr] < target(t)) return false;
@@ -858,15 +927,16 @@ int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t B, const int32_t* 
     const uint32_t base = cm.layer_base(l);
     ok = ctr[base + mk::L_QKV] == (uint32_t)in.n_qkv_tiles && ctr[base + mk::L_ATTN] == (uint32_t)(B * Hkv) &&
          ctr[base + mk::L_O] == (uint32_t)in.n_o_tiles && ctr[base + mk::L_RARR] == (uint32_t)in.n_router_tiles &&
-         ctr[base + mk::L_RREADY] == 1u && ctr[base + mk::L_MOE] == (uint32_t)in.n_rtiles;
-    for (int a = 0; a < nact[l] && ok; ++a) ok = ctr[base + cm.gu_off + a] == (uint32_t)in.n_ftiles;
-    for (int rt = 0; rt < in.n_rtiles && ok; ++rt) ok = ctr[base + cm.down_off + rt] == (uint32_t)nact[l];
+         ctr[base + mk::L_RREADY] == 1u && ctr[base + mk::L_GU] == (uint32_t)n_ctas &&
+         ctr[base + mk::L_MOE] == (uint32_t)n_ctas;
   }
   out->counters_ok = ok;
-  bool qok = true;
-  for (int l = 0; l < L; ++l)
-    for (int v : claims[l]) qok = qok && v == 1;
-  out->queue_items_ok = qok;
+  bool uok = true;
+  for (int l = 0; l < L; ++l) {
+    for (int v : gu_seen[l]) uok = uok && v == 1;
+    for (int v : dn_seen[l]) uok = uok && v == 1;
+  }
+  out->moe_units_ok = uok;
   return MK_OK;
 }
 

@@ -23,7 +23,7 @@ constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;
 
 // ---- shared-memory ring of weight / KV tiles --------------------------------
-constexpr int kSlots = 3;
+constexpr int kSlots = 2;
 constexpr int kSlotBytes = 65536;
 
 // ---- build limits --------------------------------------------------------------
@@ -33,10 +33,9 @@ constexpr int kMaxG = 8;          // query heads per KV head
 constexpr int kMaxExperts = 256;
 constexpr int kMaxK = 4096;       // GEMV input length (two 16-byte units per thread)
 constexpr int kMaxRowsPerChunk = 32;
+constexpr int kMaxCtas = 256;     // thread blocks (SMs) a step may use
+constexpr int kMoeScratch = 14336;  // floats of shared memory for the down projection of one block
 
-// ---- MoE work-queue tiles --------------------------------------------------------
-constexpr int kFTile = 16;        // expert FFN rows (gate+up pairs) per gate/up item
-constexpr int kRTile = 64;        // hidden rows per down item
 constexpr int kRouterRows = 8;    // router (expert) rows per router tile
 
 MK_HD int gemv_rows_per_chunk(int K) {
@@ -45,6 +44,29 @@ MK_HD int gemv_rows_per_chunk(int K) {
 }
 // pages of K (and as many of V) per attention chunk: K fills the slot's first half, V the second
 MK_HD int pages_per_chunk(int page_size, int head_dim) { return (kSlotBytes / 2) / (page_size * head_dim * 2); }
+
+// ---- MoE work split ---------------------------------------------------------------
+// Gate/up work of a layer is a list of units, one per FFN row f of each active expert a
+// (unit index a * F + f, active experts in ascending id).  A unit costs its weight
+// bytes plus the batch rows it serves: max(4, rows routed to the expert), so at small
+// batch every unit weighs the same and at large batch crowded experts count for more.
+// Block j takes the units whose cost prefix starts in [C*j/N, C*(j+1)/N), C the total.
+MK_HD int64_t moe_unit_cost(int routed_rows) { return routed_rows > 4 ? routed_rows : 4; }
+
+// first unit of block j of N; cum[a] = cost of the units of experts 0..a-1 (cum[nact] = C),
+// cost[a] = cost of one unit of expert a
+MK_HD int32_t moe_gu_start(int j, int N, const int64_t* cum, const int64_t* cost, int nact, int F) {
+  if (j <= 0 || nact <= 0) return 0;
+  if (j >= N) return nact * F;
+  const int64_t T = cum[nact] * j / N;
+  int lo = 0, hi = nact - 1;   // last a with cum[a] <= T
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cum[mid] <= T) lo = mid; else hi = mid - 1;
+  }
+  const int64_t f = (T - cum[lo] + cost[lo] - 1) / cost[lo];
+  return f >= F ? (lo + 1) * F : lo * F + (int32_t)f;
+}
 
 // ---- counters --------------------------------------------------------------------
 // global
@@ -56,24 +78,20 @@ enum : uint32_t {
   L_O = 2,       // O-proj tiles done
   L_RARR = 3,    // router tiles arrived
   L_RREADY = 4,  // routing published (0/1)
-  L_MOEQ = 5,    // MoE queue head (claims)
-  L_MOE = 6,     // down row-tiles combined into the residual
-  L_PAIR = 8     // [max_batch * Hkv] attention split arrivals, then GU_DONE[E], then DOWN_ARRIVE[n_rtiles]
+  L_GU = 5,      // blocks done with their gate/up units
+  L_MOE = 6,     // blocks done with their down rows (residual written)
+  L_PAIR = 8     // [max_batch * Hkv] attention split arrivals
 };
 
 struct CounterMap {
   uint32_t layer_stride;
-  uint32_t gu_off;     // offset of GU_DONE[active expert] inside a layer block
-  uint32_t down_off;   // offset of DOWN_ARRIVE[row tile]
   uint32_t total;
   MK_HD uint32_t layer_base(int l) const { return C_GLOBAL + (uint32_t)l * layer_stride; }
 };
 
-inline CounterMap counter_map(int layers, int max_batch, int n_kv, int n_exp, int n_rtiles) {
+inline CounterMap counter_map(int layers, int max_batch, int n_kv) {
   CounterMap m;
-  m.gu_off = L_PAIR + (uint32_t)(max_batch * n_kv);
-  m.down_off = m.gu_off + (uint32_t)n_exp;
-  m.layer_stride = (m.down_off + (uint32_t)n_rtiles + 7u) & ~7u;
+  m.layer_stride = (L_PAIR + (uint32_t)(max_batch * n_kv) + 7u) & ~7u;
   m.total = C_GLOBAL + (uint32_t)layers * m.layer_stride;
   return m;
 }
@@ -99,9 +117,9 @@ struct alignas(64) Params {
   int32_t nqkv;          // (Hq + 2Hkv) * D
   int32_t norm_topk;
   float eps, scale;      // RMSNorm epsilon, 1/sqrt(D)
-  int32_t B, max_batch, n_ctas;
+  int32_t B, max_batch, n_ctas, max_items;
   // static plan
-  int32_t n_qkv_tiles, n_o_tiles, n_router_tiles, n_ftiles, n_rtiles;
+  int32_t n_qkv_tiles, n_o_tiles, n_router_tiles;
   CounterMap cm;
   uint64_t watchdog_ns;
   const mk_task* tasks;
@@ -123,23 +141,23 @@ struct alignas(64) Params {
   const mk_attn_item* items;    // [n_items]
   const int32_t* item_off;      // [n_ctas + 1]
   const int32_t* pair_first;    // [B * Hkv] first item of each (row, kv head)
-  // workspace
-  float* X;        // [2L+1][max_batch][H] residual stream: layer input at 2l, after attention at 2l+1
-  float* QKV;      // [L][max_batch][nqkv]
-  float* ATT;      // [L][max_batch][Hq*D]
-  float* PO;       // [max_items][G][D]   attention split partial outputs (reused by every layer)
-  float* PML;      // [max_items][G][2]   their (max, sum)
-  float* RLOG;     // [L][max_batch][E]
-  int32_t* RIDS;   // [L][max_batch][K]
-  float* RW;       // [L][max_batch][K]
-  int32_t* ACT;    // [L][E]  active experts in ascending id
-  int32_t* NACT;   // [L]
-  int32_t* TOK;    // [L][E][max_batch]  (row << 8 | slot) of the rows routed to each expert
-  int32_t* CNT;    // [L][E]
-  float* HB;       // [L][max_batch][K][F] SwiGLU activations per (row, slot)
-  float* PART;     // [L][max_batch][K][H] down-projection output per (row, slot)
-  float* SS;       // [2L+1][n_ss_slots][max_batch] per-tile sums of squares of the residual stream
+  // workspace.  Every value one block writes and another reads is a tagged 8-byte word:
+  // the fp32 (or int32) value in the low half and the step's tag in the high half, written
+  // with one 64-bit store.  A reader that sees the current tag has the value of this step;
+  // no fence is needed between writer and reader.
+  uint32_t tag;        // this step's tag (never 0)
+  int32_t stall_layer; // test hook: the O-proj of this layer waits for a tag that never comes (-1: off)
+  uint64_t* X;     // [2L+1][max_batch][H] residual stream: layer input at 2l, after attention at 2l+1
+  uint64_t* QKV;   // [L][max_batch][nqkv]
+  uint64_t* ATT;   // [L][max_batch][Hq*D]
+  uint64_t* PO;    // [L][max_items][G][D]   attention split partial outputs
+  uint64_t* PML;   // [L][max_items][G][2]   their (max, sum)
+  uint64_t* RLOG;  // [L][max_batch][E] router logits (+ bias)
+  uint64_t* HB;    // [L][max_batch][K][F] SwiGLU activations per (row, slot)
+  uint64_t* SS;    // [2L+1][n_ss_slots][max_batch] per-block sums of squares of the residual stream
   int32_t n_ss_slots;
+  int32_t* RIDS;   // [L][max_batch][K] routing ids (copy kept by block 0 for inspection)
+  float* RW;       // [L][max_batch][K] combine weights (same)
   uint32_t* ctr;   // [cm.total]
   mk_status* status;
   // optional timeline: per block `trace_cap` events of 4 x u64 (start, dependency met, end, tag);

@@ -116,7 +116,7 @@ def test_static_plan_covers_every_row_once():
     _check_static_plan(_cfg(), 7)
     info = _check_static_plan(mk.make_config(W.MOE30B, 16, 1000, 64, 600), N_CTAS)
     assert info.n_qkv_tiles == N_CTAS and info.n_router_tiles == 16   # 8 expert rows per router tile
-    assert info.n_ftiles == 48 and info.n_rtiles == 32
+    assert info.n_down_ranges == N_CTAS
 
 
 @pytest.mark.parametrize("lens", [[65], [1], [16], [17], [512, 1, 33, 200, 16, 15, 100, 7], [8193],
@@ -167,7 +167,7 @@ def test_simulated_step_completes_tiny(seed):
     lens = [65, 1, 300, 17, 16, 512, 2, 90][: 1 + seed % 8]
     r = mk.simulate(cfg, N_CTAS if seed % 2 else 5, lens, _random_routing(cfg, len(lens), seed), seed=seed,
                     lead=1 + seed % 6)
-    assert r.finished and not r.deadlocked and r.counters_ok and r.queue_items_ok
+    assert r.finished and not r.deadlocked and r.counters_ok and r.moe_units_ok
 
 
 def test_simulated_step_completes_30b_shapes():
@@ -175,8 +175,8 @@ def test_simulated_step_completes_30b_shapes():
     for B, seed in ((1, 1), (64, 2)):
         lens = W.lengths_loguniform(B, 512, 32768) if B > 1 else [8193]
         r = mk.simulate(cfg, N_CTAS, lens, _random_routing(cfg, B, seed), seed=seed, lead=6)
-        assert r.finished and not r.deadlocked and r.counters_ok and r.queue_items_ok
-        # every MoE item and every attention item ran
+        assert r.finished and not r.deadlocked and r.counters_ok and r.moe_units_ok
+        # every attention item ran
         assert r.tiles_run[3] == len(mk.plan_attention(cfg, N_CTAS, lens)[0]) * cfg.num_layers
 
 
