@@ -226,6 +226,22 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// Two warp sums at once (a[tb] and b[tb] for every tb): afterwards lanes 0-15 hold the sums
+// of a and lanes 16-31 the sums of b.  Five shuffles per tb instead of ten.
+template <int TB>
+__device__ __forceinline__ void warp_sum2(float (&a)[TB], const float (&b)[TB]) {
+  const bool hi = (threadIdx.x & 16) != 0;
+#pragma unroll
+  for (int tb = 0; tb < TB; ++tb) {
+    float keep = hi ? b[tb] : a[tb];
+    const float send = hi ? a[tb] : b[tb];
+    keep += __shfl_xor_sync(0xffffffffu, send, 16);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) keep += __shfl_xor_sync(0xffffffffu, keep, o);
+    a[tb] = keep;
+  }
+}
+
 // --------------------------------------------------------------------------- shared memory
 enum : uint8_t { R_EMBED = 1, R_GEMV = 2, R_ATTN = 3, R_GU = 4, R_DOWN = 5, R_END = 6, R_ROUTE = 7, R_COMBINE = 8 };
 // GEMV stream kinds beyond the task ops (MK_OP_QKV / OPROJ / ROUTER / HEAD)
@@ -1102,7 +1118,7 @@ struct Consumer {
   // Stage the GEMV input of rows rb[0..nt) once per block in shared memory (S.moe, [nt][K]
   // fp32, RMS-normalised for the kinds that have a norm), so that the block reads each
   // tagged input word once instead of once per warp.
-  __device__ bool stage_input(int kind, int l, int K, const int (&rb)[TB], int nt, uint32_t tag) {
+  __device__ __noinline__ bool stage_input(int kind, int l, int K, const int (&rb)[TB], int nt, uint32_t tag) {
     const uint16_t* g = nullptr;
     int xidx = 0;
     if (kind == 0) { g = p.layers[l].attn_norm; xidx = 2 * l; }
@@ -1116,6 +1132,16 @@ struct Consumer {
     }
     float* dst = S.moe;
     cbar();   // the previous group's input has been read
+    // the row's per-block sums of squares are requested first, so they travel with the input
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool do_ss = g != nullptr && warp < nt;
+    const uint64_t* ssb = p.SS + static_cast<size_t>(xidx) * p.n_ss_slots * p.max_batch + rb[warp < TB ? warp : 0];
+    uint64_t ssw[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int i = lane + 32 * k;
+      ssw[k] = (do_ss && i < p.n_ss_slots) ? ll_ld(ssb + static_cast<size_t>(i) * p.max_batch) : ll_pack(0.f, tag);
+    }
     const uint64_t* s0 = src[0];
     const uint64_t* s1 = src[TB > 1 ? 1 : 0];
     const uint64_t* s2 = src[TB > 2 ? 2 : 0];
@@ -1125,12 +1151,15 @@ struct Consumer {
       return (tb == 0 ? s0 : tb == 1 ? s1 : tb == 2 ? s2 : s3) + k;
     }, dst, tag);
     if (g != nullptr) {
-      const int warp = threadIdx.x >> 5;
-      if (warp < nt) {
+      if (do_ss) {
         float v[8];
-        ok = ss_fetch(p, xidx, rb[warp < TB ? warp : 0], v) && ok;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (lane + 32 * k < p.n_ss_slots) LL_FIX(ssw[k], ssb + static_cast<size_t>(lane + 32 * k) * p.max_batch, tag, 0, -1, ok);
+          v[k] = ll_f(ssw[k]);
+        }
         const float r = ss_rstd(p, v);
-        if ((threadIdx.x & 31) == 0) S.rstd[warp] = r;
+        if (lane == 0) S.rstd[warp] = r;
       }
       cbar();
       for (int i = threadIdx.x * 4; i < nt * K; i += kConsumerThreads * 4) {
@@ -1228,6 +1257,34 @@ struct Consumer {
         const int b0 = g * TB;
         const int nt = min(TB, cnt - b0);
         if (kGroups && ngroups > 1) ok = stream_load(sg, moe, kind, l, b0, nt, tag, eop, rb, rj, y) && ok;
+        if (sg.S == 1 && om.resid == nullptr) {
+          // whole rows per warp, two dot products in flight and one paired reduction:
+          // gate/up: the row's gate and up; otherwise rows r and r + RPG
+          const int step = gu ? sg.RPG : 2 * sg.RPG;
+          for (int r = sg.rg; r < n; r += step) {
+            const int r2 = gu ? n + r : r + sg.RPG;
+            float a[TB], b[TB];
+#pragma unroll
+            for (int tb = 0; tb < TB; ++tb) { a[tb] = 0.f; b[tb] = 0.f; }
+            row_dot<TB>(wsm + static_cast<size_t>(r) * K * 2, sg, y, a);
+            if (gu || r2 < n) row_dot<TB>(wsm + static_cast<size_t>(r2) * K * 2, sg, y, b);
+            warp_sum2<TB>(a, b);
+            if (gu) {
+              float up[TB];
+#pragma unroll
+              for (int tb = 0; tb < TB; ++tb) up[tb] = __shfl_xor_sync(0xffffffffu, a[tb], 16);
+              if (lane < nt)
+                put(om, true, row0 + r, pick_i<TB>(rb, lane), pick_i<TB>(rj, lane), pick<TB>(a, lane),
+                    pick<TB>(up, lane), my_ss);
+            } else {
+              const int tb = lane & 15;
+              const int rr = lane < 16 ? r : r2;
+              if (tb < nt && rr < n)
+                put(om, false, row0 + rr, pick_i<TB>(rb, tb), pick_i<TB>(rj, tb), pick<TB>(a, tb), 0.f, my_ss);
+            }
+          }
+          continue;
+        }
         for (int r = sg.rg; r < n; r += sg.RPG) {
           float acc[TB], acc2[TB];
 #pragma unroll
@@ -1373,6 +1430,7 @@ struct Consumer {
       }
     }
     cbar();
+    trace_mark(18, l);
     for (int b = threadIdx.x; b < B; b += kConsumerThreads) {
       float sum = 0.f;
       for (int j = 0; j < K; ++j) sum += expf(S.rval[b * K + j] - S.rmax[b]);
@@ -1415,6 +1473,7 @@ struct Consumer {
       if (lane == 0) S.ecum[0] = 0;
     }
     cbar();
+    trace_mark(19, l);
     for (int i = threadIdx.x; i < B * K; i += kConsumerThreads) {
       const int b = i / K;
       const float ex = expf(S.rval[i] - S.rmax[b]);
@@ -1463,6 +1522,14 @@ struct Consumer {
     const int xidx = 2 * l + 1;
     float* yc = S.scr.attn;
     const uint64_t* x0 = xrow(xidx, 0);
+    const uint16_t* g = p.layers[l].ffn_norm;
+    constexpr int kGainRegs = (kAttnScratch / 4 + kConsumerThreads - 1) / kConsumerThreads;
+    uint2 gw[kGainRegs];
+#pragma unroll
+    for (int k = 0; k < kGainRegs; ++k) {
+      const int i = (threadIdx.x + k * kConsumerThreads) * 4;
+      gw[k] = i < B * H ? __ldg(reinterpret_cast<const uint2*>(g + (i % H))) : make_uint2(0u, 0u);
+    }
     bool ok = ll_gather(p, B * H, [=](int i) { return x0 + i; }, yc, p.tag);   // rows of the batch are contiguous in X
     if (warp < B) {
       float v[8];
@@ -1471,15 +1538,16 @@ struct Consumer {
       if ((threadIdx.x & 31) == 0) S.rstd[warp] = r;
     }
     cbar();
-    const uint16_t* g = p.layers[l].ffn_norm;
-    for (int i = threadIdx.x * 4; i < B * H; i += kConsumerThreads * 4) {
-      const int k = i % H;
-      const float r = S.rstd[i / H];
-      const uint2 gw = __ldg(reinterpret_cast<const uint2*>(g + k));
-      yc[i] = (yc[i] * r) * bf_lo(gw.x);
-      yc[i + 1] = (yc[i + 1] * r) * bf_hi(gw.x);
-      yc[i + 2] = (yc[i + 2] * r) * bf_lo(gw.y);
-      yc[i + 3] = (yc[i + 3] * r) * bf_hi(gw.y);
+#pragma unroll
+    for (int k = 0; k < kGainRegs; ++k) {
+      const int i = (threadIdx.x + k * kConsumerThreads) * 4;
+      if (i < B * H) {
+        const float r = S.rstd[i / H];
+        yc[i] = (yc[i] * r) * bf_lo(gw[k].x);
+        yc[i + 1] = (yc[i + 1] * r) * bf_hi(gw[k].x);
+        yc[i + 2] = (yc[i + 2] * r) * bf_lo(gw[k].y);
+        yc[i + 3] = (yc[i + 3] * r) * bf_hi(gw[k].y);
+      }
     }
     return ok;
   }
@@ -1627,17 +1695,20 @@ struct Consumer {
           const int nt = min(TD, cnt - g0);
           float y[8 / TD][8][TD];
           ok = load_h_pairs<TD>(sg, l, hc, wl + g0, nt, y) && ok;
-          for (int ii = i; ii < iend; ++ii) {
-            float acc[TD];
+          for (int ii = i; ii < iend; ii += 2) {
+            // two rows in flight, one paired reduction (lanes 0-15: row ii, 16-31: row ii+1)
+            float a[TD], b[TD];
 #pragma unroll
-            for (int tb = 0; tb < TD; ++tb) acc[tb] = 0.f;
-            row_dot<TD>(wsm + static_cast<size_t>(ii) * F * 2, sg, y, acc);
-#pragma unroll
-            for (int tb = 0; tb < TD; ++tb) acc[tb] = warp_sum(acc[tb]);
-            if (lane < nt) {
-              const int pi = wl[g0 + lane];
-              const int r = rb0 + (ii - ai * nrc) - r0;
-              P[pi * nrow + r] = S.rwcache[pi] * pick<TD>(acc, lane);
+            for (int tb = 0; tb < TD; ++tb) { a[tb] = 0.f; b[tb] = 0.f; }
+            row_dot<TD>(wsm + static_cast<size_t>(ii) * F * 2, sg, y, a);
+            if (ii + 1 < iend) row_dot<TD>(wsm + static_cast<size_t>(ii + 1) * F * 2, sg, y, b);
+            warp_sum2<TD>(a, b);
+            const int tb = lane & 15;
+            const int row = lane < 16 ? ii : ii + 1;
+            if (tb < nt && row < iend) {
+              const int pi = wl[g0 + tb];
+              const int r = rb0 + (row - ai * nrc) - r0;
+              P[pi * nrow + r] = S.rwcache[pi] * pick<TD>(a, tb);
             }
           }
         }
@@ -1951,8 +2022,6 @@ struct Consumer {
     const int GD = Gq * D;
     const int cta = blockIdx.x;
     twait = globaltimer();
-    float* wts = S.moe;                   // [n][G]: exp(m_s - M) / L per split and head
-    float* part = S.moe + kMaxCtas * kMaxG;   // [n][slice]: weighted partial outputs
     bool ok = true;
     for (int it = p.item_off[cta]; it < p.item_off[cta + 1]; ++it) {
       const mk_attn_item item = p.items[it];
@@ -1961,48 +2030,44 @@ struct Consumer {
       const int o0 = item.split * GD / ns, o1 = (item.split + 1) * GD / ns, nsl = o1 - o0;
       const uint64_t* pml = p.PML + (static_cast<size_t>(l) * p.max_items + first) * (2 * kMaxG);
       const uint64_t* po = p.PO + (static_cast<size_t>(l) * p.max_items + first) * (kMaxG * D);
-      // (max, sum) of every split and head
-      ok = ll_gather(p, ns * Gq, [=](int i) { return pml + static_cast<size_t>(i / Gq) * 2 * kMaxG + 2 * (i % Gq); },
-                     wts, p.tag) && ok;
-      ok = ll_gather(p, ns * Gq,
-                     [=](int i) { return pml + static_cast<size_t>(i / Gq) * 2 * kMaxG + 2 * (i % Gq) + 1; }, part,
-                     p.tag) && ok;
+      // one batch of loads: (max, sum) of every split and head, then the slice of every split
+      const int nml = 2 * ns * Gq;
+      const float* ml = S.moe;                  // [ns][G][2]
+      const float* part = S.moe + nml;          // [ns][nsl]
+      ok = ll_gather(p, nml + ns * nsl, [=](int i) {
+        if (i < nml) {
+          const int sp = i / (2 * Gq), r = i - sp * 2 * Gq;
+          return pml + static_cast<size_t>(sp) * 2 * kMaxG + r;
+        }
+        const int j = i - nml, sp = j / nsl;
+        return po + static_cast<size_t>(sp) * kMaxG * D + o0 + (j - sp * nsl);
+      }, S.moe + 0, p.tag) && ok;
       if (!ok) ll_timeout(p, MK_OP_ATTN, l);
       if (!cbar_and(ok)) return false;
       if (threadIdx.x < Gq) {
         const int h = threadIdx.x;
         float M = -INFINITY;
-        for (int sp = 0; sp < ns; ++sp) M = fmaxf(M, wts[sp * Gq + h]);
+        for (int sp = 0; sp < ns; ++sp) M = fmaxf(M, ml[(sp * Gq + h) * 2]);
         float L = 0.f;
         for (int sp = 0; sp < ns; ++sp) {
-          const float m = wts[sp * Gq + h];
-          L += (m == -INFINITY ? 0.f : __expf(m - M)) * part[sp * Gq + h];
+          const float m = ml[(sp * Gq + h) * 2];
+          L += (m == -INFINITY ? 0.f : __expf(m - M)) * ml[(sp * Gq + h) * 2 + 1];
         }
         S.rmax[h] = M;
         S.rz[h] = L;
       }
       cbar();
-      for (int i = threadIdx.x; i < ns * Gq; i += kConsumerThreads) {
-        const int h = i % Gq;
-        const float m = wts[i];
-        wts[i] = (m == -INFINITY ? 0.f : __expf(m - S.rmax[h])) / S.rz[h];
-      }
-      cbar();
-      // partial outputs of the slice from every split, then weighted in place
-      ok = ll_gather(p, ns * nsl, [=](int i) { return po + static_cast<size_t>(i / nsl) * kMaxG * D + o0 + i % nsl; },
-                     part, p.tag) && ok;
-      for (int i = threadIdx.x; i < ns * nsl; i += kConsumerThreads) {
-        const int sp = i / nsl;
-        part[i] *= wts[sp * Gq + (o0 + (i - sp * nsl)) / D];
-      }
-      if (!ok) ll_timeout(p, MK_OP_ATTN, l);
-      if (!cbar_and(ok)) return false;
       uint64_t* att = p.ATT + (static_cast<size_t>(l) * p.max_batch + item.b) * (p.Hq * D) +
                       static_cast<size_t>(item.kvh) * GD;
       for (int oi = threadIdx.x; oi < nsl; oi += kConsumerThreads) {
+        const int h = (o0 + oi) / D;
+        const float M = S.rmax[h], invL = 1.f / S.rz[h];
         float acc = 0.f;
-        for (int sp = 0; sp < ns; ++sp) acc += part[sp * nsl + oi];
-        ll_st(att + o0 + oi, acc, p.tag);
+        for (int sp = 0; sp < ns; ++sp) {
+          const float m = ml[(sp * Gq + h) * 2];
+          acc += (m == -INFINITY ? 0.f : __expf(m - M)) * part[sp * nsl + oi];
+        }
+        ll_st(att + o0 + oi, acc * invL, p.tag);
       }
       cbar();
     }
@@ -2067,15 +2132,35 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     fence_mbar_init();
   }
   __syncthreads();
+  {
+    // every block warms a slice of the small per-layer vectors (norm gains) in L2, so that
+    // their first read in a layer is an L2 hit rather than a DRAM access behind the stream
+    const int n_lines = (2 * p.L + 1) * ((p.H * 2 + 127) / 128);
+    for (int i = blockIdx.x * kThreads + tid; i < n_lines; i += gridDim.x * kThreads) {
+      const int lines_per = (p.H * 2 + 127) / 128;
+      const int v = i / lines_per, ln = i - v * lines_per;
+      const uint16_t* base = v == 2 * p.L ? p.final_norm : (v & 1) ? p.layers[v >> 1].ffn_norm : p.layers[v >> 1].attn_norm;
+      asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(reinterpret_cast<const uint8_t*>(base) + ln * 128));
+    }
+  }
   if (tid >= kConsumerThreads) {
+    // producer warpgroup: one thread streams, the rest only lend their registers
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
     if (tid == kConsumerThreads) {
       Producer prod(p, S);
       prod.run();
     }
     __syncwarp();
+    asm volatile("bar.sync 12, 128;" ::: "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kLaunchRegs));
   } else {
-    Consumer<TB, D> cons(p, S);
-    cons.run();
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
+    {
+      Consumer<TB, D> cons(p, S);
+      cons.run();
+    }
+    asm volatile("bar.sync %0, 128;" ::"r"(10 + (tid >> 7)) : "memory");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kLaunchRegs));
   }
   __syncthreads();
   // an aborted step may leave copies in flight: let them land before the block exits

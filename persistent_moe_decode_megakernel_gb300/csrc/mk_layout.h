@@ -17,10 +17,17 @@
 
 namespace mk {
 
-// ---- thread block shape: 8 consumer warps + 1 producer warp ---------------
+// ---- thread block shape: two consumer warpgroups + one producer warpgroup -------
+// (one producer thread issues the copies; the producer warpgroup hands most of its
+// registers to the consumers: 256 x kConsumerRegs + 128 x kProducerRegs = 384 x 168)
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kThreads = kConsumerThreads + 32;
+constexpr int kThreads = kConsumerThreads + 128;
+constexpr int kLaunchRegs = 168;
+constexpr int kConsumerRegs = 224;
+constexpr int kProducerRegs = 56;
+static_assert(kConsumerThreads * kConsumerRegs + 128 * kProducerRegs == kThreads * kLaunchRegs,
+              "register hand-over must add up to the launch allocation");
 
 // ---- shared-memory ring of weight / KV tiles --------------------------------
 constexpr int kSlots = 2;
