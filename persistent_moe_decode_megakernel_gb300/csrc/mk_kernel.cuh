@@ -284,8 +284,8 @@ struct __align__(128) Smem {
   int32_t wlist[kConsumerWarps][kMaxBatch];   // per warp: (row, slot) pairs routed to one expert
   int32_t elist[kMaxBatch];               // gate/up run: (row, slot) pairs routed to its expert
   int32_t eact[kMaxExperts];              // this layer's active experts, ascending
-  int64_t ecost[kMaxExperts];             // cost of one gate/up unit of each, and the cost prefix
-  int64_t ecum[kMaxExperts + 1];
+  int32_t ecost[kMaxExperts];             // cost of one gate/up unit of each, and the cost prefix
+  int32_t ecum[kMaxExperts + 1];
   int32_t nact;
   int32_t gu_lo, gu_hi;                   // this block's gate/up units
   uint64_t route_bar;                     // consumers -> producer: routing of the layer is in shared memory
@@ -1231,17 +1231,21 @@ struct Consumer {
     const uint32_t tag = (op == MK_OP_OPROJ && l == p.stall_layer) ? (p.tag ^ 0x80000000u) : p.tag;
     const int eop = gu ? MK_OP_MOE : op;
     trace_mark(10 + (op == MK_OP_ROUTER ? 0 : moe ? 20 : 40), l);
-    const int cnt = moe ? expert_pairs(e) : B;
+    // Gate/up with the whole batch in one register group and the MoE input cached: y is the
+    // same for every expert, so all of this block's runs (one per expert) form one tile and
+    // only the routing slots change between runs.
+    const bool gu_fused = gu && B <= TB && S.ykey == l;
+    const int cnt = gu_fused ? B : moe ? expert_pairs(e) : B;
     const int ngroups = kGroups ? (cnt + TB - 1) / TB : 1;
     const OutMap om = out_map(op, l);
     float my_ss = 0.f;    // O-proj: sum of squares of the residual values this lane wrote
     int rb[TB], rj[TB];
     float y[8 / TB][8][TB];
     bool ok = true;
-    const bool cached = gu && B <= TB && S.ykey == l;
-    if (cached) {
-      expert_rows(0, cnt, rb, rj);
-      load_y_smem(sg, rb, cnt, y);
+    if (gu_fused) {
+#pragma unroll
+      for (int tb = 0; tb < TB; ++tb) { rb[tb] = tb; rj[tb] = tb < B ? slot_of(tb, e) : -1; }
+      load_y_smem(sg, rb, B, y);
     } else {
       ok = stream_load(sg, moe, kind, l, 0, min(cnt, TB), tag, eop, rb, rj, y);
     }
@@ -1334,8 +1338,13 @@ struct Consumer {
         }
       }
       if (!ok) { wok = false; break; }
-      if (last) break;
+      if (last && (!gu_fused || (meta().aux & 1u))) break;
       if (!next_rec()) break;
+      if (last) {   // the next gate/up run of this block: its expert's slots
+        const int e2 = static_cast<int>(meta().e);
+#pragma unroll
+        for (int tb = 0; tb < TB; ++tb) rj[tb] = tb < B ? slot_of(tb, e2) : -1;
+      }
     }
     if (!ok) ll_timeout(p, eop, l);
     if (!cbar_and(wok && ok)) return false;
@@ -1413,15 +1422,15 @@ struct Consumer {
 #pragma unroll 4
         for (; e2 < E; e2 += 4) {
           const float4 q = *reinterpret_cast<const float4*>(row + e2);
-          rank += (q.x > v) || (q.x == v && e2 < e);
-          rank += (q.y > v) || (q.y == v && e2 + 1 < e);
-          rank += (q.z > v) || (q.z == v && e2 + 2 < e);
-          rank += (q.w > v) || (q.w == v && e2 + 3 < e);
+          rank += static_cast<int>(q.x > v) + (static_cast<int>(q.x == v) & static_cast<int>(e2 < e));
+          rank += static_cast<int>(q.y > v) + (static_cast<int>(q.y == v) & static_cast<int>(e2 + 1 < e));
+          rank += static_cast<int>(q.z > v) + (static_cast<int>(q.z == v) & static_cast<int>(e2 + 2 < e));
+          rank += static_cast<int>(q.w > v) + (static_cast<int>(q.w == v) & static_cast<int>(e2 + 3 < e));
         }
       }
       for (; e2 < E; ++e2) {
         const float v2 = row[e2];
-        rank += (v2 > v) || (v2 == v && e2 < e);
+        rank += static_cast<int>(v2 > v) + (static_cast<int>(v2 == v) & static_cast<int>(e2 < e));
       }
       if (rank < K) {
         S.rids[b * K + rank] = e;
@@ -1448,23 +1457,23 @@ struct Consumer {
       if (lane == 0) S.nact = nact;
       __syncwarp();
       // cost prefix of the gate/up units over the active experts (8 experts per lane, then a warp scan)
-      int64_t loc[kMaxExperts / 32];
-      int64_t run = 0;
+      int32_t loc[kMaxExperts / 32];
+      int32_t run = 0;
 #pragma unroll
       for (int k = 0; k < kMaxExperts / 32; ++k) {
         const int a = lane * (kMaxExperts / 32) + k;
-        const int64_t cst = a < nact ? moe_unit_cost(S.ecnt[S.eact[a]]) : 0;
+        const int32_t cst = a < nact ? moe_unit_cost(S.ecnt[S.eact[a]]) : 0;
         if (a < nact) S.ecost[a] = cst;
         run += cst * p.F;
         loc[k] = run;
       }
-      int64_t x = run;
+      int32_t x = run;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+        const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
         if (lane >= o) x += y;
       }
-      const int64_t before = x - run;
+      const int32_t before = x - run;
 #pragma unroll
       for (int k = 0; k < kMaxExperts / 32; ++k) {
         const int a = lane * (kMaxExperts / 32) + k;
@@ -1570,6 +1579,14 @@ struct Consumer {
         y[j][4][tb] = b.x; y[j][5][tb] = b.y; y[j][6][tb] = b.z; y[j][7][tb] = b.w;
       }
     }
+  }
+
+  // routing slot of expert e in batch row b, or -1
+  __device__ __forceinline__ int slot_of(int b, int e) const {
+    int s = -1;
+    for (int j = 0; j < p.K; ++j)
+      if (S.rcache[b * p.K + j] == e) s = j;
+    return s;
   }
 
   // pairs b0 .. b0+nt-1 of the current expert's list: (row, slot); slot -1 past the end

@@ -58,20 +58,21 @@ MK_HD int pages_per_chunk(int page_size, int head_dim) { return (kSlotBytes / 2)
 // bytes plus the batch rows it serves: max(4, rows routed to the expert), so at small
 // batch every unit weighs the same and at large batch crowded experts count for more.
 // Block j takes the units whose cost prefix starts in [C*j/N, C*(j+1)/N), C the total.
-MK_HD int64_t moe_unit_cost(int routed_rows) { return routed_rows > 4 ? routed_rows : 4; }
+MK_HD int32_t moe_unit_cost(int routed_rows) { return routed_rows > 4 ? routed_rows : 4; }
 
-// first unit of block j of N; cum[a] = cost of the units of experts 0..a-1 (cum[nact] = C),
-// cost[a] = cost of one unit of expert a
-MK_HD int32_t moe_gu_start(int j, int N, const int64_t* cum, const int64_t* cost, int nact, int F) {
+// first unit of block j of N; cum[a] = cost of the units of experts 0..a-1 (cum[nact] = C,
+// at most 256 experts x 1024 rows x 64 = 2^24), cost[a] = cost of one unit of expert a
+template <class I>
+MK_HD int32_t moe_gu_start(int j, int N, const I* cum, const I* cost, int nact, int F) {
   if (j <= 0 || nact <= 0) return 0;
   if (j >= N) return nact * F;
-  const int64_t T = cum[nact] * j / N;
+  const int64_t T = static_cast<int64_t>(static_cast<uint64_t>(cum[nact]) * static_cast<uint32_t>(j) / static_cast<uint32_t>(N));
   int lo = 0, hi = nact - 1;   // last a with cum[a] <= T
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (cum[mid] <= T) lo = mid; else hi = mid - 1;
   }
-  const int64_t f = (T - cum[lo] + cost[lo] - 1) / cost[lo];
+  const int64_t f = (T - static_cast<int64_t>(cum[lo]) + cost[lo] - 1) / cost[lo];
   return f >= F ? (lo + 1) * F : lo * F + (int32_t)f;
 }
 
