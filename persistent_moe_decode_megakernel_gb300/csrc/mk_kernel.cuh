@@ -117,6 +117,10 @@ __device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uin
   hi = *reinterpret_cast<const uint32_t*>(&h);
   lo = *reinterpret_cast<const uint32_t*>(&r);
 }
+// L2 prefetch of a contiguous byte range (16-byte aligned, size a multiple of 16)
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
@@ -461,6 +465,45 @@ struct Producer {
   uint64_t pol;
   __device__ Producer(const Params& p_, Smem& S_) : p(p_), S(S_) { pol = policy_evict_first(); }
 
+  // Warm L2 with (at most kPrefetchBytes of) a task's weights or KV pages, so that the ring's
+  // copies of a phase that starts after a dependency wait come from L2.
+  static constexpr uint32_t kPrefetchBytes = 256u * 1024u;
+  __device__ void prefetch_task(const mk_task& t) {
+    switch (t.op) {
+      case MK_OP_QKV:
+      case MK_OP_OPROJ:
+      case MK_OP_ROUTER:
+      case MK_OP_HEAD: {
+        const LayerW& lw = p.layers[t.op == MK_OP_HEAD ? 0 : t.layer];
+        const uint16_t* W = t.op == MK_OP_QKV ? lw.w_qkv : t.op == MK_OP_OPROJ ? lw.w_o
+                          : t.op == MK_OP_ROUTER ? lw.w_router : p.lm_head;
+        const int K = t.op == MK_OP_OPROJ ? p.Hq * p.D : p.H;
+        const uint64_t bytes = static_cast<uint64_t>(t.hi - t.lo) * K * 2u;
+        prefetch_l2(W + static_cast<size_t>(t.lo) * K, static_cast<uint32_t>(bytes < kPrefetchBytes ? bytes : kPrefetchBytes));
+        break;
+      }
+      case MK_OP_ATTN: {
+        const int cta = blockIdx.x;
+        const uint32_t blk = static_cast<uint32_t>(p.ps) * p.D * 2u;   // one page of K (or V) of one KV head
+        uint32_t done = 0;
+        for (int it = p.item_off[cta]; it < p.item_off[cta + 1] && done < kPrefetchBytes; ++it) {
+          const mk_attn_item item = p.items[it];
+          const int32_t* btrow = p.block_tables + static_cast<size_t>(item.b) * p.maxpg;
+          for (uint32_t pg = item.page_lo; pg < item.page_hi && done < kPrefetchBytes; ++pg) {
+            const int32_t page = btrow[pg];
+            if (page < 0 || page >= p.P) continue;
+            const size_t kb = (((static_cast<size_t>(t.layer) * p.P + page) * 2) * p.Hkv + item.kvh) * p.ps * p.D;
+            prefetch_l2(p.kv + kb, blk);
+            prefetch_l2(p.kv + kb + static_cast<size_t>(p.Hkv) * p.ps * p.D, blk);
+            done += 2 * blk;
+          }
+        }
+        break;
+      }
+      default: break;
+    }
+  }
+
   // wait for the slot of record c to be free; false if the step was aborted
   __device__ bool acquire() {
     const int s = static_cast<int>(c % kSlots);
@@ -687,9 +730,11 @@ struct Producer {
 
   __device__ void run() {
     const int cta = blockIdx.x;
+    if (p.task_off[cta] < p.task_off[cta + 1]) prefetch_task(p.tasks[p.task_off[cta]]);
     for (int ti = p.task_off[cta]; ti < p.task_off[cta + 1]; ++ti) {
       const mk_task t = p.tasks[ti];
       bool ok = true;
+      if (ti + 1 < p.task_off[cta + 1]) prefetch_task(p.tasks[ti + 1]);   // one task ahead
       switch (t.op) {
         case MK_OP_EMBED: ok = emit_control(R_EMBED, t, static_cast<uint32_t>(ti)); break;
         case MK_OP_QKV:
