@@ -33,6 +33,7 @@
 
 namespace mk {
 cudaError_t launch_step(const Params& p, cudaStream_t s);
+int tb_for_batch(int B);
 cudaError_t configure_kernels(int D);
 cudaError_t occupancy(int D, int* blocks);
 size_t smem_bytes();
@@ -559,6 +560,8 @@ int mk_decode_step(mk_ctx* c, int32_t batch, const int32_t* token_ids, const int
   p.pair_first = reinterpret_cast<const int32_t*>(d + c->off_pair);
   p.X = c->X; p.QKV = c->QKV; p.ATT = c->ATT; p.PO = c->PO; p.PML = c->PML; p.RLOG = c->RLOG; p.RIDS = c->RIDS;
   p.RW = c->RW; p.HB = c->HB; p.SS = c->SS; p.n_ss_slots = c->n_ctas;
+  // inputs wider than the staging scratch are read per warp and normalised with the SS words
+  p.need_ss = (int64_t)mk::tb_for_batch(batch) * cf.hidden > mk::kMoeScratch ? 1 : 0;
   p.max_items = c->plan.info.max_items;
   // a fresh tag per step; tagged words of an earlier step never match it.  When the tag
   // wraps, the tagged buffers are cleared so that no word from 2^32 steps ago can match.

@@ -1109,6 +1109,7 @@ struct Consumer {
         ll_st(x + col, v, p.tag);
         ss += v * v;
       }
+      if (!p.need_ss) continue;
       ss = warp_sum(ss);
       if ((threadIdx.x & 31) == 0) S.ssred[threadIdx.x >> 5][0] = ss;
       cbar();
@@ -1160,10 +1161,12 @@ struct Consumer {
     else o.plain[off] = v;
   }
 
-  // Stage the GEMV input of rows rb[0..nt) once per block in shared memory (S.moe, [nt][K]
-  // fp32, RMS-normalised for the kinds that have a norm), so that the block reads each
-  // tagged input word once instead of once per warp.
-  __device__ __noinline__ bool stage_input(int kind, int l, int K, const int (&rb)[TB], int nt, uint32_t tag) {
+  // Stage the GEMV input of rows rb[0..nt) once per block in shared memory (dst, [nt][K] fp32,
+  // RMS-normalised for the kinds that have a norm), so that the block reads each tagged input
+  // word once instead of once per warp.  One round of loads: the gains go out with the tagged
+  // words, and each row's sum of squares is reduced from the staged values themselves.
+  __device__ __noinline__ bool stage_input(int kind, int l, int K, const int (&rb)[TB], int nt, uint32_t tag,
+                                           float* dst) {
     const uint16_t* g = nullptr;
     int xidx = 0;
     if (kind == 0) { g = p.layers[l].attn_norm; xidx = 2 * l; }
@@ -1175,17 +1178,14 @@ struct Consumer {
       const int b = tb < nt ? rb[tb] : rb[0];
       src[tb] = kind == 1 ? p.ATT + (static_cast<size_t>(l) * p.max_batch + b) * (p.Hq * p.D) : xrow(xidx, b);
     }
-    float* dst = S.moe;
     cbar();   // the previous group's input has been read
-    // the row's per-block sums of squares are requested first, so they travel with the input
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const bool do_ss = g != nullptr && warp < nt;
-    const uint64_t* ssb = p.SS + static_cast<size_t>(xidx) * p.n_ss_slots * p.max_batch + rb[warp < TB ? warp : 0];
-    uint64_t ssw[8];
+    // this thread's columns for the normalisation: 4 at k4 = 4 * tid + 1024 * j
+    constexpr int kG = kMaxK / (4 * kConsumerThreads);
+    uint2 gw[kG];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int i = lane + 32 * k;
-      ssw[k] = (do_ss && i < p.n_ss_slots) ? ll_ld(ssb + static_cast<size_t>(i) * p.max_batch) : ll_pack(0.f, tag);
+    for (int j = 0; j < kG; ++j) {
+      const int k4 = 4 * threadIdx.x + 4 * kConsumerThreads * j;
+      gw[j] = (g != nullptr && k4 < K) ? __ldg(reinterpret_cast<const uint2*>(g + k4)) : make_uint2(0u, 0u);
     }
     const uint64_t* s0 = src[0];
     const uint64_t* s1 = src[TB > 1 ? 1 : 0];
@@ -1196,34 +1196,64 @@ struct Consumer {
       return (tb == 0 ? s0 : tb == 1 ? s1 : tb == 2 ? s2 : s3) + k;
     }, dst, tag);
     if (g != nullptr) {
-      if (do_ss) {
-        float v[8];
+      cbar();   // every staged value is in shared memory
+      const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+      float ss[TB];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          if (lane + 32 * k < p.n_ss_slots) LL_FIX(ssw[k], ssb + static_cast<size_t>(lane + 32 * k) * p.max_batch, tag, 0, -1, ok);
-          v[k] = ll_f(ssw[k]);
+      for (int tb = 0; tb < TB; ++tb) ss[tb] = 0.f;
+#pragma unroll
+      for (int j = 0; j < kG; ++j) {
+        const int k4 = 4 * threadIdx.x + 4 * kConsumerThreads * j;
+        if (k4 < K) {
+#pragma unroll
+          for (int tb = 0; tb < TB; ++tb) {
+            if (tb < nt) {
+              const float4 v = *reinterpret_cast<const float4*>(dst + tb * K + k4);
+              ss[tb] += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+            }
+          }
         }
-        const float r = ss_rstd(p, v);
-        if (lane == 0) S.rstd[warp] = r;
+      }
+#pragma unroll
+      for (int tb = 0; tb < TB; ++tb) {
+        const float w = warp_sum(ss[tb]);
+        if (lane == 0) S.ssred[warp][tb] = w;
       }
       cbar();
-      for (int i = threadIdx.x * 4; i < nt * K; i += kConsumerThreads * 4) {
-        const int tb = i / K, k = i - tb * K;
-        const float r = S.rstd[tb];
-        const uint2 gw = __ldg(reinterpret_cast<const uint2*>(g + k));
-        dst[i] = (dst[i] * r) * bf_lo(gw.x);
-        dst[i + 1] = (dst[i + 1] * r) * bf_hi(gw.x);
-        dst[i + 2] = (dst[i + 2] * r) * bf_lo(gw.y);
-        dst[i + 3] = (dst[i + 3] * r) * bf_hi(gw.y);
+      float r[TB];
+#pragma unroll
+      for (int tb = 0; tb < TB; ++tb) {
+        float t = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) t += S.ssred[w][tb];
+        r[tb] = 1.0f / sqrtf(t / static_cast<float>(K) + p.eps);
+      }
+#pragma unroll
+      for (int j = 0; j < kG; ++j) {
+        const int k4 = 4 * threadIdx.x + 4 * kConsumerThreads * j;
+        if (k4 < K) {
+#pragma unroll
+          for (int tb = 0; tb < TB; ++tb) {
+            if (tb < nt) {
+              float4* q = reinterpret_cast<float4*>(dst + tb * K + k4);
+              float4 v = *q;
+              v.x = (v.x * r[tb]) * bf_lo(gw[j].x);
+              v.y = (v.y * r[tb]) * bf_hi(gw[j].x);
+              v.z = (v.z * r[tb]) * bf_lo(gw[j].y);
+              v.w = (v.w * r[tb]) * bf_hi(gw[j].y);
+              *q = v;
+            }
+          }
+        }
       }
     }
     cbar();
     return ok;
   }
 
-  // this warp's segment of the staged input rows into registers
-  __device__ __forceinline__ void load_y_staged(const Seg<TB>& sg, int K, int nt, float (&y)[8 / TB][8][TB]) {
-    const float* yc = S.moe;
+  // this warp's segment of the staged input rows (yc, [nt][K]) into registers
+  __device__ __forceinline__ void load_y_staged(const float* yc, const Seg<TB>& sg, int K, int nt,
+                                                float (&y)[8 / TB][8][TB]) {
 #pragma unroll
     for (int j = 0; j < Seg<TB>::kUnits; ++j) {
       const int e = sg.unit(j);
@@ -1250,8 +1280,12 @@ struct Consumer {
       for (int tb = 0; tb < TB; ++tb) { rb[tb] = b0 + tb; rj[tb] = 0; }
     }
     if (nt * sg.K <= kMoeScratch) {
-      const bool ok = stage_input(kind, l, sg.K, rb, nt, tag);
-      load_y_staged(sg, sg.K, nt, y);
+      // the router input of a batch that fits is the MoE input: stage it into the cache
+      const bool cache = op == MK_OP_ROUTER && sg.S == 1 && p.B <= TB && p.B * sg.K <= kAttnScratch;
+      float* dst = cache ? S.scr.attn : S.moe;
+      const bool ok = stage_input(kind, l, sg.K, rb, nt, tag, dst);
+      if (cache && threadIdx.x == 0) S.ykey = l;
+      load_y_staged(dst, sg, sg.K, nt, y);
       return ok;
     }
     return load_input(sg, kind, l, rb, nt, tag, op, y);
@@ -1294,6 +1328,8 @@ struct Consumer {
     } else {
       ok = stream_load(sg, moe, kind, l, 0, min(cnt, TB), tag, eop, rb, rj, y);
     }
+    // segment sums share storage with the MoE input cache: every warp has its input first
+    if (sg.S > 1) cbar();
     trace_mark(11 + (op == MK_OP_ROUTER ? 0 : moe ? 20 : 40), l);
     for (;;) {
       const int n = meta().n;
@@ -1393,7 +1429,7 @@ struct Consumer {
     }
     if (!ok) ll_timeout(p, eop, l);
     if (!cbar_and(wok && ok)) return false;
-    if (op == MK_OP_OPROJ) {
+    if (op == MK_OP_OPROJ && p.need_ss) {
       // publish this tile's share of sum(x_mid^2) for the RMSNorm of the MoE input
       uint64_t* out = p.SS + (static_cast<size_t>(2 * l + 1) * p.n_ss_slots + blockIdx.x) * p.max_batch;
       if (B <= TB) block_token_sums<TB>(S, lane < B ? lane : -1, my_ss, B, out, 1, p.tag);
@@ -1424,11 +1460,12 @@ struct Consumer {
   // router tiles wrote), so the MoE of a layer needs nothing else from another block.
   // Top-k by logit, ties to the lower expert index: an expert's rank is the number of
   // experts with a larger logit plus those with an equal logit and a lower index; every
-  // (row, expert) pair counts its own rank against the row's logits in shared memory.
-  // Weights: exp(r - max) over the chosen experts, renormalised over them (or over all
-  // experts when norm_topk == 0).  Then the active experts, the cost split of the gate/up
-  // units over the blocks, and (batches that fit) the normalised MoE input, all in shared
-  // memory; the block's producer is released to stream the experts.
+  // (row, expert) pair counts its own rank against the row's logits in shared memory, the
+  // comparisons of a pair split over up to 8 threads.  Weights: exp(r - max) over the chosen
+  // experts, renormalised over them (or over all experts when norm_topk == 0).  Then the
+  // active experts, the cost split of the gate/up units over the blocks, and (batches that
+  // fit) the normalised MoE input, all in shared memory; the block's producer is released to
+  // stream the experts.
   __device__ __noinline__ bool route_local() {
     const int l = meta().layer;
     const int B = p.B, E = p.E, K = p.K, H = p.H;
@@ -1437,13 +1474,20 @@ struct Consumer {
     twait = globaltimer();
     trace_mark(15, l);
     bool ok = true;
-    // the normalised MoE input of every row stays in shared memory when it fits (B <= TB)
+    // the normalised MoE input of every row stays in shared memory when it fits; x_mid is
+    // complete before the router logits are, so it is staged first (unless the router tile
+    // of this block already left it there)
     const bool cache_in = B <= TB && B * H <= kAttnScratch;
+    if (cache_in && S.ykey != l) {
+      int rb[TB];
+#pragma unroll
+      for (int tb = 0; tb < TB; ++tb) rb[tb] = tb;
+      ok = stage_input(2, l, H, rb, B, p.tag, S.scr.attn);
+    }
     {
       const uint64_t* rl = p.RLOG + static_cast<size_t>(l) * p.max_batch * E;
-      ok = ll_gather(p, B * E, [=](int i) { return rl + i; }, lg, p.tag);
+      ok = ll_gather(p, B * E, [=](int i) { return rl + i; }, lg, p.tag) && ok;
     }
-    if (cache_in) ok = ffn_input(l) && ok;
     for (int e = threadIdx.x; e < E; e += kConsumerThreads) S.ecnt[e] = 0;
     if (!ok) ll_timeout(p, MK_OP_ROUTER, l);
     if (!cbar_and(ok)) return false;
@@ -1457,40 +1501,60 @@ struct Consumer {
       z = warp_sum(z);
       if (lane == 0) { S.rmax[b] = mx; S.rz[b] = z; }
     }
-    for (int i = threadIdx.x; i < B * E; i += kConsumerThreads) {
-      const int b = i / E, e = i - b * E;
-      const float* row = lg + b * E;
-      const float v = row[e];
-      int rank = 0;
-      int e2 = 0;
-      if ((E & 3) == 0) {
-#pragma unroll 4
-        for (; e2 < E; e2 += 4) {
-          const float4 q = *reinterpret_cast<const float4*>(row + e2);
-          rank += static_cast<int>(q.x > v) + (static_cast<int>(q.x == v) & static_cast<int>(e2 < e));
-          rank += static_cast<int>(q.y > v) + (static_cast<int>(q.y == v) & static_cast<int>(e2 + 1 < e));
-          rank += static_cast<int>(q.z > v) + (static_cast<int>(q.z == v) & static_cast<int>(e2 + 2 < e));
-          rank += static_cast<int>(q.w > v) + (static_cast<int>(q.w == v) & static_cast<int>(e2 + 3 < e));
+    {
+      const int n = B * E;
+      int q = 1;   // threads per (row, expert) pair
+      while (q < 8 && 2 * q * n <= kConsumerThreads) q <<= 1;
+      const int part = threadIdx.x & (q - 1);
+      const int e_lo = part * E / q, e_hi = (part + 1) * E / q;
+      for (int i0 = 0; i0 < n; i0 += kConsumerThreads / q) {   // uniform trip count: the shuffles below
+        const int i = i0 + static_cast<int>(threadIdx.x) / q;
+        const bool on = i < n;
+        const int b = on ? i / E : 0, e = on ? i - b * E : 0;
+        const float* row = lg + b * E;
+        const float v = row[e];
+        int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+        int e2 = e_lo;
+        for (; e2 + 4 <= e_hi; e2 += 4) {
+          const float a0 = row[e2], a1 = row[e2 + 1], a2 = row[e2 + 2], a3 = row[e2 + 3];
+          r0 += static_cast<int>(a0 > v) + (static_cast<int>(a0 == v) & static_cast<int>(e2 < e));
+          r1 += static_cast<int>(a1 > v) + (static_cast<int>(a1 == v) & static_cast<int>(e2 + 1 < e));
+          r2 += static_cast<int>(a2 > v) + (static_cast<int>(a2 == v) & static_cast<int>(e2 + 2 < e));
+          r3 += static_cast<int>(a3 > v) + (static_cast<int>(a3 == v) & static_cast<int>(e2 + 3 < e));
         }
-      }
-      for (; e2 < E; ++e2) {
-        const float v2 = row[e2];
-        rank += static_cast<int>(v2 > v) + (static_cast<int>(v2 == v) & static_cast<int>(e2 < e));
-      }
-      if (rank < K) {
-        S.rids[b * K + rank] = e;
-        S.rval[b * K + rank] = v;
-        atomicAdd(&S.ecnt[e], 1);
+        for (; e2 < e_hi; ++e2) {
+          const float a = row[e2];
+          r0 += static_cast<int>(a > v) + (static_cast<int>(a == v) & static_cast<int>(e2 < e));
+        }
+        int rank = (r0 + r1) + (r2 + r3);
+        for (int o = 1; o < q; o <<= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+        if (on && part == 0 && rank < K) {
+          S.rids[b * K + rank] = e;
+          S.rval[b * K + rank] = v;
+          atomicAdd(&S.ecnt[e], 1);
+        }
       }
     }
     cbar();
     trace_mark(18, l);
-    for (int b = threadIdx.x; b < B; b += kConsumerThreads) {
-      float sum = 0.f;
-      for (int j = 0; j < K; ++j) sum += expf(S.rval[b * K + j] - S.rmax[b]);
-      S.rsum[b] = sum;
+    // combine weights (a warp per row, a lane per slot) ...
+    for (int b = warp; b < B; b += kConsumerWarps) {
+      const int j = lane < K ? lane : 0;
+      const float ex = expf(S.rval[b * K + j] - S.rmax[b]);
+      const float sum = warp_sum(lane < K ? ex : 0.f);
+      if (lane < K) {
+        const int i = b * K + lane;
+        const float wgt = p.norm_topk ? ex / sum : ex / S.rz[b];
+        S.rcache[i] = S.rids[i];
+        S.rwcache[i] = wgt;
+        if (blockIdx.x == 0) {   // a copy for inspection
+          p.RIDS[static_cast<size_t>(l) * p.max_batch * K + i] = S.rids[i];
+          p.RW[static_cast<size_t>(l) * p.max_batch * K + i] = wgt;
+        }
+      }
     }
-    if (warp == 0) {
+    // ... while the last warp lists the active experts and their gate/up cost prefix
+    if (warp == kConsumerWarps - 1) {
       int nact = 0;
       for (int e0 = 0; e0 < E; e0 += 32) {
         const int e = e0 + lane;
@@ -1501,7 +1565,7 @@ struct Consumer {
       }
       if (lane == 0) S.nact = nact;
       __syncwarp();
-      // cost prefix of the gate/up units over the active experts (8 experts per lane, then a warp scan)
+      // 8 experts per lane, then a warp scan
       int32_t loc[kMaxExperts / 32];
       int32_t run = 0;
 #pragma unroll
@@ -1528,22 +1592,13 @@ struct Consumer {
     }
     cbar();
     trace_mark(19, l);
-    for (int i = threadIdx.x; i < B * K; i += kConsumerThreads) {
-      const int b = i / K;
-      const float ex = expf(S.rval[i] - S.rmax[b]);
-      const float wgt = p.norm_topk ? ex / S.rsum[b] : ex / S.rz[b];
-      S.rcache[i] = S.rids[i];
-      S.rwcache[i] = wgt;
-      if (blockIdx.x == 0) {   // a copy for inspection
-        p.RIDS[static_cast<size_t>(l) * p.max_batch * K + i] = S.rids[i];
-        p.RW[static_cast<size_t>(l) * p.max_batch * K + i] = wgt;
-      }
+    // this block's gate/up units: the two ends by two warps at once
+    if (lane == 0 && warp < 2) {
+      const int32_t u = moe_gu_start(blockIdx.x + warp, p.n_ctas, S.ecum, S.ecost, S.nact, p.F);
+      if (warp == 0) S.gu_lo = u; else S.gu_hi = u;
     }
-    if (threadIdx.x == 0) {
-      S.gu_lo = moe_gu_start(blockIdx.x, p.n_ctas, S.ecum, S.ecost, S.nact, p.F);
-      S.gu_hi = moe_gu_start(blockIdx.x + 1, p.n_ctas, S.ecum, S.ecost, S.nact, p.F);
-      S.ykey = cache_in ? l : -1;
-    }
+    if (threadIdx.x == 0 && !cache_in) S.ykey = -1;
+    if (threadIdx.x == 0 && cache_in) S.ykey = l;
     cbar();
     trace_mark(17, l);
     if (threadIdx.x == 0) mbar_arrive(&S.route_bar);   // hand the routing to this block's producer
@@ -1566,44 +1621,6 @@ struct Consumer {
     }
     cbar();
     return S.flag;
-  }
-
-  // the normalised MoE input of every row into scr.attn (B <= TB, B*H <= kAttnScratch);
-  // loads are issued before the row's rstd is known and scaled afterwards
-  __device__ __noinline__ bool ffn_input(int l) {
-    const int B = p.B, H = p.H;
-    const int warp = threadIdx.x >> 5;
-    const int xidx = 2 * l + 1;
-    float* yc = S.scr.attn;
-    const uint64_t* x0 = xrow(xidx, 0);
-    const uint16_t* g = p.layers[l].ffn_norm;
-    constexpr int kGainRegs = (kAttnScratch / 4 + kConsumerThreads - 1) / kConsumerThreads;
-    uint2 gw[kGainRegs];
-#pragma unroll
-    for (int k = 0; k < kGainRegs; ++k) {
-      const int i = (threadIdx.x + k * kConsumerThreads) * 4;
-      gw[k] = i < B * H ? __ldg(reinterpret_cast<const uint2*>(g + (i % H))) : make_uint2(0u, 0u);
-    }
-    bool ok = ll_gather(p, B * H, [=](int i) { return x0 + i; }, yc, p.tag);   // rows of the batch are contiguous in X
-    if (warp < B) {
-      float v[8];
-      ok = ss_fetch(p, xidx, warp, v) && ok;
-      const float r = ss_rstd(p, v);
-      if ((threadIdx.x & 31) == 0) S.rstd[warp] = r;
-    }
-    cbar();
-#pragma unroll
-    for (int k = 0; k < kGainRegs; ++k) {
-      const int i = (threadIdx.x + k * kConsumerThreads) * 4;
-      if (i < B * H) {
-        const float r = S.rstd[i / H];
-        yc[i] = (yc[i] * r) * bf_lo(gw[k].x);
-        yc[i + 1] = (yc[i + 1] * r) * bf_hi(gw[k].x);
-        yc[i + 2] = (yc[i + 2] * r) * bf_lo(gw[k].y);
-        yc[i + 3] = (yc[i + 3] * r) * bf_hi(gw[k].y);
-      }
-    }
-    return ok;
   }
 
   // inputs of up to TB (row, slot) pairs from the cached MoE input
@@ -1717,7 +1734,8 @@ struct Consumer {
     uint64_t* ssout = p.SS + (static_cast<size_t>(2 * l + 2) * p.n_ss_slots + blockIdx.x) * p.max_batch;
     twait = globaltimer();
     if (m0.n == 0) {   // no hidden rows here (or nothing routed): the block's share of sum(x^2) is 0
-      for (int t = threadIdx.x; t < B; t += kConsumerThreads) ll_st(ssout + t, 0.f, p.tag);
+      if (p.need_ss)
+        for (int t = threadIdx.x; t < B; t += kConsumerThreads) ll_st(ssout + t, 0.f, p.tag);
       return true;
     }
     float* P = S.moe;                                  // [B][K][nrow] products
@@ -1792,8 +1810,10 @@ struct Consumer {
         ll_st(p.X + (2 * static_cast<size_t>(l) + 2) * xs + static_cast<size_t>(t) * p.H + r0 + r, v, p.tag);
         ss += v * v;
       }
-      ss = warp_sum(ss);
-      if (lane == 0) ll_st(ssout + t, ss, p.tag);
+      if (p.need_ss) {
+        ss = warp_sum(ss);
+        if (lane == 0) ll_st(ssout + t, ss, p.tag);
+      }
     }
     return true;
   }
@@ -2078,11 +2098,14 @@ struct Consumer {
   // This block's share of merging the splits of every (row, KV head) pair it holds a split
   // of: split s of n merges outputs [s*G*D/n, (s+1)*G*D/n) of the pair over all n splits, in
   // split order, from their tagged partials, and writes them as the attention output.
+  // A warp per head finds the head's max and normaliser over the splits (a lane per split)
+  // and leaves each split's scale exp(m_s - M) / L; then 8 lanes per output sum the splits.
   __device__ __noinline__ bool attn_combine() {
     const int l = meta().layer;
     const int Gq = p.G;
     const int GD = Gq * D;
     const int cta = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     twait = globaltimer();
     bool ok = true;
     for (int it = p.item_off[cta]; it < p.item_off[cta + 1]; ++it) {
@@ -2096,6 +2119,7 @@ struct Consumer {
       const int nml = 2 * ns * Gq;
       const float* ml = S.moe;                  // [ns][G][2]
       const float* part = S.moe + nml;          // [ns][nsl]
+      float* fs = S.moe + nml + ns * nsl;       // [ns][G] split scales
       ok = ll_gather(p, nml + ns * nsl, [=](int i) {
         if (i < nml) {
           const int sp = i / (2 * Gq), r = i - sp * 2 * Gq;
@@ -2106,30 +2130,37 @@ struct Consumer {
       }, S.moe + 0, p.tag) && ok;
       if (!ok) ll_timeout(p, MK_OP_ATTN, l);
       if (!cbar_and(ok)) return false;
-      if (threadIdx.x < Gq) {
-        const int h = threadIdx.x;
+      for (int h = warp; h < Gq; h += kConsumerWarps) {
         float M = -INFINITY;
-        for (int sp = 0; sp < ns; ++sp) M = fmaxf(M, ml[(sp * Gq + h) * 2]);
+        for (int sp = lane; sp < ns; sp += 32) M = fmaxf(M, ml[(sp * Gq + h) * 2]);
+        M = warp_max(M);
         float L = 0.f;
-        for (int sp = 0; sp < ns; ++sp) {
+        for (int sp = lane; sp < ns; sp += 32) {
           const float m = ml[(sp * Gq + h) * 2];
           L += (m == -INFINITY ? 0.f : __expf(m - M)) * ml[(sp * Gq + h) * 2 + 1];
         }
-        S.rmax[h] = M;
-        S.rz[h] = L;
+        L = warp_sum(L);
+        const float invL = 1.f / L;
+        for (int sp = lane; sp < ns; sp += 32) {
+          const float m = ml[(sp * Gq + h) * 2];
+          fs[sp * Gq + h] = (m == -INFINITY ? 0.f : __expf(m - M)) * invL;
+        }
       }
       cbar();
       uint64_t* att = p.ATT + (static_cast<size_t>(l) * p.max_batch + item.b) * (p.Hq * D) +
                       static_cast<size_t>(item.kvh) * GD;
-      for (int oi = threadIdx.x; oi < nsl; oi += kConsumerThreads) {
-        const int h = (o0 + oi) / D;
-        const float M = S.rmax[h], invL = 1.f / S.rz[h];
+      const int og = threadIdx.x >> 3, sub = threadIdx.x & 7;
+      for (int base = 0; base < nsl; base += kConsumerThreads / 8) {   // uniform trip count: the shuffles below
+        const int oi = base + og;
         float acc = 0.f;
-        for (int sp = 0; sp < ns; ++sp) {
-          const float m = ml[(sp * Gq + h) * 2];
-          acc += (m == -INFINITY ? 0.f : __expf(m - M)) * part[sp * nsl + oi];
+        if (oi < nsl) {
+          const int h = (o0 + oi) / D;
+          for (int sp = sub; sp < ns; sp += 8) acc += fs[sp * Gq + h] * part[sp * nsl + oi];
         }
-        ll_st(att + o0 + oi, acc * invL, p.tag);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+        if (oi < nsl && sub == 0) ll_st(att + o0 + oi, acc, p.tag);
       }
       cbar();
     }

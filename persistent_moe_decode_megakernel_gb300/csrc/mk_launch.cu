@@ -16,7 +16,7 @@ size_t smem_bytes_impl();
 size_t smem_bytes() { return smem_bytes_impl(); }
 
 // rows of the batch held in registers at once by a GEMV tile
-static int tb_for_batch(int B) { return B <= 1 ? 1 : (B <= 2 ? 2 : 4); }
+int tb_for_batch(int B) { return B <= 1 ? 1 : (B <= 2 ? 2 : 4); }
 
 cudaError_t configure_kernels(int D) { return D == 128 ? configure_d128(smem_bytes()) : configure_d64(smem_bytes()); }
 

@@ -61,19 +61,21 @@ MK_HD int pages_per_chunk(int page_size, int head_dim) { return (kSlotBytes / 2)
 MK_HD int32_t moe_unit_cost(int routed_rows) { return routed_rows > 4 ? routed_rows : 4; }
 
 // first unit of block j of N; cum[a] = cost of the units of experts 0..a-1 (cum[nact] = C,
-// at most 256 experts x 1024 rows x 64 = 2^24), cost[a] = cost of one unit of expert a
+// at most 256 experts x 1024 rows x 64 = 2^24), cost[a] = cost of one unit of expert a.
+// With 0 < j < N <= 256, C * j < 2^32: the arithmetic stays in 32 bits.
 template <class I>
 MK_HD int32_t moe_gu_start(int j, int N, const I* cum, const I* cost, int nact, int F) {
   if (j <= 0 || nact <= 0) return 0;
   if (j >= N) return nact * F;
-  const int64_t T = static_cast<int64_t>(static_cast<uint64_t>(cum[nact]) * static_cast<uint32_t>(j) / static_cast<uint32_t>(N));
+  const uint32_t T = static_cast<uint32_t>(cum[nact]) * static_cast<uint32_t>(j) / static_cast<uint32_t>(N);
   int lo = 0, hi = nact - 1;   // last a with cum[a] <= T
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (cum[mid] <= T) lo = mid; else hi = mid - 1;
+    if (static_cast<uint32_t>(cum[mid]) <= T) lo = mid; else hi = mid - 1;
   }
-  const int64_t f = (T - static_cast<int64_t>(cum[lo]) + cost[lo] - 1) / cost[lo];
-  return f >= F ? (lo + 1) * F : lo * F + (int32_t)f;
+  const uint32_t c = static_cast<uint32_t>(cost[lo]);
+  const uint32_t f = (T - static_cast<uint32_t>(cum[lo]) + c - 1u) / c;
+  return f >= static_cast<uint32_t>(F) ? (lo + 1) * F : lo * F + static_cast<int32_t>(f);
 }
 
 // ---- counters --------------------------------------------------------------------
@@ -164,6 +166,7 @@ struct alignas(64) Params {
   uint64_t* HB;    // [L][max_batch][K][F] SwiGLU activations per (row, slot)
   uint64_t* SS;    // [2L+1][n_ss_slots][max_batch] per-block sums of squares of the residual stream
   int32_t n_ss_slots;
+  int32_t need_ss;      // some GEMV input is too wide to stage and reads SS (else SS is not written)
   int32_t* RIDS;   // [L][max_batch][K] routing ids (copy kept by block 0 for inspection)
   float* RW;       // [L][max_batch][K] combine weights (same)
   uint32_t* ctr;   // [cm.total]
