@@ -964,6 +964,11 @@ __device__ void block_token_sums(Smem& S, int my_tb, float v, int nt, uint64_t* 
 // record of a tile); block-wide barriers are taken only at tile boundaries --
 // the dependency wait at a tile's start and the signal at its end -- and, where
 // S warps split a row, over those S warps only.
+// Every consumer function is inlined into the dispatch loop, so the consumer's state
+// (record index, flags) and the small arrays passed between its functions stay in
+// registers (the consumer warpgroups hold 224 each).  A call that took the object's
+// address would put that state in local memory, and with nearly all of the SM's L1
+// given to shared memory, those accesses would miss to L2 after every barrier.
 template <int TB, int D>
 struct Consumer {
   const Params& p;
@@ -1089,7 +1094,7 @@ struct Consumer {
   }
 
   // ------------------------------------------------------------------ EMBED
-  __device__ __noinline__ bool embed() {
+  __device__ __forceinline__ bool embed() {
     const Meta m = meta();
     const int H = p.H;
     uint64_t* ssout = p.SS + static_cast<size_t>(blockIdx.x) * p.max_batch;   // vector 0, slot = this block
@@ -1165,7 +1170,7 @@ struct Consumer {
   // RMS-normalised for the kinds that have a norm), so that the block reads each tagged input
   // word once instead of once per warp.  One round of loads: the gains go out with the tagged
   // words, and each row's sum of squares is reduced from the staged values themselves.
-  __device__ __noinline__ bool stage_input(int kind, int l, int K, const int (&rb)[TB], int nt, uint32_t tag,
+  __device__ __forceinline__ bool stage_input(int kind, int l, int K, const int (&rb)[TB], int nt, uint32_t tag,
                                            float* dst) {
     const uint16_t* g = nullptr;
     int xidx = 0;
@@ -1291,7 +1296,7 @@ struct Consumer {
     return load_input(sg, kind, l, rb, nt, tag, op, y);
   }
 
-  __device__ __noinline__ bool stream_gemv(int op) {
+  __device__ __forceinline__ bool stream_gemv(int op) {
     constexpr bool kGroups = TB == 4;   // only the widest instantiation sees batches wider than its registers
     const int l = meta().layer;
     const uint32_t lo = meta().lo, hi = meta().hi;
@@ -1466,7 +1471,7 @@ struct Consumer {
   // active experts, the cost split of the gate/up units over the blocks, and (batches that
   // fit) the normalised MoE input, all in shared memory; the block's producer is released to
   // stream the experts.
-  __device__ __noinline__ bool route_local() {
+  __device__ __forceinline__ bool route_local() {
     const int l = meta().layer;
     const int B = p.B, E = p.E, K = p.K, H = p.H;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1724,7 +1729,7 @@ struct Consumer {
   // in shared memory; after the last chunk the slots are summed in slot order and added to
   // x_mid, and the block publishes its share of sum(x_out^2) for the next RMSNorm.
   template <int TD>
-  __device__ __noinline__ bool moe_down_t() {
+  __device__ __forceinline__ bool moe_down_t() {
     const Meta m0 = meta();
     const int l = m0.layer;
     const int B = p.B, K = p.K, F = p.F;
@@ -1834,7 +1839,7 @@ struct Consumer {
     return static_cast<uint32_t>((d >> 6) * rows_cap * 128 + r * 128 + ((((d & 63) >> 3) ^ (r & 7)) << 4) + (d & 7) * 2);
   }
 
-  __device__ __noinline__ bool attn_item() {
+  __device__ __forceinline__ bool attn_item() {
     constexpr int KS = D / 16;                              // k-steps over head dims (Q K^T)
     constexpr int MT = D / 16;                              // 16-dim tiles of the output (P V)
     constexpr int ROWS = (kSlotBytes / 2) / (D * 2);        // positions a chunk's K (or V) region holds
@@ -2100,7 +2105,7 @@ struct Consumer {
   // split order, from their tagged partials, and writes them as the attention output.
   // A warp per head finds the head's max and normaliser over the splits (a lane per split)
   // and leaves each split's scale exp(m_s - M) / L; then 8 lanes per output sum the splits.
-  __device__ __noinline__ bool attn_combine() {
+  __device__ __forceinline__ bool attn_combine() {
     const int l = meta().layer;
     const int Gq = p.G;
     const int GD = Gq * D;
