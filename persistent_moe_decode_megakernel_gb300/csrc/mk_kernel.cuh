@@ -246,6 +246,16 @@ __device__ __forceinline__ void warp_sum2(float (&a)[TB], const float (&b)[TB]) 
   }
 }
 
+// Division by a divisor fixed for a loop (1 <= d < 2^16), exact for 0 <= n < 2^16: with
+// m = ceil(2^32 / d) = m * d - 2^32 + ... the error term e = m * d - 2^32 < d, and n * e < 2^32,
+// so floor(n * m / 2^32) = floor(n / d).  One wide multiply instead of a division routine.
+struct FastDiv {
+  uint32_t d;
+  uint64_t m;
+  __device__ __forceinline__ explicit FastDiv(int d_) : d(static_cast<uint32_t>(d_)), m(0xffffffffull / static_cast<uint32_t>(d_) + 1ull) {}
+  __device__ __forceinline__ int div(int n) const { return static_cast<int>((static_cast<uint64_t>(n) * m) >> 32); }
+};
+
 // --------------------------------------------------------------------------- shared memory
 enum : uint8_t { R_EMBED = 1, R_GEMV = 2, R_ATTN = 3, R_GU = 4, R_DOWN = 5, R_END = 6, R_ROUTE = 7, R_COMBINE = 8 };
 // GEMV stream kinds beyond the task ops (MK_OP_QKV / OPROJ / ROUTER / HEAD)
@@ -300,7 +310,7 @@ struct __align__(128) Smem {
 };
 
 // --------------------------------------------------------------------------- errors / waits
-__device__ void record_error(const Params& p, int code, int op, int layer, uint32_t ctr, uint32_t observed,
+__device__ __noinline__ void record_error(const Params& p, int code, int op, int layer, uint32_t ctr, uint32_t observed,
                              uint32_t target, int detail, bool abort) {
   if (atomicCAS(&p.status->code, 0, code) == 0) {
     p.status->op = op;
@@ -362,14 +372,38 @@ __device__ __noinline__ void ll_timeout(const Params& p, int op, int layer) {
       }                                                                                   \
     }                                                                                     \
   }
+// Re-poll the words of one gather batch whose tags were stale (bit k: the word of index
+// base + k * kConsumerThreads) until each is current; a compact loop, since it is the
+// uncommon path.  False if the watchdog or an abort ended the wait.
+template <class Addr>
+__device__ __noinline__ bool ll_gather_fix(const Params& p, Addr addr, int base, uint32_t stale, float* dst,
+                                           uint32_t tag) {
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1; stale != 0u; ++it) {
+#pragma unroll 1
+    for (int k = 0; k < 32; ++k) {
+      if ((stale >> k) & 1u) {
+        const int i = base + k * kConsumerThreads;
+        const uint64_t x = ll_ld(addr(i));
+        if (ll_ok(x, tag)) {
+          dst[i] = ll_f(x);
+          stale &= ~(1u << k);
+        }
+      }
+    }
+    if (stale != 0u && (it & 15u) == 0u && (aborted(p) || globaltimer() - t0 > p.watchdog_ns)) return false;
+  }
+  return true;
+}
+
 // Gather n tagged words into shared-memory floats: dst[i] = value of word addr(i), i over
 // this thread's indices threadIdx.x + k * kConsumerThreads.  Loads go out 16 at a time;
-// stale words are re-polled in sweeps (all stale words of a batch per sweep).
+// words that carried a stale tag are re-polled by ll_gather_fix.
 template <class Addr>
-__device__ bool ll_gather(const Params& p, int n, Addr addr, float* dst, uint32_t tag) {
+__device__ __forceinline__ bool ll_gather(const Params& p, int n, Addr addr, float* dst, uint32_t tag) {
   constexpr int kB = 16;
   bool ok = true;
-  for (int base = threadIdx.x; base < n && ok; base += kB * kConsumerThreads) {
+  for (int base = threadIdx.x; base < n; base += kB * kConsumerThreads) {
     uint64_t x[kB];
 #pragma unroll
     for (int k = 0; k < kB; ++k) {
@@ -385,22 +419,8 @@ __device__ bool ll_gather(const Params& p, int n, Addr addr, float* dst, uint32_
         else stale |= 1u << k;
       }
     }
-    if (stale == 0u) continue;
-    const uint64_t t0 = globaltimer();
-    for (uint32_t it = 1; stale != 0u; ++it) {
-#pragma unroll
-      for (int k = 0; k < kB; ++k)
-        if ((stale >> k) & 1u) x[k] = ll_ld(addr(base + k * kConsumerThreads));
-#pragma unroll
-      for (int k = 0; k < kB; ++k) {
-        if (((stale >> k) & 1u) && ll_ok(x[k], tag)) {
-          dst[base + k * kConsumerThreads] = ll_f(x[k]);
-          stale &= ~(1u << k);
-        }
-      }
-      if (stale != 0u && (it & 15u) == 0u && (aborted(p) || globaltimer() - t0 > p.watchdog_ns)) ok = false;
-      if (!ok) break;
-    }
+    if (stale != 0u) ok = ll_gather_fix(p, addr, base, stale, dst, tag) && ok;
+    if (!ok) break;
   }
   return ok;
 }
@@ -959,6 +979,29 @@ __device__ void block_token_sums(Smem& S, int my_tb, float v, int nt, uint64_t* 
   cbar();
 }
 
+// 8 consecutive tagged words, re-polling until every one carries the step's tag (the
+// unstaged SwiGLU input of wide batches); ok is false if the watchdog or an abort ended it.
+// Returned by value so that the caller's registers never need an address.
+struct H8 { float v[8]; bool ok; };
+__device__ __noinline__ H8 load_h8(const Params& p, const uint64_t* src) {
+  H8 r;
+  r.ok = true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    uint32_t st = 0;
+#pragma unroll
+    for (int q = 0; q < 8; q += 2) {
+      uint64_t a, b;
+      ll_ld2(src + q, a, b);
+      st |= ll_stale(a, p.tag) | ll_stale(b, p.tag);
+      r.v[q] = ll_f(a);
+      r.v[q + 1] = ll_f(b);
+    }
+    if (st == 0u) return r;
+    if ((it & 15u) == 0u && (aborted(p) || globaltimer() - t0 > p.watchdog_ns)) { r.ok = false; return r; }
+  }
+}
+
 // --------------------------------------------------------------------------- consumer
 // Warps consume ring records independently (each waits for and releases every
 // record of a tile); block-wide barriers are taken only at tile boundaries --
@@ -1196,8 +1239,9 @@ struct Consumer {
     const uint64_t* s1 = src[TB > 1 ? 1 : 0];
     const uint64_t* s2 = src[TB > 2 ? 2 : 0];
     const uint64_t* s3 = src[TB > 3 ? 3 : 0];
+    const FastDiv dK(K);   // nt * K <= the scratch size < 2^16
     bool ok = ll_gather(p, nt * K, [=](int i) {
-      const int tb = i / K, k = i - tb * K;
+      const int tb = dK.div(i), k = i - tb * K;
       return (tb == 0 ? s0 : tb == 1 ? s1 : tb == 2 ? s2 : s3) + k;
     }, dst, tag);
     if (g != nullptr) {
@@ -1293,7 +1337,11 @@ struct Consumer {
       load_y_staged(dst, sg, sg.K, nt, y);
       return ok;
     }
-    return load_input(sg, kind, l, rb, nt, tag, op, y);
+    if constexpr (TB * kMaxK > kMoeScratch) {
+      return load_input(sg, kind, l, rb, nt, tag, op, y);
+    } else {
+      return false;   // unreachable: every input of this batch width fits the scratch
+    }
   }
 
   __device__ __forceinline__ bool stream_gemv(int op) {
@@ -1701,17 +1749,10 @@ struct Consumer {
             const float4 b = *reinterpret_cast<const float4*>(hc + static_cast<size_t>(i) * p.F + e + 4);
             v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
           } else {
-            const uint64_t* src = p.HB + (static_cast<size_t>(l) * p.max_batch * p.K + i) * p.F + e;
-            LL_RETRY_BEGIN
+            const H8 h = load_h8(p, p.HB + (static_cast<size_t>(l) * p.max_batch * p.K + i) * p.F + e);
 #pragma unroll
-            for (int q = 0; q < 8; q += 2) {
-              uint64_t a, b;
-              ll_ld2(src + q, a, b);
-              st_ |= ll_stale(a, p.tag) | ll_stale(b, p.tag);
-              v[q] = ll_f(a);
-              v[q + 1] = ll_f(b);
-            }
-            LL_RETRY_END(ok)
+            for (int q = 0; q < 8; ++q) v[q] = h.v[q];
+            ok = h.ok && ok;
           }
         }
 #pragma unroll
@@ -2054,6 +2095,7 @@ struct Consumer {
     // slot it still holds (the producer refills it only after the release that follows), then
     // each thread folds the 8 states of 4 output dims of one head, in warp order
     constexpr int kStride = kMaxG * D + 2 * kMaxG;
+    static_assert(kConsumerWarps * kStride * 4 <= kSlotBytes, "the warps' merge states must fit in the held slot");
     float* st = reinterpret_cast<float*>(const_cast<uint8_t*>(slot()));
     {
       float* dst = st + warp * kStride;
@@ -2125,12 +2167,13 @@ struct Consumer {
       const float* ml = S.moe;                  // [ns][G][2]
       const float* part = S.moe + nml;          // [ns][nsl]
       float* fs = S.moe + nml + ns * nsl;       // [ns][G] split scales
+      const FastDiv d2g(2 * Gq), dsl(nsl);   // indices below the scratch size < 2^16
       ok = ll_gather(p, nml + ns * nsl, [=](int i) {
         if (i < nml) {
-          const int sp = i / (2 * Gq), r = i - sp * 2 * Gq;
+          const int sp = d2g.div(i), r = i - sp * 2 * Gq;
           return pml + static_cast<size_t>(sp) * 2 * kMaxG + r;
         }
-        const int j = i - nml, sp = j / nsl;
+        const int j = i - nml, sp = dsl.div(j);
         return po + static_cast<size_t>(sp) * kMaxG * D + o0 + (j - sp * nsl);
       }, S.moe + 0, p.tag) && ok;
       if (!ok) ll_timeout(p, MK_OP_ATTN, l);
@@ -2185,9 +2228,11 @@ struct Consumer {
       wok = true;
       switch (m0.kind) {
         case R_EMBED: ok = embed(); break;
-        case R_GEMV: ok = stream_gemv(m0.op); break;
+        case R_GEMV:
+        case R_GU:   // one inlined copy of the GEMV stream serves both kinds
+          ok = (m0.kind == R_GU && meta().n == 0) ? true : stream_gemv(m0.kind == R_GU ? int(R_OP_GU) : int(m0.op));
+          break;
         case R_ATTN: ok = attn_item(); break;
-        case R_GU: ok = meta().n ? stream_gemv(R_OP_GU) : true; break;
         case R_DOWN: ok = moe_down(); break;
         case R_ROUTE: ok = route_local(); break;
         case R_COMBINE: ok = attn_combine(); break;
