@@ -1508,6 +1508,53 @@ struct Consumer {
     cbar();
   }
 
+  // Ranks of every (row, expert) pair of the batch (see route_local): the consumer threads
+  // form G groups, one row each at a time; in a group, 8 threads split the row's logits into
+  // slices of at most LEN values held in registers, and the candidates (experts) are dealt
+  // over the group's slots.  Each thread counts its slice's values above the candidate (ties:
+  // lower index first); the 8 partial counts meet by shuffles.  Pairs ranked below top_k are
+  // recorded with their logit, and each chosen expert's row count is incremented.
+  template <int LEN>
+  __device__ __forceinline__ void rank_rows(const float* lg) {
+    const int B = p.B, E = p.E, K = p.K;
+    const int G = B >= 8 ? 8 : B >= 4 ? 4 : B >= 2 ? 2 : 1;
+    const int gsz = kConsumerThreads / G;
+    const int grp = threadIdx.x / gsz, gt = threadIdx.x - grp * gsz;
+    const int part = gt & 7, slot = gt >> 3, nslot = gsz >> 3;
+    const int e_lo = part * E / 8, e_hi = (part + 1) * E / 8;   // at most LEN values (E <= 8 * LEN)
+    const int ncand = (E + nslot - 1) / nslot;
+    for (int b0 = 0; b0 < B; b0 += G) {   // uniform trip counts: the shuffles below
+      const int b = b0 + grp;
+      const bool bon = b < B;
+      const float* row = lg + (bon ? b : 0) * E;
+      float sl[LEN];
+#pragma unroll
+      for (int k = 0; k < LEN; ++k) sl[k] = (e_lo + k < e_hi) ? row[e_lo + k] : -INFINITY;
+      for (int j = 0; j < ncand; ++j) {
+        const int e = slot + j * nslot;
+        const bool on = bon && e < E;
+        const float v = row[on ? e : 0];
+        int r0 = 0, r1 = 0;
+#pragma unroll
+        for (int k = 0; k < LEN; ++k) {
+          // padding (-inf, index past the slice) never counts: finite logits only exceed it
+          const int c = static_cast<int>(sl[k] > v) +
+                        (static_cast<int>(sl[k] == v) & static_cast<int>(e_lo + k < e) & static_cast<int>(e_lo + k < e_hi));
+          if (k & 1) r1 += c; else r0 += c;
+        }
+        int rank = r0 + r1;
+        rank += __shfl_xor_sync(0xffffffffu, rank, 1);
+        rank += __shfl_xor_sync(0xffffffffu, rank, 2);
+        rank += __shfl_xor_sync(0xffffffffu, rank, 4);
+        if (on && part == 0 && rank < K) {
+          S.rids[b * K + rank] = e;
+          S.rval[b * K + rank] = v;
+          atomicAdd(&S.ecnt[e], 1);
+        }
+      }
+    }
+  }
+
   // ------------------------------------------------------------------ routing (every block)
   // Every block routes the whole batch itself from the router logits (tagged words the
   // router tiles wrote), so the MoE of a layer needs nothing else from another block.
@@ -1545,55 +1592,25 @@ struct Consumer {
     if (!ok) ll_timeout(p, MK_OP_ROUTER, l);
     if (!cbar_and(ok)) return false;
     trace_mark(16, l);
-    for (int b = warp; b < B; b += kConsumerWarps) {
-      float mx = -INFINITY;
-      for (int e = lane; e < E; e += 32) mx = fmaxf(mx, lg[b * E + e]);
-      mx = warp_max(mx);
-      float z = 0.f;
-      for (int e = lane; e < E; e += 32) z += expf(lg[b * E + e] - mx);
-      z = warp_sum(z);
-      if (lane == 0) { S.rmax[b] = mx; S.rz[b] = z; }
-    }
-    {
-      const int n = B * E;
-      int q = 1;   // threads per (row, expert) pair
-      while (q < 8 && 2 * q * n <= kConsumerThreads) q <<= 1;
-      const int part = threadIdx.x & (q - 1);
-      const int e_lo = part * E / q, e_hi = (part + 1) * E / q;
-      for (int i0 = 0; i0 < n; i0 += kConsumerThreads / q) {   // uniform trip count: the shuffles below
-        const int i = i0 + static_cast<int>(threadIdx.x) / q;
-        const bool on = i < n;
-        const int b = on ? i / E : 0, e = on ? i - b * E : 0;
-        const float* row = lg + b * E;
-        const float v = row[e];
-        int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-        int e2 = e_lo;
-        for (; e2 + 4 <= e_hi; e2 += 4) {
-          const float a0 = row[e2], a1 = row[e2 + 1], a2 = row[e2 + 2], a3 = row[e2 + 3];
-          r0 += static_cast<int>(a0 > v) + (static_cast<int>(a0 == v) & static_cast<int>(e2 < e));
-          r1 += static_cast<int>(a1 > v) + (static_cast<int>(a1 == v) & static_cast<int>(e2 + 1 < e));
-          r2 += static_cast<int>(a2 > v) + (static_cast<int>(a2 == v) & static_cast<int>(e2 + 2 < e));
-          r3 += static_cast<int>(a3 > v) + (static_cast<int>(a3 == v) & static_cast<int>(e2 + 3 < e));
-        }
-        for (; e2 < e_hi; ++e2) {
-          const float a = row[e2];
-          r0 += static_cast<int>(a > v) + (static_cast<int>(a == v) & static_cast<int>(e2 < e));
-        }
-        int rank = (r0 + r1) + (r2 + r3);
-        for (int o = 1; o < q; o <<= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
-        if (on && part == 0 && rank < K) {
-          S.rids[b * K + rank] = e;
-          S.rval[b * K + rank] = v;
-          atomicAdd(&S.ecnt[e], 1);
-        }
+    if (!p.norm_topk) {   // weights over all experts need each row's max and normaliser
+      for (int b = warp; b < B; b += kConsumerWarps) {
+        float mx = -INFINITY;
+        for (int e = lane; e < E; e += 32) mx = fmaxf(mx, lg[b * E + e]);
+        mx = warp_max(mx);
+        float z = 0.f;
+        for (int e = lane; e < E; e += 32) z += expf(lg[b * E + e] - mx);
+        z = warp_sum(z);
+        if (lane == 0) { S.rmax[b] = mx; S.rz[b] = z; }
       }
     }
+    if (E <= 128) rank_rows<16>(lg); else rank_rows<32>(lg);
     cbar();
     trace_mark(18, l);
     // combine weights (a warp per row, a lane per slot) ...
     for (int b = warp; b < B; b += kConsumerWarps) {
       const int j = lane < K ? lane : 0;
-      const float ex = expf(S.rval[b * K + j] - S.rmax[b]);
+      const float mx = p.norm_topk ? S.rval[b * K] : S.rmax[b];   // rank 0 holds the row's largest logit
+      const float ex = expf(S.rval[b * K + j] - mx);
       const float sum = warp_sum(lane < K ? ex : 0.f);
       if (lane < K) {
         const int i = b * K + lane;
