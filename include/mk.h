@@ -61,6 +61,15 @@ typedef struct CUstream_st* mk_stream_t;
  *   page_size*head_dim*2 <= 32768 bytes, page_size a multiple of 8; max_batch <= 64;
  *   max_batch*(top_k+1)*ceil(hidden/SMs) <= 14336; max_batch*num_experts <= 14336.
  */
+/*
+ * mk_config.flags.  By default mk_create keeps a transposed device copy of every layer's
+ * w_down ([num_experts, expert_ffn, hidden], num_layers*num_experts*expert_ffn*hidden*2 bytes)
+ * so that steps of 1-2 rows run each expert's gate/up and down rows together on one SM
+ * (no exchange of SwiGLU activations between SMs).  MK_FLAG_NO_DOWN_COPY skips the copy;
+ * every batch then takes the general MoE path.  Results agree within rounding either way.
+ */
+#define MK_FLAG_NO_DOWN_COPY 1
+
 typedef struct mk_config {
   int32_t num_layers;
   int32_t hidden;
@@ -78,7 +87,7 @@ typedef struct mk_config {
   int32_t max_batch;         /* largest batch a step may use */
   int32_t max_pages_per_seq; /* row length of the block table */
   int32_t norm_topk;         /* 1: router weights renormalised over the k chosen experts; 0: raw softmax probs */
-  int32_t flags;             /* reserved, must be 0 */
+  int32_t flags;             /* 0 or MK_FLAG_NO_DOWN_COPY */
   uint32_t watchdog_ms;      /* per-wait device budget in ms; 0 selects the default (1000 ms) */
 } mk_config;
 
@@ -121,7 +130,8 @@ typedef struct mk_ctx mk_ctx;
  *                 pointers that must outlive the context.
  *   out:          receives the new context.
  * Allocates the library's workspace (per-layer activations, counters, task
- * lists, pinned staging).  Errors: MK_ERR_INVALID_ARG (null or non-positive or
+ * lists, pinned staging) and, unless cfg->flags has MK_FLAG_NO_DOWN_COPY, the
+ * transposed copy of the down projections, filled on the device before return.  Errors: MK_ERR_INVALID_ARG (null or non-positive or
  * misaligned argument), MK_ERR_UNSUPPORTED (device or shape outside the
  * build's limits), MK_ERR_OOM, MK_ERR_CUDA.
  */

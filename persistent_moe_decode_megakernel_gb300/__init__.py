@@ -171,8 +171,12 @@ def _check(rc):
     return rc
 
 
+# mk_config.flags: skip the transposed down-projection copy (every batch takes the general MoE path)
+FLAG_NO_DOWN_COPY = 1
+
+
 def make_config(model: dict, page_size: int, num_pages: int, max_batch: int, max_pages_per_seq: int,
-                watchdog_ms: int = 0) -> Config:
+                watchdog_ms: int = 0, flags: int = 0) -> Config:
     c = Config()
     c.num_layers, c.hidden, c.num_q_heads = model["layers"], model["hidden"], model["n_q"]
     c.num_kv_heads, c.head_dim, c.num_experts = model["n_kv"], model["head_dim"], model["n_exp"]
@@ -180,7 +184,7 @@ def make_config(model: dict, page_size: int, num_pages: int, max_batch: int, max
     c.rope_theta, c.rms_eps = float(model["rope_theta"]), float(model["rms_eps"])
     c.page_size, c.num_pages, c.max_batch, c.max_pages_per_seq = page_size, num_pages, max_batch, max_pages_per_seq
     c.norm_topk = int(model.get("norm_topk", 1))
-    c.flags = 0
+    c.flags = int(flags)
     c.watchdog_ms = int(watchdog_ms)
     return c
 
@@ -229,10 +233,10 @@ class Engine:
     """
 
     def __init__(self, model: dict, weights: dict, page_size: int, num_pages: int, max_batch: int,
-                 max_pages_per_seq: int, watchdog_ms: int = 0):
+                 max_pages_per_seq: int, watchdog_ms: int = 0, flags: int = 0):
         import torch
         self.model = dict(model)
-        self.cfg = make_config(model, page_size, num_pages, max_batch, max_pages_per_seq, watchdog_ms)
+        self.cfg = make_config(model, page_size, num_pages, max_batch, max_pages_per_seq, watchdog_ms, flags)
         self._keep = weights
         L = model["layers"]
         lws = (LayerWeights * L)()

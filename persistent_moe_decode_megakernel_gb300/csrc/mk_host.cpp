@@ -34,6 +34,7 @@
 namespace mk {
 cudaError_t launch_step(const Params& p, cudaStream_t s);
 int tb_for_batch(int B);
+cudaError_t transpose_down(const uint16_t* in, uint16_t* out, int E, int H, int F, cudaStream_t s);
 cudaError_t configure_kernels(int D);
 cudaError_t occupancy(int D, int* blocks);
 size_t smem_bytes();
@@ -82,7 +83,7 @@ int check_config(const mk_config* c) {
     if (f.v <= 0) return fail(MK_ERR_INVALID_ARG, "config.%s must be > 0 (got %d)", f.n, f.v);
   if (!(c->rope_theta > 0.f) || !(c->rms_eps >= 0.f)) return fail(MK_ERR_INVALID_ARG, "rope_theta must be > 0, rms_eps >= 0");
   if (c->norm_topk != 0 && c->norm_topk != 1) return fail(MK_ERR_INVALID_ARG, "norm_topk must be 0 or 1");
-  if (c->flags != 0) return fail(MK_ERR_INVALID_ARG, "flags must be 0");
+  if (c->flags & ~MK_FLAG_NO_DOWN_COPY) return fail(MK_ERR_INVALID_ARG, "unknown bits in flags");
   if (c->num_q_heads % c->num_kv_heads) return fail(MK_ERR_INVALID_ARG, "num_q_heads must be a multiple of num_kv_heads");
   if (c->top_k > c->num_experts) return fail(MK_ERR_INVALID_ARG, "top_k > num_experts");
   // limits of this build
@@ -101,6 +102,24 @@ int check_config(const mk_config* c) {
   if (c->max_batch > mk::kMaxBatch) return fail(MK_ERR_UNSUPPORTED, "max_batch > 64");
   if ((int64_t)c->max_pages_per_seq * c->page_size > (int64_t)1 << 30) return fail(MK_ERR_UNSUPPORTED, "sequence too long");
   return MK_OK;
+}
+
+// Whether a context on n_ctas SMs can run the small-batch MoE path at all: the SwiGLU
+// outputs of one block's gate/up units stay on chip (with at most kSmallMaxB rows every
+// unit costs the same, so a block gets at most units/n_ctas + 2 of them), and the partial
+// outputs of every block for the block's own hidden rows fit the reduction scratch.
+bool small_moe_fits(const mk_config& c, int n_ctas) {
+  if (c.flags & MK_FLAG_NO_DOWN_COPY) return false;
+  const int64_t act = std::min<int64_t>(c.num_experts, (int64_t)mk::kSmallMaxB * c.top_k);
+  if (act * c.expert_ffn / n_ctas + 2 > mk::kMaxUnits) return false;
+  const int64_t nr = (c.hidden + n_ctas - 1) / n_ctas;
+  return (int64_t)mk::kSmallMaxB * n_ctas * nr <= mk::kMoeScratch;
+}
+
+// the MoE path of one step: small-batch when the context has the transposed down copy and
+// the batch's MoE input fits the on-chip input cache
+bool small_moe_step(const mk_config& c, int n_ctas, int B) {
+  return small_moe_fits(c, n_ctas) && mk::small_moe_batch(B, c.hidden);
 }
 
 // ---------------------------------------------------------------- static plan
@@ -274,7 +293,9 @@ struct mk_ctx {
   uint8_t* ws = nullptr;
   // tagged 8-byte words (value | step tag << 32)
   uint64_t *X = nullptr, *QKV = nullptr, *ATT = nullptr, *PO = nullptr, *PML = nullptr, *RLOG = nullptr,
-           *HB = nullptr, *SS = nullptr;
+           *HB = nullptr, *SS = nullptr, *PT = nullptr;
+  uint16_t* wdt = nullptr;   // transposed down projections [L][E][F][H] (small-batch MoE path), or null
+  bool small_ok = false;
   float* RW = nullptr;
   int n_ss_slots = 0;
   int32_t* RIDS = nullptr;
@@ -337,6 +358,7 @@ void free_ctx(mk_ctx* c) {
   cudaFree(c->d_tasks);
   cudaFree(c->d_task_off);
   cudaFree(c->ws);
+  cudaFree(c->wdt);
   cudaFree(c->trace);
   for (int i = 0; i < 2; ++i) {
     if (c->h_step[i]) cudaFreeHost(c->h_step[i]);
@@ -415,13 +437,25 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_ctx** out) {
   c->inv_freq.resize(D / 2);
   for (int i = 0; i < D / 2; ++i) c->inv_freq[i] = std::pow((double)cfg->rope_theta, -2.0 * i / D);
 
+  c->small_ok = small_moe_fits(c->cfg, c->n_ctas);
+  const size_t dt_layer = (size_t)E * F * H;   // elements of one layer's down projections
+  if (c->small_ok) {
+    if ((e = cudaMalloc(&c->wdt, dt_layer * L * sizeof(uint16_t))) != cudaSuccess) {
+      free_ctx(c);
+      return cuda_fail(e, "transposed down projections");
+    }
+    for (int l = 0; l < L && e == cudaSuccess; ++l)
+      e = mk::transpose_down(static_cast<const uint16_t*>(w->layers[l].w_down), c->wdt + dt_layer * l, E, H, F, 0);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) { free_ctx(c); return cuda_fail(e, "down projection transpose"); }
+  }
   std::vector<mk::LayerW> lws(L);
   for (int l = 0; l < L; ++l) {
     const mk_layer_weights& s = w->layers[l];
     lws[l] = {static_cast<const uint16_t*>(s.attn_norm), static_cast<const uint16_t*>(s.w_qkv),
               static_cast<const uint16_t*>(s.w_o), static_cast<const uint16_t*>(s.ffn_norm),
               static_cast<const uint16_t*>(s.w_router), s.router_bias, static_cast<const uint16_t*>(s.w_gate_up),
-              static_cast<const uint16_t*>(s.w_down)};
+              static_cast<const uint16_t*>(s.w_down), c->wdt ? c->wdt + dt_layer * l : nullptr};
   }
   // workspace
   struct Part { void** ptr; size_t bytes; };
@@ -435,6 +469,7 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_ctx** out) {
       {(void**)&c->RLOG, (size_t)L * MB * E * w8},
       {(void**)&c->HB, (size_t)L * MB * K * F * w8},
       {(void**)&c->SS, (size_t)(2 * L + 1) * c->n_ctas * MB * w8},
+      {(void**)&c->PT, c->small_ok ? (size_t)L * c->n_ctas * mk::kSmallMaxB * H * w8 : 0},
       {(void**)&c->RIDS, (size_t)L * MB * K * i4},
       {(void**)&c->RW, (size_t)L * MB * K * f4},
       {(void**)&c->ctr, (size_t)c->plan.cm.total * 4},
@@ -562,6 +597,8 @@ int mk_decode_step(mk_ctx* c, int32_t batch, const int32_t* token_ids, const int
   p.RW = c->RW; p.HB = c->HB; p.SS = c->SS; p.n_ss_slots = c->n_ctas;
   // inputs wider than the staging scratch are read per warp and normalised with the SS words
   p.need_ss = (int64_t)mk::tb_for_batch(batch) * cf.hidden > mk::kMoeScratch ? 1 : 0;
+  p.small_moe = c->small_ok && mk::small_moe_batch(batch, cf.hidden) ? 1 : 0;
+  p.PT = c->PT;
   p.max_items = c->plan.info.max_items;
   // a fresh tag per step; tagged words of an earlier step never match it.  When the tag
   // wraps, the tagged buffers are cleared so that no word from 2^32 steps ago can match.
@@ -778,14 +815,19 @@ int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t B, const int32_t* 
     const int nact = (int)act[l].size();
     for (int j = 0; j <= n_ctas; ++j) gu_start[l].push_back(mk::moe_gu_start(j, n_ctas, cum.data(), cost.data(), nact, F));
   }
-  // coverage of the MoE work: gate/up units and (active expert, hidden row) pairs of the down projection
-  std::vector<std::vector<int>> gu_seen(L), dn_seen(L);
+  // coverage of the MoE work: gate/up units and (active expert, hidden row) pairs of the down
+  // projection, or on the small-batch path the transposed down row of every unit
+  const bool small = small_moe_step(*cfg, n_ctas, B);
+  std::vector<std::vector<int>> gu_seen(L), dn_seen(L), dt_seen(L);
   for (int l = 0; l < L; ++l) {
     gu_seen[l].assign(act[l].size() * F, 0);
     dn_seen[l].assign(act[l].size() * H, 0);
+    dt_seen[l].assign(act[l].size() * F, 0);
   }
 
-  // record kinds: a task op, or 100 = gate/up chunk, 101 = down chunk
+  // record kinds: a task op, or 100 = gate/up chunk, 101 = down chunk; small-batch path:
+  // 105 = gate/up chunk, 102 = transposed down chunk, 104 = publish the partial output,
+  // 103 = reduce every block's partials
   struct Rec { int kind; int task; int layer; uint32_t a; uint32_t x; int flags; };
   enum { F_FIRST = 1, F_LAST = 2, F_LAST_GU = 4 };
   struct Sm {
@@ -804,6 +846,25 @@ int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t B, const int32_t* 
     std::vector<Rec> r;
     const int nact = (int)act[l].size();
     const int u0 = gu_start[l][i], u1 = gu_start[l][i + 1];
+    if (small) {   // the device producer's small-batch loops
+      for (int u = u0; u < u1;) {
+        const int a = u / F, f0 = u % F, fend = std::min(F, u1 - a * F);
+        for (int g0 = f0; g0 < fend; g0 += 2 * fpc) {
+          const int gend = std::min(fend, g0 + 2 * fpc);
+          for (int f = g0; f < gend; f += fpc) {
+            const int n = std::min(fpc, gend - f);
+            for (int k = 0; k < n; ++k) gu_seen[l][(size_t)a * F + f + k]++;
+            r.push_back({105, task, l, (uint32_t)a, (uint32_t)f, 0});
+          }
+          for (int f = g0; f < gend; ++f) dt_seen[l][(size_t)a * F + f]++;
+          r.push_back({102, task, l, (uint32_t)a, (uint32_t)g0, 0});
+        }
+        u = a * F + fend;
+      }
+      r.push_back({104, task, l, 0, 0, 0});
+      r.push_back({103, task, l, 0, 0, 0});
+      return r;
+    }
     if (u0 >= u1) r.push_back({100, task, l, 0, 0, F_FIRST | F_LAST | F_LAST_GU});
     for (int u = u0; u < u1;) {
       const int a = u / F, f0 = u % F, fend = std::min(F, u1 - a * F);
@@ -888,6 +949,16 @@ int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t B, const int32_t* 
         if ((r.flags & F_FIRST) && ctr[base + mk::L_GU] < (uint32_t)n_ctas) return false;
         if (r.flags & F_LAST) ctr[base + mk::L_MOE]++;
         break;
+      case 102:
+      case 105:
+        break;
+      case 104:   // this block's partial output is published
+        ctr[base + mk::L_GU]++;
+        break;
+      case 103:   // the reduction needs every block's partial
+        if (ctr[base + mk::L_GU] < (uint32_t)n_ctas) return false;
+        ctr[base + mk::L_MOE]++;
+        break;
       case MK_OP_ROUTER:
         if (ctr[t.wait_ctr] < target(t)) return false;
         if (++ctr[base + mk::L_RARR] == (uint32_t)in.n_router_tiles) ctr[base + mk::L_RREADY] = 1;
@@ -937,7 +1008,7 @@ int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t B, const int32_t* 
   bool uok = true;
   for (int l = 0; l < L; ++l) {
     for (int v : gu_seen[l]) uok = uok && v == 1;
-    for (int v : dn_seen[l]) uok = uok && v == 1;
+    for (int v : (small ? dt_seen[l] : dn_seen[l])) uok = uok && v == 1;
   }
   out->moe_units_ok = uok;
   return MK_OK;

@@ -257,7 +257,8 @@ struct FastDiv {
 };
 
 // --------------------------------------------------------------------------- shared memory
-enum : uint8_t { R_EMBED = 1, R_GEMV = 2, R_ATTN = 3, R_GU = 4, R_DOWN = 5, R_END = 6, R_ROUTE = 7, R_COMBINE = 8 };
+enum : uint8_t { R_EMBED = 1, R_GEMV = 2, R_ATTN = 3, R_GU = 4, R_DOWN = 5, R_END = 6, R_ROUTE = 7, R_COMBINE = 8,
+                 R_DT = 9, R_RED = 10 };   // small-batch MoE: transposed down rows; partial-sum reduction
 // GEMV stream kinds beyond the task ops (MK_OP_QKV / OPROJ / ROUTER / HEAD)
 enum : int { R_OP_GU = 100 };
 
@@ -274,7 +275,6 @@ struct Meta {
 };
 static_assert(sizeof(Meta) == 64, "meta size");
 
-constexpr int kAttnScratch = 4 * kMaxG * (128 + 2);
 
 struct __align__(128) Smem {
   uint8_t ring[kSlots][kSlotBytes];
@@ -302,12 +302,15 @@ struct __align__(128) Smem {
   int32_t ecum[kMaxExperts + 1];
   int32_t nact;
   int32_t gu_lo, gu_hi;                   // this block's gate/up units
+  float hsm[kSmallMaxB * kMaxUnits];      // small-batch MoE: weighted SwiGLU outputs of this block's units
   uint64_t route_bar;                     // consumers -> producer: routing of the layer is in shared memory
   int32_t ykey;                           // layer whose normalised MoE input scr.attn holds, or -1
   uint32_t prod_count, cons_count;
   int32_t flag;
   int32_t is_last;
 };
+
+static_assert(sizeof(Smem) + 1024 <= 227 * 1024, "shared memory (with the 1024-byte alignment pad) exceeds 227 KB");
 
 // --------------------------------------------------------------------------- errors / waits
 __device__ __noinline__ void record_error(const Params& p, int code, int op, int layer, uint32_t ctr, uint32_t observed,
@@ -675,6 +678,7 @@ struct Producer {
     const int u0 = S.gu_lo, u1 = S.gu_hi;
     const LayerW& lw = p.layers[l];
     const int H = p.H, F = p.F;
+    if (p.small_moe) return small_moe_tasks(l, u0, u1);
     // gate/up
     const int fpc = gemv_rows_per_chunk(H) / 2;    // gate rows (and as many up rows) per chunk
     if (u0 >= u1) {
@@ -734,6 +738,57 @@ struct Producer {
       }
     }
     return true;
+  }
+
+  // Small-batch MoE records of layer l: this block's gate/up units [u0, u1) in groups of at
+  // most two gate/up chunks, each group followed by one chunk of the same FFN rows of the
+  // transposed down projection (so a group's SwiGLU outputs are consumed on this SM), then
+  // the reduction record: publish this block's partial output, sum every block's partials
+  // for the block's own hidden rows.
+  __device__ bool small_moe_tasks(int l, int u0, int u1) {
+    const LayerW& lw = p.layers[l];
+    const int H = p.H, F = p.F;
+    const int fpc = gemv_rows_per_chunk(H) / 2;   // 2 * fpc transposed down rows fill at most one slot
+    for (int u = u0; u < u1;) {
+      const int a = u / F, f0 = u - a * F;
+      const int fend = min(F, u1 - a * F);
+      const int e = S.eact[a];
+      const uint16_t* gate = lw.w_gate_up + static_cast<size_t>(e) * 2 * F * H;
+      for (int g0 = f0; g0 < fend; g0 += 2 * fpc) {
+        const int gend = min(fend, g0 + 2 * fpc);
+        for (int f = g0; f < gend; f += fpc) {
+          const int n = min(fpc, gend - f);
+          if (!acquire()) return false;
+          Meta& m = meta();
+          m.kind = R_GU; m.op = MK_OP_MOE; m.first = (f == g0); m.last = (f + n >= gend);
+          m.layer = static_cast<uint16_t>(l); m.n = static_cast<uint16_t>(n); m.row0 = f;
+          m.idx = static_cast<uint32_t>(a); m.e = static_cast<uint32_t>(e); m.aux = 1u;   // a group is one tile
+          m.wait_ctr = MK_NO_COUNTER; m.wait_target = 0; m.signal_ctr = MK_NO_COUNTER;
+          m.lo = g0; m.hi = gend;
+          const uint32_t bytes = static_cast<uint32_t>(n) * H * 2u;
+          mbar_arrive_expect_tx(full(), 2u * bytes);
+          bulk_g2s(slot(), gate + static_cast<size_t>(f) * H, bytes, full(), pol);
+          bulk_g2s(slot() + bytes, gate + static_cast<size_t>(F + f) * H, bytes, full(), pol);
+          ++c;
+        }
+        if (!acquire()) return false;
+        Meta& m = meta();
+        m.kind = R_DT; m.op = MK_OP_MOE; m.first = 1; m.last = 1;
+        m.layer = static_cast<uint16_t>(l); m.n = static_cast<uint16_t>(gend - g0); m.row0 = g0;
+        m.idx = static_cast<uint32_t>(a); m.e = static_cast<uint32_t>(e);
+        m.aux = static_cast<uint32_t>(a * F + g0 - u0);   // unit index of the chunk's first row
+        m.wait_ctr = MK_NO_COUNTER; m.wait_target = 0; m.signal_ctr = MK_NO_COUNTER;
+        m.lo = g0; m.hi = gend;
+        const uint32_t bytes = static_cast<uint32_t>(gend - g0) * H * 2u;
+        mbar_arrive_expect_tx(full(), bytes);
+        bulk_g2s(slot(), lw.w_down_t + (static_cast<size_t>(e) * F + g0) * H, bytes, full(), pol);
+        ++c;
+      }
+      u = a * F + fend;
+    }
+    const uint32_t r0 = static_cast<uint32_t>(static_cast<uint64_t>(H) * blockIdx.x / p.n_ctas);
+    const uint32_t r1 = static_cast<uint32_t>(static_cast<uint64_t>(H) * (blockIdx.x + 1) / p.n_ctas);
+    return moe_control(R_RED, l, r0, r1);
   }
 
   // an empty MoE record: a block with no gate/up units or no hidden rows still signals
@@ -1178,11 +1233,13 @@ struct Consumer {
     size_t sb, sj;        // strides per batch row and per routing slot
     const uint64_t* resid;  // O-proj: residual input rows this block wrote itself, else null
     const float* bias;    // router bias by matrix row, or null
+    float* hs;            // small-batch MoE: on-chip weighted SwiGLU outputs [kSmallMaxB][kMaxUnits], or null
+    int hoff;             // unit index (relative to the block's first) of FFN row 0 of the tile's expert
   };
 
   __device__ __forceinline__ OutMap out_map(int op, int l) const {
     const size_t MB = p.max_batch, xs = MB * p.H;
-    OutMap o{nullptr, nullptr, 0, 0, nullptr, nullptr};
+    OutMap o{nullptr, nullptr, 0, 0, nullptr, nullptr, nullptr, 0};
     switch (op) {
       case MK_OP_QKV: o.base = p.QKV + l * MB * p.nqkv; o.sb = p.nqkv; break;
       case MK_OP_OPROJ: o.base = p.X + (2 * l + 1) * xs; o.sb = p.H; o.resid = p.X + 2 * l * xs; break;
@@ -1199,7 +1256,15 @@ struct Consumer {
                                       float& my_ss, float rv = NAN) {
     if (j < 0) return;
     const size_t off = static_cast<size_t>(b) * o.sb + static_cast<size_t>(j) * o.sj + row;
-    if (gu) v = (v / (1.0f + expf(-v))) * v2;
+    if (gu) {
+      v = (v / (1.0f + expf(-v))) * v2;
+      // small-batch MoE: the combine weight is applied here, and the down projection of this
+      // block's own units reads the value from shared memory
+      if constexpr (TB <= kSmallMaxB) {
+        const int u = o.hoff + static_cast<int>(row);
+        if (o.hs != nullptr && u >= 0 && u < kMaxUnits) o.hs[b * kMaxUnits + u] = v * S.rwcache[b * p.K + j];
+      }
+    }
     if (o.resid != nullptr) {
       v += isnan(rv) ? ll_f(ll_ld(o.resid + off)) : rv;
       my_ss += v * v;
@@ -1356,7 +1421,9 @@ struct Consumer {
     const int B = p.B;
     const int lane = threadIdx.x & 31;
     const int K = op == MK_OP_OPROJ ? p.Hq * p.D : p.H;
-    const Seg<TB> sg(K, gu ? (nf0 >= kConsumerWarps ? 1 : kConsumerWarps / nf0) : 1);
+    // (the small-batch MoE path keeps whole rows per warp: split rows would reuse the storage of
+    // the cached MoE input, which every gate/up tile of the layer reads)
+    const Seg<TB> sg(K, gu && !p.small_moe ? (nf0 >= kConsumerWarps ? 1 : kConsumerWarps / nf0) : 1);
     // GEMV input: 0 x_in/attn_norm, 1 attention output, 2 x_mid/ffn_norm, 3 x_final/final_norm
     const int kind = op == MK_OP_QKV ? 0 : op == MK_OP_OPROJ ? 1 : (op == MK_OP_ROUTER || gu) ? 2 : 3;
     // the test hook waits for a tag that is never written
@@ -1369,7 +1436,11 @@ struct Consumer {
     const bool gu_fused = gu && B <= TB && S.ykey == l;
     const int cnt = gu_fused ? B : moe ? expert_pairs(e) : B;
     const int ngroups = kGroups ? (cnt + TB - 1) / TB : 1;
-    const OutMap om = out_map(op, l);
+    OutMap om = out_map(op, l);
+    if (TB <= kSmallMaxB && gu && p.small_moe) {
+      om.hs = S.hsm;
+      om.hoff = static_cast<int>(meta().idx) * p.F - S.gu_lo;
+    }
     float my_ss = 0.f;    // O-proj: sum of squares of the residual values this lane wrote
     int rb[TB], rj[TB];
     float y[8 / TB][8][TB];
@@ -1606,6 +1677,12 @@ struct Consumer {
     if (E <= 128) rank_rows<16>(lg); else rank_rows<32>(lg);
     cbar();
     trace_mark(18, l);
+    // small-batch MoE: the logits are consumed; the scratch becomes the [B][H] partial output
+    // (and a row that is not routed to a unit's expert contributes zero to it)
+    if (p.small_moe) {
+      for (int i = threadIdx.x; i < B * H; i += kConsumerThreads) S.moe[i] = 0.f;
+      for (int i = threadIdx.x; i < B * kMaxUnits; i += kConsumerThreads) S.hsm[i] = 0.f;
+    }
     // combine weights (a warp per row, a lane per slot) ...
     for (int b = warp; b < B; b += kConsumerWarps) {
       const int j = lane < K ? lane : 0;
@@ -1882,6 +1959,125 @@ struct Consumer {
   }
 
   __device__ bool moe_down() { return moe_down_t<(TB > 2 ? 2 : TB)>(); }
+
+  // ------------------------------------------------------------------ small-batch MoE
+  // One chunk of the transposed down projection: rows f = row0 .. row0+n-1 of expert idx
+  // ([H] each, bf16), whose weighted SwiGLU outputs this block computed in the preceding
+  // gate/up tile.  Thread t owns the 8-column groups c = 8 * (t + 256 k) of the [B][H] partial
+  // output in shared memory: it adds h_b[f] * Wd^T[f][c..c+8) for every row f (no reductions).
+  __device__ __forceinline__ bool moe_dt() {
+    const Meta m0 = meta();
+    const int H = p.H, B = p.B, n = m0.n, u0 = static_cast<int>(m0.aux);
+    twait = globaltimer();
+    const uint8_t* wsm = slot();
+    float* acc = S.moe;
+    const float* hs = S.hsm;
+    for (int c8 = threadIdx.x * 8; c8 < H; c8 += kConsumerThreads * 8) {
+      float a[kSmallMaxB][8];
+#pragma unroll
+      for (int tb = 0; tb < kSmallMaxB; ++tb) {
+        float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
+        if (tb < B) {
+          x0 = *reinterpret_cast<const float4*>(acc + tb * H + c8);
+          x1 = *reinterpret_cast<const float4*>(acc + tb * H + c8 + 4);
+        }
+        a[tb][0] = x0.x; a[tb][1] = x0.y; a[tb][2] = x0.z; a[tb][3] = x0.w;
+        a[tb][4] = x1.x; a[tb][5] = x1.y; a[tb][6] = x1.z; a[tb][7] = x1.w;
+      }
+#pragma unroll 4
+      for (int r = 0; r < n; ++r) {
+        float wf[8];
+        unpack8(*reinterpret_cast<const uint4*>(wsm + (static_cast<size_t>(r) * H + c8) * 2), wf);
+        const int u = u0 + r < kMaxUnits ? u0 + r : kMaxUnits - 1;
+#pragma unroll
+        for (int tb = 0; tb < kSmallMaxB; ++tb) {
+          if (tb < B) {
+            const float h = hs[tb * kMaxUnits + u];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) a[tb][q] = fmaf(h, wf[q], a[tb][q]);
+          }
+        }
+      }
+#pragma unroll
+      for (int tb = 0; tb < kSmallMaxB; ++tb) {
+        if (tb < B) {
+          *reinterpret_cast<float4*>(acc + tb * H + c8) = make_float4(a[tb][0], a[tb][1], a[tb][2], a[tb][3]);
+          *reinterpret_cast<float4*>(acc + tb * H + c8 + 4) = make_float4(a[tb][4], a[tb][5], a[tb][6], a[tb][7]);
+        }
+      }
+    }
+    return true;   // the next record starts behind a block barrier
+  }
+
+  // Reduction record of the small-batch MoE: publish this block's [B][H] partial output, then
+  // for the block's hidden rows [lo, hi): gather every block's partial (one batch of loads),
+  // sum them in block order per lane group and by a warp reduction, add x_mid, and write the
+  // layer output (and its sums of squares where a later input is too wide to stage).
+  __device__ __forceinline__ bool moe_reduce() {
+    const Meta m0 = meta();
+    const int l = m0.layer, B = p.B, H = p.H, N = p.n_ctas;
+    const int r0 = static_cast<int>(m0.lo), nrow = static_cast<int>(m0.hi) - r0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const size_t xs = static_cast<size_t>(p.max_batch) * H;
+    twait = globaltimer();
+    trace_mark(40, l);
+    {
+      uint64_t* mine = p.PT + (static_cast<size_t>(l) * N + blockIdx.x) * kSmallMaxB * H;
+      for (int i = threadIdx.x * 2; i < B * H; i += kConsumerThreads * 2) ll_st2(mine + i, S.moe[i], S.moe[i + 1], p.tag);
+    }
+    cbar();   // the partial output has been read out of the scratch
+    if (nrow <= 0) return true;
+    // one batch of loads: x_mid of the block's rows ([B][nrow], written by its O-proj tile),
+    // then every block's partial for them ([B][N][nrow])
+    const int ni = B * nrow;
+    const uint64_t* xmid = p.X + (2 * static_cast<size_t>(l) + 1) * xs + r0;
+    const uint64_t* pt = p.PT + static_cast<size_t>(l) * N * kSmallMaxB * H + r0;
+    const FastDiv dnr(nrow), dbn(N * nrow);   // indices below ni + B * N * nrow <= the scratch size < 2^16
+    bool ok = ll_gather(p, ni + B * N * nrow, [=](int i) {
+      if (i < ni) {
+        const int b = dnr.div(i);
+        return xmid + static_cast<size_t>(b) * H + (i - b * nrow);
+      }
+      const int q = i - ni, b = dbn.div(q), rem = q - b * N * nrow;
+      const int j = dnr.div(rem), rr = rem - j * nrow;
+      return pt + (static_cast<size_t>(j) * kSmallMaxB + b) * H + rr;
+    }, S.moe, p.tag);
+    if (!ok) ll_timeout(p, MK_OP_MOE, l);
+    if (!cbar_and(ok)) return false;
+    trace_mark(42, l);
+    const float* part = S.moe + ni;
+    uint64_t* ssout = p.SS + (static_cast<size_t>(2 * l + 2) * p.n_ss_slots + blockIdx.x) * p.max_batch;
+    float ssb[kSmallMaxB];
+#pragma unroll
+    for (int tb = 0; tb < kSmallMaxB; ++tb) ssb[tb] = 0.f;
+    for (int k = 0; k * kConsumerWarps < ni; ++k) {   // warp-uniform trip count
+      const int it = warp + k * kConsumerWarps;
+      const int b = it < ni ? it / nrow : 0, rr = it - b * nrow;
+      float v = 0.f;
+      if (it < ni)
+        for (int j = lane; j < N; j += 32) v += part[(b * N + j) * nrow + rr];
+      v = warp_sum(v);
+      if (it < ni) {
+        const float xv = S.moe[it] + v;
+        if (lane == 0) ll_st(p.X + (2 * static_cast<size_t>(l) + 2) * xs + static_cast<size_t>(b) * H + r0 + rr, xv, p.tag);
+#pragma unroll
+        for (int tb = 0; tb < kSmallMaxB; ++tb)
+          if (b == tb) ssb[tb] += xv * xv;
+      }
+    }
+    if (p.need_ss) {   // per row of the batch: this warp's share, then the block's sum
+#pragma unroll
+      for (int tb = 0; tb < kSmallMaxB; ++tb)
+        if (lane == 0) S.ssred[warp][tb] = ssb[tb];
+      cbar();
+      if (threadIdx.x < B) {
+        float t = 0.f;
+        for (int w = 0; w < kConsumerWarps; ++w) t += S.ssred[w][threadIdx.x];
+        ll_st(ssout + threadIdx.x, t, p.tag);
+      }
+    }
+    return true;
+  }
 
 
   // ------------------------------------------------------------------ attention split item
@@ -2253,10 +2449,17 @@ struct Consumer {
         case R_DOWN: ok = moe_down(); break;
         case R_ROUTE: ok = route_local(); break;
         case R_COMBINE: ok = attn_combine(); break;
+        case R_DT:   // small-batch MoE records exist only for batches of at most kSmallMaxB rows
+          if constexpr (TB <= kSmallMaxB) ok = moe_dt();
+          break;
+        case R_RED:
+          if constexpr (TB <= kSmallMaxB) ok = moe_reduce();
+          break;
         default: break;
       }
       if (!ok) break;
-      if (m0.kind != R_END) trace_event(m0.kind == R_ATTN || m0.kind == R_GU || m0.kind == R_DOWN ? TR_ITEM : TR_TILE,
+      if (m0.kind != R_END) trace_event(m0.kind == R_ATTN || m0.kind == R_GU || m0.kind == R_DOWN || m0.kind == R_DT ||
+                                                m0.kind == R_RED ? TR_ITEM : TR_TILE,
                                         m0, t0);
       trace_chunk_done();
       warp_release_record(S, c);

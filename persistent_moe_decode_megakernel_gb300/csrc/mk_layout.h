@@ -44,6 +44,21 @@ constexpr int kMaxCtas = 256;     // thread blocks (SMs) a step may use
 constexpr int kMoeScratch = 14336;  // floats of shared memory for the down projection of one block
 
 constexpr int kRouterRows = 8;    // router (expert) rows per router tile
+constexpr int kAttnScratch = 4 * kMaxG * (128 + 2);   // floats: attention prologue / cached MoE input
+
+// ---- small-batch MoE path ----------------------------------------------------------
+// For batches of at most kSmallMaxB rows whose MoE input fits the input cache, each block
+// runs its gate/up units end to end: gate/up rows, then the same FFN rows of the transposed
+// down projection (w_down_t, [E][F][H]), accumulated into an on-chip [B][H] partial output;
+// the blocks' partials are then summed per hidden row by the row's owner block.
+constexpr int kSmallMaxB = 2;
+constexpr int kMaxUnits = 256;    // gate/up units of one block whose SwiGLU outputs stay on chip
+// (a warp's register slice covers 2048/TB input values, TB the rows of a register group: the
+// gate/up rows must fit one warp whole, or split rows would reuse the input cache's storage)
+MK_HD bool small_moe_batch(int B, int H) {
+  const int tb = B <= 1 ? 1 : 2;
+  return B <= kSmallMaxB && tb * H <= 8 * kConsumerThreads && B * H <= kAttnScratch;
+}
 
 MK_HD int gemv_rows_per_chunk(int K) {
   int r = kSlotBytes / (2 * K);
@@ -116,6 +131,7 @@ struct LayerW {
   const float* router_bias;
   const uint16_t* w_gate_up;
   const uint16_t* w_down;
+  const uint16_t* w_down_t;   // [E][F][H] copy of w_down (small-batch MoE path), or null
 };
 
 struct alignas(64) Params {
@@ -167,6 +183,8 @@ struct alignas(64) Params {
   uint64_t* SS;    // [2L+1][n_ss_slots][max_batch] per-block sums of squares of the residual stream
   int32_t n_ss_slots;
   int32_t need_ss;      // some GEMV input is too wide to stage and reads SS (else SS is not written)
+  int32_t small_moe;    // this step runs the small-batch MoE path
+  uint64_t* PT;         // [L][n_ctas][kSmallMaxB][H] per-block partial MoE outputs (small-batch path)
   int32_t* RIDS;   // [L][max_batch][K] routing ids (copy kept by block 0 for inspection)
   float* RW;       // [L][max_batch][K] combine weights (same)
   uint32_t* ctr;   // [cm.total]

@@ -23,9 +23,9 @@ def to_device(w: dict, dev="cuda"):
     return out
 
 
-def engine_for(setup: dict, w_dev: dict, max_batch: int = 8, watchdog_ms: int = 0):
+def engine_for(setup: dict, w_dev: dict, max_batch: int = 8, watchdog_ms: int = 0, flags: int = 0):
     return mk.Engine(setup["model"], w_dev, setup["page_size"], setup["num_pages"], max_batch, setup["max_pages"],
-                     watchdog_ms=watchdog_ms)
+                     watchdog_ms=watchdog_ms, flags=flags)
 
 
 def gpu_step(eng, tokens_np, seq_lens_np, bt_np, kv_dev):

@@ -26,11 +26,11 @@ def built():
     mk.build()
 
 
-def _parity_one_step(setup, max_batch=8, check_layers=True):
+def _parity_one_step(setup, max_batch=8, check_layers=True, flags=0):
     orc = Oracle("f32")
     w_dev = to_device(setup["wt"])
     kv_dev = kv_to_device(setup["kv"])
-    eng = engine_for(setup, w_dev, max_batch=max_batch)
+    eng = engine_for(setup, w_dev, max_batch=max_batch, flags=flags)
     got = gpu_step(eng, setup["tokens"], setup["seq_lens"], setup["bt"], kv_dev)
     kv_ref = setup["kv"].copy()
     ref = orc.decode_step(setup["dims"], setup["wn"], setup["tokens"], setup["seq_lens"], setup["bt"], kv_ref)
@@ -77,6 +77,15 @@ def _parity_one_step(setup, max_batch=8, check_layers=True):
 def test_tiny_bs1_ctx64():
     s = tiny_setup(W.TINY, [65])
     _parity_one_step(s)
+
+
+@pytest.mark.parametrize("flags", [0, mk.FLAG_NO_DOWN_COPY])
+@pytest.mark.parametrize("model,lens", [(W.TINY, [65]), (W.TINY, [200, 3]), (MEDIUM, [300]), (MEDIUM, [1000, 65])])
+def test_both_moe_paths(model, lens, flags):
+    # batches of 1-2 rows run the small-batch MoE path (per-SM gate/up + transposed down rows,
+    # then a reduction of per-SM partials) unless the context was built without the transposed
+    # copy; either way the step must match the oracle
+    _parity_one_step(tiny_setup(model, lens), flags=flags)
 
 
 def test_tiny_deterministic():

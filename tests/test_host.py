@@ -180,6 +180,25 @@ def test_simulated_step_completes_30b_shapes():
         assert r.tiles_run[3] == len(mk.plan_attention(cfg, N_CTAS, lens)[0]) * cfg.num_layers
 
 
+@pytest.mark.parametrize("flags", [0, mk.FLAG_NO_DOWN_COPY])
+@pytest.mark.parametrize("B", [1, 2, 3])
+def test_simulated_moe_paths(B, flags):
+    # the small-batch path (B <= 2 with the transposed copy) and the general path both cover
+    # every gate/up unit and every down-projection element exactly once, without deadlock
+    cfg = mk.make_config(W.MOE30B, 16, 40000, 64, 2100, flags=flags)
+    for seed in range(3):
+        lens = [8193, 700, 33][:B]
+        r = mk.simulate(cfg, N_CTAS, lens, _random_routing(cfg, B, seed), seed=seed, lead=1 + seed)
+        assert r.finished and not r.deadlocked and r.counters_ok and r.moe_units_ok
+
+
+def test_config_flags_are_checked():
+    cfg = _cfg()
+    cfg.flags = 2
+    with pytest.raises(mk.MkError):
+        mk.plan_static(cfg, 8)
+
+
 def test_simulator_detects_a_missing_producer():
     # a routing table that names an out-of-range expert is rejected up front
     cfg = _cfg()
