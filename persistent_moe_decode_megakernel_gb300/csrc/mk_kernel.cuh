@@ -742,9 +742,9 @@ struct Producer {
 
   // Small-batch MoE records of layer l: this block's gate/up units [u0, u1) in groups of at
   // most two gate/up chunks, each group followed by one chunk of the same FFN rows of the
-  // transposed down projection (so a group's SwiGLU outputs are consumed on this SM), then
-  // the reduction record: publish this block's partial output, sum every block's partials
-  // for the block's own hidden rows.
+  // transposed down projection (so a group's SwiGLU outputs are consumed on this SM); the
+  // consumers run all of them as one tile.  Then the reduction record: publish this block's
+  // partial output, sum every block's partials for the block's own hidden rows.
   __device__ bool small_moe_tasks(int l, int u0, int u1) {
     const LayerW& lw = p.layers[l];
     const int H = p.H, F = p.F;
@@ -762,7 +762,7 @@ struct Producer {
           Meta& m = meta();
           m.kind = R_GU; m.op = MK_OP_MOE; m.first = (f == g0); m.last = (f + n >= gend);
           m.layer = static_cast<uint16_t>(l); m.n = static_cast<uint16_t>(n); m.row0 = f;
-          m.idx = static_cast<uint32_t>(a); m.e = static_cast<uint32_t>(e); m.aux = 1u;   // a group is one tile
+          m.idx = static_cast<uint32_t>(a); m.e = static_cast<uint32_t>(e); m.aux = 0u;   // the tile runs on
           m.wait_ctr = MK_NO_COUNTER; m.wait_target = 0; m.signal_ctr = MK_NO_COUNTER;
           m.lo = g0; m.hi = gend;
           const uint32_t bytes = static_cast<uint32_t>(n) * H * 2u;
@@ -773,7 +773,8 @@ struct Producer {
         }
         if (!acquire()) return false;
         Meta& m = meta();
-        m.kind = R_DT; m.op = MK_OP_MOE; m.first = 1; m.last = 1;
+        m.kind = R_DT; m.op = MK_OP_MOE; m.first = 1;
+        m.last = (a * F + gend >= u1);   // the block's last group ends the gate/up tile
         m.layer = static_cast<uint16_t>(l); m.n = static_cast<uint16_t>(gend - g0); m.row0 = g0;
         m.idx = static_cast<uint32_t>(a); m.e = static_cast<uint32_t>(e);
         m.aux = static_cast<uint32_t>(a * F + g0 - u0);   // unit index of the chunk's first row
@@ -1544,11 +1545,26 @@ struct Consumer {
       }
       if (!ok) { wok = false; break; }
       if (last && (!gu_fused || (meta().aux & 1u))) break;
-      if (!next_rec()) break;
+      bool got = next_rec();
+      if (TB <= kSmallMaxB && gu && p.small_moe) {
+        // small-batch MoE: the block's gate/up chunks and the transposed down chunk after each
+        // group are one tile; the warps move through it together (a down chunk reads every
+        // warp's SwiGLU outputs of the group)
+        if (!cbar_and(got)) break;
+        if (meta().kind == R_DT) {
+          moe_dt();
+          if (meta().last) break;
+          got = next_rec();
+          if (!cbar_and(got)) break;
+        }
+      } else if (!got) {
+        break;
+      }
       if (last) {   // the next gate/up run of this block: its expert's slots
         const int e2 = static_cast<int>(meta().e);
 #pragma unroll
         for (int tb = 0; tb < TB; ++tb) rj[tb] = tb < B ? slot_of(tb, e2) : -1;
+        if (TB <= kSmallMaxB && gu && p.small_moe) om.hoff = static_cast<int>(meta().idx) * p.F - S.gu_lo;
       }
     }
     if (!ok) ll_timeout(p, eop, l);
