@@ -58,8 +58,8 @@ typedef struct CUstream_st* mk_stream_t;
  *   head_dim in {64, 128}; num_q_heads % num_kv_heads == 0 with at most 8 query
  *   heads per KV head; hidden, num_q_heads*head_dim and expert_ffn multiples of 8
  *   and <= 4096, expert_ffn <= 1024; num_experts <= 256; top_k <= min(8, num_experts);
- *   page_size*head_dim*2 <= 32768 bytes, page_size a multiple of 8; max_batch <= 64;
- *   max_batch*(top_k+1)*ceil(hidden/SMs) <= 14336; max_batch*num_experts <= 14336.
+ *   page_size*head_dim*2 <= 34816 bytes, page_size a multiple of 8; max_batch <= 64;
+ *   max_batch*(top_k+1)*ceil(hidden/SMs) <= 12288; max_batch*num_experts <= 12288.
  */
 /*
  * mk_config.flags.  By default mk_create keeps a transposed device copy of every layer's

@@ -95,7 +95,8 @@ int check_config(const mk_config* c) {
   if (c->num_experts > mk::kMaxExperts) return fail(MK_ERR_UNSUPPORTED, "num_experts > 256");
   if (c->expert_ffn > 1024) return fail(MK_ERR_UNSUPPORTED, "expert_ffn > 1024");
   if (c->top_k > mk::kMaxTopK) return fail(MK_ERR_UNSUPPORTED, "top_k > 8");
-  if (c->page_size * c->head_dim * 2 > mk::kSlotBytes / 2) return fail(MK_ERR_UNSUPPORTED, "page_size*head_dim*2 > 32768");
+  if (c->page_size * c->head_dim * 2 > mk::kSlotBytes / 2)
+    return fail(MK_ERR_UNSUPPORTED, "page_size*head_dim*2 > %d", mk::kSlotBytes / 2);
   if (c->page_size % 8) return fail(MK_ERR_UNSUPPORTED, "page_size must be a multiple of 8");
   if ((int64_t)c->num_layers * c->num_pages * 2 * c->num_kv_heads * c->page_size >= ((int64_t)1 << 31))
     return fail(MK_ERR_UNSUPPORTED, "KV pool has 2^31 or more rows");

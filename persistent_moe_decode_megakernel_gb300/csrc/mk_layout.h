@@ -31,7 +31,7 @@ static_assert(kConsumerThreads * kConsumerRegs + 128 * kProducerRegs == kThreads
 
 // ---- shared-memory ring of weight / KV tiles --------------------------------
 constexpr int kSlots = 2;
-constexpr int kSlotBytes = 65536;
+constexpr int kSlotBytes = 69632;
 
 // ---- build limits --------------------------------------------------------------
 constexpr int kMaxBatch = 64;
@@ -41,7 +41,7 @@ constexpr int kMaxExperts = 256;
 constexpr int kMaxK = 4096;       // GEMV input length (two 16-byte units per thread)
 constexpr int kMaxRowsPerChunk = 32;
 constexpr int kMaxCtas = 256;     // thread blocks (SMs) a step may use
-constexpr int kMoeScratch = 14336;  // floats of shared memory for the down projection of one block
+constexpr int kMoeScratch = 12288;  // floats of shared memory for the down projection of one block
 
 constexpr int kRouterRows = 8;    // router (expert) rows per router tile
 constexpr int kAttnScratch = 4 * kMaxG * (128 + 2);   // floats: attention prologue / cached MoE input
