@@ -1752,19 +1752,21 @@ struct Consumer {
         if (a < nact) S.ecum[a + 1] = before + loc[k];
       }
       if (lane == 0) S.ecum[0] = 0;
+      __syncwarp();
+      // this block's gate/up units (the two ends by two lanes at once); the producer needs only
+      // the active list and this range, so this warp hands them over at once (the arrival
+      // releases the warp's writes, ordered by the warp barrier) while the other warps finish
+      // the combine weights
+      if (lane < 2) {
+        const int32_t u = moe_gu_start(blockIdx.x + lane, p.n_ctas, S.ecum, S.ecost, nact, p.F);
+        if (lane == 0) S.gu_lo = u; else S.gu_hi = u;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.route_bar);
     }
-    cbar();
-    trace_mark(19, l);
-    // this block's gate/up units: the two ends by two warps at once
-    if (lane == 0 && warp < 2) {
-      const int32_t u = moe_gu_start(blockIdx.x + warp, p.n_ctas, S.ecum, S.ecost, S.nact, p.F);
-      if (warp == 0) S.gu_lo = u; else S.gu_hi = u;
-    }
-    if (threadIdx.x == 0 && !cache_in) S.ykey = -1;
-    if (threadIdx.x == 0 && cache_in) S.ykey = l;
+    if (threadIdx.x == 0) S.ykey = cache_in ? l : -1;
     cbar();
     trace_mark(17, l);
-    if (threadIdx.x == 0) mbar_arrive(&S.route_bar);   // hand the routing to this block's producer
     return true;
   }
 
