@@ -159,6 +159,20 @@ int mk_decode_step(mk_ctx* ctx, int32_t batch, const int32_t* token_ids, const i
                    const int32_t* block_tables, void* kv_pages, float* logits_out, mk_stream_t stream);
 
 /*
+ * mk_decode_step plus greedy selection in the same launch: for every row b,
+ *   next_token[b] = the index of the largest logit (the lowest index among equal maxima),
+ *   margin[b]     = that logit minus the largest logit at any other index (0 at a tie),
+ * both computed on the device from the fp32 logits the step writes to logits_out (so they
+ * agree exactly with an argmax of logits_out).  next_token: device int32 [batch];
+ * margin: device fp32 [batch], or NULL.  Each SM reduces its own LM-head rows; the last SM
+ * to finish merges the SMs' (max, index, second) per row.  Other arguments, ownership and
+ * errors as mk_decode_step (MK_ERR_INVALID_ARG also for a NULL or misaligned next_token).
+ */
+int mk_decode_step_greedy(mk_ctx* ctx, int32_t batch, const int32_t* token_ids, const int32_t* seq_lens,
+                          const int32_t* block_tables, void* kv_pages, float* logits_out, int32_t* next_token,
+                          float* margin, mk_stream_t stream);
+
+/*
  * Wait for the last enqueued step and report device-side errors.  Fills `out`
  * and returns out->code (MK_OK when the step ran clean).  Reading clears the
  * record.  After an error the context stays usable.

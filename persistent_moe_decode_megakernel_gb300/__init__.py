@@ -129,7 +129,7 @@ class SimResult(ctypes.Structure):
                 ("moe_units_ok", ctypes.c_int32)]
 
 
-EXPORTS = ("mk_create", "mk_decode_step", "mk_get_status", "mk_last_error", "mk_destroy", "mk_plan_static",
+EXPORTS = ("mk_create", "mk_decode_step", "mk_decode_step_greedy", "mk_get_status", "mk_last_error", "mk_destroy", "mk_plan_static",
            "mk_plan_attention", "mk_simulate", "mk_debug_read", "mk_debug_inject_stall", "mk_num_ctas",
            "mk_debug_trace", "mk_debug_trace_read", "mk_paged_attention_noalloc")
 
@@ -148,6 +148,7 @@ def lib():
             vp, i32, u32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint32
             L.mk_create.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(Weights), ctypes.POINTER(vp)]
             L.mk_decode_step.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp]
+            L.mk_decode_step_greedy.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]
             L.mk_get_status.argtypes = [vp, ctypes.POINTER(Status)]
             L.mk_last_error.restype = ctypes.c_char_p
             L.mk_destroy.argtypes = [vp]
@@ -259,11 +260,13 @@ class Engine:
         self.n_ctas = lib().mk_num_ctas(self.ctx)
         self._last_b = 0
 
-    def step(self, tokens, seq_lens, block_tables, kv, logits=None, stream=None):
+    def step(self, tokens, seq_lens, block_tables, kv, logits=None, stream=None, greedy=False):
         """Enqueue one decode step on ``stream`` (default: torch's current stream).
 
         tokens: int32 CUDA [B]; seq_lens: host int32 sequence [B]; block_tables: int32
         CUDA [B, max_pages_per_seq]; kv: bf16 CUDA cache; logits: fp32 CUDA [B, V] or None.
+        Returns the logits, or with ``greedy`` the tuple (logits, next_token int32 [B],
+        margin fp32 [B]) selected on the device in the same launch.
         """
         import torch
         sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
@@ -277,6 +280,14 @@ class Engine:
         assert logits.is_cuda and logits.dtype == torch.float32 and logits.is_contiguous()
         if stream is None:
             stream = torch.cuda.current_stream()
+        if greedy:
+            nxt = torch.empty(B, dtype=torch.int32, device=tokens.device)
+            mrg = torch.empty(B, dtype=torch.float32, device=tokens.device)
+            _check(lib().mk_decode_step_greedy(self.ctx, B, _ptr(tokens), sl.ctypes.data, _ptr(block_tables),
+                                               _ptr(kv), _ptr(logits), _ptr(nxt), _ptr(mrg),
+                                               ctypes.c_void_p(stream.cuda_stream)))
+            self._last_b = B
+            return logits, nxt, mrg
         _check(lib().mk_decode_step(self.ctx, B, _ptr(tokens), sl.ctypes.data, _ptr(block_tables), _ptr(kv),
                                     _ptr(logits), ctypes.c_void_p(stream.cuda_stream)))
         self._last_b = B

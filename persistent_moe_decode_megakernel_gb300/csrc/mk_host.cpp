@@ -296,6 +296,7 @@ struct mk_ctx {
   uint64_t *X = nullptr, *QKV = nullptr, *ATT = nullptr, *PO = nullptr, *PML = nullptr, *RLOG = nullptr,
            *HB = nullptr, *SS = nullptr, *PT = nullptr;
   uint16_t* wdt = nullptr;   // transposed down projections [L][E][F][H] (small-batch MoE path), or null
+  float* argp = nullptr;     // greedy selection: per-block (max, second, index) of its LM-head rows
   bool small_ok = false;
   float* RW = nullptr;
   int n_ss_slots = 0;
@@ -472,6 +473,7 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_ctx** out) {
       {(void**)&c->SS, (size_t)(2 * L + 1) * c->n_ctas * MB * w8},
       {(void**)&c->PT, c->small_ok ? (size_t)L * c->n_ctas * mk::kSmallMaxB * H * w8 : 0},
       {(void**)&c->RIDS, (size_t)L * MB * K * i4},
+      {(void**)&c->argp, (size_t)c->n_ctas * MB * 4 * f4},
       {(void**)&c->RW, (size_t)L * MB * K * f4},
       {(void**)&c->ctr, (size_t)c->plan.cm.total * 4},
       {(void**)&c->d_status, sizeof(mk_status)},
@@ -524,8 +526,28 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_ctx** out) {
   return MK_OK;
 }
 
+static int decode_step(mk_ctx* c, int32_t batch, const int32_t* token_ids, const int32_t* seq_lens,
+                       const int32_t* block_tables, void* kv_pages, float* logits_out, int32_t* next_token,
+                       float* margin, mk_stream_t stream);
+
 int mk_decode_step(mk_ctx* c, int32_t batch, const int32_t* token_ids, const int32_t* seq_lens,
                    const int32_t* block_tables, void* kv_pages, float* logits_out, mk_stream_t stream) {
+  return decode_step(c, batch, token_ids, seq_lens, block_tables, kv_pages, logits_out, nullptr, nullptr, stream);
+}
+
+int mk_decode_step_greedy(mk_ctx* c, int32_t batch, const int32_t* token_ids, const int32_t* seq_lens,
+                          const int32_t* block_tables, void* kv_pages, float* logits_out, int32_t* next_token,
+                          float* margin, mk_stream_t stream) {
+  g_err.clear();
+  if (!next_token) return fail(MK_ERR_INVALID_ARG, "next_token is NULL");
+  if ((reinterpret_cast<uintptr_t>(next_token) | reinterpret_cast<uintptr_t>(margin)) & 3u)
+    return fail(MK_ERR_INVALID_ARG, "next_token and margin must be 4-byte aligned");
+  return decode_step(c, batch, token_ids, seq_lens, block_tables, kv_pages, logits_out, next_token, margin, stream);
+}
+
+static int decode_step(mk_ctx* c, int32_t batch, const int32_t* token_ids, const int32_t* seq_lens,
+                       const int32_t* block_tables, void* kv_pages, float* logits_out, int32_t* next_token,
+                       float* margin, mk_stream_t stream) {
   g_err.clear();
   if (!c) return fail(MK_ERR_INVALID_ARG, "ctx is NULL");
   const mk_config& cf = c->cfg;
@@ -600,6 +622,7 @@ int mk_decode_step(mk_ctx* c, int32_t batch, const int32_t* token_ids, const int
   p.need_ss = (int64_t)mk::tb_for_batch(batch) * cf.hidden > mk::kMoeScratch ? 1 : 0;
   p.small_moe = c->small_ok && mk::small_moe_batch(batch, cf.hidden) ? 1 : 0;
   p.PT = c->PT;
+  p.next_token = next_token; p.margin = margin; p.argp = c->argp;
   p.max_items = c->plan.info.max_items;
   // a fresh tag per step; tagged words of an earlier step never match it.  When the tag
   // wraps, the tagged buffers are cleared so that no word from 2^32 steps ago can match.

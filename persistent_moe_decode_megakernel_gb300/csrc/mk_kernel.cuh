@@ -230,6 +230,36 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// Greedy selection state over (value, index) pairs: m1 the largest value, i1 its lowest index,
+// m2 the largest value at any other index.
+struct Top2 {
+  float m1, m2;
+  int i1;
+};
+__device__ __forceinline__ void top2_add(Top2& t, float v, int i) {
+  if (v > t.m1 || (v == t.m1 && i < t.i1)) { t.m2 = t.m1; t.m1 = v; t.i1 = i; }
+  else t.m2 = fmaxf(t.m2, v);
+}
+__device__ __forceinline__ void top2_merge(Top2& t, const Top2& o) {   // (m1 >= m2 on both sides)
+  if (o.m1 > t.m1 || (o.m1 == t.m1 && o.i1 < t.i1)) {
+    t.m2 = fmaxf(t.m1, o.m2);
+    t.m1 = o.m1;
+    t.i1 = o.i1;
+  } else {
+    t.m2 = fmaxf(t.m2, o.m1);
+  }
+}
+__device__ __forceinline__ void top2_warp(Top2& t) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    Top2 x;
+    x.m1 = __shfl_xor_sync(0xffffffffu, t.m1, o);
+    x.m2 = __shfl_xor_sync(0xffffffffu, t.m2, o);
+    x.i1 = __shfl_xor_sync(0xffffffffu, t.i1, o);
+    top2_merge(t, x);
+  }
+}
+
 // Two warp sums at once (a[tb] and b[tb] for every tb): afterwards lanes 0-15 hold the sums
 // of a and lanes 16-31 the sums of b.  Five shuffles per tb instead of ten.
 template <int TB>
@@ -1569,6 +1599,7 @@ struct Consumer {
     }
     if (!ok) ll_timeout(p, eop, l);
     if (!cbar_and(wok && ok)) return false;
+    if (op == MK_OP_HEAD && p.next_token != nullptr) head_top2(lo, hi);
     if (op == MK_OP_OPROJ && p.need_ss) {
       // publish this tile's share of sum(x_mid^2) for the RMSNorm of the MoE input
       uint64_t* out = p.SS + (static_cast<size_t>(2 * l + 1) * p.n_ss_slots + blockIdx.x) * p.max_batch;
@@ -1576,6 +1607,37 @@ struct Consumer {
       else oproj_ss_wide(l, lo, hi, out);
     }
     return true;
+  }
+
+  // Greedy selection, first level: this block's (max, index, second) of its LM-head rows
+  // [lo, hi) for every row of the batch, from the logits it has just written (a block
+  // barrier separates the writes from these reads), into p.argp.
+  __device__ __forceinline__ void head_top2(uint32_t lo, uint32_t hi) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int b = 0; b < p.B; ++b) {
+      Top2 t{-INFINITY, -INFINITY, 0x7fffffff};
+      const float* row = p.logits + static_cast<size_t>(b) * p.V;
+      for (uint32_t r = lo + threadIdx.x; r < hi; r += kConsumerThreads) top2_add(t, row[r], static_cast<int>(r));
+      top2_warp(t);
+      if (lane == 0) {
+        S.ssred[warp][0] = t.m1;
+        S.ssred[warp][1] = t.m2;
+        S.ssred[warp][2] = __int_as_float(t.i1);
+      }
+      cbar();
+      if (threadIdx.x == 0) {
+        Top2 a{S.ssred[0][0], S.ssred[0][1], __float_as_int(S.ssred[0][2])};
+        for (int w = 1; w < kConsumerWarps; ++w) {
+          const Top2 o{S.ssred[w][0], S.ssred[w][1], __float_as_int(S.ssred[w][2])};
+          top2_merge(a, o);
+        }
+        float* out = p.argp + (static_cast<size_t>(blockIdx.x) * p.max_batch + b) * 4;
+        out[0] = a.m1;
+        out[1] = a.m2;
+        out[2] = __int_as_float(a.i1);
+      }
+      cbar();
+    }
   }
 
   // sums of squares of this O-proj tile's rows for every batch row (batches wider than TB)
@@ -2561,6 +2623,28 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
   __syncthreads();
   if (S.is_last) {
     for (uint32_t i = tid; i < p.cm.total; i += kThreads) p.ctr[i] = 0u;
+    // Greedy selection, second level: every other block has finished (their partials are
+    // ordered before their arrivals on the finish counter, which this block acquired); a warp
+    // per row of the batch merges the blocks' partials, read through L2.
+    if (p.next_token != nullptr && !aborted(p)) {
+      const int warp = tid >> 5, lane = tid & 31;
+      for (int b = warp; b < p.B; b += kThreads / 32) {
+        Top2 t{-INFINITY, -INFINITY, 0x7fffffff};
+        for (int j = lane; j < static_cast<int>(gridDim.x); j += 32) {
+          // (blocks with no LM-head rows -- the host's split of the vocabulary -- wrote nothing)
+          const uint64_t V = static_cast<uint64_t>(p.V), N = gridDim.x;
+          if (V * (j + 1) / N == V * j / N) continue;
+          const float* a = p.argp + (static_cast<size_t>(j) * p.max_batch + b) * 4;
+          const Top2 o{__ldcg(a), __ldcg(a + 1), __float_as_int(__ldcg(a + 2))};
+          top2_merge(t, o);
+        }
+        top2_warp(t);
+        if (lane == 0) {
+          p.next_token[b] = t.i1;
+          if (p.margin != nullptr) p.margin[b] = t.m1 - t.m2;
+        }
+      }
+    }
   }
 }
 

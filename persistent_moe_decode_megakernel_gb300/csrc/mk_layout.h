@@ -185,6 +185,9 @@ struct alignas(64) Params {
   int32_t need_ss;      // some GEMV input is too wide to stage and reads SS (else SS is not written)
   int32_t small_moe;    // this step runs the small-batch MoE path
   uint64_t* PT;         // [L][n_ctas][kSmallMaxB][H] per-block partial MoE outputs (small-batch path)
+  int32_t* next_token;  // greedy selection: [B] argmax of the logits, or null (not requested)
+  float* margin;        // [B] top-1 minus top-2 logit, or null
+  float* argp;          // [n_ctas][max_batch][4] per-block (max, second, index bits) of its LM-head rows
   int32_t* RIDS;   // [L][max_batch][K] routing ids (copy kept by block 0 for inspection)
   float* RW;       // [L][max_batch][K] combine weights (same)
   uint32_t* ctr;   // [cm.total]

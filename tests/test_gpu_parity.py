@@ -88,6 +88,37 @@ def test_both_moe_paths(model, lens, flags):
     _parity_one_step(tiny_setup(model, lens), flags=flags)
 
 
+@pytest.mark.parametrize("model,lens", [(W.TINY, [65]), (W.TINY, [200, 3, 17, 9, 64, 1, 30, 511]), (MEDIUM, [300, 20])])
+def test_greedy_selection(model, lens):
+    # next_token / margin from the same launch: exactly the argmax (lowest index at a tie) and
+    # top-1 minus top-2 of the logits the step wrote, and the oracle's argmax where its margin
+    # exceeds MARGIN
+    s = tiny_setup(model, lens)
+    w_dev = to_device(s["wt"])
+    eng = engine_for(s, w_dev)
+    kv = kv_to_device(s["kv"])
+    tok = torch.from_numpy(np.ascontiguousarray(s["tokens"], dtype=np.int32)).cuda()
+    bt = torch.from_numpy(np.ascontiguousarray(s["bt"], dtype=np.int32)).cuda()
+    logits, nxt, mrg = eng.step(tok, s["seq_lens"], bt, kv, greedy=True)
+    torch.cuda.synchronize()
+    eng.check()
+    lg = logits.cpu().numpy()
+    nxt, mrg = nxt.cpu().numpy(), mrg.cpu().numpy()
+    for b in range(lg.shape[0]):
+        i = int(np.argmax(lg[b]))
+        assert nxt[b] == i
+        rest = np.delete(lg[b], i)
+        assert mrg[b] == np.float32(lg[b][i] - rest.max())
+    ref = Oracle("f32").decode_step(s["dims"], s["wn"], s["tokens"], s["seq_lens"], s["bt"], s["kv"].copy())
+    for b in range(lg.shape[0]):
+        if top2_margin(ref[b]) > MARGIN:
+            assert int(nxt[b]) == int(np.argmax(ref[b]))
+    # a plain step afterwards leaves the greedy buffers alone and agrees on the logits
+    again = gpu_step(eng, s["tokens"], s["seq_lens"], s["bt"], kv_to_device(s["kv"]))
+    assert np.array_equal(again.view(np.uint32), lg.view(np.uint32))
+    eng.close()
+
+
 def test_tiny_deterministic():
     s = tiny_setup(W.TINY, [65, 7, 300])
     w_dev = to_device(s["wt"])
