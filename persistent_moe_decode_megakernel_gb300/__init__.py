@@ -131,7 +131,9 @@ class SimResult(ctypes.Structure):
 
 EXPORTS = ("mk_create", "mk_decode_step", "mk_decode_step_greedy", "mk_get_status", "mk_last_error", "mk_destroy", "mk_plan_static",
            "mk_plan_attention", "mk_simulate", "mk_debug_read", "mk_debug_inject_stall", "mk_num_ctas",
-           "mk_debug_trace", "mk_debug_trace_read", "mk_paged_attention_noalloc")
+           "mk_debug_trace", "mk_debug_trace_read", "mk_paged_attention_noalloc", "mk_kv_pool_create",
+           "mk_kv_pool_destroy", "mk_kv_admit", "mk_kv_reserve", "mk_kv_evict", "mk_kv_fill", "mk_kv_free_pages",
+           "mk_kv_len")
 
 _lib = None
 _lock = threading.Lock()
@@ -149,6 +151,15 @@ def lib():
             L.mk_create.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(Weights), ctypes.POINTER(vp)]
             L.mk_decode_step.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp]
             L.mk_decode_step_greedy.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+            L.mk_kv_pool_create.argtypes = [i32, i32, i32, i32, vp, ctypes.POINTER(vp)]
+            L.mk_kv_pool_destroy.argtypes = [vp]
+            L.mk_kv_pool_destroy.restype = None
+            L.mk_kv_admit.argtypes = [vp, i32, ctypes.POINTER(i32)]
+            L.mk_kv_reserve.argtypes = [vp, i32, i32]
+            L.mk_kv_evict.argtypes = [vp, i32]
+            L.mk_kv_fill.argtypes = [vp, vp, i32, vp, vp]
+            L.mk_kv_free_pages.argtypes = [vp]
+            L.mk_kv_len.argtypes = [vp, i32]
             L.mk_get_status.argtypes = [vp, ctypes.POINTER(Status)]
             L.mk_last_error.restype = ctypes.c_char_p
             L.mk_destroy.argtypes = [vp]
@@ -218,6 +229,55 @@ def simulate(cfg: Config, n_ctas: int, seq_lens, routing_ids, seed: int = 0, lea
     _check(lib().mk_simulate(ctypes.byref(cfg), n_ctas, sl.size, sl.ctypes.data, ids.ctypes.data, seed, lead,
                              ctypes.byref(r)))
     return r
+
+
+# ---------------------------------------------------------------- paged-KV block allocator
+class KvPool:
+    """Host-side page bookkeeping for continuous batching (``include/mk_kv.h``): a FIFO free
+    list of pool pages and sequence slots, and the step's ``seq_lens`` / block tables."""
+
+    def __init__(self, num_pages: int, page_size: int, max_slots: int, max_pages_per_seq: int, order=None):
+        self.page_size, self.max_pages = page_size, max_pages_per_seq
+        ptr = ctypes.c_void_p()
+        o = None if order is None else np.ascontiguousarray(order, dtype=np.int32)
+        _check(lib().mk_kv_pool_create(num_pages, page_size, max_slots, max_pages_per_seq,
+                                       None if o is None else o.ctypes.data, ctypes.byref(ptr)))
+        self.pool = ptr
+
+    def admit(self, length: int) -> int:
+        slot = ctypes.c_int32()
+        _check(lib().mk_kv_admit(self.pool, int(length), ctypes.byref(slot)))
+        return slot.value
+
+    def reserve(self, slot: int, length: int):
+        _check(lib().mk_kv_reserve(self.pool, int(slot), int(length)))
+
+    def evict(self, slot: int):
+        _check(lib().mk_kv_evict(self.pool, int(slot)))
+
+    def fill(self, slots):
+        sl = np.ascontiguousarray(slots, dtype=np.int32)
+        lens = np.zeros(sl.size, dtype=np.int32)
+        bt = np.zeros((sl.size, self.max_pages), dtype=np.int32)
+        _check(lib().mk_kv_fill(self.pool, sl.ctypes.data, sl.size, lens.ctypes.data, bt.ctypes.data))
+        return lens, bt
+
+    def free_pages(self) -> int:
+        return lib().mk_kv_free_pages(self.pool)
+
+    def length(self, slot: int) -> int:
+        return lib().mk_kv_len(self.pool, int(slot))
+
+    def close(self):
+        if self.pool:
+            lib().mk_kv_pool_destroy(self.pool)
+            self.pool = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 # ---------------------------------------------------------------- the engine

@@ -158,7 +158,9 @@ def test_medium_batch_above_register_group():
 def test_tiny_bs8_ragged_continuous_batching():
     """32 greedy steps, teacher-forced with the oracle's argmax; at step 16 row 0
     finishes and a new sequence (length U{1..512}, prefilled by the oracle) takes
-    its place with fresh pages from the shuffled free list."""
+    its place.  The pages come from the library's block allocator (include/mk_kv.h):
+    its free list starts in the seeded shuffled order the setup dealt, rows grow a
+    page when they cross a page boundary, and the evicted row's pages return to it."""
     wl = W.get("tiny_bs8_ragged")
     lens = list(wl.lengths)
     s = tiny_setup(W.TINY, lens, extra_pages=36)
@@ -167,8 +169,11 @@ def test_tiny_bs8_ragged_continuous_batching():
     w_dev = to_device(s["wt"])
     kv_dev = kv_to_device(s["kv"])
     kv_ref = s["kv"]
-    bt = s["bt"].copy()
-    free = list(s["free"])
+    B = len(lens)
+    order = np.concatenate([s["bt"][b, :-(-L // ps)] for b, L in enumerate(lens)] + [np.array(s["free"], np.int32)])
+    pool = mk.KvPool(s["num_pages"], ps, B, s["max_pages"], order=order)
+    slots = [pool.admit(L) for L in lens]
+    assert np.array_equal(pool.fill(slots)[1], s["bt"])      # the setup's block tables, reproduced
     eng = engine_for(s, w_dev)
     tokens = s["tokens"].copy()
     seq = np.array(lens, dtype=np.int32)
@@ -176,35 +181,34 @@ def test_tiny_bs8_ragged_continuous_batching():
     compared = 0
     for step in range(wl.steps):
         if step == wl.admit_step:
-            # evict row 0, admit a new sequence
-            n_old = (seq[0] - 1 + ps - 1) // ps
-            free.extend(int(p) for p in bt[0, :n_old])
+            # evict row 0, admit a new sequence in its slot
+            pool.evict(slots[0])
             newlen = int(torch.randint(1, 513, (1,), generator=g))
             prefix = torch.randint(0, m["vocab"], (newlen,), generator=g).numpy().astype(np.int32)
-            npg = (newlen + ps - 1) // ps
-            bt[0, :] = -1
-            bt[0, :npg] = free[:npg]
-            del free[:npg]
+            slots[0] = pool.admit(newlen)
+            bt0 = pool.fill([slots[0]])[1]
             for t in range(newlen - 1):
-                orc.decode_step(s["dims"], s["wn"], prefix[t:t + 1], np.array([t + 1], np.int32), bt[:1], kv_ref)
-            pages = torch.tensor(bt[0, :npg].astype(np.int64))
+                orc.decode_step(s["dims"], s["wn"], prefix[t:t + 1], np.array([t + 1], np.int32), bt0, kv_ref)
+            npg = -(-newlen // ps)
+            pages = torch.tensor(bt0[0, :npg].astype(np.int64))
             kv_dev[:, pages.cuda()] = kv_to_device(kv_ref)[:, pages.cuda()]
             seq[0] = newlen
             tokens[0] = prefix[-1]
-        for b in range(len(seq)):   # a row that crosses a page boundary gets the next free page
-            need = (int(seq[b]) + ps - 1) // ps
-            if bt[b, need - 1] < 0:
-                bt[b, need - 1] = free.pop(0)
+        for b in range(B):   # a row that crosses a page boundary gets the next free page
+            pool.reserve(slots[b], int(seq[b]))
+        lens_now, bt = pool.fill(slots)
+        assert np.array_equal(lens_now, seq)
         got = gpu_step(eng, tokens, seq, bt, kv_dev)
         ref = orc.decode_step(s["dims"], s["wn"], tokens, seq, bt, kv_ref)
         assert rel_l2(got, ref) <= TOL_LOGITS, (step, rel_l2(got, ref))
-        for b in range(len(seq)):
+        for b in range(B):
             if top2_margin(ref[b]) > MARGIN:
                 assert int(np.argmax(got[b])) == int(np.argmax(ref[b])), (step, b)
                 compared += 1
         tokens = np.argmax(ref, axis=1).astype(np.int32)
         seq = seq + 1
     assert compared > 100
+    pool.close()
     eng.close()
 
 
