@@ -88,6 +88,13 @@ def test_both_moe_paths(model, lens, flags):
     _parity_one_step(tiny_setup(model, lens), flags=flags)
 
 
+@pytest.mark.parametrize("lens", [[65], [200, 3], [40, 3, 70, 1]])
+def test_router_weights_over_all_experts(lens):
+    # norm_topk = 0: the combine weights are the softmax over all experts (not renormalised
+    # over the chosen k), on the small-batch and the general MoE paths
+    _parity_one_step(tiny_setup(dict(W.TINY, norm_topk=0), lens))
+
+
 @pytest.mark.parametrize("model,lens", [(W.TINY, [65]), (W.TINY, [200, 3, 17, 9, 64, 1, 30, 511]), (MEDIUM, [300, 20])])
 def test_greedy_selection(model, lens):
     # next_token / margin from the same launch: exactly the argmax (lowest index at a tie) and
