@@ -133,6 +133,11 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -515,8 +520,11 @@ struct Producer {
   uint32_t c = 0;
   uint32_t pev = 0;   // producer trace events (written from the end of the block's trace area)
   uint32_t rphase = 0;  // parity of the next routing hand-over from the consumers
-  uint64_t pol;
-  __device__ Producer(const Params& p_, Smem& S_) : p(p_), S(S_) { pol = policy_evict_first(); }
+  uint64_t pol, pol_reuse;
+  __device__ Producer(const Params& p_, Smem& S_) : p(p_), S(S_) {
+    pol = policy_evict_first();
+    pol_reuse = policy_evict_normal();
+  }
 
   // Warm L2 with (at most kPrefetchBytes of) a task's weights or KV pages, so that the ring's
   // copies of a phase that starts after a dependency wait come from L2.
@@ -609,18 +617,27 @@ struct Producer {
       default: W = p.lm_head; K = p.H; break;
     }
     const int rpc = gemv_rows_per_chunk(K);
-    for (uint32_t r0 = t.lo; r0 < t.hi; r0 += rpc) {
-      const uint32_t n = min(static_cast<uint32_t>(rpc), t.hi - r0);
-      if (!acquire()) return false;
-      Meta& m = meta();
-      m.kind = R_GEMV; m.op = static_cast<uint8_t>(t.op); m.first = (r0 == t.lo); m.last = (r0 + n >= t.hi);
-      m.layer = t.layer; m.n = static_cast<uint16_t>(n); m.row0 = r0; m.idx = ti; m.e = 0; m.aux = 0;
-      m.wait_ctr = t.wait_ctr; m.wait_target = t.wait_base + t.wait_per_b * static_cast<uint32_t>(p.B);
-      m.signal_ctr = t.signal_ctr; m.lo = t.lo; m.hi = t.hi;
-      const uint32_t bytes = n * static_cast<uint32_t>(K) * 2u;
-      mbar_arrive_expect_tx(full(), bytes);
-      bulk_g2s(slot(), W + static_cast<size_t>(r0) * K, bytes, full(), pol);
-      ++c;
+    // A batch wider than one register group (groups of 4 rows) is served group-major: the tile
+    // is streamed once per group (aux = group), so the consumers stage each group's input once
+    // per tile; the repeated reads of the tile come from L2 (evict-normal while it is reused).
+    const int ng = p.B > 2 ? (p.B + 3) / 4 : 1;
+    const uint64_t pl = ng > 1 ? pol_reuse : pol;
+    for (int g = 0; g < ng; ++g) {
+      for (uint32_t r0 = t.lo; r0 < t.hi; r0 += rpc) {
+        const uint32_t n = min(static_cast<uint32_t>(rpc), t.hi - r0);
+        if (!acquire()) return false;
+        Meta& m = meta();
+        m.kind = R_GEMV; m.op = static_cast<uint8_t>(t.op); m.first = (g == 0 && r0 == t.lo);
+        m.last = (g == ng - 1 && r0 + n >= t.hi);
+        m.layer = t.layer; m.n = static_cast<uint16_t>(n); m.row0 = r0; m.idx = ti; m.e = 0;
+        m.aux = static_cast<uint32_t>(g);
+        m.wait_ctr = t.wait_ctr; m.wait_target = t.wait_base + t.wait_per_b * static_cast<uint32_t>(p.B);
+        m.signal_ctr = t.signal_ctr; m.lo = t.lo; m.hi = t.hi;
+        const uint32_t bytes = n * static_cast<uint32_t>(K) * 2u;
+        mbar_arrive_expect_tx(full(), bytes);
+        bulk_g2s(slot(), W + static_cast<size_t>(r0) * K, bytes, full(), g == ng - 1 ? pol : pl);
+        ++c;
+      }
     }
     return true;
   }
@@ -1417,7 +1434,8 @@ struct Consumer {
 
   __device__ __forceinline__ bool stream_load(const Seg<TB>& sg, bool moe, int kind, int l, int b0, int nt,
                                               uint32_t tag, int op, int (&rb)[TB], int (&rj)[TB],
-                                              float (&y)[8 / TB][8][TB]) {
+                                              float (&y)[8 / TB][8][TB], const float*& ysrc) {
+    ysrc = nullptr;
     if (moe) {
       expert_rows(b0, nt, rb, rj);
     } else {
@@ -1431,6 +1449,7 @@ struct Consumer {
       const bool ok = stage_input(kind, l, sg.K, rb, nt, tag, dst);
       if (cache && threadIdx.x == 0) S.ykey = l;
       load_y_staged(dst, sg, sg.K, nt, y);
+      ysrc = dst;
       return ok;
     }
     if constexpr (TB * kMaxK > kMoeScratch) {
@@ -1475,14 +1494,16 @@ struct Consumer {
     float my_ss = 0.f;    // O-proj: sum of squares of the residual values this lane wrote
     int rb[TB], rj[TB];
     float y[8 / TB][8][TB];
+    const float* ysrc = nullptr;   // the staged input rows of the current group, when staged
     bool ok = true;
     if (gu_fused) {
 #pragma unroll
       for (int tb = 0; tb < TB; ++tb) { rb[tb] = tb; rj[tb] = tb < B ? slot_of(tb, e) : -1; }
       load_y_smem(sg, rb, B, y);
     } else {
-      ok = stream_load(sg, moe, kind, l, 0, min(cnt, TB), tag, eop, rb, rj, y);
+      ok = stream_load(sg, moe, kind, l, 0, min(cnt, TB), tag, eop, rb, rj, y, ysrc);
     }
+    int cur_g = 0;   // register group whose input is staged
     // segment sums share storage with the MoE input cache: every warp has its input first
     if (sg.S > 1) cbar();
     trace_mark(11 + (op == MK_OP_ROUTER ? 0 : moe ? 20 : 40), l);
@@ -1493,10 +1514,50 @@ struct Consumer {
       const uint8_t* wsm = slot();
       const int par = c & 1;
       ok = true;
-      for (int g = 0; g < ngroups && ok; ++g) {
+      // dense tiles of wide batches arrive group-major (the record's aux is its register group):
+      // a group's input is staged when its first chunk arrives; MoE runs hold every group's
+      // rows in each chunk
+      const bool gmajor = kGroups && !moe && ngroups > 1;
+      const int g_lo = gmajor ? static_cast<int>(meta().aux) : 0;
+      const int g_hi = gmajor ? g_lo + 1 : ngroups;
+      for (int g = g_lo; g < g_hi && ok; ++g) {
         const int b0 = g * TB;
         const int nt = min(TB, cnt - b0);
-        if (kGroups && ngroups > 1) ok = stream_load(sg, moe, kind, l, b0, nt, tag, eop, rb, rj, y) && ok;
+        if (kGroups && ngroups > 1 && (!gmajor || g != cur_g)) {
+          ok = stream_load(sg, moe, kind, l, b0, nt, tag, eop, rb, rj, y, ysrc) && ok;
+          cur_g = g;
+        }
+        if constexpr (TB == 4) {
+          if (!moe && sg.S > 1 && om.resid == nullptr && ysrc != nullptr) {
+            // wide batch, staged input: a warp keeps whole rows (rows warp + 8i) and sweeps K in
+            // sg.S passes, reloading its register slice of the staged rows per pass; one paired
+            // reduction per two rows at the end, instead of per-segment sums across warps
+            float acc[4][TB];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+              for (int tb = 0; tb < TB; ++tb) acc[i][tb] = 0.f;
+            Seg<TB> sp = sg;
+            for (int pass = 0; pass < sg.S; ++pass) {
+              sp.s = pass;
+              load_y_staged(ysrc, sp, K, nt, y);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int r = (threadIdx.x >> 5) + kConsumerWarps * i;
+                if (r < n) row_dot<TB>(wsm + static_cast<size_t>(r) * K * 2, sp, y, acc[i]);
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; i += 2) {
+              warp_sum2<TB>(acc[i], acc[i + 1]);
+              const int tb = lane & 15;
+              const int rr = (threadIdx.x >> 5) + kConsumerWarps * (lane < 16 ? i : i + 1);
+              if (tb < nt && rr < n)
+                put(om, false, row0 + rr, pick_i<TB>(rb, tb), pick_i<TB>(rj, tb), pick<TB>(acc[i], tb), 0.f, my_ss);
+            }
+            continue;
+          }
+        }
         if (sg.S == 1 && om.resid == nullptr) {
           // whole rows per warp, two dot products in flight and one paired reduction:
           // gate/up: the row's gate and up; otherwise rows r and r + RPG
