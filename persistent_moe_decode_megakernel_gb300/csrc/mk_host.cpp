@@ -819,10 +819,11 @@ int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t B, const int32_t* 
   const int F = cfg->expert_ffn, H = cfg->hidden;
   std::vector<uint32_t> ctr(cm.total, 0);
   // per layer: active experts (ascending) and the gate/up unit range of every block
-  std::vector<std::vector<int>> act(L);
+  std::vector<std::vector<int>> act(L), rows_of(L);   // active experts; rows routed to each expert
   std::vector<std::vector<int32_t>> gu_start(L);
   for (int l = 0; l < L; ++l) {
-    std::vector<int> cnt(E, 0);
+    std::vector<int>& cnt = rows_of[l];
+    cnt.assign(E, 0);
     for (int b = 0; b < B; ++b)
       for (int j = 0; j < K; ++j) {
         const int e = routing_ids[((size_t)l * B + b) * K + j];
@@ -892,11 +893,17 @@ int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t B, const int32_t* 
     if (u0 >= u1) r.push_back({100, task, l, 0, 0, F_FIRST | F_LAST | F_LAST_GU});
     for (int u = u0; u < u1;) {
       const int a = u / F, f0 = u % F, fend = std::min(F, u1 - a * F);
-      for (int f = f0; f < fend; f += fpc) {
-        const int n = std::min(fpc, fend - f);
-        for (int k = 0; k < n; ++k) gu_seen[l][(size_t)a * F + f + k]++;
-        r.push_back({100, task, l, (uint32_t)a, (uint32_t)f,
-                     (f == f0 ? F_FIRST : 0) | (f + n >= fend ? F_LAST : 0) | (a * F + fend >= u1 ? F_LAST_GU : 0)});
+      // batches of 3 or more: the run is streamed once per register group of its routed rows
+      const int ng = B > 2 ? (rows_of[l][act[l][a]] + 3) / 4 : 1;
+      for (int g = 0; g < ng; ++g) {
+        for (int f = f0; f < fend; f += fpc) {
+          const int n = std::min(fpc, fend - f);
+          if (g == 0)
+            for (int k = 0; k < n; ++k) gu_seen[l][(size_t)a * F + f + k]++;
+          r.push_back({100, task, l, (uint32_t)a, (uint32_t)f,
+                       (g == 0 && f == f0 ? F_FIRST : 0) | (g == ng - 1 && f + n >= fend ? F_LAST : 0) |
+                           (a * F + fend >= u1 ? F_LAST_GU : 0)});
+        }
       }
       u = a * F + fend;
     }

@@ -737,20 +737,28 @@ struct Producer {
       const uint32_t lastgu = (a * F + fend >= u1) ? 1u : 0u;
       const int e = S.eact[a];
       const uint16_t* gate = lw.w_gate_up + static_cast<size_t>(e) * 2 * F * H;
-      for (int f = f0; f < fend; f += fpc) {
-        const int n = min(fpc, fend - f);
-        if (!acquire()) return false;
-        Meta& m = meta();
-        m.kind = R_GU; m.op = MK_OP_MOE; m.first = (f == f0); m.last = (f + n >= fend);
-        m.layer = static_cast<uint16_t>(l); m.n = static_cast<uint16_t>(n); m.row0 = f;
-        m.idx = static_cast<uint32_t>(a); m.e = static_cast<uint32_t>(e); m.aux = lastgu;
-        m.wait_ctr = MK_NO_COUNTER; m.wait_target = 0; m.signal_ctr = MK_NO_COUNTER;
-        m.lo = f0; m.hi = fend;
-        const uint32_t bytes = static_cast<uint32_t>(n) * H * 2u;
-        mbar_arrive_expect_tx(full(), 2u * bytes);
-        bulk_g2s(slot(), gate + static_cast<size_t>(f) * H, bytes, full(), pol);
-        bulk_g2s(slot() + bytes, gate + static_cast<size_t>(F + f) * H, bytes, full(), pol);
-        ++c;
+      // an expert whose routed rows exceed one register group (groups of 4 rows, batches of 3
+      // or more) is streamed once per group (group in aux >> 1), so each group's input is
+      // staged once per run; the repeated reads come from L2
+      const int ng = p.B > 2 ? (S.ecnt[e] + 3) / 4 : 1;
+      for (int g = 0; g < ng; ++g) {
+        for (int f = f0; f < fend; f += fpc) {
+          const int n = min(fpc, fend - f);
+          if (!acquire()) return false;
+          Meta& m = meta();
+          m.kind = R_GU; m.op = MK_OP_MOE; m.first = (g == 0 && f == f0); m.last = (g == ng - 1 && f + n >= fend);
+          m.layer = static_cast<uint16_t>(l); m.n = static_cast<uint16_t>(n); m.row0 = f;
+          m.idx = static_cast<uint32_t>(a); m.e = static_cast<uint32_t>(e);
+          m.aux = lastgu | (static_cast<uint32_t>(g) << 1);
+          m.wait_ctr = MK_NO_COUNTER; m.wait_target = 0; m.signal_ctr = MK_NO_COUNTER;
+          m.lo = f0; m.hi = fend;
+          const uint32_t bytes = static_cast<uint32_t>(n) * H * 2u;
+          const uint64_t pl = g == ng - 1 ? pol : pol_reuse;
+          mbar_arrive_expect_tx(full(), 2u * bytes);
+          bulk_g2s(slot(), gate + static_cast<size_t>(f) * H, bytes, full(), pl);
+          bulk_g2s(slot() + bytes, gate + static_cast<size_t>(F + f) * H, bytes, full(), pl);
+          ++c;
+        }
       }
       u = a * F + fend;
     }
@@ -1514,11 +1522,10 @@ struct Consumer {
       const uint8_t* wsm = slot();
       const int par = c & 1;
       ok = true;
-      // dense tiles of wide batches arrive group-major (the record's aux is its register group):
-      // a group's input is staged when its first chunk arrives; MoE runs hold every group's
-      // rows in each chunk
-      const bool gmajor = kGroups && !moe && ngroups > 1;
-      const int g_lo = gmajor ? static_cast<int>(meta().aux) : 0;
+      // tiles and expert runs of wide batches arrive group-major (the record's register group is
+      // its aux, or aux >> 1 for gate/up): a group's input is staged when its first chunk arrives
+      const bool gmajor = kGroups && !gu_fused && ngroups > 1;
+      const int g_lo = gmajor ? static_cast<int>(moe ? meta().aux >> 1 : meta().aux) : 0;
       const int g_hi = gmajor ? g_lo + 1 : ngroups;
       for (int g = g_lo; g < g_hi && ok; ++g) {
         const int b0 = g * TB;
@@ -1528,6 +1535,40 @@ struct Consumer {
           cur_g = g;
         }
         if constexpr (TB == 4) {
+          if (gu && sg.S > 1 && ysrc != nullptr) {
+            // the same for an expert run: a warp keeps FFN rows f = warp + 8i whole (gate row f and
+            // up row n + f), K in passes, one paired reduction per row
+            float ag[2][TB], au[2][TB];
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+              for (int tb = 0; tb < TB; ++tb) { ag[i][tb] = 0.f; au[i][tb] = 0.f; }
+            Seg<TB> sp = sg;
+            for (int pass = 0; pass < sg.S; ++pass) {
+              sp.s = pass;
+              load_y_staged(ysrc, sp, K, nt, y);
+#pragma unroll
+              for (int i = 0; i < 2; ++i) {
+                const int f = (threadIdx.x >> 5) + kConsumerWarps * i;
+                if (f < n) {
+                  row_dot<TB>(wsm + static_cast<size_t>(f) * K * 2, sp, y, ag[i]);
+                  row_dot<TB>(wsm + static_cast<size_t>(n + f) * K * 2, sp, y, au[i]);
+                }
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const int f = (threadIdx.x >> 5) + kConsumerWarps * i;
+              warp_sum2<TB>(ag[i], au[i]);
+              float up[TB];
+#pragma unroll
+              for (int tb = 0; tb < TB; ++tb) up[tb] = __shfl_xor_sync(0xffffffffu, ag[i][tb], 16);
+              if (f < n && lane < nt)
+                put(om, true, row0 + f, pick_i<TB>(rb, lane), pick_i<TB>(rj, lane), pick<TB>(ag[i], lane),
+                    pick<TB>(up, lane), my_ss);
+            }
+            continue;
+          }
           if (!moe && sg.S > 1 && om.resid == nullptr && ysrc != nullptr) {
             // wide batch, staged input: a warp keeps whole rows (rows warp + 8i) and sweeps K in
             // sg.S passes, reloading its register slice of the staged rows per pass; one paired
