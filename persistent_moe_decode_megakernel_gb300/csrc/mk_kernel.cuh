@@ -410,57 +410,45 @@ __device__ __noinline__ void ll_timeout(const Params& p, int op, int layer) {
       }                                                                                   \
     }                                                                                     \
   }
-// Re-poll the words of one gather batch whose tags were stale (bit k: the word of index
-// base + k * kConsumerThreads) until each is current; a compact loop, since it is the
-// uncommon path.  False if the watchdog or an abort ended the wait.
-template <class Addr>
-__device__ __noinline__ bool ll_gather_fix(const Params& p, Addr addr, int base, uint32_t stale, float* dst,
-                                           uint32_t tag) {
-  const uint64_t t0 = globaltimer();
-  for (uint32_t it = 1; stale != 0u; ++it) {
-#pragma unroll 1
-    for (int k = 0; k < 32; ++k) {
-      if ((stale >> k) & 1u) {
-        const int i = base + k * kConsumerThreads;
-        const uint64_t x = ll_ld(addr(i));
-        if (ll_ok(x, tag)) {
-          dst[i] = ll_f(x);
-          stale &= ~(1u << k);
-        }
-      }
-    }
-    if (stale != 0u && (it & 15u) == 0u && (aborted(p) || globaltimer() - t0 > p.watchdog_ns)) return false;
-  }
-  return true;
+// True once the watchdog has run out for a wait that started at t0, or the step was aborted.
+__device__ __noinline__ bool ll_expired(const Params& p, uint64_t t0) {
+  return aborted(p) || globaltimer() - t0 > p.watchdog_ns;
 }
 
 // Gather n tagged words into shared-memory floats: dst[i] = value of word addr(i), i over
-// this thread's indices threadIdx.x + k * kConsumerThreads.  Loads go out 16 at a time;
-// words that carried a stale tag are re-polled by ll_gather_fix.
+// this thread's indices threadIdx.x + k * kConsumerThreads.  Loads go out 16 at a time; a
+// batch is issued again for the words whose tags were stale, all of them at once, until
+// every word is current (one loaded L2 round trip per pass, the same code for the first and
+// the later passes).  False if the watchdog or an abort ended the wait.
 template <class Addr>
 __device__ __forceinline__ bool ll_gather(const Params& p, int n, Addr addr, float* dst, uint32_t tag) {
   constexpr int kB = 16;
-  bool ok = true;
   for (int base = threadIdx.x; base < n; base += kB * kConsumerThreads) {
-    uint64_t x[kB];
+    uint32_t want = (1u << kB) - 1u;   // words of this batch not yet seen with the step's tag
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+      uint64_t x[kB];
 #pragma unroll
-    for (int k = 0; k < kB; ++k) {
-      const int i = base + k * kConsumerThreads;
-      x[k] = i < n ? ll_ld(addr(i)) : 0ull;
-    }
-    uint32_t stale = 0;
-#pragma unroll
-    for (int k = 0; k < kB; ++k) {
-      const int i = base + k * kConsumerThreads;
-      if (i < n) {
-        if (ll_ok(x[k], tag)) dst[i] = ll_f(x[k]);
-        else stale |= 1u << k;
+      for (int k = 0; k < kB; ++k) {
+        const int i = base + k * kConsumerThreads;
+        x[k] = (i < n && ((want >> k) & 1u)) ? ll_ld(addr(i)) : 0ull;
       }
+      uint32_t stale = 0;
+#pragma unroll
+      for (int k = 0; k < kB; ++k) {
+        const int i = base + k * kConsumerThreads;
+        if (i < n && ((want >> k) & 1u)) {
+          if (ll_ok(x[k], tag)) dst[i] = ll_f(x[k]);
+          else stale |= 1u << k;
+        }
+      }
+      want = stale;
+      if (want == 0u) break;
+      if (it == 0u) t0 = globaltimer();
+      else if ((it & 15u) == 0u && ll_expired(p, t0)) return false;
     }
-    if (stale != 0u) ok = ll_gather_fix(p, addr, base, stale, dst, tag) && ok;
-    if (!ok) break;
   }
-  return ok;
+  return true;
 }
 
 // stale-tag bits of a word (0 when current)
@@ -1806,6 +1794,45 @@ struct Consumer {
     }
   }
 
+  // Top-k of every row for wider batches: a warp per row holds the row's logits in registers
+  // (up to 8 per lane) and runs k rounds of a warp argmax over (value, lower index); each
+  // round's winner is recorded in rank order and taken out of the row.  Exact, with the same
+  // tie rule as rank_rows.
+  __device__ __forceinline__ void topk_rows_warp(const float* lg) {
+    const int B = p.B, E = p.E, K = p.K;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int b = warp; b < B; b += kConsumerWarps) {
+      float v[kMaxExperts / 32];
+#pragma unroll
+      for (int k = 0; k < kMaxExperts / 32; ++k) {
+        const int e = lane + 32 * k;
+        v[k] = e < E ? lg[b * E + e] : -INFINITY;
+      }
+      uint32_t taken = 0;   // this lane's values already chosen (bit k)
+      for (int j = 0; j < K; ++j) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int k = 0; k < kMaxExperts / 32; ++k) {
+          const int e = lane + 32 * k;
+          if (e < E && !((taken >> k) & 1u) && (v[k] > bv || (v[k] == bv && e < bi))) { bv = v[k]; bi = e; }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+          if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+        }
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        if (lane == 0) {
+          S.rids[b * K + j] = bi;
+          S.rval[b * K + j] = bv;
+          atomicAdd(&S.ecnt[bi], 1);
+        }
+      }
+    }
+  }
+
   // ------------------------------------------------------------------ routing (every block)
   // Every block routes the whole batch itself from the router logits (tagged words the
   // router tiles wrote), so the MoE of a layer needs nothing else from another block.
@@ -1854,7 +1881,9 @@ struct Consumer {
         if (lane == 0) { S.rmax[b] = mx; S.rz[b] = z; }
       }
     }
-    if (E <= 128) rank_rows<16>(lg); else rank_rows<32>(lg);
+    if (TB == 4 && B >= 8) topk_rows_warp(lg);   // (only the widest instantiation sees such batches)
+    else if (E <= 128) rank_rows<16>(lg);
+    else rank_rows<32>(lg);
     cbar();
     trace_mark(18, l);
     // small-batch MoE: the logits are consumed; the scratch becomes the [B][H] partial output
@@ -2008,9 +2037,51 @@ struct Consumer {
 
   // SwiGLU activations of up to TD (row, slot) pairs into registers, from the shared-memory
   // copy (hc) or from the tagged global buffer
+  // The same from the tagged global buffer for pair groups of wide batches: the loads of half
+  // the units go out together (one L2 round trip per half; a stale word sends its half again)
+  template <int TD>
+  __device__ __forceinline__ bool load_h_pairs_ll(const Seg<TD>& sg, int l, const int* pr, int nt,
+                                                  float (&y)[8 / TD][8][TD]) {
+    constexpr int kU = Seg<TD>::kUnits;
+    const uint64_t* src[TD];
+#pragma unroll
+    for (int tb = 0; tb < TD; ++tb)
+      src[tb] = p.HB + (static_cast<size_t>(l) * p.max_batch * p.K + pr[tb < nt ? tb : 0]) * p.F;
+    bool ok = true;
+#pragma unroll
+    for (int h0 = 0; h0 < kU; h0 += kU / 2) {
+      LL_RETRY_BEGIN
+#pragma unroll
+      for (int j = h0; j < h0 + kU / 2; ++j) {
+        const int e = sg.unit(j);
+#pragma unroll
+        for (int tb = 0; tb < TD; ++tb) {
+          if (e >= 0 && tb < nt) {
+#pragma unroll
+            for (int q = 0; q < 8; q += 2) {
+              uint64_t a, b;
+              ll_ld2(src[tb] + e + q, a, b);
+              st_ |= ll_stale(a, p.tag) | ll_stale(b, p.tag);
+              y[j][q][tb] = ll_f(a);
+              y[j][q + 1][tb] = ll_f(b);
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) y[j][q][tb] = 0.f;
+          }
+        }
+      }
+      LL_RETRY_END(ok)
+    }
+    return ok;
+  }
+
   template <int TD>
   __device__ __forceinline__ bool load_h_pairs(const Seg<TD>& sg, int l, const float* hc, const int* pr, int nt,
                                                float (&y)[8 / TD][8][TD]) {
+    if constexpr (TD > 1 && TB == 4) {   // (batches of two take the small-batch path by default)
+      if (hc == nullptr) return load_h_pairs_ll<TD>(sg, l, pr, nt, y);
+    }
     bool ok = true;
 #pragma unroll
     for (int j = 0; j < Seg<TD>::kUnits; ++j) {
