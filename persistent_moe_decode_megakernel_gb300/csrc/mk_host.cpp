@@ -157,7 +157,8 @@ void build_static_plan(const mk_config& c, int n_ctas, Plan& plan) {
   in.n_embed_tiles = count((uint32_t)H);
   in.n_qkv_tiles = count((uint32_t)nqkv);
   in.n_o_tiles = count((uint32_t)H);
-  in.n_router_tiles = (E + mk::kRouterRows - 1) / mk::kRouterRows;
+  const int rr = mk::router_tile_rows(E, n_ctas, c.max_batch);
+  in.n_router_tiles = (E + rr - 1) / rr;
   in.n_head_tiles = count((uint32_t)V);
   in.n_down_ranges = count((uint32_t)H);
   const CounterMap& cm = plan.cm;
@@ -185,7 +186,7 @@ void build_static_plan(const mk_config& c, int n_ctas, Plan& plan) {
       split_range((uint32_t)H, n_ctas, i, &lo, &hi);
       if (hi > lo) push(MK_OP_OPROJ, l, lo, hi, base + mk::L_ATTN, 0, (uint32_t)c.num_kv_heads, base + mk::L_O);
       for (int t = i; t < in.n_router_tiles; t += n_ctas)
-        push(MK_OP_ROUTER, l, (uint32_t)(t * mk::kRouterRows), (uint32_t)std::min(E, (t + 1) * mk::kRouterRows),
+        push(MK_OP_ROUTER, l, (uint32_t)(t * rr), (uint32_t)std::min(E, (t + 1) * rr),
              base + mk::L_O, (uint32_t)in.n_o_tiles, 0, MK_NO_COUNTER);
       push(MK_OP_MOE, l, 0, 0, base + mk::L_RREADY, 1, 0, MK_NO_COUNTER);
     }
@@ -294,12 +295,11 @@ struct mk_ctx {
   uint8_t* ws = nullptr;
   // tagged 8-byte words (value | step tag << 32)
   uint64_t *X = nullptr, *QKV = nullptr, *ATT = nullptr, *PO = nullptr, *PML = nullptr, *RLOG = nullptr,
-           *HB = nullptr, *SS = nullptr, *PT = nullptr;
+           *HB = nullptr, *PT = nullptr;
   uint16_t* wdt = nullptr;   // transposed down projections [L][E][F][H] (small-batch MoE path), or null
   float* argp = nullptr;     // greedy selection: per-block (max, second, index) of its LM-head rows
   bool small_ok = false;
   float* RW = nullptr;
-  int n_ss_slots = 0;
   int32_t* RIDS = nullptr;
   uint32_t tag = 0;        // tag of the last step (0: none yet)
   size_t tagged_bytes = 0; // bytes of the tagged buffers (cleared when the tag wraps)
@@ -470,7 +470,6 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_ctx** out) {
       {(void**)&c->PML, (size_t)L * in.max_items * mk::kMaxG * 2 * w8},
       {(void**)&c->RLOG, (size_t)L * MB * E * w8},
       {(void**)&c->HB, (size_t)L * MB * K * F * w8},
-      {(void**)&c->SS, (size_t)(2 * L + 1) * c->n_ctas * MB * w8},
       {(void**)&c->PT, c->small_ok ? (size_t)L * c->n_ctas * mk::kSmallMaxB * H * w8 : 0},
       {(void**)&c->RIDS, (size_t)L * MB * K * i4},
       {(void**)&c->argp, (size_t)c->n_ctas * MB * 4 * f4},
@@ -617,9 +616,7 @@ static int decode_step(mk_ctx* c, int32_t batch, const int32_t* token_ids, const
   p.item_off = reinterpret_cast<const int32_t*>(d + c->off_item_off);
   p.pair_first = reinterpret_cast<const int32_t*>(d + c->off_pair);
   p.X = c->X; p.QKV = c->QKV; p.ATT = c->ATT; p.PO = c->PO; p.PML = c->PML; p.RLOG = c->RLOG; p.RIDS = c->RIDS;
-  p.RW = c->RW; p.HB = c->HB; p.SS = c->SS; p.n_ss_slots = c->n_ctas;
-  // inputs wider than the staging scratch are read per warp and normalised with the SS words
-  p.need_ss = (int64_t)mk::tb_for_batch(batch) * cf.hidden > mk::kMoeScratch ? 1 : 0;
+  p.RW = c->RW; p.HB = c->HB;
   p.small_moe = c->small_ok && mk::small_moe_batch(batch, cf.hidden) ? 1 : 0;
   p.PT = c->PT;
   p.next_token = next_token; p.margin = margin; p.argp = c->argp;
@@ -894,7 +891,7 @@ int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t B, const int32_t* 
     for (int u = u0; u < u1;) {
       const int a = u / F, f0 = u % F, fend = std::min(F, u1 - a * F);
       // batches of 3 or more: the run is streamed once per register group of its routed rows
-      const int ng = B > 2 ? (rows_of[l][act[l][a]] + 3) / 4 : 1;
+      const int ng = B > 2 ? (rows_of[l][act[l][a]] + mk::wide_group_rows(H) - 1) / mk::wide_group_rows(H) : 1;
       for (int g = 0; g < ng; ++g) {
         for (int f = f0; f < fend; f += fpc) {
           const int n = std::min(fpc, fend - f);

@@ -292,7 +292,7 @@ struct FastDiv {
 };
 
 // --------------------------------------------------------------------------- shared memory
-enum : uint8_t { R_EMBED = 1, R_GEMV = 2, R_ATTN = 3, R_GU = 4, R_DOWN = 5, R_END = 6, R_ROUTE = 7, R_COMBINE = 8,
+enum : uint8_t { R_EMBED = 1, R_GEMV = 2, R_ATTN = 3, R_GU = 4, R_DOWN = 5, R_END = 6, R_ROUTE = 7,
                  R_DT = 9, R_RED = 10 };   // small-batch MoE: transposed down rows; partial-sum reduction
 // GEMV stream kinds beyond the task ops (MK_OP_QKV / OPROJ / ROUTER / HEAD)
 enum : int { R_OP_GU = 100 };
@@ -608,7 +608,7 @@ struct Producer {
     // A batch wider than one register group (groups of 4 rows) is served group-major: the tile
     // is streamed once per group (aux = group), so the consumers stage each group's input once
     // per tile; the repeated reads of the tile come from L2 (evict-normal while it is reused).
-    const int ng = p.B > 2 ? (p.B + 3) / 4 : 1;
+    const int ng = p.B > 2 ? (p.B + wide_group_rows(K) - 1) / wide_group_rows(K) : 1;
     const uint64_t pl = ng > 1 ? pol_reuse : pol;
     for (int g = 0; g < ng; ++g) {
       for (uint32_t r0 = t.lo; r0 < t.hi; r0 += rpc) {
@@ -671,8 +671,8 @@ struct Producer {
         ++c;
       }
     }
-    // then this block merges its share of every pair it holds a split of
-    if (p.item_off[cta + 1] > p.item_off[cta]) return moe_control(R_COMBINE, t.layer, 0u, 0u, MK_OP_ATTN);
+    // the consumers then merge this block's share of every pair it holds a split of, with no
+    // record of their own: both slots are free meanwhile for the weights of the next tile
     return true;
   }
 
@@ -728,7 +728,7 @@ struct Producer {
       // an expert whose routed rows exceed one register group (groups of 4 rows, batches of 3
       // or more) is streamed once per group (group in aux >> 1), so each group's input is
       // staged once per run; the repeated reads come from L2
-      const int ng = p.B > 2 ? (S.ecnt[e] + 3) / 4 : 1;
+      const int ng = p.B > 2 ? (S.ecnt[e] + wide_group_rows(H) - 1) / wide_group_rows(H) : 1;
       for (int g = 0; g < ng; ++g) {
         for (int f = f0; f < fend; f += fpc) {
           const int n = min(fpc, fend - f);
@@ -949,97 +949,6 @@ __device__ __forceinline__ void row_dot(const uint8_t* row, const Seg<TB>& sg, c
   for (int tb = 0; tb < TB; ++tb) acc[tb] += part[tb][0] + part[tb][1];
 }
 
-// Sums of squares of residual-stream vector `xidx`, row b, as published per block by
-// its producers: issue every load at once (slots <= 256), re-poll stale ones, then
-// reduce in fixed order so every warp gets the same value.
-__device__ __forceinline__ bool ss_fetch(const Params& p, int xidx, int b, float (&v)[8]) {
-  const uint64_t* ss = p.SS + static_cast<size_t>(xidx) * p.n_ss_slots * p.max_batch + b;
-  const int lane = threadIdx.x & 31;
-  bool ok = true;
-  LL_RETRY_BEGIN
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const int i = lane + 32 * k;
-    v[k] = 0.f;
-    if (i < p.n_ss_slots) {
-      const uint64_t x = ll_ld(ss + static_cast<size_t>(i) * p.max_batch);
-      st_ |= ll_stale(x, p.tag);
-      v[k] = ll_f(x);
-    }
-  }
-  LL_RETRY_END(ok)
-  return ok;
-}
-__device__ __forceinline__ float ss_rstd(const Params& p, const float (&v)[8]) {
-  float t = 0.f;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) t += v[k];
-  t = warp_sum(t);
-  return 1.0f / sqrtf(t / static_cast<float>(p.H) + p.eps);
-}
-
-// Load this warp's segment of nt tagged input vectors into registers (raw values).
-// src[tb] points at vector tb; vectors tb >= nt read as zero.  Stale words are re-polled.
-template <int TB>
-__device__ __forceinline__ bool load_y(const Params& p, const Seg<TB>& sg, const uint64_t* const (&src)[TB], int nt,
-                                       uint32_t tag, float (&y)[8 / TB][8][TB], uint32_t& sweeps) {
-  // one pass of loads; words that carried a stale tag are marked and re-polled one by one
-  // (unrolled, so that y stays in registers)
-  uint64_t stale = 0;
-#pragma unroll
-  for (int j = 0; j < Seg<TB>::kUnits; ++j) {
-    const int e = sg.unit(j);
-#pragma unroll
-    for (int tb = 0; tb < TB; ++tb) {
-      if (e >= 0 && tb < nt) {
-#pragma unroll
-        for (int q = 0; q < 8; q += 2) {
-          uint64_t a, b;
-          ll_ld2(src[tb] + e + q, a, b);
-          const int bit = (j * TB + tb) * 8 + q;
-          stale |= static_cast<uint64_t>(ll_stale(a, tag) != 0u) << bit;
-          stale |= static_cast<uint64_t>(ll_stale(b, tag) != 0u) << (bit + 1);
-          y[j][q][tb] = ll_f(a);
-          y[j][q + 1][tb] = ll_f(b);
-        }
-      } else {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) y[j][q][tb] = 0.f;
-      }
-    }
-  }
-  bool ok = true;
-  if (stale != 0ull) {
-    // re-poll the stale words, all of them per sweep, until every one is current
-    const uint64_t t0 = globaltimer();
-    for (uint32_t it = 1; stale != 0ull; ++it) {
-      sweeps = it;
-      uint64_t still = 0;
-#pragma unroll
-      for (int j = 0; j < Seg<TB>::kUnits; ++j) {
-#pragma unroll
-        for (int tb = 0; tb < TB; ++tb) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const int bit = (j * TB + tb) * 8 + q;
-            if ((stale >> bit) & 1ull) {
-              const uint64_t x = ll_ld(src[tb] + sg.unit(j) + q);
-              still |= static_cast<uint64_t>(ll_stale(x, tag) != 0u) << bit;
-              y[j][q][tb] = ll_f(x);
-            }
-          }
-        }
-      }
-      stale = still;
-      if (stale != 0ull && (it & 15u) == 0u && (aborted(p) || globaltimer() - t0 > p.watchdog_ns)) {
-        ok = false;
-        break;
-      }
-    }
-  }
-  return ok;
-}
-
 template <int TB>
 __device__ __forceinline__ int pick_i(const int (&a)[TB], int i) {
   int v = a[0];
@@ -1056,26 +965,6 @@ __device__ __forceinline__ float pick(const float (&a)[TB], int i) {
   for (int k = 1; k < TB; ++k)
     if (i == k) v = a[k];
   return v;
-}
-
-// per-row-of-the-batch sums of one value per thread (thread's row tb, or tb < 0
-// for none) over all consumer threads, in fixed order -> out[0..nt)
-template <int TB>
-__device__ void block_token_sums(Smem& S, int my_tb, float v, int nt, uint64_t* out, size_t out_stride, uint32_t tag) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-#pragma unroll
-  for (int tb = 0; tb < TB; ++tb) {
-    const float w = warp_sum(my_tb == tb ? v : 0.f);
-    if (lane == 0) S.ssred[warp][tb] = w;
-  }
-  cbar();
-  if (threadIdx.x < nt) {
-    float tot = 0.f;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) tot += S.ssred[w][threadIdx.x];
-    ll_st(out + threadIdx.x * out_stride, tot, tag);
-  }
-  cbar();
 }
 
 // 8 consecutive tagged words, re-polling until every one carries the step's tag (the
@@ -1190,56 +1079,10 @@ struct Consumer {
     return p.X + (static_cast<size_t>(xidx) * p.max_batch + b) * p.H;
   }
 
-  // Load the GEMV input of `kind` for rows rb[0..nt) into y (this warp's segment).
-  // kinds: 0 attention input (x_in, attn_norm), 1 O-proj input (attention output),
-  //        2 MoE input (x_mid, ffn_norm), 3 head input (x_final, final_norm)
-  __device__ __forceinline__ bool load_input(const Seg<TB>& sg, int kind, int l, const int (&rb)[TB], int nt,
-                                             uint32_t tag, int op, float (&y)[8 / TB][8][TB]) {
-    const uint64_t* src[TB];
-    const uint16_t* g = nullptr;
-    int xidx = 0;
-    if (kind == 0) { g = p.layers[l].attn_norm; xidx = 2 * l; }
-    else if (kind == 2) { g = p.layers[l].ffn_norm; xidx = 2 * l + 1; }
-    else if (kind == 3) { g = p.final_norm; xidx = 2 * p.L; }
-#pragma unroll
-    for (int tb = 0; tb < TB; ++tb) {
-      const int b = tb < nt ? rb[tb] : rb[0];
-      src[tb] = kind == 1 ? p.ATT + (static_cast<size_t>(l) * p.max_batch + b) * (p.Hq * p.D) : xrow(xidx, b);
-    }
-    uint32_t sweeps = 0;
-    bool ok = load_y<TB>(p, sg, src, nt, tag, y, sweeps);   // raw values; the loads below overlap with these
-    trace_mark(52, l, sweeps);
-    if (g == nullptr) return ok;
-    uint4 gw[Seg<TB>::kUnits];
-#pragma unroll
-    for (int j = 0; j < Seg<TB>::kUnits; ++j) {
-      const int e = sg.unit(j);
-      gw[j] = e >= 0 ? __ldg(reinterpret_cast<const uint4*>(g + e)) : make_uint4(0, 0, 0, 0);
-    }
-    float ssv[TB][8];
-#pragma unroll
-    for (int tb = 0; tb < TB; ++tb) ok = ss_fetch(p, xidx, tb < nt ? rb[tb] : rb[0], ssv[tb]) && ok;
-    trace_mark(53, l);
-    float rs[TB];
-#pragma unroll
-    for (int tb = 0; tb < TB; ++tb) rs[tb] = ss_rstd(p, ssv[tb]);
-#pragma unroll
-    for (int j = 0; j < Seg<TB>::kUnits; ++j) {
-      float gv[8];
-      unpack8(gw[j], gv);
-#pragma unroll
-      for (int tb = 0; tb < TB; ++tb)
-#pragma unroll
-        for (int q = 0; q < 8; ++q) y[j][q][tb] = (y[j][q][tb] * rs[tb]) * gv[q];
-    }
-    return ok;
-  }
-
   // ------------------------------------------------------------------ EMBED
   __device__ __forceinline__ bool embed() {
     const Meta m = meta();
     const int H = p.H;
-    uint64_t* ssout = p.SS + static_cast<size_t>(blockIdx.x) * p.max_batch;   // vector 0, slot = this block
     for (int b = 0; b < p.B; ++b) {
       int tok = __ldg(p.tokens + b);
       if (tok < 0 || tok >= p.V) {
@@ -1250,22 +1093,7 @@ struct Consumer {
       }
       const uint16_t* row = p.embed + static_cast<size_t>(tok) * H;
       uint64_t* x = p.X + static_cast<size_t>(b) * H;
-      float ss = 0.f;
-      for (uint32_t col = m.lo + threadIdx.x; col < m.hi; col += kConsumerThreads) {
-        const float v = bf1(row[col]);
-        ll_st(x + col, v, p.tag);
-        ss += v * v;
-      }
-      if (!p.need_ss) continue;
-      ss = warp_sum(ss);
-      if ((threadIdx.x & 31) == 0) S.ssred[threadIdx.x >> 5][0] = ss;
-      cbar();
-      if (threadIdx.x == 0) {
-        float tot = 0.f;
-        for (int w = 0; w < kConsumerWarps; ++w) tot += S.ssred[w][0];
-        ll_st(ssout + b, tot, p.tag);
-      }
-      cbar();
+      for (uint32_t col = m.lo + threadIdx.x; col < m.hi; col += kConsumerThreads) ll_st(x + col, bf1(row[col]), p.tag);
     }
     return true;
   }
@@ -1297,7 +1125,7 @@ struct Consumer {
   // result v (v2: the matching up row for gate/up) of matrix row `row` for batch row b, slot j;
   // rv: the residual input of that element when the caller already loaded it (O-proj), else NAN
   __device__ __forceinline__ void put(const OutMap& o, bool gu, uint32_t row, int b, int j, float v, float v2,
-                                      float& my_ss, float rv = NAN) {
+                                      float rv = NAN) {
     if (j < 0) return;
     const size_t off = static_cast<size_t>(b) * o.sb + static_cast<size_t>(j) * o.sj + row;
     if (gu) {
@@ -1309,10 +1137,7 @@ struct Consumer {
         if (o.hs != nullptr && u >= 0 && u < kMaxUnits) o.hs[b * kMaxUnits + u] = v * S.rwcache[b * p.K + j];
       }
     }
-    if (o.resid != nullptr) {
-      v += isnan(rv) ? ll_f(ll_ld(o.resid + off)) : rv;
-      my_ss += v * v;
-    }
+    if (o.resid != nullptr) v += isnan(rv) ? ll_f(ll_ld(o.resid + off)) : rv;
     if (o.bias != nullptr) v += __ldg(o.bias + row);
     if (o.base != nullptr) ll_st(o.base + off, v, p.tag);
     else o.plain[off] = v;
@@ -1448,11 +1273,7 @@ struct Consumer {
       ysrc = dst;
       return ok;
     }
-    if constexpr (TB * kMaxK > kMoeScratch) {
-      return load_input(sg, kind, l, rb, nt, tag, op, y);
-    } else {
-      return false;   // unreachable: every input of this batch width fits the scratch
-    }
+    return false;   // unreachable: register groups are sized so that their input fits the scratch
   }
 
   __device__ __forceinline__ bool stream_gemv(int op) {
@@ -1481,13 +1302,13 @@ struct Consumer {
     // only the routing slots change between runs.
     const bool gu_fused = gu && B <= TB && S.ykey == l;
     const int cnt = gu_fused ? B : moe ? expert_pairs(e) : B;
-    const int ngroups = kGroups ? (cnt + TB - 1) / TB : 1;
+    const int GR = kGroups ? wide_group_rows(K) : TB;   // rows per register group (at most TB)
+    const int ngroups = kGroups ? (cnt + GR - 1) / GR : 1;
     OutMap om = out_map(op, l);
     if (TB <= kSmallMaxB && gu && p.small_moe) {
       om.hs = S.hsm;
       om.hoff = static_cast<int>(meta().idx) * p.F - S.gu_lo;
     }
-    float my_ss = 0.f;    // O-proj: sum of squares of the residual values this lane wrote
     int rb[TB], rj[TB];
     float y[8 / TB][8][TB];
     const float* ysrc = nullptr;   // the staged input rows of the current group, when staged
@@ -1497,7 +1318,7 @@ struct Consumer {
       for (int tb = 0; tb < TB; ++tb) { rb[tb] = tb; rj[tb] = tb < B ? slot_of(tb, e) : -1; }
       load_y_smem(sg, rb, B, y);
     } else {
-      ok = stream_load(sg, moe, kind, l, 0, min(cnt, TB), tag, eop, rb, rj, y, ysrc);
+      ok = stream_load(sg, moe, kind, l, 0, min(cnt, GR), tag, eop, rb, rj, y, ysrc);
     }
     int cur_g = 0;   // register group whose input is staged
     // segment sums share storage with the MoE input cache: every warp has its input first
@@ -1516,8 +1337,8 @@ struct Consumer {
       const int g_lo = gmajor ? static_cast<int>(moe ? meta().aux >> 1 : meta().aux) : 0;
       const int g_hi = gmajor ? g_lo + 1 : ngroups;
       for (int g = g_lo; g < g_hi && ok; ++g) {
-        const int b0 = g * TB;
-        const int nt = min(TB, cnt - b0);
+        const int b0 = g * GR;
+        const int nt = min(GR, cnt - b0);
         if (kGroups && ngroups > 1 && (!gmajor || g != cur_g)) {
           ok = stream_load(sg, moe, kind, l, b0, nt, tag, eop, rb, rj, y, ysrc) && ok;
           cur_g = g;
@@ -1553,7 +1374,7 @@ struct Consumer {
               for (int tb = 0; tb < TB; ++tb) up[tb] = __shfl_xor_sync(0xffffffffu, ag[i][tb], 16);
               if (f < n && lane < nt)
                 put(om, true, row0 + f, pick_i<TB>(rb, lane), pick_i<TB>(rj, lane), pick<TB>(ag[i], lane),
-                    pick<TB>(up, lane), my_ss);
+                    pick<TB>(up, lane));
             }
             continue;
           }
@@ -1582,7 +1403,7 @@ struct Consumer {
               const int tb = lane & 15;
               const int rr = (threadIdx.x >> 5) + kConsumerWarps * (lane < 16 ? i : i + 1);
               if (tb < nt && rr < n)
-                put(om, false, row0 + rr, pick_i<TB>(rb, tb), pick_i<TB>(rj, tb), pick<TB>(acc[i], tb), 0.f, my_ss);
+                put(om, false, row0 + rr, pick_i<TB>(rb, tb), pick_i<TB>(rj, tb), pick<TB>(acc[i], tb), 0.f);
             }
             continue;
           }
@@ -1605,12 +1426,12 @@ struct Consumer {
               for (int tb = 0; tb < TB; ++tb) up[tb] = __shfl_xor_sync(0xffffffffu, a[tb], 16);
               if (lane < nt)
                 put(om, true, row0 + r, pick_i<TB>(rb, lane), pick_i<TB>(rj, lane), pick<TB>(a, lane),
-                    pick<TB>(up, lane), my_ss);
+                    pick<TB>(up, lane));
             } else {
               const int tb = lane & 15;
               const int rr = lane < 16 ? r : r2;
               if (tb < nt && rr < n)
-                put(om, false, row0 + rr, pick_i<TB>(rb, tb), pick_i<TB>(rj, tb), pick<TB>(a, tb), 0.f, my_ss);
+                put(om, false, row0 + rr, pick_i<TB>(rb, tb), pick_i<TB>(rj, tb), pick<TB>(a, tb), 0.f);
             }
           }
           continue;
@@ -1629,7 +1450,7 @@ struct Consumer {
           if (sg.S == 1) {
             if (lane < nt)
               put(om, gu, row0 + r, pick_i<TB>(rb, lane), pick_i<TB>(rj, lane), pick<TB>(acc, lane),
-                  pick<TB>(acc2, lane), my_ss);
+                  pick<TB>(acc2, lane));
           } else if (lane < nt) {
             S.scr.seg[par][r][sg.s][lane] = pick<TB>(acc, lane);
             if (gu) S.scr.seg[par][kMaxRowsPerChunk / 2 + r][sg.s][lane] = pick<TB>(acc2, lane);
@@ -1656,7 +1477,7 @@ struct Consumer {
                 v += S.scr.seg[par][r][q][lane];
                 if (gu) v2 += S.scr.seg[par][kMaxRowsPerChunk / 2 + r][q][lane];
               }
-              put(om, gu, row0 + r, pick_i<TB>(rb, lane), pick_i<TB>(rj, lane), v, v2, my_ss,
+              put(om, gu, row0 + r, pick_i<TB>(rb, lane), pick_i<TB>(rj, lane), v, v2,
                   i == 0 ? rv[0] : i == 1 ? rv[1] : i == 2 ? rv[2] : i == 3 ? rv[3] : NAN);
             }
           }
@@ -1690,12 +1511,6 @@ struct Consumer {
     if (!ok) ll_timeout(p, eop, l);
     if (!cbar_and(wok && ok)) return false;
     if (op == MK_OP_HEAD && p.next_token != nullptr) head_top2(lo, hi);
-    if (op == MK_OP_OPROJ && p.need_ss) {
-      // publish this tile's share of sum(x_mid^2) for the RMSNorm of the MoE input
-      uint64_t* out = p.SS + (static_cast<size_t>(2 * l + 1) * p.n_ss_slots + blockIdx.x) * p.max_batch;
-      if (B <= TB) block_token_sums<TB>(S, lane < B ? lane : -1, my_ss, B, out, 1, p.tag);
-      else oproj_ss_wide(l, lo, hi, out);
-    }
     return true;
   }
 
@@ -1728,23 +1543,6 @@ struct Consumer {
       }
       cbar();
     }
-  }
-
-  // sums of squares of this O-proj tile's rows for every batch row (batches wider than TB)
-  __device__ void oproj_ss_wide(int l, uint32_t lo, uint32_t hi, uint64_t* out) {
-    const size_t xs = static_cast<size_t>(p.max_batch) * p.H;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    cbar();   // every row of the tile is written (by this block)
-    for (int b = warp; b < p.B; b += kConsumerWarps) {
-      float ss = 0.f;
-      for (uint32_t r = lo + lane; r < hi; r += 32) {
-        const float v = ll_f(ll_ld(p.X + (2 * static_cast<size_t>(l) + 1) * xs + static_cast<size_t>(b) * p.H + r));
-        ss += v * v;
-      }
-      ss = warp_sum(ss);
-      if (lane == 0) ll_st(out + b, ss, p.tag);
-    }
-    cbar();
   }
 
   // Ranks of every (row, expert) pair of the batch (see route_local): the consumer threads
@@ -2115,7 +1913,7 @@ struct Consumer {
   // the chunk's rows; for each expert in its share it lists the (row, slot) pairs routed there
   // and dots their SwiGLU activations with the rows.  Every product w_j * (Wd_j . h_j) lands once
   // in shared memory; after the last chunk the slots are summed in slot order and added to
-  // x_mid, and the block publishes its share of sum(x_out^2) for the next RMSNorm.
+  // x_mid.
   template <int TD>
   __device__ __forceinline__ bool moe_down_t() {
     const Meta m0 = meta();
@@ -2124,13 +1922,8 @@ struct Consumer {
     const int r0 = static_cast<int>(m0.lo), nrow = static_cast<int>(m0.hi) - r0;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const size_t xs = static_cast<size_t>(p.max_batch) * p.H;
-    uint64_t* ssout = p.SS + (static_cast<size_t>(2 * l + 2) * p.n_ss_slots + blockIdx.x) * p.max_batch;
     twait = globaltimer();
-    if (m0.n == 0) {   // no hidden rows here (or nothing routed): the block's share of sum(x^2) is 0
-      if (p.need_ss)
-        for (int t = threadIdx.x; t < B; t += kConsumerThreads) ll_st(ssout + t, 0.f, p.tag);
-      return true;
-    }
+    if (m0.n == 0) return true;   // no hidden rows here, or nothing routed
     float* P = S.moe;                                  // [B][K][nrow] products
     float* XM = P + B * K * nrow;                      // [B][nrow] x_mid of the block's rows
     const int hoff = (B * K * nrow + B * nrow + 3) & ~3;
@@ -2193,19 +1986,13 @@ struct Consumer {
     if (!ok) ll_timeout(p, MK_OP_MOE, l);
     if (!cbar_and(wok && ok)) return false;
     trace_mark(42, l);
-    // combine in slot order, residual, sums of squares
+    // combine in slot order, residual
     for (int t = warp; t < B; t += kConsumerWarps) {
-      float ss = 0.f;
       for (int r = lane; r < nrow; r += 32) {
         float acc = 0.f;
         for (int j = 0; j < K; ++j) acc += P[(t * K + j) * nrow + r];
-        const float v = XM[t * nrow + r] + acc;
-        ll_st(p.X + (2 * static_cast<size_t>(l) + 2) * xs + static_cast<size_t>(t) * p.H + r0 + r, v, p.tag);
-        ss += v * v;
-      }
-      if (p.need_ss) {
-        ss = warp_sum(ss);
-        if (lane == 0) ll_st(ssout + t, ss, p.tag);
+        ll_st(p.X + (2 * static_cast<size_t>(l) + 2) * xs + static_cast<size_t>(t) * p.H + r0 + r,
+              XM[t * nrow + r] + acc, p.tag);
       }
     }
     return true;
@@ -2265,7 +2052,7 @@ struct Consumer {
   // Reduction record of the small-batch MoE: publish this block's [B][H] partial output, then
   // for the block's hidden rows [lo, hi): gather every block's partial (one batch of loads),
   // sum them in block order per lane group and by a warp reduction, add x_mid, and write the
-  // layer output (and its sums of squares where a later input is too wide to stage).
+  // layer output.
   __device__ __forceinline__ bool moe_reduce() {
     const Meta m0 = meta();
     const int l = m0.layer, B = p.B, H = p.H, N = p.n_ctas;
@@ -2299,10 +2086,6 @@ struct Consumer {
     if (!cbar_and(ok)) return false;
     trace_mark(42, l);
     const float* part = S.moe + ni;
-    uint64_t* ssout = p.SS + (static_cast<size_t>(2 * l + 2) * p.n_ss_slots + blockIdx.x) * p.max_batch;
-    float ssb[kSmallMaxB];
-#pragma unroll
-    for (int tb = 0; tb < kSmallMaxB; ++tb) ssb[tb] = 0.f;
     for (int k = 0; k * kConsumerWarps < ni; ++k) {   // warp-uniform trip count
       const int it = warp + k * kConsumerWarps;
       const int b = it < ni ? it / nrow : 0, rr = it - b * nrow;
@@ -2310,24 +2093,8 @@ struct Consumer {
       if (it < ni)
         for (int j = lane; j < N; j += 32) v += part[(b * N + j) * nrow + rr];
       v = warp_sum(v);
-      if (it < ni) {
-        const float xv = S.moe[it] + v;
-        if (lane == 0) ll_st(p.X + (2 * static_cast<size_t>(l) + 2) * xs + static_cast<size_t>(b) * H + r0 + rr, xv, p.tag);
-#pragma unroll
-        for (int tb = 0; tb < kSmallMaxB; ++tb)
-          if (b == tb) ssb[tb] += xv * xv;
-      }
-    }
-    if (p.need_ss) {   // per row of the batch: this warp's share, then the block's sum
-#pragma unroll
-      for (int tb = 0; tb < kSmallMaxB; ++tb)
-        if (lane == 0) S.ssred[warp][tb] = ssb[tb];
-      cbar();
-      if (threadIdx.x < B) {
-        float t = 0.f;
-        for (int w = 0; w < kConsumerWarps; ++w) t += S.ssred[w][threadIdx.x];
-        ll_st(ssout + threadIdx.x, t, p.tag);
-      }
+      if (it < ni && lane == 0)
+        ll_st(p.X + (2 * static_cast<size_t>(l) + 2) * xs + static_cast<size_t>(b) * H + r0 + rr, S.moe[it] + v, p.tag);
     }
     return true;
   }
@@ -2613,8 +2380,7 @@ struct Consumer {
   // split order, from their tagged partials, and writes them as the attention output.
   // A warp per head finds the head's max and normaliser over the splits (a lane per split)
   // and leaves each split's scale exp(m_s - M) / L; then 8 lanes per output sum the splits.
-  __device__ __forceinline__ bool attn_combine() {
-    const int l = meta().layer;
+  __device__ __forceinline__ bool attn_combine(int l) {
     const int Gq = p.G;
     const int GD = Gq * D;
     const int cta = blockIdx.x;
@@ -2701,7 +2467,6 @@ struct Consumer {
         case R_ATTN: ok = attn_item(); break;
         case R_DOWN: ok = moe_down(); break;
         case R_ROUTE: ok = route_local(); break;
-        case R_COMBINE: ok = attn_combine(); break;
         case R_DT:   // small-batch MoE records exist only for batches of at most kSmallMaxB rows
           if constexpr (TB <= kSmallMaxB) ok = moe_dt();
           break;
@@ -2715,8 +2480,12 @@ struct Consumer {
                                                 m0.kind == R_RED ? TR_ITEM : TR_TILE,
                                         m0, t0);
       trace_chunk_done();
+      // after its last attention item the block merges its splits' partials; that needs no ring
+      // slot, so the record is released first and the producer streams on meanwhile
+      const bool merge = m0.kind == R_ATTN && static_cast<int>(m0.idx) == p.item_off[blockIdx.x + 1] - 1;
       warp_release_record(S, c);
       ++c;
+      if (merge && !attn_combine(m0.layer)) break;
       if (m0.kind == R_END) break;
     }
     if ((threadIdx.x & 31) == 0) atomicMin(&S.cons_count, c);

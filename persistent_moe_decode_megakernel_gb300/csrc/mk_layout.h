@@ -44,6 +44,16 @@ constexpr int kMaxCtas = 256;     // thread blocks (SMs) a step may use
 constexpr int kMoeScratch = 12288;  // floats of shared memory for the down projection of one block
 
 constexpr int kRouterRows = 8;    // router (expert) rows per router tile
+// Router rows per tile: kRouterRows, or for engines sized for batches of 8 or more (where a
+// tile's cost grows with the batch) as few as spreads the experts over every block.
+MK_HD int router_tile_rows(int E, int n_ctas, int max_batch) {
+  return max_batch >= 8 ? (E + n_ctas - 1) / n_ctas : kRouterRows;
+}
+
+// Rows of the batch per register group in the widest GEMV instantiation: four, or as many
+// rows of length K as the input staging area holds (three at K = 4096), so that every
+// group's input is staged once in shared memory.
+MK_HD int wide_group_rows(int K) { return 4 * K <= kMoeScratch ? 4 : kMoeScratch / K; }
 constexpr int kAttnScratch = 4 * kMaxG * (128 + 2);   // floats: attention prologue / cached MoE input
 
 // ---- small-batch MoE path ----------------------------------------------------------
@@ -180,9 +190,6 @@ struct alignas(64) Params {
   uint64_t* PML;   // [L][max_items][G][2]   their (max, sum)
   uint64_t* RLOG;  // [L][max_batch][E] router logits (+ bias)
   uint64_t* HB;    // [L][max_batch][K][F] SwiGLU activations per (row, slot)
-  uint64_t* SS;    // [2L+1][n_ss_slots][max_batch] per-block sums of squares of the residual stream
-  int32_t n_ss_slots;
-  int32_t need_ss;      // some GEMV input is too wide to stage and reads SS (else SS is not written)
   int32_t small_moe;    // this step runs the small-batch MoE path
   uint64_t* PT;         // [L][n_ctas][kSmallMaxB][H] per-block partial MoE outputs (small-batch path)
   int32_t* next_token;  // greedy selection: [B] argmax of the logits, or null (not requested)

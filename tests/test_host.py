@@ -114,9 +114,12 @@ def _check_static_plan(cfg, n_ctas):
 def test_static_plan_covers_every_row_once():
     _check_static_plan(_cfg(), N_CTAS)
     _check_static_plan(_cfg(), 7)
-    info = _check_static_plan(mk.make_config(W.MOE30B, 16, 1000, 64, 600), N_CTAS)
+    info = _check_static_plan(mk.make_config(W.MOE30B, 16, 1000, 1, 600), N_CTAS)
     assert info.n_qkv_tiles == N_CTAS and info.n_router_tiles == 16   # 8 expert rows per router tile
     assert info.n_down_ranges == N_CTAS
+    # engines sized for wide batches spread the router over the blocks: one expert row per tile
+    info = _check_static_plan(mk.make_config(W.MOE30B, 16, 1000, 64, 600), N_CTAS)
+    assert info.n_router_tiles == 128
 
 
 @pytest.mark.parametrize("lens", [[65], [1], [16], [17], [512, 1, 33, 200, 16, 15, 100, 7], [8193],
