@@ -117,6 +117,17 @@ __device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uin
   hi = *reinterpret_cast<const uint32_t*>(&h);
   lo = *reinterpret_cast<const uint32_t*>(&r);
 }
+// two floats -> three bf16x2 terms (high, middle, low) whose sum keeps the floats' 24-bit
+// significands: each term is the bf16 rounding of what the previous ones left over
+__device__ __forceinline__ void split3_bf16x2(float a, float b, uint32_t& hi, uint32_t& mid, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  const float a1 = a - __low2float(h), b1 = b - __high2float(h);
+  const __nv_bfloat162 m = __floats2bfloat162_rn(a1, b1);
+  const __nv_bfloat162 r = __floats2bfloat162_rn(a1 - __low2float(m), b1 - __high2float(m));
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  mid = *reinterpret_cast<const uint32_t*>(&m);
+  lo = *reinterpret_cast<const uint32_t*>(&r);
+}
 // L2 prefetch of a contiguous byte range (16-byte aligned, size a multiple of 16)
 __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
@@ -1276,6 +1287,90 @@ struct Consumer {
     return false;   // unreachable: register groups are sized so that their input fits the scratch
   }
 
+  // Wide batches: one chunk of n weight rows (gate/up: n gate rows, then their n up rows)
+  // against the staged input rows of the current register group, on tensor cores.
+  // mma.m16n8k16 (bf16 operands, fp32 accumulation): A = 16 weight rows, B = 16 input
+  // positions of the group's rows as the 8 columns (rows nt..7 zero).  The input is split into
+  // three bf16 terms (high, middle, low), three MMAs into separate accumulators, so the
+  // products keep the fp32 input's full significand; the weights are exact.  (Two terms,
+  // ~16 bits, move the k and v the step appends across bf16 rounding boundaries often enough
+  // to matter downstream.)  The warps split K; a lane's 16-byte load of a weight row
+  // (8 positions) feeds two k-steps, and the input positions are permuted alike (the terms of a
+  // dot product may be taken in any order).  The warps' partial sums meet in shared memory.
+  __device__ __forceinline__ void mma_chunk(const OutMap& om, bool gu, int n, int K, uint32_t row0, const uint8_t* wsm,
+                                            const float* ys, int nt, const int (&rb)[TB], const int (&rj)[TB], int par) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int NR = gu ? 2 * n : n;   // weight rows in the chunk, at most kMaxRowsPerChunk
+    const bool two = NR > 16;        // a second 16-row tile
+    const int KP = (K + 31) >> 5;    // 32-position steps of K, split over the warps
+    const int kp0 = warp * KP / kConsumerWarps, kp1 = (warp + 1) * KP / kConsumerWarps;
+    const uint8_t* wrow = wsm + static_cast<size_t>(g) * K * 2;   // rows g, g + 8, g + 16, g + 24
+    const size_t r8 = static_cast<size_t>(8) * K * 2;
+    const float* xrow = ys + static_cast<size_t>(g) * K;
+    const bool xin = g < nt;
+    float acc[2][3][4];   // [row tile][high, middle, low term of the input][fragment]
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+      for (int h = 0; h < 3; ++h)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[m][h][i] = 0.f;
+    for (int kp = kp0; kp < kp1; ++kp) {
+      const int k = kp * 32 + 8 * t;   // this lane's 8 positions (K is a multiple of 8)
+      const bool kin = k < K;
+      uint4 wa[4];
+#pragma unroll
+      for (int h = 0; h < 4; ++h)
+        wa[h] = (kin && g + 8 * h < NR) ? *reinterpret_cast<const uint4*>(wrow + h * r8 + k * 2) : make_uint4(0u, 0u, 0u, 0u);
+      float4 xv[2];
+#pragma unroll
+      for (int s = 0; s < 2; ++s)
+        xv[s] = (kin && xin) ? *reinterpret_cast<const float4*>(xrow + k + 4 * s) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        // k-step s: fragment positions (2t, 2t+1) and (2t+8, 2t+9) are the lane's positions
+        // 4s, 4s+1 and 4s+2, 4s+3
+        uint32_t bh0, bm0, bl0, bh1, bm1, bl1;
+        split3_bf16x2(xv[s].x, xv[s].y, bh0, bm0, bl0);
+        split3_bf16x2(xv[s].z, xv[s].w, bh1, bm1, bl1);
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          if (m == 1 && !two) break;
+          const uint4 u0 = wa[2 * m], u1 = wa[2 * m + 1];
+          const uint32_t a[4] = {s ? u0.z : u0.x, s ? u1.z : u1.x, s ? u0.w : u0.y, s ? u1.w : u1.y};
+          mma_bf16(acc[m][0], a, bh0, bh1);
+          mma_bf16(acc[m][1], a, bm0, bm1);
+          mma_bf16(acc[m][2], a, bl0, bl1);
+        }
+      }
+    }
+    // the partial sums share storage with the MoE input cache, which may be this chunk's input
+    if (ys == S.scr.attn) cbar();
+    if (threadIdx.x == 0) S.ykey = -1;
+    float (*seg)[kConsumerWarps][4] = S.scr.seg[par];
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      if (m == 1 && !two) break;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int row = 16 * m + g + (i >= 2 ? 8 : 0), col = 2 * t + (i & 1);
+        if (col < 4 && row < NR) seg[row][warp][col] = acc[m][0][i] + (acc[m][1][i] + acc[m][2][i]);
+      }
+    }
+    cbar();
+    const int r = threadIdx.x >> 2, tb = threadIdx.x & 3;
+    if (r < n && tb < nt) {
+      float v = 0.f, v2 = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        v += seg[r][w][tb];
+        if (gu) v2 += seg[n + r][w][tb];
+      }
+      put(om, gu, row0 + r, pick_i<TB>(rb, tb), pick_i<TB>(rj, tb), v, v2);
+    }
+  }
+
   __device__ __forceinline__ bool stream_gemv(int op) {
     constexpr bool kGroups = TB == 4;   // only the widest instantiation sees batches wider than its registers
     const int l = meta().layer;
@@ -1344,67 +1439,8 @@ struct Consumer {
           cur_g = g;
         }
         if constexpr (TB == 4) {
-          if (gu && sg.S > 1 && ysrc != nullptr) {
-            // the same for an expert run: a warp keeps FFN rows f = warp + 8i whole (gate row f and
-            // up row n + f), K in passes, one paired reduction per row
-            float ag[2][TB], au[2][TB];
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-#pragma unroll
-              for (int tb = 0; tb < TB; ++tb) { ag[i][tb] = 0.f; au[i][tb] = 0.f; }
-            Seg<TB> sp = sg;
-            for (int pass = 0; pass < sg.S; ++pass) {
-              sp.s = pass;
-              load_y_staged(ysrc, sp, K, nt, y);
-#pragma unroll
-              for (int i = 0; i < 2; ++i) {
-                const int f = (threadIdx.x >> 5) + kConsumerWarps * i;
-                if (f < n) {
-                  row_dot<TB>(wsm + static_cast<size_t>(f) * K * 2, sp, y, ag[i]);
-                  row_dot<TB>(wsm + static_cast<size_t>(n + f) * K * 2, sp, y, au[i]);
-                }
-              }
-            }
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-              const int f = (threadIdx.x >> 5) + kConsumerWarps * i;
-              warp_sum2<TB>(ag[i], au[i]);
-              float up[TB];
-#pragma unroll
-              for (int tb = 0; tb < TB; ++tb) up[tb] = __shfl_xor_sync(0xffffffffu, ag[i][tb], 16);
-              if (f < n && lane < nt)
-                put(om, true, row0 + f, pick_i<TB>(rb, lane), pick_i<TB>(rj, lane), pick<TB>(ag[i], lane),
-                    pick<TB>(up, lane));
-            }
-            continue;
-          }
-          if (!moe && sg.S > 1 && om.resid == nullptr && ysrc != nullptr) {
-            // wide batch, staged input: a warp keeps whole rows (rows warp + 8i) and sweeps K in
-            // sg.S passes, reloading its register slice of the staged rows per pass; one paired
-            // reduction per two rows at the end, instead of per-segment sums across warps
-            float acc[4][TB];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-              for (int tb = 0; tb < TB; ++tb) acc[i][tb] = 0.f;
-            Seg<TB> sp = sg;
-            for (int pass = 0; pass < sg.S; ++pass) {
-              sp.s = pass;
-              load_y_staged(ysrc, sp, K, nt, y);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const int r = (threadIdx.x >> 5) + kConsumerWarps * i;
-                if (r < n) row_dot<TB>(wsm + static_cast<size_t>(r) * K * 2, sp, y, acc[i]);
-              }
-            }
-#pragma unroll
-            for (int i = 0; i < 4; i += 2) {
-              warp_sum2<TB>(acc[i], acc[i + 1]);
-              const int tb = lane & 15;
-              const int rr = (threadIdx.x >> 5) + kConsumerWarps * (lane < 16 ? i : i + 1);
-              if (tb < nt && rr < n)
-                put(om, false, row0 + rr, pick_i<TB>(rb, tb), pick_i<TB>(rj, tb), pick<TB>(acc[i], tb), 0.f);
-            }
+          if (ysrc != nullptr) {   // the group's input is staged: the chunk runs on tensor cores
+            mma_chunk(om, gu, n, K, row0, wsm, ysrc, nt, rb, rj, par);
             continue;
           }
         }
@@ -2381,6 +2417,7 @@ struct Consumer {
   // A warp per head finds the head's max and normaliser over the splits (a lane per split)
   // and leaves each split's scale exp(m_s - M) / L; then 8 lanes per output sum the splits.
   __device__ __forceinline__ bool attn_combine(int l) {
+    trace_mark(66, l);
     const int Gq = p.G;
     const int GD = Gq * D;
     const int cta = blockIdx.x;
@@ -2410,6 +2447,7 @@ struct Consumer {
       }, S.moe + 0, p.tag) && ok;
       if (!ok) ll_timeout(p, MK_OP_ATTN, l);
       if (!cbar_and(ok)) return false;
+      trace_mark(64, l);
       for (int h = warp; h < Gq; h += kConsumerWarps) {
         float M = -INFINITY;
         for (int sp = lane; sp < ns; sp += 32) M = fmaxf(M, ml[(sp * Gq + h) * 2]);
