@@ -70,7 +70,7 @@ def _bind(lib):
         getattr(lib, f"orc_softmax_{suf}").argtypes = [i32, vp, vp]
         getattr(lib, f"orc_topk_{suf}").argtypes = [i32, i32, vp, vp]
         getattr(lib, f"orc_embed_{suf}").argtypes = [vp, vp, i32, vp, vp]
-        getattr(lib, f"orc_attn_block_{suf}").argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp]
+        getattr(lib, f"orc_attn_block_{suf}").argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, i32]
         getattr(lib, f"orc_attn_block_{suf}").restype = i32
         getattr(lib, f"orc_route_{suf}").argtypes = [vp, vp, i32, vp, vp, vp, vp, vp]
         getattr(lib, f"orc_moe_{suf}").argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]
@@ -227,7 +227,7 @@ class Oracle:
             kv = fetch.kv_layer(l)
             assert kv.dtype == np.uint16 and kv.flags.c_contiguous
             rc = self._fn("attn_block")(ctypes.byref(dims), ctypes.byref(L), B, _p(x), _p(sl), _p(bt), _p(kv),
-                                        None, None)
+                                        None, None, 1)
             if rc != 0:
                 raise ValueError(f"oracle attention rejected its inputs (code {rc})")
             self._fn("route")(ctypes.byref(dims), ctypes.byref(L), B, _p(x), _p(y), _p(r), _p(ids), _p(wts))
@@ -250,8 +250,10 @@ class Oracle:
         return logits
 
     # ---- one layer's pieces (for per-op traces in the tests) ----------------
-    def layer_trace(self, dims: Dims, lw: dict, x, seq_lens, block_tables, kv_layer):
-        """Run one layer on ``x`` ([B,H]); return a dict of every intermediate."""
+    def layer_trace(self, dims: Dims, lw: dict, x, seq_lens, block_tables, kv_layer, append: bool = True):
+        """Run one layer on ``x`` ([B,H]); return a dict of every intermediate.  With
+        ``append=False`` the cache already holds the current token's k and v (codes written by
+        the implementation under test) and attention reads them instead of writing its own."""
         keep = []
         L = self._layer_struct(lw, keep)
         x = np.array(x, dtype=self.dt, copy=True, order="C")
@@ -262,7 +264,7 @@ class Oracle:
         qkv = np.empty((B, nqkv), dtype=self.dt)
         attn = np.empty((B, dims.n_q * dims.head_dim), dtype=self.dt)
         rc = self._fn("attn_block")(ctypes.byref(dims), ctypes.byref(L), B, _p(x), _p(sl), _p(bt), _p(kv_layer),
-                                    _p(qkv), _p(attn))
+                                    _p(qkv), _p(attn), 1 if append else 0)
         if rc != 0:
             raise ValueError(f"oracle attention rejected its inputs (code {rc})")
         x_mid = x.copy()

@@ -153,9 +153,12 @@ inline size_t kv_offset(const orc_dims& d, int page, int which, int kvh, int slo
   return ((((static_cast<size_t>(page) * 2 + which) * d.n_kv + kvh) * d.page_size + slot) * d.head_dim);
 }
 
+// append = false: the cache already holds the current token's k and v at position
+// seq_len-1 (codes another implementation wrote); they are read, not recomputed, so a check
+// of the attention can use the same bf16 codes as the implementation it checks.
 template <typename T>
 int attn_block(const orc_dims& d, const orc_layer& w, int B, T* x, const int32_t* seq_lens,
-               const int32_t* bt, uint16_t* kv, T* trace_qkv, T* trace_attn) {
+               const int32_t* bt, uint16_t* kv, T* trace_qkv, T* trace_attn, bool append = true) {
   const int H = d.hidden, D = d.head_dim, Hq = d.n_q, Hkv = d.n_kv, G = Hq / Hkv;
   const int NQKV = (Hq + 2 * Hkv) * D;
   const T scale = static_cast<T>(1) / tsqrt<T>(static_cast<T>(D));
@@ -173,7 +176,7 @@ int attn_block(const orc_dims& d, const orc_layer& w, int B, T* x, const int32_t
     // append the current token's k and v to the cache (bf16, RNE)
     const int page = tab[pos / d.page_size], slot = pos % d.page_size;
     if (page < 0 || page >= d.num_pages) return -2;
-    for (int g = 0; g < Hkv; ++g) {
+    for (int g = 0; g < Hkv && append; ++g) {
       const T* kg = qkv.data() + static_cast<size_t>(Hq + g) * D;
       const T* vg = qkv.data() + static_cast<size_t>(Hq + Hkv + g) * D;
       uint16_t* kd = kv + kv_offset(d, page, 0, g, slot);
@@ -323,8 +326,8 @@ float orc_bf16_to_f32(uint16_t u) { return bf16_to_f32(u); }
     embed<T>(*d, table, B, tok, x);                                                                               \
   }                                                                                                               \
   int orc_attn_block_##SUF(const orc_dims* d, const orc_layer* w, int B, T* x, const int32_t* seq_lens,           \
-                           const int32_t* bt, uint16_t* kv_layer, T* trace_qkv, T* trace_attn) {                  \
-    return attn_block<T>(*d, *w, B, x, seq_lens, bt, kv_layer, trace_qkv, trace_attn);                            \
+                           const int32_t* bt, uint16_t* kv_layer, T* trace_qkv, T* trace_attn, int append) {      \
+    return attn_block<T>(*d, *w, B, x, seq_lens, bt, kv_layer, trace_qkv, trace_attn, append != 0);               \
   }                                                                                                               \
   void orc_route_##SUF(const orc_dims* d, const orc_layer* w, int B, const T* x, T* y, T* logits, int32_t* ids,  \
                        T* wts) {                                                                                  \

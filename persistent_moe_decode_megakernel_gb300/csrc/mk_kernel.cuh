@@ -615,7 +615,8 @@ struct Producer {
       case MK_OP_ROUTER: W = lw.w_router; K = p.H; break;
       default: W = p.lm_head; K = p.H; break;
     }
-    const int rpc = gemv_rows_per_chunk(K);
+    int rpc = gemv_rows_per_chunk(K);
+    if (p.B > kSmallMaxB && rpc > 16) rpc &= ~15;   // tensor-core tiles of wide batches: whole 16-row tiles
     // A batch wider than one register group (groups of 4 rows) is served group-major: the tile
     // is streamed once per group (aux = group), so the consumers stage each group's input once
     // per tile; the repeated reads of the tile come from L2 (evict-normal while it is reused).
@@ -1291,14 +1292,17 @@ struct Consumer {
   // against the staged input rows of the current register group, on tensor cores.
   // mma.m16n8k16 (bf16 operands, fp32 accumulation): A = 16 weight rows, B = 16 input
   // positions of the group's rows as the 8 columns (rows nt..7 zero).  The input is split into
-  // three bf16 terms (high, middle, low), three MMAs into separate accumulators, so the
-  // products keep the fp32 input's full significand; the weights are exact.  (Two terms,
-  // ~16 bits, move the k and v the step appends across bf16 rounding boundaries often enough
-  // to matter downstream.)  The warps split K; a lane's 16-byte load of a weight row
+  // bf16 terms (high, middle, low), one MMA each into separate accumulators; the weights are
+  // exact.  All three (exact: the fp32 input's full significand) for the QKV projection,
+  // whose k and v the step rounds to bf16 for the cache (with two, ~16 bits, they cross bf16
+  // rounding boundaries often enough to matter downstream), and for the O-proj, whose output
+  // is the residual stream.  Two for the router, gate/up and LM head; the MMA issue rate
+  // bounds these tiles.  The warps split K; a lane's 16-byte load of a weight row
   // (8 positions) feeds two k-steps, and the input positions are permuted alike (the terms of a
   // dot product may be taken in any order).  The warps' partial sums meet in shared memory.
-  __device__ __forceinline__ void mma_chunk(const OutMap& om, bool gu, int n, int K, uint32_t row0, const uint8_t* wsm,
-                                            const float* ys, int nt, const int (&rb)[TB], const int (&rj)[TB], int par) {
+  __device__ __forceinline__ void mma_chunk(const OutMap& om, bool gu, bool exact, int n, int K, uint32_t row0,
+                                            const uint8_t* wsm, const float* ys, int nt, const int (&rb)[TB],
+                                            const int (&rj)[TB], int par) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     const int NR = gu ? 2 * n : n;   // weight rows in the chunk, at most kMaxRowsPerChunk
@@ -1341,7 +1345,7 @@ struct Consumer {
           const uint32_t a[4] = {s ? u0.z : u0.x, s ? u1.z : u1.x, s ? u0.w : u0.y, s ? u1.w : u1.y};
           mma_bf16(acc[m][0], a, bh0, bh1);
           mma_bf16(acc[m][1], a, bm0, bm1);
-          mma_bf16(acc[m][2], a, bl0, bl1);
+          if (exact) mma_bf16(acc[m][2], a, bl0, bl1);
         }
       }
     }
@@ -1440,7 +1444,7 @@ struct Consumer {
         }
         if constexpr (TB == 4) {
           if (ysrc != nullptr) {   // the group's input is staged: the chunk runs on tensor cores
-            mma_chunk(om, gu, n, K, row0, wsm, ysrc, nt, rb, rj, par);
+            mma_chunk(om, gu, op == MK_OP_QKV || op == MK_OP_OPROJ, n, K, row0, wsm, ysrc, nt, rb, rj, par);
             continue;
           }
         }

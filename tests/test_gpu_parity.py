@@ -40,14 +40,18 @@ def _parity_one_step(setup, max_batch=8, check_layers=True, flags=0):
         if top2_margin(ref[b]) > MARGIN:
             assert int(np.argmax(got[b])) == int(np.argmax(ref[b]))
     if check_layers:
-        # per-op check, layer by layer, each layer fed the GPU's own input so errors do not compound
+        # per-op check, layer by layer, each layer fed the GPU's own input so errors do not compound.
+        # Attention reads the cache the GPU left (the prefix plus the k and v codes it appended; those
+        # codes are checked against the oracle's below): an appended value whose fp32 k or v lies within
+        # the GEMV's rounding error of a bf16 rounding boundary may round the other way, and that one-ulp
+        # difference is not an attention error.
         m = setup["model"]
         x_all = eng.debug_read("x")
-        kv_layer_in = setup["kv"].copy()
+        kv_after = W.bf16_bits(kv_dev)
         for l in range(m["layers"]):
             x_in = x_all[2 * l]
             tr = orc.layer_trace(setup["dims"], setup["wn"]["layers"][l], x_in, setup["seq_lens"], setup["bt"],
-                                 kv_layer_in[l])
+                                 np.ascontiguousarray(kv_after[l]), append=False)
             assert rel_l2(eng.debug_read("qkv", l), tr["qkv"]) < 1e-5
             assert rel_l2(eng.debug_read("attn", l), tr["attn"]) < 1e-4
             assert rel_l2(x_all[2 * l + 1], tr["x_mid"]) < 1e-5

@@ -95,6 +95,35 @@ def test_one_token_attention_returns_v(oracle32, tiny_w):
     assert np.array_equal(cached, v_bf16)
 
 
+def test_layer_trace_over_given_codes(oracle32, tiny_w):
+    # append=False reads the current token's k and v from the cache instead of writing them: over
+    # the codes an appending run left, every intermediate is bit-identical; with one appended v
+    # code moved by one bf16 ulp, the one-token row's attention (which is v) moves by exactly that
+    m = W.TINY
+    dims = make_dims(m, 16, 4, 2)
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((2, m["hidden"])).astype(np.float32)
+    kv = np.zeros(W.kv_shape(dict(m, layers=1), 4, 16), dtype=np.uint16)[0]
+    prefix = rng.standard_normal((2, m["n_kv"], 3, m["head_dim"])).astype(np.float32).view(np.uint32).astype(np.uint64)
+    kv[0, :, :, :3, :] = ((prefix + 0x7FFF + ((prefix >> 16) & 1)) >> 16).astype(np.uint16)   # bf16 codes (RNE)
+    bt = np.array([[0, 1], [2, 3]], dtype=np.int32)
+    a = oracle32.layer_trace(dims, tiny_w["layers"][0], x, [4, 1], bt, kv)   # appends into kv
+    b = oracle32.layer_trace(dims, tiny_w["layers"][0], x, [4, 1], bt, kv.copy(), append=False)
+    for k in ("qkv", "attn", "x_mid", "router_logits", "h", "x_out"):
+        assert np.array_equal(a[k].view(np.uint32), b[k].view(np.uint32)), k
+    moved = kv.copy()
+    moved[2, 1, 0, 0, 5] += 1                  # row 1 (one token): page 2, V, KV head 0, slot 0, dim 5
+    c = oracle32.layer_trace(dims, tiny_w["layers"][0], x, [4, 1], bt, moved, append=False)
+    d_attn = c["attn"] - a["attn"]
+    G, D = m["n_q"] // m["n_kv"], m["head_dim"]
+    want = np.float32(BF.bf16_to_f64(moved[2, 1, 0, 0, 5]) - BF.bf16_to_f64(kv[2, 1, 0, 0, 5]))
+    for h in range(m["n_q"]):
+        for i in range(D):
+            exp = want if (h // G == 0 and i == 5) else 0.0
+            assert d_attn[1, h * D + i] == exp
+    assert np.array_equal(c["attn"][0], a["attn"][0])
+
+
 def test_single_expert_reduces_to_dense_swiglu(oracle64):
     m = _model(n_exp=1, top_k=1)
     wn = np_weights(W.make_weights(m, "cpu", seed=99))
