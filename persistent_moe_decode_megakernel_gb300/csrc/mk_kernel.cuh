@@ -1293,11 +1293,10 @@ struct Consumer {
   // mma.m16n8k16 (bf16 operands, fp32 accumulation): A = 16 weight rows, B = 16 input
   // positions of the group's rows as the 8 columns (rows nt..7 zero).  The input is split into
   // bf16 terms (high, middle, low), one MMA each into separate accumulators; the weights are
-  // exact.  All three (exact: the fp32 input's full significand) for the QKV projection,
-  // whose k and v the step rounds to bf16 for the cache (with two, ~16 bits, they cross bf16
-  // rounding boundaries often enough to matter downstream), and for the O-proj, whose output
-  // is the residual stream.  Two for the router, gate/up and LM head; the MMA issue rate
-  // bounds these tiles.  The warps split K; a lane's 16-byte load of a weight row
+  // exact.  Two terms keep ~16 bits of the fp32 input (relative error of a dot product ~3e-6
+  // of its terms' magnitude), the third all of it.  The MMA issue rate bounds these tiles, so
+  // three (`exact`) serve only the QKV projection: the step rounds its k and v to bf16 for
+  // the cache, and a component that cancels to near zero must keep fp32 accuracy there.  The warps split K; a lane's 16-byte load of a weight row
   // (8 positions) feeds two k-steps, and the input positions are permuted alike (the terms of a
   // dot product may be taken in any order).  The warps' partial sums meet in shared memory.
   __device__ __forceinline__ void mma_chunk(const OutMap& om, bool gu, bool exact, int n, int K, uint32_t row0,
@@ -1444,7 +1443,7 @@ struct Consumer {
         }
         if constexpr (TB == 4) {
           if (ysrc != nullptr) {   // the group's input is staged: the chunk runs on tensor cores
-            mma_chunk(om, gu, op == MK_OP_QKV || op == MK_OP_OPROJ, n, K, row0, wsm, ysrc, nt, rb, rj, par);
+            mma_chunk(om, gu, op == MK_OP_QKV, n, K, row0, wsm, ysrc, nt, rb, rj, par);
             continue;
           }
         }
