@@ -1990,6 +1990,43 @@ struct Consumer {
       const int a0 = static_cast<int>(meta().idx);
       const bool last = meta().last;
       const uint8_t* wsm = slot();
+      if constexpr (TB == 4) {
+        if (B >= 16) {
+          // wide batches: the chunk's (expert, group of TD pairs) units are dealt over the
+          // warps; a warp fetches its pairs' SwiGLU inputs once and runs all of the expert's
+          // rows in the chunk against them
+          int gbase = 0;   // pair groups of the chunk's earlier experts
+          for (int ai = 0; ai < ne; ++ai) {
+            const int cnt = warp_expert_pairs(S.eact[a0 + ai], wl);
+            const int ng = (cnt + TD - 1) / TD;
+            const int i0 = ai * nrc, iend = i0 + nrc;
+            for (int g = (warp + kConsumerWarps - gbase % kConsumerWarps) % kConsumerWarps; g < ng;
+                 g += kConsumerWarps) {
+              const int g0 = g * TD, nt = min(TD, cnt - g0);
+              float y[8 / TD][8][TD];
+              ok = load_h_pairs<TD>(sg, l, hc, wl + g0, nt, y) && ok;
+              for (int ii = i0; ii < iend; ii += 2) {
+                float a[TD], b[TD];
+#pragma unroll
+                for (int tb = 0; tb < TD; ++tb) { a[tb] = 0.f; b[tb] = 0.f; }
+                row_dot<TD>(wsm + static_cast<size_t>(ii) * F * 2, sg, y, a);
+                if (ii + 1 < iend) row_dot<TD>(wsm + static_cast<size_t>(ii + 1) * F * 2, sg, y, b);
+                warp_sum2<TD>(a, b);
+                const int tb = lane & 15;
+                const int row = lane < 16 ? ii : ii + 1;
+                if (tb < nt && row < iend) {
+                  const int pi = wl[g0 + tb];
+                  P[pi * nrow + rb0 + (row - i0) - r0] = S.rwcache[pi] * pick<TD>(a, tb);
+                }
+              }
+            }
+            gbase += ng;
+          }
+          if (last) break;
+          if (!next_rec()) break;
+          continue;
+        }
+      }
       const int R = ne * nrc;
       const int i1 = (warp + 1) * R / kConsumerWarps;
       for (int i = warp * R / kConsumerWarps; i < i1;) {

@@ -166,6 +166,14 @@ def test_medium_batch_above_register_group():
     _parity_one_step(s, max_batch=8, check_layers=False)
 
 
+@pytest.mark.parametrize("model", [W.TINY, MEDIUM])
+def test_wide_batch_tensor_core_path(model):
+    # 20 rows: dense and gate/up tiles on tensor cores in register groups of four, and the down
+    # projection dealing (expert, pair group) units over the warps; every layer checked
+    lens = [int(x) for x in np.random.default_rng(21).integers(1, 160, 20)]
+    _parity_one_step(tiny_setup(model, lens), max_batch=24)
+
+
 def test_tiny_bs8_ragged_continuous_batching():
     """32 greedy steps, teacher-forced with the oracle's argmax; at step 16 row 0
     finishes and a new sequence (length U{1..512}, prefilled by the oracle) takes
