@@ -195,6 +195,25 @@ def test_simulated_moe_paths(B, flags):
         assert r.finished and not r.deadlocked and r.counters_ok and r.moe_units_ok
 
 
+@pytest.mark.parametrize("B", [3, 7, 16])
+def test_simulated_wide_batches_hidden_4096(B):
+    # at hidden 4096 a register group holds three rows (their staged inputs fill the scratch), so
+    # expert runs are streamed in ceil(rows / 3) passes; every unit is still covered once
+    m = W.scaled_model(W.MOE30B, hidden=4096, layers=2)
+    cfg = mk.make_config(m, 16, 4000, 16, 200)
+    rng = np.random.default_rng(B)
+    lens = [int(x) for x in rng.integers(1, 2000, B)]
+    r = mk.simulate(cfg, N_CTAS, lens, _random_routing(cfg, B, B), seed=B, lead=3)
+    assert r.finished and not r.deadlocked and r.counters_ok and r.moe_units_ok
+
+
+def test_router_tiles_follow_engine_width():
+    # engines sized for batches of 8 or more take one expert row per router tile, smaller ones 8
+    for mb, tiles in ((1, 16), (7, 16), (8, 128), (64, 128)):
+        info, _, _ = mk.plan_static(mk.make_config(W.MOE30B, 16, 1000, mb, 600), N_CTAS)
+        assert info.n_router_tiles == tiles, (mb, info.n_router_tiles)
+
+
 def test_config_flags_are_checked():
     cfg = _cfg()
     cfg.flags = 2
