@@ -198,6 +198,25 @@ class Oracle:
             raise ValueError(f"oracle decode_step rejected its inputs (code {rc})")
         return logits
 
+    def final(self, dims: Dims, final_norm, lm_head, x):
+        """Final RMSNorm and LM head of the residual rows ``x`` ([B, H]); returns [B, vocab]."""
+        x = np.ascontiguousarray(x, dtype=self.dt)
+        fn, head = _u16(final_norm), _u16(lm_head)
+        B = x.shape[0]
+        logits = np.empty((B, dims.vocab), dtype=self.dt)
+        self._fn("final")(ctypes.byref(dims), _p(fn), _p(head), B, _p(x), _p(logits))
+        return logits
+
+    @staticmethod
+    def _expert_ptrs(ids, expert):
+        """Per (row, slot) of ``ids`` ([B, K], row-major), the addresses of the routed expert's
+        gate/up and down matrices; ``expert(e)`` returns that expert's (gate_up, down) arrays,
+        which must stay alive while the addresses are used."""
+        flat = [int(e) for e in np.asarray(ids).ravel()]
+        gu_p = (ctypes.c_void_p * len(flat))(*[expert(e)[0].ctypes.data for e in flat])
+        dn_p = (ctypes.c_void_p * len(flat))(*[expert(e)[1].ctypes.data for e in flat])
+        return gu_p, dn_p
+
     # ---- the same step, layer by layer, fetching weights on demand ------------
     def decode_step_lazy(self, dims: Dims, fetch, tokens, seq_lens, block_tables, trace: dict | None = None):
         """Decode step with weights fetched per layer.
@@ -239,15 +258,11 @@ class Oracle:
             for e in sorted(set(int(v) for v in ids.ravel())):
                 gu, dn = fetch.expert(l, e)
                 experts[e] = (_u16(gu), _u16(dn))
-            gu_p = (ctypes.c_void_p * (B * K))(*[experts[int(e)][0].ctypes.data for e in ids.ravel()])
-            dn_p = (ctypes.c_void_p * (B * K))(*[experts[int(e)][1].ctypes.data for e in ids.ravel()])
+            gu_p, dn_p = self._expert_ptrs(ids, lambda e: experts[e])
             self._fn("moe")(ctypes.byref(dims), B, _p(y), _p(ids), _p(wts), gu_p, dn_p, _p(x), None, None)
             del experts, keep, kv
         fn, head = fetch.final()
-        fn, head = _u16(fn), _u16(head)
-        logits = np.empty((B, dims.vocab), dtype=self.dt)
-        self._fn("final")(ctypes.byref(dims), _p(fn), _p(head), B, _p(x), _p(logits))
-        return logits
+        return self.final(dims, fn, head, x)
 
     # ---- one layer's pieces (for per-op traces in the tests) ----------------
     def layer_trace(self, dims: Dims, lw: dict, x, seq_lens, block_tables, kv_layer, append: bool = True):
@@ -274,8 +289,7 @@ class Oracle:
         wts = np.empty((B, K), dtype=self.dt)
         self._fn("route")(ctypes.byref(dims), ctypes.byref(L), B, _p(x), _p(y), _p(r), _p(ids), _p(wts))
         gu_all, dn_all = _u16(lw["w_gate_up"]), _u16(lw["w_down"])
-        gu_p = (ctypes.c_void_p * (B * K))(*[gu_all[int(e)].ctypes.data for e in ids.ravel()])
-        dn_p = (ctypes.c_void_p * (B * K))(*[dn_all[int(e)].ctypes.data for e in ids.ravel()])
+        gu_p, dn_p = self._expert_ptrs(ids, lambda e: (gu_all[e], dn_all[e]))
         h = np.empty((B, K, F), dtype=self.dt)
         moe_out = np.empty((B, H), dtype=self.dt)
         self._fn("moe")(ctypes.byref(dims), B, _p(y), _p(ids), _p(wts), gu_p, dn_p, _p(x), _p(h), _p(moe_out))

@@ -20,7 +20,7 @@
 // norm, LM head) and the fp32-accumulation rule come from the problem
 // statement the library implements; the pages do not spell them out.
 //
-// Readings where the pages are silent (each is also listed in the design doc):
+// Readings where the pages are silent:
 //   RMSNorm y = x * (1/sqrt(mean(x^2)+eps)) * g; NeoX rotate-half RoPE with
 //   angles pos*theta^(-2i/D) evaluated in fp64 then cast to fp32; pos =
 //   seq_len-1; k and v are rounded to bf16 (round-to-nearest-even) when

@@ -53,9 +53,11 @@ def route_mismatches(gpu_ids, orc_ids, orc_logits, K):
 
 
 class DeviceFetch:
-    """Weights and KV of a device-resident model, copied to the host on demand
-    (only the layer being computed and only the experts the oracle routed to).
-    ``rows`` selects batch rows; their KV pages are gathered into a compact pool."""
+    """Weights and KV of a torch-resident model (any device), copied to host arrays on
+    demand (only the layer being computed and only the experts the oracle routed to).
+    ``rows`` selects batch rows; their KV pages are gathered into a compact pool, page
+    k of the pool being the k-th page of the selected rows in row order, with block
+    tables ``self.bt`` that address it."""
 
     def __init__(self, w_dev: dict, kv_dev, bt_np, seq_lens, rows, page_size):
         self.w, self.kv = w_dev, kv_dev
@@ -77,7 +79,8 @@ class DeviceFetch:
         self.max_pages = maxp
 
     def embed_rows(self, tok):
-        return W.bf16_bits(self.w["embed"][torch.as_tensor(tok, dtype=torch.int64, device="cuda")])
+        emb = self.w["embed"]
+        return W.bf16_bits(emb[torch.as_tensor(tok, dtype=torch.int64, device=emb.device)])
 
     def layer(self, l):
         lw = self.w["layers"][l]
