@@ -17,6 +17,10 @@ timed with CUDA events on the launching stream with inputs resident in HBM;
 and block tables copied in, logits copied out, every step).  ``roofline``
 relates the algorithmic bytes of a step to the measured HBM copy bandwidth.
 ``cpu_baseline`` times the CPU oracle on a bounded sample of the same step.
+With the default 30B workload the same line also carries, under ``configs``, the
+other 30B workloads of the metric (batch 64 with ragged lengths and a Zipf
+router prior; batch 1 at 32K, 128K and 256K of context), each timed for a few
+seconds with its own clocks, roofline, e2e and CPU sample.
 Under torchrun each rank runs an independent replica (the step does not shard).
 """
 from __future__ import annotations
@@ -50,7 +54,32 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-s", type=float, default=12.0, help="target seconds of oracle work for the baseline")
+    ap.add_argument("--configs", default="all",
+                    help="other 30B workloads measured in the same run and reported under 'configs' "
+                         "(comma-separated names, 'all' or 'none')")
     return ap.parse_args()
+
+
+# the 30B workloads besides the headline one, measured in the same run
+OTHER_30B = ("moe30b_bs64_ragged", "moe30b_bs1_ctx32k", "moe30b_bs1_ctx128k", "moe30b_bs1_ctx256k")
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu model")):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
 
 
 def measured_peaks():
@@ -107,13 +136,20 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(self.rows)}
 
 
-def setup_workload(wl, layers_override, device):
+def setup_workload(wl, layers_override, device, weights=None):
+    """Seeded inputs of one workload; ``weights`` (the same model's bf16 tensors) are reused
+    when given, with the workload's router bias attached."""
     import torch
     m = dict(wl.model)
     if layers_override:
         m["layers"] = layers_override
     bias = W.zipf_router_bias(m, wl.zipf) if wl.zipf else None
-    w = W.make_weights(m, device, router_bias=bias)
+    if weights is None:
+        w = W.make_weights(m, device, router_bias=bias)
+    else:
+        w = dict(weights)
+        w["layers"] = [dict(lw, router_bias=None if bias is None else bias[l].to(device).contiguous())
+                       for l, lw in enumerate(weights["layers"])]
     ps = wl.page_size
     lens = list(wl.lengths)
     B = len(lens)
@@ -168,7 +204,7 @@ def cpu_baseline(st, budget_s: float):
     step_s = t_head + statistics.mean(layer_times) * m["layers"]
     cores = os.cpu_count()
     return {"value": B / step_s, "unit": "tok/s", "cores": int(os.environ.get("OMP_NUM_THREADS", cores)),
-            "kind": "oracle", "seconds_per_step": step_s,
+            "cpu_model": cpu_model(), "kind": "oracle", "seconds_per_step": step_s,
             "sample": f"{len(layer_times)} of {m['layers']} layers + final norm/LM head of one step "
                       f"(batch {B}), timed on the host, scaled to the whole step"}
 
@@ -217,6 +253,107 @@ def replica_value(ms_per_step: float, batch: int, device: str):
     return ms_per_step, world * batch / (ms_per_step / 1e3)
 
 
+def measure(eng, st, steps, warmup, local, world, with_e2e):
+    """Time ``steps`` decode steps of one workload (after ``warmup`` untimed ones): CUDA events
+    around every step on the launching stream, nvidia-smi clocks sampled meanwhile, then the same
+    through host buffers (e2e).  Returns (mean ms over ranks, median ms, tok/s, clocks, e2e, wall s)."""
+    import torch
+    m, B = st["model"], st["B"]
+    stream = torch.cuda.Stream()
+    tok_d = st["tokens"].cuda()
+    bt_d = st["bt"].cuda()
+    sl = np.array(st["lens"], dtype=np.int32)
+    logits = torch.empty(B, m["vocab"], dtype=torch.float32, device="cuda")
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            eng.step(tok_d, sl, bt_d, st["kv"], logits, stream=stream)
+    stream.synchronize()
+    eng.check()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    with ClockSampler(local) as clocks:
+        barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(steps):
+            ev[i][0].record(stream)
+            eng.step(tok_d, sl, bt_d, st["kv"], logits, stream=stream)
+            ev[i][1].record(stream)
+        stream.synchronize()
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        barrier()
+    eng.check()
+    per = [a.elapsed_time(b) for a, b in ev]
+    ms_mean = sum(per) / len(per)
+    ms_med = statistics.median(per)
+    ms_mean, value = replica_value(ms_mean, B, "cuda")
+
+    e2e = None
+    if with_e2e:
+        tok_h = st["tokens"].clone().pin_memory()
+        bt_h = st["bt"].clone().pin_memory()
+        out_h = torch.empty(B, m["vocab"], dtype=torch.float32).pin_memory()
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                tok_d.copy_(tok_h, non_blocking=True)
+                bt_d.copy_(bt_h, non_blocking=True)
+                eng.step(tok_d, sl, bt_d, st["kv"], logits, stream=stream)
+                out_h.copy_(logits, non_blocking=True)
+        stream.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(steps):
+                tok_d.copy_(tok_h, non_blocking=True)
+                bt_d.copy_(bt_h, non_blocking=True)
+                eng.step(tok_d, sl, bt_d, st["kv"], logits, stream=stream)
+                out_h.copy_(logits, non_blocking=True)
+            e1.record(stream)
+        stream.synchronize()
+        e2e_ms, e2e_value = replica_value(e0.elapsed_time(e1) / steps, B, "cuda")
+        e2e = {"value": e2e_value, "unit": "tok/s",
+               "h2d_bytes_per_step": int(tok_h.numel() * 4 + bt_h.numel() * 4),
+               "d2h_bytes_per_step": int(out_h.numel() * 4), "ms_per_step": e2e_ms,
+               "note": "token ids and block tables copied from pinned host memory, logits copied back, every step"}
+        eng.check()
+    return ms_mean, ms_med, value, clocks.summary(), e2e, wall
+
+
+def roofline_of(eng, st, wl_name, ms_mean):
+    """HBM roofline of the step kernel: algorithmic bytes of one step (the routed-expert union
+    read back from the step at batch > 1) over the mean step time, against the measured peak."""
+    m, B = st["model"], st["B"]
+    union = None
+    if B > 1:
+        union = [len(set(eng.debug_read("route_ids", l).ravel().tolist())) for l in range(m["layers"])]
+    by = R.step_bytes(m, st["lens"], expert_union=union, router_bias=st["bias"] is not None)
+    peak, peak_kind = measured_peaks()
+    achieved = by["total"] / (ms_mean / 1e3) / 1e9
+    sol = R.sol_tokens_per_s(by["total"], peak * 1e9, B)
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
+            "traffic": None, "algorithmic_bytes_per_step": by["total"], "bytes_breakdown": by,
+            "sol_tok_s": sol, "frac_of_nominal_8tbs": achieved / 8000.0,
+            "kernel": "mk::step_kernel (one launch per step; events also cover the 1 small per-step H2D copy)"}
+    if union is not None:
+        roof["expert_union_per_layer_mean"] = sum(union) / len(union)
+    traffic_file = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(traffic_file):
+        try:
+            tr = json.load(open(traffic_file)).get(wl_name)
+            if tr and tr.get("kernel_source_hash") == _kernel_hash():
+                roof["traffic"] = tr["bytes_per_step"]
+        except Exception:
+            pass
+    return roof
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -238,109 +375,62 @@ def main():
     st = setup_workload(wl, args.layers, "cuda")
     m, B = st["model"], st["B"]
     eng = mk.Engine(m, st["w"], st["ps"], st["num_pages"], max(B, 1), st["max_pages"])
-    stream = torch.cuda.Stream()
-    tok_d = st["tokens"].cuda()
-    bt_d = st["bt"].cuda()
-    sl = np.array(st["lens"], dtype=np.int32)
-    logits = torch.empty(B, m["vocab"], dtype=torch.float32, device="cuda")
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            eng.step(tok_d, sl, bt_d, st["kv"], logits, stream=stream)
-    stream.synchronize()
-    eng.check()
-
-    def barrier():
-        if world > 1:
-            torch.distributed.barrier()
-
-    # ---- device-resident timing: events around each step on the launching stream
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    with ClockSampler(local) as clocks:
-        barrier()
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        for i in range(args.steps):
-            ev[i][0].record(stream)
-            eng.step(tok_d, sl, bt_d, st["kv"], logits, stream=stream)
-            ev[i][1].record(stream)
-        stream.synchronize()
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - t0
-        barrier()
-    eng.check()
-    per = [a.elapsed_time(b) for a, b in ev]
-    ms_mean = sum(per) / len(per)
-    ms_med = statistics.median(per)
-    ms_mean, value = replica_value(ms_mean, B, "cuda")
-
-    # ---- end to end through the C ABI with host buffers
-    e2e = None
-    if not args.no_e2e:
-        tok_h = st["tokens"].clone().pin_memory()
-        bt_h = st["bt"].clone().pin_memory()
-        out_h = torch.empty(B, m["vocab"], dtype=torch.float32).pin_memory()
-        with torch.cuda.stream(stream):
-            for _ in range(2):
-                tok_d.copy_(tok_h, non_blocking=True)
-                bt_d.copy_(bt_h, non_blocking=True)
-                eng.step(tok_d, sl, bt_d, st["kv"], logits, stream=stream)
-                out_h.copy_(logits, non_blocking=True)
-        stream.synchronize()
-        barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(args.steps):
-                tok_d.copy_(tok_h, non_blocking=True)
-                bt_d.copy_(bt_h, non_blocking=True)
-                eng.step(tok_d, sl, bt_d, st["kv"], logits, stream=stream)
-                out_h.copy_(logits, non_blocking=True)
-            e1.record(stream)
-        stream.synchronize()
-        e2e_ms, e2e_value = replica_value(e0.elapsed_time(e1) / args.steps, B, "cuda")
-        e2e = {"value": e2e_value, "unit": "tok/s",
-               "h2d_bytes_per_step": int(tok_h.numel() * 4 + bt_h.numel() * 4),
-               "d2h_bytes_per_step": int(out_h.numel() * 4), "ms_per_step": e2e_ms,
-               "note": "token ids and block tables copied from pinned host memory, logits copied back, every step"}
-        eng.check()
-
-    # ---- roofline of the (single) step kernel
-    union = None
-    if B > 1:
-        union = [len(set(eng.debug_read("route_ids", l).ravel().tolist())) for l in range(m["layers"])]
-    by = R.step_bytes(m, st["lens"], expert_union=union, router_bias=st["bias"] is not None)
-    peak, peak_kind = measured_peaks()
-    achieved = by["total"] / (ms_mean / 1e3) / 1e9
-    sol = R.sol_tokens_per_s(by["total"], peak * 1e9, B)
-    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
-            "traffic": None, "algorithmic_bytes_per_step": by["total"], "bytes_breakdown": by,
-            "sol_tok_s": sol, "frac_of_nominal_8tbs": achieved / 8000.0,
-            "kernel": "mk::step_kernel (one launch per step; events also cover the 1 small per-step H2D copy)"}
-    traffic_file = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(traffic_file):
-        try:
-            tr = json.load(open(traffic_file)).get(wl.name)
-            if tr and tr.get("kernel_source_hash") == _kernel_hash():
-                roof["traffic"] = tr["bytes_per_step"]
-        except Exception:
-            pass
-
+    ms_mean, ms_med, value, cs, e2e, wall = measure(eng, st, args.steps, args.warmup, local, world,
+                                                    not args.no_e2e)
+    roof = roofline_of(eng, st, wl.name, ms_mean)
+    eng.close()
     cb = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb = cpu_baseline(st, args.cpu_sample_s)
 
+    # the other 30B workloads of the metric, measured in the same run on the same weights
+    others = {}
+    names = []
+    if wl.model is W.MOE30B and args.configs != "none":
+        names = list(OTHER_30B) if args.configs == "all" else [n for n in args.configs.split(",") if n]
+        names = [n for n in names if n != wl.name]
+    base_w = st["w"]
+    del st
+    torch.cuda.empty_cache()
+    for name in names:
+        wlx = W.get(name)
+        stx = setup_workload(wlx, args.layers, "cuda", weights=base_w)
+        engx = mk.Engine(stx["model"], stx["w"], stx["ps"], stx["num_pages"], max(stx["B"], 1), stx["max_pages"])
+        # a few seconds of timed work per workload (at least 5 steps), after the same warm-up
+        t0 = time.perf_counter()
+        engx.step(stx["tokens"].cuda(), np.array(stx["lens"], np.int32), stx["bt"].cuda(), stx["kv"])
+        torch.cuda.synchronize()
+        est_ms = (time.perf_counter() - t0) * 1e3
+        steps_x = max(5, min(args.steps, int(3000.0 / max(est_ms, 1e-3))))
+        msx, medx, valx, csx, e2ex, wallx = measure(engx, stx, steps_x, args.warmup, local, world, not args.no_e2e)
+        entry = {"value": valx, "unit": "tok/s", "ms_per_step": msx, "ms_per_step_median": medx, "steps": steps_x,
+                 "batch": stx["B"], "context": int(max(stx["lens"]) - 1) if stx["B"] == 1 else "ragged 512-32768",
+                 "page_size": stx["ps"], "roofline": roofline_of(engx, stx, name, msx),
+                 "clocks": {"sm_mhz": csx["sm_mhz"], "sm_max_mhz": csx["sm_max_mhz"], "reasons": csx["reasons"],
+                            "samples": csx["samples"]},
+                 "gpu_launches": steps_x, "wall_s_timed": wallx}
+        if wlx.zipf:
+            entry["router_prior"] = f"Zipf({wlx.zipf}) router bias"
+        if e2ex:
+            entry["e2e"] = e2ex
+        engx.close()
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            entry["cpu_baseline"] = cpu_baseline(stx, min(4.0, args.cpu_sample_s))
+        others[name] = entry
+        del stx, engx
+        torch.cuda.empty_cache()
+
     if rank == 0:
-        cs = clocks.summary()
         line = {"metric": "decode tok/s at bs=1 and bs=64; % of HBM SoL (active weights+KV bytes/step)",
                 "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": ms_mean, "ms_per_step_median": ms_med, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16", "accumulate": "f32",
                 "data": "synthetic (seeded random-init bf16 weights ~N(0,0.02), KV ~N(0,1))",
-                "config": {"workload": wl.name, "batch": B, "context": int(max(st["lens"]) - 1),
-                           "page_size": st["ps"], "layers": m["layers"], "hidden": m["hidden"],
+                "config": {"workload": wl.name, "batch": B, "context": int(max(wl.lengths) - 1),
+                           "page_size": wl.page_size, "layers": m["layers"], "hidden": m["hidden"],
                            "experts": f"{m['n_exp']} top-{m['top_k']}", "parallelism": f"replicas x{world}",
-                           "l2": "inputs larger than L2 (%.1f GB read per step), no flush" % (by["total"] / 1e9)},
+                           "l2": "inputs larger than L2 (%.1f GB read per step), no flush"
+                                 % (roof["algorithmic_bytes_per_step"] / 1e9)},
                 "roofline": roof, "clocks": {"sm_mhz": cs["sm_mhz"], "sm_max_mhz": cs["sm_max_mhz"],
                                              "reasons": cs["reasons"], "samples": cs["samples"]},
                 "gpu_launches": args.steps, "wall_s_timed": wall}
@@ -348,8 +438,9 @@ def main():
             line["e2e"] = e2e
         if cb:
             line["cpu_baseline"] = cb
+        if others:
+            line["configs"] = others
         print(json.dumps(line))
-    eng.close()
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0

@@ -200,8 +200,12 @@ void mk_destroy(mk_ctx* ctx);
  *   kv_layer:     device bf16 pages of ONE layer: [num_pages][2 (K,V)][num_kv_heads][page_size][head_dim]
  *   out:          device fp32 [batch][num_q_heads*head_dim]
  *   status_out:   device int32 [1] or NULL; receives MK_OK, or MK_ERR_DEVICE_BOUNDS if a
- *                 block-table entry was outside 0..num_pages-1 (such pages are skipped)
- * Limits: batch <= 64, head_dim 64 or 128, at most 8 query heads per KV head.
+ *                 block-table entry was outside 0..num_pages-1.  Such pages are skipped (never
+ *                 read): the row attends over its other positions, and a row none of whose
+ *                 pages is in range gets zeros in out.  status_out is the only report of a bad
+ *                 entry; with status_out NULL the call still returns MK_OK.
+ * Limits: batch <= 64, head_dim 64 or 128, at most 8 query heads per KV head,
+ * max_pages_per_seq*page_size <= 2^30 (MK_ERR_UNSUPPORTED beyond).
  * Its only scratch is one fixed 4 MiB __device__ array inside the library,
  * which every GPU that loads the library keeps until the process exits:
  * batch * num_kv_heads * (num_q_heads/num_kv_heads) * (head_dim+2) * 4 bytes

@@ -22,7 +22,10 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _ROOT = os.path.dirname(_HERE)
 _CSRC = os.path.join(_HERE, "csrc")
 _INC = os.path.join(_ROOT, "include")
-_BUILD = os.path.join(_HERE, "_build")
+# MK_TRACE=1 in the environment selects a separate build that records the per-tile timeline
+# (mk_debug_trace); the default build compiles that instrumentation out of the step kernel.
+TRACE = os.environ.get("MK_TRACE", "0") == "1"
+_BUILD = os.path.join(_HERE, "_build_trace" if TRACE else "_build")
 LIB_PATH = os.path.join(_BUILD, "libmk.so")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
@@ -60,10 +63,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
         src = os.path.join(_CSRC, f)
         if f.endswith(".cu"):
             cmds.append([nvcc, ARCH, "-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", _INC, "-I", _CSRC,
-                         "-c", src, "-o", obj] + (["-Xptxas", "-v"] if verbose else []))
+                         "-DMK_TRACE=%d" % TRACE, "-c", src, "-o", obj] + (["-Xptxas", "-v"] if verbose else []))
         else:
             cmds.append(["g++", "-O2", "-std=c++17", "-fPIC", "-Wall", "-I", _INC, "-I", _CSRC, "-I",
-                         os.path.join(cuda, "include"), "-c", src, "-o", obj])
+                         os.path.join(cuda, "include"), "-DMK_TRACE=%d" % TRACE, "-c", src, "-o", obj])
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -388,7 +391,7 @@ class Engine:
         return out
 
     def trace(self, enable: bool = True, events_per_cta: int = 2048):
-        """Record the timeline of the following steps (see ``trace.summarize``)."""
+        """Record the timeline of the following steps (a library built with MK_TRACE=1 only)."""
         self._trace_cap = events_per_cta if enable else 0
         _check(lib().mk_debug_trace(self.ctx, 1 if enable else 0, events_per_cta))
 

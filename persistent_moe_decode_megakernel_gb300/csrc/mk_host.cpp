@@ -730,6 +730,7 @@ int mk_debug_read(mk_ctx* c, int32_t what, int32_t layer, void* dst, size_t byte
 int mk_debug_trace(mk_ctx* c, int32_t enable, int32_t events_per_cta) {
   g_err.clear();
   if (!c) return fail(MK_ERR_INVALID_ARG, "ctx is NULL");
+  if (!mk::kTrace && enable) return fail(MK_ERR_UNSUPPORTED, "the timeline is compiled out of this build (MK_TRACE=0)");
   cudaError_t e;
   if (c->stepped && (e = cudaEventSynchronize(c->ev_done)) != cudaSuccess) return cuda_fail(e, "step");
   cudaFree(c->trace);

@@ -302,6 +302,10 @@ struct FastDiv {
   __device__ __forceinline__ int div(int n) const { return static_cast<int>((static_cast<uint64_t>(n) * m) >> 32); }
 };
 
+// The per-tile timeline (mk_debug_trace) exists only in builds with MK_TRACE=1; elsewhere every
+// trace write folds away at compile time.
+__device__ __forceinline__ bool tr_on(const Params& p) { return kTrace && p.trace != nullptr; }
+
 // --------------------------------------------------------------------------- shared memory
 enum : uint8_t { R_EMBED = 1, R_GEMV = 2, R_ATTN = 3, R_GU = 4, R_DOWN = 5, R_END = 6, R_ROUTE = 7,
                  R_DT = 9, R_RED = 10 };   // small-batch MoE: transposed down rows; partial-sum reduction
@@ -585,7 +589,7 @@ struct Producer {
   }
   __device__ Meta& meta() {
     Meta& m = S.meta[c % kSlots];
-    if (p.trace) {
+    if (tr_on(p)) {
       const uint64_t t = globaltimer();
       m.pad[0] = static_cast<uint32_t>(t);
       m.pad[1] = static_cast<uint32_t>(t >> 32);
@@ -699,7 +703,7 @@ struct Producer {
   __device__ bool moe_tasks(const mk_task& t) {
     const int l = t.layer;
     if (!moe_control(R_ROUTE, l, 0u, 0u)) return false;
-    const uint64_t t0 = p.trace ? globaltimer() : 0;
+    const uint64_t t0 = tr_on(p) ? globaltimer() : 0;
     {
       const uint64_t tw = globaltimer();
       for (uint32_t it = 1; !mbar_try_wait(&S.route_bar, rphase); ++it) {
@@ -713,7 +717,7 @@ struct Producer {
       }
       rphase ^= 1u;
     }
-    if (p.trace && pev < static_cast<uint32_t>(p.trace_cap) / 2) {
+    if (tr_on(p) && pev < static_cast<uint32_t>(p.trace_cap) / 2) {
       uint64_t* e = p.trace + (static_cast<size_t>(blockIdx.x) * p.trace_cap + p.trace_cap - 1 - pev) * 4;
       e[0] = t0;
       e[1] = globaltimer();
@@ -882,7 +886,7 @@ struct Producer {
       if (!ok) break;
     }
     S.prod_count = c;
-    if (p.trace) p.trace[static_cast<size_t>(blockIdx.x) * p.trace_cap * 4 + 2] = pev;
+    if (tr_on(p)) p.trace[static_cast<size_t>(blockIdx.x) * p.trace_cap * 4 + 2] = pev;
   }
 };
 
@@ -1026,7 +1030,7 @@ struct Consumer {
   __device__ Consumer(const Params& p_, Smem& S_) : p(p_), S(S_) {}
 
   __device__ void trace_event(uint32_t kind, const Meta& m, uint64_t t0) {
-    if (p.trace == nullptr || threadIdx.x != 0) return;
+    if (!tr_on(p) || threadIdx.x != 0) return;
     if (nev < static_cast<uint32_t>(p.trace_cap) / 2) {
       uint64_t* e = p.trace + (static_cast<size_t>(blockIdx.x) * p.trace_cap + nev) * 4;
       e[0] = t0;
@@ -1041,7 +1045,7 @@ struct Consumer {
 
   // a timestamped point inside a tile (tracing only)
   __device__ void trace_mark(uint32_t id, int layer, uint32_t val = 0) {
-    if (p.trace == nullptr || threadIdx.x != 0) return;
+    if (!tr_on(p) || threadIdx.x != 0) return;
     if (nev < static_cast<uint32_t>(p.trace_cap) / 2) {
       const uint64_t t = globaltimer();
       uint64_t* ev = p.trace + (static_cast<size_t>(blockIdx.x) * p.trace_cap + nev) * 4;
@@ -1058,10 +1062,10 @@ struct Consumer {
   // chunk timeline (tracing only): issue time, when warp 0 saw the data, when it released the slot
   uint64_t tchunk = 0;
   __device__ void trace_chunk_seen() {
-    if (p.trace && threadIdx.x == 0) tchunk = globaltimer();
+    if (tr_on(p) && threadIdx.x == 0) tchunk = globaltimer();
   }
   __device__ void trace_chunk_done() {
-    if (p.trace == nullptr || threadIdx.x != 0) return;
+    if (!tr_on(p) || threadIdx.x != 0) return;
     if (nev < static_cast<uint32_t>(p.trace_cap) / 2) {
       const Meta& m = meta();
       uint64_t* ev = p.trace + (static_cast<size_t>(blockIdx.x) * p.trace_cap + nev) * 4;
@@ -2535,7 +2539,7 @@ struct Consumer {
       trace_chunk_seen();
       if (!cbar_and(ok)) break;   // every warp starts a tile together
       const Meta m0 = meta();
-      const uint64_t t0 = p.trace ? globaltimer() : 0;
+      const uint64_t t0 = tr_on(p) ? globaltimer() : 0;
       twait = 0;
       wok = true;
       switch (m0.kind) {
@@ -2569,7 +2573,7 @@ struct Consumer {
       if (m0.kind == R_END) break;
     }
     if ((threadIdx.x & 31) == 0) atomicMin(&S.cons_count, c);
-    if (threadIdx.x == 0 && p.trace) {
+    if (threadIdx.x == 0 && tr_on(p)) {
       uint64_t* h = p.trace + static_cast<size_t>(blockIdx.x) * p.trace_cap * 4;
       h[0] = nev;
     }
@@ -2593,7 +2597,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     S.prod_count = 0;
     S.cons_count = 0xffffffffu;
     S.ykey = -1;
-    if (p.trace) p.trace[static_cast<size_t>(blockIdx.x) * p.trace_cap * 4 + 1] = globaltimer();
+    if (tr_on(p)) p.trace[static_cast<size_t>(blockIdx.x) * p.trace_cap * 4 + 1] = globaltimer();
     fence_mbar_init();
   }
   __syncthreads();

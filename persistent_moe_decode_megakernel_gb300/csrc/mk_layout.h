@@ -15,7 +15,15 @@
 #define MK_HD inline
 #endif
 
+// Builds with MK_TRACE=1 record the per-tile timeline of mk_debug_trace; the default build
+// compiles it out of the step kernel.
+#ifndef MK_TRACE
+#define MK_TRACE 0
+#endif
+
 namespace mk {
+
+constexpr bool kTrace = MK_TRACE != 0;
 
 // ---- thread block shape: two consumer warpgroups + one producer warpgroup -------
 // (one producer thread issues the copies; the producer warpgroup hands most of its

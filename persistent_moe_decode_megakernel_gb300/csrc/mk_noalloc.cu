@@ -168,7 +168,9 @@ __global__ void __launch_bounds__(kBlock) merge_kernel(int Hq, int Hkv, int nran
       L += f * pr[D + 1];
       acc = fmaf(f, pr[d], acc);
     }
-    out[(static_cast<size_t>(b) * Hq + kvh * G + h) * D + d] = acc / L;
+    // a row none of whose pages was in range has no positions (L == 0): it gets zeros, and the
+    // bounds error in the scratch's error word is its only report
+    out[(static_cast<size_t>(b) * Hq + kvh * G + h) * D + d] = L > 0.f ? acc / L : 0.f;
   }
   if (status_out != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
     *status_out = *reinterpret_cast<const int*>(scratch);
@@ -214,6 +216,8 @@ extern "C" int mk_paged_attention_noalloc(int32_t batch, int32_t num_q_heads, in
   RowLens lens;
   int max_npg = 0;
   const int64_t max_len = static_cast<int64_t>(max_pages_per_seq) * page_size;
+  // positions and page offsets are 32-bit on the device
+  if (max_len > (int64_t(1) << 30)) return fail(MK_ERR_UNSUPPORTED, "max_pages_per_seq*page_size above 2^30");
   for (int b = 0; b < batch; ++b) {
     if (seq_lens[b] < 1 || seq_lens[b] > max_len) return fail(MK_ERR_INVALID_ARG, "a seq_len is outside 1..max_pages_per_seq*page_size");
     lens.len[b] = seq_lens[b];

@@ -52,6 +52,34 @@ def route_mismatches(gpu_ids, orc_ids, orc_logits, K):
     return bad, ties
 
 
+def own_topk_mismatches(ids, logits, K):
+    """Rows whose routing ids are not exactly the top-k of the same implementation's own router
+    logits: the k largest logits in descending order (softmax is monotone, so this is descending
+    probability), equal logits taken lower expert index first.  Returns the row indices."""
+    bad = []
+    for b in range(ids.shape[0]):
+        want = np.argsort(-np.asarray(logits[b], dtype=np.float32), kind="stable")[:K]
+        if not np.array_equal(np.asarray(ids[b]), want):
+            bad.append(b)
+    return bad
+
+
+def check_rows(got, ref, tol=None, margin=None):
+    """Per-row logits check: relative L2 of every row within ``tol``, and the same argmax
+    wherever the oracle's top-1/top-2 margin exceeds ``margin``.  Returns the rows' errors."""
+    from tests.helpers import rel_l2, top2_margin
+    tol = TOL_LOGITS if tol is None else tol
+    margin = MARGIN if margin is None else margin
+    errs = []
+    for b in range(ref.shape[0]):
+        e = rel_l2(got[b], ref[b])
+        assert e <= tol, ("row", b, e)
+        if top2_margin(ref[b]) > margin:
+            assert int(np.argmax(got[b])) == int(np.argmax(ref[b])), ("argmax", b)
+        errs.append(e)
+    return errs
+
+
 class DeviceFetch:
     """Weights and KV of a torch-resident model (any device), copied to host arrays on
     demand (only the layer being computed and only the experts the oracle routed to).

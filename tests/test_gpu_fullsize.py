@@ -4,11 +4,13 @@ tokens; one cooperative launch per step over every SM).
 
 The oracle runs layer by layer on the host, fetching only the layer in hand,
 the experts it routed to and the KV pages of the rows it checks.  At batch 64
-it checks a sample of rows (rows are independent in a decode step).
+it checks every row.
 
 A routing difference is allowed only at an exact router tie (oracle gap at the
 k-th place <= 1e-4*max(1,|r|)); a row that takes such a tie is no longer
-comparable downstream and is counted, not compared."""
+comparable downstream and is counted, not compared.  Independently of the oracle,
+every row's routing must be exactly the top-k of the GPU's own router logits in
+every layer (ties to the lower expert index, slots by descending logit)."""
 import numpy as np
 import pytest
 import torch
@@ -16,7 +18,7 @@ import torch
 import workloads as W
 import persistent_moe_decode_megakernel_gb300 as mk
 from oracle import Oracle, make_dims
-from tests.gpu_common import MARGIN, TOL_LOGITS, DeviceFetch, route_mismatches
+from tests.gpu_common import MARGIN, TOL_LOGITS, DeviceFetch, own_topk_mismatches, route_mismatches
 from tests.helpers import rel_l2, top2_margin
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
@@ -56,6 +58,9 @@ def _run(wl_name, w_dev, rows=None, bias=None):
     eng.check()
     got = logits.cpu().numpy()[rows]
     gpu_ids = [eng.debug_read("route_ids", l)[rows] for l in range(m["layers"])]
+    for l in range(m["layers"]):
+        bad_own = own_topk_mismatches(eng.debug_read("route_ids", l), eng.debug_read("router", l), m["top_k"])
+        assert not bad_own, (wl_name, l, bad_own)
     eng.close()
     del kv
     torch.cuda.empty_cache()
@@ -77,7 +82,8 @@ def _run(wl_name, w_dev, rows=None, bias=None):
         if top2_margin(ref[i]) > MARGIN:
             assert int(np.argmax(got[i])) == int(np.argmax(ref[i]))
         compared += 1
-    print(f"{wl_name}: rows compared {compared}, rows that took a router tie {tie_rows}")
+    print(f"{wl_name}: rows compared {compared} of {len(rows)}, rows that took an exact router tie "
+          f"{len(tie_rows)} {tie_rows}")
     assert compared >= max(1, len(rows) - 1)
     return got, ref
 
@@ -91,9 +97,11 @@ def test_30b_long_context(weights30b, name):
     _run(name, weights30b["plain"])
 
 
-def test_30b_bs64_ragged_zipf_sampled_rows(weights30b):
+def test_30b_bs64_ragged_zipf_all_rows(weights30b):
+    # every row: the wide-batch path serves the batch in register groups and 16-row tensor-core
+    # chunks, so each position in a group and a chunk is compared
     wl = W.get("moe30b_bs64_ragged")
     bias = W.zipf_router_bias(wl.model, wl.zipf).cuda()
     w = dict(weights30b["plain"])
     w["layers"] = [dict(lw, router_bias=bias[l].contiguous()) for l, lw in enumerate(w["layers"])]
-    _run("moe30b_bs64_ragged", w, rows=[0, 21, 42, 63])
+    _run("moe30b_bs64_ragged", w)

@@ -14,8 +14,8 @@ import torch
 import workloads as W
 import persistent_moe_decode_megakernel_gb300 as mk
 from oracle import Oracle, make_dims
-from tests.gpu_common import (MARGIN, MEDIUM, TOL_LOGITS, engine_for, gpu_step, kv_to_device, route_mismatches,
-                              to_device)
+from tests.gpu_common import (MARGIN, MEDIUM, TOL_LOGITS, check_rows, engine_for, gpu_step, kv_to_device,
+                              own_topk_mismatches, route_mismatches, to_device)
 from tests.helpers import rel_l2, tiny_setup, top2_margin
 
 pytestmark = pytest.mark.gpu
@@ -34,11 +34,13 @@ def _parity_one_step(setup, max_batch=8, check_layers=True, flags=0):
     got = gpu_step(eng, setup["tokens"], setup["seq_lens"], setup["bt"], kv_dev)
     kv_ref = setup["kv"].copy()
     ref = orc.decode_step(setup["dims"], setup["wn"], setup["tokens"], setup["seq_lens"], setup["bt"], kv_ref)
-    err = rel_l2(got, ref)
-    assert err <= TOL_LOGITS, err
-    for b in range(got.shape[0]):
-        if top2_margin(ref[b]) > MARGIN:
-            assert int(np.argmax(got[b])) == int(np.argmax(ref[b]))
+    check_rows(got, ref)    # every row within the bar, and the argmax where the oracle's margin is clear
+    m = setup["model"]
+    n_ties = 0
+    for l in range(m["layers"]):
+        # the routing of every row is exactly the top-k of the GPU's own router logits
+        ids = eng.debug_read("route_ids", l)
+        assert not own_topk_mismatches(ids, eng.debug_read("router", l), m["top_k"]), l
     if check_layers:
         # per-op check, layer by layer, each layer fed the GPU's own input so errors do not compound.
         # Attention reads the cache the GPU left (the prefix plus the k and v codes it appended; those
@@ -59,6 +61,7 @@ def _parity_one_step(setup, max_batch=8, check_layers=True, flags=0):
             ids = eng.debug_read("route_ids", l)
             bad, ties = route_mismatches(ids, tr["ids"], tr["router_logits"], m["top_k"])
             assert not bad, bad
+            n_ties += len(ties)
             if not ties:
                 assert np.array_equal(ids, tr["ids"])
                 assert np.allclose(eng.debug_read("route_w", l), tr["w"], rtol=1e-5, atol=1e-7)
@@ -74,6 +77,7 @@ def _parity_one_step(setup, max_batch=8, check_layers=True, flags=0):
     assert changed.any()
     rms = np.sqrt(np.mean(r * r))
     assert np.all(np.abs(g - r) <= 2.0 ** -7 * np.maximum(np.abs(r), np.abs(g)) + 1e-4 * rms)
+    print(f"rows {got.shape[0]}: routing differences at exact router ties: {n_ties}")
     eng.close()
     return got, ref
 
@@ -219,7 +223,8 @@ def test_tiny_bs8_ragged_continuous_batching():
         assert np.array_equal(lens_now, seq)
         got = gpu_step(eng, tokens, seq, bt, kv_dev)
         ref = orc.decode_step(s["dims"], s["wn"], tokens, seq, bt, kv_ref)
-        assert rel_l2(got, ref) <= TOL_LOGITS, (step, rel_l2(got, ref))
+        for b in range(B):
+            assert rel_l2(got[b], ref[b]) <= TOL_LOGITS, (step, b, rel_l2(got[b], ref[b]))
         for b in range(B):
             if top2_margin(ref[b]) > MARGIN:
                 assert int(np.argmax(got[b])) == int(np.argmax(ref[b])), (step, b)
