@@ -2,37 +2,46 @@
 //
 // One thread block per SM stays resident for the whole step ("Inside the
 // megakernel serving engine for North Mini Code", section "What is a
-// Megakernel?").  Each block walks its own host-built task list; dependencies
-// between tiles are counters in global memory that a finished tile increments
-// (release) and a consumer spins on (acquire), bounded by a watchdog.
+// Megakernel?").  Each block walks its own host-built task list.  A task waits
+// for the tiles that produce what it reads, not for a whole phase: every value
+// one block hands to another is an 8-byte tagged word -- the fp32 or int32 value and this step's
+// tag, written with one relaxed store -- and the reader polls the words it
+// needs until they carry the step's tag.  No counter, fence or barrier sits
+// between blocks; every wait is bounded by a %globaltimer watchdog that records
+// an error and ends the step.
 //
-// Block layout: 8 consumer warps + 1 producer warp.  The producer streams the
-// operand each tile reads from HBM -- weight rows, KV pages -- into a ring of
-// shared-memory slots with 1-D bulk async copies (cp.async.bulk, completion on
-// an mbarrier, L2 evict-first).  Weights never depend on activations and the
-// cached KV never depends on this step, so the producer runs ahead across
-// every dependency wait: while consumers wait for the previous phase, the ring
-// fills with the next phase's operands.  The only producer-side wait is on
-// routing, because expert weights are chosen by it.
+// Block layout: two consumer warpgroups and one producer warpgroup.  One
+// producer thread streams the operand each tile reads from HBM -- weight rows
+// with 1-D bulk copies, KV pages with 2-D TMA boxes (128-byte swizzle) -- into a
+// two-slot shared-memory ring (completion on mbarriers, L2 evict-first).
+// Weights never depend on activations and the cached KV never depends on this
+// step, so the producer runs ahead across every data wait; its only wait is for
+// the layer's routing, because expert weights are chosen by it.  The producer
+// warpgroup hands its registers to the consumers (setmaxnreg).
 //
-// Consumers do the arithmetic on CUDA cores in fp32: GEMV rows against the
-// input vector held in registers (RMSNorm fused into the load), paged GQA
-// attention with an online softmax per split, SwiGLU, and the combines.
+// Consumers: GEMV rows on CUDA cores in fp32 at batches of 1-2 rows (RMSNorm
+// fused into the staging of the input), mma.sync tensor-core tiles for wider
+// batches; paged GQA attention on mma.sync tiles with an online softmax.
 //
-// Work kinds (task list entries, see mk_debug.h):
-//   EMBED   residual stream <- embedding rows (a column range)
-//   QKV     RMSNorm + fused QKV rows                          wait: layer input complete
-//   ATTN    this block's split items of the step's plan        wait: all QKV tiles
-//           last split of a (row, KV head) merges the splits -> attention output
-//   OPROJ   O-proj rows + residual                             wait: all (row, KV head) pairs merged
-//   ROUTER  RMSNorm + router rows; the last router tile routes: top-k, weights,
-//           per-expert row lists, active-expert list -> publishes the MoE queue
-//   MOE     drain the MoE queue (shared by all blocks, claimed with atomics):
-//           gate/up items (expert, 16 FFN rows)  then  down items (expert, 64
-//           hidden rows); the last down item of a row tile adds the k slots
-//           into the residual in rank order
-//   HEAD    final RMSNorm + LM-head rows
-// The last block to finish resets every counter for the next step.
+// Work kinds (task list entries, see mk_debug.h), per layer:
+//   QKV     RMSNorm + fused QKV rows               reads the layer input (all rows)
+//   ATTN    this block's split items of the step's attention plan: RoPE, the KV
+//           append (split 0), partial (max, sum, output) per split
+//                                                  reads q, k, v of its (row, KV head)
+//           then the block merges a slice of the outputs of every pair it holds a
+//           split of, over all that pair's splits   reads their partials
+//   OPROJ   O-proj rows + residual                 reads the attention output (all)
+//   ROUTER  RMSNorm + router rows (a few experts)  reads x after attention (all)
+//   MOE     every block routes the batch itself from the router logits (softmax,
+//           top-k, weights, active experts, a cost-balanced split of the gate/up
+//           units over the blocks) and hands the result to its producer; then
+//           small batches: the block's gate/up units and the same FFN rows of the
+//             transposed down projection, an on-chip [B][H] partial, published and
+//             summed per hidden row by the row's owner block  reads every block's partial
+//           wider batches: gate/up units -> SwiGLU outputs; down projection by
+//             hidden rows of every active expert      reads every unit's SwiGLU outputs
+//   HEAD    final RMSNorm + LM-head rows           reads the last layer's output (all)
+// The last block to finish clears the step's flags (abort, finish count).
 
 #pragma once
 
@@ -440,9 +449,11 @@ __device__ __noinline__ bool ll_expired(const Params& p, uint64_t t0) {
 template <class Addr>
 __device__ __forceinline__ bool ll_gather(const Params& p, int n, Addr addr, float* dst, uint32_t tag) {
   constexpr int kB = 8;
+  #pragma unroll 1
   for (int base = threadIdx.x; base < n; base += kB * kConsumerThreads) {
     uint32_t want = (1u << kB) - 1u;   // words of this batch not yet seen with the step's tag
     uint64_t t0 = 0;
+    #pragma unroll 1
     for (uint32_t it = 0;; ++it) {
       uint64_t x[kB];
 #pragma unroll
@@ -479,6 +490,7 @@ __device__ bool warp_wait_record(const Params& p, Smem& S, uint32_t c) {
   bool ok = mbar_try_wait(&S.full[s], ph);
   if (!ok) {
     const uint64_t t0 = globaltimer();
+    #pragma unroll 1
     for (uint32_t it = 1;; ++it) {
       if (mbar_try_wait(&S.full[s], ph)) { ok = true; break; }
       if ((it & 63u) == 0u) {
@@ -552,9 +564,11 @@ struct Producer {
         const int cta = blockIdx.x;
         const uint32_t blk = static_cast<uint32_t>(p.ps) * p.D * 2u;   // one page of K (or V) of one KV head
         uint32_t done = 0;
+        #pragma unroll 1
         for (int it = p.item_off[cta]; it < p.item_off[cta + 1] && done < kPrefetchBytes; ++it) {
           const mk_attn_item item = p.items[it];
           const int32_t* btrow = p.block_tables + static_cast<size_t>(item.b) * p.maxpg;
+          #pragma unroll 1
           for (uint32_t pg = item.page_lo; pg < item.page_hi && done < kPrefetchBytes; ++pg) {
             const int32_t page = btrow[pg];
             if (page < 0 || page >= p.P) continue;
@@ -576,6 +590,7 @@ struct Producer {
     const uint32_t ph = ((c / kSlots) & 1u) ^ 1u;
     if (mbar_try_wait(&S.empty[s], ph)) return true;
     const uint64_t t0 = globaltimer();
+    #pragma unroll 1
     for (uint32_t it = 1;; ++it) {
       if (mbar_try_wait(&S.empty[s], ph)) return true;
       if ((it & 63u) == 0u) {
@@ -628,7 +643,9 @@ struct Producer {
     // per tile; the repeated reads of the tile come from L2 (evict-normal while it is reused).
     const int ng = p.B > 2 ? (p.B + wide_group_rows(K) - 1) / wide_group_rows(K) : 1;
     const uint64_t pl = ng > 1 ? pol_reuse : pol;
+    #pragma unroll 1
     for (int g = 0; g < ng; ++g) {
+      #pragma unroll 1
       for (uint32_t r0 = t.lo; r0 < t.hi; r0 += rpc) {
         const uint32_t n = min(static_cast<uint32_t>(rpc), t.hi - r0);
         if (!acquire()) return false;
@@ -657,9 +674,11 @@ struct Producer {
     const int rows_cap = (kSlotBytes / 2) / (p.D * 2);
     const int halves = p.D / 64;
     const uint32_t box = static_cast<uint32_t>(p.ps) * 128u;
+    #pragma unroll 1
     for (int it = p.item_off[cta]; it < p.item_off[cta + 1]; ++it) {
       const mk_attn_item item = p.items[it];
       const int32_t* btrow = p.block_tables + static_cast<size_t>(item.b) * p.maxpg;
+      #pragma unroll 1
       for (uint32_t pg = item.page_lo; pg < item.page_hi; pg += ppc) {
         const uint32_t n = min(static_cast<uint32_t>(ppc), item.page_hi - pg);
         if (!acquire()) return false;
@@ -671,6 +690,7 @@ struct Producer {
         m.signal_ctr = t.signal_ctr; m.lo = item.page_lo; m.hi = item.page_hi;
         mbar_arrive_expect_tx(full(), 2u * halves * n * box);
         uint8_t* dst = slot();
+        #pragma unroll 1
         for (uint32_t i = 0; i < n; ++i) {
           int32_t page = btrow[pg + i];
           if (page < 0 || page >= p.P) {
@@ -680,6 +700,7 @@ struct Producer {
           }
           const int rowk = (((t.layer * p.P + page) * 2) * p.Hkv + item.kvh) * p.ps;
           const int rowv = rowk + p.Hkv * p.ps;
+          #pragma unroll 1
           for (int h = 0; h < halves; ++h) {
             uint8_t* kd = dst + h * rows_cap * 128 + i * box;
             tma_load_2d(kd, p.kv_map, 64 * h, rowk, full(), pol);
@@ -706,6 +727,7 @@ struct Producer {
     const uint64_t t0 = tr_on(p) ? globaltimer() : 0;
     {
       const uint64_t tw = globaltimer();
+      #pragma unroll 1
       for (uint32_t it = 1; !mbar_try_wait(&S.route_bar, rphase); ++it) {
         if ((it & 63u) == 0u) {
           if (aborted(p)) return false;
@@ -737,6 +759,7 @@ struct Producer {
     if (u0 >= u1) {
       if (!moe_control(R_GU, l, 0u, 1u)) return false;
     }
+    #pragma unroll 1
     for (int u = u0; u < u1;) {
       const int a = u / F, f0 = u - a * F;
       const int fend = min(F, u1 - a * F);
@@ -747,7 +770,9 @@ struct Producer {
       // or more) is streamed once per group (group in aux >> 1), so each group's input is
       // staged once per run; the repeated reads come from L2
       const int ng = p.B > 2 ? (S.ecnt[e] + wide_group_rows(H) - 1) / wide_group_rows(H) : 1;
+      #pragma unroll 1
       for (int g = 0; g < ng; ++g) {
+        #pragma unroll 1
         for (int f = f0; f < fend; f += fpc) {
           const int n = min(fpc, fend - f);
           if (!acquire()) return false;
@@ -775,9 +800,11 @@ struct Producer {
     if (r1 <= r0 || nact == 0) return moe_control(R_DOWN, l, r0, r1);
     const int rpc = min(static_cast<int>(r1 - r0), static_cast<int>(kSlotBytes / rowb));
     bool first = true;
+    #pragma unroll 1
     for (int rb = static_cast<int>(r0); rb < static_cast<int>(r1); rb += rpc) {
       const int nrc = min(rpc, static_cast<int>(r1) - rb);
       const int epc = max(1, min(255, static_cast<int>(kSlotBytes / (nrc * rowb))));
+      #pragma unroll 1
       for (int a = 0; a < nact; a += epc) {
         const int ne = min(epc, nact - a);
         if (!acquire()) return false;
@@ -790,6 +817,7 @@ struct Producer {
         m.lo = r0; m.hi = r1;
         const uint32_t bytes = static_cast<uint32_t>(nrc) * rowb;
         mbar_arrive_expect_tx(full(), static_cast<uint32_t>(ne) * bytes);
+        #pragma unroll 1
         for (int k = 0; k < ne; ++k) {
           const uint16_t* down = lw.w_down + (static_cast<size_t>(S.eact[a + k]) * H + rb) * F;
           bulk_g2s(slot() + k * bytes, down, bytes, full(), pol);
@@ -810,13 +838,16 @@ struct Producer {
     const LayerW& lw = p.layers[l];
     const int H = p.H, F = p.F;
     const int fpc = gemv_rows_per_chunk(H) / 2;   // 2 * fpc transposed down rows fill at most one slot
+    #pragma unroll 1
     for (int u = u0; u < u1;) {
       const int a = u / F, f0 = u - a * F;
       const int fend = min(F, u1 - a * F);
       const int e = S.eact[a];
       const uint16_t* gate = lw.w_gate_up + static_cast<size_t>(e) * 2 * F * H;
+      #pragma unroll 1
       for (int g0 = f0; g0 < fend; g0 += 2 * fpc) {
         const int gend = min(fend, g0 + 2 * fpc);
+        #pragma unroll 1
         for (int f = g0; f < gend; f += fpc) {
           const int n = min(fpc, gend - f);
           if (!acquire()) return false;
@@ -868,6 +899,7 @@ struct Producer {
   __device__ void run() {
     const int cta = blockIdx.x;
     if (p.task_off[cta] < p.task_off[cta + 1]) prefetch_task(p.tasks[p.task_off[cta]]);
+    #pragma unroll 1
     for (int ti = p.task_off[cta]; ti < p.task_off[cta + 1]; ++ti) {
       const mk_task t = p.tasks[ti];
       bool ok = true;
@@ -993,6 +1025,7 @@ __device__ __noinline__ H8 load_h8(const Params& p, const uint64_t* src) {
   H8 r;
   r.ok = true;
   const uint64_t t0 = globaltimer();
+  #pragma unroll 1
   for (uint32_t it = 1;; ++it) {
     uint32_t st = 0;
 #pragma unroll
@@ -1101,6 +1134,7 @@ struct Consumer {
   __device__ __forceinline__ bool embed() {
     const Meta m = meta();
     const int H = p.H;
+    #pragma unroll 1
     for (int b = 0; b < p.B; ++b) {
       int tok = __ldg(p.tokens + b);
       if (tok < 0 || tok >= p.V) {
@@ -1111,6 +1145,7 @@ struct Consumer {
       }
       const uint16_t* row = p.embed + static_cast<size_t>(tok) * H;
       uint64_t* x = p.X + static_cast<size_t>(b) * H;
+      #pragma unroll 1
       for (uint32_t col = m.lo + threadIdx.x; col < m.hi; col += kConsumerThreads) ll_st(x + col, bf1(row[col]), p.tag);
     }
     return true;
@@ -1516,8 +1551,10 @@ struct Consumer {
           ok = group_bar_and(ok, sg.S);
           if (ok && sg.s == 0 && lane < nt) {
             int i = 0;
+            #pragma unroll 1
             for (int r = sg.rg; r < n; r += sg.RPG, ++i) {
               float v = 0.f, v2 = 0.f;
+              #pragma unroll 1
               for (int q = 0; q < sg.S; ++q) {
                 v += S.scr.seg[par][r][q][lane];
                 if (gu) v2 += S.scr.seg[par][kMaxRowsPerChunk / 2 + r][q][lane];
@@ -1564,9 +1601,11 @@ struct Consumer {
   // barrier separates the writes from these reads), into p.argp.
   __device__ __forceinline__ void head_top2(uint32_t lo, uint32_t hi) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    #pragma unroll 1
     for (int b = 0; b < p.B; ++b) {
       Top2 t{-INFINITY, -INFINITY, 0x7fffffff};
       const float* row = p.logits + static_cast<size_t>(b) * p.V;
+      #pragma unroll 1
       for (uint32_t r = lo + threadIdx.x; r < hi; r += kConsumerThreads) top2_add(t, row[r], static_cast<int>(r));
       top2_warp(t);
       if (lane == 0) {
@@ -1577,6 +1616,7 @@ struct Consumer {
       cbar();
       if (threadIdx.x == 0) {
         Top2 a{S.ssred[0][0], S.ssred[0][1], __float_as_int(S.ssred[0][2])};
+        #pragma unroll 1
         for (int w = 1; w < kConsumerWarps; ++w) {
           const Top2 o{S.ssred[w][0], S.ssred[w][1], __float_as_int(S.ssred[w][2])};
           top2_merge(a, o);
@@ -1605,6 +1645,7 @@ struct Consumer {
     const int part = gt & 7, slot = gt >> 3, nslot = gsz >> 3;
     const int e_lo = part * E / 8, e_hi = (part + 1) * E / 8;   // at most LEN values (E <= 8 * LEN)
     const int ncand = (E + nslot - 1) / nslot;
+    #pragma unroll 1
     for (int b0 = 0; b0 < B; b0 += G) {   // uniform trip counts: the shuffles below
       const int b = b0 + grp;
       const bool bon = b < B;
@@ -1612,6 +1653,7 @@ struct Consumer {
       float sl[LEN];
 #pragma unroll
       for (int k = 0; k < LEN; ++k) sl[k] = (e_lo + k < e_hi) ? row[e_lo + k] : -INFINITY;
+      #pragma unroll 1
       for (int j = 0; j < ncand; ++j) {
         const int e = slot + j * nslot;
         const bool on = bon && e < E;
@@ -1644,6 +1686,7 @@ struct Consumer {
   __device__ __forceinline__ void topk_rows_warp(const float* lg) {
     const int B = p.B, E = p.E, K = p.K;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    #pragma unroll 1
     for (int b = warp; b < B; b += kConsumerWarps) {
       float v[kMaxExperts / 32];
 #pragma unroll
@@ -1652,6 +1695,7 @@ struct Consumer {
         v[k] = e < E ? lg[b * E + e] : -INFINITY;
       }
       uint32_t taken = 0;   // this lane's values already chosen (bit k)
+      #pragma unroll 1
       for (int j = 0; j < K; ++j) {
         float bv = -INFINITY;
         int bi = 0x7fffffff;
@@ -1709,16 +1753,20 @@ struct Consumer {
       const uint64_t* rl = p.RLOG + static_cast<size_t>(l) * p.max_batch * E;
       ok = ll_gather(p, B * E, [=](int i) { return rl + i; }, lg, p.tag) && ok;
     }
+    #pragma unroll 1
     for (int e = threadIdx.x; e < E; e += kConsumerThreads) S.ecnt[e] = 0;
     if (!ok) ll_timeout(p, MK_OP_ROUTER, l);
     if (!cbar_and(ok)) return false;
     trace_mark(16, l);
     if (!p.norm_topk) {   // weights over all experts need each row's max and normaliser
+      #pragma unroll 1
       for (int b = warp; b < B; b += kConsumerWarps) {
         float mx = -INFINITY;
+        #pragma unroll 1
         for (int e = lane; e < E; e += 32) mx = fmaxf(mx, lg[b * E + e]);
         mx = warp_max(mx);
         float z = 0.f;
+        #pragma unroll 1
         for (int e = lane; e < E; e += 32) z += expf(lg[b * E + e] - mx);
         z = warp_sum(z);
         if (lane == 0) { S.rmax[b] = mx; S.rz[b] = z; }
@@ -1732,10 +1780,13 @@ struct Consumer {
     // small-batch MoE: the logits are consumed; the scratch becomes the [B][H] partial output
     // (and a row that is not routed to a unit's expert contributes zero to it)
     if (p.small_moe) {
+      #pragma unroll 1
       for (int i = threadIdx.x; i < B * H; i += kConsumerThreads) S.moe[i] = 0.f;
+      #pragma unroll 1
       for (int i = threadIdx.x; i < B * kMaxUnits; i += kConsumerThreads) S.hsm[i] = 0.f;
     }
     // combine weights (a warp per row, a lane per slot) ...
+    #pragma unroll 1
     for (int b = warp; b < B; b += kConsumerWarps) {
       const int j = lane < K ? lane : 0;
       const float mx = p.norm_topk ? S.rval[b * K] : S.rmax[b];   // rank 0 holds the row's largest logit
@@ -1755,6 +1806,7 @@ struct Consumer {
     // ... while the last warp lists the active experts and their gate/up cost prefix
     if (warp == kConsumerWarps - 1) {
       int nact = 0;
+      #pragma unroll 1
       for (int e0 = 0; e0 < E; e0 += 32) {
         const int e = e0 + lane;
         const bool on = e < E && S.ecnt[e] > 0;
@@ -1811,6 +1863,7 @@ struct Consumer {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, n = p.B * p.K;
     if (warp == 0) {
       int cnt = 0;
+      #pragma unroll 1
       for (int i0 = 0; i0 < n; i0 += 32) {
         const int i = i0 + lane;
         const bool hit = i < n && S.rcache[i] == e;
@@ -1847,6 +1900,7 @@ struct Consumer {
   // routing slot of expert e in batch row b, or -1
   __device__ __forceinline__ int slot_of(int b, int e) const {
     int s = -1;
+    #pragma unroll 1
     for (int j = 0; j < p.K; ++j)
       if (S.rcache[b * p.K + j] == e) s = j;
     return s;
@@ -1867,6 +1921,7 @@ struct Consumer {
   __device__ int warp_expert_pairs(int e, int* wl) {
     const int lane = threadIdx.x & 31, n = p.B * p.K;
     int cnt = 0;
+    #pragma unroll 1
     for (int i0 = 0; i0 < n; i0 += 32) {
       const int i = i0 + lane;
       const bool hit = i < n && S.rcache[i] == e;
@@ -1977,6 +2032,7 @@ struct Consumer {
     bool ok = true;
     {
       // x_mid of the block's own rows (written by its O-proj tile), and the SwiGLU inputs
+      #pragma unroll 1
       for (int i = threadIdx.x; i < B * nrow; i += kConsumerThreads) {
         const int t = i / nrow, r = i - t * nrow;
         XM[i] = ll_f(ll_ld(p.X + (2 * static_cast<size_t>(l) + 1) * xs + static_cast<size_t>(t) * p.H + r0 + r));
@@ -2002,10 +2058,12 @@ struct Consumer {
           // warps; a warp fetches its pairs' SwiGLU inputs once and runs all of the expert's
           // rows in the chunk against them
           int gbase = 0;   // pair groups of the chunk's earlier experts
+          #pragma unroll 1
           for (int ai = 0; ai < ne; ++ai) {
             const int cnt = warp_expert_pairs(S.eact[a0 + ai], wl);
             const int ng = (cnt + TD - 1) / TD;
             const int i0 = ai * nrc, iend = i0 + nrc;
+            #pragma unroll 1
             for (int g = (warp + kConsumerWarps - gbase % kConsumerWarps) % kConsumerWarps; g < ng;
                  g += kConsumerWarps) {
               const int g0 = g * TD, nt = min(TD, cnt - g0);
@@ -2035,10 +2093,12 @@ struct Consumer {
       }
       const int R = ne * nrc;
       const int i1 = (warp + 1) * R / kConsumerWarps;
+      #pragma unroll 1
       for (int i = warp * R / kConsumerWarps; i < i1;) {
         const int ai = i / nrc;
         const int iend = min(i1, (ai + 1) * nrc);
         const int cnt = warp_expert_pairs(S.eact[a0 + ai], wl);
+        #pragma unroll 1
         for (int g0 = 0; g0 < cnt; g0 += TD) {
           const int nt = min(TD, cnt - g0);
           float y[8 / TD][8][TD];
@@ -2069,9 +2129,12 @@ struct Consumer {
     if (!cbar_and(wok && ok)) return false;
     trace_mark(42, l);
     // combine in slot order, residual
+    #pragma unroll 1
     for (int t = warp; t < B; t += kConsumerWarps) {
+      #pragma unroll 1
       for (int r = lane; r < nrow; r += 32) {
         float acc = 0.f;
+        #pragma unroll 1
         for (int j = 0; j < K; ++j) acc += P[(t * K + j) * nrow + r];
         ll_st(p.X + (2 * static_cast<size_t>(l) + 2) * xs + static_cast<size_t>(t) * p.H + r0 + r,
               XM[t * nrow + r] + acc, p.tag);
@@ -2145,6 +2208,7 @@ struct Consumer {
     trace_mark(40, l);
     {
       uint64_t* mine = p.PT + (static_cast<size_t>(l) * N + blockIdx.x) * kSmallMaxB * H;
+      #pragma unroll 1
       for (int i = threadIdx.x * 2; i < B * H; i += kConsumerThreads * 2) ll_st2(mine + i, S.moe[i], S.moe[i + 1], p.tag);
     }
     cbar();   // the partial output has been read out of the scratch
@@ -2168,11 +2232,13 @@ struct Consumer {
     if (!cbar_and(ok)) return false;
     trace_mark(42, l);
     const float* part = S.moe + ni;
+    #pragma unroll 1
     for (int k = 0; k * kConsumerWarps < ni; ++k) {   // warp-uniform trip count
       const int it = warp + k * kConsumerWarps;
       const int b = it < ni ? it / nrow : 0, rr = it - b * nrow;
       float v = 0.f;
       if (it < ni)
+        #pragma unroll 1
         for (int j = lane; j < N; j += 32) v += part[(b * N + j) * nrow + rr];
       v = warp_sum(v);
       if (it < ni && lane == 0)
@@ -2247,6 +2313,7 @@ struct Consumer {
       for (int k = 0; k < 11; ++k) stale |= static_cast<uint32_t>(((need >> k) & 1u) && !ll_ok(w[k], p.tag)) << k;
       if (stale != 0u) {   // re-poll the stale words, all of them per sweep
         const uint64_t t0 = globaltimer();
+        #pragma unroll 1
         for (uint32_t it = 1; stale != 0u; ++it) {
 #pragma unroll
           for (int k = 0; k < 11; ++k)
@@ -2294,6 +2361,7 @@ struct Consumer {
       if (page >= 0 && page < p.P) {
         const size_t kb = (((static_cast<size_t>(l) * p.P + page) * 2 * p.Hkv + kvh) * p.ps + sl) * D;
         const size_t vb = kb + static_cast<size_t>(p.Hkv) * p.ps * D;
+        #pragma unroll 1
         for (int d = threadIdx.x; d < D; d += kConsumerThreads) {
           p.kv[kb + d] = kvcur[d];
           p.kv[vb + d] = kvcur[D + d];
@@ -2321,6 +2389,7 @@ struct Consumer {
         if (pos >= p0 + r0 && pos < p0 + r0 + 16) {
           // this token's k and v are not in the copied page yet: put them in its rows
           const int rr = pos - p0;
+          #pragma unroll 1
           for (int cidx = lane; cidx < 2 * (D / 8); cidx += 32) {
             const int which = cidx / (D / 8), d = (cidx - which * (D / 8)) * 8;
             const uint4 v = *reinterpret_cast<const uint4*>(kvcur + which * D + d);
@@ -2332,6 +2401,7 @@ struct Consumer {
         }
         if (r0 + 16 > npos) {
           // rows past the sequence: zero them so that 0-probability rows cannot carry NaN into P V
+          #pragma unroll 1
           for (int cidx = lane; cidx < 16 * 2 * (D / 8); cidx += 32) {
             const int rr = r0 + cidx / (2 * (D / 8));
             const int rem = cidx % (2 * (D / 8));
@@ -2432,6 +2502,7 @@ struct Consumer {
     {
       uint64_t* po = p.PO + (static_cast<size_t>(l) * p.max_items + m0.idx) * (kMaxG * D);
       uint64_t* pml = p.PML + (static_cast<size_t>(l) * p.max_items + m0.idx) * (2 * kMaxG);
+      #pragma unroll 1
       for (int q4 = threadIdx.x; q4 * 4 < Gq * D; q4 += kConsumerThreads) {
         const int h = (q4 * 4) / D, d = q4 * 4 - h * D;
         float M = -INFINITY;
@@ -2470,6 +2541,7 @@ struct Consumer {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     twait = globaltimer();
     bool ok = true;
+    #pragma unroll 1
     for (int it = p.item_off[cta]; it < p.item_off[cta + 1]; ++it) {
       const mk_attn_item item = p.items[it];
       const int pair = item.b * p.Hkv + item.kvh;
@@ -2494,17 +2566,21 @@ struct Consumer {
       if (!ok) ll_timeout(p, MK_OP_ATTN, l);
       if (!cbar_and(ok)) return false;
       trace_mark(64, l);
+      #pragma unroll 1
       for (int h = warp; h < Gq; h += kConsumerWarps) {
         float M = -INFINITY;
+        #pragma unroll 1
         for (int sp = lane; sp < ns; sp += 32) M = fmaxf(M, ml[(sp * Gq + h) * 2]);
         M = warp_max(M);
         float L = 0.f;
+        #pragma unroll 1
         for (int sp = lane; sp < ns; sp += 32) {
           const float m = ml[(sp * Gq + h) * 2];
           L += (m == -INFINITY ? 0.f : __expf(m - M)) * ml[(sp * Gq + h) * 2 + 1];
         }
         L = warp_sum(L);
         const float invL = 1.f / L;
+        #pragma unroll 1
         for (int sp = lane; sp < ns; sp += 32) {
           const float m = ml[(sp * Gq + h) * 2];
           fs[sp * Gq + h] = (m == -INFINITY ? 0.f : __expf(m - M)) * invL;
@@ -2514,11 +2590,13 @@ struct Consumer {
       uint64_t* att = p.ATT + (static_cast<size_t>(l) * p.max_batch + item.b) * (p.Hq * D) +
                       static_cast<size_t>(item.kvh) * GD;
       const int og = threadIdx.x >> 3, sub = threadIdx.x & 7;
+      #pragma unroll 1
       for (int base = 0; base < nsl; base += kConsumerThreads / 8) {   // uniform trip count: the shuffles below
         const int oi = base + og;
         float acc = 0.f;
         if (oi < nsl) {
           const int h = (o0 + oi) / D;
+          #pragma unroll 1
           for (int sp = sub; sp < ns; sp += 8) acc += fs[sp * Gq + h] * part[sp * nsl + oi];
         }
         acc += __shfl_xor_sync(0xffffffffu, acc, 1);
@@ -2589,6 +2667,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
   Smem& S = *reinterpret_cast<Smem*>(smem_raw + pad);
   const int tid = threadIdx.x;
   if (tid == 0) {
+    #pragma unroll 1
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(&S.full[s], 1);
       mbar_init(&S.empty[s], kConsumerWarps);
@@ -2605,6 +2684,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     // every block warms a slice of the small per-layer vectors (norm gains) in L2, so that
     // their first read in a layer is an L2 hit rather than a DRAM access behind the stream
     const int n_lines = (2 * p.L + 1) * ((p.H * 2 + 127) / 128);
+    #pragma unroll 1
     for (int i = blockIdx.x * kThreads + tid; i < n_lines; i += gridDim.x * kThreads) {
       const int lines_per = (p.H * 2 + 127) / 128;
       const int v = i / lines_per, ln = i - v * lines_per;
@@ -2634,6 +2714,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
   __syncthreads();
   // an aborted step may leave copies in flight: let them land before the block exits
   if (tid == 0) {
+    #pragma unroll 1
     for (uint32_t c = S.cons_count; c < S.prod_count; ++c) {
       const int s = static_cast<int>(c % kSlots);
       const uint32_t ph = (c / kSlots) & 1u;
@@ -2648,14 +2729,17 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
   }
   __syncthreads();
   if (S.is_last) {
+    #pragma unroll 1
     for (uint32_t i = tid; i < p.cm.total; i += kThreads) p.ctr[i] = 0u;
     // Greedy selection, second level: every other block has finished (their partials are
     // ordered before their arrivals on the finish counter, which this block acquired); a warp
     // per row of the batch merges the blocks' partials, read through L2.
     if (p.next_token != nullptr && !aborted(p)) {
       const int warp = tid >> 5, lane = tid & 31;
+      #pragma unroll 1
       for (int b = warp; b < p.B; b += kThreads / 32) {
         Top2 t{-INFINITY, -INFINITY, 0x7fffffff};
+        #pragma unroll 1
         for (int j = lane; j < static_cast<int>(gridDim.x); j += 32) {
           // (blocks with no LM-head rows -- the host's split of the vocabulary -- wrote nothing)
           const uint64_t V = static_cast<uint64_t>(p.V), N = gridDim.x;
