@@ -4,9 +4,10 @@
  * One call of mk_decode_step runs one decode step of a mixture-of-experts
  * transformer for a batch of sequences as a single persistent kernel: one
  * thread block per SM stays resident for the whole step, walks a task list
- * prepared on the host, and waits on dependency counters in global memory
- * ("Inside the megakernel serving engine for North Mini Code", section "What
- * is a Megakernel?" and the "Image 2" paragraph).  The step covers RMSNorm,
+ * prepared on the host, and waits only for the data each task reads -- values
+ * other SMs wrote as words tagged with the step -- rather than for whole
+ * phases ("Inside the megakernel serving engine for North Mini Code", section
+ * "What is a Megakernel?" and the "Image 2" paragraph).  The step covers RMSNorm,
  * fused QKV, RoPE, paged GQA decode attention over ragged lengths with block
  * tables, O-proj + residual, router softmax/top-k, SwiGLU experts, the
  * weighted combine, the final norm and the LM head.
@@ -46,7 +47,7 @@ extern "C" {
 #define MK_ERR_CUDA (-2)          /* a CUDA runtime call failed */
 #define MK_ERR_OOM (-3)           /* device or pinned allocation failed */
 #define MK_ERR_UNSUPPORTED (-4)   /* not an sm_103 device, no cooperative launch, shape outside the compiled limits */
-#define MK_ERR_TIMEOUT (-5)       /* device: a dependency wait exceeded the watchdog budget (mk_get_status) */
+#define MK_ERR_TIMEOUT (-5)       /* device: a wait exceeded the watchdog budget (mk_get_status) */
 #define MK_ERR_DEVICE_BOUNDS (-6) /* device: a token id or block-table page id was out of range (mk_get_status) */
 
 /* CUDA stream handle; ABI-identical to cudaStream_t (NULL = legacy default stream). */
@@ -110,15 +111,20 @@ typedef struct mk_weights {
   const mk_layer_weights* layers; /* host array [num_layers]; copied by mk_create */
 } mk_weights;
 
+/* What a wait that ran out was waiting for (mk_status.wait). */
+#define MK_WAIT_DATA 1   /* words another SM writes (they did not carry the step's tag in time) */
+#define MK_WAIT_RING 2   /* a shared-memory ring slot of the SM (its copy did not land, or was not released) */
+#define MK_WAIT_ROUTE 3  /* the SM's own routing of the layer, which its expert stream waits for */
+
 /* Device-side error record of the last failing step (see mk_get_status). */
 typedef struct mk_status {
   int32_t code;      /* MK_OK, MK_ERR_TIMEOUT or MK_ERR_DEVICE_BOUNDS */
-  int32_t op;        /* task kind that failed (1 embed, 2 qkv, 3 attention, 4 o-proj, 5 router, 6 moe, 7 head) */
-  int32_t layer;
+  int32_t op;        /* task kind that failed (1 embed, 2 qkv, 3 attention, 4 o-proj, 5 router, 6 moe, 7 head; 0 ring) */
+  int32_t layer;     /* its layer, or -1 */
   int32_t cta;       /* thread block that recorded the error */
-  uint32_t counter;  /* counter index waited on (timeout) */
-  uint32_t observed; /* its value when the wait gave up (timeout) / the bad value (bounds) */
-  uint32_t target;   /* the value the wait needed (timeout) */
+  uint32_t wait;     /* timeout: MK_WAIT_*; bounds error: 0 */
+  uint32_t observed; /* timeout on the ring: the record index; bounds error: the bad token or page id */
+  uint32_t tag;      /* timeout on data: the step tag the words had to carry */
   int32_t detail;    /* row / page slot involved, or -1 */
 } mk_status;
 
@@ -129,8 +135,8 @@ typedef struct mk_ctx mk_ctx;
  *   cfg, weights: host structs, read during the call; weight tensors are device
  *                 pointers that must outlive the context.
  *   out:          receives the new context.
- * Allocates the library's workspace (per-layer activations, counters, task
- * lists, pinned staging) and, unless cfg->flags has MK_FLAG_NO_DOWN_COPY, the
+ * Allocates the library's workspace (per-layer tagged activations, step flags,
+ * task lists, pinned staging) and, unless cfg->flags has MK_FLAG_NO_DOWN_COPY, the
  * transposed copy of the down projections, filled on the device before return.  Errors: MK_ERR_INVALID_ARG (null or non-positive or
  * misaligned argument), MK_ERR_UNSUPPORTED (device or shape outside the
  * build's limits), MK_ERR_OOM, MK_ERR_CUDA.

@@ -7,12 +7,13 @@
  * Scheduling model ("Inside the megakernel serving engine for North Mini
  * Code", section "What is a Megakernel?" and the "Image 2" paragraph): the
  * host splits the step into tasks of one tile of one operation each and deals
- * them round-robin over the SMs, one task list per SM in global memory.
- * Dependencies are counters in global memory that a task increments when it
- * finishes and that a consumer spins on.  Attention and MoE work depends on
- * live lengths and on routing: here the attention split plan is rebuilt on the
- * host every step from the host-side seq_lens, and the MoE tiles go into a
- * device work queue filled by the router and drained by every SM.
+ * them over the SMs, one task list per SM in global memory.  A task needs only
+ * the data it reads: every value one SM hands to another is a tagged word (the
+ * value and the step's tag), and the reading SM polls exactly the words it
+ * needs until they carry this step's tag.  Attention and MoE work depend on
+ * live lengths and on routing: the attention split plan is rebuilt on the host
+ * every step from the host-side seq_lens, and every SM routes the batch itself
+ * from the router logits and takes a cost-balanced share of the MoE work.
  */
 #ifndef MK_DEBUG_H
 #define MK_DEBUG_H
@@ -23,29 +24,24 @@
 extern "C" {
 #endif
 
-/* Task kinds (mk_task.op). */
-#define MK_OP_EMBED 1  /* copy embedding rows into the residual stream (a column range of every row) */
-#define MK_OP_QKV 2    /* RMSNorm + fused QKV GEMV, a range of output rows */
-#define MK_OP_ATTN 3   /* this SM's attention split items of the layer (from the per-step plan) */
-#define MK_OP_OPROJ 4  /* O-proj GEMV + residual, a range of output rows */
-#define MK_OP_ROUTER 5 /* RMSNorm + router GEMV, a range of experts; the last one routes */
-#define MK_OP_MOE 6    /* drain the layer's MoE work queue (gate/up tiles, then down tiles) */
-#define MK_OP_HEAD 7   /* final RMSNorm + LM head GEMV, a range of vocab rows */
+/* Task kinds (mk_task.op) and the data each one waits for. */
+#define MK_OP_EMBED 1  /* copy embedding rows into the residual stream (a column range of every row); no wait */
+#define MK_OP_QKV 2    /* RMSNorm + fused QKV GEMV, a range of output rows; waits for the whole layer input */
+#define MK_OP_ATTN 3   /* this SM's attention split items of the layer (from the per-step plan); each item waits
+                          for q, k, v of its (row, KV head); after its last item the SM merges a slice of every
+                          pair it holds a split of, waiting for all of that pair's split partials */
+#define MK_OP_OPROJ 4  /* O-proj GEMV + residual, a range of output rows; waits for the whole attention output */
+#define MK_OP_ROUTER 5 /* RMSNorm + router GEMV, a range of experts; waits for the whole post-attention residual */
+#define MK_OP_MOE 6    /* route the batch from all router logits (every SM), then this SM's share of the
+                          experts; the down projection's combine waits for every SM's share */
+#define MK_OP_HEAD 7   /* final RMSNorm + LM head GEMV, a range of vocab rows; waits for the last layer's output */
 #define MK_OP_END 8    /* end of this SM's list */
 
-#define MK_NO_COUNTER 0xffffffffu
-
-/* One task of an SM's list (32 bytes).  The task may start once
- * counter[wait_ctr] >= wait_base + wait_per_b * batch; when its tile is done
- * it adds 1 to counter[signal_ctr] (MK_NO_COUNTER: none). */
+/* One task of an SM's list (16 bytes): an operation, its layer and its row range. */
 typedef struct mk_task {
   uint16_t op;
   uint16_t layer;
   uint32_t lo, hi; /* row (or column) range [lo, hi) */
-  uint32_t wait_ctr;
-  uint32_t wait_base;
-  uint32_t wait_per_b;
-  uint32_t signal_ctr;
   uint32_t reserved;
 } mk_task;
 
@@ -64,7 +60,7 @@ typedef struct mk_plan_info {
   int32_t n_qkv_tiles, n_o_tiles, n_router_tiles, n_head_tiles, n_embed_tiles;
   int32_t n_down_ranges;    /* blocks that own hidden rows of the down projection */
   int32_t reserved[3];
-  int32_t n_counters;       /* counters the step uses */
+  int32_t n_flags;          /* words of step flags (abort flag, finish count); all other exchange is tagged data */
   int32_t max_items;        /* attention items a step can produce for max_batch */
 } mk_plan_info;
 
@@ -85,15 +81,22 @@ typedef struct mk_sim_result {
   int32_t deadlocked;      /* 1 if no SM could make progress before the end */
   int64_t events;          /* scheduling events simulated */
   int32_t tiles_run[9];    /* tiles / items executed, indexed by op */
-  int32_t counters_ok;     /* 1 if every counter ended at its expected value */
+  int32_t writes_ok;       /* 1 if every tile that writes data another SM reads ran exactly once */
   int32_t moe_units_ok;    /* 1 if every gate/up unit and every (expert, hidden row) of the down
                               projection was assigned to exactly one block */
 } mk_sim_result;
 
 /* Run the step's task graph on the CPU with `n_ctas` virtual SMs under a seeded
  * random interleaving.  Each virtual SM has a producer that runs at most
- * `producer_lead` records ahead of its consumer (splitting the MoE work with the
- * same rule as the device) and a consumer that honours every counter wait.
+ * `producer_lead` records ahead of its consumer (routing is handed from the
+ * consumer to its own producer before the MoE records exist, and the MoE work
+ * is split with the same rule as the device) and a consumer whose every record
+ * waits for exactly the writer tiles of the data the device reads there: an
+ * attention item for the QKV tiles holding its (row, KV head)'s q, k and v,
+ * the split merge for all splits of its pairs, O-proj for every merge slice
+ * and its own residual rows, a router tile for every O-proj tile, routing for
+ * every router tile, the MoE combine for every SM's share, QKV and the LM head
+ * for every writer of their input.
  * routing_ids: host [num_layers][batch][top_k] expert ids the router is taken to
  * choose. */
 int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t batch, const int32_t* seq_lens,
@@ -113,9 +116,9 @@ int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t batch, const int32
  * step's batch. */
 int mk_debug_read(mk_ctx* ctx, int32_t what, int32_t layer, void* host_dst, size_t bytes);
 
-/* Test hook: the next step's first O-proj task of `layer` waits on a counter
- * nothing increments, so the watchdog must end the step with MK_ERR_TIMEOUT
- * after `watchdog_ms` (0 keeps the context's budget).  layer < 0 disarms. */
+/* Test hook: the O-proj tasks of `layer` in the next step wait for a tag that
+ * no SM writes, so the watchdog must end the step with MK_ERR_TIMEOUT after
+ * `watchdog_ms` (0 keeps the context's budget).  layer < 0 disarms. */
 int mk_debug_inject_stall(mk_ctx* ctx, int32_t layer, uint32_t watchdog_ms);
 
 /* Timeline of later steps.  enable != 0 allocates a device buffer of

@@ -32,6 +32,7 @@ ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 MK_OK, MK_ERR_INVALID_ARG, MK_ERR_CUDA, MK_ERR_OOM = 0, -1, -2, -3
 MK_ERR_UNSUPPORTED, MK_ERR_TIMEOUT, MK_ERR_DEVICE_BOUNDS = -4, -5, -6
 OPS = {1: "embed", 2: "qkv", 3: "attn", 4: "oproj", 5: "router", 6: "moe", 7: "head", 8: "end"}
+WAITS = {0: None, 1: "data", 2: "ring", 3: "route"}   # mk_status.wait
 DBG = dict(x=1, qkv=2, attn=3, router=4, route_ids=5, route_w=6, h=7)
 
 
@@ -105,14 +106,13 @@ class Weights(ctypes.Structure):
 
 class Status(ctypes.Structure):
     _fields_ = [("code", ctypes.c_int32), ("op", ctypes.c_int32), ("layer", ctypes.c_int32), ("cta", ctypes.c_int32),
-                ("counter", ctypes.c_uint32), ("observed", ctypes.c_uint32), ("target", ctypes.c_uint32),
+                ("wait", ctypes.c_uint32), ("observed", ctypes.c_uint32), ("tag", ctypes.c_uint32),
                 ("detail", ctypes.c_int32)]
 
 
 class Task(ctypes.Structure):
     _fields_ = [("op", ctypes.c_uint16), ("layer", ctypes.c_uint16), ("lo", ctypes.c_uint32), ("hi", ctypes.c_uint32),
-                ("wait_ctr", ctypes.c_uint32), ("wait_base", ctypes.c_uint32), ("wait_per_b", ctypes.c_uint32),
-                ("signal_ctr", ctypes.c_uint32), ("reserved", ctypes.c_uint32)]
+                ("reserved", ctypes.c_uint32)]
 
 
 class AttnItem(ctypes.Structure):
@@ -123,12 +123,12 @@ class AttnItem(ctypes.Structure):
 class PlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("n_ctas", "n_tasks", "n_qkv_tiles", "n_o_tiles", "n_router_tiles",
                                                "n_head_tiles", "n_embed_tiles", "n_down_ranges", "reserved0",
-                                               "reserved1", "reserved2", "n_counters", "max_items")]
+                                               "reserved1", "reserved2", "n_flags", "max_items")]
 
 
 class SimResult(ctypes.Structure):
     _fields_ = [("finished", ctypes.c_int32), ("deadlocked", ctypes.c_int32), ("events", ctypes.c_int64),
-                ("tiles_run", ctypes.c_int32 * 9), ("counters_ok", ctypes.c_int32),
+                ("tiles_run", ctypes.c_int32 * 9), ("writes_ok", ctypes.c_int32),
                 ("moe_units_ok", ctypes.c_int32)]
 
 
@@ -369,8 +369,8 @@ class Engine:
         rc = lib().mk_get_status(self.ctx, ctypes.byref(st))
         if rc not in (MK_OK, MK_ERR_TIMEOUT, MK_ERR_DEVICE_BOUNDS):
             raise MkError(rc, lib().mk_last_error().decode())
-        return dict(code=st.code, op=OPS.get(st.op, st.op), layer=st.layer, cta=st.cta, counter=st.counter,
-                    observed=st.observed, target=st.target, detail=st.detail)
+        return dict(code=st.code, op=OPS.get(st.op, st.op), layer=st.layer, cta=st.cta,
+                    wait=WAITS.get(st.wait, st.wait), observed=st.observed, tag=st.tag, detail=st.detail)
 
     def check(self):
         st = self.status()

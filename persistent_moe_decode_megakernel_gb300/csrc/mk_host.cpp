@@ -1,16 +1,16 @@
 // mk_host.cpp -- host side of the megakernel library: argument checks, the
 // static task lists, the per-step attention split plan, the workspace, the
 // cooperative launch, status readback, debug reads and a CPU simulator of the
-// task graph.
+// step's data dependencies.
 //
 // Scheduling follows "Inside the megakernel serving engine for North Mini
 // Code" ("Image 2" paragraph): the step is split into tasks of one tile of one
 // operation, dealt over the SMs, one list per SM in global memory; attention
 // and MoE work depend on live lengths and routing.  Here the static lists (all
-// GEMV tiles, one "drain attention" and one "drain MoE" task per layer) are
-// built once per context; the attention split plan is rebuilt on the host each
-// step from the host-side lengths; the MoE tiles are queued on the device by
-// the router.
+// GEMV tiles, one attention task and one MoE task per layer) are built once per
+// context; the attention split plan is rebuilt on the host each step from the
+// host-side lengths; the MoE work is split on the device by every SM from its
+// own routing of the batch.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -39,8 +39,6 @@ cudaError_t configure_kernels(int D);
 cudaError_t occupancy(int D, int* blocks);
 size_t smem_bytes();
 }  // namespace mk
-
-using mk::CounterMap;
 
 namespace {
 
@@ -128,7 +126,6 @@ struct Plan {
   std::vector<mk_task> tasks;
   std::vector<int32_t> off;
   mk_plan_info info;
-  CounterMap cm;
 };
 
 void split_range(uint32_t n, int parts, int i, uint32_t* lo, uint32_t* hi) {
@@ -142,8 +139,7 @@ void build_static_plan(const mk_config& c, int n_ctas, Plan& plan) {
   const int L = c.num_layers, H = c.hidden, E = c.num_experts, V = c.vocab;
   const int nqkv = (c.num_q_heads + 2 * c.num_kv_heads) * c.head_dim;
   in.n_ctas = n_ctas;
-  plan.cm = mk::counter_map(L, c.max_batch, c.num_kv_heads);
-  in.n_counters = (int32_t)plan.cm.total;
+  in.n_flags = (int32_t)mk::kStepFlags;
   in.max_items = n_ctas + c.max_batch * c.num_kv_heads;
   auto count = [&](uint32_t rows) {
     int n = 0;
@@ -161,39 +157,33 @@ void build_static_plan(const mk_config& c, int n_ctas, Plan& plan) {
   in.n_router_tiles = (E + rr - 1) / rr;
   in.n_head_tiles = count((uint32_t)V);
   in.n_down_ranges = count((uint32_t)H);
-  const CounterMap& cm = plan.cm;
   plan.tasks.clear();
   plan.off.assign(n_ctas + 1, 0);
-  auto push = [&](uint16_t op, int layer, uint32_t lo, uint32_t hi, uint32_t wc, uint32_t wb, uint32_t wpb, uint32_t sc) {
+  auto push = [&](uint16_t op, int layer, uint32_t lo, uint32_t hi) {
     mk_task t;
-    t.op = op; t.layer = (uint16_t)layer; t.lo = lo; t.hi = hi;
-    t.wait_ctr = wc; t.wait_base = wb; t.wait_per_b = wpb; t.signal_ctr = sc; t.reserved = 0;
+    t.op = op; t.layer = (uint16_t)layer; t.lo = lo; t.hi = hi; t.reserved = 0;
     plan.tasks.push_back(t);
   };
+  // Every list runs the layers in order and, within a layer, the phases in data order; a
+  // task waits on the device for exactly the tagged words it reads (see mk_debug.h).
   for (int i = 0; i < n_ctas; ++i) {
     plan.off[i] = (int32_t)plan.tasks.size();
     uint32_t lo, hi;
     split_range((uint32_t)H, n_ctas, i, &lo, &hi);
-    if (hi > lo) push(MK_OP_EMBED, 0, lo, hi, MK_NO_COUNTER, 0, 0, mk::C_EMBED);
+    if (hi > lo) push(MK_OP_EMBED, 0, lo, hi);
     for (int l = 0; l < L; ++l) {
-      const uint32_t base = cm.layer_base(l);
       split_range((uint32_t)nqkv, n_ctas, i, &lo, &hi);
-      if (hi > lo) {
-        if (l == 0) push(MK_OP_QKV, l, lo, hi, mk::C_EMBED, (uint32_t)in.n_embed_tiles, 0, base + mk::L_QKV);
-        else push(MK_OP_QKV, l, lo, hi, cm.layer_base(l - 1) + mk::L_MOE, (uint32_t)n_ctas, 0, base + mk::L_QKV);
-      }
-      push(MK_OP_ATTN, l, 0, 0, base + mk::L_QKV, (uint32_t)in.n_qkv_tiles, 0, MK_NO_COUNTER);
+      if (hi > lo) push(MK_OP_QKV, l, lo, hi);
+      push(MK_OP_ATTN, l, 0, 0);
       split_range((uint32_t)H, n_ctas, i, &lo, &hi);
-      if (hi > lo) push(MK_OP_OPROJ, l, lo, hi, base + mk::L_ATTN, 0, (uint32_t)c.num_kv_heads, base + mk::L_O);
+      if (hi > lo) push(MK_OP_OPROJ, l, lo, hi);
       for (int t = i; t < in.n_router_tiles; t += n_ctas)
-        push(MK_OP_ROUTER, l, (uint32_t)(t * rr), (uint32_t)std::min(E, (t + 1) * rr),
-             base + mk::L_O, (uint32_t)in.n_o_tiles, 0, MK_NO_COUNTER);
-      push(MK_OP_MOE, l, 0, 0, base + mk::L_RREADY, 1, 0, MK_NO_COUNTER);
+        push(MK_OP_ROUTER, l, (uint32_t)(t * rr), (uint32_t)std::min(E, (t + 1) * rr));
+      push(MK_OP_MOE, l, 0, 0);
     }
     split_range((uint32_t)V, n_ctas, i, &lo, &hi);
-    if (hi > lo)
-      push(MK_OP_HEAD, L, lo, hi, cm.layer_base(L - 1) + mk::L_MOE, (uint32_t)n_ctas, 0, MK_NO_COUNTER);
-    push(MK_OP_END, 0, 0, 0, MK_NO_COUNTER, 0, 0, MK_NO_COUNTER);
+    if (hi > lo) push(MK_OP_HEAD, L, lo, hi);
+    push(MK_OP_END, 0, 0, 0);
   }
   plan.off[n_ctas] = (int32_t)plan.tasks.size();
   in.n_tasks = (int32_t)plan.tasks.size();
@@ -303,7 +293,7 @@ struct mk_ctx {
   int32_t* RIDS = nullptr;
   uint32_t tag = 0;        // tag of the last step (0: none yet)
   size_t tagged_bytes = 0; // bytes of the tagged buffers (cleared when the tag wraps)
-  uint32_t* ctr = nullptr;
+  uint32_t* flags = nullptr;   // [kStepFlags] abort flag, finish count
   mk_status* d_status = nullptr;
   // per-step staging (double-buffered)
   size_t step_bytes = 0;
@@ -474,7 +464,7 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_ctx** out) {
       {(void**)&c->RIDS, (size_t)L * MB * K * i4},
       {(void**)&c->argp, (size_t)c->n_ctas * MB * 4 * f4},
       {(void**)&c->RW, (size_t)L * MB * K * f4},
-      {(void**)&c->ctr, (size_t)c->plan.cm.total * 4},
+      {(void**)&c->flags, (size_t)mk::kStepFlags * 4},
       {(void**)&c->d_status, sizeof(mk_status)},
   };
   size_t total = 0;
@@ -604,7 +594,6 @@ static int decode_step(mk_ctx* c, int32_t batch, const int32_t* token_ids, const
   p.B = batch; p.max_batch = cf.max_batch; p.n_ctas = c->n_ctas;
   const mk_plan_info& in = c->plan.info;
   p.n_qkv_tiles = in.n_qkv_tiles; p.n_o_tiles = in.n_o_tiles; p.n_router_tiles = in.n_router_tiles;
-  p.cm = c->plan.cm;
   uint32_t wd_ms = cf.watchdog_ms;
   p.tasks = c->d_tasks; p.task_off = c->d_task_off;
   p.layers = c->d_layers; p.embed = c->embed; p.final_norm = c->final_norm; p.lm_head = c->lm_head;
@@ -628,7 +617,7 @@ static int decode_step(mk_ctx* c, int32_t batch, const int32_t* token_ids, const
     c->tag = 1;
   }
   p.tag = c->tag;
-  p.ctr = c->ctr; p.status = c->d_status;
+  p.flags = c->flags; p.status = c->d_status;
   p.trace = c->trace; p.trace_cap = c->trace_cap;
   if (kv_pages != c->kv_map_ptr) {
     int rc2 = encode_kv_map(cf, kv_pages, &c->kv_map);
@@ -812,10 +801,10 @@ int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t B, const int32_t* 
   std::vector<int32_t> ioff, pf;
   build_attention_plan(*cfg, n_ctas, B, seq_lens, items, ioff, pf);
   const mk_plan_info& in = plan.info;
-  const CounterMap& cm = plan.cm;
   const int L = cfg->num_layers, E = cfg->num_experts, K = cfg->top_k, Hkv = cfg->num_kv_heads;
-  const int F = cfg->expert_ffn, H = cfg->hidden;
-  std::vector<uint32_t> ctr(cm.total, 0);
+  const int F = cfg->expert_ffn, H = cfg->hidden, D = cfg->head_dim, Hq = cfg->num_q_heads, G = Hq / Hkv;
+  const uint32_t nqkv = (uint32_t)(Hq + 2 * Hkv) * D;
+  const int n_items = (int)items.size();
   // per layer: active experts (ascending) and the gate/up unit range of every block
   std::vector<std::vector<int>> act(L), rows_of(L);   // active experts; rows routed to each expert
   std::vector<std::vector<int32_t>> gu_start(L);
@@ -848,15 +837,57 @@ int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t B, const int32_t* 
     dt_seen[l].assign(act[l].size() * F, 0);
   }
 
-  // record kinds: a task op, or 100 = gate/up chunk, 101 = down chunk; small-batch path:
-  // 105 = gate/up chunk, 102 = transposed down chunk, 104 = publish the partial output,
-  // 103 = reduce every block's partials
+  // ---- what has been written this step, by writer tile (the device polls the tagged words
+  // those tiles write; a reader proceeds once every word it reads carries the step's tag)
+  std::vector<uint32_t> hlo(n_ctas), hhi(n_ctas), qlo(n_ctas), qhi(n_ctas);
+  int n_hrow_blocks = 0;   // blocks owning hidden rows: writers of every residual vector
+  for (int i = 0; i < n_ctas; ++i) {
+    split_range((uint32_t)H, n_ctas, i, &hlo[i], &hhi[i]);
+    split_range(nqkv, n_ctas, i, &qlo[i], &qhi[i]);
+    n_hrow_blocks += hhi[i] > hlo[i];
+  }
+  int n_item_blocks = 0;   // blocks that hold attention items (each merges a slice after its last one)
+  for (int i = 0; i < n_ctas; ++i) n_item_blocks += ioff[i + 1] > ioff[i];
+  // xout[l][i]: block i wrote its hidden rows of the layer-l input X[2l] (l = 0: the embedding,
+  // l = L: the last layer's output); its count per layer
+  std::vector<std::vector<char>> xout(L + 1, std::vector<char>(n_ctas, 0));
+  std::vector<int> xout_n(L + 1, 0);
+  std::vector<std::vector<char>> qkv_done(L, std::vector<char>(n_ctas, 0));
+  std::vector<std::vector<char>> item_done(L, std::vector<char>(std::max(1, n_items), 0));
+  std::vector<int> merged_n(L, 0), oproj_n(L, 0), router_n(L, 0), moe_share_n(L, 0);
+  std::vector<std::vector<char>> oproj_done(L, std::vector<char>(n_ctas, 0));
+  std::vector<std::vector<char>> routed(n_ctas, std::vector<char>(L, 0));
+  int writes_twice = 0;
+  auto mark = [&](char& f) { if (f) writes_twice++; f = 1; };
+  // QKV tiles holding rows [r0, r1) of the fused output: the device's attention item polls
+  // those words (q of the pair's query heads, k and v of its KV head)
+  auto qkv_rows_ready = [&](int l, uint32_t r0, uint32_t r1) {
+    for (int i = 0; i < n_ctas; ++i)
+      if (qhi[i] > qlo[i] && qlo[i] < r1 && qhi[i] > r0 && !qkv_done[l][i]) return false;
+    return true;
+  };
+  // residual rows [r0, r1) of X[2l] (the block's own O-proj residual input)
+  auto xrows_ready = [&](int l, uint32_t r0, uint32_t r1) {
+    for (int i = 0; i < n_ctas; ++i)
+      if (hhi[i] > hlo[i] && hlo[i] < r1 && hhi[i] > r0 && !xout[l][i]) return false;
+    return true;
+  };
+  auto orows_ready = [&](int l, uint32_t r0, uint32_t r1) {
+    for (int i = 0; i < n_ctas; ++i)
+      if (hhi[i] > hlo[i] && hlo[i] < r1 && hhi[i] > r0 && !oproj_done[l][i]) return false;
+    return true;
+  };
+
+  // record kinds: a task op (ATTN: one per item), 110 = routing (every block), 100 = gate/up
+  // chunk, 101 = down chunk; small-batch path: 105 = gate/up chunk, 102 = transposed down
+  // chunk, 104 = publish the partial output, 103 = reduce every block's partials
   struct Rec { int kind; int task; int layer; uint32_t a; uint32_t x; int flags; };
-  enum { F_FIRST = 1, F_LAST = 2, F_LAST_GU = 4 };
+  enum { F_FIRST = 1, F_LAST = 2, F_LAST_GU = 4, F_EMPTY = 8 };
   struct Sm {
     std::vector<Rec> q; size_t qhead = 0; int ti;
-    std::vector<Rec> moe; size_t moe_next = 0; bool moe_open = false;
+    std::vector<Rec> moe; size_t moe_next = 0; bool moe_open = false; bool route_sent = false;
     bool prod_done = false; bool done = false;
+    int merge_layer = -1;   // the split merge the consumer runs after its last attention item
   };
   std::vector<Sm> sm(n_ctas);
   for (int i = 0; i < n_ctas; ++i) sm[i].ti = plan.off[i];
@@ -885,10 +916,10 @@ int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t B, const int32_t* 
         u = a * F + fend;
       }
       r.push_back({104, task, l, 0, 0, 0});
-      r.push_back({103, task, l, 0, 0, 0});
+      r.push_back({103, task, l, 0, 0, hhi[i] > hlo[i] ? 0 : F_EMPTY});
       return r;
     }
-    if (u0 >= u1) r.push_back({100, task, l, 0, 0, F_FIRST | F_LAST | F_LAST_GU});
+    if (u0 >= u1) r.push_back({100, task, l, 0, 0, F_FIRST | F_LAST | F_LAST_GU | F_EMPTY});
     for (int u = u0; u < u1;) {
       const int a = u / F, f0 = u % F, fend = std::min(F, u1 - a * F);
       // batches of 3 or more: the run is streamed once per register group of its routed rows
@@ -905,10 +936,9 @@ int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t B, const int32_t* 
       }
       u = a * F + fend;
     }
-    uint32_t r0, r1;
-    split_range((uint32_t)H, n_ctas, i, &r0, &r1);
-    if (r1 <= r0) {
-      r.push_back({101, task, l, 0, r0, F_FIRST | F_LAST});
+    const uint32_t r0 = hlo[i], r1 = hhi[i];
+    if (r1 <= r0 || nact == 0) {
+      r.push_back({101, task, l, 0, r0, F_FIRST | F_LAST | F_EMPTY});
       return r;
     }
     const int rpc = std::min((int)(r1 - r0), rows_fit);
@@ -925,11 +955,9 @@ int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t B, const int32_t* 
         first = false;
       }
     }
-    if (nact == 0) r.push_back({101, task, l, 0, r0, F_FIRST | F_LAST});
     return r;
   };
 
-  auto target = [&](const mk_task& t) { return t.wait_base + t.wait_per_b * (uint32_t)B; };
   auto produce = [&](int i) -> bool {   // one record; false if blocked or finished
     Sm& s = sm[i];
     if (s.prod_done || (int)(s.q.size() - s.qhead) >= lead) return false;
@@ -940,8 +968,13 @@ int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t B, const int32_t* 
         break;
       case MK_OP_MOE: {
         const int l = t.layer;
+        if (!s.route_sent) {            // the routing record, then wait for this block's routing
+          s.q.push_back({110, s.ti, l, 0, 0, 0});
+          s.route_sent = true;
+          return true;
+        }
         if (!s.moe_open) {
-          if (ctr[cm.layer_base(l) + mk::L_RREADY] < 1) return false;
+          if (!routed[i][l]) return false;
           s.moe = moe_records(i, l, s.ti);
           s.moe_next = 0;
           s.moe_open = true;
@@ -949,6 +982,7 @@ int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t B, const int32_t* 
         s.q.push_back(s.moe[s.moe_next++]);
         if (s.moe_next < s.moe.size()) return true;   // stay on this task
         s.moe_open = false;
+        s.route_sent = false;
         break;
       }
       default: s.q.push_back({t.op, s.ti, t.layer, 0, 0, 0}); break;
@@ -959,49 +993,88 @@ int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t B, const int32_t* 
   };
   auto consume = [&](int i) -> bool {
     Sm& s = sm[i];
-    if (s.done || s.qhead >= s.q.size()) return false;
+    if (s.done) return false;
+    if (s.merge_layer >= 0) {
+      // the split merge after the block's last item: every split of each pair it holds a split of
+      const int l = s.merge_layer;
+      for (int it = ioff[i]; it < ioff[i + 1]; ++it) {
+        const int first = pf[items[it].b * Hkv + items[it].kvh];
+        for (int k = 0; k < items[it].nsplit; ++k)
+          if (!item_done[l][first + k]) return false;
+      }
+      merged_n[l]++;
+      s.merge_layer = -1;
+      return true;
+    }
+    if (s.qhead >= s.q.size()) return false;
     const Rec& r = s.q[s.qhead];
     const mk_task& t = plan.tasks[r.task];
-    const uint32_t base = cm.layer_base(r.layer);
+    const int l = r.layer;
     switch (r.kind) {
+      case MK_OP_EMBED:
+        mark(xout[0][i]);
+        xout_n[0]++;
+        break;
+      case MK_OP_QKV:
+        if (xout_n[l] < n_hrow_blocks) return false;
+        mark(qkv_done[l][i]);
+        break;
       case MK_OP_ATTN: {
-        if (ctr[t.wait_ctr] < target(t)) return false;
         const mk_attn_item& it = items[r.a];
-        const uint32_t pc = base + mk::L_PAIR + it.b * Hkv + it.kvh;
-        if (++ctr[pc] == it.nsplit) ctr[base + mk::L_ATTN]++;
+        const uint32_t q0 = (uint32_t)it.kvh * G * D, k0 = (uint32_t)(Hq + it.kvh) * D,
+                       v0 = (uint32_t)(Hq + Hkv + it.kvh) * D;
+        if (!qkv_rows_ready(l, q0, q0 + (uint32_t)G * D) || !qkv_rows_ready(l, k0, k0 + D) ||
+            !qkv_rows_ready(l, v0, v0 + D))
+          return false;
+        mark(item_done[l][r.a]);
+        if ((int)r.a == ioff[i + 1] - 1) s.merge_layer = l;
         break;
       }
-      case 100:   // the device signals once, at the end of the block's last gate/up run
-        if ((r.flags & F_LAST_GU) && (r.flags & F_LAST)) ctr[base + mk::L_GU]++;
+      case MK_OP_OPROJ:
+        if (merged_n[l] < n_item_blocks || !xrows_ready(l, t.lo, t.hi)) return false;
+        mark(oproj_done[l][i]);
+        oproj_n[l]++;
         break;
-      case 101:
-        if ((r.flags & F_FIRST) && ctr[base + mk::L_GU] < (uint32_t)n_ctas) return false;
-        if (r.flags & F_LAST) ctr[base + mk::L_MOE]++;
+      case MK_OP_ROUTER:
+        if (oproj_n[l] < in.n_o_tiles) return false;
+        router_n[l]++;
+        break;
+      case 110:   // routing: every router logit (and the MoE input, x after attention)
+        if (router_n[l] < in.n_router_tiles || oproj_n[l] < in.n_o_tiles) return false;
+        mark(routed[i][l]);
+        break;
+      case 100:   // a block's gate/up share is complete after its last run's last chunk
+        if ((r.flags & F_LAST_GU) && (r.flags & F_LAST)) moe_share_n[l]++;
+        break;
+      case 101:   // the down projection reads every block's SwiGLU outputs and its own x rows
+        if (!(r.flags & F_EMPTY) && (r.flags & F_FIRST) &&
+            (moe_share_n[l] < n_ctas || !orows_ready(l, hlo[i], hhi[i])))
+          return false;
+        if (!(r.flags & F_EMPTY) && (r.flags & F_LAST)) { mark(xout[l + 1][i]); xout_n[l + 1]++; }
         break;
       case 102:
       case 105:
         break;
       case 104:   // this block's partial output is published
-        ctr[base + mk::L_GU]++;
+        moe_share_n[l]++;
         break;
-      case 103:   // the reduction needs every block's partial
-        if (ctr[base + mk::L_GU] < (uint32_t)n_ctas) return false;
-        ctr[base + mk::L_MOE]++;
+      case 103:   // the reduction reads every block's partial and its own x rows
+        if (!(r.flags & F_EMPTY)) {
+          if (moe_share_n[l] < n_ctas || !orows_ready(l, hlo[i], hhi[i])) return false;
+          mark(xout[l + 1][i]);
+          xout_n[l + 1]++;
+        }
         break;
-      case MK_OP_ROUTER:
-        if (ctr[t.wait_ctr] < target(t)) return false;
-        if (++ctr[base + mk::L_RARR] == (uint32_t)in.n_router_tiles) ctr[base + mk::L_RREADY] = 1;
+      case MK_OP_HEAD:
+        if (xout_n[L] < n_hrow_blocks) return false;
         break;
       case MK_OP_END:
-        ctr[mk::C_FINISH]++;
         s.done = true;
         break;
       default:
-        if (t.wait_ctr != MK_NO_COUNTER && ctr[t.wait_ctr] < target(t)) return false;
-        if (t.signal_ctr != MK_NO_COUNTER) ctr[t.signal_ctr]++;
-        break;
+        return false;
     }
-    int op = r.kind >= 100 ? MK_OP_MOE : r.kind;
+    const int op = r.kind == 110 || r.kind >= 100 ? MK_OP_MOE : r.kind;
     out->tiles_run[op]++;
     s.qhead++;
     return true;
@@ -1025,15 +1098,17 @@ int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t B, const int32_t* 
     if (!progress) { out->deadlocked = 1; break; }
   }
   out->finished = finished == n_ctas;
-  bool ok = ctr[mk::C_EMBED] == (uint32_t)in.n_embed_tiles && ctr[mk::C_FINISH] == (uint32_t)n_ctas;
+  // every writer ran exactly once
+  bool ok = writes_twice == 0 && xout_n[0] == in.n_embed_tiles;
   for (int l = 0; l < L && ok; ++l) {
-    const uint32_t base = cm.layer_base(l);
-    ok = ctr[base + mk::L_QKV] == (uint32_t)in.n_qkv_tiles && ctr[base + mk::L_ATTN] == (uint32_t)(B * Hkv) &&
-         ctr[base + mk::L_O] == (uint32_t)in.n_o_tiles && ctr[base + mk::L_RARR] == (uint32_t)in.n_router_tiles &&
-         ctr[base + mk::L_RREADY] == 1u && ctr[base + mk::L_GU] == (uint32_t)n_ctas &&
-         ctr[base + mk::L_MOE] == (uint32_t)n_ctas;
+    int nq = 0, ni = 0;
+    for (int i = 0; i < n_ctas; ++i) nq += qkv_done[l][i];
+    for (int it = 0; it < n_items; ++it) ni += item_done[l][it];
+    ok = nq == in.n_qkv_tiles && ni == n_items && merged_n[l] == n_item_blocks && oproj_n[l] == in.n_o_tiles &&
+         router_n[l] == in.n_router_tiles && moe_share_n[l] == n_ctas && xout_n[l + 1] == n_hrow_blocks;
+    for (int i = 0; i < n_ctas && ok; ++i) ok = routed[i][l] == 1;
   }
-  out->counters_ok = ok;
+  out->writes_ok = ok;
   bool uok = true;
   for (int l = 0; l < L; ++l) {
     for (int v : gu_seen[l]) uok = uok && v == 1;

@@ -158,19 +158,6 @@ __device__ __forceinline__ uint64_t policy_evict_normal() {
   asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 __device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
   uint32_t old;
   asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
@@ -328,9 +315,8 @@ struct Meta {
   uint32_t idx;          // task index (GEMV/EMBED) / item index (ATTN) / active expert (GU/DOWN)
   uint32_t e;            // expert id (GU/DOWN)
   uint32_t aux;          // row tile (DOWN)
-  uint32_t wait_ctr, wait_target, signal_ctr;
   uint32_t lo, hi;       // tile range
-  uint32_t pad[5];
+  uint32_t pad[8];       // pad[0..1]: issue time of the record (timeline builds)
 };
 static_assert(sizeof(Meta) == 64, "meta size");
 
@@ -372,23 +358,25 @@ struct __align__(128) Smem {
 static_assert(sizeof(Smem) + 1024 <= 227 * 1024, "shared memory (with the 1024-byte alignment pad) exceeds 227 KB");
 
 // --------------------------------------------------------------------------- errors / waits
-__device__ __noinline__ void record_error(const Params& p, int code, int op, int layer, uint32_t ctr, uint32_t observed,
-                             uint32_t target, int detail, bool abort) {
+// wait: MK_WAIT_* for a timeout (what the wait was on), 0 for a bounds error; observed: the ring
+// record (timeout on the ring) or the bad value (bounds); tag: the step tag a data wait needed
+__device__ __noinline__ void record_error(const Params& p, int code, int op, int layer, uint32_t wait, uint32_t observed,
+                             uint32_t tag, int detail, bool abort) {
   if (atomicCAS(&p.status->code, 0, code) == 0) {
     p.status->op = op;
     p.status->layer = layer;
     p.status->cta = blockIdx.x;
-    p.status->counter = ctr;
+    p.status->wait = wait;
     p.status->observed = observed;
-    p.status->target = target;
+    p.status->tag = tag;
     p.status->detail = detail;
     __threadfence();
   }
-  if (abort) atomicExch(&p.ctr[C_ABORT], 1u);
+  if (abort) atomicExch(&p.flags[F_ABORT], 1u);
 }
 
 __device__ __forceinline__ bool aborted(const Params& p) {
-  return *reinterpret_cast<const volatile uint32_t*>(&p.ctr[C_ABORT]) != 0u;
+  return *reinterpret_cast<const volatile uint32_t*>(&p.flags[F_ABORT]) != 0u;
 }
 
 // A tagged read that found a stale tag re-polls the word in place (no call, so that the
@@ -411,7 +399,7 @@ __device__ __forceinline__ bool aborted(const Params& p) {
   } while (0)
 
 __device__ __noinline__ void ll_timeout(const Params& p, int op, int layer) {
-  record_error(p, MK_ERR_TIMEOUT, op, layer, MK_NO_COUNTER, 0, p.tag, -1, true);
+  record_error(p, MK_ERR_TIMEOUT, op, layer, MK_WAIT_DATA, 0, p.tag, -1, true);
 }
 
 // A batch of tagged loads written between LL_RETRY_BEGIN and LL_RETRY_END(ok) ORs the
@@ -496,7 +484,7 @@ __device__ bool warp_wait_record(const Params& p, Smem& S, uint32_t c) {
       if ((it & 63u) == 0u) {
         if (aborted(p)) break;
         if (globaltimer() - t0 > p.watchdog_ns) {
-          if ((threadIdx.x & 31) == 0) record_error(p, MK_ERR_TIMEOUT, 0, -1, MK_NO_COUNTER, c, 0, -1, true);
+          if ((threadIdx.x & 31) == 0) record_error(p, MK_ERR_TIMEOUT, 0, -1, MK_WAIT_RING, c, 0, -1, true);
           break;
         }
       }
@@ -596,7 +584,7 @@ struct Producer {
       if ((it & 63u) == 0u) {
         if (aborted(p)) return false;
         if (globaltimer() - t0 > p.watchdog_ns) {
-          record_error(p, MK_ERR_TIMEOUT, 0, -1, MK_NO_COUNTER, c, 0, -1, true);
+          record_error(p, MK_ERR_TIMEOUT, 0, -1, MK_WAIT_RING, c, 0, -1, true);
           return false;
         }
       }
@@ -619,8 +607,7 @@ struct Producer {
     Meta& m = meta();
     m.kind = kind; m.op = static_cast<uint8_t>(t.op); m.first = 1; m.last = 1;
     m.layer = t.layer; m.n = 0; m.row0 = t.lo; m.idx = idx; m.e = 0; m.aux = 0;
-    m.wait_ctr = t.wait_ctr; m.wait_target = t.wait_base + t.wait_per_b * static_cast<uint32_t>(p.B);
-    m.signal_ctr = t.signal_ctr; m.lo = t.lo; m.hi = t.hi;
+    m.lo = t.lo; m.hi = t.hi;
     mbar_arrive(full());
     ++c;
     return true;
@@ -654,8 +641,7 @@ struct Producer {
         m.last = (g == ng - 1 && r0 + n >= t.hi);
         m.layer = t.layer; m.n = static_cast<uint16_t>(n); m.row0 = r0; m.idx = ti; m.e = 0;
         m.aux = static_cast<uint32_t>(g);
-        m.wait_ctr = t.wait_ctr; m.wait_target = t.wait_base + t.wait_per_b * static_cast<uint32_t>(p.B);
-        m.signal_ctr = t.signal_ctr; m.lo = t.lo; m.hi = t.hi;
+        m.lo = t.lo; m.hi = t.hi;
         const uint32_t bytes = n * static_cast<uint32_t>(K) * 2u;
         mbar_arrive_expect_tx(full(), bytes);
         bulk_g2s(slot(), W + static_cast<size_t>(r0) * K, bytes, full(), g == ng - 1 ? pol : pl);
@@ -685,16 +671,14 @@ struct Producer {
         Meta& m = meta();
         m.kind = R_ATTN; m.op = MK_OP_ATTN; m.first = (pg == item.page_lo); m.last = (pg + n >= item.page_hi);
         m.layer = t.layer; m.n = static_cast<uint16_t>(n); m.row0 = pg; m.idx = static_cast<uint32_t>(it);
-        m.e = 0; m.aux = 0; m.wait_ctr = t.wait_ctr;
-        m.wait_target = t.wait_base + t.wait_per_b * static_cast<uint32_t>(p.B);
-        m.signal_ctr = t.signal_ctr; m.lo = item.page_lo; m.hi = item.page_hi;
+        m.e = 0; m.aux = 0; m.lo = item.page_lo; m.hi = item.page_hi;
         mbar_arrive_expect_tx(full(), 2u * halves * n * box);
         uint8_t* dst = slot();
         #pragma unroll 1
         for (uint32_t i = 0; i < n; ++i) {
           int32_t page = btrow[pg + i];
           if (page < 0 || page >= p.P) {
-            record_error(p, MK_ERR_DEVICE_BOUNDS, MK_OP_ATTN, t.layer, MK_NO_COUNTER, static_cast<uint32_t>(page), 0,
+            record_error(p, MK_ERR_DEVICE_BOUNDS, MK_OP_ATTN, t.layer, 0u, static_cast<uint32_t>(page), 0,
                          static_cast<int>(pg + i), false);
             page = 0;  // keep the byte count of the slot; the result is flagged invalid
           }
@@ -732,7 +716,7 @@ struct Producer {
         if ((it & 63u) == 0u) {
           if (aborted(p)) return false;
           if (globaltimer() - tw > p.watchdog_ns) {
-            record_error(p, MK_ERR_TIMEOUT, MK_OP_MOE, l, MK_NO_COUNTER, 0, 0, -1, true);
+            record_error(p, MK_ERR_TIMEOUT, MK_OP_MOE, l, MK_WAIT_ROUTE, 0, 0, -1, true);
             return false;
           }
         }
@@ -781,7 +765,6 @@ struct Producer {
           m.layer = static_cast<uint16_t>(l); m.n = static_cast<uint16_t>(n); m.row0 = f;
           m.idx = static_cast<uint32_t>(a); m.e = static_cast<uint32_t>(e);
           m.aux = lastgu | (static_cast<uint32_t>(g) << 1);
-          m.wait_ctr = MK_NO_COUNTER; m.wait_target = 0; m.signal_ctr = MK_NO_COUNTER;
           m.lo = f0; m.hi = fend;
           const uint32_t bytes = static_cast<uint32_t>(n) * H * 2u;
           const uint64_t pl = g == ng - 1 ? pol : pol_reuse;
@@ -813,7 +796,6 @@ struct Producer {
         m.last = (rb + nrc >= static_cast<int>(r1)) && (a + ne >= nact);
         m.layer = static_cast<uint16_t>(l); m.n = static_cast<uint16_t>(ne); m.row0 = static_cast<uint32_t>(rb);
         m.idx = static_cast<uint32_t>(a); m.e = 0; m.aux = static_cast<uint32_t>(nrc);
-        m.wait_ctr = MK_NO_COUNTER; m.wait_target = 0; m.signal_ctr = MK_NO_COUNTER;
         m.lo = r0; m.hi = r1;
         const uint32_t bytes = static_cast<uint32_t>(nrc) * rowb;
         mbar_arrive_expect_tx(full(), static_cast<uint32_t>(ne) * bytes);
@@ -855,7 +837,6 @@ struct Producer {
           m.kind = R_GU; m.op = MK_OP_MOE; m.first = (f == g0); m.last = (f + n >= gend);
           m.layer = static_cast<uint16_t>(l); m.n = static_cast<uint16_t>(n); m.row0 = f;
           m.idx = static_cast<uint32_t>(a); m.e = static_cast<uint32_t>(e); m.aux = 0u;   // the tile runs on
-          m.wait_ctr = MK_NO_COUNTER; m.wait_target = 0; m.signal_ctr = MK_NO_COUNTER;
           m.lo = g0; m.hi = gend;
           const uint32_t bytes = static_cast<uint32_t>(n) * H * 2u;
           mbar_arrive_expect_tx(full(), 2u * bytes);
@@ -870,7 +851,6 @@ struct Producer {
         m.layer = static_cast<uint16_t>(l); m.n = static_cast<uint16_t>(gend - g0); m.row0 = g0;
         m.idx = static_cast<uint32_t>(a); m.e = static_cast<uint32_t>(e);
         m.aux = static_cast<uint32_t>(a * F + g0 - u0);   // unit index of the chunk's first row
-        m.wait_ctr = MK_NO_COUNTER; m.wait_target = 0; m.signal_ctr = MK_NO_COUNTER;
         m.lo = g0; m.hi = gend;
         const uint32_t bytes = static_cast<uint32_t>(gend - g0) * H * 2u;
         mbar_arrive_expect_tx(full(), bytes);
@@ -890,7 +870,7 @@ struct Producer {
     Meta& m = meta();
     m.kind = kind; m.op = op; m.first = 1; m.last = 1;
     m.layer = static_cast<uint16_t>(l); m.n = 0; m.row0 = lo; m.idx = 0; m.e = 0; m.aux = 1;
-    m.wait_ctr = MK_NO_COUNTER; m.wait_target = 0; m.signal_ctr = MK_NO_COUNTER; m.lo = lo; m.hi = hi;
+    m.lo = lo; m.hi = hi;
     mbar_arrive(full());
     ++c;
     return true;
@@ -1139,7 +1119,7 @@ struct Consumer {
       int tok = __ldg(p.tokens + b);
       if (tok < 0 || tok >= p.V) {
         if (threadIdx.x == 0)
-          record_error(p, MK_ERR_DEVICE_BOUNDS, MK_OP_EMBED, -1, MK_NO_COUNTER, static_cast<uint32_t>(tok), 0, b,
+          record_error(p, MK_ERR_DEVICE_BOUNDS, MK_OP_EMBED, -1, 0u, static_cast<uint32_t>(tok), 0, b,
                        false);
         tok = 0;
       }
@@ -2367,7 +2347,7 @@ struct Consumer {
           p.kv[vb + d] = kvcur[D + d];
         }
       } else if (threadIdx.x == 0) {
-        record_error(p, MK_ERR_DEVICE_BOUNDS, MK_OP_ATTN, l, MK_NO_COUNTER, static_cast<uint32_t>(page), 0, pg,
+        record_error(p, MK_ERR_DEVICE_BOUNDS, MK_OP_ATTN, l, 0u, static_cast<uint32_t>(page), 0, pg,
                      false);
       }
     }
@@ -2724,13 +2704,13 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
       }
     }
     __threadfence();
-    const uint32_t old = atom_add_acq_rel(p.ctr + C_FINISH, 1u);
+    const uint32_t old = atom_add_acq_rel(p.flags + F_FINISH, 1u);
     S.is_last = (old + 1u == gridDim.x) ? 1 : 0;
   }
   __syncthreads();
   if (S.is_last) {
     #pragma unroll 1
-    for (uint32_t i = tid; i < p.cm.total; i += kThreads) p.ctr[i] = 0u;
+    for (uint32_t i = tid; i < kStepFlags; i += kThreads) p.flags[i] = 0u;
     // Greedy selection, second level: every other block has finished (their partials are
     // ordered before their arrivals on the finish counter, which this block acquired); a warp
     // per row of the batch merges the blocks' partials, read through L2.

@@ -1,6 +1,6 @@
 // mk_layout.h -- layout shared by the host library and the persistent kernel:
-// geometry of the shared-memory ring, tile sizes, the counter map and the
-// kernel's parameter block.  Plain C++ (no CUDA types) so both g++ and nvcc
+// geometry of the shared-memory ring, tile sizes, the MoE work split, the step
+// flags and the kernel's parameter block.  Plain C++ (no CUDA types) so both g++ and nvcc
 // compile it.
 #pragma once
 
@@ -111,33 +111,11 @@ MK_HD int32_t moe_gu_start(int j, int N, const I* cum, const I* cost, int nact, 
   return f >= static_cast<uint32_t>(F) ? (lo + 1) * F : lo * F + static_cast<int32_t>(f);
 }
 
-// ---- counters --------------------------------------------------------------------
-// global
-enum : uint32_t { C_EMBED = 0, C_FINISH = 1, C_ABORT = 2, C_NEVER = 3, C_GLOBAL = 8 };
-// per layer, at layer_base(l) + ...
-enum : uint32_t {
-  L_QKV = 0,     // QKV tiles done
-  L_ATTN = 1,    // (row, kv head) attention pairs combined
-  L_O = 2,       // O-proj tiles done
-  L_RARR = 3,    // router tiles arrived
-  L_RREADY = 4,  // routing published (0/1)
-  L_GU = 5,      // blocks done with their gate/up units
-  L_MOE = 6,     // blocks done with their down rows (residual written)
-  L_PAIR = 8     // [max_batch * Hkv] attention split arrivals
-};
-
-struct CounterMap {
-  uint32_t layer_stride;
-  uint32_t total;
-  MK_HD uint32_t layer_base(int l) const { return C_GLOBAL + (uint32_t)l * layer_stride; }
-};
-
-inline CounterMap counter_map(int layers, int max_batch, int n_kv) {
-  CounterMap m;
-  m.layer_stride = (L_PAIR + (uint32_t)(max_batch * n_kv) + 7u) & ~7u;
-  m.total = C_GLOBAL + (uint32_t)layers * m.layer_stride;
-  return m;
-}
+// ---- step flags ------------------------------------------------------------------
+// The only words of the step that are not tagged data: the abort flag (set by the block that
+// records an error, polled by every wait) and the count of blocks that have finished (the
+// last one clears both for the next step and merges the greedy selection).
+enum : uint32_t { F_FINISH = 1, F_ABORT = 2, kStepFlags = 8 };
 
 // ---- kernel parameters -------------------------------------------------------------
 struct LayerW {
@@ -164,7 +142,6 @@ struct alignas(64) Params {
   int32_t B, max_batch, n_ctas, max_items;
   // static plan
   int32_t n_qkv_tiles, n_o_tiles, n_router_tiles;
-  CounterMap cm;
   uint64_t watchdog_ns;
   const mk_task* tasks;
   const int32_t* task_off;      // [n_ctas + 1]
@@ -205,7 +182,7 @@ struct alignas(64) Params {
   float* argp;          // [n_ctas][max_batch][4] per-block (max, second, index bits) of its LM-head rows
   int32_t* RIDS;   // [L][max_batch][K] routing ids (copy kept by block 0 for inspection)
   float* RW;       // [L][max_batch][K] combine weights (same)
-  uint32_t* ctr;   // [cm.total]
+  uint32_t* flags; // [kStepFlags] abort flag, finish count
   mk_status* status;
   // optional timeline: per block `trace_cap` events of 4 x u64 (start, dependency met, end, tag);
   // event 0 of each block holds (consumer events, kernel start, producer events, 0)

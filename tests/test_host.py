@@ -1,7 +1,9 @@
 """Host-side tests of the CUDA library (no GPU needed): it loads and exports every
 symbol the headers declare, rejects bad arguments before any launch, builds
 plans that cover every tile exactly once in a dependency-respecting order, and
-its task graph runs to completion without deadlock in the CPU simulator."""
+its data dependencies -- each record waiting for the writer tiles of exactly the
+tagged words the device reads there -- run to completion without deadlock in the
+CPU simulator."""
 import ctypes
 import os
 import re
@@ -170,7 +172,7 @@ def test_simulated_step_completes_tiny(seed):
     lens = [65, 1, 300, 17, 16, 512, 2, 90][: 1 + seed % 8]
     r = mk.simulate(cfg, N_CTAS if seed % 2 else 5, lens, _random_routing(cfg, len(lens), seed), seed=seed,
                     lead=1 + seed % 6)
-    assert r.finished and not r.deadlocked and r.counters_ok and r.moe_units_ok
+    assert r.finished and not r.deadlocked and r.writes_ok and r.moe_units_ok
 
 
 def test_simulated_step_completes_30b_shapes():
@@ -178,7 +180,7 @@ def test_simulated_step_completes_30b_shapes():
     for B, seed in ((1, 1), (64, 2)):
         lens = W.lengths_loguniform(B, 512, 32768) if B > 1 else [8193]
         r = mk.simulate(cfg, N_CTAS, lens, _random_routing(cfg, B, seed), seed=seed, lead=6)
-        assert r.finished and not r.deadlocked and r.counters_ok and r.moe_units_ok
+        assert r.finished and not r.deadlocked and r.writes_ok and r.moe_units_ok
         # every attention item ran
         assert r.tiles_run[3] == len(mk.plan_attention(cfg, N_CTAS, lens)[0]) * cfg.num_layers
 
@@ -192,7 +194,7 @@ def test_simulated_moe_paths(B, flags):
     for seed in range(3):
         lens = [8193, 700, 33][:B]
         r = mk.simulate(cfg, N_CTAS, lens, _random_routing(cfg, B, seed), seed=seed, lead=1 + seed)
-        assert r.finished and not r.deadlocked and r.counters_ok and r.moe_units_ok
+        assert r.finished and not r.deadlocked and r.writes_ok and r.moe_units_ok
 
 
 @pytest.mark.parametrize("B", [3, 7, 16])
@@ -204,7 +206,7 @@ def test_simulated_wide_batches_hidden_4096(B):
     rng = np.random.default_rng(B)
     lens = [int(x) for x in rng.integers(1, 2000, B)]
     r = mk.simulate(cfg, N_CTAS, lens, _random_routing(cfg, B, B), seed=B, lead=3)
-    assert r.finished and not r.deadlocked and r.counters_ok and r.moe_units_ok
+    assert r.finished and not r.deadlocked and r.writes_ok and r.moe_units_ok
 
 
 def test_router_tiles_follow_engine_width():
@@ -217,8 +219,9 @@ def test_router_tiles_follow_engine_width():
 @pytest.mark.parametrize("seed", range(24))
 def test_simulated_step_random_shapes(seed):
     # random widths, expert counts, top-k, head geometry, page sizes, batches (1-64), grid sizes
-    # and Zipf-skewed routing: the dependency graph finishes without deadlock, every counter
-    # reaches its target and every MoE unit and down-projection element is covered once
+    # and Zipf-skewed routing: the dependency graph finishes without deadlock, every tile that
+    # writes data another SM reads runs exactly once and every MoE unit and down-projection
+    # element is covered once
     rng = np.random.default_rng(1000 + seed)
     E = int(rng.choice([8, 32, 128]))
     K = min(int(rng.choice([1, 2, 4, 8])), E)
@@ -235,7 +238,7 @@ def test_simulated_step_random_shapes(seed):
     ids = np.stack([np.stack([perm[rng.choice(E, K, replace=False, p=pop / pop.sum())] for _ in range(B)])
                     for _ in range(m["layers"])]).astype(np.int32)
     r = mk.simulate(cfg, int(rng.choice([7, 33, 152])), lens, ids, seed=seed, lead=int(rng.integers(1, 7)))
-    assert r.finished and not r.deadlocked and r.counters_ok and r.moe_units_ok
+    assert r.finished and not r.deadlocked and r.writes_ok and r.moe_units_ok
 
 
 def test_config_flags_are_checked():
