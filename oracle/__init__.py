@@ -51,7 +51,7 @@ def build(force: bool = False) -> str:
 class Dims(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "layers", "hidden", "n_q", "n_kv", "head_dim", "n_exp", "top_k", "ffn", "vocab",
-        "page_size", "num_pages", "max_pages_per_seq", "norm_topk", "reserved")] + [
+        "page_size", "num_pages", "max_pages_per_seq", "norm_topk", "kv_q8")] + [
         ("rope_theta", ctypes.c_double), ("rms_eps", ctypes.c_double)]
 
 
@@ -81,6 +81,11 @@ def _bind(lib):
     lib.orc_f32_to_bf16.restype = ctypes.c_uint16
     lib.orc_bf16_to_f32.argtypes = [ctypes.c_uint16]
     lib.orc_bf16_to_f32.restype = ctypes.c_float
+    lib.orc_f32_to_f16.argtypes = [ctypes.c_float]
+    lib.orc_f32_to_f16.restype = ctypes.c_uint16
+    lib.orc_f16_to_f32.argtypes = [ctypes.c_uint16]
+    lib.orc_f16_to_f32.restype = ctypes.c_float
+    lib.orc_q8_quantize.argtypes = [i32, vp, vp, vp]
     return lib
 
 
@@ -106,12 +111,15 @@ def _u16(a):
     return a.view(np.uint16) if a.dtype != np.uint16 else a
 
 
-def make_dims(model: dict, page_size: int, num_pages: int, max_pages_per_seq: int) -> Dims:
+def make_dims(model: dict, page_size: int, num_pages: int, max_pages_per_seq: int, kv_q8: bool = False) -> Dims:
+    """Shape of a step; ``kv_q8`` selects the q8_0 cache (per layer: int8 code plane
+    [pages][2][Hkv][page_size][D], then f16 scale plane [pages][2][Hkv][page_size][D/32])."""
     d = Dims()
     for k in ("layers", "hidden", "n_q", "n_kv", "head_dim", "n_exp", "top_k", "ffn", "vocab"):
         setattr(d, k, int(model[k]))
     d.page_size, d.num_pages, d.max_pages_per_seq = int(page_size), int(num_pages), int(max_pages_per_seq)
     d.norm_topk = int(model.get("norm_topk", 1))
+    d.kv_q8 = 1 if kv_q8 else 0
     d.rope_theta = float(model["rope_theta"])
     d.rms_eps = float(model["rms_eps"])
     return d
@@ -164,6 +172,21 @@ class Oracle:
     def f32_to_bf16(self, f):
         return int(self.lib.orc_f32_to_bf16(float(f)))
 
+    def f32_to_f16(self, f):
+        return int(self.lib.orc_f32_to_f16(float(f)))
+
+    def f16_to_f32(self, h):
+        return float(self.lib.orc_f16_to_f32(int(h)))
+
+    def q8_quantize(self, x):
+        """q8_0 blocks of ``x`` (fp32, length a multiple of 32): (int8 codes, f16 scale bits)."""
+        x = np.ascontiguousarray(x, dtype=np.float32).ravel()
+        n = x.size // 32
+        q = np.empty(n * 32, dtype=np.int8)
+        d = np.empty(n, dtype=np.uint16)
+        self.lib.orc_q8_quantize(n, _p(x), _p(q), _p(d))
+        return q, d
+
     # ---- whole step, all weights on the host -------------------------------
     @staticmethod
     def _layer_struct(lw: dict, keep: list) -> Layer:
@@ -182,13 +205,14 @@ class Oracle:
         return L
 
     def decode_step(self, dims: Dims, weights: dict, tokens, seq_lens, block_tables, kv):
-        """One decode step.  ``kv`` (uint16 bf16 bits, [L][P][2][Hkv][ps][D]) is updated in place."""
+        """One decode step.  ``kv`` is updated in place: uint16 bf16 bits [L][P][2][Hkv][ps][D], or
+        with ``dims.kv_q8`` a uint8 array holding each layer's q8_0 planes one after the other."""
         keep = []
         layers = (Layer * dims.layers)(*[self._layer_struct(lw, keep) for lw in weights["layers"]])
         tok = np.ascontiguousarray(tokens, dtype=np.int32)
         sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
         bt = np.ascontiguousarray(block_tables, dtype=np.int32)
-        assert kv.dtype == np.uint16 and kv.flags.c_contiguous
+        assert kv.dtype == (np.uint8 if dims.kv_q8 else np.uint16) and kv.flags.c_contiguous
         emb, fn, head = _u16(weights["embed"]), _u16(weights["final_norm"]), _u16(weights["lm_head"])
         B = tok.size
         logits = np.empty((B, dims.vocab), dtype=self.dt)
@@ -244,7 +268,7 @@ class Oracle:
             keep = []
             L = self._layer_struct(fetch.layer(l), keep)
             kv = fetch.kv_layer(l)
-            assert kv.dtype == np.uint16 and kv.flags.c_contiguous
+            assert kv.dtype == (np.uint8 if dims.kv_q8 else np.uint16) and kv.flags.c_contiguous
             rc = self._fn("attn_block")(ctypes.byref(dims), ctypes.byref(L), B, _p(x), _p(sl), _p(bt), _p(kv),
                                         None, None, 1)
             if rc != 0:

@@ -31,6 +31,18 @@
 //   weights renormalised over the k selected experts; silu(a) = a/(1+exp(-a));
 //   the combine sums the k slots in rank order.
 //
+// Reduced-byte KV cache (dims.kv_q8 = 1; the Kinetic engine's pages, the
+// --cache-type-k/v option and the paragraph on the quantized cache: keys and
+// values kept as blocks of 32 int8 values with one f16 scale, 34 bytes where
+// f16 takes 64, outputs close to but not equal to the full-precision cache's).
+// The pages give no quantizer; the plain symmetric one is taken: per block of
+// 32 consecutive values of one K or V row (along head_dim), d = max|x| / 127
+// in fp32, stored rounded to f16 (nearest, ties to even); code q = x * (1/d)
+// rounded to the nearest integer, ties away from zero (|q| <= 127); a block of
+// zeros has d = 0 and codes 0.  A cached value reads back as q * d (exact in
+// fp32).  Per layer the cache is a code plane [pages][2][Hkv][page_size][D]
+// int8 followed by a scale plane [pages][2][Hkv][page_size][D/32] f16.
+//
 // Accumulation: every dot product and sum runs in ascending index order in
 // the template type T.  The *_f32 entry points are the parity reference
 // (fp32, as fixed by the problem statement); the *_f64 entry points run the
@@ -46,7 +58,7 @@ extern "C" {
 
 struct orc_dims {
   int32_t layers, hidden, n_q, n_kv, head_dim, n_exp, top_k, ffn, vocab;
-  int32_t page_size, num_pages, max_pages_per_seq, norm_topk, reserved;
+  int32_t page_size, num_pages, max_pages_per_seq, norm_topk, kv_q8;   // kv_q8: 0 bf16 cache, 1 q8_0 cache
   double rope_theta, rms_eps;
 };
 
@@ -80,6 +92,59 @@ inline uint16_t f32_to_bf16(float f) {
   uint32_t lsb = (bits >> 16) & 1u;
   bits += 0x7fffu + lsb;
   return static_cast<uint16_t>(bits >> 16);
+}
+
+// fp32 -> IEEE binary16, round to nearest, ties to even (subnormals and overflow to inf handled).
+inline uint16_t f32_to_f16(float f) {
+  uint32_t x;
+  std::memcpy(&x, &f, 4);
+  const uint32_t sign = (x >> 16) & 0x8000u;
+  const uint32_t ax = x & 0x7fffffffu;
+  if (ax >= 0x7f800000u) return static_cast<uint16_t>(sign | (ax > 0x7f800000u ? 0x7e00u : 0x7c00u));
+  const int e = static_cast<int>(ax >> 23) - 127;     // unbiased exponent
+  if (e > 15) return static_cast<uint16_t>(sign | 0x7c00u);
+  uint32_t mant = (ax & 0x7fffffu) | 0x800000u;       // 24-bit significand with the hidden bit
+  int shift;                                          // bits of the 24-bit significand dropped
+  uint32_t base;                                      // exponent field of the result
+  if (e >= -14) { shift = 13; base = static_cast<uint32_t>(e + 15) << 10; mant &= 0x7fffffu; mant |= 0x800000u; }
+  else {
+    if (e < -25) return static_cast<uint16_t>(sign);  // below half the smallest subnormal
+    shift = 13 + (-14 - e);
+    base = 0;
+  }
+  uint32_t q = mant >> shift;
+  const uint32_t rem = mant & ((1u << shift) - 1u), half = 1u << (shift - 1);
+  if (rem > half || (rem == half && (q & 1u))) ++q;
+  // normal: q holds the hidden bit at 2^10; adding base - (1 << 10) keeps a carry into the exponent
+  const uint32_t h = e >= -14 ? base + q - 0x400u : q;
+  return static_cast<uint16_t>(sign | h);
+}
+
+inline float f16_to_f32(uint16_t h) {
+  const uint32_t sign = static_cast<uint32_t>(h & 0x8000u) << 16;
+  const uint32_t ex = (h >> 10) & 0x1fu, man = h & 0x3ffu;
+  float f;
+  if (ex == 0) {
+    f = std::ldexp(static_cast<float>(man), -24);   // zero or subnormal: man * 2^-24
+    uint32_t b;
+    std::memcpy(&b, &f, 4);
+    b |= sign;
+    std::memcpy(&f, &b, 4);
+    return f;
+  }
+  uint32_t b = ex == 31 ? (sign | 0x7f800000u | (man << 13)) : (sign | ((ex + 112u) << 23) | (man << 13));
+  std::memcpy(&f, &b, 4);
+  return f;
+}
+
+// One q8_0 block: 32 fp32 values -> 32 codes and the f16 scale (see the reading above).
+inline void q8_quantize_block(const float* x, int8_t* q, uint16_t* d_f16) {
+  float amax = 0.f;
+  for (int i = 0; i < 32; ++i) amax = std::fabs(x[i]) > amax ? std::fabs(x[i]) : amax;
+  const float d = amax / 127.0f;
+  const float id = d != 0.f ? 1.0f / d : 0.f;
+  for (int i = 0; i < 32; ++i) q[i] = static_cast<int8_t>(std::round(x[i] * id));
+  *d_f16 = f32_to_f16(d);
 }
 
 template <typename T> inline T texp(T v);
@@ -149,9 +214,47 @@ void topk(int n, int k, const T* r, int32_t* ids) {
 }
 
 inline size_t kv_offset(const orc_dims& d, int page, int which, int kvh, int slot) {
-  // per-layer cache layout [num_pages][2 (K,V)][Hkv][page_size][D]
+  // per-layer cache layout [num_pages][2 (K,V)][Hkv][page_size][D] (elements of the bf16 cache,
+  // codes of the q8_0 cache)
   return ((((static_cast<size_t>(page) * 2 + which) * d.n_kv + kvh) * d.page_size + slot) * d.head_dim);
 }
+
+// Bytes of one layer of the cache.
+inline size_t kv_layer_bytes(const orc_dims& d) {
+  const size_t n = static_cast<size_t>(d.num_pages) * 2 * d.n_kv * d.page_size * d.head_dim;
+  return d.kv_q8 ? n + n / 32 * 2 : n * 2;
+}
+
+// One layer of the cache, in either format: rows are written from fp32 values (rounded to bf16,
+// or quantized block by block) and read back element by element as fp32.
+struct KvLayer {
+  const orc_dims& d;
+  uint16_t* bf = nullptr;     // bf16 cache
+  int8_t* codes = nullptr;    // q8_0 code plane
+  uint16_t* scales = nullptr; // q8_0 scale plane (f16 bits)
+  KvLayer(const orc_dims& d_, void* base) : d(d_) {
+    if (d.kv_q8) {
+      codes = static_cast<int8_t*>(base);
+      scales = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(base) +
+                                           static_cast<size_t>(d.num_pages) * 2 * d.n_kv * d.page_size * d.head_dim);
+    } else {
+      bf = static_cast<uint16_t*>(base);
+    }
+  }
+  float get(int page, int which, int kvh, int slot, int i) const {
+    const size_t o = kv_offset(d, page, which, kvh, slot);
+    if (bf) return bf16_to_f32(bf[o + i]);
+    return static_cast<float>(codes[o + i]) * f16_to_f32(scales[o / 32 + i / 32]);
+  }
+  void put(int page, int which, int kvh, int slot, const float* v) {
+    const size_t o = kv_offset(d, page, which, kvh, slot);
+    if (bf) {
+      for (int i = 0; i < d.head_dim; ++i) bf[o + i] = f32_to_bf16(v[i]);
+      return;
+    }
+    for (int b = 0; b < d.head_dim / 32; ++b) q8_quantize_block(v + 32 * b, codes + o + 32 * b, scales + o / 32 + b);
+  }
+};
 
 // append = false: the cache already holds the current token's k and v at position
 // seq_len-1 (codes another implementation wrote); they are read, not recomputed, so a check
@@ -160,6 +263,9 @@ template <typename T>
 int attn_block(const orc_dims& d, const orc_layer& w, int B, T* x, const int32_t* seq_lens,
                const int32_t* bt, uint16_t* kv, T* trace_qkv, T* trace_attn, bool append = true) {
   const int H = d.hidden, D = d.head_dim, Hq = d.n_q, Hkv = d.n_kv, G = Hq / Hkv;
+  if (d.kv_q8 && D % 32) return -4;
+  KvLayer cache(d, kv);
+  std::vector<float> row(D);
   const int NQKV = (Hq + 2 * Hkv) * D;
   const T scale = static_cast<T>(1) / tsqrt<T>(static_cast<T>(D));
   std::vector<T> y(H), qkv(NQKV), attn(static_cast<size_t>(Hq) * D), o(H);
@@ -173,18 +279,17 @@ int attn_block(const orc_dims& d, const orc_layer& w, int B, T* x, const int32_t
     gemv<T>(NQKV, H, w.w_qkv, y.data(), qkv.data());
     if (trace_qkv) std::memcpy(trace_qkv + static_cast<size_t>(b) * NQKV, qkv.data(), sizeof(T) * NQKV);
     for (int h = 0; h < Hq + Hkv; ++h) rope<T>(D, pos, d.rope_theta, qkv.data() + static_cast<size_t>(h) * D);
-    // append the current token's k and v to the cache (bf16, RNE)
+    // append the current token's k and v to the cache (rounded to bf16, or quantized to q8_0, from
+    // their fp32 values)
     const int page = tab[pos / d.page_size], slot = pos % d.page_size;
     if (page < 0 || page >= d.num_pages) return -2;
     for (int g = 0; g < Hkv && append; ++g) {
       const T* kg = qkv.data() + static_cast<size_t>(Hq + g) * D;
       const T* vg = qkv.data() + static_cast<size_t>(Hq + Hkv + g) * D;
-      uint16_t* kd = kv + kv_offset(d, page, 0, g, slot);
-      uint16_t* vd = kv + kv_offset(d, page, 1, g, slot);
-      for (int i = 0; i < D; ++i) {
-        kd[i] = f32_to_bf16(static_cast<float>(kg[i]));
-        vd[i] = f32_to_bf16(static_cast<float>(vg[i]));
-      }
+      for (int i = 0; i < D; ++i) row[i] = static_cast<float>(kg[i]);
+      cache.put(page, 0, g, slot, row.data());
+      for (int i = 0; i < D; ++i) row[i] = static_cast<float>(vg[i]);
+      cache.put(page, 1, g, slot, row.data());
     }
     // attention: every q head over positions 0..Lc-1, read from the paged cache
 #pragma omp parallel for schedule(static) if (static_cast<long>(Lc) * Hq > 4096)
@@ -193,9 +298,9 @@ int attn_block(const orc_dims& d, const orc_layer& w, int B, T* x, const int32_t
       const T* q = qkv.data() + static_cast<size_t>(h) * D;
       std::vector<T> s(Lc), acc(D, static_cast<T>(0));
       for (int t = 0; t < Lc; ++t) {
-        const uint16_t* kr = kv + kv_offset(d, tab[t / d.page_size], 0, g, t % d.page_size);
+        const int pg = tab[t / d.page_size], sl = t % d.page_size;
         T dot = 0;
-        for (int i = 0; i < D; ++i) dot += q[i] * static_cast<T>(bf16_to_f32(kr[i]));
+        for (int i = 0; i < D; ++i) dot += q[i] * static_cast<T>(cache.get(pg, 0, g, sl, i));
         s[t] = dot * scale;
       }
       T m = s[0];
@@ -203,8 +308,8 @@ int attn_block(const orc_dims& d, const orc_layer& w, int B, T* x, const int32_t
       T l = 0;
       for (int t = 0; t < Lc; ++t) { s[t] = texp<T>(s[t] - m); l += s[t]; }
       for (int t = 0; t < Lc; ++t) {
-        const uint16_t* vr = kv + kv_offset(d, tab[t / d.page_size], 1, g, t % d.page_size);
-        for (int i = 0; i < D; ++i) acc[i] += s[t] * static_cast<T>(bf16_to_f32(vr[i]));
+        const int pg = tab[t / d.page_size], sl = t % d.page_size;
+        for (int i = 0; i < D; ++i) acc[i] += s[t] * static_cast<T>(cache.get(pg, 1, g, sl, i));
       }
       for (int i = 0; i < D; ++i) attn[static_cast<size_t>(h) * D + i] = acc[i] / l;
     }
@@ -293,10 +398,11 @@ int decode_step(const orc_dims& d, const uint16_t* emb, const orc_layer* layers,
   std::vector<int32_t> ids(static_cast<size_t>(B) * K);
   std::vector<const uint16_t*> gu(static_cast<size_t>(B) * K), dn(static_cast<size_t>(B) * K);
   embed<T>(d, emb, B, tokens, x.data());
-  const size_t layer_kv = static_cast<size_t>(d.num_pages) * 2 * d.n_kv * d.page_size * d.head_dim;
+  const size_t layer_bytes = kv_layer_bytes(d);
   for (int l = 0; l < d.layers; ++l) {
     const orc_layer& w = layers[l];
-    int rc = attn_block<T>(d, w, B, x.data(), seq_lens, bt, kv + l * layer_kv, nullptr, nullptr);
+    uint16_t* kvl = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(kv) + l * layer_bytes);
+    int rc = attn_block<T>(d, w, B, x.data(), seq_lens, bt, kvl, nullptr, nullptr);
     if (rc) return rc;
     route<T>(d, w, B, x.data(), y.data(), r.data(), ids.data(), wts.data());
     for (size_t s = 0; s < gu.size(); ++s) {
@@ -315,6 +421,12 @@ extern "C" {
 
 uint16_t orc_f32_to_bf16(float f) { return f32_to_bf16(f); }
 float orc_bf16_to_f32(uint16_t u) { return bf16_to_f32(u); }
+uint16_t orc_f32_to_f16(float f) { return f32_to_f16(f); }
+float orc_f16_to_f32(uint16_t h) { return f16_to_f32(h); }
+// n blocks of 32 values -> n * 32 codes and n f16 scales
+void orc_q8_quantize(int n, const float* x, int8_t* q, uint16_t* d) {
+  for (int b = 0; b < n; ++b) q8_quantize_block(x + 32 * b, q + 32 * b, d + b);
+}
 
 #define ORC_EXPORT_ALL(SUF, T)                                                                                     \
   void orc_gemv_##SUF(int rows, int cols, const uint16_t* W, const T* x, T* y) { gemv<T>(rows, cols, W, x, y); }  \

@@ -33,6 +33,24 @@ def round_bf16(x):
     return bf16_to_f64(bits.astype(np.uint16))
 
 
+def round_q8(x):
+    """float -> float32 -> q8_0 blocks of 32 along the last axis -> float64.  The cache reading of
+    the Kinetic pages' quantized cache: per block d = max|x| / 127 in float32, kept as IEEE half
+    (numpy's conversion); codes x * (1/d) in float32, rounded to the nearest integer with ties away
+    from zero; a value reads back as code * d."""
+    f = np.asarray(x, dtype=np.float32)
+    shp = f.shape
+    b = f.reshape(shp[:-1] + (shp[-1] // 32, 32))
+    amax = np.abs(b).max(axis=-1, keepdims=True)
+    d = (amax / np.float32(127)).astype(np.float32)
+    safe = np.where(d != 0, d, np.float32(1)).astype(np.float32)
+    inv = np.where(d != 0, np.float32(1) / safe, np.float32(0)).astype(np.float32)
+    v = (b * inv).astype(np.float32).astype(np.float64)
+    t = np.trunc(v)
+    q = np.where(np.abs(v - t) >= 0.5, t + np.sign(v), t)
+    return (q * d.astype(np.float16).astype(np.float64)).reshape(shp)
+
+
 def _rms(x, g, eps):
     return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps) * g
 
@@ -56,8 +74,10 @@ def _silu(a):
     return a / (1.0 + np.exp(-a))
 
 
-def forward_sequence(model: dict, w: dict, tokens, mlp: str = "moe", router_bias=None):
-    """Logits [T, V] for every position of ``tokens`` (causal)."""
+def forward_sequence(model: dict, w: dict, tokens, mlp: str = "moe", router_bias=None, kv_round: str = "bf16"):
+    """Logits [T, V] for every position of ``tokens`` (causal).  ``kv_round`` is how cached keys
+    and values are stored: "bf16" or "q8" (q8_0 blocks along head_dim)."""
+    rnd = round_bf16 if kv_round == "bf16" else round_q8
     H, D, Hq, Hkv = model["hidden"], model["head_dim"], model["n_q"], model["n_kv"]
     E, K, F = model["n_exp"], model["top_k"], model["ffn"]
     eps, theta = model["rms_eps"], model["rope_theta"]
@@ -75,8 +95,8 @@ def forward_sequence(model: dict, w: dict, tokens, mlp: str = "moe", router_bias
         k = qkv[:, Hq * D:(Hq + Hkv) * D].reshape(T, Hkv, D)
         v = qkv[:, (Hq + Hkv) * D:].reshape(T, Hkv, D)
         q = _rotate(q, cos, sin)
-        k = round_bf16(_rotate(k, cos, sin))
-        v = round_bf16(v)
+        k = rnd(_rotate(k, cos, sin))
+        v = rnd(v)
         o = np.empty((T, Hq, D))
         for h in range(Hq):
             s = (q[:, h, :] @ k[:, h // G, :].T) / np.sqrt(D)

@@ -87,10 +87,12 @@ class DeviceFetch:
     k of the pool being the k-th page of the selected rows in row order, with block
     tables ``self.bt`` that address it."""
 
-    def __init__(self, w_dev: dict, kv_dev, bt_np, seq_lens, rows, page_size):
+    def __init__(self, w_dev: dict, kv_dev, bt_np, seq_lens, rows, page_size, model=None, num_pages=None):
         self.w, self.kv = w_dev, kv_dev
         self.rows = list(rows)
         ps = page_size
+        self.page_size = ps
+        self.model_for_q8, self.kv_num_pages = model, num_pages   # needed to split a q8_0 pool's planes
         pages = []
         for b in self.rows:
             n = (int(seq_lens[b]) + ps - 1) // ps
@@ -121,6 +123,12 @@ class DeviceFetch:
         return W.bf16_bits(lw["w_gate_up"][e]), W.bf16_bits(lw["w_down"][e])
 
     def kv_layer(self, l):
+        if self.kv.dtype == torch.uint8:   # q8_0 pool: compact the code plane and the scale plane alike
+            m = self.model_for_q8
+            codes, scales = W.kv_q8_planes(self.kv[l], m, self.kv_num_pages, self.page_size)
+            c = codes.index_select(0, self.page_ids).contiguous().view(torch.uint8).reshape(-1)
+            d = scales.index_select(0, self.page_ids).contiguous().view(torch.uint8).reshape(-1)
+            return torch.cat([c, d]).cpu().numpy()
         return W.bf16_bits(self.kv[l].index_select(0, self.page_ids))
 
     def final(self):

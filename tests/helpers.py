@@ -20,8 +20,10 @@ def np_weights(w: dict) -> dict:
     return out
 
 
-def tiny_setup(model: dict, lengths, page_size: int = 16, extra_pages: int = 0, seed_tokens: int = 11):
-    """Tiny model + a paged cache whose prefix is filled by teacher-forced oracle steps.
+def tiny_setup(model: dict, lengths, page_size: int = 16, extra_pages: int = 0, seed_tokens: int = 11,
+               kv_q8: bool = False):
+    """Tiny model + a paged cache whose prefix is filled by teacher-forced oracle steps
+    (``kv_q8``: a q8_0 cache, uint8 [L][layer_bytes], quantized by the oracle as it writes).
 
     Each row b gets ``lengths[b]-1`` random prefix tokens (seeded) decoded one at a
     time by the fp32 oracle; the row's next token is its last drawn token.  Returns
@@ -34,10 +36,13 @@ def tiny_setup(model: dict, lengths, page_size: int = 16, extra_pages: int = 0, 
     wt = W.make_weights(model, "cpu")
     wn = np_weights(wt)
     bt, free = W.make_block_tables(lengths, page_size, num_pages, max_pages)
-    kv = np.zeros(W.kv_shape(model, num_pages, page_size), dtype=np.uint16)
+    if kv_q8:
+        kv = np.zeros((model["layers"], W.kv_q8_layer_bytes(model, num_pages, page_size)), dtype=np.uint8)
+    else:
+        kv = np.zeros(W.kv_shape(model, num_pages, page_size), dtype=np.uint16)
     g = torch.Generator().manual_seed(seed_tokens)
     seqs = [torch.randint(0, model["vocab"], (L,), generator=g).numpy().astype(np.int32) for L in lengths]
-    dims = make_dims(model, page_size, num_pages, max_pages)
+    dims = make_dims(model, page_size, num_pages, max_pages, kv_q8=kv_q8)
     orc = Oracle("f32")
     # prefill: step t decodes token seqs[b][t] at seq_len t+1 for every row still in its prefix
     Tmax = max(lengths)
@@ -51,7 +56,7 @@ def tiny_setup(model: dict, lengths, page_size: int = 16, extra_pages: int = 0, 
     tokens = np.array([seqs[b][lengths[b] - 1] for b in range(B)], dtype=np.int32)
     return dict(model=model, wt=wt, wn=wn, dims=dims, tokens=tokens, seq_lens=np.array(lengths, dtype=np.int32),
                 bt=bt.numpy(), kv=kv, free=free, num_pages=num_pages, max_pages=max_pages, page_size=page_size,
-                seqs=seqs)
+                seqs=seqs, kv_q8=kv_q8)
 
 
 def rel_l2(a, b):

@@ -152,3 +152,38 @@ def test_planted_layer_mixup_in_fetch_is_caught(orc):
 
     bad = orc.decode_step_lazy(dims, Mixed(s["wn"], s["kv"]), s["tokens"], s["lens"], s["bt"])
     assert rel_l2(bad, ref) > 1e-3
+
+
+@pytest.mark.parametrize("name", ["tiny", "medium"])
+def test_drivers_bit_identical_on_the_q8_cache(orc, name):
+    # the same three drivers over a q8_0 cache: the compacting fetch moves the code plane and the
+    # scale plane of the pages it keeps
+    model = W.TINY if name == "tiny" else MEDIUM
+    m = dict(model)
+    B, ps = 3, 16
+    wt = W.make_weights(m, "cpu")
+    wn = np_weights(wt)
+    lens = W.lengths_uniform(B, 1, 300, seed=41)
+    max_pages = max((L + ps - 1) // ps for L in lens)
+    P = W.pages_needed(lens, ps) + 5
+    bt = W.make_block_tables(lens, ps, P, max_pages, seed=42)[0].numpy()
+    kv_t = W.make_kv_q8_random(m, P, ps, "cpu", seed=43, used_pages=[int(p) for p in bt.flatten() if p >= 0])
+    kv = kv_t.numpy().copy()
+    tokens = W.make_tokens(B, m["vocab"], seed=44).numpy()
+    sl = np.array(lens, np.int32)
+    dims = make_dims(m, ps, P, max_pages, kv_q8=True)
+    ref = orc.decode_step(dims, wn, tokens, sl, bt, kv.copy())
+    lazy = orc.decode_step_lazy(dims, HostFetch(wn, kv), tokens, sl, bt)
+    assert np.array_equal(lazy.view(np.uint32), ref.view(np.uint32))
+    rows = [2, 0]
+    fetch = DeviceFetch(wt, kv_t, bt, sl, rows, ps, model=m, num_pages=P)
+    dsub = make_dims(m, ps, fetch.num_pages, fetch.max_pages, kv_q8=True)
+    sub = orc.decode_step_lazy(dsub, fetch, tokens[rows], sl[rows], fetch.bt)
+    assert np.array_equal(sub.view(np.uint32), ref[rows].view(np.uint32))
+    x = (wn["embed"][tokens].astype(np.uint32) << 16).view(np.float32)
+    kvc = kv.copy()
+    for l in range(m["layers"]):
+        kvl = np.ascontiguousarray(kvc[l])
+        x = orc.layer_trace(dims, wn["layers"][l], x, sl, bt, kvl)["x_out"]
+    chain = orc.final(dims, wn["final_norm"], wn["lm_head"], x)
+    assert np.array_equal(chain.view(np.uint32), ref.view(np.uint32))

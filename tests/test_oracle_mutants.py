@@ -26,10 +26,9 @@ MUTANTS = [
     ("attention residual dropped", "xb[i] = xb[i] + o[i];", "xb[i] = o[i];"),
     ("rope sign", "v[i] = a * c - b * s;", "v[i] = a * c + b * s;"),
     ("attention scale missing", "s[t] = dot * scale;", "s[t] = dot;"),
-    ("current token excluded", "for (int t = 0; t < Lc; ++t) {\n        const uint16_t* kr",
-     "for (int t = 0; t < Lc - 1; ++t) {\n        const uint16_t* kr"),
-    ("values read from key plane", "kv_offset(d, tab[t / d.page_size], 1, g, t % d.page_size)",
-     "kv_offset(d, tab[t / d.page_size], 0, g, t % d.page_size)"),
+    ("current token excluded", "for (int t = 0; t < Lc; ++t) {\n        const int pg = tab[t / d.page_size], sl = t % d.page_size;\n        T dot = 0;",
+     "for (int t = 0; t < Lc - 1; ++t) {\n        const int pg = tab[t / d.page_size], sl = t % d.page_size;\n        T dot = 0;"),
+    ("values read from key plane", "cache.get(pg, 1, g, sl, i)", "cache.get(pg, 0, g, sl, i)"),
     ("router not renormalised", "d.norm_topk ? p[ids[j]] / z : p[ids[j]]", "p[ids[j]]"),
     ("top-k tie to higher index", "if (best < 0 || r[i] > r[best]) best = i;",
      "if (best < 0 || r[i] >= r[best]) best = i;"),
@@ -45,6 +44,14 @@ MUTANTS = [
     ("kv written unrounded-then-truncated", "bits += 0x7fffu + lsb;", "bits += 0;"),
     ("rope pair offset", "T a = v[i], b = v[i + half];", "T a = v[i], b = v[half - 1 - i];"),
     ("router bias dropped", "r[e] = r[e] + static_cast<T>(w.router_bias[e]);", "r[e] = r[e];"),
+    # the q8_0 cache
+    ("q8 scale of the next block", "f16_to_f32(scales[o / 32 + i / 32])",
+     "f16_to_f32(scales[o / 32 + (i / 32 + 1) % (d.head_dim / 32)])"),
+    ("q8 codes truncated", "q[i] = static_cast<int8_t>(std::round(x[i] * id));",
+     "q[i] = static_cast<int8_t>(std::trunc(x[i] * id));"),
+    ("q8 max over half a block", "for (int i = 0; i < 32; ++i) amax", "for (int i = 0; i < 16; ++i) amax"),
+    ("f16 scale truncated", "if (rem > half || (rem == half && (q & 1u))) ++q;", "(void)half;"),
+    ("q8 scale step 1/128", "const float d = amax / 127.0f;", "const float d = amax / 128.0f;"),
 ]
 
 
@@ -62,6 +69,15 @@ def _battery(orc64: Oracle, orc32: Oracle, wn, wn_bias, bias, wn_nonorm) -> list
         return np.stack([orc.decode_step(dims, w, np.array([tokens[t]], np.int32), np.array([t + 1], np.int32),
                                          bt.numpy(), kv)[0] for t in range(T)])
 
+    def inc_q8(orc, model, w, tokens):
+        T = len(tokens)
+        mp = (T + 15) // 16
+        bt, _ = W.make_block_tables([T], 16, mp + 3, mp, seed=3)
+        dims = make_dims(model, 16, mp + 3, mp, kv_q8=True)
+        kv = np.zeros((model["layers"], W.kv_q8_layer_bytes(model, mp + 3, 16)), dtype=np.uint8)
+        return np.stack([orc.decode_step(dims, w, np.array([tokens[t]], np.int32), np.array([t + 1], np.int32),
+                                         bt.numpy(), kv)[0] for t in range(T)])
+
     def close(a, b):
         return np.abs(a - b).max() / np.abs(b).max() < 1e-9
 
@@ -76,6 +92,22 @@ def _battery(orc64: Oracle, orc32: Oracle, wn, wn_bias, bias, wn_nonorm) -> list
             failed.append("bruteforce-nonorm")
     except Exception:
         failed.append("bruteforce-error")
+    # q8_0 cache: the paged incremental oracle against the brute force through the same reading
+    try:
+        if not close(inc_q8(orc64, m, wn, tokens[:12]), BF.forward_sequence(m, wn, tokens[:12], kv_round="q8")[0]):
+            failed.append("bruteforce-q8")
+    except Exception:
+        failed.append("bruteforce-q8-error")
+    with np.errstate(over="ignore"):
+        f16 = np.array([1 + 2 ** -11, 1 + 3 * 2 ** -11, 65520.0, 3 * 2 ** -25, 0.1], np.float32)
+        if [orc32.f32_to_f16(float(v)) for v in f16] != f16.astype(np.float16).view(np.uint16).tolist():
+            failed.append("f16-rne")
+    xb = np.linspace(-1.0, 0.9, 32).astype(np.float32)
+    qb, db = orc32.q8_quantize(xb)
+    step = np.float64(np.float32(1.0) / np.float32(127))
+    if int(qb[0]) != -127 or np.abs(xb - qb.astype(np.float64) * db.view(np.float16).astype(np.float64)).max() > \
+            (0.5 + 127 * 2.0 ** -11) * step:
+        failed.append("q8-block")
     r = np.array([0.5, 1.0, 1.0, 0.2, 1.0], dtype=np.float32)
     if list(orc32.topk(r, 2)) != [1, 2]:
         failed.append("topk-ties")

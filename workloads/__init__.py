@@ -215,6 +215,45 @@ def make_kv_random(m: dict, num_pages: int, page_size: int, device="cpu", seed: 
     return kv
 
 
+# ---------------------------------------------------------------- q8_0 KV cache layout
+# Per layer: an int8 code plane [num_pages][2 (K, V)][Hkv][page_size][D] followed by an f16
+# scale plane [num_pages][2][Hkv][page_size][D / 32] (one scale per 32 consecutive values of a
+# K or V row).  The pool is a uint8 tensor [L][layer_bytes].
+
+def kv_q8_layer_bytes(m: dict, num_pages: int, page_size: int) -> int:
+    n = num_pages * 2 * m["n_kv"] * page_size * m["head_dim"]
+    return n + (n // 32) * 2
+
+
+def kv_q8_planes(layer_u8: torch.Tensor, m: dict, num_pages: int, page_size: int):
+    """Views of one layer of a q8_0 pool: (codes int8 [P][2][Hkv][ps][D], scales f16 [P][2][Hkv][ps][D/32])."""
+    D, Hkv = m["head_dim"], m["n_kv"]
+    n = num_pages * 2 * Hkv * page_size * D
+    codes = layer_u8[:n].view(torch.int8).view(num_pages, 2, Hkv, page_size, D)
+    scales = layer_u8[n:n + (n // 32) * 2].view(torch.float16).view(num_pages, 2, Hkv, page_size, D // 32)
+    return codes, scales
+
+
+def make_kv_q8_random(m: dict, num_pages: int, page_size: int, device="cpu", seed: int = KV_SEED, used_pages=None):
+    """q8_0 pool whose used pages hold random codes, round(N(0, 42^2)) clipped to [-127, 127], and
+    random scales U(0.012, 0.024) stored as f16 (decoded values about N(0, 0.76^2)); other pages zero."""
+    L = m["layers"]
+    lb = kv_q8_layer_bytes(m, num_pages, page_size)
+    kv = torch.zeros(L, lb, dtype=torch.uint8, device=device)
+    g = _gen(seed, device)
+    pages = range(num_pages) if used_pages is None else sorted(set(int(p) for p in used_pages))
+    idx = torch.tensor(list(pages), dtype=torch.int64, device=device)
+    for l in range(L):
+        codes, scales = kv_q8_planes(kv[l], m, num_pages, page_size)
+        for s in range(0, idx.numel(), 4096):
+            sel = idx[s:s + 4096]
+            c = torch.randn((sel.numel(),) + tuple(codes.shape[1:]), generator=g, device=device) * 42.0
+            codes.index_copy_(0, sel, c.round().clamp_(-127, 127).to(torch.int8))
+            d = torch.rand((sel.numel(),) + tuple(scales.shape[1:]), generator=g, device=device) * 0.012 + 0.012
+            scales.index_copy_(0, sel, d.to(torch.float16))
+    return kv
+
+
 def bf16_bits(t: torch.Tensor):
     """Host numpy uint16 view of a bf16 tensor's bits (copies to host if needed)."""
     import numpy as np
