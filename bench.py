@@ -61,7 +61,8 @@ def parse():
 
 
 # the 30B workloads besides the headline one, measured in the same run
-OTHER_30B = ("moe30b_bs64_ragged", "moe30b_bs1_ctx32k", "moe30b_bs1_ctx128k", "moe30b_bs1_ctx256k")
+OTHER_30B = ("moe30b_bs64_ragged", "moe30b_bs1_ctx32k", "moe30b_bs1_ctx128k", "moe30b_bs1_ctx256k",
+             "moe30b_bs1_ctx256k_q8")
 
 
 def cpu_model() -> str:
@@ -157,11 +158,19 @@ def setup_workload(wl, layers_override, device, weights=None):
     num_pages = W.pages_needed(lens, ps) + 8
     bt, _ = W.make_block_tables(lens, ps, num_pages, max_pages)
     used = [int(p) for p in bt.flatten() if p >= 0]
-    kv = W.make_kv_random(m, num_pages, ps, device, used_pages=used)
+    if wl.kv_q8:
+        kv = W.make_kv_q8_random(m, num_pages, ps, device, used_pages=used)
+    else:
+        kv = W.make_kv_random(m, num_pages, ps, device, used_pages=used)
     tokens = W.make_tokens(B, m["vocab"])
     torch.cuda.synchronize()
     return dict(model=m, w=w, lens=lens, B=B, ps=ps, num_pages=num_pages, max_pages=max_pages, bt=bt, kv=kv,
-                tokens=tokens, bias=bias)
+                tokens=tokens, bias=bias, kv_q8=wl.kv_q8)
+
+
+def engine_flags(st) -> int:
+    import persistent_moe_decode_megakernel_gb300 as mk
+    return mk.FLAG_KV_Q8 if st["kv_q8"] else 0
 
 
 def cpu_baseline(st, budget_s: float):
@@ -172,7 +181,7 @@ def cpu_baseline(st, budget_s: float):
     from oracle import Oracle, make_dims
     m, B = st["model"], st["B"]
     orc = Oracle("f32")
-    dims = make_dims(m, st["ps"], st["num_pages"], st["max_pages"])
+    dims = make_dims(m, st["ps"], st["num_pages"], st["max_pages"], kv_q8=st["kv_q8"])
     bt = st["bt"].numpy()
     sl = np.array(st["lens"], dtype=np.int32)
     x = W.bf16_bits(st["w"]["embed"][st["tokens"].long().cuda()]).astype(np.uint32) << 16
@@ -192,7 +201,7 @@ def cpu_baseline(st, budget_s: float):
         host = {k: W.bf16_bits(lw[k]) for k in ("attn_norm", "w_qkv", "w_o", "ffn_norm", "w_router", "w_gate_up",
                                                "w_down")}
         host["router_bias"] = None if lw.get("router_bias") is None else lw["router_bias"].cpu().numpy()
-        kvl = W.bf16_bits(st["kv"][l]).copy()
+        kvl = st["kv"][l].cpu().numpy().copy() if st["kv_q8"] else W.bf16_bits(st["kv"][l]).copy()
         t0 = time.perf_counter()
         tr = orc.layer_trace(dims, host, x, sl, bt, kvl)
         dt = time.perf_counter() - t0
@@ -332,7 +341,7 @@ def roofline_of(eng, st, wl_name, ms_mean):
     union = None
     if B > 1:
         union = [len(set(eng.debug_read("route_ids", l).ravel().tolist())) for l in range(m["layers"])]
-    by = R.step_bytes(m, st["lens"], expert_union=union, router_bias=st["bias"] is not None)
+    by = R.step_bytes(m, st["lens"], expert_union=union, router_bias=st["bias"] is not None, kv_q8=st["kv_q8"])
     peak, peak_kind = measured_peaks()
     achieved = by["total"] / (ms_mean / 1e3) / 1e9
     sol = R.sol_tokens_per_s(by["total"], peak * 1e9, B)
@@ -374,7 +383,7 @@ def main():
     wl = W.get(args.workload)
     st = setup_workload(wl, args.layers, "cuda")
     m, B = st["model"], st["B"]
-    eng = mk.Engine(m, st["w"], st["ps"], st["num_pages"], max(B, 1), st["max_pages"])
+    eng = mk.Engine(m, st["w"], st["ps"], st["num_pages"], max(B, 1), st["max_pages"], flags=engine_flags(st))
     ms_mean, ms_med, value, cs, e2e, wall = measure(eng, st, args.steps, args.warmup, local, world,
                                                     not args.no_e2e)
     roof = roofline_of(eng, st, wl.name, ms_mean)
@@ -395,7 +404,8 @@ def main():
     for name in names:
         wlx = W.get(name)
         stx = setup_workload(wlx, args.layers, "cuda", weights=base_w)
-        engx = mk.Engine(stx["model"], stx["w"], stx["ps"], stx["num_pages"], max(stx["B"], 1), stx["max_pages"])
+        engx = mk.Engine(stx["model"], stx["w"], stx["ps"], stx["num_pages"], max(stx["B"], 1), stx["max_pages"],
+                         flags=engine_flags(stx))
         # a few seconds of timed work per workload (at least 5 steps), after the same warm-up
         t0 = time.perf_counter()
         engx.step(stx["tokens"].cuda(), np.array(stx["lens"], np.int32), stx["bt"].cuda(), stx["kv"])
@@ -405,12 +415,15 @@ def main():
         msx, medx, valx, csx, e2ex, wallx = measure(engx, stx, steps_x, args.warmup, local, world, not args.no_e2e)
         entry = {"value": valx, "unit": "tok/s", "ms_per_step": msx, "ms_per_step_median": medx, "steps": steps_x,
                  "batch": stx["B"], "context": int(max(stx["lens"]) - 1) if stx["B"] == 1 else "ragged 512-32768",
+                 "kv_cache": "bf16",
                  "page_size": stx["ps"], "roofline": roofline_of(engx, stx, name, msx),
                  "clocks": {"sm_mhz": csx["sm_mhz"], "sm_max_mhz": csx["sm_max_mhz"], "reasons": csx["reasons"],
                             "samples": csx["samples"]},
                  "gpu_launches": steps_x, "wall_s_timed": wallx}
         if wlx.zipf:
             entry["router_prior"] = f"Zipf({wlx.zipf}) router bias"
+        if wlx.kv_q8:
+            entry["kv_cache"] = "q8_0 (blocks of 32 int8 codes + one f16 scale); not a bf16 workload of the metric"
         if e2ex:
             entry["e2e"] = e2ex
         engx.close()

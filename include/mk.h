@@ -70,6 +70,18 @@ typedef struct CUstream_st* mk_stream_t;
  * every batch then takes the general MoE path.  Results agree within rounding either way.
  */
 #define MK_FLAG_NO_DOWN_COPY 1
+/*
+ * MK_FLAG_KV_Q8: the KV pool holds q8_0 blocks instead of bf16 ("Kinetic" pages: a quantized
+ * cache keeps keys and values as blocks of 32 int8 values with one f16 scale, 34 bytes where
+ * bf16 takes 64; outputs are close to, not equal to, the bf16 cache's).  Layout, per layer,
+ * one layer after the other (layer_bytes = num_pages*2*Hkv*page_size*head_dim*17/16):
+ *   int8 codes   [num_pages][2 (K,V)][Hkv][page_size][head_dim]
+ *   f16 scales   [num_pages][2 (K,V)][Hkv][page_size][head_dim/32]
+ * A cached value is code * scale.  The step quantizes this token's k (after RoPE) and v from
+ * their fp32 values: per block of 32, scale = max|x|/127 (stored rounded to f16), code =
+ * x*(1/scale) rounded to nearest, ties away from zero.  Requires head_dim 128.
+ */
+#define MK_FLAG_KV_Q8 2
 
 typedef struct mk_config {
   int32_t num_layers;
@@ -88,7 +100,7 @@ typedef struct mk_config {
   int32_t max_batch;         /* largest batch a step may use */
   int32_t max_pages_per_seq; /* row length of the block table */
   int32_t norm_topk;         /* 1: router weights renormalised over the k chosen experts; 0: raw softmax probs */
-  int32_t flags;             /* 0 or MK_FLAG_NO_DOWN_COPY */
+  int32_t flags;             /* 0 or MK_FLAG_NO_DOWN_COPY | MK_FLAG_KV_Q8 */
   uint32_t watchdog_ms;      /* per-wait device budget in ms; 0 selects the default (1000 ms) */
 } mk_config;
 
@@ -154,9 +166,10 @@ int mk_create(const mk_config* cfg, const mk_weights* weights, mk_ctx** out);
  *                 the pool page holding positions p*page_size..; entries past
  *                 ceil(seq_len/page_size) are not read.
  *   kv_pages:     device bf16 [num_layers][num_pages][2 (K,V)][num_kv_heads]
- *                 [page_size][head_dim].  K is stored after RoPE.  The step
- *                 writes this token's K and V at position seq_len-1 of every
- *                 layer and reads positions 0..seq_len-2.
+ *                 [page_size][head_dim] (or the q8_0 layout of MK_FLAG_KV_Q8).
+ *                 K is stored after RoPE.  The step writes this token's K and V
+ *                 at position seq_len-1 of every layer and reads positions
+ *                 0..seq_len-2.
  *   logits_out:   device fp32 [batch, vocab].
  * Re-running a step with the same arguments is idempotent.  Steps on one
  * context must not run concurrently (the workspace is shared).

@@ -188,6 +188,8 @@ def _check(rc):
 
 # mk_config.flags: skip the transposed down-projection copy (every batch takes the general MoE path)
 FLAG_NO_DOWN_COPY = 1
+# mk_config.flags: the KV pool holds q8_0 blocks (uint8 [L][layer_bytes]: codes, then f16 scales)
+FLAG_KV_Q8 = 2
 
 
 def make_config(model: dict, page_size: int, num_pages: int, max_batch: int, max_pages_per_seq: int,
@@ -337,7 +339,8 @@ class Engine:
         assert tokens.is_cuda and tokens.dtype == torch.int32 and tokens.numel() == B and tokens.is_contiguous()
         assert block_tables.is_cuda and block_tables.dtype == torch.int32 and block_tables.is_contiguous()
         assert block_tables.shape[-1] == self.cfg.max_pages_per_seq and block_tables.shape[0] >= B
-        assert kv.is_cuda and kv.dtype == torch.bfloat16 and kv.is_contiguous()
+        kv_dtype = torch.uint8 if (self.cfg.flags & FLAG_KV_Q8) else torch.bfloat16
+        assert kv.is_cuda and kv.dtype == kv_dtype and kv.is_contiguous()
         if logits is None:
             logits = torch.empty(B, self.cfg.vocab, dtype=torch.float32, device=tokens.device)
         assert logits.is_cuda and logits.dtype == torch.float32 and logits.is_contiguous()

@@ -35,7 +35,7 @@ namespace mk {
 cudaError_t launch_step(const Params& p, cudaStream_t s);
 int tb_for_batch(int B);
 cudaError_t transpose_down(const uint16_t* in, uint16_t* out, int E, int H, int F, cudaStream_t s);
-cudaError_t configure_kernels(int D);
+cudaError_t configure_kernels(int D, bool kv_q8);
 cudaError_t occupancy(int D, int* blocks);
 size_t smem_bytes();
 }  // namespace mk
@@ -81,7 +81,7 @@ int check_config(const mk_config* c) {
     if (f.v <= 0) return fail(MK_ERR_INVALID_ARG, "config.%s must be > 0 (got %d)", f.n, f.v);
   if (!(c->rope_theta > 0.f) || !(c->rms_eps >= 0.f)) return fail(MK_ERR_INVALID_ARG, "rope_theta must be > 0, rms_eps >= 0");
   if (c->norm_topk != 0 && c->norm_topk != 1) return fail(MK_ERR_INVALID_ARG, "norm_topk must be 0 or 1");
-  if (c->flags & ~MK_FLAG_NO_DOWN_COPY) return fail(MK_ERR_INVALID_ARG, "unknown bits in flags");
+  if (c->flags & ~(MK_FLAG_NO_DOWN_COPY | MK_FLAG_KV_Q8)) return fail(MK_ERR_INVALID_ARG, "unknown bits in flags");
   if (c->num_q_heads % c->num_kv_heads) return fail(MK_ERR_INVALID_ARG, "num_q_heads must be a multiple of num_kv_heads");
   if (c->top_k > c->num_experts) return fail(MK_ERR_INVALID_ARG, "top_k > num_experts");
   // limits of this build
@@ -96,6 +96,10 @@ int check_config(const mk_config* c) {
   if (c->page_size * c->head_dim * 2 > mk::kSlotBytes / 2)
     return fail(MK_ERR_UNSUPPORTED, "page_size*head_dim*2 > %d", mk::kSlotBytes / 2);
   if (c->page_size % 8) return fail(MK_ERR_UNSUPPORTED, "page_size must be a multiple of 8");
+  if ((c->flags & MK_FLAG_KV_Q8) && c->head_dim != 128)
+    return fail(MK_ERR_UNSUPPORTED, "the q8_0 KV cache needs head_dim 128");
+  if ((c->flags & MK_FLAG_KV_Q8) && mk::pages_per_chunk_q8(c->page_size, c->head_dim) < 1)
+    return fail(MK_ERR_UNSUPPORTED, "a q8_0 page does not fit one ring slot");
   if ((int64_t)c->num_layers * c->num_pages * 2 * c->num_kv_heads * c->page_size >= ((int64_t)1 << 31))
     return fail(MK_ERR_UNSUPPORTED, "KV pool has 2^31 or more rows");
   if (c->max_batch > mk::kMaxBatch) return fail(MK_ERR_UNSUPPORTED, "max_batch > 64");
@@ -321,7 +325,16 @@ namespace {
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
-// Describe the KV pool [L][P][2][Hkv][ps][D] to TMA as 2-D rows of D elements.
+// Bytes of one layer of the q8_0 KV pool (code plane, then scale plane), and of its code plane.
+size_t kv_q8_code_bytes(const mk_config& cf) {
+  return (size_t)cf.num_pages * 2 * cf.num_kv_heads * cf.page_size * cf.head_dim;
+}
+size_t kv_q8_layer_bytes(const mk_config& cf) { return kv_q8_code_bytes(cf) / 16 * 17; }
+
+// Describe the KV pool to TMA: the bf16 pool [L][P][2][Hkv][ps][D] as 2-D rows of D elements
+// (boxes of 64 elements x page_size rows); the q8_0 pool's code planes as 3-D [layer][row][D
+// bytes], rows of one layer contiguous, layers layer_bytes apart (boxes of D bytes x page_size
+// rows).  Both with the 128-byte swizzle.
 int encode_kv_map(const mk_config& cf, void* kv, CUtensorMap* out) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
@@ -331,6 +344,18 @@ int encode_kv_map(const mk_config& cf, void* kv, CUtensorMap* out) {
     if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
       return fail(MK_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  if (cf.flags & MK_FLAG_KV_Q8) {
+    const cuuint64_t rows = (cuuint64_t)cf.num_pages * 2 * cf.num_kv_heads * cf.page_size;
+    const cuuint64_t dims[3] = {(cuuint64_t)cf.head_dim, rows, (cuuint64_t)cf.num_layers};
+    const cuuint64_t strides[2] = {(cuuint64_t)cf.head_dim, (cuuint64_t)kv_q8_layer_bytes(cf)};
+    const cuuint32_t box[3] = {(cuuint32_t)cf.head_dim, (cuuint32_t)cf.page_size, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = encode(out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, kv, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MK_ERR_CUDA, "cuTensorMapEncodeTiled (q8_0 codes) failed (%d)", (int)r);
+    return MK_OK;
   }
   const cuuint64_t rows = (cuuint64_t)cf.num_layers * cf.num_pages * 2 * cf.num_kv_heads * cf.page_size;
   const cuuint64_t dims[2] = {(cuuint64_t)cf.head_dim, rows};
@@ -399,7 +424,8 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_ctx** out) {
   if (prop.sharedMemPerBlockOptin < smem)
     return fail(MK_ERR_UNSUPPORTED, "needs %zu bytes of shared memory per block, device offers %zu", smem,
                 (size_t)prop.sharedMemPerBlockOptin);
-  if ((e = mk::configure_kernels(cfg->head_dim)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+  if ((e = mk::configure_kernels(cfg->head_dim, (cfg->flags & MK_FLAG_KV_Q8) != 0)) != cudaSuccess)
+    return cuda_fail(e, "cudaFuncSetAttribute");
   int blocks = 0;
   if ((e = mk::occupancy(cfg->head_dim, &blocks)) != cudaSuccess) return cuda_fail(e, "occupancy");
   if (blocks < 1) return fail(MK_ERR_UNSUPPORTED, "the step kernel does not fit on an SM");
@@ -598,6 +624,9 @@ static int decode_step(mk_ctx* c, int32_t batch, const int32_t* token_ids, const
   p.tasks = c->d_tasks; p.task_off = c->d_task_off;
   p.layers = c->d_layers; p.embed = c->embed; p.final_norm = c->final_norm; p.lm_head = c->lm_head;
   p.tokens = token_ids; p.block_tables = block_tables; p.kv = static_cast<uint16_t*>(kv_pages); p.logits = logits_out;
+  p.kv_q8 = (cf.flags & MK_FLAG_KV_Q8) ? 1 : 0;
+  p.kv_layer_bytes = p.kv_q8 ? kv_q8_layer_bytes(cf) : 0;
+  p.kv_code_bytes = p.kv_q8 ? kv_q8_code_bytes(cf) : 0;
   p.seq_lens = reinterpret_cast<const int32_t*>(d + c->off_lens);
   p.rope_cos = reinterpret_cast<const float*>(d + c->off_cos);
   p.rope_sin = reinterpret_cast<const float*>(d + c->off_sin);

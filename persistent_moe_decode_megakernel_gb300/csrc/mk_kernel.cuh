@@ -47,6 +47,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "mk_layout.h"
@@ -96,6 +97,15 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, 
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(pol)
       : "memory");
 }
+// 3-D tiled TMA load of box (x, y, z) of the tensor map into shared memory (completion on an mbarrier)
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int x, int y, int z, uint64_t* bar,
+                                            uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3, "
+      "%4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -119,6 +129,23 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
   return y;
 }
+// the two signed bytes in the low half of u (first in bits 0-7) -> bf16x2, exactly (|v| <= 128)
+__device__ __forceinline__ uint32_t s8x2_bf16x2(uint32_t u) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(static_cast<float>(static_cast<int8_t>(u & 0xffu)),
+                                                 static_cast<float>(static_cast<int8_t>((u >> 8) & 0xffu)));
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds_u8(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ float f16_f32(uint16_t h) { return __half2float(__ushort_as_half(h)); }
 // two floats -> bf16x2 (first in the low half), and the bf16x2 of what rounding left over
 __device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
@@ -519,6 +546,8 @@ __device__ __forceinline__ bool group_bar_and(bool v, int nw) {
 }
 
 // --------------------------------------------------------------------------- producer
+// Q8: the KV pool holds q8_0 blocks (codes and scales) instead of bf16 values.
+template <bool Q8>
 struct Producer {
   const Params& p;
   Smem& S;
@@ -550,7 +579,8 @@ struct Producer {
       }
       case MK_OP_ATTN: {
         const int cta = blockIdx.x;
-        const uint32_t blk = static_cast<uint32_t>(p.ps) * p.D * 2u;   // one page of K (or V) of one KV head
+        // one page of K (or V) of one KV head (q8_0: its codes; the small scale runs are not warmed)
+        const uint32_t blk = static_cast<uint32_t>(p.ps) * p.D * (Q8 ? 1u : 2u);
         uint32_t done = 0;
         #pragma unroll 1
         for (int it = p.item_off[cta]; it < p.item_off[cta + 1] && done < kPrefetchBytes; ++it) {
@@ -560,9 +590,16 @@ struct Producer {
           for (uint32_t pg = item.page_lo; pg < item.page_hi && done < kPrefetchBytes; ++pg) {
             const int32_t page = btrow[pg];
             if (page < 0 || page >= p.P) continue;
-            const size_t kb = (((static_cast<size_t>(t.layer) * p.P + page) * 2) * p.Hkv + item.kvh) * p.ps * p.D;
-            prefetch_l2(p.kv + kb, blk);
-            prefetch_l2(p.kv + kb + static_cast<size_t>(p.Hkv) * p.ps * p.D, blk);
+            if constexpr (Q8) {
+              const uint8_t* base = reinterpret_cast<const uint8_t*>(p.kv) + t.layer * p.kv_layer_bytes;
+              const size_t kb = ((static_cast<size_t>(page) * 2) * p.Hkv + item.kvh) * p.ps * p.D;
+              prefetch_l2(base + kb, blk);
+              prefetch_l2(base + kb + static_cast<size_t>(p.Hkv) * p.ps * p.D, blk);
+            } else {
+              const size_t kb = (((static_cast<size_t>(t.layer) * p.P + page) * 2) * p.Hkv + item.kvh) * p.ps * p.D;
+              prefetch_l2(p.kv + kb, blk);
+              prefetch_l2(p.kv + kb + static_cast<size_t>(p.Hkv) * p.ps * p.D, blk);
+            }
             done += 2 * blk;
           }
         }
@@ -655,6 +692,7 @@ struct Producer {
   // [page_size rows][64 dims] (128-byte swizzle).  Within a slot, K occupies the first half
   // and V the second; each holds [dim half][rows][64 dims], page i at rows i*page_size.
   __device__ bool attn_items(const mk_task& t) {
+    if constexpr (Q8) return attn_items_q8(t);
     const int cta = blockIdx.x;
     const int ppc = pages_per_chunk(p.ps, p.D);
     const int rows_cap = (kSlotBytes / 2) / (p.D * 2);
@@ -696,6 +734,53 @@ struct Producer {
     }
     // the consumers then merge this block's share of every pair it holds a split of, with no
     // record of their own: both slots are free meanwhile for the weights of the next tile
+    return true;
+  }
+
+  // q8_0 cache: per page, the K codes and V codes of the item's KV head (3-D TMA boxes of
+  // page_size rows of head_dim bytes, 128-byte swizzle) and their scale runs (1-D bulk copies).
+  // A slot holds [K codes][V codes][K scales][V scales], each for pages_per_chunk_q8 pages.
+  __device__ bool attn_items_q8(const mk_task& t) {
+    const int cta = blockIdx.x;
+    const int ppc = pages_per_chunk_q8(p.ps, p.D);
+    const int rows_cap = ppc * p.ps;
+    const uint32_t cbox = static_cast<uint32_t>(p.ps) * p.D;                 // codes of one page, one head
+    const uint32_t srow = static_cast<uint32_t>(p.D / 32) * 2u;              // scale bytes of one row
+    const uint32_t sbox = static_cast<uint32_t>(p.ps) * srow;                // scales of one page, one head
+    const uint8_t* sbase = reinterpret_cast<const uint8_t*>(p.kv) + t.layer * p.kv_layer_bytes + p.kv_code_bytes;
+#pragma unroll 1
+    for (int it = p.item_off[cta]; it < p.item_off[cta + 1]; ++it) {
+      const mk_attn_item item = p.items[it];
+      const int32_t* btrow = p.block_tables + static_cast<size_t>(item.b) * p.maxpg;
+#pragma unroll 1
+      for (uint32_t pg = item.page_lo; pg < item.page_hi; pg += ppc) {
+        const uint32_t n = min(static_cast<uint32_t>(ppc), item.page_hi - pg);
+        if (!acquire()) return false;
+        Meta& m = meta();
+        m.kind = R_ATTN; m.op = MK_OP_ATTN; m.first = (pg == item.page_lo); m.last = (pg + n >= item.page_hi);
+        m.layer = t.layer; m.n = static_cast<uint16_t>(n); m.row0 = pg; m.idx = static_cast<uint32_t>(it);
+        m.e = 0; m.aux = 0; m.lo = item.page_lo; m.hi = item.page_hi;
+        mbar_arrive_expect_tx(full(), 2u * n * (cbox + sbox));
+        uint8_t* dst = slot();
+#pragma unroll 1
+        for (uint32_t i = 0; i < n; ++i) {
+          int32_t page = btrow[pg + i];
+          if (page < 0 || page >= p.P) {
+            record_error(p, MK_ERR_DEVICE_BOUNDS, MK_OP_ATTN, t.layer, 0u, static_cast<uint32_t>(page), 0,
+                         static_cast<int>(pg + i), false);
+            page = 0;  // keep the byte count of the slot; the result is flagged invalid
+          }
+          const int rowk = ((page * 2) * p.Hkv + item.kvh) * p.ps;   // row of the layer's code plane
+          const int rowv = rowk + p.Hkv * p.ps;
+          tma_load_3d(dst + i * cbox, p.kv_map, 0, rowk, t.layer, full(), pol);
+          tma_load_3d(dst + static_cast<size_t>(rows_cap) * p.D + i * cbox, p.kv_map, 0, rowv, t.layer, full(), pol);
+          uint8_t* sd = dst + static_cast<size_t>(2 * rows_cap) * p.D;
+          bulk_g2s(sd + i * sbox, sbase + static_cast<size_t>(rowk) * srow, sbox, full(), pol);
+          bulk_g2s(sd + rows_cap * srow + i * sbox, sbase + static_cast<size_t>(rowv) * srow, sbox, full(), pol);
+        }
+        ++c;
+      }
+    }
     return true;
   }
 
@@ -1031,7 +1116,7 @@ __device__ __noinline__ H8 load_h8(const Params& p, const uint64_t* src) {
 // registers (the consumer warpgroups hold 224 each).  A call that took the object's
 // address would put that state in local memory, and with nearly all of the SM's L1
 // given to shared memory, those accesses would miss to L2 after every barrier.
-template <int TB, int D>
+template <int TB, int D, bool Q8>
 struct Consumer {
   const Params& p;
   Smem& S;
@@ -2241,6 +2326,129 @@ struct Consumer {
     return static_cast<uint32_t>((d >> 6) * rows_cap * 128 + r * 128 + ((((d & 63) >> 3) ^ (r & 7)) << 4) + (d & 7) * 2);
   }
 
+  // q8_0 chunks: the slot holds [K codes][V codes][K scales][V scales] of pages_per_chunk_q8 pages,
+  // codes as rows of D bytes with the TMA 128-byte swizzle (16-byte piece j of row r at piece
+  // j ^ (r & 7)).  S^T = K Q^T runs per 32-dim block on the codes (exact in bf16), and each block's
+  // partial is multiplied by the row's K scale; O^T += V^T P^T runs per 32-dim block with the row's
+  // V scale folded into P.  Rows past the sequence get scale 0 (their codes are finite).
+  static __device__ __forceinline__ uint32_t swz8(int r, int c) {
+    return static_cast<uint32_t>(r * D + ((((c >> 4) ^ r) & 7) << 4) + (c & 15));
+  }
+  __device__ __forceinline__ void attn_chunks_q8(int Lc, int pos, const uint16_t* kvcur, float (&o)[D / 16][4],
+                                                 float (&mx)[2], float (&ls)[2]) {
+    constexpr int NB = D / 32;   // scale blocks per row
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const uint4* qf = reinterpret_cast<const uint4*>(S.scr.attn);
+    const int rows_cap = pages_per_chunk_q8(p.ps, D) * p.ps;
+    for (;;) {
+      const int p0 = static_cast<int>(meta().row0) * p.ps;            // first position of the chunk
+      const int npos = min(static_cast<int>(meta().n) * p.ps, Lc - p0);
+      const bool last = meta().last;
+      uint8_t* sl8 = const_cast<uint8_t*>(slot());
+      const uint32_t Kc = smem_u32(sl8);
+      const uint32_t Vc = Kc + rows_cap * D;
+      uint16_t* ksc = reinterpret_cast<uint16_t*>(sl8 + 2 * rows_cap * D);
+      uint16_t* vsc = ksc + rows_cap * NB;
+#pragma unroll 1
+      for (int tile = warp; tile * 16 < npos; tile += kConsumerWarps) {
+        const int r0 = tile * 16;
+        if (pos >= p0 + r0 && pos < p0 + r0 + 16) {
+          // this token's codes and scales are not in the copied page yet: put them in its rows
+          const int rr = pos - p0;
+          const uint8_t* c8 = reinterpret_cast<const uint8_t*>(kvcur);
+#pragma unroll 1
+          for (int cidx = lane; cidx < 2 * (D / 16); cidx += 32) {
+            const int which = cidx / (D / 16), d = (cidx - which * (D / 16)) * 16;
+            const uint4 v = *reinterpret_cast<const uint4*>(c8 + which * D + d);
+            const uint32_t a = (which ? Vc : Kc) + swz8(rr, d);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                         : "memory");
+          }
+          if (lane < 2 * NB) {
+            const uint16_t* s8 = reinterpret_cast<const uint16_t*>(c8 + 2 * D);
+            (lane < NB ? ksc : vsc)[rr * NB + (lane % NB)] = s8[lane];
+          }
+          fence_proxy_async_smem();   // these generic writes precede the slot's next TMA fill
+          __syncwarp();
+        }
+        const int ra = r0 + g, rb = r0 + g + 8;
+        // S^T = K Q^T, block by block
+        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          float ab[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int s2 = 2 * b + h2;
+            const int col = 16 * s2 + 2 * t;
+            uint32_t a[4];
+            a[0] = s8x2_bf16x2(lds_u16(Kc + swz8(ra, col)));
+            a[1] = s8x2_bf16x2(lds_u16(Kc + swz8(rb, col)));
+            a[2] = s8x2_bf16x2(lds_u16(Kc + swz8(ra, col + 8)));
+            a[3] = s8x2_bf16x2(lds_u16(Kc + swz8(rb, col + 8)));
+            const uint4 q = qf[s2 * 32 + lane];
+            mma_bf16(ab, a, q.x, q.y);
+            mma_bf16(ab, a, q.z, q.w);
+          }
+          const float da = ra < npos ? f16_f32(ksc[ra * NB + b]) : 0.f;
+          const float db = rb < npos ? f16_f32(ksc[rb * NB + b]) : 0.f;
+          sc[0] = fmaf(ab[0], da, sc[0]);
+          sc[1] = fmaf(ab[1], da, sc[1]);
+          sc[2] = fmaf(ab[2], db, sc[2]);
+          sc[3] = fmaf(ab[3], db, sc[3]);
+        }
+        if (ra >= npos) { sc[0] = -INFINITY; sc[1] = -INFINITY; }
+        if (rb >= npos) { sc[2] = -INFINITY; sc[3] = -INFINITY; }
+        // online softmax per head column (heads 2t, 2t+1 on this lane)
+        float pa[2], pb[2], cr[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          float tm = fmaxf(sc[j], sc[j + 2]);
+          tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 4));
+          tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 8));
+          tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
+          const float mn = fmaxf(mx[j], tm);
+          cr[j] = mx[j] == -INFINITY ? 0.f : __expf(mx[j] - mn);
+          pa[j] = sc[j] == -INFINITY ? 0.f : __expf(sc[j] - mn);
+          pb[j] = sc[j + 2] == -INFINITY ? 0.f : __expf(sc[j + 2] - mn);
+          ls[j] = ls[j] * cr[j] + pa[j] + pb[j];
+          mx[j] = mn;
+        }
+#pragma unroll
+        for (int mm = 0; mm < D / 16; ++mm) {
+          o[mm][0] *= cr[0]; o[mm][1] *= cr[1]; o[mm][2] *= cr[0]; o[mm][3] *= cr[1];
+        }
+        // O^T += V^T P^T, block by block with the block's V scales in P
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          const float va = ra < npos ? f16_f32(vsc[ra * NB + b]) : 0.f;
+          const float vb = rb < npos ? f16_f32(vsc[rb * NB + b]) : 0.f;
+          uint32_t xa_h, xa_l, xb_h, xb_l;
+          split_bf16x2(pa[0] * va, pa[1] * va, xa_h, xa_l);
+          split_bf16x2(pb[0] * vb, pb[1] * vb, xb_h, xb_l);
+          const uint32_t b0h = movmatrix_t(xa_h), b0l = movmatrix_t(xa_l);
+          const uint32_t b1h = movmatrix_t(xb_h), b1l = movmatrix_t(xb_l);
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int mm = 2 * b + h2;
+            const int dc = 16 * mm + g;      // this lane's A rows: dims dc and dc + 8
+            const int pr = r0 + 2 * t;       // its A columns: positions pr, pr + 1, pr + 8, pr + 9
+            uint32_t a[4];
+            a[0] = s8x2_bf16x2(lds_u8(Vc + swz8(pr, dc)) | (lds_u8(Vc + swz8(pr + 1, dc)) << 8));
+            a[1] = s8x2_bf16x2(lds_u8(Vc + swz8(pr, dc + 8)) | (lds_u8(Vc + swz8(pr + 1, dc + 8)) << 8));
+            a[2] = s8x2_bf16x2(lds_u8(Vc + swz8(pr + 8, dc)) | (lds_u8(Vc + swz8(pr + 9, dc)) << 8));
+            a[3] = s8x2_bf16x2(lds_u8(Vc + swz8(pr + 8, dc + 8)) | (lds_u8(Vc + swz8(pr + 9, dc + 8)) << 8));
+            mma_bf16(o[mm], a, b0h, b1h);
+            mma_bf16(o[mm], a, b0l, b1l);
+          }
+        }
+      }
+      if (last) break;
+      if (!next_rec()) break;
+    }
+  }
+
   __device__ __forceinline__ bool attn_item() {
     constexpr int KS = D / 16;                              // k-steps over head dims (Q K^T)
     constexpr int MT = D / 16;                              // 16-dim tiles of the output (P V)
@@ -2325,7 +2533,30 @@ struct Consumer {
         split_bf16x2(v[2], v[3], f.y, f.w);
         qf[i] = f;
       }
-      if (kvon) {
+      if constexpr (Q8) {
+        // q8_0 blocks of this token's k (after RoPE) and v, from their fp32 values: a warp per 32
+        // dims (warps past head_dim / 32 take part in the reductions with zeros)
+        float kf = 0.f, vf = 0.f;
+        if (kvon) {
+          const float raw = ll_f(w[8]), other = ll_f(w[9]);
+          const float c = __ldg(cs + (i % (D / 2))), sv = __ldg(sn + (i % (D / 2)));
+          kf = i < D / 2 ? raw * c - other * sv : raw * c + other * sv;
+          vf = ll_f(w[10]);
+        }
+        const float ka = warp_max(fabsf(kf)), va = warp_max(fabsf(vf));
+        if (kvon) {
+          const float dk = ka / 127.0f, dv = va / 127.0f;
+          const float ik = dk != 0.f ? 1.0f / dk : 0.f, iv = dv != 0.f ? 1.0f / dv : 0.f;
+          uint8_t* c8 = reinterpret_cast<uint8_t*>(kvcur);          // [2][D] codes, then [2][D/32] scales
+          c8[i] = static_cast<uint8_t>(static_cast<int8_t>(roundf(kf * ik)));
+          c8[D + i] = static_cast<uint8_t>(static_cast<int8_t>(roundf(vf * iv)));
+          if ((i & 31) == 0) {
+            uint16_t* s8 = reinterpret_cast<uint16_t*>(c8 + 2 * D);
+            s8[i >> 5] = __half_as_ushort(__float2half_rn(dk));
+            s8[D / 32 + (i >> 5)] = __half_as_ushort(__float2half_rn(dv));
+          }
+        }
+      } else if (kvon) {
         const float raw = ll_f(w[8]), other = ll_f(w[9]);
         const float c = __ldg(cs + (i % (D / 2))), sv = __ldg(sn + (i % (D / 2)));
         kvcur[i] = to_bf16_bits(i < D / 2 ? raw * c - other * sv : raw * c + other * sv);
@@ -2339,12 +2570,30 @@ struct Consumer {
       const int pg = pos / p.ps, sl = pos % p.ps;
       const int32_t page = __ldg(p.block_tables + static_cast<size_t>(b) * p.maxpg + pg);
       if (page >= 0 && page < p.P) {
-        const size_t kb = (((static_cast<size_t>(l) * p.P + page) * 2 * p.Hkv + kvh) * p.ps + sl) * D;
-        const size_t vb = kb + static_cast<size_t>(p.Hkv) * p.ps * D;
-        #pragma unroll 1
-        for (int d = threadIdx.x; d < D; d += kConsumerThreads) {
-          p.kv[kb + d] = kvcur[d];
-          p.kv[vb + d] = kvcur[D + d];
+        if constexpr (Q8) {
+          uint8_t* base = reinterpret_cast<uint8_t*>(p.kv) + l * p.kv_layer_bytes;
+          const size_t rowk = ((static_cast<size_t>(page) * 2) * p.Hkv + kvh) * p.ps + sl;
+          const size_t rowv = rowk + static_cast<size_t>(p.Hkv) * p.ps;
+          const uint8_t* c8 = reinterpret_cast<const uint8_t*>(kvcur);
+#pragma unroll 1
+          for (int d = threadIdx.x; d < D; d += kConsumerThreads) {
+            base[rowk * D + d] = c8[d];
+            base[rowv * D + d] = c8[D + d];
+          }
+          if (threadIdx.x < D / 32) {
+            uint16_t* sb = reinterpret_cast<uint16_t*>(base + p.kv_code_bytes);
+            const uint16_t* s8 = reinterpret_cast<const uint16_t*>(c8 + 2 * D);
+            sb[rowk * (D / 32) + threadIdx.x] = s8[threadIdx.x];
+            sb[rowv * (D / 32) + threadIdx.x] = s8[D / 32 + threadIdx.x];
+          }
+        } else {
+          const size_t kb = (((static_cast<size_t>(l) * p.P + page) * 2 * p.Hkv + kvh) * p.ps + sl) * D;
+          const size_t vb = kb + static_cast<size_t>(p.Hkv) * p.ps * D;
+#pragma unroll 1
+          for (int d = threadIdx.x; d < D; d += kConsumerThreads) {
+            p.kv[kb + d] = kvcur[d];
+            p.kv[vb + d] = kvcur[D + d];
+          }
         }
       } else if (threadIdx.x == 0) {
         record_error(p, MK_ERR_DEVICE_BOUNDS, MK_OP_ATTN, l, 0u, static_cast<uint32_t>(page), 0, pg,
@@ -2357,7 +2606,9 @@ struct Consumer {
     for (int mm = 0; mm < MT; ++mm) o[mm][0] = o[mm][1] = o[mm][2] = o[mm][3] = 0.f;
     float mx[2] = {-INFINITY, -INFINITY}, ls[2] = {0.f, 0.f};   // heads 2t, 2t+1 (ls: this lane's share)
 
-    for (;;) {
+    if constexpr (Q8) {
+      attn_chunks_q8(Lc, pos, kvcur, o, mx, ls);
+    } else for (;;) {
       const int p0 = static_cast<int>(meta().row0) * p.ps;            // first position of the chunk
       const int npos = min(static_cast<int>(meta().n) * p.ps, Lc - p0);
       const bool last = meta().last;
@@ -2639,7 +2890,7 @@ struct Consumer {
 };
 
 // --------------------------------------------------------------------------- the kernel
-template <int TB, int D>
+template <int TB, int D, bool Q8>
 __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   // the ring holds 128-byte-swizzled TMA tiles, whose pattern repeats every 1024 bytes
@@ -2676,7 +2927,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     // producer warpgroup: one thread streams, the rest only lend their registers
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
     if (tid == kConsumerThreads) {
-      Producer prod(p, S);
+      Producer<Q8> prod(p, S);
       prod.run();
     }
     __syncwarp();
@@ -2685,7 +2936,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
     {
-      Consumer<TB, D> cons(p, S);
+      Consumer<TB, D, Q8> cons(p, S);
       cons.run();
     }
     asm volatile("bar.sync %0, 128;" ::"r"(10 + (tid >> 7)) : "memory");
@@ -2738,36 +2989,37 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
   }
 }
 
-template <int TB, int D>
+template <int TB, int D, bool Q8>
 cudaError_t configure_t(size_t smem) {
-  return cudaFuncSetAttribute(step_kernel<TB, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  return cudaFuncSetAttribute(step_kernel<TB, D, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(smem));
 }
 
-template <int TB, int D>
+template <int TB, int D, bool Q8>
 cudaError_t launch_t(const Params& p, size_t smem, cudaStream_t s) {
   void* args[] = {const_cast<Params*>(&p)};
-  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(step_kernel<TB, D>), dim3(p.n_ctas),
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(step_kernel<TB, D, Q8>), dim3(p.n_ctas),
                                      dim3(kThreads), args, smem, s);
 }
 
-template <int D>
+template <int D, bool Q8>
 cudaError_t configure_all(size_t smem) {
   cudaError_t e;
-  if ((e = configure_t<1, D>(smem)) != cudaSuccess) return e;
-  if ((e = configure_t<2, D>(smem)) != cudaSuccess) return e;
-  return configure_t<4, D>(smem);
+  if ((e = configure_t<1, D, Q8>(smem)) != cudaSuccess) return e;
+  if ((e = configure_t<2, D, Q8>(smem)) != cudaSuccess) return e;
+  return configure_t<4, D, Q8>(smem);
 }
 
-template <int D>
+template <int D, bool Q8>
 cudaError_t launch_any(const Params& p, int tb, size_t smem, cudaStream_t s) {
-  if (tb == 1) return launch_t<1, D>(p, smem, s);
-  if (tb == 2) return launch_t<2, D>(p, smem, s);
-  return launch_t<4, D>(p, smem, s);
+  if (tb == 1) return launch_t<1, D, Q8>(p, smem, s);
+  if (tb == 2) return launch_t<2, D, Q8>(p, smem, s);
+  return launch_t<4, D, Q8>(p, smem, s);
 }
 
 template <int D>
 cudaError_t occupancy_d(int* blocks, size_t smem) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, step_kernel<1, D>, kThreads, smem);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, step_kernel<1, D, false>, kThreads, smem);
 }
 
 }  // namespace

@@ -7,7 +7,9 @@ namespace mk {
 
 cudaError_t configure_d128(size_t smem);
 cudaError_t configure_d64(size_t smem);
+cudaError_t configure_d128_q8(size_t smem);
 cudaError_t launch_d128(const Params& p, int tb, size_t smem, cudaStream_t s);
+cudaError_t launch_d128_q8(const Params& p, int tb, size_t smem, cudaStream_t s);
 cudaError_t launch_d64(const Params& p, int tb, size_t smem, cudaStream_t s);
 cudaError_t occupancy_d128(int* blocks, size_t smem);
 cudaError_t occupancy_d64(int* blocks, size_t smem);
@@ -18,7 +20,10 @@ size_t smem_bytes() { return smem_bytes_impl(); }
 // rows of the batch held in registers at once by a GEMV tile
 int tb_for_batch(int B) { return B <= 1 ? 1 : (B <= 2 ? 2 : 4); }
 
-cudaError_t configure_kernels(int D) { return D == 128 ? configure_d128(smem_bytes()) : configure_d64(smem_bytes()); }
+cudaError_t configure_kernels(int D, bool kv_q8) {
+  if (kv_q8) return D == 128 ? configure_d128_q8(smem_bytes()) : cudaErrorInvalidValue;
+  return D == 128 ? configure_d128(smem_bytes()) : configure_d64(smem_bytes());
+}
 
 cudaError_t occupancy(int D, int* blocks) {
   return D == 128 ? occupancy_d128(blocks, smem_bytes()) : occupancy_d64(blocks, smem_bytes());
@@ -26,6 +31,7 @@ cudaError_t occupancy(int D, int* blocks) {
 
 cudaError_t launch_step(const Params& p, cudaStream_t s) {
   const int tb = tb_for_batch(p.B);
+  if (p.kv_q8) return p.D == 128 ? launch_d128_q8(p, tb, smem_bytes(), s) : cudaErrorInvalidValue;
   return p.D == 128 ? launch_d128(p, tb, smem_bytes(), s) : launch_d64(p, tb, smem_bytes(), s);
 }
 

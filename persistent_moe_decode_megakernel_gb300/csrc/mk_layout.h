@@ -84,6 +84,11 @@ MK_HD int gemv_rows_per_chunk(int K) {
 }
 // pages of K (and as many of V) per attention chunk: K fills the slot's first half, V the second
 MK_HD int pages_per_chunk(int page_size, int head_dim) { return (kSlotBytes / 2) / (page_size * head_dim * 2); }
+// q8_0 cache: pages per chunk, each page's K and V codes (page_size rows of head_dim bytes) and
+// their f16 scales (head_dim/32 per row); the slot holds [K codes][V codes][K scales][V scales]
+MK_HD int pages_per_chunk_q8(int page_size, int head_dim) {
+  return kSlotBytes / (page_size * (2 * head_dim + 2 * (head_dim / 32) * 2));
+}
 
 // ---- MoE work split ---------------------------------------------------------------
 // Gate/up work of a layer is a list of units, one per FFN row f of each active expert a
@@ -153,7 +158,10 @@ struct alignas(64) Params {
   // step inputs / outputs
   const int32_t* tokens;
   const int32_t* block_tables;
-  uint16_t* kv;
+  uint16_t* kv;           // the KV pool (bf16 elements, or the bytes of the q8_0 layout)
+  int32_t kv_q8;          // the pool holds q8_0 blocks (MK_FLAG_KV_Q8)
+  uint64_t kv_layer_bytes; // q8_0: bytes of one layer (codes, then scales)
+  uint64_t kv_code_bytes;  // q8_0: bytes of one layer's code plane
   float* logits;
   // per-step plan (device copy of the host-built step buffer)
   const int32_t* seq_lens;      // [B]

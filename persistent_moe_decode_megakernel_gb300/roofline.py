@@ -18,8 +18,11 @@ counts those bytes for a model shape and a batch:
 from __future__ import annotations
 
 
-def kv_bytes_per_token(m: dict) -> int:
-    return m["layers"] * 2 * m["n_kv"] * m["head_dim"] * 2
+def kv_bytes_per_token(m: dict, kv_q8: bool = False) -> int:
+    """Cache bytes of one position over all layers: bf16 K and V, or q8_0 (one int8 per value
+    plus an f16 scale per 32 values: 34 bytes per 32 values)."""
+    n = m["layers"] * 2 * m["n_kv"] * m["head_dim"]
+    return n * 2 if not kv_q8 else n + (n // 32) * 2
 
 
 def param_counts(m: dict) -> dict:
@@ -34,7 +37,7 @@ def param_counts(m: dict) -> dict:
                 active_with_tables=active_with_tables)
 
 
-def step_bytes(m: dict, seq_lens, expert_union=None, router_bias: bool = False) -> dict:
+def step_bytes(m: dict, seq_lens, expert_union=None, router_bias: bool = False, kv_q8: bool = False) -> dict:
     """Algorithmic bytes for one step.  ``seq_lens`` includes the decoded token.
     ``expert_union``: distinct experts per layer (a list of L ints); defaults to
     min(E, B*k) per layer (exact at batch 1)."""
@@ -48,7 +51,7 @@ def step_bytes(m: dict, seq_lens, expert_union=None, router_bias: bool = False) 
     experts = sum(expert_union) * pc["per_expert"] * 2
     head = (V * H + H) * 2
     embed = B * H * 2
-    kvt = kv_bytes_per_token(m)
+    kvt = kv_bytes_per_token(m, kv_q8)
     kv_read = sum(int(s) - 1 for s in seq_lens) * kvt     # cached positions; the new token comes from registers
     kv_write = B * kvt
     logits = B * V * 4

@@ -44,15 +44,19 @@ def _run(wl_name, w_dev, rows=None, bias=None):
     max_pages = max((L + ps - 1) // ps for L in lens)
     num_pages = W.pages_needed(lens, ps) + 8
     bt, _ = W.make_block_tables(lens, ps, num_pages, max_pages)
-    kv = W.make_kv_random(m, num_pages, ps, "cuda", used_pages=[int(p) for p in bt.flatten() if p >= 0])
+    used = [int(p) for p in bt.flatten() if p >= 0]
+    if wl.kv_q8:
+        kv = W.make_kv_q8_random(m, num_pages, ps, "cuda", used_pages=used)
+    else:
+        kv = W.make_kv_random(m, num_pages, ps, "cuda", used_pages=used)
     tokens = W.make_tokens(B, m["vocab"])
     rows = list(range(B)) if rows is None else rows
     # the oracle first: it reads the cache as it is before the step (the step appends this token)
-    fetch = DeviceFetch(w_dev, kv, bt.numpy(), lens, rows, ps)
-    dims = make_dims(m, ps, fetch.num_pages, fetch.max_pages)
+    fetch = DeviceFetch(w_dev, kv, bt.numpy(), lens, rows, ps, model=m, num_pages=num_pages)
+    dims = make_dims(m, ps, fetch.num_pages, fetch.max_pages, kv_q8=wl.kv_q8)
     trace = {}
     ref = Oracle("f32").decode_step_lazy(dims, fetch, tokens.numpy()[rows], np.array(lens)[rows], fetch.bt, trace)
-    eng = mk.Engine(m, w_dev, ps, num_pages, max(B, 1), max_pages)
+    eng = mk.Engine(m, w_dev, ps, num_pages, max(B, 1), max_pages, flags=mk.FLAG_KV_Q8 if wl.kv_q8 else 0)
     logits = eng.step(tokens.cuda(), np.array(lens, dtype=np.int32), bt.cuda(), kv)
     torch.cuda.synchronize()
     eng.check()
@@ -94,6 +98,12 @@ def test_30b_bs1_ctx8k(weights30b):
 
 @pytest.mark.parametrize("name", ["moe30b_bs1_ctx32k", "moe30b_bs1_ctx128k", "moe30b_bs1_ctx256k"])
 def test_30b_long_context(weights30b, name):
+    _run(name, weights30b["plain"])
+
+
+@pytest.mark.parametrize("name", ["moe30b_bs1_ctx128k_q8", "moe30b_bs1_ctx256k_q8"])
+def test_30b_long_context_q8_cache(weights30b, name):
+    # the reduced-byte cache at the contexts where the KV read dominates the step
     _run(name, weights30b["plain"])
 
 

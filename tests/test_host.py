@@ -53,7 +53,7 @@ def _cfg(model=W.TINY, ps=16, pages=64, mb=8, mpp=32, **over):
     ("num_q_heads", 3, mk.MK_ERR_INVALID_ARG), ("top_k", 9, mk.MK_ERR_INVALID_ARG),
     ("head_dim", 96, mk.MK_ERR_UNSUPPORTED), ("max_batch", 65, mk.MK_ERR_UNSUPPORTED),
     ("hidden", 4100, mk.MK_ERR_UNSUPPORTED), ("page_size", 512, mk.MK_ERR_UNSUPPORTED),
-    ("norm_topk", 2, mk.MK_ERR_INVALID_ARG), ("flags", 2, mk.MK_ERR_INVALID_ARG),
+    ("norm_topk", 2, mk.MK_ERR_INVALID_ARG), ("flags", 4, mk.MK_ERR_INVALID_ARG),
     ("num_experts", 300, mk.MK_ERR_UNSUPPORTED),
 ])
 def test_create_rejects_bad_config(field, value, code):
@@ -243,7 +243,7 @@ def test_simulated_step_random_shapes(seed):
 
 def test_config_flags_are_checked():
     cfg = _cfg()
-    cfg.flags = 2
+    cfg.flags = 4   # no such flag
     with pytest.raises(mk.MkError):
         mk.plan_static(cfg, 8)
 

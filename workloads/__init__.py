@@ -21,6 +21,8 @@ Workloads (each names its model, batch, lengths and page size):
   * ``moe30b_bs1_ctx32k`` / ``_ctx128k`` / ``_ctx256k`` -- batch 1, page 64.
   * ``moe30b_bs64_ragged`` -- batch 64, lengths floor(exp(U(ln 512, ln 32768))),
     tokens uniform over the vocab, Zipf(1.1) router prior, page 16.
+  * ``moe30b_bs1_ctx128k_q8`` / ``_ctx256k_q8`` -- batch 1, page 64, over a q8_0
+    cache (the reduced-byte variant; not one of the bf16 workloads of the metric).
 
 Random draws (seeds are fixed; each tensor of the model gets seed 1234 + its
 index in a fixed tensor list):
@@ -55,6 +57,7 @@ class Workload:
     steps: int = 1
     admit_step: int | None = None
     kv_source: str = "random"    # "random": N(0,1) bf16 pages; "prefill": the tests run teacher-forced steps
+    kv_q8: bool = False          # the cache holds q8_0 blocks (random codes and scales, see make_kv_q8_random)
 
 
 def _gen(seed: int, device) -> torch.Generator:
@@ -86,11 +89,14 @@ def get(name: str) -> Workload:
         return Workload(name, MOE30B, 1, 64, [ctx + 1])
     if name == "moe30b_bs64_ragged":
         return Workload(name, MOE30B, 64, 16, lengths_loguniform(64, 512, 32768), zipf=1.1)
+    if name in ("moe30b_bs1_ctx128k_q8", "moe30b_bs1_ctx256k_q8"):
+        ctx = 131072 if "128k" in name else 262144
+        return Workload(name, MOE30B, 1, 64, [ctx + 1], kv_q8=True)
     raise KeyError(name)
 
 
 NAMES = ("tiny_bs1_ctx64", "tiny_bs8_ragged", "moe30b_bs1_ctx8k", "moe30b_bs1_ctx32k", "moe30b_bs1_ctx128k",
-         "moe30b_bs1_ctx256k", "moe30b_bs64_ragged")
+         "moe30b_bs1_ctx256k", "moe30b_bs64_ragged", "moe30b_bs1_ctx128k_q8", "moe30b_bs1_ctx256k_q8")
 
 
 def scaled_model(model: dict, **over) -> dict:
