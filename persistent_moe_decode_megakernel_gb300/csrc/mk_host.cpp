@@ -36,7 +36,7 @@ cudaError_t launch_step(const Params& p, cudaStream_t s);
 int tb_for_batch(int B);
 cudaError_t transpose_down(const uint16_t* in, uint16_t* out, int E, int H, int F, cudaStream_t s);
 cudaError_t configure_kernels(int D, bool kv_q8);
-cudaError_t occupancy(int D, int* blocks);
+cudaError_t occupancy(int D, bool kv_q8, int* blocks);
 size_t smem_bytes();
 }  // namespace mk
 
@@ -427,7 +427,8 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_ctx** out) {
   if ((e = mk::configure_kernels(cfg->head_dim, (cfg->flags & MK_FLAG_KV_Q8) != 0)) != cudaSuccess)
     return cuda_fail(e, "cudaFuncSetAttribute");
   int blocks = 0;
-  if ((e = mk::occupancy(cfg->head_dim, &blocks)) != cudaSuccess) return cuda_fail(e, "occupancy");
+  if ((e = mk::occupancy(cfg->head_dim, (cfg->flags & MK_FLAG_KV_Q8) != 0, &blocks)) != cudaSuccess)
+    return cuda_fail(e, "occupancy");
   if (blocks < 1) return fail(MK_ERR_UNSUPPORTED, "the step kernel does not fit on an SM");
 
   if (prop.multiProcessorCount > mk::kMaxCtas) return fail(MK_ERR_UNSUPPORTED, "more than 256 SMs");

@@ -3017,9 +3017,9 @@ cudaError_t launch_any(const Params& p, int tb, size_t smem, cudaStream_t s) {
   return launch_t<4, D, Q8>(p, smem, s);
 }
 
-template <int D>
+template <int D, bool Q8>
 cudaError_t occupancy_d(int* blocks, size_t smem) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, step_kernel<1, D, false>, kThreads, smem);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, step_kernel<1, D, Q8>, kThreads, smem);
 }
 
 }  // namespace

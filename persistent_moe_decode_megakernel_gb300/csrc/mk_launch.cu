@@ -13,6 +13,7 @@ cudaError_t launch_d128_q8(const Params& p, int tb, size_t smem, cudaStream_t s)
 cudaError_t launch_d64(const Params& p, int tb, size_t smem, cudaStream_t s);
 cudaError_t occupancy_d128(int* blocks, size_t smem);
 cudaError_t occupancy_d64(int* blocks, size_t smem);
+cudaError_t occupancy_d128_q8(int* blocks, size_t smem);
 size_t smem_bytes_impl();
 
 size_t smem_bytes() { return smem_bytes_impl(); }
@@ -25,7 +26,8 @@ cudaError_t configure_kernels(int D, bool kv_q8) {
   return D == 128 ? configure_d128(smem_bytes()) : configure_d64(smem_bytes());
 }
 
-cudaError_t occupancy(int D, int* blocks) {
+cudaError_t occupancy(int D, bool kv_q8, int* blocks) {
+  if (kv_q8) return D == 128 ? occupancy_d128_q8(blocks, smem_bytes()) : cudaErrorInvalidValue;
   return D == 128 ? occupancy_d128(blocks, smem_bytes()) : occupancy_d64(blocks, smem_bytes());
 }
 

@@ -7,5 +7,6 @@ cudaError_t configure_d128_q8(size_t smem) { return configure_all<128, true>(sme
 cudaError_t launch_d128_q8(const Params& p, int tb, size_t smem, cudaStream_t s) {
   return launch_any<128, true>(p, tb, smem, s);
 }
+cudaError_t occupancy_d128_q8(int* blocks, size_t smem) { return occupancy_d<128, true>(blocks, smem); }
 
 }  // namespace mk
