@@ -192,6 +192,30 @@ int mk_decode_step_greedy(mk_ctx* ctx, int32_t batch, const int32_t* token_ids, 
                           float* margin, mk_stream_t stream);
 
 /*
+ * A decode step captured as a CUDA graph, for callers that decode the same batch shape many
+ * times: the host builds step n+1's data (tag, lengths, RoPE rows, attention split plan) into
+ * one of two pinned staging buffers while step n runs, and the launch is one graph replay
+ * (an upload node and the step kernel).  The plan's NEXT-2 ("Image 2" paragraph: the host
+ * schedules the step; per-step task counts follow the live lengths).
+ *   mk_graph_create: capture a step of `batch` rows over fixed device buffers token_ids,
+ *     block_tables, kv_pages and logits_out (meaning and layout as mk_decode_step).  Their
+ *     CONTENTS may change between launches; their addresses may not.  Captures on a private
+ *     stream; allocates two pinned and two device staging buffers and two graphs.  Errors:
+ *     MK_ERR_INVALID_ARG, MK_ERR_CUDA (e.g. a driver that cannot capture the launch), MK_ERR_OOM.
+ *   mk_graph_launch: this step's seq_lens (HOST int32 [batch], as mk_decode_step) and one
+ *     replay on `stream` (not the legacy default stream while another stream captures);
+ *     asynchronous; device errors through mk_get_status.  Steps of one context, captured or not,
+ *     must not overlap on the GPU.
+ *   mk_graph_destroy: waits for the graph's launches and frees it (NULL is ignored); the
+ *     context stays valid.
+ */
+typedef struct mk_graph mk_graph;
+int mk_graph_create(mk_ctx* ctx, int32_t batch, const int32_t* token_ids, const int32_t* block_tables, void* kv_pages,
+                    float* logits_out, mk_graph** out);
+int mk_graph_launch(mk_graph* graph, const int32_t* seq_lens, mk_stream_t stream);
+void mk_graph_destroy(mk_graph* graph);
+
+/*
  * Wait for the last enqueued step and report device-side errors.  Fills `out`
  * and returns out->code (MK_OK when the step ran clean).  Reading clears the
  * record.  After an error the context stays usable.

@@ -136,7 +136,7 @@ EXPORTS = ("mk_create", "mk_decode_step", "mk_decode_step_greedy", "mk_get_statu
            "mk_plan_attention", "mk_simulate", "mk_debug_read", "mk_debug_inject_stall", "mk_num_ctas",
            "mk_debug_trace", "mk_debug_trace_read", "mk_paged_attention_noalloc", "mk_kv_pool_create",
            "mk_kv_pool_destroy", "mk_kv_admit", "mk_kv_reserve", "mk_kv_evict", "mk_kv_fill", "mk_kv_free_pages",
-           "mk_kv_len")
+           "mk_kv_len", "mk_graph_create", "mk_graph_launch", "mk_graph_destroy")
 
 _lib = None
 _lock = threading.Lock()
@@ -174,6 +174,10 @@ def lib():
             L.mk_debug_read.argtypes = [vp, i32, i32, vp, ctypes.c_size_t]
             L.mk_debug_inject_stall.argtypes = [vp, i32, u32]
             L.mk_num_ctas.argtypes = [vp]
+            L.mk_graph_create.argtypes = [vp, i32, vp, vp, vp, vp, ctypes.POINTER(vp)]
+            L.mk_graph_launch.argtypes = [vp, vp, vp]
+            L.mk_graph_destroy.argtypes = [vp]
+            L.mk_graph_destroy.restype = None
             L.mk_debug_trace.argtypes = [vp, i32, i32]
             L.mk_debug_trace_read.argtypes = [vp, vp, ctypes.c_size_t]
             _lib = L
@@ -367,6 +371,20 @@ class Engine:
                                     ctypes.c_void_p(block_tables_ptr), ctypes.c_void_p(kv_ptr),
                                     ctypes.c_void_p(logits_ptr), ctypes.c_void_p(stream_ptr)))
 
+    def capture(self, tokens, block_tables, kv, logits):
+        """A CUDA graph of one step over these fixed device buffers (``mk_graph_create``); the
+        returned ``StepGraph`` launches it with each step's host lengths."""
+        import torch
+        B = tokens.numel()
+        assert tokens.is_cuda and tokens.dtype == torch.int32 and tokens.is_contiguous()
+        assert block_tables.is_cuda and block_tables.dtype == torch.int32 and block_tables.is_contiguous()
+        assert logits.is_cuda and logits.dtype == torch.float32 and logits.is_contiguous() and logits.shape[0] == B
+        g = ctypes.c_void_p()
+        _check(lib().mk_graph_create(self.ctx, B, _ptr(tokens), _ptr(block_tables), _ptr(kv), _ptr(logits),
+                                     ctypes.byref(g)))
+        self._last_b = B
+        return StepGraph(self, g, (tokens, block_tables, kv, logits))
+
     def status(self) -> dict:
         st = Status()
         rc = lib().mk_get_status(self.ctx, ctypes.byref(st))
@@ -410,6 +428,31 @@ class Engine:
         if self.ctx:
             lib().mk_destroy(self.ctx)
             self.ctx = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class StepGraph:
+    """A captured decode step (``mk_graph_*``): ``launch(seq_lens)`` replays it on a stream."""
+
+    def __init__(self, engine, handle, keep):
+        self.engine, self.g, self._keep = engine, handle, keep
+
+    def launch(self, seq_lens, stream=None):
+        import torch
+        sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        _check(lib().mk_graph_launch(self.g, sl.ctypes.data, ctypes.c_void_p(stream.cuda_stream)))
+
+    def close(self):
+        if self.g:
+            lib().mk_graph_destroy(self.g)
+            self.g = ctypes.c_void_p()
 
     def __del__(self):
         try:

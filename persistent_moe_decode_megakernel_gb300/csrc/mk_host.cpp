@@ -301,7 +301,7 @@ struct mk_ctx {
   mk_status* d_status = nullptr;
   // per-step staging (double-buffered)
   size_t step_bytes = 0;
-  size_t off_lens = 0, off_cos = 0, off_sin = 0, off_items = 0, off_item_off = 0, off_pair = 0;
+  size_t off_tag = 0, off_lens = 0, off_cos = 0, off_sin = 0, off_items = 0, off_item_off = 0, off_pair = 0;
   uint8_t* h_step[2] = {nullptr, nullptr};
   uint8_t* d_step[2] = {nullptr, nullptr};
   cudaEvent_t ev_step[2] = {nullptr, nullptr};
@@ -519,6 +519,7 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_ctx** out) {
   // per-step buffer layout
   size_t so = 0;
   auto take = [&](size_t bytes) { size_t r = so; so += (bytes + 15) & ~(size_t)15; return r; };
+  c->off_tag = take(16);
   c->off_lens = take((size_t)MB * i4);
   c->off_cos = take((size_t)MB * (D / 2) * f4);
   c->off_sin = take((size_t)MB * (D / 2) * f4);
@@ -561,34 +562,49 @@ int mk_decode_step_greedy(mk_ctx* c, int32_t batch, const int32_t* token_ids, co
   return decode_step(c, batch, token_ids, seq_lens, block_tables, kv_pages, logits_out, next_token, margin, stream);
 }
 
-static int decode_step(mk_ctx* c, int32_t batch, const int32_t* token_ids, const int32_t* seq_lens,
-                       const int32_t* block_tables, void* kv_pages, float* logits_out, int32_t* next_token,
-                       float* margin, mk_stream_t stream) {
-  g_err.clear();
+// Checks of one step's arguments shared by the plain and the captured step.
+static int check_step(mk_ctx* c, int32_t batch, const int32_t* token_ids, const int32_t* seq_lens,
+                      const int32_t* block_tables, void* kv_pages, float* logits_out) {
   if (!c) return fail(MK_ERR_INVALID_ARG, "ctx is NULL");
   const mk_config& cf = c->cfg;
   if (batch < 1 || batch > cf.max_batch) return fail(MK_ERR_INVALID_ARG, "batch %d outside 1..%d", batch, cf.max_batch);
-  if (!token_ids || !seq_lens || !block_tables || !kv_pages || !logits_out)
+  if (!token_ids || !block_tables || !kv_pages || !logits_out)
     return fail(MK_ERR_INVALID_ARG, "a step pointer is NULL");
   if (!aligned16(kv_pages)) return fail(MK_ERR_INVALID_ARG, "kv_pages must be 16-byte aligned");
   if ((reinterpret_cast<uintptr_t>(token_ids) | reinterpret_cast<uintptr_t>(block_tables) |
        reinterpret_cast<uintptr_t>(logits_out)) & 3u)
     return fail(MK_ERR_INVALID_ARG, "token_ids, block_tables and logits_out must be 4-byte aligned");
-  const int64_t max_len = (int64_t)cf.max_pages_per_seq * cf.page_size;
-  for (int b = 0; b < batch; ++b)
-    if (seq_lens[b] < 1 || seq_lens[b] > max_len)
-      return fail(MK_ERR_INVALID_ARG, "seq_lens[%d]=%d outside 1..%lld", b, seq_lens[b], (long long)max_len);
-  cudaError_t e;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // host-built per-step data into the staging buffer not used by the previous step
-  const int cur = c->cur;
-  if ((e = cudaEventSynchronize(c->ev_step[cur])) != cudaSuccess) return cuda_fail(e, "staging event");
-  uint8_t* h = c->h_step[cur];
+  if (seq_lens) {
+    const int64_t max_len = (int64_t)cf.max_pages_per_seq * cf.page_size;
+    for (int b = 0; b < batch; ++b)
+      if (seq_lens[b] < 1 || seq_lens[b] > max_len)
+        return fail(MK_ERR_INVALID_ARG, "seq_lens[%d]=%d outside 1..%lld", b, seq_lens[b], (long long)max_len);
+  }
+  return MK_OK;
+}
+
+// The next step tag (never 0).  Tagged words of an earlier step never match it; when the tag
+// wraps, the tagged buffers are cleared on `s` first, so that no word from 2^32 steps ago can.
+static int next_tag(mk_ctx* c, cudaStream_t s, uint32_t* tag) {
+  if (++c->tag == 0) {
+    cudaError_t e = cudaMemsetAsync(c->X, 0, c->tagged_bytes, s);
+    if (e != cudaSuccess) return cuda_fail(e, "tag wrap clear");
+    c->tag = 1;
+  }
+  *tag = c->tag;
+  return MK_OK;
+}
+
+// Host-built data of one step into staging buffer h (the layout the kernel reads from the
+// device copy): tag, lengths, RoPE rows (angles in fp64), attention split plan.
+static int fill_step(mk_ctx* c, uint8_t* h, int32_t batch, const int32_t* seq_lens, uint32_t tag) {
+  const mk_config& cf = c->cfg;
   std::vector<mk_attn_item> items;
   std::vector<int32_t> item_off, pair_first;
   build_attention_plan(cf, c->n_ctas, batch, seq_lens, items, item_off, pair_first);
   if ((int)items.size() > c->plan.info.max_items) return fail(MK_ERR_INVALID_ARG, "attention plan overflow");
   const int D = cf.head_dim;
+  std::memcpy(h + c->off_tag, &tag, sizeof tag);
   std::memcpy(h + c->off_lens, seq_lens, sizeof(int32_t) * batch);
   float* cs = reinterpret_cast<float*>(h + c->off_cos);
   float* sn = reinterpret_cast<float*>(h + c->off_sin);
@@ -603,13 +619,15 @@ static int decode_step(mk_ctx* c, int32_t batch, const int32_t* token_ids, const
   std::memcpy(h + c->off_items, items.data(), sizeof(mk_attn_item) * items.size());
   std::memcpy(h + c->off_item_off, item_off.data(), sizeof(int32_t) * item_off.size());
   std::memcpy(h + c->off_pair, pair_first.data(), sizeof(int32_t) * pair_first.size());
-  uint8_t* d = c->d_step[cur];
-  if ((e = cudaMemcpyAsync(d, h, c->step_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
-    return cuda_fail(e, "step upload");
-  if ((e = cudaEventRecord(c->ev_step[cur], s)) != cudaSuccess) return cuda_fail(e, "event record");
-  c->cur ^= 1;
+  return MK_OK;
+}
 
-  mk::Params p;
+// Launch parameters of a step whose device step data is at d.
+static int make_params(mk_ctx* c, mk::Params& p, int32_t batch, const uint8_t* d, const int32_t* token_ids,
+                       const int32_t* block_tables, void* kv_pages, float* logits_out, int32_t* next_token,
+                       float* margin) {
+  const mk_config& cf = c->cfg;
+  const int D = cf.head_dim;
   std::memset(&p, 0, sizeof p);
   p.L = cf.num_layers; p.H = cf.hidden; p.Hq = cf.num_q_heads; p.Hkv = cf.num_kv_heads; p.D = D;
   p.G = cf.num_q_heads / cf.num_kv_heads; p.E = cf.num_experts; p.K = cf.top_k; p.F = cf.expert_ffn;
@@ -621,13 +639,13 @@ static int decode_step(mk_ctx* c, int32_t batch, const int32_t* token_ids, const
   p.B = batch; p.max_batch = cf.max_batch; p.n_ctas = c->n_ctas;
   const mk_plan_info& in = c->plan.info;
   p.n_qkv_tiles = in.n_qkv_tiles; p.n_o_tiles = in.n_o_tiles; p.n_router_tiles = in.n_router_tiles;
-  uint32_t wd_ms = cf.watchdog_ms;
   p.tasks = c->d_tasks; p.task_off = c->d_task_off;
   p.layers = c->d_layers; p.embed = c->embed; p.final_norm = c->final_norm; p.lm_head = c->lm_head;
   p.tokens = token_ids; p.block_tables = block_tables; p.kv = static_cast<uint16_t*>(kv_pages); p.logits = logits_out;
   p.kv_q8 = (cf.flags & MK_FLAG_KV_Q8) ? 1 : 0;
   p.kv_layer_bytes = p.kv_q8 ? kv_q8_layer_bytes(cf) : 0;
   p.kv_code_bytes = p.kv_q8 ? kv_q8_code_bytes(cf) : 0;
+  p.step_tag = reinterpret_cast<const uint32_t*>(d + c->off_tag);
   p.seq_lens = reinterpret_cast<const int32_t*>(d + c->off_lens);
   p.rope_cos = reinterpret_cast<const float*>(d + c->off_cos);
   p.rope_sin = reinterpret_cast<const float*>(d + c->off_sin);
@@ -640,13 +658,6 @@ static int decode_step(mk_ctx* c, int32_t batch, const int32_t* token_ids, const
   p.PT = c->PT;
   p.next_token = next_token; p.margin = margin; p.argp = c->argp;
   p.max_items = c->plan.info.max_items;
-  // a fresh tag per step; tagged words of an earlier step never match it.  When the tag
-  // wraps, the tagged buffers are cleared so that no word from 2^32 steps ago can match.
-  if (++c->tag == 0) {
-    if ((e = cudaMemsetAsync(c->X, 0, c->tagged_bytes, s)) != cudaSuccess) return cuda_fail(e, "tag wrap clear");
-    c->tag = 1;
-  }
-  p.tag = c->tag;
   p.flags = c->flags; p.status = c->d_status;
   p.trace = c->trace; p.trace_cap = c->trace_cap;
   if (kv_pages != c->kv_map_ptr) {
@@ -656,19 +667,145 @@ static int decode_step(mk_ctx* c, int32_t batch, const int32_t* token_ids, const
   }
   static_assert(sizeof(CUtensorMap) == sizeof(p.kv_map), "tensor map size");
   std::memcpy(p.kv_map, &c->kv_map, sizeof(p.kv_map));
-
-  // test hook: the O-proj tiles of one layer wait for a tag that is never written
   p.stall_layer = -1;
+  p.watchdog_ns = (uint64_t)cf.watchdog_ms * 1000000ull;
+  return MK_OK;
+}
+
+static int decode_step(mk_ctx* c, int32_t batch, const int32_t* token_ids, const int32_t* seq_lens,
+                       const int32_t* block_tables, void* kv_pages, float* logits_out, int32_t* next_token,
+                       float* margin, mk_stream_t stream) {
+  g_err.clear();
+  if (!seq_lens) return fail(MK_ERR_INVALID_ARG, "a step pointer is NULL");
+  int rc = check_step(c, batch, token_ids, seq_lens, block_tables, kv_pages, logits_out);
+  if (rc) return rc;
+  cudaError_t e;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // host-built per-step data into the staging buffer not used by the previous step
+  const int cur = c->cur;
+  if ((e = cudaEventSynchronize(c->ev_step[cur])) != cudaSuccess) return cuda_fail(e, "staging event");
+  uint32_t tag;
+  if ((rc = next_tag(c, s, &tag))) return rc;
+  uint8_t* h = c->h_step[cur];
+  if ((rc = fill_step(c, h, batch, seq_lens, tag))) return rc;
+  uint8_t* d = c->d_step[cur];
+  if ((e = cudaMemcpyAsync(d, h, c->step_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    return cuda_fail(e, "step upload");
+  if ((e = cudaEventRecord(c->ev_step[cur], s)) != cudaSuccess) return cuda_fail(e, "event record");
+  c->cur ^= 1;
+  mk::Params p;
+  if ((rc = make_params(c, p, batch, d, token_ids, block_tables, kv_pages, logits_out, next_token, margin))) return rc;
+  // test hook: the O-proj tiles of one layer wait for a tag that is never written
   if (c->stall_layer >= 0) {
     p.stall_layer = c->stall_layer;
-    if (c->stall_ms) wd_ms = c->stall_ms;
+    if (c->stall_ms) p.watchdog_ns = (uint64_t)c->stall_ms * 1000000ull;
     c->stall_layer = -1;
   }
-  p.watchdog_ns = (uint64_t)wd_ms * 1000000ull;
   if ((e = mk::launch_step(p, s)) != cudaSuccess) return cuda_fail(e, "cooperative launch");
   if ((e = cudaEventRecord(c->ev_done, s)) != cudaSuccess) return cuda_fail(e, "event record");
   c->stepped = true;
   c->last_B = batch;
+  return MK_OK;
+}
+
+// ---------------------------------------------------------------- captured steps (CUDA graphs)
+struct mk_graph {
+  mk_ctx* c = nullptr;
+  int32_t batch = 0;
+  uint8_t* h[2] = {nullptr, nullptr};      // pinned host staging, one per graph
+  uint8_t* d[2] = {nullptr, nullptr};      // its device copy, read by the graph's kernel
+  cudaEvent_t ev[2] = {nullptr, nullptr};  // the graph's copy has read h (recorded after its launch)
+  cudaGraph_t g[2] = {nullptr, nullptr};
+  cudaGraphExec_t x[2] = {nullptr, nullptr};
+  int cur = 0;
+};
+
+void mk_graph_destroy(mk_graph* g) {
+  if (!g) return;
+  for (int i = 0; i < 2; ++i) {
+    if (g->ev[i]) cudaEventSynchronize(g->ev[i]);
+    if (g->x[i]) cudaGraphExecDestroy(g->x[i]);
+    if (g->g[i]) cudaGraphDestroy(g->g[i]);
+    if (g->h[i]) cudaFreeHost(g->h[i]);
+    cudaFree(g->d[i]);
+    if (g->ev[i]) cudaEventDestroy(g->ev[i]);
+  }
+  delete g;
+}
+
+int mk_graph_create(mk_ctx* c, int32_t batch, const int32_t* token_ids, const int32_t* block_tables, void* kv_pages,
+                    float* logits_out, mk_graph** out) {
+  g_err.clear();
+  if (!out) return fail(MK_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  int rc = check_step(c, batch, token_ids, nullptr, block_tables, kv_pages, logits_out);
+  if (rc) return rc;
+  mk_graph* g = new mk_graph();
+  g->c = c;
+  g->batch = batch;
+  cudaError_t e;
+  cudaStream_t cs = nullptr;
+  for (int i = 0; i < 2; ++i) {
+    if ((e = cudaHostAlloc((void**)&g->h[i], c->step_bytes, cudaHostAllocDefault)) != cudaSuccess ||
+        (e = cudaMalloc(&g->d[i], c->step_bytes)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&g->ev[i], cudaEventDisableTiming)) != cudaSuccess) {
+      mk_graph_destroy(g);
+      return cuda_fail(e, "graph staging");
+    }
+    std::memset(g->h[i], 0, c->step_bytes);
+  }
+  if ((e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking)) != cudaSuccess) {
+    mk_graph_destroy(g);
+    return cuda_fail(e, "capture stream");
+  }
+  for (int i = 0; i < 2 && rc == MK_OK; ++i) {
+    mk::Params p;
+    if ((rc = make_params(c, p, batch, g->d[i], token_ids, block_tables, kv_pages, logits_out, nullptr, nullptr)))
+      break;
+    if ((e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal)) != cudaSuccess) {
+      rc = cuda_fail(e, "begin capture");
+      break;
+    }
+    cudaError_t e1 = cudaMemcpyAsync(g->d[i], g->h[i], c->step_bytes, cudaMemcpyHostToDevice, cs);
+    cudaError_t e2 = e1 == cudaSuccess ? mk::launch_step(p, cs) : e1;
+    e = cudaStreamEndCapture(cs, &g->g[i]);
+    if (e2 != cudaSuccess) { rc = cuda_fail(e2, "capture of the step"); break; }
+    if (e != cudaSuccess) { rc = cuda_fail(e, "end capture"); break; }
+    if ((e = cudaGraphInstantiate(&g->x[i], g->g[i], 0)) != cudaSuccess) { rc = cuda_fail(e, "graph instantiate"); break; }
+  }
+  cudaStreamDestroy(cs);
+  if (rc) {
+    mk_graph_destroy(g);
+    return rc;
+  }
+  *out = g;
+  return MK_OK;
+}
+
+int mk_graph_launch(mk_graph* g, const int32_t* seq_lens, mk_stream_t stream) {
+  g_err.clear();
+  if (!g || !seq_lens) return fail(MK_ERR_INVALID_ARG, "graph or seq_lens is NULL");
+  mk_ctx* c = g->c;
+  const mk_config& cf = c->cfg;
+  const int64_t max_len = (int64_t)cf.max_pages_per_seq * cf.page_size;
+  for (int b = 0; b < g->batch; ++b)
+    if (seq_lens[b] < 1 || seq_lens[b] > max_len)
+      return fail(MK_ERR_INVALID_ARG, "seq_lens[%d]=%d outside 1..%lld", b, seq_lens[b], (long long)max_len);
+  cudaError_t e;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int i = g->cur;
+  // the graph that read this staging buffer two launches ago has finished with it
+  if ((e = cudaEventSynchronize(g->ev[i])) != cudaSuccess) return cuda_fail(e, "graph staging event");
+  uint32_t tag;
+  int rc = next_tag(c, s, &tag);
+  if (rc) return rc;
+  if ((rc = fill_step(c, g->h[i], g->batch, seq_lens, tag))) return rc;
+  if ((e = cudaGraphLaunch(g->x[i], s)) != cudaSuccess) return cuda_fail(e, "graph launch");
+  if ((e = cudaEventRecord(g->ev[i], s)) != cudaSuccess) return cuda_fail(e, "event record");
+  if ((e = cudaEventRecord(c->ev_done, s)) != cudaSuccess) return cuda_fail(e, "event record");
+  g->cur ^= 1;
+  c->stepped = true;
+  c->last_B = g->batch;
   return MK_OK;
 }
 

@@ -380,6 +380,7 @@ struct __align__(128) Smem {
   uint32_t prod_count, cons_count;
   int32_t flag;
   int32_t is_last;
+  uint32_t tag;          // this step's tag, read from the uploaded step data
 };
 
 static_assert(sizeof(Smem) + 1024 <= 227 * 1024, "shared memory (with the 1024-byte alignment pad) exceeds 227 KB");
@@ -425,8 +426,8 @@ __device__ __forceinline__ bool aborted(const Params& p) {
     }                                                                                       \
   } while (0)
 
-__device__ __noinline__ void ll_timeout(const Params& p, int op, int layer) {
-  record_error(p, MK_ERR_TIMEOUT, op, layer, MK_WAIT_DATA, 0, p.tag, -1, true);
+__device__ __noinline__ void ll_timeout(const Params& p, int op, int layer, uint32_t tag) {
+  record_error(p, MK_ERR_TIMEOUT, op, layer, MK_WAIT_DATA, 0, tag, -1, true);
 }
 
 // A batch of tagged loads written between LL_RETRY_BEGIN and LL_RETRY_END(ok) ORs the
@@ -455,18 +456,17 @@ __device__ __noinline__ bool ll_expired(const Params& p, uint64_t t0) {
 }
 
 // Gather n tagged words into shared-memory floats: dst[i] = value of word addr(i), i over
-// this thread's indices threadIdx.x + k * kConsumerThreads.  Loads go out 8 at a time (the
+// this thread's indices threadIdx.x + k * kConsumerThreads.  Loads go out kB at a time (8: the
 // body is inlined at every call site, and instruction fetch of the step's short phases is
 // dear: 16 at a time measured 9 % slower at batch 1, 4 at a time 1 % slower); a
 // batch is issued again for the words whose tags were stale, all of them at once, until
 // every word is current (one loaded L2 round trip per pass, the same code for the first and
 // the later passes).  False if the watchdog or an abort ended the wait.
-template <class Addr>
+template <int kB = 8, class Addr>
 __device__ __forceinline__ bool ll_gather(const Params& p, int n, Addr addr, float* dst, uint32_t tag) {
-  constexpr int kB = 8;
   #pragma unroll 1
   for (int base = threadIdx.x; base < n; base += kB * kConsumerThreads) {
-    uint32_t want = (1u << kB) - 1u;   // words of this batch not yet seen with the step's tag
+    uint32_t want = kB >= 32 ? 0xffffffffu : (1u << kB) - 1u;   // words of this batch not yet seen with the step's tag
     uint64_t t0 = 0;
     #pragma unroll 1
     for (uint32_t it = 0;; ++it) {
@@ -1086,7 +1086,7 @@ __device__ __forceinline__ float pick(const float (&a)[TB], int i) {
 // unstaged SwiGLU input of wide batches); ok is false if the watchdog or an abort ended it.
 // Returned by value so that the caller's registers never need an address.
 struct H8 { float v[8]; bool ok; };
-__device__ __noinline__ H8 load_h8(const Params& p, const uint64_t* src) {
+__device__ __noinline__ H8 load_h8(const Params& p, const uint64_t* src, uint32_t tag) {
   H8 r;
   r.ok = true;
   const uint64_t t0 = globaltimer();
@@ -1097,7 +1097,7 @@ __device__ __noinline__ H8 load_h8(const Params& p, const uint64_t* src) {
     for (int q = 0; q < 8; q += 2) {
       uint64_t a, b;
       ll_ld2(src + q, a, b);
-      st |= ll_stale(a, p.tag) | ll_stale(b, p.tag);
+      st |= ll_stale(a, tag) | ll_stale(b, tag);
       r.v[q] = ll_f(a);
       r.v[q + 1] = ll_f(b);
     }
@@ -1125,7 +1125,8 @@ struct Consumer {
   uint32_t nev = 1;     // trace events written (event 0 is the header)
   uint64_t twait = 0;   // when the current tile's dependency was met
 
-  __device__ Consumer(const Params& p_, Smem& S_) : p(p_), S(S_) {}
+  uint32_t tg;          // this step's tag (read from the step data at kernel start)
+  __device__ Consumer(const Params& p_, Smem& S_) : p(p_), S(S_), tg(S_.tag) {}
 
   __device__ void trace_event(uint32_t kind, const Meta& m, uint64_t t0) {
     if (!tr_on(p) || threadIdx.x != 0) return;
@@ -1211,7 +1212,7 @@ struct Consumer {
       const uint16_t* row = p.embed + static_cast<size_t>(tok) * H;
       uint64_t* x = p.X + static_cast<size_t>(b) * H;
       #pragma unroll 1
-      for (uint32_t col = m.lo + threadIdx.x; col < m.hi; col += kConsumerThreads) ll_st(x + col, bf1(row[col]), p.tag);
+      for (uint32_t col = m.lo + threadIdx.x; col < m.hi; col += kConsumerThreads) ll_st(x + col, bf1(row[col]), tg);
     }
     return true;
   }
@@ -1257,7 +1258,7 @@ struct Consumer {
     }
     if (o.resid != nullptr) v += isnan(rv) ? ll_f(ll_ld(o.resid + off)) : rv;
     if (o.bias != nullptr) v += __ldg(o.bias + row);
-    if (o.base != nullptr) ll_st(o.base + off, v, p.tag);
+    if (o.base != nullptr) ll_st(o.base + off, v, tg);
     else o.plain[off] = v;
   }
 
@@ -1292,7 +1293,9 @@ struct Consumer {
     const uint64_t* s2 = src[TB > 2 ? 2 : 0];
     const uint64_t* s3 = src[TB > 3 ? 3 : 0];
     const FastDiv dK(K);   // nt * K <= the scratch size < 2^16
-    bool ok = ll_gather(p, nt * K, [=](int i) {
+    // (the widest instantiation stages groups of 3-4 rows, 32 loads per thread per pass: 2 %
+    // faster at batch 64; the narrow ones keep 8, where the inlined code size matters more)
+    bool ok = ll_gather<TB == 4 ? 32 : 8>(p, nt * K, [=](int i) {
       const int tb = dK.div(i), k = i - tb * K;
       return (tb == 0 ? s0 : tb == 1 ? s1 : tb == 2 ? s2 : s3) + k;
     }, dst, tag);
@@ -1498,7 +1501,7 @@ struct Consumer {
     // GEMV input: 0 x_in/attn_norm, 1 attention output, 2 x_mid/ffn_norm, 3 x_final/final_norm
     const int kind = op == MK_OP_QKV ? 0 : op == MK_OP_OPROJ ? 1 : (op == MK_OP_ROUTER || gu) ? 2 : 3;
     // the test hook waits for a tag that is never written
-    const uint32_t tag = (op == MK_OP_OPROJ && l == p.stall_layer) ? (p.tag ^ 0x80000000u) : p.tag;
+    const uint32_t tag = (op == MK_OP_OPROJ && l == p.stall_layer) ? (tg ^ 0x80000000u) : tg;
     const int eop = gu ? MK_OP_MOE : op;
     trace_mark(10 + (op == MK_OP_ROUTER ? 0 : moe ? 20 : 40), l);
     // Gate/up with the whole batch in one register group and the MoE input cached: y is the
@@ -1655,7 +1658,7 @@ struct Consumer {
         if (TB <= kSmallMaxB && gu && p.small_moe) om.hoff = static_cast<int>(meta().idx) * p.F - S.gu_lo;
       }
     }
-    if (!ok) ll_timeout(p, eop, l);
+    if (!ok) ll_timeout(p, eop, l, tg);
     if (!cbar_and(wok && ok)) return false;
     if (op == MK_OP_HEAD && p.next_token != nullptr) head_top2(lo, hi);
     return true;
@@ -1812,15 +1815,15 @@ struct Consumer {
       int rb[TB];
 #pragma unroll
       for (int tb = 0; tb < TB; ++tb) rb[tb] = tb;
-      ok = stage_input(2, l, H, rb, B, p.tag, S.scr.attn);
+      ok = stage_input(2, l, H, rb, B, tg, S.scr.attn);
     }
     {
       const uint64_t* rl = p.RLOG + static_cast<size_t>(l) * p.max_batch * E;
-      ok = ll_gather(p, B * E, [=](int i) { return rl + i; }, lg, p.tag) && ok;
+      ok = ll_gather(p, B * E, [=](int i) { return rl + i; }, lg, tg) && ok;
     }
     #pragma unroll 1
     for (int e = threadIdx.x; e < E; e += kConsumerThreads) S.ecnt[e] = 0;
-    if (!ok) ll_timeout(p, MK_OP_ROUTER, l);
+    if (!ok) ll_timeout(p, MK_OP_ROUTER, l, tg);
     if (!cbar_and(ok)) return false;
     trace_mark(16, l);
     if (!p.norm_topk) {   // weights over all experts need each row's max and normaliser
@@ -2024,7 +2027,7 @@ struct Consumer {
             for (int q = 0; q < 8; q += 2) {
               uint64_t a, b;
               ll_ld2(src[tb] + e + q, a, b);
-              st_ |= ll_stale(a, p.tag) | ll_stale(b, p.tag);
+              st_ |= ll_stale(a, tg) | ll_stale(b, tg);
               y[j][q][tb] = ll_f(a);
               y[j][q + 1][tb] = ll_f(b);
             }
@@ -2059,7 +2062,7 @@ struct Consumer {
             const float4 b = *reinterpret_cast<const float4*>(hc + static_cast<size_t>(i) * p.F + e + 4);
             v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
           } else {
-            const H8 h = load_h8(p, p.HB + (static_cast<size_t>(l) * p.max_batch * p.K + i) * p.F + e);
+            const H8 h = load_h8(p, p.HB + (static_cast<size_t>(l) * p.max_batch * p.K + i) * p.F + e, tg);
 #pragma unroll
             for (int q = 0; q < 8; ++q) v[q] = h.v[q];
             ok = h.ok && ok;
@@ -2104,9 +2107,9 @@ struct Consumer {
       }
       if (hc != nullptr) {
         const uint64_t* src = p.HB + static_cast<size_t>(l) * p.max_batch * K * F;
-        ok = ll_gather(p, B * K * F, [=](int i) { return src + i; }, hc, p.tag);
+        ok = ll_gather(p, B * K * F, [=](int i) { return src + i; }, hc, tg);
       }
-      if (!ok) ll_timeout(p, MK_OP_MOE, l);
+      if (!ok) ll_timeout(p, MK_OP_MOE, l, tg);
       if (!cbar_and(ok)) return false;
     }
     trace_mark(41, l);
@@ -2190,7 +2193,7 @@ struct Consumer {
       if (last) break;
       if (!next_rec()) break;
     }
-    if (!ok) ll_timeout(p, MK_OP_MOE, l);
+    if (!ok) ll_timeout(p, MK_OP_MOE, l, tg);
     if (!cbar_and(wok && ok)) return false;
     trace_mark(42, l);
     // combine in slot order, residual
@@ -2202,7 +2205,7 @@ struct Consumer {
         #pragma unroll 1
         for (int j = 0; j < K; ++j) acc += P[(t * K + j) * nrow + r];
         ll_st(p.X + (2 * static_cast<size_t>(l) + 2) * xs + static_cast<size_t>(t) * p.H + r0 + r,
-              XM[t * nrow + r] + acc, p.tag);
+              XM[t * nrow + r] + acc, tg);
       }
     }
     return true;
@@ -2274,7 +2277,7 @@ struct Consumer {
     {
       uint64_t* mine = p.PT + (static_cast<size_t>(l) * N + blockIdx.x) * kSmallMaxB * H;
       #pragma unroll 1
-      for (int i = threadIdx.x * 2; i < B * H; i += kConsumerThreads * 2) ll_st2(mine + i, S.moe[i], S.moe[i + 1], p.tag);
+      for (int i = threadIdx.x * 2; i < B * H; i += kConsumerThreads * 2) ll_st2(mine + i, S.moe[i], S.moe[i + 1], tg);
     }
     cbar();   // the partial output has been read out of the scratch
     if (nrow <= 0) return true;
@@ -2292,8 +2295,8 @@ struct Consumer {
       const int q = i - ni, b = dbn.div(q), rem = q - b * N * nrow;
       const int j = dnr.div(rem), rr = rem - j * nrow;
       return pt + (static_cast<size_t>(j) * kSmallMaxB + b) * H + rr;
-    }, S.moe, p.tag);
-    if (!ok) ll_timeout(p, MK_OP_MOE, l);
+    }, S.moe, tg);
+    if (!ok) ll_timeout(p, MK_OP_MOE, l, tg);
     if (!cbar_and(ok)) return false;
     trace_mark(42, l);
     const float* part = S.moe + ni;
@@ -2307,7 +2310,7 @@ struct Consumer {
         for (int j = lane; j < N; j += 32) v += part[(b * N + j) * nrow + rr];
       v = warp_sum(v);
       if (it < ni && lane == 0)
-        ll_st(p.X + (2 * static_cast<size_t>(l) + 2) * xs + static_cast<size_t>(b) * H + r0 + rr, S.moe[it] + v, p.tag);
+        ll_st(p.X + (2 * static_cast<size_t>(l) + 2) * xs + static_cast<size_t>(b) * H + r0 + rr, S.moe[it] + v, tg);
     }
     return true;
   }
@@ -2498,7 +2501,7 @@ struct Consumer {
       for (int k = 0; k < 11; ++k) w[k] = ((need >> k) & 1u) ? ll_ld(wp[k]) : 0ull;
       uint32_t stale = 0;
 #pragma unroll
-      for (int k = 0; k < 11; ++k) stale |= static_cast<uint32_t>(((need >> k) & 1u) && !ll_ok(w[k], p.tag)) << k;
+      for (int k = 0; k < 11; ++k) stale |= static_cast<uint32_t>(((need >> k) & 1u) && !ll_ok(w[k], tg)) << k;
       if (stale != 0u) {   // re-poll the stale words, all of them per sweep
         const uint64_t t0 = globaltimer();
         #pragma unroll 1
@@ -2508,7 +2511,7 @@ struct Consumer {
             if ((stale >> k) & 1u) w[k] = ll_ld(wp[k]);
           uint32_t still = 0;
 #pragma unroll
-          for (int k = 0; k < 11; ++k) still |= static_cast<uint32_t>(((stale >> k) & 1u) && !ll_ok(w[k], p.tag)) << k;
+          for (int k = 0; k < 11; ++k) still |= static_cast<uint32_t>(((stale >> k) & 1u) && !ll_ok(w[k], tg)) << k;
           stale = still;
           if (stale != 0u && (it & 15u) == 0u && (aborted(p) || globaltimer() - t0 > p.watchdog_ns)) {
             ok = false;
@@ -2563,7 +2566,7 @@ struct Consumer {
         kvcur[D + i] = to_bf16_bits(ll_f(w[10]));
       }
     }
-    if (!ok) ll_timeout(p, MK_OP_ATTN, l);
+    if (!ok) ll_timeout(p, MK_OP_ATTN, l, tg);
     if (!cbar_and(ok)) return false;
     if (item.split == 0) {
       // append this token's k and v to the cache
@@ -2749,9 +2752,9 @@ struct Consumer {
           const float4 ov = *reinterpret_cast<const float4*>(st + w * kStride + h * D + d);
           acc.x += f * ov.x; acc.y += f * ov.y; acc.z += f * ov.z; acc.w += f * ov.w;
         }
-        ll_st2(po + h * D + d, acc.x, acc.y, p.tag);
-        ll_st2(po + h * D + d + 2, acc.z, acc.w, p.tag);
-        if (d == 0) ll_st2(pml + 2 * h, M, L, p.tag);
+        ll_st2(po + h * D + d, acc.x, acc.y, tg);
+        ll_st2(po + h * D + d + 2, acc.z, acc.w, tg);
+        if (d == 0) ll_st2(pml + 2 * h, M, L, tg);
       }
     }
     fence_proxy_async_smem();   // the generic writes into the slot precede its next TMA fill
@@ -2793,8 +2796,8 @@ struct Consumer {
         }
         const int j = i - nml, sp = dsl.div(j);
         return po + static_cast<size_t>(sp) * kMaxG * D + o0 + (j - sp * nsl);
-      }, S.moe + 0, p.tag) && ok;
-      if (!ok) ll_timeout(p, MK_OP_ATTN, l);
+      }, S.moe + 0, tg) && ok;
+      if (!ok) ll_timeout(p, MK_OP_ATTN, l, tg);
       if (!cbar_and(ok)) return false;
       trace_mark(64, l);
       #pragma unroll 1
@@ -2833,7 +2836,7 @@ struct Consumer {
         acc += __shfl_xor_sync(0xffffffffu, acc, 1);
         acc += __shfl_xor_sync(0xffffffffu, acc, 2);
         acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-        if (oi < nsl && sub == 0) ll_st(att + o0 + oi, acc, p.tag);
+        if (oi < nsl && sub == 0) ll_st(att + o0 + oi, acc, tg);
       }
       cbar();
     }
@@ -2907,6 +2910,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     S.prod_count = 0;
     S.cons_count = 0xffffffffu;
     S.ykey = -1;
+    S.tag = *p.step_tag;   // a replayed launch (CUDA graph) gets a fresh tag through the step data
     if (tr_on(p)) p.trace[static_cast<size_t>(blockIdx.x) * p.trace_cap * 4 + 1] = globaltimer();
     fence_mbar_init();
   }
@@ -2995,11 +2999,21 @@ cudaError_t configure_t(size_t smem) {
                               static_cast<int>(smem));
 }
 
+// One block per SM, all resident at once (a cooperative launch: blocks wait on one another's
+// data).  Launched through cudaLaunchKernelEx so that stream capture records it in a graph.
 template <int TB, int D, bool Q8>
 cudaError_t launch_t(const Params& p, size_t smem, cudaStream_t s) {
-  void* args[] = {const_cast<Params*>(&p)};
-  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(step_kernel<TB, D, Q8>), dim3(p.n_ctas),
-                                     dim3(kThreads), args, smem, s);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.n_ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, step_kernel<TB, D, Q8>, p);
 }
 
 template <int D, bool Q8>

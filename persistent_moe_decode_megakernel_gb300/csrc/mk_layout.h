@@ -174,7 +174,8 @@ struct alignas(64) Params {
   // the fp32 (or int32) value in the low half and the step's tag in the high half, written
   // with one 64-bit store.  A reader that sees the current tag has the value of this step;
   // no fence is needed between writer and reader.
-  uint32_t tag;        // this step's tag (never 0)
+  const uint32_t* step_tag;  // this step's tag (never 0), in the uploaded step data so that a
+                             // replayed launch of a captured graph reads a fresh one
   int32_t stall_layer; // test hook: the O-proj of this layer waits for a tag that never comes (-1: off)
   uint64_t* X;     // [2L+1][max_batch][H] residual stream: layer input at 2l, after attention at 2l+1
   uint64_t* QKV;   // [L][max_batch][nqkv]

@@ -255,3 +255,12 @@ def test_simulator_detects_a_missing_producer():
     bad[0, 0, 0] = 99
     with pytest.raises(mk.MkError):
         mk.simulate(cfg, 8, [5], bad)
+
+
+def test_graph_calls_check_their_arguments():
+    # the captured-step calls reject missing arguments before touching a GPU
+    L = mk.lib()
+    out = ctypes.c_void_p()
+    assert L.mk_graph_create(None, 1, None, None, None, None, ctypes.byref(out)) == mk.MK_ERR_INVALID_ARG
+    assert L.mk_graph_launch(None, None, None) == mk.MK_ERR_INVALID_ARG
+    L.mk_graph_destroy(None)   # NULL is ignored
