@@ -54,6 +54,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-s", type=float, default=12.0, help="target seconds of oracle work for the baseline")
+    ap.add_argument("--no-down-copy", action="store_true",
+                    help="build the engine without the transposed down-projection copy (MK_FLAG_NO_DOWN_COPY)")
+    ap.add_argument("--no-graph", action="store_true", help="skip the captured-step (CUDA graph) timing")
     ap.add_argument("--configs", default="all",
                     help="other 30B workloads measured in the same run and reported under 'configs' "
                          "(comma-separated names, 'all' or 'none')")
@@ -168,9 +171,41 @@ def setup_workload(wl, layers_override, device, weights=None):
                 tokens=tokens, bias=bias, kv_q8=wl.kv_q8)
 
 
+NO_DOWN_COPY = False   # set from --no-down-copy
+
+
 def engine_flags(st) -> int:
     import persistent_moe_decode_megakernel_gb300 as mk
-    return mk.FLAG_KV_Q8 if st["kv_q8"] else 0
+    return (mk.FLAG_KV_Q8 if st["kv_q8"] else 0) | (mk.FLAG_NO_DOWN_COPY if NO_DOWN_COPY else 0)
+
+
+def measure_graph(eng, st, steps, warmup):
+    """The same step captured once as a CUDA graph and replayed (mk_graph_launch), inputs
+    resident on the device; mean ms per step from CUDA events around the replays."""
+    import torch
+    m, B = st["model"], st["B"]
+    stream = torch.cuda.Stream()
+    tok_d = st["tokens"].cuda()
+    bt_d = st["bt"].cuda()
+    sl = np.array(st["lens"], dtype=np.int32)
+    logits = torch.empty(B, m["vocab"], dtype=torch.float32, device="cuda")
+    graph = eng.capture(tok_d, bt_d, st["kv"], logits)
+    for _ in range(warmup):
+        graph.launch(sl, stream)
+    stream.synchronize()
+    eng.check()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        graph.launch(sl, stream)
+    e1.record(stream)
+    stream.synchronize()
+    eng.check()
+    graph.close()
+    ms = e0.elapsed_time(e1) / steps
+    return {"ms_per_step": ms, "value": B / (ms / 1e3), "unit": "tok/s",
+            "note": "the step captured once (mk_graph_create) and replayed per step (mk_graph_launch); "
+                    "the host builds each step's data while the previous one runs"}
 
 
 def cpu_baseline(st, budget_s: float):
@@ -367,6 +402,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    global NO_DOWN_COPY
+    NO_DOWN_COPY = args.no_down_copy
     import torch
     import persistent_moe_decode_megakernel_gb300 as mk
 
@@ -387,6 +424,7 @@ def main():
     ms_mean, ms_med, value, cs, e2e, wall = measure(eng, st, args.steps, args.warmup, local, world,
                                                     not args.no_e2e)
     roof = roofline_of(eng, st, wl.name, ms_mean)
+    graph = None if args.no_graph else measure_graph(eng, st, args.steps, args.warmup)
     eng.close()
     cb = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -449,6 +487,10 @@ def main():
                 "gpu_launches": args.steps, "wall_s_timed": wall}
         if e2e:
             line["e2e"] = e2e
+        if graph:
+            line["graph"] = graph
+        if NO_DOWN_COPY:
+            line["config"]["down_projection"] = "no transposed copy (MK_FLAG_NO_DOWN_COPY)"
         if cb:
             line["cpu_baseline"] = cb
         if others:
