@@ -129,11 +129,31 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
   return y;
 }
-// the two signed bytes in the low half of u (first in bits 0-7) -> bf16x2, exactly (|v| <= 128)
-__device__ __forceinline__ uint32_t s8x2_bf16x2(uint32_t u) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(static_cast<float>(static_cast<int8_t>(u & 0xffu)),
-                                                 static_cast<float>(static_cast<int8_t>((u >> 8) & 0xffu)));
-  return *reinterpret_cast<const uint32_t*>(&h);
+// Signed bytes -> fp16, exactly: with its sign bit flipped a byte b is the unsigned b + 128, and
+// the fp16 whose high byte is 0x64 and low byte is u has the value 1024 + u; subtracting 1152
+// leaves b.  (fp16 keeps every integer below 2048 exactly.)
+__device__ __forceinline__ uint32_t s8_to_f16x2(uint32_t x, uint32_t sel) {   // the two bytes sel picks
+  const uint32_t h = __byte_perm(x ^ 0x80808080u, 0x64646464u, sel);
+  const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&h), __half2half2(__ushort_as_half(0x6480u)));
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+// the two signed bytes in the low half of u (first in bits 0-7) -> f16x2
+__device__ __forceinline__ uint32_t s8x2_f16x2(uint32_t u) { return s8_to_f16x2(u, 0x4140u); }
+// d += a(16x16 f16, row) * b(16x8 f16, col), fp32 accumulate (a pure register operation: the
+// compiler may schedule it freely)
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// two floats -> f16x2 (first in the low half), and the f16x2 of what rounding left over
+__device__ __forceinline__ void split_f16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(a, b);
+  const __half2 r = __floats2half2_rn(a - __low2float(h), b - __high2float(h));
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&r);
 }
 __device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
   uint16_t v;
@@ -2335,17 +2355,37 @@ struct Consumer {
 
   // q8_0 chunks: the slot holds [K codes][V codes][K scales][V scales] of pages_per_chunk_q8 pages,
   // codes as rows of D bytes with the TMA 128-byte swizzle (16-byte piece j of row r at piece
-  // j ^ (r & 7)).  S^T = K Q^T runs per 32-dim block on the codes (exact in bf16), and each block's
-  // partial is multiplied by the row's K scale; O^T += V^T P^T runs per 32-dim block with the row's
-  // V scale folded into P.  Rows past the sequence get scale 0 (their codes are finite).
+  // j ^ (r & 7)), scales as rows of D / 32 f16.  A warp takes 32 rows at a time (two 16-row
+  // halves under one softmax update).  Codes become fp16 exactly, straight into MMA fragments:
+  //  * S^T = K Q^T per 32-dim block: ldmatrix (b16) hands lane (g, t) bytes 4t .. 4t + 3 of a
+  //    16-byte piece of rows g and g + 8; q's fragment takes its dims in that order.  Each
+  //    block's partial is multiplied by the row's K scale.
+  //  * O^T += V^T P^T per 32-dim block: ldmatrix.trans (b16) hands lane (g, t) dims 2g, 2g + 1
+  //    of rows 2t and 2t + 1, so output row g of tile m is dim 16m + 2g and row g + 8 is dim
+  //    16m + 2g + 1 (undone where o is stored).  The rows' V scales are folded into P.
+  // P carries a factor 2^6 (in the exponent, so ls carries it too and o / ls is unchanged) that
+  // keeps small P x scale products out of fp16's subnormal range.  Rows past the sequence are
+  // masked (their codes are finite; their V scales are replaced by 0).
   static __device__ __forceinline__ uint32_t swz8(int r, int c) {
     return static_cast<uint32_t>(r * D + ((((c >> 4) ^ r) & 7) << 4) + (c & 15));
+  }
+  static __device__ __forceinline__ uint2 lds_v2(uint32_t a) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+  }
+  static __device__ __forceinline__ void f16x4_f32(uint2 v, float (&f)[4]) {
+    const __half2 a = *reinterpret_cast<const __half2*>(&v.x), b = *reinterpret_cast<const __half2*>(&v.y);
+    f[0] = __low2float(a); f[1] = __high2float(a); f[2] = __low2float(b); f[3] = __high2float(b);
   }
   __device__ __forceinline__ void attn_chunks_q8(int Lc, int pos, const uint16_t* kvcur, float (&o)[D / 16][4],
                                                  float (&mx)[2], float (&ls)[2]) {
     constexpr int NB = D / 32;   // scale blocks per row
+    static_assert(NB == 4, "one 8-byte load holds a row's scales");
+    constexpr float kLnP = 4.15888308336f;   // ln(2^6)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
+    const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8, lpc = lane >> 4;   // ldmatrix row and piece of this lane
     const uint4* qf = reinterpret_cast<const uint4*>(S.scr.attn);
     const int rows_cap = pages_per_chunk_q8(p.ps, D) * p.ps;
     for (;;) {
@@ -2355,12 +2395,12 @@ struct Consumer {
       uint8_t* sl8 = const_cast<uint8_t*>(slot());
       const uint32_t Kc = smem_u32(sl8);
       const uint32_t Vc = Kc + rows_cap * D;
-      uint16_t* ksc = reinterpret_cast<uint16_t*>(sl8 + 2 * rows_cap * D);
-      uint16_t* vsc = ksc + rows_cap * NB;
+      const uint32_t Ks = Kc + 2 * rows_cap * D;                       // K scales, 8 bytes a row
+      const uint32_t Vs = Ks + rows_cap * NB * 2;
 #pragma unroll 1
-      for (int tile = warp; tile * 16 < npos; tile += kConsumerWarps) {
-        const int r0 = tile * 16;
-        if (pos >= p0 + r0 && pos < p0 + r0 + 16) {
+      for (int tile = warp; tile * 32 < npos; tile += kConsumerWarps) {
+        const int r0 = tile * 32;
+        if (pos >= p0 + r0 && pos < p0 + r0 + 32) {
           // this token's codes and scales are not in the copied page yet: put them in its rows
           const int rr = pos - p0;
           const uint8_t* c8 = reinterpret_cast<const uint8_t*>(kvcur);
@@ -2374,80 +2414,95 @@ struct Consumer {
           }
           if (lane < 2 * NB) {
             const uint16_t* s8 = reinterpret_cast<const uint16_t*>(c8 + 2 * D);
-            (lane < NB ? ksc : vsc)[rr * NB + (lane % NB)] = s8[lane];
+            uint16_t* sc16 = reinterpret_cast<uint16_t*>(sl8 + 2 * rows_cap * D);
+            (lane < NB ? sc16 : sc16 + rows_cap * NB)[rr * NB + (lane % NB)] = s8[lane];
           }
           fence_proxy_async_smem();   // these generic writes precede the slot's next TMA fill
           __syncwarp();
         }
-        const int ra = r0 + g, rb = r0 + g + 8;
-        // S^T = K Q^T, block by block
-        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+        // S^T = K Q^T for both halves, block by block
+        float sc[2][4];
 #pragma unroll
-        for (int b = 0; b < NB; ++b) {
-          float ab[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int h = 0; h < 2; ++h) {
+          const int ra = r0 + 16 * h + g;
+          float kd[2][4];
+          f16x4_f32(lds_v2(Ks + ra * (NB * 2)), kd[0]);
+          f16x4_f32(lds_v2(Ks + (ra + 8) * (NB * 2)), kd[1]);
+          sc[h][0] = sc[h][1] = sc[h][2] = sc[h][3] = 0.f;
+          const int lr = r0 + 16 * h + lrow;
 #pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            const int s2 = 2 * b + h2;
-            const int col = 16 * s2 + 2 * t;
-            uint32_t a[4];
-            a[0] = s8x2_bf16x2(lds_u16(Kc + swz8(ra, col)));
-            a[1] = s8x2_bf16x2(lds_u16(Kc + swz8(rb, col)));
-            a[2] = s8x2_bf16x2(lds_u16(Kc + swz8(ra, col + 8)));
-            a[3] = s8x2_bf16x2(lds_u16(Kc + swz8(rb, col + 8)));
-            const uint4 q = qf[s2 * 32 + lane];
-            mma_bf16(ab, a, q.x, q.y);
-            mma_bf16(ab, a, q.z, q.w);
+          for (int b = 0; b < NB; ++b) {
+            uint32_t x[4];   // rows g, g + 8 of piece 2b, then of piece 2b + 1
+            ldsm_x4(Kc + swz8(lr, 16 * (2 * b + lpc)), x);
+            float ab[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const uint32_t xa = x[2 * h2], xb = x[2 * h2 + 1];
+              const uint32_t a[4] = {s8_to_f16x2(xa, 0x4140u), s8_to_f16x2(xb, 0x4140u), s8_to_f16x2(xa, 0x4342u),
+                                     s8_to_f16x2(xb, 0x4342u)};
+              const uint4 q = qf[(2 * b + h2) * 32 + lane];
+              mma_f16(ab, a, q.x, q.y);
+              mma_f16(ab, a, q.z, q.w);
+            }
+            sc[h][0] = fmaf(ab[0], kd[0][b], sc[h][0]);
+            sc[h][1] = fmaf(ab[1], kd[0][b], sc[h][1]);
+            sc[h][2] = fmaf(ab[2], kd[1][b], sc[h][2]);
+            sc[h][3] = fmaf(ab[3], kd[1][b], sc[h][3]);
           }
-          const float da = ra < npos ? f16_f32(ksc[ra * NB + b]) : 0.f;
-          const float db = rb < npos ? f16_f32(ksc[rb * NB + b]) : 0.f;
-          sc[0] = fmaf(ab[0], da, sc[0]);
-          sc[1] = fmaf(ab[1], da, sc[1]);
-          sc[2] = fmaf(ab[2], db, sc[2]);
-          sc[3] = fmaf(ab[3], db, sc[3]);
+          if (ra >= npos) { sc[h][0] = -INFINITY; sc[h][1] = -INFINITY; }
+          if (ra + 8 >= npos) { sc[h][2] = -INFINITY; sc[h][3] = -INFINITY; }
         }
-        if (ra >= npos) { sc[0] = -INFINITY; sc[1] = -INFINITY; }
-        if (rb >= npos) { sc[2] = -INFINITY; sc[3] = -INFINITY; }
-        // online softmax per head column (heads 2t, 2t+1 on this lane)
-        float pa[2], pb[2], cr[2];
+        // online softmax per head column (heads 2t, 2t+1 on this lane), over the 32 rows
+        float pr[2][2][2], cr[2];   // [half][row g / g + 8][head]
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-          float tm = fmaxf(sc[j], sc[j + 2]);
+          float tm = fmaxf(fmaxf(sc[0][j], sc[0][j + 2]), fmaxf(sc[1][j], sc[1][j + 2]));
           tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 4));
           tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 8));
           tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
           const float mn = fmaxf(mx[j], tm);
+          const float me = mn - kLnP;
           cr[j] = mx[j] == -INFINITY ? 0.f : __expf(mx[j] - mn);
-          pa[j] = sc[j] == -INFINITY ? 0.f : __expf(sc[j] - mn);
-          pb[j] = sc[j + 2] == -INFINITY ? 0.f : __expf(sc[j + 2] - mn);
-          ls[j] = ls[j] * cr[j] + pa[j] + pb[j];
+          float sum = 0.f;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            pr[h][0][j] = sc[h][j] == -INFINITY ? 0.f : __expf(sc[h][j] - me);
+            pr[h][1][j] = sc[h][j + 2] == -INFINITY ? 0.f : __expf(sc[h][j + 2] - me);
+            sum += pr[h][0][j] + pr[h][1][j];
+          }
+          ls[j] = ls[j] * cr[j] + sum;
           mx[j] = mn;
         }
 #pragma unroll
         for (int mm = 0; mm < D / 16; ++mm) {
           o[mm][0] *= cr[0]; o[mm][1] *= cr[1]; o[mm][2] *= cr[0]; o[mm][3] *= cr[1];
         }
-        // O^T += V^T P^T, block by block with the block's V scales in P
+        // O^T += V^T P^T, per half and block, with the block's V scales in P
 #pragma unroll
-        for (int b = 0; b < NB; ++b) {
-          const float va = ra < npos ? f16_f32(vsc[ra * NB + b]) : 0.f;
-          const float vb = rb < npos ? f16_f32(vsc[rb * NB + b]) : 0.f;
-          uint32_t xa_h, xa_l, xb_h, xb_l;
-          split_bf16x2(pa[0] * va, pa[1] * va, xa_h, xa_l);
-          split_bf16x2(pb[0] * vb, pb[1] * vb, xb_h, xb_l);
-          const uint32_t b0h = movmatrix_t(xa_h), b0l = movmatrix_t(xa_l);
-          const uint32_t b1h = movmatrix_t(xb_h), b1l = movmatrix_t(xb_l);
+        for (int h = 0; h < 2; ++h) {
+          const int ra = r0 + 16 * h + g;
+          float vd[2][4];
+          f16x4_f32(lds_v2(Vs + ra * (NB * 2)), vd[0]);
+          f16x4_f32(lds_v2(Vs + (ra + 8) * (NB * 2)), vd[1]);
+          const bool va_on = ra < npos, vb_on = ra + 8 < npos;
+          const int lr = r0 + 16 * h + lrow;
 #pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            const int mm = 2 * b + h2;
-            const int dc = 16 * mm + g;      // this lane's A rows: dims dc and dc + 8
-            const int pr = r0 + 2 * t;       // its A columns: positions pr, pr + 1, pr + 8, pr + 9
-            uint32_t a[4];
-            a[0] = s8x2_bf16x2(lds_u8(Vc + swz8(pr, dc)) | (lds_u8(Vc + swz8(pr + 1, dc)) << 8));
-            a[1] = s8x2_bf16x2(lds_u8(Vc + swz8(pr, dc + 8)) | (lds_u8(Vc + swz8(pr + 1, dc + 8)) << 8));
-            a[2] = s8x2_bf16x2(lds_u8(Vc + swz8(pr + 8, dc)) | (lds_u8(Vc + swz8(pr + 9, dc)) << 8));
-            a[3] = s8x2_bf16x2(lds_u8(Vc + swz8(pr + 8, dc + 8)) | (lds_u8(Vc + swz8(pr + 9, dc + 8)) << 8));
-            mma_bf16(o[mm], a, b0h, b1h);
-            mma_bf16(o[mm], a, b0l, b1l);
+          for (int b = 0; b < NB; ++b) {
+            const float va = va_on ? vd[0][b] : 0.f, vb = vb_on ? vd[1][b] : 0.f;
+            uint32_t xa_h, xa_l, xb_h, xb_l;
+            split_f16x2(pr[h][0][0] * va, pr[h][0][1] * va, xa_h, xa_l);
+            split_f16x2(pr[h][1][0] * vb, pr[h][1][1] * vb, xb_h, xb_l);
+            const uint32_t b0h = movmatrix_t(xa_h), b0l = movmatrix_t(xa_l);
+            const uint32_t b1h = movmatrix_t(xb_h), b1l = movmatrix_t(xb_l);
+            uint32_t y[4];   // rows 0-7 and 8-15 of piece 2b, then of piece 2b + 1, transposed
+            ldsm_x4_t(Vc + swz8(lr, 16 * (2 * b + lpc)), y);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const uint32_t a[4] = {s8_to_f16x2(y[2 * u], 0x4240u), s8_to_f16x2(y[2 * u], 0x4341u),
+                                     s8_to_f16x2(y[2 * u + 1], 0x4240u), s8_to_f16x2(y[2 * u + 1], 0x4341u)};
+              mma_f16(o[2 * b + u], a, b0h, b1h);
+              mma_f16(o[2 * b + u], a, b0l, b1l);
+            }
           }
         }
       }
@@ -2470,8 +2525,9 @@ struct Consumer {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     // Q^T as the B operand of S^T = K Q^T, one 16-byte fragment per (k-step, lane):
-    // lane (g, t) holds head g at dims 16s + 2t (+1) and 16s + 2t + 8 (+1), hi then lo parts
-    // of the rotated, scaled q (zero for heads at or above G); then this token's bf16 k and v.
+    // lane (g, t) holds head g at dims 16s + 2t (+1) and 16s + 2t + 8 (+1) (with a q8_0 cache:
+    // dims 16s + 4t .. 16s + 4t + 3, the order its K fragments are read in), hi then lo parts
+    // of the rotated, scaled q (zero for heads at or above G); then this token's k and v.
     // Every tagged load of the prologue is issued before the first is used.
     uint4* qf = reinterpret_cast<uint4*>(S.scr.attn);                     // [KS][32]
     uint16_t* kvcur = reinterpret_cast<uint16_t*>(S.scr.attn + KS * 32 * 4);  // [2][D]
@@ -2494,7 +2550,7 @@ struct Consumer {
       const uint64_t* wp[11];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const int d = 16 * s2 + 2 * tt + 8 * (j >> 1) + (j & 1);
+        const int d = Q8 ? 16 * s2 + 4 * tt + j : 16 * s2 + 2 * tt + 8 * (j >> 1) + (j & 1);
         wp[2 * j] = qh + d;
         wp[2 * j + 1] = qh + (d < D / 2 ? d + D / 2 : d - D / 2);
       }
@@ -2527,7 +2583,7 @@ struct Consumer {
       if (qon) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const int d = 16 * s2 + 2 * tt + 8 * (j >> 1) + (j & 1);
+          const int d = Q8 ? 16 * s2 + 4 * tt + j : 16 * s2 + 2 * tt + 8 * (j >> 1) + (j & 1);
           const int dh = d % (D / 2);
           const float raw = ll_f(w[2 * j]), other = ll_f(w[2 * j + 1]);
           const float c = __ldg(cs + dh), sv = __ldg(sn + dh);
@@ -2536,8 +2592,13 @@ struct Consumer {
       }
       if (qunit) {
         uint4 f;
-        split_bf16x2(v[0], v[1], f.x, f.z);
-        split_bf16x2(v[2], v[3], f.y, f.w);
+        if constexpr (Q8) {   // the q8_0 tile multiplies codes in fp16 (exact) by fp16 parts of q
+          split_f16x2(v[0], v[1], f.x, f.z);
+          split_f16x2(v[2], v[3], f.y, f.w);
+        } else {
+          split_bf16x2(v[0], v[1], f.x, f.z);
+          split_bf16x2(v[2], v[3], f.y, f.w);
+        }
         qf[i] = f;
       }
       if constexpr (Q8) {
@@ -2724,10 +2785,13 @@ struct Consumer {
       float* dst = st + warp * kStride;
 #pragma unroll
       for (int mm = 0; mm < MT; ++mm) {
-        dst[(2 * t) * D + 16 * mm + g] = o[mm][0];
-        dst[(2 * t + 1) * D + 16 * mm + g] = o[mm][1];
-        dst[(2 * t) * D + 16 * mm + g + 8] = o[mm][2];
-        dst[(2 * t + 1) * D + 16 * mm + g + 8] = o[mm][3];
+        // output rows of tile mm: dims 16mm + g and 16mm + g + 8 (q8_0: 16mm + 2g and 16mm + 2g + 1)
+        const int d0 = Q8 ? 16 * mm + 2 * g : 16 * mm + g;
+        const int d1 = Q8 ? d0 + 1 : d0 + 8;
+        dst[(2 * t) * D + d0] = o[mm][0];
+        dst[(2 * t + 1) * D + d0] = o[mm][1];
+        dst[(2 * t) * D + d1] = o[mm][2];
+        dst[(2 * t + 1) * D + d1] = o[mm][3];
       }
       if (g == 0) {
         dst[kMaxG * D + 2 * t] = mx[0];
