@@ -313,6 +313,8 @@ struct mk_ctx {
   // TMA descriptor of the caller's KV pool (re-encoded when the pool pointer changes)
   alignas(64) CUtensorMap kv_map;
   const void* kv_map_ptr = nullptr;
+  // TMA descriptors of the dense weights for wide batches on tcgen05 ([3L + 1] maps), or null
+  uint64_t* d_wmaps = nullptr;
   // timeline
   uint64_t* trace = nullptr;
   int32_t trace_cap = 0;
@@ -335,16 +337,21 @@ size_t kv_q8_layer_bytes(const mk_config& cf) { return kv_q8_code_bytes(cf) / 16
 // (boxes of 64 elements x page_size rows); the q8_0 pool's code planes as 3-D [layer][row][D
 // bytes], rows of one layer contiguous, layers layer_bytes apart (boxes of D bytes x page_size
 // rows).  Both with the 128-byte swizzle.
-int encode_kv_map(const mk_config& cf, void* kv, CUtensorMap* out) {
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
     cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
-    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
-      return fail(MK_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    if (e == cudaSuccess && q == cudaDriverEntryPointSuccess && fn)
+      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
+  return encode;
+}
+
+int encode_kv_map(const mk_config& cf, void* kv, CUtensorMap* out) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return fail(MK_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   if (cf.flags & MK_FLAG_KV_Q8) {
     const cuuint64_t rows = (cuuint64_t)cf.num_pages * 2 * cf.num_kv_heads * cf.page_size;
     const cuuint64_t dims[3] = {(cuuint64_t)cf.head_dim, rows, (cuuint64_t)cf.num_layers};
@@ -369,8 +376,26 @@ int encode_kv_map(const mk_config& cf, void* kv, CUtensorMap* out) {
   return MK_OK;
 }
 
+// Describe a dense weight matrix [rows][K] (bf16, row-major) to TMA for the tcgen05 tiles: boxes
+// of 64 columns x 16 rows with the 128-byte swizzle (the K-major operand layout of tcgen05.mma);
+// rows past the matrix read as zeros.
+int encode_weight_map(const void* w, int rows, int K, CUtensorMap* out) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return fail(MK_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t box[2] = {64, 16};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MK_ERR_CUDA, "cuTensorMapEncodeTiled (weights) failed (%d)", (int)r);
+  return MK_OK;
+}
+
 void free_ctx(mk_ctx* c) {
   if (!c) return;
+  cudaFree(c->d_wmaps);
   cudaFree(c->d_layers);
   cudaFree(c->d_tasks);
   cudaFree(c->d_task_off);
@@ -516,6 +541,25 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_ctx** out) {
     free_ctx(c);
     return cuda_fail(e, "plan upload");
   }
+  // tensor maps of the dense weights, for the tcgen05 tiles of wide batches
+  if (cfg->max_batch >= mk::kTcMinBatch) {
+    std::vector<CUtensorMap> maps(3 * L + 1);
+    for (int l = 0; l < L && rc == MK_OK; ++l) {
+      const mk_layer_weights& s = w->layers[l];
+      rc = encode_weight_map(s.w_qkv, nqkv, H, &maps[mk::tc_map_index(MK_OP_QKV, l, L)]);
+      if (rc == MK_OK) rc = encode_weight_map(s.w_o, H, Hq * D, &maps[mk::tc_map_index(MK_OP_OPROJ, l, L)]);
+      if (rc == MK_OK) rc = encode_weight_map(s.w_router, E, H, &maps[mk::tc_map_index(MK_OP_ROUTER, l, L)]);
+    }
+    if (rc == MK_OK) rc = encode_weight_map(w->lm_head, cfg->vocab, H, &maps[mk::tc_map_index(MK_OP_HEAD, L, L)]);
+    if (rc) { free_ctx(c); return rc; }
+    static_assert(sizeof(CUtensorMap) == 128, "tensor map size");
+    if ((e = cudaMalloc(&c->d_wmaps, maps.size() * sizeof(CUtensorMap))) != cudaSuccess ||
+        (e = cudaMemcpy(c->d_wmaps, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice)) !=
+            cudaSuccess) {
+      free_ctx(c);
+      return cuda_fail(e, "weight tensor maps");
+    }
+  }
   // per-step buffer layout
   size_t so = 0;
   auto take = [&](size_t bytes) { size_t r = so; so += (bytes + 15) & ~(size_t)15; return r; };
@@ -639,6 +683,8 @@ static int make_params(mk_ctx* c, mk::Params& p, int32_t batch, const uint8_t* d
   p.B = batch; p.max_batch = cf.max_batch; p.n_ctas = c->n_ctas;
   const mk_plan_info& in = c->plan.info;
   p.n_qkv_tiles = in.n_qkv_tiles; p.n_o_tiles = in.n_o_tiles; p.n_router_tiles = in.n_router_tiles;
+  p.wmaps = c->d_wmaps;
+  p.tc = (c->d_wmaps != nullptr && batch >= mk::kTcMinBatch) ? 1 : 0;
   p.tasks = c->d_tasks; p.task_off = c->d_task_off;
   p.layers = c->d_layers; p.embed = c->embed; p.final_norm = c->final_norm; p.lm_head = c->lm_head;
   p.tokens = token_ids; p.block_tables = block_tables; p.kv = static_cast<uint16_t*>(kv_pages); p.logits = logits_out;

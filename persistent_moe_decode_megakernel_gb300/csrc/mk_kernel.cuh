@@ -155,6 +155,45 @@ __device__ __forceinline__ void split_f16x2(float a, float b, uint32_t& hi, uint
   hi = *reinterpret_cast<const uint32_t*>(&h);
   lo = *reinterpret_cast<const uint32_t*>(&r);
 }
+// ---- tcgen05: 5th-generation tensor cores, accumulators in tensor memory ----------------------
+// Shared-memory matrix descriptor of a K-major operand with the 128-byte swizzle: start address,
+// (unused) leading offset, 1024 bytes between 8-row groups, descriptor version 1, swizzle mode 2.
+// Advancing K by 16 bf16 within the 128-byte swizzle row adds 32 bytes to the start address.
+__device__ __forceinline__ uint64_t tc_desc_sw128(uint32_t addr) {
+  return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (1ull << 16) | (static_cast<uint64_t>(1024 >> 4) << 32) |
+         (1ull << 46) | (2ull << 61);
+}
+// Instruction descriptor of kind::f16 with bf16 A and B (both K-major) and an fp32 accumulator
+__device__ __forceinline__ uint32_t tc_idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+// D (tensor memory) = A * B^T, or += when acc
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, bool acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(static_cast<uint32_t>(acc)));
+}
+// one arrival on bar once every tensor-core operation this thread issued so far has completed
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// 8 consecutive accumulator columns of this warp's 32 lanes (one per thread), waited for
+__device__ __forceinline__ void tc_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(r[j]);
+}
 __device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
   uint16_t v;
   asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
@@ -351,7 +390,8 @@ __device__ __forceinline__ bool tr_on(const Params& p) { return kTrace && p.trac
 
 // --------------------------------------------------------------------------- shared memory
 enum : uint8_t { R_EMBED = 1, R_GEMV = 2, R_ATTN = 3, R_GU = 4, R_DOWN = 5, R_END = 6, R_ROUTE = 7,
-                 R_DT = 9, R_RED = 10 };   // small-batch MoE: transposed down rows; partial-sum reduction
+                 R_DT = 9, R_RED = 10,    // small-batch MoE: transposed down rows; partial-sum reduction
+                 R_TC = 11 };             // wide batch: a dense GEMV chunk for tcgen05
 // GEMV stream kinds beyond the task ops (MK_OP_QKV / OPROJ / ROUTER / HEAD)
 enum : int { R_OP_GU = 100 };
 
@@ -368,7 +408,7 @@ struct Meta {
 static_assert(sizeof(Meta) == 64, "meta size");
 
 
-struct __align__(128) Smem {
+struct __align__(1024) Smem {
   uint8_t ring[kSlots][kSlotBytes];
   uint64_t full[kSlots];
   uint64_t empty[kSlots];
@@ -386,7 +426,9 @@ struct __align__(128) Smem {
   int32_t ecnt[kMaxExperts];
   int32_t rcache[kMaxBatch * kMaxTopK];   // this layer's routing ids, cached by the first MoE item of the block
   float rwcache[kMaxBatch * kMaxTopK];    // and their combine weights
-  alignas(16) float moe[kMoeScratch];     // routing: logits; down projection: products, x_mid, SwiGLU inputs
+  // routing: logits; down projection: products, x_mid, SwiGLU inputs; tcgen05 tiles: the staged
+  // input slices (1024-byte aligned for the 128-byte swizzle)
+  alignas(1024) float moe[kMoeScratch];
   int32_t wlist[kConsumerWarps][kMaxBatch];   // per warp: (row, slot) pairs routed to one expert
   int32_t elist[kMaxBatch];               // gate/up run: (row, slot) pairs routed to its expert
   int32_t eact[kMaxExperts];              // this layer's active experts, ascending
@@ -401,6 +443,9 @@ struct __align__(128) Smem {
   int32_t flag;
   int32_t is_last;
   uint32_t tag;          // this step's tag, read from the uploaded step data
+  uint64_t xbar[kTcXBufs];  // tcgen05 tiles: the tensor cores have read input slice buffer i
+  uint64_t wbar;            // tcgen05 tiles: the tensor cores have read the current ring record
+  uint32_t tmem_base;       // tensor-memory address of this block's accumulators (wide batches)
 };
 
 static_assert(sizeof(Smem) + 1024 <= 227 * 1024, "shared memory (with the 1024-byte alignment pad) exceeds 227 KB");
@@ -708,6 +753,64 @@ struct Producer {
     return true;
   }
 
+  // Wide batches on tcgen05: the tile's weight rows as A operand units of MB rows x 64 columns
+  // (K-major, 128-byte swizzle; TMA boxes of 16 rows, rows past the tile left as they are: their
+  // accumulator rows are never read).  A pass covers as many M-blocks as the tensor memory holds
+  // accumulators for (tc_accs per M-block, each MB rows x the batch rounded up to 16 columns);
+  // within a pass, records
+  // go slice by slice, each with up to kTcChunkBytes of units: several slices of all the pass's
+  // M-blocks, or one slice of a group of M-blocks.  Meta: row0 the first M-block, n the M-blocks,
+  // aux the first slice | slices << 16, e the pass's M-blocks (first | end << 16).
+  __device__ bool tc_tile(const mk_task& t, uint32_t ti) {
+    const int K = t.op == MK_OP_OPROJ ? p.Hq * p.D : p.H;
+    const uint64_t* map = p.wmaps + static_cast<size_t>(tc_map_index(t.op, t.layer, p.L)) * 16;
+    const int R = static_cast<int>(t.hi - t.lo), MB = tc_mblock(R), nmb = (R + MB - 1) / MB;
+    const int pmb = min(nmb, kTcCols / (tc_accs(t.op, p.B, K) * tc_batch_cols(p.B)));
+    const int upc = kTcChunkBytes / (MB * 128);
+    const int ns = (K + 63) / 64;
+    #pragma unroll 1
+    for (int m0 = 0; m0 < nmb; m0 += pmb) {
+      const int m1 = min(nmb, m0 + pmb), nm = m1 - m0;
+      const int mg = nm < upc ? nm : upc;
+      const int nsc = nm < upc ? upc / nm : 1;
+      #pragma unroll 1
+      for (int s0 = 0; s0 < ns; s0 += nsc) {
+        const int s1 = min(ns, s0 + nsc);
+        #pragma unroll 1
+        for (int ma = m0; ma < m1; ma += mg) {
+          const int mb1 = min(m1, ma + mg);
+          if (!acquire()) return false;
+          Meta& m = meta();
+          m.kind = R_TC; m.op = static_cast<uint8_t>(t.op);
+          m.first = (m0 == 0 && s0 == 0 && ma == m0); m.last = (m1 == nmb && s1 == ns && mb1 == m1);
+          m.layer = t.layer; m.n = static_cast<uint16_t>(mb1 - ma); m.row0 = static_cast<uint32_t>(ma);
+          m.idx = ti; m.e = static_cast<uint32_t>(m0) | (static_cast<uint32_t>(m1) << 16);
+          m.aux = static_cast<uint32_t>(s0) | (static_cast<uint32_t>(s1 - s0) << 16);
+          m.lo = t.lo; m.hi = t.hi;
+          uint32_t bytes = 0;
+          #pragma unroll 1
+          for (int mm = ma; mm < mb1; ++mm) bytes += static_cast<uint32_t>((min(MB, R - mm * MB) + 15) / 16) * 2048u;
+          mbar_arrive_expect_tx(full(), bytes * static_cast<uint32_t>(s1 - s0));
+          uint8_t* dst = slot();
+          #pragma unroll 1
+          for (int sl = s0; sl < s1; ++sl) {
+            #pragma unroll 1
+            for (int mm = ma; mm < mb1; ++mm) {
+              const int u = (sl - s0) * (mb1 - ma) + (mm - ma);
+              const int rows = min(MB, R - mm * MB);
+              #pragma unroll 1
+              for (int j = 0; j * 16 < rows; ++j)
+                tma_load_2d(dst + u * MB * 128 + j * 2048, map, 64 * sl, static_cast<int>(t.lo) + mm * MB + 16 * j,
+                            full(), pol);
+            }
+          }
+          ++c;
+        }
+      }
+    }
+    return true;
+  }
+
   // KV pages of this block's attention items: per page, K then V, each as D/64 boxes of
   // [page_size rows][64 dims] (128-byte swizzle).  Within a slot, K occupies the first half
   // and V the second; each holds [dim half][rows][64 dims], page i at rows i*page_size.
@@ -998,7 +1101,7 @@ struct Producer {
         case MK_OP_QKV:
         case MK_OP_OPROJ:
         case MK_OP_ROUTER:
-        case MK_OP_HEAD: ok = gemv_tile(t, static_cast<uint32_t>(ti)); break;
+        case MK_OP_HEAD: ok = p.tc ? tc_tile(t, static_cast<uint32_t>(ti)) : gemv_tile(t, static_cast<uint32_t>(ti)); break;
         case MK_OP_ATTN: ok = attn_items(t); break;
         case MK_OP_MOE: ok = moe_tasks(t); break;
         case MK_OP_END: ok = emit_control(R_END, t, static_cast<uint32_t>(ti)); break;
@@ -1683,6 +1786,242 @@ struct Consumer {
       }
     }
     if (!ok) ll_timeout(p, eop, l, tg);
+    if (!cbar_and(wok && ok)) return false;
+    if (op == MK_OP_HEAD && p.next_token != nullptr) head_top2(lo, hi);
+    return true;
+  }
+
+  // ------------------------------------------------------------------ wide batches on tcgen05
+  uint32_t xst = 0;   // per input buffer i: bit i a commit on xbar[i] not yet waited for, bit 4 + i its parity
+  uint32_t wph = 0;   // parity of the next wbar phase
+
+  // every consumer thread: wait for a phase of a tensor-core commit barrier (the work behind it
+  // depends on no other block, so the limit only guards against a fault of this kernel)
+  __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t ph) {
+    if (mbar_try_wait(bar, ph)) return true;
+    const uint64_t t0 = globaltimer();
+    #pragma unroll 1
+    for (uint32_t it = 1;; ++it) {
+      if (mbar_try_wait(bar, ph)) return true;
+      if ((it & 63u) == 0u && globaltimer() - t0 > p.watchdog_ns) return false;
+    }
+  }
+
+  // Stage input slice s (columns 64s .. 64s + 63 of every batch row) into xb as T bf16 terms of
+  // the fp32 value (high, then what it left, ...): term t of row b at xb + t*Bp*128 + b*128, its
+  // 16-byte piece j at piece j ^ (b & 7) (the K-major layout with the 128-byte swizzle).  Thread
+  // i takes pieces i and i + 256 (row i/8, piece i%8).  A normalised input takes its gain here;
+  // the row's 1/rms is applied to the accumulators (a dot product is linear in it), from the
+  // sums of squares collected in ss.  Columns at or past K are zero.
+  __device__ __forceinline__ bool tc_stage(const uint64_t* xbase, size_t xstride, const uint16_t* g, int K, int s,
+                                           int T, uint8_t* xb, int Bp, uint32_t tag, float (&ss)[2]) {
+    const int B = p.B;
+    bool ok = true;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i = threadIdx.x + h * kConsumerThreads;
+      const int b = i >> 3, cg = i & 7, k = 64 * s + 8 * cg;
+      if (b >= B) continue;
+      float x[8];
+      if (k < K) {
+        const uint64_t* src = xbase + static_cast<size_t>(b) * xstride + k;
+        uint64_t w[8];
+#pragma unroll
+        for (int q = 0; q < 8; q += 2) ll_ld2(src + q, w[q], w[q + 1]);
+        uint32_t st = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) st |= ll_stale(w[q], tag);
+        if (st != 0u) {
+          const H8 r = load_h8(p, src, tag);
+          ok = ok && r.ok;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) x[q] = r.v[q];
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) x[q] = ll_f(w[q]);
+        }
+        float a = 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) a = fmaf(x[q], x[q], a);
+        ss[h] += a;
+        if (g != nullptr) {
+          const uint4 gu = __ldg(reinterpret_cast<const uint4*>(g + k));
+          x[0] *= bf_lo(gu.x); x[1] *= bf_hi(gu.x); x[2] *= bf_lo(gu.y); x[3] *= bf_hi(gu.y);
+          x[4] *= bf_lo(gu.z); x[5] *= bf_hi(gu.z); x[6] *= bf_lo(gu.w); x[7] *= bf_hi(gu.w);
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) x[q] = 0.f;
+      }
+      uint8_t* dst = xb + b * 128 + ((cg ^ (b & 7)) << 4);
+      uint4 hi, mid, lo;
+      if (T == 3) {
+        split3_bf16x2(x[0], x[1], hi.x, mid.x, lo.x);
+        split3_bf16x2(x[2], x[3], hi.y, mid.y, lo.y);
+        split3_bf16x2(x[4], x[5], hi.z, mid.z, lo.z);
+        split3_bf16x2(x[6], x[7], hi.w, mid.w, lo.w);
+        *reinterpret_cast<uint4*>(dst + 2 * Bp * 128) = lo;
+      } else {
+        split_bf16x2(x[0], x[1], hi.x, mid.x);
+        split_bf16x2(x[2], x[3], hi.y, mid.y);
+        split_bf16x2(x[4], x[5], hi.z, mid.z);
+        split_bf16x2(x[6], x[7], hi.w, mid.w);
+      }
+      *reinterpret_cast<uint4*>(dst) = hi;
+      *reinterpret_cast<uint4*>(dst + Bp * 128) = mid;
+    }
+    return ok;
+  }
+
+  // Accumulators of M-blocks [m0, m1) of the pass to the outputs: per M-block KG accumulators of
+  // the high term and one per lower term, summed here in fp32 (low terms first).  Warp w reads
+  // tensor-memory lanes
+  // 32(w % 4) .. + 31 (M = 128: row = lane; M = 64: rows 16(w % 4) + lane for lanes < 16) and
+  // half w / 4 of the batch columns.
+  __device__ __forceinline__ void tc_epilogue(const OutMap& om, bool norm, uint32_t lo, int R, int MB, int m0, int m1,
+                                              int Bp, int T, int KG) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int q = warp & 3, hh = warp >> 2;
+    const int half = Bp >> 1;
+    const int r_in = MB == 128 ? 32 * q + lane : 16 * q + lane;
+    const bool lane_ok = MB == 128 || lane < 16;
+    #pragma unroll 1
+    for (int m = m0; m < m1; ++m) {
+      const int row = m * MB + r_in;
+      const uint32_t ta = S.tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
+                          static_cast<uint32_t>((m - m0) * (KG + T - 1) * Bp + hh * half);
+      #pragma unroll 1
+      for (int c8 = 0; c8 < half; c8 += 8) {
+        float v[8], v1[8];
+        tc_ld8(ta + (KG + T - 2) * Bp + c8, v1);   // the lowest term
+        #pragma unroll 1
+        for (int a = KG + T - 3; a >= 0; --a) {     // the other terms, then the high term's groups
+          float v2[8];
+          tc_ld8(ta + a * Bp + c8, v2);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v1[j] += v2[j];
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = v1[j];
+        if (lane_ok && row < R) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int b = hh * half + c8 + j;
+            if (b < p.B) put(om, false, lo + row, b, 0, norm ? v[j] * S.rstd[b] : v[j], 0.f);
+          }
+        }
+      }
+    }
+  }
+
+  // A dense GEMV tile (QKV, O-proj, router, LM head) of a wide batch on tcgen05: for each record,
+  // per slice, the consumers stage the batch's input slice (unless an earlier record of the pass
+  // did), then one thread issues the MMAs of the record's units of that slice into the pass's
+  // accumulators; the record's slot is released once the tensor cores have read it.  At the end
+  // of a pass the accumulators go to the outputs.
+  __device__ __forceinline__ bool tc_gemv() {
+    const int op = meta().op, l = meta().layer;
+    const uint32_t lo = meta().lo, hi = meta().hi;
+    const int R = static_cast<int>(hi - lo);
+    const int K = op == MK_OP_OPROJ ? p.Hq * p.D : p.H;
+    const int kind = op == MK_OP_QKV ? 0 : op == MK_OP_OPROJ ? 1 : op == MK_OP_ROUTER ? 2 : 3;
+    const int T = tc_terms(op), KG = tc_hi_groups(op, p.B, K), NA = KG + T - 1;
+    const int Bp = tc_batch_cols(p.B), MB = tc_mblock(R), ns = (K + 63) / 64;
+    const uint32_t xsz = static_cast<uint32_t>(T * Bp * 128);
+    const int NX = min(kTcXBufs, static_cast<int>((kMoeScratch * 4) / xsz));
+    const uint16_t* g = kind == 0 ? p.layers[l].attn_norm : kind == 2 ? p.layers[l].ffn_norm
+                      : kind == 3 ? p.final_norm : nullptr;
+    const uint64_t* xbase;
+    size_t xstride;
+    if (kind == 1) {
+      xstride = static_cast<size_t>(p.Hq) * p.D;
+      xbase = p.ATT + static_cast<size_t>(l) * p.max_batch * xstride;
+    } else {
+      const int xidx = kind == 0 ? 2 * l : kind == 2 ? 2 * l + 1 : 2 * p.L;
+      xstride = static_cast<size_t>(p.H);
+      xbase = p.X + static_cast<size_t>(xidx) * p.max_batch * xstride;
+    }
+    // the test hook waits for a tag that is never written
+    const uint32_t tag = (op == MK_OP_OPROJ && l == p.stall_layer) ? (tg ^ 0x80000000u) : tg;
+    const OutMap om = out_map(op, l);
+    uint8_t* xb0 = reinterpret_cast<uint8_t*>(S.moe);
+    const uint32_t idesc = tc_idesc_bf16(MB, Bp);
+    twait = globaltimer();
+    float ss[2] = {0.f, 0.f};
+    int staged = 0, pass_m0 = -1;
+    bool ok = true;
+    #pragma unroll 1
+    for (;;) {
+      const int ma = static_cast<int>(meta().row0), nmc = meta().n;
+      const int s0 = static_cast<int>(meta().aux & 0xffffu), nsc = static_cast<int>(meta().aux >> 16);
+      const int pm0 = static_cast<int>(meta().e & 0xffffu), pm1 = static_cast<int>(meta().e >> 16);
+      const bool last = meta().last;
+      if (pm0 != pass_m0) { pass_m0 = pm0; staged = 0; ss[0] = 0.f; ss[1] = 0.f; }
+      const uint32_t wa = smem_u32(slot());
+      #pragma unroll 1
+      for (int si = 0; si < nsc; ++si) {
+        const int sl = s0 + si, buf = sl % NX;
+        if (sl >= staged) {
+          if ((xst >> buf) & 1u) {   // the tensor cores must have read the buffer's previous slice
+            ok = tc_wait(&S.xbar[buf], (xst >> (4 + buf)) & 1u) && ok;
+            xst ^= (1u << buf) | (1u << (4 + buf));
+          }
+          ok = tc_stage(xbase, xstride, g, K, sl, T, xb0 + buf * xsz, Bp, tag, ss) && ok;
+          fence_proxy_async_smem();   // generic writes, read by the tensor cores (async proxy)
+          staged = sl + 1;
+        }
+        ok = cbar_and(ok);
+        if (!ok) break;
+        const bool last_use = ma + nmc == pm1;   // the slice's last record in this pass
+        if (threadIdx.x == 0) {
+          tc_fence_after();
+          const uint32_t xa = smem_u32(xb0) + static_cast<uint32_t>(buf) * xsz;
+          #pragma unroll 1
+          for (int mi = 0; mi < nmc; ++mi) {
+            const uint32_t aa = wa + static_cast<uint32_t>((si * nmc + mi) * MB * 128);
+            // accumulators of the M-block: the high term's groups, then one per lower term
+            const uint32_t d = S.tmem_base + static_cast<uint32_t>((ma + mi - pm0) * NA * Bp);
+            const uint32_t dh = d + static_cast<uint32_t>((sl % KG) * Bp);
+            #pragma unroll
+            for (int k16 = 0; k16 < 4; ++k16) {
+              tc_mma(dh, tc_desc_sw128(aa + 32 * k16), tc_desc_sw128(xa + 32 * k16), idesc, sl >= KG || k16 > 0);
+              #pragma unroll 1
+              for (int t = 1; t < T; ++t)
+                tc_mma(d + (KG + t - 1) * Bp, tc_desc_sw128(aa + 32 * k16), tc_desc_sw128(xa + t * Bp * 128 + 32 * k16),
+                       idesc, sl > 0 || k16 > 0);
+            }
+          }
+          if (last_use) tc_commit(&S.xbar[buf]);
+        }
+        if (last_use) xst |= 1u << buf;
+      }
+      // the record's slot is refilled only after the tensor cores have read it
+      if (threadIdx.x == 0) tc_commit(&S.wbar);
+      ok = tc_wait(&S.wbar, wph) && ok;
+      wph ^= 1u;
+      if (!ok) break;
+      if (ma + nmc == pm1 && s0 + nsc == ns) {
+        // the pass is complete: its rows' norms, then the accumulators to the outputs
+        if (kind != 1) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float v = ss[h];
+            v += __shfl_xor_sync(0xffffffffu, v, 1);
+            v += __shfl_xor_sync(0xffffffffu, v, 2);
+            v += __shfl_xor_sync(0xffffffffu, v, 4);
+            const int b = (threadIdx.x >> 3) + 32 * h;
+            if ((threadIdx.x & 7) == 0 && b < p.B) S.rstd[b] = 1.0f / sqrtf(v / static_cast<float>(K) + p.eps);
+          }
+        }
+        cbar();
+        tc_fence_after();
+        tc_epilogue(om, kind != 1, lo, R, MB, pm0, pm1, Bp, T, KG);
+        tc_fence_before();   // these reads precede the next pass's MMAs (behind the next barrier)
+      }
+      if (last) break;
+      if (!next_rec()) { ok = false; break; }
+    }
+    if (!ok) ll_timeout(p, op, l, tg);
     if (!cbar_and(wok && ok)) return false;
     if (op == MK_OP_HEAD && p.next_token != nullptr) head_top2(lo, hi);
     return true;
@@ -2929,6 +3268,9 @@ struct Consumer {
           ok = (m0.kind == R_GU && meta().n == 0) ? true : stream_gemv(m0.kind == R_GU ? int(R_OP_GU) : int(m0.op));
           break;
         case R_ATTN: ok = attn_item(); break;
+        case R_TC:
+          if constexpr (TB == 4) ok = tc_gemv();
+          break;
         case R_DOWN: ok = moe_down(); break;
         case R_ROUTE: ok = route_local(); break;
         case R_DT:   // small-batch MoE records exist only for batches of at most kSmallMaxB rows
@@ -2975,6 +3317,9 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
       mbar_init(&S.empty[s], kConsumerWarps);
     }
     mbar_init(&S.route_bar, 1);
+    #pragma unroll 1
+    for (int i = 0; i < kTcXBufs; ++i) mbar_init(&S.xbar[i], 1);
+    mbar_init(&S.wbar, 1);
     S.prod_count = 0;
     S.cons_count = 0xffffffffu;
     S.ykey = -1;
@@ -2982,7 +3327,18 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     if (tr_on(p)) p.trace[static_cast<size_t>(blockIdx.x) * p.trace_cap * 4 + 1] = globaltimer();
     fence_mbar_init();
   }
+  if constexpr (TB == 4) {
+    // wide batches: warp 0 takes all of this SM's tensor memory for the tcgen05 accumulators
+    if (p.tc && (tid >> 5) == 0) {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&S.tmem_base)),
+                   "r"(kTcCols)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+  }
   __syncthreads();
+  if constexpr (TB == 4) tc_fence_after();
   {
     // every block warms a slice of the small per-layer vectors (norm gains) in L2, so that
     // their first read in a layer is an L2 hit rather than a DRAM access behind the stream
@@ -3014,7 +3370,15 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     asm volatile("bar.sync %0, 128;" ::"r"(10 + (tid >> 7)) : "memory");
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kLaunchRegs));
   }
+  if constexpr (TB == 4) tc_fence_before();
   __syncthreads();
+  if constexpr (TB == 4) {
+    // every tcgen05 operation of the block has completed (each tile waits for its commits)
+    if (p.tc && (tid >> 5) == 0) {
+      tc_fence_after();
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(S.tmem_base), "r"(kTcCols) : "memory");
+    }
+  }
   // an aborted step may leave copies in flight: let them land before the block exits
   if (tid == 0) {
     #pragma unroll 1

@@ -78,6 +78,40 @@ MK_HD bool small_moe_batch(int B, int H) {
   return B <= kSmallMaxB && tb * H <= 8 * kConsumerThreads && B * H <= kAttnScratch;
 }
 
+// ---- wide batches on tcgen05 ------------------------------------------------------
+// Batches of kTcMinBatch rows or more run the dense GEMV tiles (QKV, O-proj, router, LM head) on
+// the 5th-generation tensor cores: the weight tile is the A operand (M-blocks of 64 or 128 rows,
+// K-major, 128-byte swizzle, loaded by TMA in 64-column slices), the whole batch the B operand
+// (N = the batch rounded up to 16, staged by the consumers one 64-column slice at a time as bf16
+// terms of the fp32 input), the accumulators in tensor memory.
+constexpr int kTcMinBatch = 5;
+constexpr int kTcUnitBytes128 = 128 * 128;   // one 64-column slice of a 128-row M-block
+constexpr int kTcChunkBytes = 65536;          // A units of one ring record
+constexpr int kTcXBufs = 3;                   // input slices in flight (fewer when three terms do not fit)
+constexpr int kTcCols = 512;                  // tensor-memory columns (all of them: one block per SM)
+MK_HD int tc_mblock(int rows) { return rows <= 64 ? 64 : 128; }
+MK_HD int tc_batch_cols(int B) { return (B + 15) & ~15; }
+// bf16 terms of the fp32 input (one accumulator each: the tensor cores align a sum to its largest
+// addend, so a small term summed into a large accumulator would lose its low bits): three keep the
+// input whole for the QKV projection (the step rounds its k and v to bf16 for the cache), two
+// (~16 bits) elsewhere
+MK_HD int tc_terms(int op) { return op == MK_OP_QKV ? 3 : 2; }
+// Accumulators of the high term: the QKV projection spreads its 64-column slices over several
+// (slice s into accumulator s mod G), summed in fp32 at the end, so that each takes fewer tensor-core
+// roundings of a large running sum; one elsewhere.  Accumulators per M-block: G + terms - 1.
+MK_HD int tc_hi_groups(int op, int B, int K) {
+  if (op != MK_OP_QKV) return 1;
+  const int ns = (K + 63) / 64, fit = kTcCols / tc_batch_cols(B) - (tc_terms(op) - 1);
+  int g = fit < 8 ? fit : 8;
+  g = g < ns ? g : ns;
+  return g > 1 ? g : 1;
+}
+MK_HD int tc_accs(int op, int B, int K) { return tc_hi_groups(op, B, K) + tc_terms(op) - 1; }
+// tensor map of a dense weight matrix: QKV of layer l, O-proj, router, then the LM head
+MK_HD int tc_map_index(int op, int layer, int L) {
+  return op == MK_OP_QKV ? layer : op == MK_OP_OPROJ ? L + layer : op == MK_OP_ROUTER ? 2 * L + layer : 3 * L;
+}
+
 MK_HD int gemv_rows_per_chunk(int K) {
   int r = kSlotBytes / (2 * K);
   return r > kMaxRowsPerChunk ? kMaxRowsPerChunk : r;
@@ -147,6 +181,8 @@ struct alignas(64) Params {
   int32_t B, max_batch, n_ctas, max_items;
   // static plan
   int32_t n_qkv_tiles, n_o_tiles, n_router_tiles;
+  int32_t tc;                   // this step runs the dense GEMV tiles on tcgen05 (wide batch)
+  const uint64_t* wmaps;        // [3L + 1][16] TMA descriptors of the dense weights (box 64 x 16, 128-byte swizzle)
   uint64_t watchdog_ns;
   const mk_task* tasks;
   const int32_t* task_off;      // [n_ctas + 1]

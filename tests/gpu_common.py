@@ -64,6 +64,22 @@ def own_topk_mismatches(ids, logits, K):
     return bad
 
 
+def expected_appends(orc, dims, wn_layers, x_all, seq_lens, bt, kv_orig):
+    """The cache with the oracle's appended k and v codes of every layer, each layer's computed
+    from the GPU's own input to that layer (``x_all[2l]``, the engine's residual stream), so that
+    a value compared with the GPU's append is one rounding away from it.  (Against an end-to-end
+    oracle run, a value whose fp32 k or v lies within the GEMV's rounding error of a rounding
+    boundary may round the other way; that allowed one-step difference changes the next layer's
+    attention -- exactly, for a row whose attention covers that one position -- and so every
+    later layer's input.)"""
+    kv = np.array(kv_orig, copy=True)
+    for l in range(len(wn_layers)):
+        kvl = np.ascontiguousarray(kv_orig[l]).copy()
+        orc.layer_trace(dims, wn_layers[l], x_all[2 * l], seq_lens, bt, kvl)
+        kv[l] = kvl
+    return kv
+
+
 def check_rows(got, ref, tol=None, margin=None):
     """Per-row logits check: relative L2 of every row within ``tol``, and the same argmax
     wherever the oracle's top-1/top-2 margin exceeds ``margin``.  Returns the rows' errors."""

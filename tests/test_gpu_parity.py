@@ -14,8 +14,8 @@ import torch
 import workloads as W
 import persistent_moe_decode_megakernel_gb300 as mk
 from oracle import Oracle, make_dims
-from tests.gpu_common import (MARGIN, MEDIUM, TOL_LOGITS, check_rows, engine_for, gpu_step, kv_to_device,
-                              own_topk_mismatches, route_mismatches, to_device)
+from tests.gpu_common import (MARGIN, MEDIUM, TOL_LOGITS, check_rows, engine_for, expected_appends, gpu_step,
+                              kv_to_device, own_topk_mismatches, route_mismatches, to_device)
 from tests.helpers import rel_l2, tiny_setup, top2_margin
 
 pytestmark = pytest.mark.gpu
@@ -67,13 +67,16 @@ def _parity_one_step(setup, max_batch=8, check_layers=True, flags=0):
                 assert np.allclose(eng.debug_read("route_w", l), tr["w"], rtol=1e-5, atol=1e-7)
                 assert rel_l2(eng.debug_read("h", l), tr["h"]) < 1e-4
                 assert rel_l2(x_all[2 * l + 2], tr["x_out"]) < 1e-5
-    # the appended KV: both sides wrote position seq_len-1 of every row.  The bf16 values agree to one
-    # bf16 ulp of their own magnitude plus fp32 summation noise at the vector's scale (a value that
-    # cancels to near zero keeps only the latter).
+    # the appended KV: both sides wrote position seq_len-1 of every row and layer, the oracle's from
+    # the GPU's own input to the layer (tests.gpu_common.expected_appends).  The bf16 values agree to
+    # one bf16 ulp of their own magnitude plus fp32 summation noise at the vector's scale (a value
+    # that cancels to near zero keeps only the latter).
     kv_got = W.bf16_bits(kv_dev)
-    changed = (kv_got != setup["kv"]) | (kv_ref != setup["kv"])
+    kv_exp = expected_appends(orc, setup["dims"], setup["wn"]["layers"], eng.debug_read("x"), setup["seq_lens"],
+                              setup["bt"], setup["kv"])
+    changed = (kv_got != setup["kv"]) | (kv_exp != setup["kv"])
     g = (kv_got[changed].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-    r = (kv_ref[changed].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    r = (kv_exp[changed].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     assert changed.any()
     rms = np.sqrt(np.mean(r * r))
     assert np.all(np.abs(g - r) <= 2.0 ** -7 * np.maximum(np.abs(r), np.abs(g)) + 1e-4 * rms)
