@@ -175,6 +175,20 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, 
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(static_cast<uint32_t>(acc)));
 }
+// the same, issued by one elected lane of a converged warp (the whole warp computes the operands,
+// so that they are warp-uniform)
+__device__ __forceinline__ void tc_mma_elect(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, bool acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(static_cast<uint32_t>(acc)));
+}
+__device__ __forceinline__ void tc_commit_elect(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+      : "memory");
+}
 // one arrival on bar once every tensor-core operation this thread issued so far has completed
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
@@ -1807,51 +1821,82 @@ struct Consumer {
     }
   }
 
-  // Stage input slice s (columns 64s .. 64s + 63 of every batch row) into xb as T bf16 terms of
-  // the fp32 value (high, then what it left, ...): term t of row b at xb + t*Bp*128 + b*128, its
-  // 16-byte piece j at piece j ^ (b & 7) (the K-major layout with the 128-byte swizzle).  Thread
-  // i takes pieces i and i + 256 (row i/8, piece i%8).  A normalised input takes its gain here;
-  // the row's 1/rms is applied to the accumulators (a dot product is linear in it), from the
-  // sums of squares collected in ss.  Columns at or past K are zero.
+  // Input slice s (columns 64s .. 64s + 63 of every batch row): thread i takes pieces i and i + 256
+  // (row i/8, 8 columns from 64s + 8(i%8)), 8 tagged words each.  tc_issue starts all 16 loads
+  // (one L2 round trip per slice); tc_stage waits for them, re-polls stale words inline (no call: the caller's registers stay put), and stores
+  // T bf16 terms of the fp32 value (high, then what it left, ...) into xb: term t of row b at
+  // xb + t*Bp*128 + b*128, its 16-byte piece j at piece j ^ (b & 7) (the K-major layout with the
+  // 128-byte swizzle).  A normalised input takes its gain here; the row's 1/rms is applied to the
+  // accumulators (a dot product is linear in it), from the sums of squares collected in ss.
+  // Columns at or past K are zero.
+  __device__ __forceinline__ void tc_issue(const uint64_t* xbase, size_t xstride, int K, int s, uint64_t (&w)[16]) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i = threadIdx.x + h * kConsumerThreads;
+      const int b = i >> 3, k = 64 * s + 8 * (i & 7);
+      if (b < p.B && k < K) {
+        const uint64_t* src = xbase + static_cast<size_t>(b) * xstride + k;
+#pragma unroll
+        for (int q = 0; q < 8; q += 2) ll_ld2(src + q, w[8 * h + q], w[8 * h + q + 1]);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) w[8 * h + q] = 0ull;
+      }
+    }
+  }
   __device__ __forceinline__ bool tc_stage(const uint64_t* xbase, size_t xstride, const uint16_t* g, int K, int s,
-                                           int T, uint8_t* xb, int Bp, uint32_t tag, float (&ss)[2]) {
+                                           int T, uint8_t* xb, int Bp, uint32_t tag, uint64_t (&w)[16], float (&ss)[2]) {
     const int B = p.B;
+    // stale words (this step's tag not there yet): re-poll both pieces until every word is fresh
+    uint32_t st = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i = threadIdx.x + h * kConsumerThreads;
+      if ((i >> 3) < B && 64 * s + 8 * (i & 7) < K) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) st |= (ll_stale(w[8 * h + q], tag) != 0u ? 1u : 0u) << h;
+      }
+    }
     bool ok = true;
+    if (st != 0u) {
+      const uint64_t t0 = globaltimer();
+      #pragma unroll 1
+      for (uint32_t it = 1; st != 0u; ++it) {
+        uint32_t still = 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if ((st >> h) & 1u) {
+            const int i = threadIdx.x + h * kConsumerThreads;
+            const uint64_t* src = xbase + static_cast<size_t>(i >> 3) * xstride + 64 * s + 8 * (i & 7);
+#pragma unroll
+            for (int q = 0; q < 8; q += 2) ll_ld2(src + q, w[8 * h + q], w[8 * h + q + 1]);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) still |= (ll_stale(w[8 * h + q], tag) != 0u ? 1u : 0u) << h;
+          }
+        }
+        st = still;
+        if (st != 0u && (it & 15u) == 0u && (aborted(p) || globaltimer() - t0 > p.watchdog_ns)) {
+          ok = false;
+          break;
+        }
+      }
+    }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int i = threadIdx.x + h * kConsumerThreads;
       const int b = i >> 3, cg = i & 7, k = 64 * s + 8 * cg;
       if (b >= B) continue;
       float x[8];
-      if (k < K) {
-        const uint64_t* src = xbase + static_cast<size_t>(b) * xstride + k;
-        uint64_t w[8];
 #pragma unroll
-        for (int q = 0; q < 8; q += 2) ll_ld2(src + q, w[q], w[q + 1]);
-        uint32_t st = 0;
+      for (int q = 0; q < 8; ++q) x[q] = ll_f(w[8 * h + q]);   // zero past K
+      float a = 0.f;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) st |= ll_stale(w[q], tag);
-        if (st != 0u) {
-          const H8 r = load_h8(p, src, tag);
-          ok = ok && r.ok;
-#pragma unroll
-          for (int q = 0; q < 8; ++q) x[q] = r.v[q];
-        } else {
-#pragma unroll
-          for (int q = 0; q < 8; ++q) x[q] = ll_f(w[q]);
-        }
-        float a = 0.f;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) a = fmaf(x[q], x[q], a);
-        ss[h] += a;
-        if (g != nullptr) {
-          const uint4 gu = __ldg(reinterpret_cast<const uint4*>(g + k));
-          x[0] *= bf_lo(gu.x); x[1] *= bf_hi(gu.x); x[2] *= bf_lo(gu.y); x[3] *= bf_hi(gu.y);
-          x[4] *= bf_lo(gu.z); x[5] *= bf_hi(gu.z); x[6] *= bf_lo(gu.w); x[7] *= bf_hi(gu.w);
-        }
-      } else {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) x[q] = 0.f;
+      for (int q = 0; q < 8; ++q) a = fmaf(x[q], x[q], a);
+      ss[h] += a;
+      if (g != nullptr && k < K) {
+        const uint4 gu = __ldg(reinterpret_cast<const uint4*>(g + k));
+        x[0] *= bf_lo(gu.x); x[1] *= bf_hi(gu.x); x[2] *= bf_lo(gu.y); x[3] *= bf_hi(gu.y);
+        x[4] *= bf_lo(gu.z); x[5] *= bf_hi(gu.z); x[6] *= bf_lo(gu.w); x[7] *= bf_hi(gu.w);
       }
       uint8_t* dst = xb + b * 128 + ((cg ^ (b & 7)) << 4);
       uint4 hi, mid, lo;
@@ -1943,13 +1988,13 @@ struct Consumer {
     }
     // the test hook waits for a tag that is never written
     const uint32_t tag = (op == MK_OP_OPROJ && l == p.stall_layer) ? (tg ^ 0x80000000u) : tg;
-    const OutMap om = out_map(op, l);
     uint8_t* xb0 = reinterpret_cast<uint8_t*>(S.moe);
     const uint32_t idesc = tc_idesc_bf16(MB, Bp);
     twait = globaltimer();
     float ss[2] = {0.f, 0.f};
     int staged = 0, pass_m0 = -1;
     bool ok = true;
+    uint64_t xw[16];   // the tagged words of the slice being staged
     #pragma unroll 1
     for (;;) {
       const int ma = static_cast<int>(meta().row0), nmc = meta().n;
@@ -1966,37 +2011,41 @@ struct Consumer {
             ok = tc_wait(&S.xbar[buf], (xst >> (4 + buf)) & 1u) && ok;
             xst ^= (1u << buf) | (1u << (4 + buf));
           }
-          ok = tc_stage(xbase, xstride, g, K, sl, T, xb0 + buf * xsz, Bp, tag, ss) && ok;
+          // (one slice's 16 loads per thread at a time: a second slice's words in flight together,
+          // or the next slice's issued before the barrier, made ptxas spill)
+          tc_issue(xbase, xstride, K, sl, xw);
+          ok = tc_stage(xbase, xstride, g, K, sl, T, xb0 + buf * xsz, Bp, tag, xw, ss) && ok;
           fence_proxy_async_smem();   // generic writes, read by the tensor cores (async proxy)
           staged = sl + 1;
         }
         ok = cbar_and(ok);
         if (!ok) break;
         const bool last_use = ma + nmc == pm1;   // the slice's last record in this pass
-        if (threadIdx.x == 0) {
+        if (threadIdx.x < 32) {
+          // warp 0, converged: descriptors advance in 16-byte units (32 bytes per 16 columns of K)
           tc_fence_after();
-          const uint32_t xa = smem_u32(xb0) + static_cast<uint32_t>(buf) * xsz;
+          const uint64_t xd = tc_desc_sw128(smem_u32(xb0) + static_cast<uint32_t>(buf) * xsz);
+          const uint64_t td = static_cast<uint64_t>((Bp * 128) >> 4);   // one input term
+          const bool acc_lo = sl > 0, acc_hi = sl >= KG;
           #pragma unroll 1
           for (int mi = 0; mi < nmc; ++mi) {
-            const uint32_t aa = wa + static_cast<uint32_t>((si * nmc + mi) * MB * 128);
+            const uint64_t ad = tc_desc_sw128(wa + static_cast<uint32_t>((si * nmc + mi) * MB * 128));
             // accumulators of the M-block: the high term's groups, then one per lower term
             const uint32_t d = S.tmem_base + static_cast<uint32_t>((ma + mi - pm0) * NA * Bp);
             const uint32_t dh = d + static_cast<uint32_t>((sl % KG) * Bp);
             #pragma unroll
             for (int k16 = 0; k16 < 4; ++k16) {
-              tc_mma(dh, tc_desc_sw128(aa + 32 * k16), tc_desc_sw128(xa + 32 * k16), idesc, sl >= KG || k16 > 0);
-              #pragma unroll 1
-              for (int t = 1; t < T; ++t)
-                tc_mma(d + (KG + t - 1) * Bp, tc_desc_sw128(aa + 32 * k16), tc_desc_sw128(xa + t * Bp * 128 + 32 * k16),
-                       idesc, sl > 0 || k16 > 0);
+              tc_mma_elect(dh, ad + 2 * k16, xd + 2 * k16, idesc, acc_hi || k16 > 0);
+              tc_mma_elect(d + KG * Bp, ad + 2 * k16, xd + td + 2 * k16, idesc, acc_lo || k16 > 0);
+              if (T == 3) tc_mma_elect(d + (KG + 1) * Bp, ad + 2 * k16, xd + 2 * td + 2 * k16, idesc, acc_lo || k16 > 0);
             }
           }
-          if (last_use) tc_commit(&S.xbar[buf]);
+          if (last_use) tc_commit_elect(&S.xbar[buf]);
         }
         if (last_use) xst |= 1u << buf;
       }
       // the record's slot is refilled only after the tensor cores have read it
-      if (threadIdx.x == 0) tc_commit(&S.wbar);
+      if (threadIdx.x < 32) tc_commit_elect(&S.wbar);
       ok = tc_wait(&S.wbar, wph) && ok;
       wph ^= 1u;
       if (!ok) break;
@@ -2015,7 +2064,7 @@ struct Consumer {
         }
         cbar();
         tc_fence_after();
-        tc_epilogue(om, kind != 1, lo, R, MB, pm0, pm1, Bp, T, KG);
+        tc_epilogue(out_map(op, l), kind != 1, lo, R, MB, pm0, pm1, Bp, T, KG);
         tc_fence_before();   // these reads precede the next pass's MMAs (behind the next barrier)
       }
       if (last) break;
