@@ -313,7 +313,7 @@ struct mk_ctx {
   // TMA descriptor of the caller's KV pool (re-encoded when the pool pointer changes)
   alignas(64) CUtensorMap kv_map;
   const void* kv_map_ptr = nullptr;
-  // TMA descriptors of the dense weights for wide batches on tcgen05 ([3L + 1] maps), or null
+  // TMA descriptors of the weights for wide batches on tcgen05 ([4L + 1] maps), or null
   uint64_t* d_wmaps = nullptr;
   // timeline
   uint64_t* trace = nullptr;
@@ -541,14 +541,16 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_ctx** out) {
     free_ctx(c);
     return cuda_fail(e, "plan upload");
   }
-  // tensor maps of the dense weights, for the tcgen05 tiles of wide batches
+  // tensor maps of the weights, for the tcgen05 tiles of wide batches
   if (cfg->max_batch >= mk::kTcMinBatch) {
-    std::vector<CUtensorMap> maps(3 * L + 1);
+    std::vector<CUtensorMap> maps(mk::tc_map_count(L));
     for (int l = 0; l < L && rc == MK_OK; ++l) {
       const mk_layer_weights& s = w->layers[l];
       rc = encode_weight_map(s.w_qkv, nqkv, H, &maps[mk::tc_map_index(MK_OP_QKV, l, L)]);
       if (rc == MK_OK) rc = encode_weight_map(s.w_o, H, Hq * D, &maps[mk::tc_map_index(MK_OP_OPROJ, l, L)]);
       if (rc == MK_OK) rc = encode_weight_map(s.w_router, E, H, &maps[mk::tc_map_index(MK_OP_ROUTER, l, L)]);
+      if (rc == MK_OK)
+        rc = encode_weight_map(s.w_gate_up, E * 2 * F, H, &maps[mk::tc_map_index(MK_OP_MOE, l, L)]);
     }
     if (rc == MK_OK) rc = encode_weight_map(w->lm_head, cfg->vocab, H, &maps[mk::tc_map_index(MK_OP_HEAD, L, L)]);
     if (rc) { free_ctx(c); return rc; }

@@ -769,18 +769,18 @@ struct Producer {
 
   // Wide batches on tcgen05: the tile's weight rows as A operand units of MB rows x 64 columns
   // (K-major, 128-byte swizzle; TMA boxes of 16 rows, rows past the tile left as they are: their
-  // accumulator rows are never read).  A pass covers as many M-blocks as the tensor memory holds
-  // accumulators for (tc_accs per M-block, each MB rows x the batch rounded up to 16 columns);
-  // within a pass, records
-  // go slice by slice, each with up to kTcChunkBytes of units: several slices of all the pass's
-  // M-blocks, or one slice of a group of M-blocks.  Meta: row0 the first M-block, n the M-blocks,
-  // aux the first slice | slices << 16, e the pass's M-blocks (first | end << 16).
-  __device__ bool tc_tile(const mk_task& t, uint32_t ti) {
-    const int K = t.op == MK_OP_OPROJ ? p.Hq * p.D : p.H;
-    const uint64_t* map = p.wmaps + static_cast<size_t>(tc_map_index(t.op, t.layer, p.L)) * 16;
-    const int R = static_cast<int>(t.hi - t.lo), MB = tc_mblock(R), nmb = (R + MB - 1) / MB;
-    const int pmb = min(nmb, kTcCols / (tc_accs(t.op, p.B, K) * tc_batch_cols(p.B)));
-    const int upc = kTcChunkBytes / (MB * 128);
+  // accumulator rows are never read).  Gate/up runs have two units per (slice, M-block): the
+  // expert's gate rows, then the same FFN rows of its up projection.  A pass covers as many
+  // M-blocks as the tensor memory holds accumulators for (accs per M-block, each MB rows x the
+  // N columns); within a pass, records go slice by slice, each with up to kTcChunkBytes of
+  // units: several slices of all the pass's M-blocks, or one slice of a group of M-blocks.
+  // Meta: row0 the first M-block, n the M-blocks, aux the first slice | slices << 16, pad[2] the
+  // pass's M-blocks (first | end << 16), pad[4] the N columns the passes were sized for.
+  __device__ bool tc_emit(const mk_task& t, uint32_t ti, uint8_t op, const uint64_t* map, int K, int R, int y0, int y1,
+                          int nu, int accs, int ncols, uint32_t e, uint32_t idx, uint32_t aux_flag) {
+    const int MB = tc_mblock(R), nmb = (R + MB - 1) / MB;
+    const int pmb = min(nmb, kTcCols / (accs * ncols));
+    const int upc = kTcChunkBytes / (nu * MB * 128);   // (slice, M-block) pairs per record
     const int ns = (K + 63) / 64;
     #pragma unroll 1
     for (int m0 = 0; m0 < nmb; m0 += pmb) {
@@ -795,27 +795,33 @@ struct Producer {
           const int mb1 = min(m1, ma + mg);
           if (!acquire()) return false;
           Meta& m = meta();
-          m.kind = R_TC; m.op = static_cast<uint8_t>(t.op);
+          m.kind = R_TC; m.op = op;
           m.first = (m0 == 0 && s0 == 0 && ma == m0); m.last = (m1 == nmb && s1 == ns && mb1 == m1);
           m.layer = t.layer; m.n = static_cast<uint16_t>(mb1 - ma); m.row0 = static_cast<uint32_t>(ma);
-          m.idx = ti; m.e = static_cast<uint32_t>(m0) | (static_cast<uint32_t>(m1) << 16);
+          m.idx = idx; m.e = e;
           m.aux = static_cast<uint32_t>(s0) | (static_cast<uint32_t>(s1 - s0) << 16);
           m.lo = t.lo; m.hi = t.hi;
+          m.pad[2] = static_cast<uint32_t>(m0) | (static_cast<uint32_t>(m1) << 16);
+          m.pad[3] = aux_flag;
+          m.pad[4] = static_cast<uint32_t>(ncols);
           uint32_t bytes = 0;
           #pragma unroll 1
           for (int mm = ma; mm < mb1; ++mm) bytes += static_cast<uint32_t>((min(MB, R - mm * MB) + 15) / 16) * 2048u;
-          mbar_arrive_expect_tx(full(), bytes * static_cast<uint32_t>(s1 - s0));
+          mbar_arrive_expect_tx(full(), bytes * static_cast<uint32_t>((s1 - s0) * nu));
           uint8_t* dst = slot();
           #pragma unroll 1
           for (int sl = s0; sl < s1; ++sl) {
             #pragma unroll 1
             for (int mm = ma; mm < mb1; ++mm) {
-              const int u = (sl - s0) * (mb1 - ma) + (mm - ma);
               const int rows = min(MB, R - mm * MB);
               #pragma unroll 1
-              for (int j = 0; j * 16 < rows; ++j)
-                tma_load_2d(dst + u * MB * 128 + j * 2048, map, 64 * sl, static_cast<int>(t.lo) + mm * MB + 16 * j,
-                            full(), pol);
+              for (int un = 0; un < nu; ++un) {
+                const int u = ((sl - s0) * (mb1 - ma) + (mm - ma)) * nu + un;
+                const int y = (un == 0 ? y0 : y1) + mm * MB;
+                #pragma unroll 1
+                for (int j = 0; j * 16 < rows; ++j)
+                  tma_load_2d(dst + u * MB * 128 + j * 2048, map, 64 * sl, y + 16 * j, full(), pol);
+              }
             }
           }
           ++c;
@@ -823,6 +829,12 @@ struct Producer {
       }
     }
     return true;
+  }
+  __device__ bool tc_tile(const mk_task& t, uint32_t ti) {
+    const int K = t.op == MK_OP_OPROJ ? p.Hq * p.D : p.H;
+    const uint64_t* map = p.wmaps + static_cast<size_t>(tc_map_index(t.op, t.layer, p.L)) * 16;
+    return tc_emit(t, ti, static_cast<uint8_t>(t.op), map, K, static_cast<int>(t.hi - t.lo), static_cast<int>(t.lo), 0, 1,
+                   tc_accs(t.op, p.B, K), tc_batch_cols(p.B), 0u, ti, 0u);
   }
 
   // KV pages of this block's attention items: per page, K then V, each as D/64 boxes of
@@ -970,8 +982,26 @@ struct Producer {
     if (u0 >= u1) {
       if (!moe_control(R_GU, l, 0u, 1u)) return false;
     }
+    if (p.tc) {
+      // wide batch: each expert run on tcgen05, its routed pairs as the N columns
+      const uint64_t* map = p.wmaps + static_cast<size_t>(tc_map_index(MK_OP_MOE, l, p.L)) * 16;
+      #pragma unroll 1
+      for (int u = u0; u < u1;) {
+        const int a = u / F, f0 = u - a * F;
+        const int fend = min(F, u1 - a * F);
+        const int e = S.eact[a];
+        mk_task tt;
+        tt.op = MK_OP_MOE; tt.layer = static_cast<uint16_t>(l);
+        tt.lo = static_cast<uint32_t>(f0); tt.hi = static_cast<uint32_t>(fend); tt.reserved = 0;
+        const uint32_t lastgu = (a * F + fend >= u1) ? 1u : 0u;
+        if (!tc_emit(tt, 0u, MK_OP_MOE, map, H, fend - f0, e * 2 * F + f0, e * 2 * F + F + f0, 2, 4,
+                     tc_batch_cols(S.ecnt[e]), static_cast<uint32_t>(e), static_cast<uint32_t>(a), lastgu))
+          return false;
+        u = a * F + fend;
+      }
+    }
     #pragma unroll 1
-    for (int u = u0; u < u1;) {
+    for (int u = p.tc ? u1 : u0; u < u1;) {
       const int a = u / F, f0 = u - a * F;
       const int fend = min(F, u1 - a * F);
       const uint32_t lastgu = (a * F + fend >= u1) ? 1u : 0u;
@@ -1829,13 +1859,15 @@ struct Consumer {
   // 128-byte swizzle).  A normalised input takes its gain here; the row's 1/rms is applied to the
   // accumulators (a dot product is linear in it), from the sums of squares collected in ss.
   // Columns at or past K are zero.
-  __device__ __forceinline__ void tc_issue(const uint64_t* xbase, size_t xstride, int K, int s, uint64_t (&w)[16]) {
+  __device__ __forceinline__ int tc_row(const int32_t* rows, int n) const { return rows != nullptr ? rows[n] : n; }
+  __device__ __forceinline__ void tc_issue(const uint64_t* xbase, size_t xstride, int K, int s, int nrows,
+                                           const int32_t* rows, uint64_t (&w)[16]) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int i = threadIdx.x + h * kConsumerThreads;
-      const int b = i >> 3, k = 64 * s + 8 * (i & 7);
-      if (b < p.B && k < K) {
-        const uint64_t* src = xbase + static_cast<size_t>(b) * xstride + k;
+      const int n = i >> 3, k = 64 * s + 8 * (i & 7);
+      if (n < nrows && k < K) {
+        const uint64_t* src = xbase + static_cast<size_t>(tc_row(rows, n)) * xstride + k;
 #pragma unroll
         for (int q = 0; q < 8; q += 2) ll_ld2(src + q, w[8 * h + q], w[8 * h + q + 1]);
       } else {
@@ -1845,8 +1877,9 @@ struct Consumer {
     }
   }
   __device__ __forceinline__ bool tc_stage(const uint64_t* xbase, size_t xstride, const uint16_t* g, int K, int s,
-                                           int T, uint8_t* xb, int Bp, uint32_t tag, uint64_t (&w)[16], float (&ss)[2]) {
-    const int B = p.B;
+                                           int nrows, const int32_t* rows, int T, uint8_t* xb, int Bp, uint32_t tag,
+                                           uint64_t (&w)[16], float (&ss)[2]) {
+    const int B = nrows;
     // stale words (this step's tag not there yet): re-poll both pieces until every word is fresh
     uint32_t st = 0;
 #pragma unroll
@@ -1867,7 +1900,7 @@ struct Consumer {
         for (int h = 0; h < 2; ++h) {
           if ((st >> h) & 1u) {
             const int i = threadIdx.x + h * kConsumerThreads;
-            const uint64_t* src = xbase + static_cast<size_t>(i >> 3) * xstride + 64 * s + 8 * (i & 7);
+            const uint64_t* src = xbase + static_cast<size_t>(tc_row(rows, i >> 3)) * xstride + 64 * s + 8 * (i & 7);
 #pragma unroll
             for (int q = 0; q < 8; q += 2) ll_ld2(src + q, w[8 * h + q], w[8 * h + q + 1]);
 #pragma unroll
@@ -1924,7 +1957,7 @@ struct Consumer {
   // 32(w % 4) .. + 31 (M = 128: row = lane; M = 64: rows 16(w % 4) + lane for lanes < 16) and
   // half w / 4 of the batch columns.
   __device__ __forceinline__ void tc_epilogue(const OutMap& om, bool norm, uint32_t lo, int R, int MB, int m0, int m1,
-                                              int Bp, int T, int KG) {
+                                              int Bp, int T, int KG, int nrows, bool gu) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = warp & 3, hh = warp >> 2;
     const int half = Bp >> 1;
@@ -1933,10 +1966,33 @@ struct Consumer {
     #pragma unroll 1
     for (int m = m0; m < m1; ++m) {
       const int row = m * MB + r_in;
+      const int NA = gu ? 4 : KG + T - 1;
       const uint32_t ta = S.tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
-                          static_cast<uint32_t>((m - m0) * (KG + T - 1) * Bp + hh * half);
+                          static_cast<uint32_t>((m - m0) * NA * Bp + hh * half);
       #pragma unroll 1
       for (int c8 = 0; c8 < half; c8 += 8) {
+        if (gu) {
+          // gate (high, low accumulators) and up (high, low) of this lane's FFN row: SwiGLU of the
+          // pair's normalised input, to the pair's (row, slot)
+          float gh[8], gl[8], uh[8], ul[8];
+          tc_ld8(ta + Bp + c8, gl);
+          tc_ld8(ta + c8, gh);
+          tc_ld8(ta + 3 * Bp + c8, ul);
+          tc_ld8(ta + 2 * Bp + c8, uh);
+          if (lane_ok && row < R) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int n = hh * half + c8 + j;
+              if (n < nrows) {
+                const int ent = S.elist[n];
+                const int b = ent / p.K, slot = ent - b * p.K;
+                const float r = S.rstd[n];
+                put(om, true, lo + row, b, slot, (gl[j] + gh[j]) * r, (ul[j] + uh[j]) * r);
+              }
+            }
+          }
+          continue;
+        }
         float v[8], v1[8];
         tc_ld8(ta + (KG + T - 2) * Bp + c8, v1);   // the lowest term
         #pragma unroll 1
@@ -1969,9 +2025,28 @@ struct Consumer {
     const uint32_t lo = meta().lo, hi = meta().hi;
     const int R = static_cast<int>(hi - lo);
     const int K = op == MK_OP_OPROJ ? p.Hq * p.D : p.H;
-    const int kind = op == MK_OP_QKV ? 0 : op == MK_OP_OPROJ ? 1 : op == MK_OP_ROUTER ? 2 : 3;
-    const int T = tc_terms(op), KG = tc_hi_groups(op, p.B, K), NA = KG + T - 1;
-    const int Bp = tc_batch_cols(p.B), MB = tc_mblock(R), ns = (K + 63) / 64;
+    // gate/up of one expert run: the N columns are the (row, slot) pairs routed to the expert
+    const bool gu = op == MK_OP_MOE;
+    const int kind = op == MK_OP_QKV ? 0 : op == MK_OP_OPROJ ? 1 : (op == MK_OP_ROUTER || gu) ? 2 : 3;
+    int nrows = p.B;
+    const int32_t* rows = nullptr;
+    if (gu) {
+      nrows = expert_pairs(static_cast<int>(meta().e));   // S.elist; ends with a barrier
+      if (threadIdx.x < nrows) S.wlist[0][threadIdx.x] = S.elist[threadIdx.x] / p.K;
+      cbar();
+      rows = S.wlist[0];
+    }
+    const int T = gu ? 2 : tc_terms(op), KG = gu ? 1 : tc_hi_groups(op, p.B, K);
+    const int NA = gu ? 4 : KG + T - 1;
+    // the N columns the producer sized the passes for (the routing both sides computed agrees;
+    // the check keeps every accumulator address inside the allocation regardless)
+    const int Bp = static_cast<int>(meta().pad[4]), MB = tc_mblock(R), ns = (K + 63) / 64;
+    if (Bp != tc_batch_cols(nrows)) {
+      if (threadIdx.x == 0)
+        record_error(p, MK_ERR_DEVICE_BOUNDS, op, l, 0u, static_cast<uint32_t>(nrows), 0, Bp, true);
+      cbar();
+      return false;
+    }
     const uint32_t xsz = static_cast<uint32_t>(T * Bp * 128);
     const int NX = min(kTcXBufs, static_cast<int>((kMoeScratch * 4) / xsz));
     const uint16_t* g = kind == 0 ? p.layers[l].attn_norm : kind == 2 ? p.layers[l].ffn_norm
@@ -1999,7 +2074,7 @@ struct Consumer {
     for (;;) {
       const int ma = static_cast<int>(meta().row0), nmc = meta().n;
       const int s0 = static_cast<int>(meta().aux & 0xffffu), nsc = static_cast<int>(meta().aux >> 16);
-      const int pm0 = static_cast<int>(meta().e & 0xffffu), pm1 = static_cast<int>(meta().e >> 16);
+      const int pm0 = static_cast<int>(meta().pad[2] & 0xffffu), pm1 = static_cast<int>(meta().pad[2] >> 16);
       const bool last = meta().last;
       if (pm0 != pass_m0) { pass_m0 = pm0; staged = 0; ss[0] = 0.f; ss[1] = 0.f; }
       const uint32_t wa = smem_u32(slot());
@@ -2013,8 +2088,8 @@ struct Consumer {
           }
           // (one slice's 16 loads per thread at a time: a second slice's words in flight together,
           // or the next slice's issued before the barrier, made ptxas spill)
-          tc_issue(xbase, xstride, K, sl, xw);
-          ok = tc_stage(xbase, xstride, g, K, sl, T, xb0 + buf * xsz, Bp, tag, xw, ss) && ok;
+          tc_issue(xbase, xstride, K, sl, nrows, rows, xw);
+          ok = tc_stage(xbase, xstride, g, K, sl, nrows, rows, T, xb0 + buf * xsz, Bp, tag, xw, ss) && ok;
           fence_proxy_async_smem();   // generic writes, read by the tensor cores (async proxy)
           staged = sl + 1;
         }
@@ -2029,15 +2104,22 @@ struct Consumer {
           const bool acc_lo = sl > 0, acc_hi = sl >= KG;
           #pragma unroll 1
           for (int mi = 0; mi < nmc; ++mi) {
-            const uint64_t ad = tc_desc_sw128(wa + static_cast<uint32_t>((si * nmc + mi) * MB * 128));
-            // accumulators of the M-block: the high term's groups, then one per lower term
+            // accumulators of the M-block: the high term's groups, then one per lower term (gate/up:
+            // gate high, gate low, up high, up low)
             const uint32_t d = S.tmem_base + static_cast<uint32_t>((ma + mi - pm0) * NA * Bp);
-            const uint32_t dh = d + static_cast<uint32_t>((sl % KG) * Bp);
-            #pragma unroll
-            for (int k16 = 0; k16 < 4; ++k16) {
-              tc_mma_elect(dh, ad + 2 * k16, xd + 2 * k16, idesc, acc_hi || k16 > 0);
-              tc_mma_elect(d + KG * Bp, ad + 2 * k16, xd + td + 2 * k16, idesc, acc_lo || k16 > 0);
-              if (T == 3) tc_mma_elect(d + (KG + 1) * Bp, ad + 2 * k16, xd + 2 * td + 2 * k16, idesc, acc_lo || k16 > 0);
+            #pragma unroll 1
+            for (int un = 0; un < (gu ? 2 : 1); ++un) {
+              const int u = (si * nmc + mi) * (gu ? 2 : 1) + un;
+              const uint64_t ad = tc_desc_sw128(wa + static_cast<uint32_t>(u * MB * 128));
+              const uint32_t du = d + static_cast<uint32_t>(un * 2 * Bp);
+              const uint32_t dh = du + static_cast<uint32_t>((sl % KG) * Bp);
+              #pragma unroll
+              for (int k16 = 0; k16 < 4; ++k16) {
+                tc_mma_elect(dh, ad + 2 * k16, xd + 2 * k16, idesc, acc_hi || k16 > 0);
+                tc_mma_elect(du + KG * Bp, ad + 2 * k16, xd + td + 2 * k16, idesc, acc_lo || k16 > 0);
+                if (T == 3)
+                  tc_mma_elect(du + (KG + 1) * Bp, ad + 2 * k16, xd + 2 * td + 2 * k16, idesc, acc_lo || k16 > 0);
+              }
             }
           }
           if (last_use) tc_commit_elect(&S.xbar[buf]);
@@ -2059,12 +2141,12 @@ struct Consumer {
             v += __shfl_xor_sync(0xffffffffu, v, 2);
             v += __shfl_xor_sync(0xffffffffu, v, 4);
             const int b = (threadIdx.x >> 3) + 32 * h;
-            if ((threadIdx.x & 7) == 0 && b < p.B) S.rstd[b] = 1.0f / sqrtf(v / static_cast<float>(K) + p.eps);
+            if ((threadIdx.x & 7) == 0 && b < nrows) S.rstd[b] = 1.0f / sqrtf(v / static_cast<float>(K) + p.eps);
           }
         }
         cbar();
         tc_fence_after();
-        tc_epilogue(out_map(op, l), kind != 1, lo, R, MB, pm0, pm1, Bp, T, KG);
+        tc_epilogue(out_map(gu ? int(R_OP_GU) : op, l), kind != 1, lo, R, MB, pm0, pm1, Bp, T, KG, nrows, gu);
         tc_fence_before();   // these reads precede the next pass's MMAs (behind the next barrier)
       }
       if (last) break;

@@ -107,10 +107,13 @@ MK_HD int tc_hi_groups(int op, int B, int K) {
   return g > 1 ? g : 1;
 }
 MK_HD int tc_accs(int op, int B, int K) { return tc_hi_groups(op, B, K) + tc_terms(op) - 1; }
-// tensor map of a dense weight matrix: QKV of layer l, O-proj, router, then the LM head
+// tensor map of a weight matrix: QKV of layer l, O-proj, router, the LM head, then the experts'
+// gate/up rows of layer l ([E * 2F rows][H])
 MK_HD int tc_map_index(int op, int layer, int L) {
-  return op == MK_OP_QKV ? layer : op == MK_OP_OPROJ ? L + layer : op == MK_OP_ROUTER ? 2 * L + layer : 3 * L;
+  return op == MK_OP_QKV ? layer : op == MK_OP_OPROJ ? L + layer : op == MK_OP_ROUTER ? 2 * L + layer
+       : op == MK_OP_MOE ? 3 * L + 1 + layer : 3 * L;
 }
+constexpr int tc_map_count(int L) { return 4 * L + 1; }
 
 MK_HD int gemv_rows_per_chunk(int K) {
   int r = kSlotBytes / (2 * K);
@@ -182,7 +185,7 @@ struct alignas(64) Params {
   // static plan
   int32_t n_qkv_tiles, n_o_tiles, n_router_tiles;
   int32_t tc;                   // this step runs the dense GEMV tiles on tcgen05 (wide batch)
-  const uint64_t* wmaps;        // [3L + 1][16] TMA descriptors of the dense weights (box 64 x 16, 128-byte swizzle)
+  const uint64_t* wmaps;        // [4L + 1][16] TMA descriptors of the weights (box 64 x 16, 128-byte swizzle)
   uint64_t watchdog_ns;
   const mk_task* tasks;
   const int32_t* task_off;      // [n_ctas + 1]
