@@ -289,7 +289,7 @@ struct mk_ctx {
   uint8_t* ws = nullptr;
   // tagged 8-byte words (value | step tag << 32)
   uint64_t *X = nullptr, *QKV = nullptr, *ATT = nullptr, *PO = nullptr, *PML = nullptr, *RLOG = nullptr,
-           *HB = nullptr, *PT = nullptr;
+           *HB = nullptr, *PT = nullptr, *YD = nullptr;
   uint16_t* wdt = nullptr;   // transposed down projections [L][E][F][H] (small-batch MoE path), or null
   float* argp = nullptr;     // greedy selection: per-block (max, second, index) of its LM-head rows
   bool small_ok = false;
@@ -513,6 +513,7 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_ctx** out) {
       {(void**)&c->RLOG, (size_t)L * MB * E * w8},
       {(void**)&c->HB, (size_t)L * MB * K * F * w8},
       {(void**)&c->PT, c->small_ok ? (size_t)L * c->n_ctas * mk::kSmallMaxB * H * w8 : 0},
+      {(void**)&c->YD, MB >= mk::kTcMinBatch ? (size_t)L * MB * K * H * w8 : 0},
       {(void**)&c->RIDS, (size_t)L * MB * K * i4},
       {(void**)&c->argp, (size_t)c->n_ctas * MB * 4 * f4},
       {(void**)&c->RW, (size_t)L * MB * K * f4},
@@ -551,6 +552,7 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_ctx** out) {
       if (rc == MK_OK) rc = encode_weight_map(s.w_router, E, H, &maps[mk::tc_map_index(MK_OP_ROUTER, l, L)]);
       if (rc == MK_OK)
         rc = encode_weight_map(s.w_gate_up, E * 2 * F, H, &maps[mk::tc_map_index(MK_OP_MOE, l, L)]);
+      if (rc == MK_OK) rc = encode_weight_map(s.w_down, E * H, F, &maps[mk::tc_map_index(mk::kTcOpDown, l, L)]);
     }
     if (rc == MK_OK) rc = encode_weight_map(w->lm_head, cfg->vocab, H, &maps[mk::tc_map_index(MK_OP_HEAD, L, L)]);
     if (rc) { free_ctx(c); return rc; }
@@ -701,7 +703,7 @@ static int make_params(mk_ctx* c, mk::Params& p, int32_t batch, const uint8_t* d
   p.item_off = reinterpret_cast<const int32_t*>(d + c->off_item_off);
   p.pair_first = reinterpret_cast<const int32_t*>(d + c->off_pair);
   p.X = c->X; p.QKV = c->QKV; p.ATT = c->ATT; p.PO = c->PO; p.PML = c->PML; p.RLOG = c->RLOG; p.RIDS = c->RIDS;
-  p.RW = c->RW; p.HB = c->HB;
+  p.RW = c->RW; p.HB = c->HB; p.YD = c->YD;
   p.small_moe = c->small_ok && mk::small_moe_batch(batch, cf.hidden) ? 1 : 0;
   p.PT = c->PT;
   p.next_token = next_token; p.margin = margin; p.argp = c->argp;

@@ -405,7 +405,8 @@ __device__ __forceinline__ bool tr_on(const Params& p) { return kTrace && p.trac
 // --------------------------------------------------------------------------- shared memory
 enum : uint8_t { R_EMBED = 1, R_GEMV = 2, R_ATTN = 3, R_GU = 4, R_DOWN = 5, R_END = 6, R_ROUTE = 7,
                  R_DT = 9, R_RED = 10,    // small-batch MoE: transposed down rows; partial-sum reduction
-                 R_TC = 11 };             // wide batch: a dense GEMV chunk for tcgen05
+                 R_TC = 11,               // wide batch: a tcgen05 GEMV chunk
+                 R_YRED = 12 };           // wide batch: sum the per-slot down-projection outputs of own rows
 // GEMV stream kinds beyond the task ops (MK_OP_QKV / OPROJ / ROUTER / HEAD)
 enum : int { R_OP_GU = 100 };
 
@@ -1036,6 +1037,32 @@ struct Producer {
     // down
     const uint32_t r0 = static_cast<uint32_t>(static_cast<uint64_t>(H) * cta / p.n_ctas);
     const uint32_t r1 = static_cast<uint32_t>(static_cast<uint64_t>(H) * (cta + 1) / p.n_ctas);
+    if (p.tc) {
+      // wide batch: (active expert, 128-row block) units dealt evenly over the blocks, consecutive
+      // units of one expert forming one run (contiguous hidden rows); each run on tcgen05 writes its
+      // pairs' weighted outputs, then the block sums the slots of its own hidden rows
+      const uint64_t* map = p.wmaps + static_cast<size_t>(tc_map_index(kTcOpDown, l, p.L)) * 16;
+      const int nrb = (H + kTcDownRows - 1) / kTcDownRows;
+      const int U = nact * nrb;
+      const int ua = static_cast<int>(static_cast<int64_t>(U) * cta / p.n_ctas);
+      const int ub = static_cast<int>(static_cast<int64_t>(U) * (cta + 1) / p.n_ctas);
+      #pragma unroll 1
+      for (int u = ua; u < ub;) {
+        const int a = u / nrb, rb = u - a * nrb;
+        const int rend = min(nrb, rb + (ub - u));
+        const int e = S.eact[a];
+        mk_task tt;
+        tt.op = static_cast<uint16_t>(kTcOpDown); tt.layer = static_cast<uint16_t>(l);
+        tt.lo = static_cast<uint32_t>(rb * kTcDownRows); tt.hi = static_cast<uint32_t>(min(H, rend * kTcDownRows));
+        tt.reserved = 0;
+        if (!tc_emit(tt, 0u, static_cast<uint8_t>(kTcOpDown), map, F, static_cast<int>(tt.hi - tt.lo),
+                     e * H + static_cast<int>(tt.lo), 0, 1, 2, tc_batch_cols(S.ecnt[e]), static_cast<uint32_t>(e),
+                     static_cast<uint32_t>(a), 0u))
+          return false;
+        u += rend - rb;
+      }
+      return moe_control(R_YRED, l, r0, r1);
+    }
     const uint32_t rowb = static_cast<uint32_t>(F) * 2u;
     if (r1 <= r0 || nact == 0) return moe_control(R_DOWN, l, r0, r1);
     const int rpc = min(static_cast<int>(r1 - r0), static_cast<int>(kSlotBytes / rowb));
@@ -2015,6 +2042,70 @@ struct Consumer {
     }
   }
 
+  // Down projection run: accumulators (high, low term) of hidden rows x pairs; each pair's value,
+  // times its combine weight, to YD[l][row][slot][hidden row].
+  __device__ __forceinline__ void tc_epilogue_down(int l, uint32_t lo, int R, int MB, int m0, int m1, int Bp, int nrows) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int q = warp & 3, hh = warp >> 2;
+    const int half = Bp >> 1;
+    const int r_in = MB == 128 ? 32 * q + lane : 16 * q + lane;
+    const bool lane_ok = MB == 128 || lane < 16;
+    uint64_t* yd = p.YD + static_cast<size_t>(l) * p.max_batch * p.K * p.H;
+    #pragma unroll 1
+    for (int m = m0; m < m1; ++m) {
+      const int row = m * MB + r_in;
+      const uint32_t ta = S.tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
+                          static_cast<uint32_t>((m - m0) * 2 * Bp + hh * half);
+      #pragma unroll 1
+      for (int c8 = 0; c8 < half; c8 += 8) {
+        float hi8[8], lo8[8];
+        tc_ld8(ta + Bp + c8, lo8);
+        tc_ld8(ta + c8, hi8);
+        if (lane_ok && row < R) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int n = hh * half + c8 + j;
+            if (n < nrows) {
+              const int ent = S.elist[n];   // b * K + slot
+              ll_st(yd + static_cast<size_t>(ent) * p.H + lo + row, S.rwcache[ent] * (lo8[j] + hi8[j]), tg);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  // Wide batch: x_out of this block's hidden rows [lo, hi) = x_mid + the slots' weighted down
+  // outputs, summed in slot order (the small-batch and register-group paths' order).
+  __device__ __forceinline__ bool y_reduce() {
+    const int l = meta().layer;
+    const int r0 = static_cast<int>(meta().lo), nrow = static_cast<int>(meta().hi) - r0;
+    twait = globaltimer();
+    if (nrow <= 0) return true;
+    const int B = p.B, K = p.K;
+    const size_t xs = static_cast<size_t>(p.max_batch) * p.H;
+    const uint64_t* yd = p.YD + static_cast<size_t>(l) * p.max_batch * K * p.H;
+    float* Y = S.moe;   // [B][K][nrow]
+    const FastDiv dn(nrow);
+    bool ok = ll_gather(p, B * K * nrow, [=](int i) {
+      const int bj = dn.div(i), r = i - bj * nrow;
+      return yd + static_cast<size_t>(bj) * p.H + r0 + r;
+    }, Y, tg);
+    if (!ok) ll_timeout(p, MK_OP_MOE, l, tg);
+    if (!cbar_and(ok)) return false;
+    #pragma unroll 1
+    for (int i = threadIdx.x; i < B * nrow; i += kConsumerThreads) {
+      const int b = i / nrow, r = i - b * nrow;
+      float acc = 0.f;
+      #pragma unroll 1
+      for (int j = 0; j < K; ++j) acc += Y[(b * K + j) * nrow + r];
+      const size_t off = static_cast<size_t>(b) * p.H + r0 + r;
+      ll_st(p.X + (2 * static_cast<size_t>(l) + 2) * xs + off,
+            ll_f(ll_ld(p.X + (2 * static_cast<size_t>(l) + 1) * xs + off)) + acc, tg);
+    }
+    return true;
+  }
+
   // A dense GEMV tile (QKV, O-proj, router, LM head) of a wide batch on tcgen05: for each record,
   // per slice, the consumers stage the batch's input slice (unless an earlier record of the pass
   // did), then one thread issues the MMAs of the record's units of that slice into the pass's
@@ -2024,17 +2115,24 @@ struct Consumer {
     const int op = meta().op, l = meta().layer;
     const uint32_t lo = meta().lo, hi = meta().hi;
     const int R = static_cast<int>(hi - lo);
-    const int K = op == MK_OP_OPROJ ? p.Hq * p.D : p.H;
-    // gate/up of one expert run: the N columns are the (row, slot) pairs routed to the expert
-    const bool gu = op == MK_OP_MOE;
-    const int kind = op == MK_OP_QKV ? 0 : op == MK_OP_OPROJ ? 1 : (op == MK_OP_ROUTER || gu) ? 2 : 3;
+    // gate/up of one expert run, or a run of one expert's down projection: the N columns are the
+    // (row, slot) pairs routed to the expert
+    const bool gu = op == MK_OP_MOE, dn = op == kTcOpDown;
+    const int K = op == MK_OP_OPROJ ? p.Hq * p.D : dn ? p.F : p.H;
+    // input kinds: 0 x_in/attn_norm, 1 un-normalised (attention output; SwiGLU outputs), 2
+    // x_mid/ffn_norm, 3 x_final/final_norm
+    const int kind = op == MK_OP_QKV ? 0 : (op == MK_OP_OPROJ || dn) ? 1 : (op == MK_OP_ROUTER || gu) ? 2 : 3;
     int nrows = p.B;
     const int32_t* rows = nullptr;
-    if (gu) {
+    if (gu || dn) {
       nrows = expert_pairs(static_cast<int>(meta().e));   // S.elist; ends with a barrier
-      if (threadIdx.x < nrows) S.wlist[0][threadIdx.x] = S.elist[threadIdx.x] / p.K;
-      cbar();
-      rows = S.wlist[0];
+      if (gu) {   // gate/up reads the pairs' x_mid rows; the down projection their SwiGLU rows
+        if (threadIdx.x < nrows) S.wlist[0][threadIdx.x] = S.elist[threadIdx.x] / p.K;
+        cbar();
+        rows = S.wlist[0];
+      } else {
+        rows = S.elist;
+      }
     }
     const int T = gu ? 2 : tc_terms(op), KG = gu ? 1 : tc_hi_groups(op, p.B, K);
     const int NA = gu ? 4 : KG + T - 1;
@@ -2053,7 +2151,10 @@ struct Consumer {
                       : kind == 3 ? p.final_norm : nullptr;
     const uint64_t* xbase;
     size_t xstride;
-    if (kind == 1) {
+    if (dn) {
+      xstride = static_cast<size_t>(p.F);
+      xbase = p.HB + static_cast<size_t>(l) * p.max_batch * p.K * xstride;
+    } else if (kind == 1) {
       xstride = static_cast<size_t>(p.Hq) * p.D;
       xbase = p.ATT + static_cast<size_t>(l) * p.max_batch * xstride;
     } else {
@@ -2146,7 +2247,8 @@ struct Consumer {
         }
         cbar();
         tc_fence_after();
-        tc_epilogue(out_map(gu ? int(R_OP_GU) : op, l), kind != 1, lo, R, MB, pm0, pm1, Bp, T, KG, nrows, gu);
+        if (dn) tc_epilogue_down(l, lo, R, MB, pm0, pm1, Bp, nrows);
+        else tc_epilogue(out_map(gu ? int(R_OP_GU) : op, l), kind != 1, lo, R, MB, pm0, pm1, Bp, T, KG, nrows, gu);
         tc_fence_before();   // these reads precede the next pass's MMAs (behind the next barrier)
       }
       if (last) break;
@@ -3401,6 +3503,9 @@ struct Consumer {
         case R_ATTN: ok = attn_item(); break;
         case R_TC:
           if constexpr (TB == 4) ok = tc_gemv();
+          break;
+        case R_YRED:
+          if constexpr (TB == 4) ok = y_reduce();
           break;
         case R_DOWN: ok = moe_down(); break;
         case R_ROUTE: ok = route_local(); break;

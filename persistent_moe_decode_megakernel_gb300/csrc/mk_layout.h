@@ -107,13 +107,17 @@ MK_HD int tc_hi_groups(int op, int B, int K) {
   return g > 1 ? g : 1;
 }
 MK_HD int tc_accs(int op, int B, int K) { return tc_hi_groups(op, B, K) + tc_terms(op) - 1; }
-// tensor map of a weight matrix: QKV of layer l, O-proj, router, the LM head, then the experts'
-// gate/up rows of layer l ([E * 2F rows][H])
+// the tile kind of the experts' down projections (a record op beside the MK_OP_* of mk_debug.h)
+constexpr int kTcOpDown = 16;
+// hidden rows per down-projection unit (one 128-row M-block of one expert)
+constexpr int kTcDownRows = 128;
+// tensor map of a weight matrix: QKV of layer l, O-proj, router, the LM head, the experts' gate/up
+// rows of layer l ([E * 2F rows][H]), then their down projections ([E * H rows][F])
 MK_HD int tc_map_index(int op, int layer, int L) {
   return op == MK_OP_QKV ? layer : op == MK_OP_OPROJ ? L + layer : op == MK_OP_ROUTER ? 2 * L + layer
-       : op == MK_OP_MOE ? 3 * L + 1 + layer : 3 * L;
+       : op == MK_OP_MOE ? 3 * L + 1 + layer : op == kTcOpDown ? 4 * L + 1 + layer : 3 * L;
 }
-constexpr int tc_map_count(int L) { return 4 * L + 1; }
+constexpr int tc_map_count(int L) { return 5 * L + 1; }
 
 MK_HD int gemv_rows_per_chunk(int K) {
   int r = kSlotBytes / (2 * K);
@@ -223,6 +227,7 @@ struct alignas(64) Params {
   uint64_t* PML;   // [L][max_items][G][2]   their (max, sum)
   uint64_t* RLOG;  // [L][max_batch][E] router logits (+ bias)
   uint64_t* HB;    // [L][max_batch][K][F] SwiGLU activations per (row, slot)
+  uint64_t* YD;    // [L][max_batch][K][H] weighted down-projection output per (row, slot) (wide batches)
   int32_t small_moe;    // this step runs the small-batch MoE path
   uint64_t* PT;         // [L][n_ctas][kSmallMaxB][H] per-block partial MoE outputs (small-batch path)
   int32_t* next_token;  // greedy selection: [B] argmax of the logits, or null (not requested)
