@@ -458,6 +458,24 @@ struct __align__(1024) Smem {
   int32_t flag;
   int32_t is_last;
   uint32_t tag;          // this step's tag, read from the uploaded step data
+  // tcgen05 tiles: the consumers post one request per staged input slice; one warp of the producer
+  // warpgroup issues its MMAs
+  struct TcReq {
+    uint32_t a;       // shared address of the slice's first A unit (units of an M-block consecutive)
+    uint32_t x;       // shared address of the input buffer (terms bp * 128 bytes apart)
+    uint32_t d;       // tensor-memory address of the first M-block's accumulators
+    uint32_t idesc;
+    uint32_t nmc, nu; // M-blocks, A units per M-block (2: gate, up)
+    uint32_t ustride; // bytes between A units
+    uint32_t dstride, dunit;   // accumulator columns between M-blocks, between a block's units
+    uint32_t dh, dlo; // high-term accumulator, first lower-term accumulator (columns from a unit's)
+    uint32_t bp;      // N columns (and rows of an input term)
+    uint32_t flags;   // 1 accumulate high, 2 accumulate lower, 4 commit wbar, 8 stop, T << 4, (buffer + 1) << 8
+    uint32_t pad_[3];
+  };
+  TcReq tcreq[kTcReqs];
+  uint64_t reqbar[kTcReqs]; // consumers (all) -> issuer: request i is written and its slice staged
+  uint64_t ackbar[kTcReqs]; // issuer -> consumers: request i has been read
   uint64_t xbar[kTcXBufs];  // tcgen05 tiles: the tensor cores have read input slice buffer i
   uint64_t wbar;            // tcgen05 tiles: the tensor cores have read the current ring record
   uint32_t tmem_base;       // tensor-memory address of this block's accumulators (wide batches)
@@ -1304,6 +1322,62 @@ __device__ __noinline__ H8 load_h8(const Params& p, const uint64_t* src, uint32_
   }
 }
 
+// --------------------------------------------------------------------------- tcgen05 issuer
+// One warp of the producer warpgroup (wide batches): takes the consumers' requests in order, one
+// per staged input slice, and issues its MMAs (one elected lane; operands computed by the whole
+// warp, so they are warp-uniform), then the commits it asks for.  Ends at the stop request the
+// consumers post at the end of the step.
+__device__ void tc_issuer(const Params& p, Smem& S) {
+  const int lane = threadIdx.x & 31;
+  #pragma unroll 1
+  for (uint32_t r = 0;; ++r) {
+    const int slot = static_cast<int>(r % kTcReqs);
+    const uint32_t ph = (r / kTcReqs) & 1u;
+    if (!mbar_try_wait(&S.reqbar[slot], ph)) {
+      const uint64_t t0 = globaltimer();
+      bool got = false;
+      #pragma unroll 1
+      for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(&S.reqbar[slot], ph)) { got = true; break; }
+        // the consumers post until the end of the step, even an aborted one; this bound only
+        // guards against a fault of this kernel
+        if ((it & 255u) == 0u && globaltimer() - t0 > 4u * p.watchdog_ns + 1000000000ull) break;
+      }
+      if (!got) {
+        if (lane == 0) record_error(p, MK_ERR_TIMEOUT, 0, -1, MK_WAIT_RING, r, 0, -2, true);
+        return;
+      }
+    }
+    const Smem::TcReq q = S.tcreq[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.ackbar[slot]);
+    if (q.flags & 8u) return;
+    tc_fence_after();
+    const uint32_t T = (q.flags >> 4) & 15u;
+    const uint64_t xd = tc_desc_sw128(q.x);
+    const uint64_t td = static_cast<uint64_t>((q.bp * 128u) >> 4);   // one input term
+    const bool acc_hi = (q.flags & 1u) != 0u, acc_lo = (q.flags & 2u) != 0u;
+    #pragma unroll 1
+    for (uint32_t mi = 0; mi < q.nmc; ++mi) {
+      #pragma unroll 1
+      for (uint32_t un = 0; un < q.nu; ++un) {
+        const uint64_t ad = tc_desc_sw128(q.a + (mi * q.nu + un) * q.ustride);
+        const uint32_t du = q.d + mi * q.dstride + un * q.dunit;
+        #pragma unroll
+        for (int k16 = 0; k16 < 4; ++k16) {
+          tc_mma_elect(du + q.dh, ad + 2 * k16, xd + 2 * k16, q.idesc, acc_hi || k16 > 0);
+          #pragma unroll 1
+          for (uint32_t t = 1; t < T; ++t)
+            tc_mma_elect(du + q.dlo + (t - 1u) * q.bp, ad + 2 * k16, xd + t * td + 2 * k16, q.idesc, acc_lo || k16 > 0);
+        }
+      }
+    }
+    const uint32_t xb = (q.flags >> 8) & 15u;
+    if (xb != 0u) tc_commit_elect(&S.xbar[xb - 1u]);
+    if (q.flags & 4u) tc_commit_elect(&S.wbar);
+  }
+}
+
 // --------------------------------------------------------------------------- consumer
 // Warps consume ring records independently (each waits for and releases every
 // record of a tile); block-wide barriers are taken only at tile boundaries --
@@ -1866,6 +1940,28 @@ struct Consumer {
   uint32_t xst = 0;   // per input buffer i: bit i a commit on xbar[i] not yet waited for, bit 4 + i its parity
   uint32_t wph = 0;   // parity of the next wbar phase
 
+  // Post request rq (every consumer thread, after its share of the slice is staged and fenced):
+  // thread 0 writes the fields once the issuer has read the slot's previous request; each thread's
+  // arrival releases its staged writes to the issuer.
+  uint32_t rq = 0;
+  __device__ __forceinline__ void tc_post(uint32_t a, uint32_t x, uint32_t d, uint32_t idesc, int nmc, int nu,
+                                          int ustride, int dstride, int dunit, int dh, int dlo, int bp, uint32_t flags) {
+    const int slot = static_cast<int>(rq % kTcReqs);
+    if (threadIdx.x == 0) {
+      if (rq >= static_cast<uint32_t>(kTcReqs)) tc_wait(&S.ackbar[slot], ((rq / kTcReqs) - 1u) & 1u);
+      Smem::TcReq& r = S.tcreq[slot];
+      r.a = a; r.x = x; r.d = d; r.idesc = idesc;
+      r.nmc = static_cast<uint32_t>(nmc); r.nu = static_cast<uint32_t>(nu); r.ustride = static_cast<uint32_t>(ustride);
+      r.dstride = static_cast<uint32_t>(dstride); r.dunit = static_cast<uint32_t>(dunit);
+      r.dh = static_cast<uint32_t>(dh); r.dlo = static_cast<uint32_t>(dlo); r.bp = static_cast<uint32_t>(bp);
+      r.flags = flags;
+    }
+    mbar_arrive(&S.reqbar[slot]);
+    ++rq;
+  }
+  // the issuing warp's last request (every consumer thread, at the end of the step)
+  __device__ __forceinline__ void tc_stop() { tc_post(0u, 0u, 0u, 0u, 0, 0, 0, 0, 0, 0, 0, 0, 8u); }
+
   // every consumer thread: wait for a phase of a tensor-core commit barrier (the work behind it
   // depends on no other block, so the limit only guards against a fault of this kernel)
   __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t ph) {
@@ -2187,50 +2283,25 @@ struct Consumer {
             ok = tc_wait(&S.xbar[buf], (xst >> (4 + buf)) & 1u) && ok;
             xst ^= (1u << buf) | (1u << (4 + buf));
           }
-          // (one slice's 16 loads per thread at a time: a second slice's words in flight together,
-          // or the next slice's issued before the barrier, made ptxas spill)
           tc_issue(xbase, xstride, K, sl, nrows, rows, xw);
           ok = tc_stage(xbase, xstride, g, K, sl, nrows, rows, T, xb0 + buf * xsz, Bp, tag, xw, ss) && ok;
           fence_proxy_async_smem();   // generic writes, read by the tensor cores (async proxy)
           staged = sl + 1;
         }
-        ok = cbar_and(ok);
-        if (!ok) break;
+        // the slice's MMAs go to the issuing warp; the record's last slice also commits the ring
+        // record (its slot is refilled only after the tensor cores have read it)
         const bool last_use = ma + nmc == pm1;   // the slice's last record in this pass
-        if (threadIdx.x < 32) {
-          // warp 0, converged: descriptors advance in 16-byte units (32 bytes per 16 columns of K)
-          tc_fence_after();
-          const uint64_t xd = tc_desc_sw128(smem_u32(xb0) + static_cast<uint32_t>(buf) * xsz);
-          const uint64_t td = static_cast<uint64_t>((Bp * 128) >> 4);   // one input term
-          const bool acc_lo = sl > 0, acc_hi = sl >= KG;
-          #pragma unroll 1
-          for (int mi = 0; mi < nmc; ++mi) {
-            // accumulators of the M-block: the high term's groups, then one per lower term (gate/up:
-            // gate high, gate low, up high, up low)
-            const uint32_t d = S.tmem_base + static_cast<uint32_t>((ma + mi - pm0) * NA * Bp);
-            #pragma unroll 1
-            for (int un = 0; un < (gu ? 2 : 1); ++un) {
-              const int u = (si * nmc + mi) * (gu ? 2 : 1) + un;
-              const uint64_t ad = tc_desc_sw128(wa + static_cast<uint32_t>(u * MB * 128));
-              const uint32_t du = d + static_cast<uint32_t>(un * 2 * Bp);
-              const uint32_t dh = du + static_cast<uint32_t>((sl % KG) * Bp);
-              #pragma unroll
-              for (int k16 = 0; k16 < 4; ++k16) {
-                tc_mma_elect(dh, ad + 2 * k16, xd + 2 * k16, idesc, acc_hi || k16 > 0);
-                tc_mma_elect(du + KG * Bp, ad + 2 * k16, xd + td + 2 * k16, idesc, acc_lo || k16 > 0);
-                if (T == 3)
-                  tc_mma_elect(du + (KG + 1) * Bp, ad + 2 * k16, xd + 2 * td + 2 * k16, idesc, acc_lo || k16 > 0);
-              }
-            }
-          }
-          if (last_use) tc_commit_elect(&S.xbar[buf]);
-        }
+        const int nu = gu ? 2 : 1;
+        tc_post(wa + static_cast<uint32_t>(si * nmc * nu * MB * 128), smem_u32(xb0) + static_cast<uint32_t>(buf) * xsz,
+                S.tmem_base + static_cast<uint32_t>((ma - pm0) * NA * Bp), idesc, nmc, nu, MB * 128, NA * Bp, 2 * Bp,
+                (sl % KG) * Bp, KG * Bp, Bp,
+                (sl >= KG ? 1u : 0u) | (sl > 0 ? 2u : 0u) | (si + 1 == nsc ? 4u : 0u) | (static_cast<uint32_t>(T) << 4) |
+                    (last_use ? static_cast<uint32_t>(buf + 1) << 8 : 0u));
         if (last_use) xst |= 1u << buf;
       }
-      // the record's slot is refilled only after the tensor cores have read it
-      if (threadIdx.x < 32) tc_commit_elect(&S.wbar);
       ok = tc_wait(&S.wbar, wph) && ok;
       wph ^= 1u;
+      ok = cbar_and(ok);
       if (!ok) break;
       if (ma + nmc == pm1 && s0 + nsc == ns) {
         // the pass is complete: its rows' norms, then the accumulators to the outputs
@@ -3555,6 +3626,11 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     mbar_init(&S.route_bar, 1);
     #pragma unroll 1
     for (int i = 0; i < kTcXBufs; ++i) mbar_init(&S.xbar[i], 1);
+    #pragma unroll 1
+    for (int i = 0; i < kTcReqs; ++i) {
+      mbar_init(&S.reqbar[i], kConsumerThreads);
+      mbar_init(&S.ackbar[i], 1);
+    }
     mbar_init(&S.wbar, 1);
     S.prod_count = 0;
     S.cons_count = 0xffffffffu;
@@ -3594,6 +3670,9 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
       Producer<Q8> prod(p, S);
       prod.run();
     }
+    if constexpr (TB == 4) {
+      if (p.tc && (tid >> 5) == (kConsumerThreads >> 5) + 1) tc_issuer(p, S);   // the next warp
+    }
     __syncwarp();
     asm volatile("bar.sync 12, 128;" ::: "memory");
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kLaunchRegs));
@@ -3602,6 +3681,9 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     {
       Consumer<TB, D, Q8> cons(p, S);
       cons.run();
+      if constexpr (TB == 4) {
+        if (p.tc) cons.tc_stop();
+      }
     }
     asm volatile("bar.sync %0, 128;" ::"r"(10 + (tid >> 7)) : "memory");
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kLaunchRegs));

@@ -88,6 +88,7 @@ constexpr int kTcMinBatch = 5;
 constexpr int kTcUnitBytes128 = 128 * 128;   // one 64-column slice of a 128-row M-block
 constexpr int kTcChunkBytes = 65536;          // A units of one ring record
 constexpr int kTcXBufs = 3;                   // input slices in flight (fewer when three terms do not fit)
+constexpr int kTcReqs = 4;                    // MMA requests in flight from the consumers to the issuing warp
 constexpr int kTcCols = 512;                  // tensor-memory columns (all of them: one block per SM)
 MK_HD int tc_mblock(int rows) { return rows <= 64 ? 64 : 128; }
 MK_HD int tc_batch_cols(int B) { return (B + 15) & ~15; }
