@@ -470,14 +470,16 @@ struct __align__(1024) Smem {
     uint32_t dstride, dunit;   // accumulator columns between M-blocks, between a block's units
     uint32_t dh, dlo; // high-term accumulator, first lower-term accumulator (columns from a unit's)
     uint32_t bp;      // N columns (and rows of an input term)
-    uint32_t flags;   // 1 accumulate high, 2 accumulate lower, 4 commit wbar, 8 stop, T << 4, (buffer + 1) << 8
+    uint32_t flags;   // 1 accumulate high, 2 accumulate lower, 4 release the ring record, 8 stop, T << 4,
+                      // (buffer + 1) << 8, 1 << 16 the pass's last request, ring slot << 20
     uint32_t pad_[3];
   };
   TcReq tcreq[kTcReqs];
   uint64_t reqbar[kTcReqs]; // consumers (all) -> issuer: request i is written and its slice staged
   uint64_t ackbar[kTcReqs]; // issuer -> consumers: request i has been read
   uint64_t xbar[kTcXBufs];  // tcgen05 tiles: the tensor cores have read input slice buffer i
-  uint64_t wbar;            // tcgen05 tiles: the tensor cores have read the current ring record
+  uint64_t wbar;            // tcgen05 tiles: the tensor cores have read the issuer's current record
+  uint64_t pbar;            // tcgen05 tiles: the current pass's MMAs have completed (issuer -> consumers)
   uint32_t tmem_base;       // tensor-memory address of this block's accumulators (wide batches)
 };
 
@@ -1329,6 +1331,7 @@ __device__ __noinline__ H8 load_h8(const Params& p, const uint64_t* src, uint32_
 // consumers post at the end of the step.
 __device__ void tc_issuer(const Params& p, Smem& S) {
   const int lane = threadIdx.x & 31;
+  uint32_t wph = 0;
   #pragma unroll 1
   for (uint32_t r = 0;; ++r) {
     const int slot = static_cast<int>(r % kTcReqs);
@@ -1374,7 +1377,25 @@ __device__ void tc_issuer(const Params& p, Smem& S) {
     }
     const uint32_t xb = (q.flags >> 8) & 15u;
     if (xb != 0u) tc_commit_elect(&S.xbar[xb - 1u]);
-    if (q.flags & 4u) tc_commit_elect(&S.wbar);
+    if (q.flags & 4u) {
+      // the ring record is released (for all consumer warps) once the tensor cores have read it;
+      // at the end of a pass, the consumers may then read the accumulators
+      tc_commit_elect(&S.wbar);
+      {
+        const uint64_t t0 = globaltimer();
+        #pragma unroll 1
+        for (uint32_t it = 1; !mbar_try_wait(&S.wbar, wph); ++it)
+          if ((it & 255u) == 0u && globaltimer() - t0 > p.watchdog_ns) break;
+        wph ^= 1u;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(&S.empty[q.flags >> 20])),
+                     "r"(static_cast<uint32_t>(kConsumerWarps))
+                     : "memory");
+        if (q.flags & (1u << 16)) mbar_arrive(&S.pbar);
+      }
+    }
   }
 }
 
@@ -1938,7 +1959,8 @@ struct Consumer {
 
   // ------------------------------------------------------------------ wide batches on tcgen05
   uint32_t xst = 0;   // per input buffer i: bit i a commit on xbar[i] not yet waited for, bit 4 + i its parity
-  uint32_t wph = 0;   // parity of the next wbar phase
+  uint32_t pph = 0;   // parity of the next pbar phase
+  bool tc_held = false;   // the last record was a tcgen05 record, released by the issuing warp
 
   // Post request rq (every consumer thread, after its share of the slice is staged and fenced):
   // thread 0 writes the fields once the issuer has read the slot's previous request; each thread's
@@ -2292,18 +2314,21 @@ struct Consumer {
         // record (its slot is refilled only after the tensor cores have read it)
         const bool last_use = ma + nmc == pm1;   // the slice's last record in this pass
         const int nu = gu ? 2 : 1;
+        const bool pass_end = last_use && sl == ns - 1;
         tc_post(wa + static_cast<uint32_t>(si * nmc * nu * MB * 128), smem_u32(xb0) + static_cast<uint32_t>(buf) * xsz,
                 S.tmem_base + static_cast<uint32_t>((ma - pm0) * NA * Bp), idesc, nmc, nu, MB * 128, NA * Bp, 2 * Bp,
                 (sl % KG) * Bp, KG * Bp, Bp,
                 (sl >= KG ? 1u : 0u) | (sl > 0 ? 2u : 0u) | (si + 1 == nsc ? 4u : 0u) | (static_cast<uint32_t>(T) << 4) |
-                    (last_use ? static_cast<uint32_t>(buf + 1) << 8 : 0u));
+                    (last_use ? static_cast<uint32_t>(buf + 1) << 8 : 0u) | (pass_end ? 1u << 16 : 0u) |
+                    (static_cast<uint32_t>(c % kSlots) << 20));
         if (last_use) xst |= 1u << buf;
       }
-      ok = tc_wait(&S.wbar, wph) && ok;
-      wph ^= 1u;
-      ok = cbar_and(ok);
-      if (!ok) break;
+      // (the issuing warp releases the record once the tensor cores have read it)
       if (ma + nmc == pm1 && s0 + nsc == ns) {
+        ok = tc_wait(&S.pbar, pph) && ok;   // the pass's MMAs have completed
+        pph ^= 1u;
+        ok = cbar_and(ok);
+        if (!ok) break;
         // the pass is complete: its rows' norms, then the accumulators to the outputs
         if (kind != 1) {
 #pragma unroll
@@ -2323,8 +2348,10 @@ struct Consumer {
         tc_fence_before();   // these reads precede the next pass's MMAs (behind the next barrier)
       }
       if (last) break;
-      if (!next_rec()) { ok = false; break; }
+      ++c;
+      if (!warp_wait_record(p, S, c)) { ok = false; wok = false; break; }
     }
+    tc_held = true;   // (run() must not release the tile's last record either)
     if (!ok) ll_timeout(p, op, l, tg);
     if (!cbar_and(wok && ok)) return false;
     if (op == MK_OP_HEAD && p.next_token != nullptr) head_top2(lo, hi);
@@ -3596,7 +3623,8 @@ struct Consumer {
       // after its last attention item the block merges its splits' partials; that needs no ring
       // slot, so the record is released first and the producer streams on meanwhile
       const bool merge = m0.kind == R_ATTN && static_cast<int>(m0.idx) == p.item_off[blockIdx.x + 1] - 1;
-      warp_release_record(S, c);
+      if (tc_held) tc_held = false;
+      else warp_release_record(S, c);
       ++c;
       if (merge && !attn_combine(m0.layer)) break;
       if (m0.kind == R_END) break;
@@ -3632,6 +3660,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
       mbar_init(&S.ackbar[i], 1);
     }
     mbar_init(&S.wbar, 1);
+    mbar_init(&S.pbar, 1);
     S.prod_count = 0;
     S.cons_count = 0xffffffffu;
     S.ykey = -1;
