@@ -1022,6 +1022,8 @@ int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t B, const int32_t* 
   const int F = cfg->expert_ffn, H = cfg->hidden, D = cfg->head_dim, Hq = cfg->num_q_heads, G = Hq / Hkv;
   const uint32_t nqkv = (uint32_t)(Hq + 2 * Hkv) * D;
   const int n_items = (int)items.size();
+  // wide batches run the dense tiles and the MoE on tcgen05 (the engine has the weight maps)
+  const bool tcs = cfg->max_batch >= mk::kTcMinBatch && B >= mk::kTcMinBatch;
   // per layer: active experts (ascending) and the gate/up unit range of every block
   std::vector<std::vector<int>> act(L), rows_of(L);   // active experts; rows routed to each expert
   std::vector<std::vector<int32_t>> gu_start(L);
@@ -1038,7 +1040,7 @@ int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t B, const int32_t* 
     for (int e = 0; e < E; ++e)
       if (cnt[e]) {
         act[l].push_back(e);
-        cost.push_back(mk::moe_unit_cost(cnt[e]));
+        cost.push_back(mk::moe_unit_cost(cnt[e], tcs));
         cum.push_back(cum.back() + (int64_t)F * cost.back());
       }
     const int nact = (int)act[l].size();
@@ -1071,7 +1073,8 @@ int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t B, const int32_t* 
   std::vector<int> xout_n(L + 1, 0);
   std::vector<std::vector<char>> qkv_done(L, std::vector<char>(n_ctas, 0));
   std::vector<std::vector<char>> item_done(L, std::vector<char>(std::max(1, n_items), 0));
-  std::vector<int> merged_n(L, 0), oproj_n(L, 0), router_n(L, 0), moe_share_n(L, 0);
+  std::vector<int> merged_n(L, 0), oproj_n(L, 0), router_n(L, 0), moe_share_n(L, 0), down_n(L, 0);
+  const int nrb = (H + mk::kTcDownRows - 1) / mk::kTcDownRows;   // tcgen05 down projection: row blocks
   std::vector<std::vector<char>> oproj_done(L, std::vector<char>(n_ctas, 0));
   std::vector<std::vector<char>> routed(n_ctas, std::vector<char>(L, 0));
   int writes_twice = 0;
@@ -1097,7 +1100,8 @@ int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t B, const int32_t* 
 
   // record kinds: a task op (ATTN: one per item), 110 = routing (every block), 100 = gate/up
   // chunk, 101 = down chunk; small-batch path: 105 = gate/up chunk, 102 = transposed down
-  // chunk, 104 = publish the partial output, 103 = reduce every block's partials
+  // chunk, 104 = publish the partial output, 103 = reduce every block's partials; tcgen05 path:
+  // 100 = a gate/up run, 106 = an (expert, row block) down unit, 107 = sum of own rows' slots
   struct Rec { int kind; int task; int layer; uint32_t a; uint32_t x; int flags; };
   enum { F_FIRST = 1, F_LAST = 2, F_LAST_GU = 4, F_EMPTY = 8 };
   struct Sm {
@@ -1137,6 +1141,23 @@ int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t B, const int32_t* 
       return r;
     }
     if (u0 >= u1) r.push_back({100, task, l, 0, 0, F_FIRST | F_LAST | F_LAST_GU | F_EMPTY});
+    if (tcs) {   // the device producer's tcgen05 loops (one record stands for a run's chunks)
+      for (int u = u0; u < u1;) {
+        const int a = u / F, f0 = u % F, fend = std::min(F, u1 - a * F);
+        for (int f = f0; f < fend; ++f) gu_seen[l][(size_t)a * F + f]++;
+        r.push_back({100, task, l, (uint32_t)a, (uint32_t)f0, F_FIRST | F_LAST | (a * F + fend >= u1 ? F_LAST_GU : 0)});
+        u = a * F + fend;
+      }
+      const int U = nact * nrb;
+      const int ua = (int)((int64_t)U * i / n_ctas), ub = (int)((int64_t)U * (i + 1) / n_ctas);
+      for (int u = ua; u < ub; ++u) {
+        const int a = u / nrb, rb = u % nrb;
+        for (int x = rb * mk::kTcDownRows; x < std::min(H, (rb + 1) * mk::kTcDownRows); ++x) dn_seen[l][(size_t)a * H + x]++;
+        r.push_back({106, task, l, (uint32_t)a, (uint32_t)rb, 0});
+      }
+      r.push_back({107, task, l, 0, hlo[i], hhi[i] > hlo[i] ? 0 : F_EMPTY});
+      return r;
+    }
     for (int u = u0; u < u1;) {
       const int a = u / F, f0 = u % F, fend = std::min(F, u1 - a * F);
       // batches of 3 or more: the run is streamed once per register group of its routed rows
@@ -1268,6 +1289,18 @@ int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t B, const int32_t* 
             (moe_share_n[l] < n_ctas || !orows_ready(l, hlo[i], hhi[i])))
           return false;
         if (!(r.flags & F_EMPTY) && (r.flags & F_LAST)) { mark(xout[l + 1][i]); xout_n[l + 1]++; }
+        break;
+      case 106:   // a tcgen05 down unit reads the SwiGLU outputs of its expert's pairs
+        if (moe_share_n[l] < n_ctas) return false;
+        down_n[l]++;
+        break;
+      case 107:   // the slots of the block's own rows: every down unit, and its own x rows
+        if (down_n[l] < (int)act[l].size() * nrb) return false;
+        if (!(r.flags & F_EMPTY)) {
+          if (!orows_ready(l, hlo[i], hhi[i])) return false;
+          mark(xout[l + 1][i]);
+          xout_n[l + 1]++;
+        }
         break;
       case 102:
       case 105:

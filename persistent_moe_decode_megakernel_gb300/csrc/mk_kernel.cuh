@@ -2584,7 +2584,7 @@ struct Consumer {
 #pragma unroll
       for (int k = 0; k < kMaxExperts / 32; ++k) {
         const int a = lane * (kMaxExperts / 32) + k;
-        const int32_t cst = a < nact ? moe_unit_cost(S.ecnt[S.eact[a]]) : 0;
+        const int32_t cst = a < nact ? moe_unit_cost(S.ecnt[S.eact[a]], p.tc != 0) : 0;
         if (a < nact) S.ecost[a] = cst;
         run += cst * p.F;
         loc[k] = run;

@@ -138,7 +138,9 @@ MK_HD int pages_per_chunk_q8(int page_size, int head_dim) {
 // bytes plus the batch rows it serves: max(4, rows routed to the expert), so at small
 // batch every unit weighs the same and at large batch crowded experts count for more.
 // Block j takes the units whose cost prefix starts in [C*j/N, C*(j+1)/N), C the total.
-MK_HD int32_t moe_unit_cost(int routed_rows) { return routed_rows > 4 ? routed_rows : 4; }
+// (On the tcgen05 path of wide batches the routed rows are the N columns of one MMA: a unit costs
+// its weight bytes whatever its rows, and the split is by FFN rows alone.)
+MK_HD int32_t moe_unit_cost(int routed_rows, bool tc) { return tc ? 1 : (routed_rows > 4 ? routed_rows : 4); }
 
 // first unit of block j of N; cum[a] = cost of the units of experts 0..a-1 (cum[nact] = C,
 // at most 256 experts x 1024 rows x 64 = 2^24), cost[a] = cost of one unit of expert a.

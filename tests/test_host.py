@@ -200,7 +200,9 @@ def test_simulated_moe_paths(B, flags):
 @pytest.mark.parametrize("B", [3, 7, 16])
 def test_simulated_wide_batches_hidden_4096(B):
     # at hidden 4096 a register group holds three rows (their staged inputs fill the scratch), so
-    # expert runs are streamed in ceil(rows / 3) passes; every unit is still covered once
+    # at B = 3 expert runs are streamed in ceil(rows / 3) passes; batches of 5 or more take the
+    # tcgen05 path (gate/up runs, (expert, row block) down units, the per-slot sum); every unit is
+    # still covered once
     m = W.scaled_model(W.MOE30B, hidden=4096, layers=2)
     cfg = mk.make_config(m, 16, 4000, 16, 200)
     rng = np.random.default_rng(B)
