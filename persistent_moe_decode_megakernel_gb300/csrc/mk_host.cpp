@@ -289,7 +289,8 @@ struct mk_ctx {
   uint8_t* ws = nullptr;
   // tagged 8-byte words (value | step tag << 32)
   uint64_t *X = nullptr, *QKV = nullptr, *ATT = nullptr, *PO = nullptr, *PML = nullptr, *RLOG = nullptr,
-           *HB = nullptr, *PT = nullptr, *YD = nullptr;
+           *HB = nullptr, *PT = nullptr, *YD = nullptr, *PSK = nullptr, *PSQ = nullptr;
+  int32_t psk_cap = 0;
   uint16_t* wdt = nullptr;   // transposed down projections [L][E][F][H] (small-batch MoE path), or null
   float* argp = nullptr;     // greedy selection: per-block (max, second, index) of its LM-head rows
   bool small_ok = false;
@@ -501,6 +502,33 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_ctx** out) {
               static_cast<const uint16_t*>(s.w_router), s.router_bias, static_cast<const uint16_t*>(s.w_gate_up),
               static_cast<const uint16_t*>(s.w_down), c->wdt ? c->wdt + dt_layer * l : nullptr};
   }
+  // split-K partials of the dense tcgen05 tiles: one block's group rows x max_batch words
+  {
+    int rows = 0;
+    const int nrt = c->plan.info.n_router_tiles, rr = mk::router_tile_rows(E, c->n_ctas, MB);
+    for (int op : {MK_OP_QKV, MK_OP_OPROJ, MK_OP_ROUTER}) {
+      const int ks = mk::tc_ksplit(op, c->n_ctas, nrt, op == MK_OP_QKV ? nqkv : H);
+      if (ks == 1) continue;
+      for (int g = 0; g + ks <= (op == MK_OP_ROUTER ? nrt : c->n_ctas); g += ks) {
+        uint32_t lo, hi, lo2, hi2;
+        if (op == MK_OP_ROUTER) {
+          lo = (uint32_t)(g * rr); hi = (uint32_t)std::min(E, (g + ks) * rr);
+        } else {
+          const uint32_t n = op == MK_OP_QKV ? (uint32_t)nqkv : (uint32_t)H;
+          split_range(n, c->n_ctas, g, &lo, &hi2);
+          split_range(n, c->n_ctas, g + ks - 1, &lo2, &hi);
+        }
+        rows = std::max(rows, (int)(hi - lo));
+      }
+      // a block's finalisation gathers the group's partials of its own rows into the scratch
+      const int own = op == MK_OP_ROUTER ? rr : ((op == MK_OP_QKV ? nqkv : H) + c->n_ctas - 1) / c->n_ctas;
+      if ((int64_t)ks * (own + 1) * MB > mk::kMoeScratch) {
+        free_ctx(c);
+        return fail(MK_ERR_UNSUPPORTED, "split-K partials of %d rows x %d exceed the scratch", own, MB);
+      }
+    }
+    c->psk_cap = rows * MB;
+  }
   // workspace
   struct Part { void** ptr; size_t bytes; };
   const size_t f4 = sizeof(float), i4 = sizeof(int32_t), w8 = sizeof(uint64_t);
@@ -514,6 +542,8 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_ctx** out) {
       {(void**)&c->HB, (size_t)L * MB * K * F * w8},
       {(void**)&c->PT, c->small_ok ? (size_t)L * c->n_ctas * mk::kSmallMaxB * H * w8 : 0},
       {(void**)&c->YD, MB >= mk::kTcMinBatch ? (size_t)L * MB * K * H * w8 : 0},
+      {(void**)&c->PSK, MB >= mk::kTcMinBatch ? (size_t)L * 3 * c->n_ctas * c->psk_cap * w8 : 0},
+      {(void**)&c->PSQ, MB >= mk::kTcMinBatch ? (size_t)L * 3 * c->n_ctas * MB * w8 : 0},
       {(void**)&c->RIDS, (size_t)L * MB * K * i4},
       {(void**)&c->argp, (size_t)c->n_ctas * MB * 4 * f4},
       {(void**)&c->RW, (size_t)L * MB * K * f4},
@@ -703,7 +733,7 @@ static int make_params(mk_ctx* c, mk::Params& p, int32_t batch, const uint8_t* d
   p.item_off = reinterpret_cast<const int32_t*>(d + c->off_item_off);
   p.pair_first = reinterpret_cast<const int32_t*>(d + c->off_pair);
   p.X = c->X; p.QKV = c->QKV; p.ATT = c->ATT; p.PO = c->PO; p.PML = c->PML; p.RLOG = c->RLOG; p.RIDS = c->RIDS;
-  p.RW = c->RW; p.HB = c->HB; p.YD = c->YD;
+  p.RW = c->RW; p.HB = c->HB; p.YD = c->YD; p.PSK = c->PSK; p.PSQ = c->PSQ; p.psk_cap = c->psk_cap;
   p.small_moe = c->small_ok && mk::small_moe_batch(batch, cf.hidden) ? 1 : 0;
   p.PT = c->PT;
   p.next_token = next_token; p.margin = margin; p.argp = c->argp;

@@ -645,6 +645,21 @@ __device__ __forceinline__ bool group_bar_and(bool v, int nw) {
   return r != 0;
 }
 
+// --------------------------------------------------------------------------- tcgen05 split-K
+// The rows of this block's split-K group (KS consecutive blocks) of a dense tile kind.
+__device__ __forceinline__ void tc_group_rows(const Params& p, int op, int KS, uint32_t& glo, uint32_t& ghi) {
+  const int g0 = (static_cast<int>(blockIdx.x) / KS) * KS, g1 = g0 + KS;
+  if (op == MK_OP_ROUTER) {
+    const int rr = router_tile_rows(p.E, p.n_ctas, p.max_batch);
+    glo = static_cast<uint32_t>(g0 * rr);
+    ghi = static_cast<uint32_t>(min(p.E, g1 * rr));
+  } else {
+    const uint64_t n = op == MK_OP_QKV ? static_cast<uint64_t>(p.nqkv) : static_cast<uint64_t>(p.H);
+    glo = static_cast<uint32_t>(n * g0 / p.n_ctas);
+    ghi = static_cast<uint32_t>(n * g1 / p.n_ctas);
+  }
+}
+
 // --------------------------------------------------------------------------- producer
 // Q8: the KV pool holds q8_0 blocks (codes and scales) instead of bf16 values.
 template <bool Q8>
@@ -798,18 +813,19 @@ struct Producer {
   // Meta: row0 the first M-block, n the M-blocks, aux the first slice | slices << 16, pad[2] the
   // pass's M-blocks (first | end << 16), pad[4] the N columns the passes were sized for.
   __device__ bool tc_emit(const mk_task& t, uint32_t ti, uint8_t op, const uint64_t* map, int K, int R, int y0, int y1,
-                          int nu, int accs, int ncols, uint32_t e, uint32_t idx, uint32_t aux_flag) {
+                          int nu, int accs, int ncols, uint32_t e, uint32_t idx, uint32_t aux_flag, int s_lo = 0,
+                          int s_hi = -1, uint32_t own_lo = 0, uint32_t own_hi = 0) {
     const int MB = tc_mblock(R), nmb = (R + MB - 1) / MB;
     const int pmb = min(nmb, kTcCols / (accs * ncols));
     const int upc = kTcChunkBytes / (nu * MB * 128);   // (slice, M-block) pairs per record
-    const int ns = (K + 63) / 64;
+    const int ns = s_hi < 0 ? (K + 63) / 64 : s_hi;     // (the end of this block's slices)
     #pragma unroll 1
     for (int m0 = 0; m0 < nmb; m0 += pmb) {
       const int m1 = min(nmb, m0 + pmb), nm = m1 - m0;
       const int mg = nm < upc ? nm : upc;
       const int nsc = nm < upc ? upc / nm : 1;
       #pragma unroll 1
-      for (int s0 = 0; s0 < ns; s0 += nsc) {
+      for (int s0 = s_lo; s0 < ns; s0 += nsc) {
         const int s1 = min(ns, s0 + nsc);
         #pragma unroll 1
         for (int ma = m0; ma < m1; ma += mg) {
@@ -817,7 +833,7 @@ struct Producer {
           if (!acquire()) return false;
           Meta& m = meta();
           m.kind = R_TC; m.op = op;
-          m.first = (m0 == 0 && s0 == 0 && ma == m0); m.last = (m1 == nmb && s1 == ns && mb1 == m1);
+          m.first = (m0 == 0 && s0 == s_lo && ma == m0); m.last = (m1 == nmb && s1 == ns && mb1 == m1);
           m.layer = t.layer; m.n = static_cast<uint16_t>(mb1 - ma); m.row0 = static_cast<uint32_t>(ma);
           m.idx = idx; m.e = e;
           m.aux = static_cast<uint32_t>(s0) | (static_cast<uint32_t>(s1 - s0) << 16);
@@ -825,6 +841,9 @@ struct Producer {
           m.pad[2] = static_cast<uint32_t>(m0) | (static_cast<uint32_t>(m1) << 16);
           m.pad[3] = aux_flag;
           m.pad[4] = static_cast<uint32_t>(ncols);
+          m.pad[5] = own_lo;
+          m.pad[6] = static_cast<uint32_t>(s_lo) | (static_cast<uint32_t>(ns) << 16);
+          m.pad[7] = own_hi;
           uint32_t bytes = 0;
           #pragma unroll 1
           for (int mm = ma; mm < mb1; ++mm) bytes += static_cast<uint32_t>((min(MB, R - mm * MB) + 15) / 16) * 2048u;
@@ -854,8 +873,19 @@ struct Producer {
   __device__ bool tc_tile(const mk_task& t, uint32_t ti) {
     const int K = t.op == MK_OP_OPROJ ? p.Hq * p.D : p.H;
     const uint64_t* map = p.wmaps + static_cast<size_t>(tc_map_index(t.op, t.layer, p.L)) * 16;
-    return tc_emit(t, ti, static_cast<uint8_t>(t.op), map, K, static_cast<int>(t.hi - t.lo), static_cast<int>(t.lo), 0, 1,
-                   tc_accs(t.op, p.B, K), tc_batch_cols(p.B), 0u, ti, 0u);
+    const int KS = tc_ksplit(t.op, p.n_ctas, p.n_router_tiles, t.op == MK_OP_QKV ? p.nqkv : p.H);
+    const int ns = (K + 63) / 64;
+    mk_task tt = t;
+    int s_lo = 0, s_hi = ns;
+    if (KS > 1) {   // the group's rows, this block's share of K
+      tc_group_rows(p, t.op, KS, tt.lo, tt.hi);
+      const int q = static_cast<int>(blockIdx.x) % KS;
+      s_lo = q * ns / KS;
+      s_hi = (q + 1) * ns / KS;
+    }
+    return tc_emit(tt, ti, static_cast<uint8_t>(t.op), map, K, static_cast<int>(tt.hi - tt.lo), static_cast<int>(tt.lo), 0,
+                   1, tc_accs(t.op, p.B, K), tc_batch_cols(p.B), 0u, ti, static_cast<uint32_t>(KS), s_lo, s_hi, t.lo,
+                   t.hi);
   }
 
   // KV pages of this block's attention items: per page, K then V, each as D/64 boxes of
@@ -2096,13 +2126,118 @@ struct Consumer {
     return ok;
   }
 
+  // The fp32 sum of one M-block's accumulators for 8 columns of this warp's lanes: the lower
+  // terms (lowest first), then the nhg high-term accumulators that received a slice
+  __device__ __forceinline__ void tc_sum_accs(uint32_t ta, int Bp, int T, int KG, int nhg, float (&v)[8]) {
+    tc_ld8(ta + (KG + T - 2) * Bp, v);
+    #pragma unroll 1
+    for (int a = KG + T - 3; a >= KG; --a) {
+      float w[8];
+      tc_ld8(ta + a * Bp, w);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] += w[j];
+    }
+    #pragma unroll 1
+    for (int a = nhg - 1; a >= 0; --a) {
+      float w[8];
+      tc_ld8(ta + a * Bp, w);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] += w[j];
+    }
+  }
+
+  // Split-K: this block's partial sums of the group's rows (its share of K, no norm) to
+  // PSK[l][op][block][row][b], and its share of each input row's sum of squares to PSQ.
+  __device__ __forceinline__ void tc_epilogue_split(int op, int l, int R, int MB, int m0, int m1, int Bp, int T, int KG,
+                                                    int nhg, const float (&ss)[2]) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int q = warp & 3, hh = warp >> 2;
+    const int half = Bp >> 1;
+    const int r_in = MB == 128 ? 32 * q + lane : 16 * q + lane;
+    const bool lane_ok = MB == 128 || lane < 16;
+    const int B = p.B;
+    const size_t blk = (static_cast<size_t>(l) * 3 + tc_split_slot(op)) * p.n_ctas + blockIdx.x;
+    uint64_t* dst = p.PSK + blk * p.psk_cap;
+    #pragma unroll 1
+    for (int m = m0; m < m1; ++m) {
+      const int row = m * MB + r_in;
+      const uint32_t ta = S.tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
+                          static_cast<uint32_t>((m - m0) * (KG + T - 1) * Bp + hh * half);
+      #pragma unroll 1
+      for (int c8 = 0; c8 < half; c8 += 8) {
+        float v[8];
+        tc_sum_accs(ta + c8, Bp, T, KG, nhg, v);
+        if (lane_ok && row < R) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int b = hh * half + c8 + j;
+            if (b < B) ll_st(dst + static_cast<size_t>(row) * B + b, v[j], tg);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float v = ss[h];
+      v += __shfl_xor_sync(0xffffffffu, v, 1);
+      v += __shfl_xor_sync(0xffffffffu, v, 2);
+      v += __shfl_xor_sync(0xffffffffu, v, 4);
+      const int b = (threadIdx.x >> 3) + 32 * h;
+      if ((threadIdx.x & 7) == 0 && b < B) ll_st(p.PSQ + blk * p.max_batch + b, v, tg);
+    }
+  }
+
+  // Split-K: this block's own rows [own_lo, own_hi) from the KS partials of its group (in block
+  // order) and, for normalised inputs, 1/rms from the group's sums of squares; then the tile's
+  // epilogue (residual, bias, tagged outputs).
+  __device__ __forceinline__ bool tc_finalize(int op, int l, bool norm, int K, int KS, uint32_t glo, uint32_t own_lo,
+                                              uint32_t own_hi) {
+    const int B = p.B;
+    const int nown = static_cast<int>(own_hi - own_lo), roff = static_cast<int>(own_lo - glo);
+    if (nown <= 0) return true;
+    const int g0 = (static_cast<int>(blockIdx.x) / KS) * KS;
+    const size_t blk0 = (static_cast<size_t>(l) * 3 + tc_split_slot(op)) * p.n_ctas + g0;
+    const uint64_t* psk = p.PSK + blk0 * p.psk_cap;
+    const uint64_t* psq = p.PSQ + blk0 * p.max_batch;
+    const int per = nown * B;             // one block's words for these rows
+    float* Y = S.moe;                     // [KS][nown][B], then [KS][B]
+    const int cap = p.psk_cap;
+    const int maxb = p.max_batch;
+    const FastDiv dper(per), dB(B);
+    bool ok = ll_gather(p, KS * per + KS * B, [=](int i) -> const uint64_t* {
+      if (i < KS * per) {
+        const int q = dper.div(i), r = i - q * per;
+        return psk + static_cast<size_t>(q) * cap + static_cast<size_t>(roff) * B + r;
+      }
+      const int j = i - KS * per, q = dB.div(j);
+      return psq + static_cast<size_t>(q) * maxb + (j - q * B);
+    }, Y, tg);
+    if (!cbar_and(ok)) return false;
+    const OutMap om = out_map(op, l);
+    #pragma unroll 1
+    for (int i = threadIdx.x; i < per; i += kConsumerThreads) {
+      const int r = i / B, b = i - r * B;
+      float d = 0.f;
+      #pragma unroll 1
+      for (int q = 0; q < KS; ++q) d += Y[q * per + i];
+      if (norm) {
+        float t = 0.f;
+        #pragma unroll 1
+        for (int q = 0; q < KS; ++q) t += Y[KS * per + q * B + b];
+        d *= 1.0f / sqrtf(t / static_cast<float>(K) + p.eps);
+      }
+      put(om, false, own_lo + r, b, 0, d, 0.f);
+    }
+    return true;
+  }
+
   // Accumulators of M-blocks [m0, m1) of the pass to the outputs: per M-block KG accumulators of
   // the high term and one per lower term, summed here in fp32 (low terms first).  Warp w reads
   // tensor-memory lanes
   // 32(w % 4) .. + 31 (M = 128: row = lane; M = 64: rows 16(w % 4) + lane for lanes < 16) and
   // half w / 4 of the batch columns.
   __device__ __forceinline__ void tc_epilogue(const OutMap& om, bool norm, uint32_t lo, int R, int MB, int m0, int m1,
-                                              int Bp, int T, int KG, int nrows, bool gu) {
+                                              int Bp, int T, int KG, int nhg, int nrows, bool gu) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = warp & 3, hh = warp >> 2;
     const int half = Bp >> 1;
@@ -2138,17 +2273,8 @@ struct Consumer {
           }
           continue;
         }
-        float v[8], v1[8];
-        tc_ld8(ta + (KG + T - 2) * Bp + c8, v1);   // the lowest term
-        #pragma unroll 1
-        for (int a = KG + T - 3; a >= 0; --a) {     // the other terms, then the high term's groups
-          float v2[8];
-          tc_ld8(ta + a * Bp + c8, v2);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) v1[j] += v2[j];
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = v1[j];
+        float v[8];
+        tc_sum_accs(ta + c8, Bp, T, KG, nhg, v);
         if (lane_ok && row < R) {
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
@@ -2256,7 +2382,12 @@ struct Consumer {
     const int NA = gu ? 4 : KG + T - 1;
     // the N columns the producer sized the passes for (the routing both sides computed agrees;
     // the check keeps every accumulator address inside the allocation regardless)
-    const int Bp = static_cast<int>(meta().pad[4]), MB = tc_mblock(R), ns = (K + 63) / 64;
+    const int Bp = static_cast<int>(meta().pad[4]), MB = tc_mblock(R);
+    // this block's slices of K [s_lo, ns) (split-K groups: a share; KS > 1 only for dense tiles)
+    const int s_lo = static_cast<int>(meta().pad[6] & 0xffffu), ns = static_cast<int>(meta().pad[6] >> 16);
+    const int KS = (gu || dn) ? 1 : static_cast<int>(meta().pad[3]);
+    const uint32_t own_lo = meta().pad[5], own_hi = meta().pad[7];
+    const int nhg = min(KG, ns - s_lo);   // high-term accumulators that receive a slice
     if (Bp != tc_batch_cols(nrows)) {
       if (threadIdx.x == 0)
         record_error(p, MK_ERR_DEVICE_BOUNDS, op, l, 0u, static_cast<uint32_t>(nrows), 0, Bp, true);
@@ -2315,10 +2446,11 @@ struct Consumer {
         const bool last_use = ma + nmc == pm1;   // the slice's last record in this pass
         const int nu = gu ? 2 : 1;
         const bool pass_end = last_use && sl == ns - 1;
+        const int rs = sl - s_lo;   // the slice's place in this block's share
         tc_post(wa + static_cast<uint32_t>(si * nmc * nu * MB * 128), smem_u32(xb0) + static_cast<uint32_t>(buf) * xsz,
                 S.tmem_base + static_cast<uint32_t>((ma - pm0) * NA * Bp), idesc, nmc, nu, MB * 128, NA * Bp, 2 * Bp,
-                (sl % KG) * Bp, KG * Bp, Bp,
-                (sl >= KG ? 1u : 0u) | (sl > 0 ? 2u : 0u) | (si + 1 == nsc ? 4u : 0u) | (static_cast<uint32_t>(T) << 4) |
+                (rs % KG) * Bp, KG * Bp, Bp,
+                (rs >= KG ? 1u : 0u) | (rs > 0 ? 2u : 0u) | (si + 1 == nsc ? 4u : 0u) | (static_cast<uint32_t>(T) << 4) |
                     (last_use ? static_cast<uint32_t>(buf + 1) << 8 : 0u) | (pass_end ? 1u << 16 : 0u) |
                     (static_cast<uint32_t>(c % kSlots) << 20));
         if (last_use) xst |= 1u << buf;
@@ -2344,7 +2476,15 @@ struct Consumer {
         cbar();
         tc_fence_after();
         if (dn) tc_epilogue_down(l, lo, R, MB, pm0, pm1, Bp, nrows);
-        else tc_epilogue(out_map(gu ? int(R_OP_GU) : op, l), kind != 1, lo, R, MB, pm0, pm1, Bp, T, KG, nrows, gu);
+        else if (KS > 1) {
+          // split-K: publish this block's partials (and sums of squares), then finalise its own
+          // rows from the group's
+          tc_epilogue_split(op, l, R, MB, pm0, pm1, Bp, T, KG, nhg, ss);
+          tc_fence_before();
+          ok = tc_finalize(op, l, kind != 1, K, KS, lo, own_lo, own_hi) && ok;
+        } else {
+          tc_epilogue(out_map(gu ? int(R_OP_GU) : op, l), kind != 1, lo, R, MB, pm0, pm1, Bp, T, KG, nhg, nrows, gu);
+        }
         tc_fence_before();   // these reads precede the next pass's MMAs (behind the next barrier)
       }
       if (last) break;

@@ -108,6 +108,19 @@ MK_HD int tc_hi_groups(int op, int B, int K) {
   return g > 1 ? g : 1;
 }
 MK_HD int tc_accs(int op, int B, int K) { return tc_hi_groups(op, B, K) + tc_terms(op) - 1; }
+// Split-K of the dense tcgen05 tiles: every block reads its tile's whole input from L2, so the
+// QKV projection (2), the O-proj and the router (4) run in groups of consecutive blocks that
+// share the group's rows, each over a 1/KS share of K; each block publishes its partial sums and
+// sums of squares, then finalises its own rows from the group's partials in block order.  Only
+// where the groups tile the blocks (and the router tiles) evenly and every block holds rows (rows:
+// the QKV width for the QKV projection, the hidden size for the O-proj).
+MK_HD int tc_ksplit(int op, int n_ctas, int n_router_tiles, int rows) {
+  const int ks = op == MK_OP_QKV ? 2 : (op == MK_OP_OPROJ || op == MK_OP_ROUTER) ? 4 : 1;
+  if (ks == 1 || n_ctas % ks != 0 || (op == MK_OP_ROUTER && n_router_tiles % ks != 0)) return 1;
+  if (op != MK_OP_ROUTER && rows < n_ctas) return 1;
+  return ks;
+}
+MK_HD int tc_split_slot(int op) { return op == MK_OP_QKV ? 0 : op == MK_OP_OPROJ ? 1 : 2; }
 // the tile kind of the experts' down projections (a record op beside the MK_OP_* of mk_debug.h)
 constexpr int kTcOpDown = 16;
 // hidden rows per down-projection unit (one 128-row M-block of one expert)
@@ -231,6 +244,9 @@ struct alignas(64) Params {
   uint64_t* RLOG;  // [L][max_batch][E] router logits (+ bias)
   uint64_t* HB;    // [L][max_batch][K][F] SwiGLU activations per (row, slot)
   uint64_t* YD;    // [L][max_batch][K][H] weighted down-projection output per (row, slot) (wide batches)
+  uint64_t* PSK;   // [L][3][n_ctas][psk_cap] split-K partial sums of the QKV, O-proj, router tiles (wide)
+  uint64_t* PSQ;   // [L][3][n_ctas][max_batch] their blocks' partial sums of squares of the input rows
+  int32_t psk_cap; // words of one block's partial: its group's rows x max_batch
   int32_t small_moe;    // this step runs the small-batch MoE path
   uint64_t* PT;         // [L][n_ctas][kSmallMaxB][H] per-block partial MoE outputs (small-batch path)
   int32_t* next_token;  // greedy selection: [B] argmax of the logits, or null (not requested)
