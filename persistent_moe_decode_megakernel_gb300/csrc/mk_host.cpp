@@ -507,7 +507,7 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_ctx** out) {
     int rows = 0;
     const int nrt = c->plan.info.n_router_tiles, rr = mk::router_tile_rows(E, c->n_ctas, MB);
     for (int op : {MK_OP_QKV, MK_OP_OPROJ, MK_OP_ROUTER}) {
-      const int ks = mk::tc_ksplit(op, c->n_ctas, nrt, op == MK_OP_QKV ? nqkv : H);
+      const int ks = mk::tc_ksplit(op, c->n_ctas, nrt, op == MK_OP_QKV ? nqkv : H, op == MK_OP_OPROJ ? Hq * D : H);
       if (ks == 1) continue;
       for (int g = 0; g + ks <= (op == MK_OP_ROUTER ? nrt : c->n_ctas); g += ks) {
         uint32_t lo, hi, lo2, hi2;

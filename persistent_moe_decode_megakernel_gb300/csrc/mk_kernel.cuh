@@ -873,7 +873,7 @@ struct Producer {
   __device__ bool tc_tile(const mk_task& t, uint32_t ti) {
     const int K = t.op == MK_OP_OPROJ ? p.Hq * p.D : p.H;
     const uint64_t* map = p.wmaps + static_cast<size_t>(tc_map_index(t.op, t.layer, p.L)) * 16;
-    const int KS = tc_ksplit(t.op, p.n_ctas, p.n_router_tiles, t.op == MK_OP_QKV ? p.nqkv : p.H);
+    const int KS = tc_ksplit(t.op, p.n_ctas, p.n_router_tiles, t.op == MK_OP_QKV ? p.nqkv : p.H, K);
     const int ns = (K + 63) / 64;
     mk_task tt = t;
     int s_lo = 0, s_hi = ns;

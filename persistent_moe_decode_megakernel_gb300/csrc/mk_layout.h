@@ -109,15 +109,18 @@ MK_HD int tc_hi_groups(int op, int B, int K) {
 }
 MK_HD int tc_accs(int op, int B, int K) { return tc_hi_groups(op, B, K) + tc_terms(op) - 1; }
 // Split-K of the dense tcgen05 tiles: every block reads its tile's whole input from L2, so the
-// QKV projection (2), the O-proj and the router (4) run in groups of consecutive blocks that
+// QKV projection (2), the O-proj and the router (8) run in groups of consecutive blocks that
 // share the group's rows, each over a 1/KS share of K; each block publishes its partial sums and
 // sums of squares, then finalises its own rows from the group's partials in block order.  Only
-// where the groups tile the blocks (and the router tiles) evenly and every block holds rows (rows:
-// the QKV width for the QKV projection, the hidden size for the O-proj).
-MK_HD int tc_ksplit(int op, int n_ctas, int n_router_tiles, int rows) {
-  const int ks = op == MK_OP_QKV ? 2 : (op == MK_OP_OPROJ || op == MK_OP_ROUTER) ? 4 : 1;
+// where the groups tile the blocks (and the router tiles) evenly, every block holds rows (rows:
+// the QKV width for the QKV projection, the hidden size for the O-proj) and every block gets at
+// least one 64-column slice of K.  (QKV stays at 2: a group of 4 would hold two 128-row M-blocks,
+// and its accumulators would not fit the tensor memory in one pass.)
+MK_HD int tc_ksplit(int op, int n_ctas, int n_router_tiles, int rows, int K) {
+  const int ks = op == MK_OP_QKV ? 2 : (op == MK_OP_OPROJ || op == MK_OP_ROUTER) ? 8 : 1;
   if (ks == 1 || n_ctas % ks != 0 || (op == MK_OP_ROUTER && n_router_tiles % ks != 0)) return 1;
   if (op != MK_OP_ROUTER && rows < n_ctas) return 1;
+  if ((K + 63) / 64 < ks) return 1;
   return ks;
 }
 MK_HD int tc_split_slot(int op) { return op == MK_OP_QKV ? 0 : op == MK_OP_OPROJ ? 1 : 2; }
