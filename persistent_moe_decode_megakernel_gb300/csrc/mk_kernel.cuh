@@ -888,6 +888,24 @@ struct Producer {
                    t.hi);
   }
 
+  // Up to kIdBatch page ids of a chunk, read with independent loads (the block table is not
+  // written during a step), so that their latencies overlap instead of adding up per page.
+  static constexpr int kIdBatch = 8;
+  __device__ __forceinline__ void page_ids(const int32_t* src, uint32_t n, int32_t (&ids)[kIdBatch]) const {
+    #pragma unroll
+    for (int j = 0; j < kIdBatch; ++j) ids[j] = static_cast<uint32_t>(j) < n ? __ldg(src + j) : 0;
+  }
+  // a page id outside the pool is recorded and replaced by page 0, which keeps the slot's byte
+  // count; the step's result is then flagged invalid
+  __device__ __forceinline__ int32_t checked_page(int32_t page, int layer, uint32_t pos) const {
+    if (page < 0 || page >= p.P) {
+      record_error(p, MK_ERR_DEVICE_BOUNDS, MK_OP_ATTN, layer, 0u, static_cast<uint32_t>(page), 0,
+                   static_cast<int>(pos), false);
+      return 0;
+    }
+    return page;
+  }
+
   // KV pages of this block's attention items: per page, K then V, each as D/64 boxes of
   // [page_size rows][64 dims] (128-byte swizzle).  Within a slot, K occupies the first half
   // and V the second; each holds [dim half][rows][64 dims], page i at rows i*page_size.
@@ -905,6 +923,8 @@ struct Producer {
       #pragma unroll 1
       for (uint32_t pg = item.page_lo; pg < item.page_hi; pg += ppc) {
         const uint32_t n = min(static_cast<uint32_t>(ppc), item.page_hi - pg);
+        int32_t ids[kIdBatch];
+        page_ids(btrow + pg, n, ids);   // in flight across the slot wait
         if (!acquire()) return false;
         Meta& m = meta();
         m.kind = R_ATTN; m.op = MK_OP_ATTN; m.first = (pg == item.page_lo); m.last = (pg + n >= item.page_hi);
@@ -913,20 +933,21 @@ struct Producer {
         mbar_arrive_expect_tx(full(), 2u * halves * n * box);
         uint8_t* dst = slot();
         #pragma unroll 1
-        for (uint32_t i = 0; i < n; ++i) {
-          int32_t page = btrow[pg + i];
-          if (page < 0 || page >= p.P) {
-            record_error(p, MK_ERR_DEVICE_BOUNDS, MK_OP_ATTN, t.layer, 0u, static_cast<uint32_t>(page), 0,
-                         static_cast<int>(pg + i), false);
-            page = 0;  // keep the byte count of the slot; the result is flagged invalid
-          }
-          const int rowk = (((t.layer * p.P + page) * 2) * p.Hkv + item.kvh) * p.ps;
-          const int rowv = rowk + p.Hkv * p.ps;
-          #pragma unroll 1
-          for (int h = 0; h < halves; ++h) {
-            uint8_t* kd = dst + h * rows_cap * 128 + i * box;
-            tma_load_2d(kd, p.kv_map, 64 * h, rowk, full(), pol);
-            tma_load_2d(kd + kSlotBytes / 2, p.kv_map, 64 * h, rowv, full(), pol);
+        for (uint32_t i0 = 0; i0 < n; i0 += kIdBatch) {
+          if (i0 > 0) page_ids(btrow + pg + i0, n - i0, ids);
+          #pragma unroll
+          for (int j = 0; j < kIdBatch; ++j) {
+            const uint32_t i = i0 + j;
+            if (i >= n) break;
+            const int32_t page = checked_page(ids[j], t.layer, pg + i);
+            const int rowk = (((t.layer * p.P + page) * 2) * p.Hkv + item.kvh) * p.ps;
+            const int rowv = rowk + p.Hkv * p.ps;
+            #pragma unroll 1
+            for (int h = 0; h < halves; ++h) {
+              uint8_t* kd = dst + h * rows_cap * 128 + i * box;
+              tma_load_2d(kd, p.kv_map, 64 * h, rowk, full(), pol);
+              tma_load_2d(kd + kSlotBytes / 2, p.kv_map, 64 * h, rowv, full(), pol);
+            }
           }
         }
         ++c;
@@ -955,6 +976,8 @@ struct Producer {
 #pragma unroll 1
       for (uint32_t pg = item.page_lo; pg < item.page_hi; pg += ppc) {
         const uint32_t n = min(static_cast<uint32_t>(ppc), item.page_hi - pg);
+        int32_t ids[kIdBatch];
+        page_ids(btrow + pg, n, ids);   // in flight across the slot wait
         if (!acquire()) return false;
         Meta& m = meta();
         m.kind = R_ATTN; m.op = MK_OP_ATTN; m.first = (pg == item.page_lo); m.last = (pg + n >= item.page_hi);
@@ -962,21 +985,22 @@ struct Producer {
         m.e = 0; m.aux = 0; m.lo = item.page_lo; m.hi = item.page_hi;
         mbar_arrive_expect_tx(full(), 2u * n * (cbox + sbox));
         uint8_t* dst = slot();
+        uint8_t* sd = dst + static_cast<size_t>(2 * rows_cap) * p.D;
 #pragma unroll 1
-        for (uint32_t i = 0; i < n; ++i) {
-          int32_t page = btrow[pg + i];
-          if (page < 0 || page >= p.P) {
-            record_error(p, MK_ERR_DEVICE_BOUNDS, MK_OP_ATTN, t.layer, 0u, static_cast<uint32_t>(page), 0,
-                         static_cast<int>(pg + i), false);
-            page = 0;  // keep the byte count of the slot; the result is flagged invalid
+        for (uint32_t i0 = 0; i0 < n; i0 += kIdBatch) {
+          if (i0 > 0) page_ids(btrow + pg + i0, n - i0, ids);
+#pragma unroll
+          for (int j = 0; j < kIdBatch; ++j) {
+            const uint32_t i = i0 + j;
+            if (i >= n) break;
+            const int32_t page = checked_page(ids[j], t.layer, pg + i);
+            const int rowk = ((page * 2) * p.Hkv + item.kvh) * p.ps;   // row of the layer's code plane
+            const int rowv = rowk + p.Hkv * p.ps;
+            tma_load_3d(dst + i * cbox, p.kv_map, 0, rowk, t.layer, full(), pol);
+            tma_load_3d(dst + static_cast<size_t>(rows_cap) * p.D + i * cbox, p.kv_map, 0, rowv, t.layer, full(), pol);
+            bulk_g2s(sd + i * sbox, sbase + static_cast<size_t>(rowk) * srow, sbox, full(), pol);
+            bulk_g2s(sd + rows_cap * srow + i * sbox, sbase + static_cast<size_t>(rowv) * srow, sbox, full(), pol);
           }
-          const int rowk = ((page * 2) * p.Hkv + item.kvh) * p.ps;   // row of the layer's code plane
-          const int rowv = rowk + p.Hkv * p.ps;
-          tma_load_3d(dst + i * cbox, p.kv_map, 0, rowk, t.layer, full(), pol);
-          tma_load_3d(dst + static_cast<size_t>(rows_cap) * p.D + i * cbox, p.kv_map, 0, rowv, t.layer, full(), pol);
-          uint8_t* sd = dst + static_cast<size_t>(2 * rows_cap) * p.D;
-          bulk_g2s(sd + i * sbox, sbase + static_cast<size_t>(rowk) * srow, sbox, full(), pol);
-          bulk_g2s(sd + rows_cap * srow + i * sbox, sbase + static_cast<size_t>(rowv) * srow, sbox, full(), pol);
         }
         ++c;
       }
