@@ -95,6 +95,8 @@ int check_config(const mk_config* c) {
   if (c->top_k > mk::kMaxTopK) return fail(MK_ERR_UNSUPPORTED, "top_k > 8");
   if (c->page_size * c->head_dim * 2 > mk::kSlotBytes / 2)
     return fail(MK_ERR_UNSUPPORTED, "page_size*head_dim*2 > %d", mk::kSlotBytes / 2);
+  if (!(c->flags & MK_FLAG_KV_Q8) && mk::pages_per_chunk(c->page_size, c->head_dim) < 1)
+    return fail(MK_ERR_UNSUPPORTED, "page_size %d: no whole 16-row tiles of KV pages fit one ring slot", c->page_size);
   if (c->page_size % 8) return fail(MK_ERR_UNSUPPORTED, "page_size must be a multiple of 8");
   if ((c->flags & MK_FLAG_KV_Q8) && c->head_dim != 128)
     return fail(MK_ERR_UNSUPPORTED, "the q8_0 KV cache needs head_dim 128");
@@ -334,10 +336,15 @@ size_t kv_q8_code_bytes(const mk_config& cf) {
 }
 size_t kv_q8_layer_bytes(const mk_config& cf) { return kv_q8_code_bytes(cf) / 16 * 17; }
 
-// Describe the KV pool to TMA: the bf16 pool [L][P][2][Hkv][ps][D] as 2-D rows of D elements
-// (boxes of 64 elements x page_size rows); the q8_0 pool's code planes as 3-D [layer][row][D
-// bytes], rows of one layer contiguous, layers layer_bytes apart (boxes of D bytes x page_size
-// rows).  Both with the 128-byte swizzle.
+// Describe the KV pool to TMA: the bf16 pool [L][P][2][Hkv][ps][D] as 4-D (innermost first)
+// {64 dims, Hkv*ps positions, D/64 dim halves, L*P*2 K/V blocks}, positions 2*D bytes apart and
+// dim halves 128, so that one box {64, ps, D/64, 2} at position kvh*ps is the K and the V of
+// one page and KV head, landing as [K, V][dim half][position][64 dims]: the 8 consecutive
+// positions an ldmatrix reads sit on 8 distinct swizzle phases.  (One box per page: a 4-D box
+// costs the producer about what one 2-D box does, a 5-D box several times more.)  The q8_0
+// pool's code planes as 3-D [layer][row][D bytes],
+// rows of one layer contiguous, layers layer_bytes apart (boxes of D bytes x page_size rows).
+// Both with the 128-byte swizzle.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
@@ -365,12 +372,13 @@ int encode_kv_map(const mk_config& cf, void* kv, CUtensorMap* out) {
     if (r != CUDA_SUCCESS) return fail(MK_ERR_CUDA, "cuTensorMapEncodeTiled (q8_0 codes) failed (%d)", (int)r);
     return MK_OK;
   }
-  const cuuint64_t rows = (cuuint64_t)cf.num_layers * cf.num_pages * 2 * cf.num_kv_heads * cf.page_size;
-  const cuuint64_t dims[2] = {(cuuint64_t)cf.head_dim, rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)cf.head_dim * 2};
-  const cuuint32_t box[2] = {64, (cuuint32_t)cf.page_size};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv, dims, strides, box, estr,
+  const cuuint64_t row = (cuuint64_t)cf.head_dim * 2;   // bytes of one position
+  const cuuint64_t dims[4] = {64, (cuuint64_t)cf.page_size * cf.num_kv_heads, (cuuint64_t)cf.head_dim / 64,
+                              (cuuint64_t)cf.num_layers * cf.num_pages * 2};
+  const cuuint64_t strides[3] = {row, 128, row * cf.page_size * cf.num_kv_heads};
+  const cuuint32_t box[4] = {64, (cuuint32_t)cf.page_size, (cuuint32_t)cf.head_dim / 64, 2};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, kv, dims, strides, box, estr,
                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(MK_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);

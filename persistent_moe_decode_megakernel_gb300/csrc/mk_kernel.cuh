@@ -106,6 +106,15 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int x, 
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(pol)
       : "memory");
 }
+// 4-D tiled TMA load of box (x, y, z, w) of the tensor map into shared memory (completion on an mbarrier)
+__device__ __forceinline__ void tma_load_4d(void* dst, const void* tmap, int x, int y, int z, int w,
+                                            uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3, "
+      "%4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -906,16 +915,14 @@ struct Producer {
     return page;
   }
 
-  // KV pages of this block's attention items: per page, K then V, each as D/64 boxes of
-  // [page_size rows][64 dims] (128-byte swizzle).  Within a slot, K occupies the first half
-  // and V the second; each holds [dim half][rows][64 dims], page i at rows i*page_size.
+  // KV pages of this block's attention items: one TMA box per page holds its K rows then its
+  // V rows for the item's KV head, each as [dim half][position][64 dims] (128-byte swizzle);
+  // page i of a chunk sits at i * 2 * page_size * D * 2 bytes of the slot.
   __device__ bool attn_items(const mk_task& t) {
     if constexpr (Q8) return attn_items_q8(t);
     const int cta = blockIdx.x;
     const int ppc = pages_per_chunk(p.ps, p.D);
-    const int rows_cap = (kSlotBytes / 2) / (p.D * 2);
-    const int halves = p.D / 64;
-    const uint32_t box = static_cast<uint32_t>(p.ps) * 128u;
+    const uint32_t box = 2u * static_cast<uint32_t>(p.ps) * p.D * 2u;   // K and V of one page
     #pragma unroll 1
     for (int it = p.item_off[cta]; it < p.item_off[cta + 1]; ++it) {
       const mk_attn_item item = p.items[it];
@@ -930,7 +937,7 @@ struct Producer {
         m.kind = R_ATTN; m.op = MK_OP_ATTN; m.first = (pg == item.page_lo); m.last = (pg + n >= item.page_hi);
         m.layer = t.layer; m.n = static_cast<uint16_t>(n); m.row0 = pg; m.idx = static_cast<uint32_t>(it);
         m.e = 0; m.aux = 0; m.lo = item.page_lo; m.hi = item.page_hi;
-        mbar_arrive_expect_tx(full(), 2u * halves * n * box);
+        mbar_arrive_expect_tx(full(), n * box);
         uint8_t* dst = slot();
         #pragma unroll 1
         for (uint32_t i0 = 0; i0 < n; i0 += kIdBatch) {
@@ -940,14 +947,7 @@ struct Producer {
             const uint32_t i = i0 + j;
             if (i >= n) break;
             const int32_t page = checked_page(ids[j], t.layer, pg + i);
-            const int rowk = (((t.layer * p.P + page) * 2) * p.Hkv + item.kvh) * p.ps;
-            const int rowv = rowk + p.Hkv * p.ps;
-            #pragma unroll 1
-            for (int h = 0; h < halves; ++h) {
-              uint8_t* kd = dst + h * rows_cap * 128 + i * box;
-              tma_load_2d(kd, p.kv_map, 64 * h, rowk, full(), pol);
-              tma_load_2d(kd + kSlotBytes / 2, p.kv_map, 64 * h, rowv, full(), pol);
-            }
+            tma_load_4d(dst + i * box, p.kv_map, 0, item.kvh * p.ps, 0, (t.layer * p.P + page) * 2, full(), pol);
           }
         }
         ++c;
@@ -3183,8 +3183,25 @@ struct Consumer {
   // Warp w takes the 16-position tiles w, w+8, ... of each chunk; at the end of the item
   // the warps merge their (max, sum, output) states and the split's partial goes to
   // global memory; the last split of (row, KV head) merges all splits in split order.
-  __device__ __forceinline__ uint32_t swz(int r, int d, int rows_cap) const {
-    return static_cast<uint32_t>((d >> 6) * rows_cap * 128 + r * 128 + ((((d & 63) >> 3) ^ (r & 7)) << 4) + (d & 7) * 2);
+  // A bf16 chunk is page-major: page i holds its K then its V, each as [dim half][position][64
+  // dims] in lines of 128 bytes, and 16-byte piece j of line n sits at piece j ^ (n & 7) (TMA
+  // 128-byte swizzle; every page starts on a 1024-byte boundary, page_size is a multiple of 8).
+  // kv_line: the line of dims 0 .. 63 of chunk position r of K (which = 0) or V (which = 1);
+  // kv_at: the byte offset of dims d .. d + 7 of that position.
+  __device__ __forceinline__ int kv_line(int which, int r) const {
+    const int pg = r / p.ps;
+    return (2 * pg + which) * (D / 64) * p.ps + (r - pg * p.ps);
+  }
+  // the same for position r0 + x of a 16-position tile whose first page is pg0 = r0 / page_size
+  // (x < 16, so at most one page boundary lies inside the tile)
+  __device__ __forceinline__ int kv_line_in(int which, int r0, int pg0, int x) const {
+    int pg = pg0, rr = r0 - pg0 * p.ps + x;
+    if (rr >= p.ps) { rr -= p.ps; ++pg; }
+    return (2 * pg + which) * (D / 64) * p.ps + rr;
+  }
+  __device__ __forceinline__ uint32_t kv_at(int line0, int d) const {
+    const int n = line0 + (d >> 6) * p.ps;
+    return static_cast<uint32_t>(n * 128 + ((((d & 63) >> 3) ^ (n & 7)) << 4) + (d & 7) * 2);
   }
 
   // q8_0 chunks: the slot holds [K codes][V codes][K scales][V scales] of pages_per_chunk_q8 pages,
@@ -3348,7 +3365,6 @@ struct Consumer {
   __device__ __forceinline__ bool attn_item() {
     constexpr int KS = D / 16;                              // k-steps over head dims (Q K^T)
     constexpr int MT = D / 16;                              // 16-dim tiles of the output (P V)
-    constexpr int ROWS = (kSlotBytes / 2) / (D * 2);        // positions a chunk's K (or V) region holds
     const Meta m0 = meta();
     const int l = m0.layer;
     twait = globaltimer();
@@ -3515,7 +3531,6 @@ struct Consumer {
       const int npos = min(static_cast<int>(meta().n) * p.ps, Lc - p0);
       const bool last = meta().last;
       const uint32_t Kb = smem_u32(slot());
-      const uint32_t Vb = Kb + kSlotBytes / 2;
       for (int tile = warp; tile * 16 < npos; tile += kConsumerWarps) {
         const int r0 = tile * 16;
         bool patched = false;
@@ -3526,7 +3541,7 @@ struct Consumer {
           for (int cidx = lane; cidx < 2 * (D / 8); cidx += 32) {
             const int which = cidx / (D / 8), d = (cidx - which * (D / 8)) * 8;
             const uint4 v = *reinterpret_cast<const uint4*>(kvcur + which * D + d);
-            const uint32_t a = (which ? Vb : Kb) + swz(rr, d, ROWS);
+            const uint32_t a = Kb + kv_at(kv_line(which, rr), d);
             asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                          : "memory");
           }
@@ -3540,7 +3555,7 @@ struct Consumer {
             const int rem = cidx % (2 * (D / 8));
             const int which = rem / (D / 8), d = (rem - which * (D / 8)) * 8;
             if (rr >= npos) {
-              const uint32_t a = (which ? Vb : Kb) + swz(rr, d, ROWS);
+              const uint32_t a = Kb + kv_at(kv_line(which, rr), d);
               asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
             }
           }
@@ -3552,10 +3567,13 @@ struct Consumer {
         }
         // S^T = K Q^T for this tile
         float sc[4] = {0.f, 0.f, 0.f, 0.f};
+        const int pg0 = r0 / p.ps;
+        const int lk = kv_line_in(0, r0, pg0, (lane & 7) + ((lane >> 3) & 1) * 8);
+        const int lv = kv_line_in(1, r0, pg0, (lane & 7) + (lane >> 4) * 8);
 #pragma unroll
         for (int s2 = 0; s2 < KS; ++s2) {
           uint32_t a[4];
-          ldsm_x4(Kb + swz(r0 + (lane & 7) + ((lane >> 3) & 1) * 8, 16 * s2 + (lane >> 4) * 8, ROWS), a);
+          ldsm_x4(Kb + kv_at(lk, 16 * s2 + (lane >> 4) * 8), a);
           const uint4 q = qf[s2 * 32 + lane];
           mma_bf16(sc, a, q.x, q.y);
           mma_bf16(sc, a, q.z, q.w);
@@ -3591,7 +3609,7 @@ struct Consumer {
 #pragma unroll
         for (int mm = 0; mm < MT; ++mm) {
           uint32_t a[4];
-          ldsm_x4_t(Vb + swz(r0 + (lane & 7) + (lane >> 4) * 8, 16 * mm + ((lane >> 3) & 1) * 8, ROWS), a);
+          ldsm_x4_t(Kb + kv_at(lv, 16 * mm + ((lane >> 3) & 1) * 8), a);
           mma_bf16(o[mm], a, b0h, b1h);
           mma_bf16(o[mm], a, b0l, b1l);
         }

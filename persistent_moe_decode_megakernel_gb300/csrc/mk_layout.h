@@ -140,8 +140,14 @@ MK_HD int gemv_rows_per_chunk(int K) {
   int r = kSlotBytes / (2 * K);
   return r > kMaxRowsPerChunk ? kMaxRowsPerChunk : r;
 }
-// pages of K (and as many of V) per attention chunk: K fills the slot's first half, V the second
-MK_HD int pages_per_chunk(int page_size, int head_dim) { return (kSlotBytes / 2) / (page_size * head_dim * 2); }
+// bf16 cache: pages per attention chunk, each page's K rows then its V rows (page_size rows of
+// head_dim bf16 each), rounded down so that the chunk's positions are whole 16-row tiles (the
+// consumers' unit of work); 0 when a single page cannot be held that way
+MK_HD int pages_per_chunk(int page_size, int head_dim) {
+  int n = kSlotBytes / (2 * page_size * head_dim * 2);
+  while (n > 0 && (n * page_size) % 16 != 0) --n;
+  return n;
+}
 // q8_0 cache: pages per chunk, each page's K and V codes (page_size rows of head_dim bytes) and
 // their f16 scales (head_dim/32 per row); the slot holds [K codes][V codes][K scales][V scales]
 MK_HD int pages_per_chunk_q8(int page_size, int head_dim) {

@@ -168,6 +168,13 @@ def test_medium_multi_chunk_tiles():
     _parity_one_step(s)
 
 
+@pytest.mark.parametrize("model,ps", [(W.TINY, 8), (MEDIUM, 8), (MEDIUM, 24), (MEDIUM, 64)])
+def test_page_sizes_chunk_layout(model, ps):
+    # page sizes that are not 16: 16-position tiles that span two pages (8, 24) and chunks of a
+    # few large pages (64), with lengths that leave partial pages, partial tiles and full chunks
+    _parity_one_step(tiny_setup(model, [1, 9, 130, 300, 47], page_size=ps))
+
+
 def test_medium_batch_above_register_group():
     s = tiny_setup(MEDIUM, [40, 3, 70, 1, 17, 33])
     _parity_one_step(s, max_batch=8, check_layers=False)
