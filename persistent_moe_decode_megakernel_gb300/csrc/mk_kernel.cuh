@@ -412,6 +412,7 @@ struct FastDiv {
 __device__ __forceinline__ bool tr_on(const Params& p) { return kTrace && p.trace != nullptr; }
 
 // --------------------------------------------------------------------------- shared memory
+constexpr int kCmbItems = 16;   // split items one attention merge group takes at most
 enum : uint8_t { R_EMBED = 1, R_GEMV = 2, R_ATTN = 3, R_GU = 4, R_DOWN = 5, R_END = 6, R_ROUTE = 7,
                  R_DT = 9, R_RED = 10,    // small-batch MoE: transposed down rows; partial-sum reduction
                  R_TC = 11,               // wide batch: a tcgen05 GEMV chunk
@@ -490,6 +491,13 @@ struct __align__(1024) Smem {
   uint64_t wbar;            // tcgen05 tiles: the tensor cores have read the issuer's current record
   uint64_t pbar;            // tcgen05 tiles: the current pass's MMAs have completed (issuer -> consumers)
   uint32_t tmem_base;       // tensor-memory address of this block's accumulators (wide batches)
+  // attention merge: the split items of the group being merged (gathered words from g0, split
+  // scales from fs in the scratch; att: the output's word offset; m: FastDiv multiplier of nsl)
+  struct CmbItem {
+    int32_t g0, ns, o0, nsl, fs, first, att, pad_;
+    uint64_t m;
+  };
+  CmbItem cmb[kCmbItems];
 };
 
 static_assert(sizeof(Smem) + 1024 <= 227 * 1024, "shared memory (with the 1024-byte alignment pad) exceeds 227 KB");
@@ -3654,7 +3662,12 @@ struct Consumer {
     }
     cbar();
     {
-      uint64_t* po = p.PO + (static_cast<size_t>(l) * p.max_items + m0.idx) * (kMaxG * D);
+      // a split's partial state (output, max, normaliser) for the merge; an unsplit pair's
+      // state is the attention output itself, written at once (the same arithmetic as a merge
+      // of one split: every output times 1 / L)
+      const bool whole = item.nsplit == 1;
+      uint64_t* po = whole ? p.ATT + (static_cast<size_t>(l) * p.max_batch + b) * (p.Hq * D) + static_cast<size_t>(kvh) * Gq * D
+                           : p.PO + (static_cast<size_t>(l) * p.max_items + m0.idx) * (kMaxG * D);
       uint64_t* pml = p.PML + (static_cast<size_t>(l) * p.max_items + m0.idx) * (2 * kMaxG);
       #pragma unroll 1
       for (int q4 = threadIdx.x; q4 * 4 < Gq * D; q4 += kConsumerThreads) {
@@ -3672,9 +3685,13 @@ struct Consumer {
           const float4 ov = *reinterpret_cast<const float4*>(st + w * kStride + h * D + d);
           acc.x += f * ov.x; acc.y += f * ov.y; acc.z += f * ov.z; acc.w += f * ov.w;
         }
+        if (whole) {
+          const float invL = 1.f / L;
+          acc.x *= invL; acc.y *= invL; acc.z *= invL; acc.w *= invL;
+        }
         ll_st2(po + h * D + d, acc.x, acc.y, tg);
         ll_st2(po + h * D + d + 2, acc.z, acc.w, tg);
-        if (d == 0) ll_st2(pml + 2 * h, M, L, tg);
+        if (d == 0 && !whole) ll_st2(pml + 2 * h, M, L, tg);
       }
     }
     fence_proxy_async_smem();   // the generic writes into the slot precede its next TMA fill
@@ -3683,82 +3700,128 @@ struct Consumer {
   }
 
   // This block's share of merging the splits of every (row, KV head) pair it holds a split
-  // of: split s of n merges outputs [s*G*D/n, (s+1)*G*D/n) of the pair over all n splits, in
-  // split order, from their tagged partials, and writes them as the attention output.
-  // A warp per head finds the head's max and normaliser over the splits (a lane per split)
-  // and leaves each split's scale exp(m_s - M) / L; then 8 lanes per output sum the splits.
+  // of (pairs in one piece were written out by their item): split s of n merges outputs
+  // [s*G*D/n, (s+1)*G*D/n) of the pair over all n splits, in split order, from their tagged
+  // partials, and writes them as the attention output.  The block's split items go in groups
+  // whose words fit the scratch, each group with one gather (one wait for the slowest split):
+  // then a warp per (item, head) finds the head's max and normaliser over the splits (a lane
+  // per split) and leaves each split's scale exp(m_s - M) / L, and 8 lanes per output sum the
+  // splits.
   __device__ __forceinline__ bool attn_combine(int l) {
     trace_mark(66, l);
     const int Gq = p.G;
     const int GD = Gq * D;
     const int cta = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int i_end = p.item_off[cta + 1];
     twait = globaltimer();
     bool ok = true;
+    int it = p.item_off[cta];
     #pragma unroll 1
-    for (int it = p.item_off[cta]; it < p.item_off[cta + 1]; ++it) {
-      const mk_attn_item item = p.items[it];
-      const int pair = item.b * p.Hkv + item.kvh;
-      const int first = p.pair_first[pair], ns = item.nsplit;
-      const int o0 = item.split * GD / ns, o1 = (item.split + 1) * GD / ns, nsl = o1 - o0;
-      const uint64_t* pml = p.PML + (static_cast<size_t>(l) * p.max_items + first) * (2 * kMaxG);
-      const uint64_t* po = p.PO + (static_cast<size_t>(l) * p.max_items + first) * (kMaxG * D);
-      // one batch of loads: (max, sum) of every split and head, then the slice of every split
-      const int nml = 2 * ns * Gq;
-      const float* ml = S.moe;                  // [ns][G][2]
-      const float* part = S.moe + nml;          // [ns][nsl]
-      float* fs = S.moe + nml + ns * nsl;       // [ns][G] split scales
-      const FastDiv d2g(2 * Gq), dsl(nsl);   // indices below the scratch size < 2^16
-      ok = ll_gather(p, nml + ns * nsl, [=](int i) {
-        if (i < nml) {
-          const int sp = d2g.div(i), r = i - sp * 2 * Gq;
-          return pml + static_cast<size_t>(sp) * 2 * kMaxG + r;
+    for (;;) {
+      // the next group: split items, gathered words [g0, g0 + 2*ns*G + ns*nsl) each, then their
+      // split scales at fs (every thread walks the same items and takes the same group)
+      int nk = 0, gtot = 0, ftot = 0;
+      Smem::CmbItem e0{};   // the group's first item, also in registers (a group of one, the
+                            // batch-1 case, needs no table and no barrier for it)
+      // batches of one or two rows have at most 2 * Hkv pairs, so every block holds one item;
+      // their kernels keep the one-item code alone (instruction fetch is dear at batch 1)
+      constexpr int kmax = TB == 4 ? kCmbItems : 1;
+      #pragma unroll 1
+      for (; it < i_end && nk < kmax; ++it) {
+        const mk_attn_item item = p.items[it];
+        const int ns = item.nsplit;
+        if (ns <= 1) continue;
+        const int o0 = item.split * GD / ns, nsl = (item.split + 1) * GD / ns - o0;
+        const int nw = 2 * ns * Gq + ns * nsl;
+        if (nk > 0 && gtot + nw + ftot + ns * Gq > kMoeScratch) break;
+        Smem::CmbItem e;
+        e.g0 = gtot; e.ns = ns; e.o0 = o0; e.nsl = nsl; e.fs = ftot; e.pad_ = 0;
+        e.first = p.pair_first[item.b * p.Hkv + item.kvh];
+        e.att = (l * p.max_batch + item.b) * (p.Hq * D) + item.kvh * GD;
+        e.m = FastDiv(nsl).m;
+        if (nk == 0) e0 = e;
+        if (threadIdx.x == 0) S.cmb[nk] = e;
+        ++nk; gtot += nw; ftot += ns * Gq;
+      }
+      if (nk == 0) break;
+      const float* g = S.moe;
+      float* fsb = S.moe + gtot;
+      const FastDiv d2g(2 * Gq);
+      const uint64_t* pml0 = p.PML + static_cast<size_t>(l) * p.max_items * (2 * kMaxG);
+      const uint64_t* po0 = p.PO + static_cast<size_t>(l) * p.max_items * (kMaxG * D);
+      const Smem::CmbItem* tab = S.cmb;
+      auto word = [=](const Smem::CmbItem& e, int j) {   // gathered word j of item e
+        const int nml = 2 * e.ns * Gq;
+        if (j < nml) {
+          const int sp = d2g.div(j);
+          return pml0 + static_cast<size_t>(e.first + sp) * (2 * kMaxG) + (j - sp * 2 * Gq);
         }
-        const int j = i - nml, sp = dsl.div(j);
-        return po + static_cast<size_t>(sp) * kMaxG * D + o0 + (j - sp * nsl);
-      }, S.moe + 0, tg) && ok;
+        j -= nml;
+        const int sp = static_cast<int>((static_cast<uint64_t>(j) * e.m) >> 32);
+        return po0 + static_cast<size_t>(e.first + sp) * (kMaxG * D) + e.o0 + (j - sp * e.nsl);
+      };
+      if (TB != 4 || nk == 1) {
+        ok = ll_gather(p, gtot, [=](int i) { return word(e0, i); }, S.moe + 0, tg) && ok;
+      } else {
+        cbar();   // the table
+        ok = ll_gather(p, gtot, [=](int i) {
+          int k = 0;
+          while (k + 1 < nk && i >= tab[k + 1].g0) ++k;
+          return word(tab[k], i - tab[k].g0);
+        }, S.moe + 0, tg) && ok;
+      }
       if (!ok) ll_timeout(p, MK_OP_ATTN, l, tg);
       if (!cbar_and(ok)) return false;
       trace_mark(64, l);
       #pragma unroll 1
-      for (int h = warp; h < Gq; h += kConsumerWarps) {
+      for (int x = warp; x < nk * Gq; x += kConsumerWarps) {
+        const int k = x / Gq, h = x - k * Gq;
+        const Smem::CmbItem e = (TB != 4 || nk == 1) ? e0 : tab[k];
+        const float* ml = g + e.g0;
+        float* fs = fsb + e.fs;
         float M = -INFINITY;
         #pragma unroll 1
-        for (int sp = lane; sp < ns; sp += 32) M = fmaxf(M, ml[(sp * Gq + h) * 2]);
+        for (int sp = lane; sp < e.ns; sp += 32) M = fmaxf(M, ml[(sp * Gq + h) * 2]);
         M = warp_max(M);
         float L = 0.f;
         #pragma unroll 1
-        for (int sp = lane; sp < ns; sp += 32) {
+        for (int sp = lane; sp < e.ns; sp += 32) {
           const float m = ml[(sp * Gq + h) * 2];
           L += (m == -INFINITY ? 0.f : __expf(m - M)) * ml[(sp * Gq + h) * 2 + 1];
         }
         L = warp_sum(L);
         const float invL = 1.f / L;
         #pragma unroll 1
-        for (int sp = lane; sp < ns; sp += 32) {
+        for (int sp = lane; sp < e.ns; sp += 32) {
           const float m = ml[(sp * Gq + h) * 2];
           fs[sp * Gq + h] = (m == -INFINITY ? 0.f : __expf(m - M)) * invL;
         }
       }
       cbar();
-      uint64_t* att = p.ATT + (static_cast<size_t>(l) * p.max_batch + item.b) * (p.Hq * D) +
-                      static_cast<size_t>(item.kvh) * GD;
       const int og = threadIdx.x >> 3, sub = threadIdx.x & 7;
       #pragma unroll 1
-      for (int base = 0; base < nsl; base += kConsumerThreads / 8) {   // uniform trip count: the shuffles below
-        const int oi = base + og;
-        float acc = 0.f;
-        if (oi < nsl) {
-          const int h = (o0 + oi) / D;
-          #pragma unroll 1
-          for (int sp = sub; sp < ns; sp += 8) acc += fs[sp * Gq + h] * part[sp * nsl + oi];
+      for (int k = 0; k < nk; ++k) {
+        const Smem::CmbItem e = (TB != 4 || nk == 1) ? e0 : tab[k];
+        const float* part = g + e.g0 + 2 * e.ns * Gq;
+        const float* fs = fsb + e.fs;
+        uint64_t* att = p.ATT + static_cast<size_t>(e.att);
+        #pragma unroll 1
+        for (int base = 0; base < e.nsl; base += kConsumerThreads / 8) {   // uniform trip count: the shuffles below
+          const int oi = base + og;
+          float acc = 0.f;
+          if (oi < e.nsl) {
+            const int h = (e.o0 + oi) / D;
+            #pragma unroll 1
+            for (int sp = sub; sp < e.ns; sp += 8) acc += fs[sp * Gq + h] * part[sp * e.nsl + oi];
+          }
+          acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+          acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+          acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+          if (oi < e.nsl && sub == 0) ll_st(att + e.o0 + oi, acc, tg);
         }
-        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-        acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-        if (oi < nsl && sub == 0) ll_st(att + o0 + oi, acc, tg);
       }
-      cbar();
+      cbar();   // the scratch and the table are reused by the next group
     }
     trace_mark(65, l);
     return true;
