@@ -2628,26 +2628,30 @@ struct Consumer {
         const int e = lane + 32 * k;
         v[k] = e < E ? lg[b * E + e] : -INFINITY;
       }
+      // logits as unsigned keys in the same order (-0 taken as +0, so that equal logits have
+      // equal keys); a key of 0 is below every logit
+      uint32_t key[kMaxExperts / 32];
+#pragma unroll
+      for (int k = 0; k < kMaxExperts / 32; ++k) {
+        const uint32_t u = __float_as_uint(v[k] + 0.f);
+        key[k] = lane + 32 * k < E ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
+      }
       uint32_t taken = 0;   // this lane's values already chosen (bit k)
       #pragma unroll 1
       for (int j = 0; j < K; ++j) {
-        float bv = -INFINITY;
+        // this lane's best (a strict > keeps the lower expert of equal keys), then the warp's
+        // largest key and the lowest expert holding it, one warp reduction each
+        uint32_t bk = 0u;
         int bi = 0x7fffffff;
 #pragma unroll
-        for (int k = 0; k < kMaxExperts / 32; ++k) {
-          const int e = lane + 32 * k;
-          if (e < E && !((taken >> k) & 1u) && (v[k] > bv || (v[k] == bv && e < bi))) { bv = v[k]; bi = e; }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-          if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-        }
+        for (int k = 0; k < kMaxExperts / 32; ++k)
+          if (!((taken >> k) & 1u) && key[k] > bk) { bk = key[k]; bi = lane + 32 * k; }
+        const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+        bi = static_cast<int>(__reduce_min_sync(0xffffffffu, bk == mk ? static_cast<uint32_t>(bi) : 0x7fffffffu));
         if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
         if (lane == 0) {
           S.rids[b * K + j] = bi;
-          S.rval[b * K + j] = bv;
+          S.rval[b * K + j] = __uint_as_float((mk & 0x80000000u) ? (mk & 0x7fffffffu) : ~mk);
           atomicAdd(&S.ecnt[bi], 1);
         }
       }
