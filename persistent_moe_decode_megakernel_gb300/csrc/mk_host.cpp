@@ -1064,7 +1064,7 @@ int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t B, const int32_t* 
   const bool tcs = cfg->max_batch >= mk::kTcMinBatch && B >= mk::kTcMinBatch;
   // per layer: active experts (ascending) and the gate/up unit range of every block
   std::vector<std::vector<int>> act(L), rows_of(L);   // active experts; rows routed to each expert
-  std::vector<std::vector<int32_t>> gu_start(L);
+  std::vector<std::vector<int32_t>> gu_start(L), dn_start(L);
   for (int l = 0; l < L; ++l) {
     std::vector<int>& cnt = rows_of[l];
     cnt.assign(E, 0);
@@ -1083,6 +1083,11 @@ int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t B, const int32_t* 
       }
     const int nact = (int)act[l].size();
     for (int j = 0; j <= n_ctas; ++j) gu_start[l].push_back(mk::moe_gu_start(j, n_ctas, cum.data(), cost.data(), nact, F));
+    // the tcgen05 down projection deals its (expert, row block) units by the same costs
+    const int nrb = (H + mk::kTcDownRows - 1) / mk::kTcDownRows;
+    std::vector<int64_t> dcum(cum.size());
+    for (size_t a = 0; a < cum.size(); ++a) dcum[a] = cum[a] / F * nrb;
+    for (int j = 0; j <= n_ctas; ++j) dn_start[l].push_back(mk::moe_gu_start(j, n_ctas, dcum.data(), cost.data(), nact, nrb));
   }
   // coverage of the MoE work: gate/up units and (active expert, hidden row) pairs of the down
   // projection, or on the small-batch path the transposed down row of every unit
@@ -1186,8 +1191,7 @@ int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t B, const int32_t* 
         r.push_back({100, task, l, (uint32_t)a, (uint32_t)f0, F_FIRST | F_LAST | (a * F + fend >= u1 ? F_LAST_GU : 0)});
         u = a * F + fend;
       }
-      const int U = nact * nrb;
-      const int ua = (int)((int64_t)U * i / n_ctas), ub = (int)((int64_t)U * (i + 1) / n_ctas);
+      const int ua = dn_start[l][i], ub = dn_start[l][i + 1];
       for (int u = ua; u < ub; ++u) {
         const int a = u / nrb, rb = u % nrb;
         for (int x = rb * mk::kTcDownRows; x < std::min(H, (rb + 1) * mk::kTcDownRows); ++x) dn_seen[l][(size_t)a * H + x]++;

@@ -1016,6 +1016,13 @@ struct Producer {
     return true;
   }
 
+  // cost prefix of the down projection's units: ecum counts F units per expert, these nrb
+  struct DownCum {
+    const int32_t* ecum;
+    int F, nrb;
+    __device__ int32_t operator[](int a) const { return ecum[a] / F * nrb; }
+  };
+
   // MoE records of layer l.  First a routing record: the consumers of this block read the
   // router logits, route every row of the batch and split the layer's gate/up units over the
   // blocks, all in shared memory, then hand over.  Gate/up: this block's units (FFN rows of
@@ -1125,9 +1132,9 @@ struct Producer {
       // pairs' weighted outputs, then the block sums the slots of its own hidden rows
       const uint64_t* map = p.wmaps + static_cast<size_t>(tc_map_index(kTcOpDown, l, p.L)) * 16;
       const int nrb = (H + kTcDownRows - 1) / kTcDownRows;
-      const int U = nact * nrb;
-      const int ua = static_cast<int>(static_cast<int64_t>(U) * cta / p.n_ctas);
-      const int ub = static_cast<int>(static_cast<int64_t>(U) * (cta + 1) / p.n_ctas);
+      const DownCum dcum{S.ecum, F, nrb};   // the gate/up cost prefix, per row block
+      const int ua = moe_gu_start(cta, p.n_ctas, dcum, S.ecost, nact, nrb);
+      const int ub = moe_gu_start(cta + 1, p.n_ctas, dcum, S.ecost, nact, nrb);
       #pragma unroll 1
       for (int u = ua; u < ub;) {
         const int a = u / nrb, rb = u - a * nrb;

@@ -160,15 +160,20 @@ MK_HD int pages_per_chunk_q8(int page_size, int head_dim) {
 // bytes plus the batch rows it serves: max(4, rows routed to the expert), so at small
 // batch every unit weighs the same and at large batch crowded experts count for more.
 // Block j takes the units whose cost prefix starts in [C*j/N, C*(j+1)/N), C the total.
-// (On the tcgen05 path of wide batches the routed rows are the N columns of one MMA: a unit costs
-// its weight bytes whatever its rows, and the split is by FFN rows alone.)
-MK_HD int32_t moe_unit_cost(int routed_rows, bool tc) { return tc ? 1 : (routed_rows > 4 ? routed_rows : 4); }
+// (On the tcgen05 path of wide batches the routed rows are the N columns of the MMAs: a unit
+// costs its weight bytes plus a share that grows with its rows' 16-column groups, the MMA time.
+// The down projection's (expert, row block) units are dealt by the same per-expert cost.)
+constexpr int kTcUnitBase = 4;
+MK_HD int32_t moe_unit_cost(int routed_rows, bool tc) {
+  return tc ? kTcUnitBase + (routed_rows + 15) / 16 : (routed_rows > 4 ? routed_rows : 4);
+}
 
-// first unit of block j of N; cum[a] = cost of the units of experts 0..a-1 (cum[nact] = C,
-// at most 256 experts x 1024 rows x 64 = 2^24), cost[a] = cost of one unit of expert a.
-// With 0 < j < N <= 256, C * j < 2^32: the arithmetic stays in 32 bits.
-template <class I>
-MK_HD int32_t moe_gu_start(int j, int N, const I* cum, const I* cost, int nact, int F) {
+// first unit of block j of N, with `per` units per expert; cum[a] = cost of the units of
+// experts 0..a-1 (cum[nact] = C, at most 256 experts x 1024 units x 64 = 2^24), cost[a] = cost
+// of one unit of expert a (cum and cost: arrays or anything indexable).  With 0 < j < N <= 256,
+// C * j < 2^32: the arithmetic stays in 32 bits.
+template <class C, class K>
+MK_HD int32_t moe_gu_start(int j, int N, const C& cum, const K& cost, int nact, int F) {
   if (j <= 0 || nact <= 0) return 0;
   if (j >= N) return nact * F;
   const uint32_t T = static_cast<uint32_t>(cum[nact]) * static_cast<uint32_t>(j) / static_cast<uint32_t>(N);
