@@ -1085,9 +1085,8 @@ int mk_simulate(const mk_config* cfg, int32_t n_ctas, int32_t B, const int32_t* 
     for (int j = 0; j <= n_ctas; ++j) gu_start[l].push_back(mk::moe_gu_start(j, n_ctas, cum.data(), cost.data(), nact, F));
     // the tcgen05 down projection deals its (expert, row block) units by the same costs
     const int nrb = (H + mk::kTcDownRows - 1) / mk::kTcDownRows;
-    std::vector<int64_t> dcum(cum.size());
-    for (size_t a = 0; a < cum.size(); ++a) dcum[a] = cum[a] / F * nrb;
-    for (int j = 0; j <= n_ctas; ++j) dn_start[l].push_back(mk::moe_gu_start(j, n_ctas, dcum.data(), cost.data(), nact, nrb));
+    for (int j = 0; j <= n_ctas; ++j)
+      dn_start[l].push_back(mk::moe_gu_start(j, n_ctas, cum.data(), cost.data(), nact, nrb, nrb, F));
   }
   // coverage of the MoE work: gate/up units and (active expert, hidden row) pairs of the down
   // projection, or on the small-batch path the transposed down row of every unit

@@ -678,8 +678,10 @@ __device__ __forceinline__ void tc_group_rows(const Params& p, int op, int KS, u
 }
 
 // --------------------------------------------------------------------------- producer
-// Q8: the KV pool holds q8_0 blocks (codes and scales) instead of bf16 values.
-template <bool Q8>
+// Q8: the KV pool holds q8_0 blocks (codes and scales) instead of bf16 values.  TC: the
+// tcgen05 paths of wide batches are compiled in (the widest instantiation only: the code the
+// narrower kernels never run would still cost them instruction fetch).
+template <bool Q8, bool TC>
 struct Producer {
   const Params& p;
   Smem& S;
@@ -1016,13 +1018,6 @@ struct Producer {
     return true;
   }
 
-  // cost prefix of the down projection's units: ecum counts F units per expert, these nrb
-  struct DownCum {
-    const int32_t* ecum;
-    int F, nrb;
-    __device__ int32_t operator[](int a) const { return ecum[a] / F * nrb; }
-  };
-
   // MoE records of layer l.  First a routing record: the consumers of this block read the
   // router logits, route every row of the batch and split the layer's gate/up units over the
   // blocks, all in shared memory, then hand over.  Gate/up: this block's units (FFN rows of
@@ -1072,7 +1067,7 @@ struct Producer {
     if (u0 >= u1) {
       if (!moe_control(R_GU, l, 0u, 1u)) return false;
     }
-    if (p.tc) {
+    if (TC && p.tc) {
       // wide batch: each expert run on tcgen05, its routed pairs as the N columns
       const uint64_t* map = p.wmaps + static_cast<size_t>(tc_map_index(MK_OP_MOE, l, p.L)) * 16;
       #pragma unroll 1
@@ -1091,7 +1086,7 @@ struct Producer {
       }
     }
     #pragma unroll 1
-    for (int u = p.tc ? u1 : u0; u < u1;) {
+    for (int u = (TC && p.tc) ? u1 : u0; u < u1;) {
       const int a = u / F, f0 = u - a * F;
       const int fend = min(F, u1 - a * F);
       const uint32_t lastgu = (a * F + fend >= u1) ? 1u : 0u;
@@ -1126,15 +1121,15 @@ struct Producer {
     // down
     const uint32_t r0 = static_cast<uint32_t>(static_cast<uint64_t>(H) * cta / p.n_ctas);
     const uint32_t r1 = static_cast<uint32_t>(static_cast<uint64_t>(H) * (cta + 1) / p.n_ctas);
-    if (p.tc) {
+    if (TC && p.tc) {
       // wide batch: (active expert, 128-row block) units dealt evenly over the blocks, consecutive
       // units of one expert forming one run (contiguous hidden rows); each run on tcgen05 writes its
       // pairs' weighted outputs, then the block sums the slots of its own hidden rows
       const uint64_t* map = p.wmaps + static_cast<size_t>(tc_map_index(kTcOpDown, l, p.L)) * 16;
       const int nrb = (H + kTcDownRows - 1) / kTcDownRows;
-      const DownCum dcum{S.ecum, F, nrb};   // the gate/up cost prefix, per row block
-      const int ua = moe_gu_start(cta, p.n_ctas, dcum, S.ecost, nact, nrb);
-      const int ub = moe_gu_start(cta + 1, p.n_ctas, dcum, S.ecost, nact, nrb);
+      // the gate/up cost prefix (F units per expert) scaled to nrb units per expert
+      const int ua = moe_gu_start(cta, p.n_ctas, S.ecum, S.ecost, nact, nrb, nrb, F);
+      const int ub = moe_gu_start(cta + 1, p.n_ctas, S.ecum, S.ecost, nact, nrb, nrb, F);
       #pragma unroll 1
       for (int u = ua; u < ub;) {
         const int a = u / nrb, rb = u - a * nrb;
@@ -1261,7 +1256,7 @@ struct Producer {
         case MK_OP_QKV:
         case MK_OP_OPROJ:
         case MK_OP_ROUTER:
-        case MK_OP_HEAD: ok = p.tc ? tc_tile(t, static_cast<uint32_t>(ti)) : gemv_tile(t, static_cast<uint32_t>(ti)); break;
+        case MK_OP_HEAD: ok = (TC && p.tc) ? tc_tile(t, static_cast<uint32_t>(ti)) : gemv_tile(t, static_cast<uint32_t>(ti)); break;
         case MK_OP_ATTN: ok = attn_items(t); break;
         case MK_OP_MOE: ok = moe_tasks(t); break;
         case MK_OP_END: ok = emit_control(R_END, t, static_cast<uint32_t>(ti)); break;
@@ -2767,7 +2762,7 @@ struct Consumer {
 #pragma unroll
       for (int k = 0; k < kMaxExperts / 32; ++k) {
         const int a = lane * (kMaxExperts / 32) + k;
-        const int32_t cst = a < nact ? moe_unit_cost(S.ecnt[S.eact[a]], p.tc != 0) : 0;
+        const int32_t cst = a < nact ? moe_unit_cost(S.ecnt[S.eact[a]], TB == 4 && p.tc != 0) : 0;
         if (a < nact) S.ecost[a] = cst;
         run += cst * p.F;
         loc[k] = run;
@@ -3952,7 +3947,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     // producer warpgroup: one thread streams, the rest only lend their registers
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
     if (tid == kConsumerThreads) {
-      Producer<Q8> prod(p, S);
+      Producer<Q8, TB == 4> prod(p, S);
       prod.run();
     }
     if constexpr (TB == 4) {

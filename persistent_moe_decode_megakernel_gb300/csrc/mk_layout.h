@@ -168,22 +168,23 @@ MK_HD int32_t moe_unit_cost(int routed_rows, bool tc) {
   return tc ? kTcUnitBase + (routed_rows + 15) / 16 : (routed_rows > 4 ? routed_rows : 4);
 }
 
-// first unit of block j of N, with `per` units per expert; cum[a] = cost of the units of
-// experts 0..a-1 (cum[nact] = C, at most 256 experts x 1024 units x 64 = 2^24), cost[a] = cost
-// of one unit of expert a (cum and cost: arrays or anything indexable).  With 0 < j < N <= 256,
-// C * j < 2^32: the arithmetic stays in 32 bits.
-template <class C, class K>
-MK_HD int32_t moe_gu_start(int j, int N, const C& cum, const K& cost, int nact, int F) {
+// first unit of block j of N, with F units per expert; cum[a] = cost of the units of experts
+// 0..a-1 (cum[nact] = C, at most 256 experts x 1024 units x 64 = 2^24), cost[a] = cost of one
+// unit of expert a.  With 0 < j < N <= 256, C * j < 2^32: the arithmetic stays in 32 bits.
+// The cost prefix of F units per expert also serves nb units per expert when scaled by nb / F
+// (cum[a] is a multiple of F): scale = {nb, F}, {1, 1} for the prefix as it is.
+template <class I>
+MK_HD int32_t moe_gu_start(int j, int N, const I* cum, const I* cost, int nact, int F, int sn = 1, int sd = 1) {
   if (j <= 0 || nact <= 0) return 0;
   if (j >= N) return nact * F;
-  const uint32_t T = static_cast<uint32_t>(cum[nact]) * static_cast<uint32_t>(j) / static_cast<uint32_t>(N);
+  const uint32_t T = static_cast<uint32_t>(cum[nact] / sd * sn) * static_cast<uint32_t>(j) / static_cast<uint32_t>(N);
   int lo = 0, hi = nact - 1;   // last a with cum[a] <= T
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (static_cast<uint32_t>(cum[mid]) <= T) lo = mid; else hi = mid - 1;
+    if (static_cast<uint32_t>(cum[mid] / sd * sn) <= T) lo = mid; else hi = mid - 1;
   }
   const uint32_t c = static_cast<uint32_t>(cost[lo]);
-  const uint32_t f = (T - static_cast<uint32_t>(cum[lo]) + c - 1u) / c;
+  const uint32_t f = (T - static_cast<uint32_t>(cum[lo] / sd * sn) + c - 1u) / c;
   return f >= static_cast<uint32_t>(F) ? (lo + 1) * F : lo * F + static_cast<int32_t>(f);
 }
 
