@@ -680,8 +680,10 @@ __device__ __forceinline__ void tc_group_rows(const Params& p, int op, int KS, u
 // --------------------------------------------------------------------------- producer
 // Q8: the KV pool holds q8_0 blocks (codes and scales) instead of bf16 values.  TC: the
 // tcgen05 paths of wide batches are compiled in (the widest instantiation only: the code the
-// narrower kernels never run would still cost them instruction fetch).
-template <bool Q8, bool TC>
+// narrower kernels never run would still cost them instruction fetch).  SMALL: the small-batch
+// MoE path, the only one of the narrow instantiations (the host launches the widest one for
+// every step that cannot take it).
+template <bool Q8, bool TC, bool SMALL>
 struct Producer {
   const Params& p;
   Smem& S;
@@ -1061,7 +1063,7 @@ struct Producer {
     const int nact = S.nact;
     const int u0 = S.gu_lo, u1 = S.gu_hi;
     const int H = p.H, F = p.F;
-    if (p.small_moe) return small_moe_tasks(l, u0, u1, w_gu, w_dt);
+    if constexpr (SMALL) return small_moe_tasks(l, u0, u1, w_gu, w_dt);
     // gate/up
     const int fpc = gemv_rows_per_chunk(H) / 2;    // gate rows (and as many up rows) per chunk
     if (u0 >= u1) {
@@ -1475,6 +1477,9 @@ __device__ void tc_issuer(const Params& p, Smem& S) {
 // given to shared memory, those accesses would miss to L2 after every barrier.
 template <int TB, int D, bool Q8>
 struct Consumer {
+  // the MoE path of this instantiation: small-batch in the narrow ones, general in the widest
+  // (the host picks the instantiation by the step's path)
+  static constexpr bool kSmallMoe = TB <= kSmallMaxB;
   const Params& p;
   Smem& S;
   uint32_t c = 0;       // this warp's current record
@@ -1854,7 +1859,7 @@ struct Consumer {
     const int K = op == MK_OP_OPROJ ? p.Hq * p.D : p.H;
     // (the small-batch MoE path keeps whole rows per warp: split rows would reuse the storage of
     // the cached MoE input, which every gate/up tile of the layer reads)
-    const Seg<TB> sg(K, gu && !p.small_moe ? (nf0 >= kConsumerWarps ? 1 : kConsumerWarps / nf0) : 1);
+    const Seg<TB> sg(K, gu && !kSmallMoe ? (nf0 >= kConsumerWarps ? 1 : kConsumerWarps / nf0) : 1);
     // GEMV input: 0 x_in/attn_norm, 1 attention output, 2 x_mid/ffn_norm, 3 x_final/final_norm
     const int kind = op == MK_OP_QKV ? 0 : op == MK_OP_OPROJ ? 1 : (op == MK_OP_ROUTER || gu) ? 2 : 3;
     // the test hook waits for a tag that is never written
@@ -1869,7 +1874,7 @@ struct Consumer {
     const int GR = kGroups ? wide_group_rows(K) : TB;   // rows per register group (at most TB)
     const int ngroups = kGroups ? (cnt + GR - 1) / GR : 1;
     OutMap om = out_map(op, l);
-    if (TB <= kSmallMaxB && gu && p.small_moe) {
+    if (kSmallMoe && gu) {
       om.hs = S.hsm;
       om.hoff = static_cast<int>(meta().idx) * p.F - S.gu_lo;
     }
@@ -1994,7 +1999,7 @@ struct Consumer {
       if (!ok) { wok = false; break; }
       if (last && (!gu_fused || (meta().aux & 1u))) break;
       bool got = next_rec();
-      if (TB <= kSmallMaxB && gu && p.small_moe) {
+      if (kSmallMoe && gu) {
         // small-batch MoE: the block's gate/up chunks and the transposed down chunk after each
         // group are one tile; the warps move through it together (a down chunk reads every
         // warp's SwiGLU outputs of the group)
@@ -2012,7 +2017,7 @@ struct Consumer {
         const int e2 = static_cast<int>(meta().e);
 #pragma unroll
         for (int tb = 0; tb < TB; ++tb) rj[tb] = tb < B ? slot_of(tb, e2) : -1;
-        if (TB <= kSmallMaxB && gu && p.small_moe) om.hoff = static_cast<int>(meta().idx) * p.F - S.gu_lo;
+        if (kSmallMoe && gu) om.hoff = static_cast<int>(meta().idx) * p.F - S.gu_lo;
       }
     }
     if (!ok) ll_timeout(p, eop, l, tg);
@@ -2719,7 +2724,7 @@ struct Consumer {
     trace_mark(18, l);
     // small-batch MoE: the logits are consumed; the scratch becomes the [B][H] partial output
     // (and a row that is not routed to a unit's expert contributes zero to it)
-    if (p.small_moe) {
+    if constexpr (kSmallMoe) {
       #pragma unroll 1
       for (int i = threadIdx.x; i < B * H; i += kConsumerThreads) S.moe[i] = 0.f;
       #pragma unroll 1
@@ -3856,7 +3861,9 @@ struct Consumer {
         case R_YRED:
           if constexpr (TB == 4) ok = y_reduce();
           break;
-        case R_DOWN: ok = moe_down(); break;
+        case R_DOWN:   // the general MoE path: the widest instantiation only
+          if constexpr (!kSmallMoe) ok = moe_down();
+          break;
         case R_ROUTE: ok = route_local(); break;
         case R_DT:   // small-batch MoE records exist only for batches of at most kSmallMaxB rows
           if constexpr (TB <= kSmallMaxB) ok = moe_dt();
@@ -3947,7 +3954,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     // producer warpgroup: one thread streams, the rest only lend their registers
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
     if (tid == kConsumerThreads) {
-      Producer<Q8, TB == 4> prod(p, S);
+      Producer<Q8, TB == 4, (TB <= kSmallMaxB)> prod(p, S);
       prod.run();
     }
     if constexpr (TB == 4) {
