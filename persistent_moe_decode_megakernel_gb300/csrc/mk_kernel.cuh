@@ -1476,10 +1476,13 @@ __device__ void tc_issuer(const Params& p, Smem& S) {
 // registers (the consumer warpgroups hold 224 each).  A call that took the object's
 // address would put that state in local memory, and with nearly all of the SM's L1
 // given to shared memory, those accesses would miss to L2 after every barrier.
-template <int TB, int D, bool Q8>
+// TB: rows per register group (1, 2 or 4); W: the tcgen05 instantiation (batches of
+// kTcMinBatch rows or more: every GEMV a tcgen05 tile), which carries none of the CUDA-core and
+// mma.sync GEMV code, as the others carry none of the tcgen05 code.
+template <int TB, int D, bool Q8, bool W>
 struct Consumer {
-  // the MoE path of this instantiation: small-batch in the narrow ones, general in the widest
-  // (the host picks the instantiation by the step's path)
+  // the MoE path of this instantiation: small-batch in the narrow ones, general (or tcgen05) in
+  // the widest (the host picks the instantiation by the step's path)
   static constexpr bool kSmallMoe = TB <= kSmallMaxB;
   const Params& p;
   Smem& S;
@@ -2718,7 +2721,7 @@ struct Consumer {
         if (lane == 0) { S.rmax[b] = mx; S.rz[b] = z; }
       }
     }
-    if (TB == 4 && B >= 8) topk_rows_warp(lg);   // (only the widest instantiation sees such batches)
+    if (W && B >= 8) topk_rows_warp(lg);   // (only the tcgen05 instantiation sees such batches)
     else if (E <= 128) rank_rows<16>(lg);
     else rank_rows<32>(lg);
     cbar();
@@ -2768,7 +2771,7 @@ struct Consumer {
 #pragma unroll
       for (int k = 0; k < kMaxExperts / 32; ++k) {
         const int a = lane * (kMaxExperts / 32) + k;
-        const int32_t cst = a < nact ? moe_unit_cost(S.ecnt[S.eact[a]], TB == 4 && p.tc != 0) : 0;
+        const int32_t cst = a < nact ? moe_unit_cost(S.ecnt[S.eact[a]], W) : 0;
         if (a < nact) S.ecost[a] = cst;
         run += cst * p.F;
         loc[k] = run;
@@ -3738,7 +3741,7 @@ struct Consumer {
                             // batch-1 case, needs no table and no barrier for it)
       // batches of one or two rows have at most 2 * Hkv pairs, so every block holds one item;
       // their kernels keep the one-item code alone (instruction fetch is dear at batch 1)
-      constexpr int kmax = TB == 4 ? kCmbItems : 1;
+      constexpr int kmax = W ? kCmbItems : 1;
       #pragma unroll 1
       for (; it < i_end && nk < kmax; ++it) {
         const mk_attn_item item = p.items[it];
@@ -3773,7 +3776,7 @@ struct Consumer {
         const int sp = static_cast<int>((static_cast<uint64_t>(j) * e.m) >> 32);
         return po0 + static_cast<size_t>(e.first + sp) * (kMaxG * D) + e.o0 + (j - sp * e.nsl);
       };
-      if (TB != 4 || nk == 1) {
+      if (!W || nk == 1) {
         ok = ll_gather(p, gtot, [=](int i) { return word(e0, i); }, S.moe + 0, tg) && ok;
       } else {
         cbar();   // the table
@@ -3789,7 +3792,7 @@ struct Consumer {
       #pragma unroll 1
       for (int x = warp; x < nk * Gq; x += kConsumerWarps) {
         const int k = x / Gq, h = x - k * Gq;
-        const Smem::CmbItem e = (TB != 4 || nk == 1) ? e0 : tab[k];
+        const Smem::CmbItem e = (!W || nk == 1) ? e0 : tab[k];
         const float* ml = g + e.g0;
         float* fs = fsb + e.fs;
         float M = -INFINITY;
@@ -3814,7 +3817,7 @@ struct Consumer {
       const int og = threadIdx.x >> 3, sub = threadIdx.x & 7;
       #pragma unroll 1
       for (int k = 0; k < nk; ++k) {
-        const Smem::CmbItem e = (TB != 4 || nk == 1) ? e0 : tab[k];
+        const Smem::CmbItem e = (!W || nk == 1) ? e0 : tab[k];
         const float* part = g + e.g0 + 2 * e.ns * Gq;
         const float* fs = fsb + e.fs;
         uint64_t* att = p.ATT + static_cast<size_t>(e.att);
@@ -3853,17 +3856,18 @@ struct Consumer {
         case R_EMBED: ok = embed(); break;
         case R_GEMV:
         case R_GU:   // one inlined copy of the GEMV stream serves both kinds
-          ok = (m0.kind == R_GU && meta().n == 0) ? true : stream_gemv(m0.kind == R_GU ? int(R_OP_GU) : int(m0.op));
+          if constexpr (W) ok = m0.kind == R_GU && meta().n == 0;   // (only a block's empty gate/up share)
+          else ok = (m0.kind == R_GU && meta().n == 0) ? true : stream_gemv(m0.kind == R_GU ? int(R_OP_GU) : int(m0.op));
           break;
         case R_ATTN: ok = attn_item(); break;
         case R_TC:
-          if constexpr (TB == 4) ok = tc_gemv();
+          if constexpr (W) ok = tc_gemv();
           break;
         case R_YRED:
-          if constexpr (TB == 4) ok = y_reduce();
+          if constexpr (W) ok = y_reduce();
           break;
         case R_DOWN:   // the general MoE path: the widest instantiation only
-          if constexpr (!kSmallMoe) ok = moe_down();
+          if constexpr (!kSmallMoe && !W) ok = moe_down();
           break;
         case R_ROUTE: ok = route_local(); break;
         case R_DT:   // small-batch MoE records exist only for batches of at most kSmallMaxB rows
@@ -3897,7 +3901,7 @@ struct Consumer {
 };
 
 // --------------------------------------------------------------------------- the kernel
-template <int TB, int D, bool Q8>
+template <int TB, int D, bool Q8, bool W>
 __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   // the ring holds 128-byte-swizzled TMA tiles, whose pattern repeats every 1024 bytes
@@ -3927,7 +3931,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     if (tr_on(p)) p.trace[static_cast<size_t>(blockIdx.x) * p.trace_cap * 4 + 1] = globaltimer();
     fence_mbar_init();
   }
-  if constexpr (TB == 4) {
+  if constexpr (W) {
     // wide batches: warp 0 takes all of this SM's tensor memory for the tcgen05 accumulators
     if (p.tc && (tid >> 5) == 0) {
       asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&S.tmem_base)),
@@ -3938,7 +3942,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     tc_fence_before();
   }
   __syncthreads();
-  if constexpr (TB == 4) tc_fence_after();
+  if constexpr (W) tc_fence_after();
   {
     // every block warms a slice of the small per-layer vectors (norm gains) in L2, so that
     // their first read in a layer is an L2 hit rather than a DRAM access behind the stream
@@ -3955,10 +3959,10 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     // producer warpgroup: one thread streams, the rest only lend their registers
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
     if (tid == kConsumerThreads) {
-      Producer<Q8, TB == 4, (TB <= kSmallMaxB)> prod(p, S);
+      Producer<Q8, W, (TB <= kSmallMaxB)> prod(p, S);
       prod.run();
     }
-    if constexpr (TB == 4) {
+    if constexpr (W) {
       if (p.tc && (tid >> 5) == (kConsumerThreads >> 5) + 1) tc_issuer(p, S);   // the next warp
     }
     __syncwarp();
@@ -3967,18 +3971,18 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
     {
-      Consumer<TB, D, Q8> cons(p, S);
+      Consumer<TB, D, Q8, W> cons(p, S);
       cons.run();
-      if constexpr (TB == 4) {
+      if constexpr (W) {
         if (p.tc) cons.tc_stop();
       }
     }
     asm volatile("bar.sync %0, 128;" ::"r"(10 + (tid >> 7)) : "memory");
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kLaunchRegs));
   }
-  if constexpr (TB == 4) tc_fence_before();
+  if constexpr (W) tc_fence_before();
   __syncthreads();
-  if constexpr (TB == 4) {
+  if constexpr (W) {
     // every tcgen05 operation of the block has completed (each tile waits for its commits)
     if (p.tc && (tid >> 5) == 0) {
       tc_fence_after();
@@ -4031,15 +4035,15 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
   }
 }
 
-template <int TB, int D, bool Q8>
+template <int TB, int D, bool Q8, bool W>
 cudaError_t configure_t(size_t smem) {
-  return cudaFuncSetAttribute(step_kernel<TB, D, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(step_kernel<TB, D, Q8, W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(smem));
 }
 
 // One block per SM, all resident at once (a cooperative launch: blocks wait on one another's
 // data).  Launched through cudaLaunchKernelEx so that stream capture records it in a graph.
-template <int TB, int D, bool Q8>
+template <int TB, int D, bool Q8, bool W>
 cudaError_t launch_t(const Params& p, size_t smem, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.n_ctas);
@@ -4051,27 +4055,30 @@ cudaError_t launch_t(const Params& p, size_t smem, cudaStream_t s) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, step_kernel<TB, D, Q8>, p);
+  return cudaLaunchKernelEx(&cfg, step_kernel<TB, D, Q8, W>, p);
 }
 
 template <int D, bool Q8>
 cudaError_t configure_all(size_t smem) {
   cudaError_t e;
-  if ((e = configure_t<1, D, Q8>(smem)) != cudaSuccess) return e;
-  if ((e = configure_t<2, D, Q8>(smem)) != cudaSuccess) return e;
-  return configure_t<4, D, Q8>(smem);
+  if ((e = configure_t<1, D, Q8, false>(smem)) != cudaSuccess) return e;
+  if ((e = configure_t<2, D, Q8, false>(smem)) != cudaSuccess) return e;
+  if ((e = configure_t<4, D, Q8, false>(smem)) != cudaSuccess) return e;
+  return configure_t<4, D, Q8, true>(smem);
 }
 
+// tb: 1, 2 or 4 rows per register group; 5: the tcgen05 instantiation
 template <int D, bool Q8>
 cudaError_t launch_any(const Params& p, int tb, size_t smem, cudaStream_t s) {
-  if (tb == 1) return launch_t<1, D, Q8>(p, smem, s);
-  if (tb == 2) return launch_t<2, D, Q8>(p, smem, s);
-  return launch_t<4, D, Q8>(p, smem, s);
+  if (tb == 1) return launch_t<1, D, Q8, false>(p, smem, s);
+  if (tb == 2) return launch_t<2, D, Q8, false>(p, smem, s);
+  if (tb == 4) return launch_t<4, D, Q8, false>(p, smem, s);
+  return launch_t<4, D, Q8, true>(p, smem, s);
 }
 
 template <int D, bool Q8>
 cudaError_t occupancy_d(int* blocks, size_t smem) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, step_kernel<1, D, Q8>, kThreads, smem);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, step_kernel<1, D, Q8, false>, kThreads, smem);
 }
 
 }  // namespace
