@@ -1473,7 +1473,7 @@ __device__ void tc_issuer(const Params& p, Smem& S) {
 // S warps split a row, over those S warps only.
 // Every consumer function is inlined into the dispatch loop, so the consumer's state
 // (record index, flags) and the small arrays passed between its functions stay in
-// registers (the consumer warpgroups hold 224 each).  A call that took the object's
+// registers (the consumer warpgroups hold 216 each).  A call that took the object's
 // address would put that state in local memory, and with nearly all of the SM's L1
 // given to shared memory, those accesses would miss to L2 after every barrier.
 // TB: rows per register group (1, 2 or 4); W: the tcgen05 instantiation (batches of

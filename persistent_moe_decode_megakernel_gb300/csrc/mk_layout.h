@@ -27,13 +27,16 @@ constexpr bool kTrace = MK_TRACE != 0;
 
 // ---- thread block shape: two consumer warpgroups + one producer warpgroup -------
 // (one producer thread issues the copies; the producer warpgroup hands most of its
-// registers to the consumers: 256 x kConsumerRegs + 128 x kProducerRegs = 384 x 168)
+// registers to the consumers: 256 x kConsumerRegs + 128 x kProducerRegs = 384 x 168.  72 for
+// the producer: with 56 its MoE task loops spilled in the tcgen05 instantiation and the
+// narrow ones spilled too; 216 keeps the consumers of every instantiation but the 4-row one
+// free of spills)
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 128;
 constexpr int kLaunchRegs = 168;
-constexpr int kConsumerRegs = 224;
-constexpr int kProducerRegs = 56;
+constexpr int kConsumerRegs = 216;
+constexpr int kProducerRegs = 72;
 static_assert(kConsumerThreads * kConsumerRegs + 128 * kProducerRegs == kThreads * kLaunchRegs,
               "register hand-over must add up to the launch allocation");
 
