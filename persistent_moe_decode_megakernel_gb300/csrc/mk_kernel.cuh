@@ -1478,12 +1478,13 @@ __device__ void tc_issuer(const Params& p, Smem& S) {
 // given to shared memory, those accesses would miss to L2 after every barrier.
 // TB: rows per register group (1, 2 or 4); W: the tcgen05 instantiation (batches of
 // kTcMinBatch rows or more: every GEMV a tcgen05 tile), which carries none of the CUDA-core and
-// mma.sync GEMV code, as the others carry none of the tcgen05 code.
-template <int TB, int D, bool Q8, bool W>
+// mma.sync GEMV code, as the others carry none of the tcgen05 code; SM: the small-batch MoE
+// path (narrow instantiations only), else the general one (or tcgen05).  The host picks the
+// instantiation by the step's batch and path.
+template <int TB, int D, bool Q8, bool W, bool SM>
 struct Consumer {
-  // the MoE path of this instantiation: small-batch in the narrow ones, general (or tcgen05) in
-  // the widest (the host picks the instantiation by the step's path)
-  static constexpr bool kSmallMoe = TB <= kSmallMaxB;
+  static_assert(!SM || (TB <= kSmallMaxB && !W), "the small-batch MoE path serves 1-2 rows");
+  static constexpr bool kSmallMoe = SM;
   const Params& p;
   Smem& S;
   uint32_t c = 0;       // this warp's current record
@@ -1617,7 +1618,7 @@ struct Consumer {
       v = (v / (1.0f + expf(-v))) * v2;
       // small-batch MoE: the combine weight is applied here, and the down projection of this
       // block's own units reads the value from shared memory
-      if constexpr (TB <= kSmallMaxB) {
+      if constexpr (kSmallMoe) {
         const int u = o.hoff + static_cast<int>(row);
         if (o.hs != nullptr && u >= 0 && u < kMaxUnits) o.hs[b * kMaxUnits + u] = v * S.rwcache[b * p.K + j];
       }
@@ -3871,10 +3872,10 @@ struct Consumer {
           break;
         case R_ROUTE: ok = route_local(); break;
         case R_DT:   // small-batch MoE records exist only for batches of at most kSmallMaxB rows
-          if constexpr (TB <= kSmallMaxB) ok = moe_dt();
+          if constexpr (kSmallMoe) ok = moe_dt();
           break;
         case R_RED:
-          if constexpr (TB <= kSmallMaxB) ok = moe_reduce();
+          if constexpr (kSmallMoe) ok = moe_reduce();
           break;
         default: break;
       }
@@ -3901,7 +3902,7 @@ struct Consumer {
 };
 
 // --------------------------------------------------------------------------- the kernel
-template <int TB, int D, bool Q8, bool W>
+template <int TB, int D, bool Q8, bool W, bool SM>
 __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   // the ring holds 128-byte-swizzled TMA tiles, whose pattern repeats every 1024 bytes
@@ -3959,7 +3960,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     // producer warpgroup: one thread streams, the rest only lend their registers
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
     if (tid == kConsumerThreads) {
-      Producer<Q8, W, (TB <= kSmallMaxB)> prod(p, S);
+      Producer<Q8, W, SM> prod(p, S);
       prod.run();
     }
     if constexpr (W) {
@@ -3971,7 +3972,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
     {
-      Consumer<TB, D, Q8, W> cons(p, S);
+      Consumer<TB, D, Q8, W, SM> cons(p, S);
       cons.run();
       if constexpr (W) {
         if (p.tc) cons.tc_stop();
@@ -4035,15 +4036,15 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
   }
 }
 
-template <int TB, int D, bool Q8, bool W>
+template <int TB, int D, bool Q8, bool W, bool SM>
 cudaError_t configure_t(size_t smem) {
-  return cudaFuncSetAttribute(step_kernel<TB, D, Q8, W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(step_kernel<TB, D, Q8, W, SM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(smem));
 }
 
 // One block per SM, all resident at once (a cooperative launch: blocks wait on one another's
 // data).  Launched through cudaLaunchKernelEx so that stream capture records it in a graph.
-template <int TB, int D, bool Q8, bool W>
+template <int TB, int D, bool Q8, bool W, bool SM>
 cudaError_t launch_t(const Params& p, size_t smem, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.n_ctas);
@@ -4055,30 +4056,37 @@ cudaError_t launch_t(const Params& p, size_t smem, cudaStream_t s) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, step_kernel<TB, D, Q8, W>, p);
+  return cudaLaunchKernelEx(&cfg, step_kernel<TB, D, Q8, W, SM>, p);
 }
 
 template <int D, bool Q8>
 cudaError_t configure_all(size_t smem) {
   cudaError_t e;
-  if ((e = configure_t<1, D, Q8, false>(smem)) != cudaSuccess) return e;
-  if ((e = configure_t<2, D, Q8, false>(smem)) != cudaSuccess) return e;
-  if ((e = configure_t<4, D, Q8, false>(smem)) != cudaSuccess) return e;
-  return configure_t<4, D, Q8, true>(smem);
+  if ((e = configure_t<1, D, Q8, false, true>(smem)) != cudaSuccess) return e;
+  if ((e = configure_t<2, D, Q8, false, true>(smem)) != cudaSuccess) return e;
+  if ((e = configure_t<1, D, Q8, false, false>(smem)) != cudaSuccess) return e;
+  if ((e = configure_t<2, D, Q8, false, false>(smem)) != cudaSuccess) return e;
+  if ((e = configure_t<4, D, Q8, false, false>(smem)) != cudaSuccess) return e;
+  return configure_t<4, D, Q8, true, false>(smem);
 }
 
-// tb: 1, 2 or 4 rows per register group; 5: the tcgen05 instantiation
+// kind: 1 or 2 rows per register group with the small-batch MoE path; 11 or 12: the same
+// without it (the general MoE path); 4: 3-4 rows; 5: the tcgen05 instantiation
 template <int D, bool Q8>
-cudaError_t launch_any(const Params& p, int tb, size_t smem, cudaStream_t s) {
-  if (tb == 1) return launch_t<1, D, Q8, false>(p, smem, s);
-  if (tb == 2) return launch_t<2, D, Q8, false>(p, smem, s);
-  if (tb == 4) return launch_t<4, D, Q8, false>(p, smem, s);
-  return launch_t<4, D, Q8, true>(p, smem, s);
+cudaError_t launch_any(const Params& p, int kind, size_t smem, cudaStream_t s) {
+  switch (kind) {
+    case 1: return launch_t<1, D, Q8, false, true>(p, smem, s);
+    case 2: return launch_t<2, D, Q8, false, true>(p, smem, s);
+    case 11: return launch_t<1, D, Q8, false, false>(p, smem, s);
+    case 12: return launch_t<2, D, Q8, false, false>(p, smem, s);
+    case 4: return launch_t<4, D, Q8, false, false>(p, smem, s);
+    default: return launch_t<4, D, Q8, true, false>(p, smem, s);
+  }
 }
 
 template <int D, bool Q8>
 cudaError_t occupancy_d(int* blocks, size_t smem) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, step_kernel<1, D, Q8, false>, kThreads, smem);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, step_kernel<1, D, Q8, false, true>, kThreads, smem);
 }
 
 }  // namespace

@@ -20,10 +20,14 @@ size_t smem_bytes() { return smem_bytes_impl(); }
 
 // rows of the batch held in registers at once by a GEMV tile
 int tb_for_batch(int B) { return B <= 1 ? 1 : (B <= 2 ? 2 : 4); }
-// the instantiation of a step: 5 for the tcgen05 one (batches of kTcMinBatch rows or more);
-// the narrow ones (1-2 rows) carry only the small-batch MoE path, so a batch of 1-2 rows that
-// cannot take it runs the 4-row one
-int tb_for_step(const Params& p) { return p.tc ? 5 : p.small_moe ? tb_for_batch(p.B) : 4; }
+// the instantiation of a step (see launch_any): 5 for the tcgen05 one (batches of kTcMinBatch
+// rows or more), 4 for 3-4 rows; batches of 1-2 rows run a narrow one with the small-batch MoE
+// path (1, 2) or, where the step cannot take it, with the general path (11, 12)
+int tb_for_step(const Params& p) {
+  if (p.tc) return 5;
+  const int tb = tb_for_batch(p.B);
+  return tb == 4 ? 4 : p.small_moe ? tb : 10 + tb;
+}
 
 cudaError_t configure_kernels(int D, bool kv_q8) {
   if (kv_q8) return D == 128 ? configure_d128_q8(smem_bytes()) : cudaErrorInvalidValue;
