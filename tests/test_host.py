@@ -55,6 +55,9 @@ def _cfg(model=W.TINY, ps=16, pages=64, mb=8, mpp=32, **over):
     ("hidden", 4100, mk.MK_ERR_UNSUPPORTED), ("page_size", 512, mk.MK_ERR_UNSUPPORTED),
     ("norm_topk", 2, mk.MK_ERR_INVALID_ARG), ("flags", 4, mk.MK_ERR_INVALID_ARG),
     ("num_experts", 300, mk.MK_ERR_UNSUPPORTED),
+    # a page of 264 positions fits half a ring slot at head_dim 64, but a chunk must hold whole
+    # 16-position tiles and two such pages do not fit
+    ("page_size", 264, mk.MK_ERR_UNSUPPORTED), ("page_size", 12, mk.MK_ERR_UNSUPPORTED),
 ])
 def test_create_rejects_bad_config(field, value, code):
     c = _cfg(**{field: value})
@@ -64,6 +67,20 @@ def test_create_rejects_bad_config(field, value, code):
     assert rc == code
     assert not ctx.value
     assert mk.lib().mk_last_error().decode() != ""
+
+
+@pytest.mark.parametrize("ps", [8, 24, 64, 256])
+def test_create_accepts_page_sizes_of_whole_tiles(ps):
+    # page sizes that are multiples of 8 pass the configuration checks as long as a chunk can
+    # hold whole 16-position tiles (at 8 and 24 a tile can span two pages); the call then stops
+    # at the missing weights
+    c = _cfg(ps=ps)
+    ctx = ctypes.c_void_p()
+    w = mk.Weights()
+    rc = mk.lib().mk_create(ctypes.byref(c), ctypes.byref(w), ctypes.byref(ctx))
+    assert rc == mk.MK_ERR_INVALID_ARG, mk.lib().mk_last_error().decode()
+    assert "weights" in mk.lib().mk_last_error().decode()
+    assert not ctx.value
 
 
 def test_create_rejects_null_and_misaligned_weights():
